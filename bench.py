@@ -1,0 +1,373 @@
+#!/usr/bin/env python
+"""Benchmark of the TTT inner loop on one B300 (tokens/s and roofline fraction).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one call of the library over the whole workload (every chain, every
+token): the full TTT inner loop -- loads, key forward, LayerNorm
+forward/backward, in-batch mixing, output, weight update, final state.
+Default workload: TTT-Linear, 8 sequences x 12 heads, d=64, T=2048, b=16.
+
+Prints one JSON line. ``value`` is whole-job throughput (B*T*H tokens per
+second over all ranks) with inputs resident in HBM, timed per step with CUDA
+events on the launching stream and L2 flushed (256 MiB write) between steps.
+``e2e`` is the same metric through the C ABI with pinned host buffers: the
+host->device copies of the step's inputs and the device->host copy of Z and
+the per-token loss are inside the timed region. ``cpu_baseline`` times the
+fp64 CPU oracle on a bounded sample of the same workload.
+
+``--impl reference`` runs the reference arm: the fp64 CPU oracle as it stands,
+one bounded sample of the workload per step, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from test_weight_sequence_ttt_b300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "linear_b8h12_d64_t2k"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm_gbs=j["hbm_gbs"], bf16_tflops=j["bf16_tflops"],
+                    bf16_tflops_sustained=j.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+def algorithmic_cost(w):
+    """Per-launch algorithmic bytes (Q/K/V/Z in the io dtype, eta fp32) and
+    dense-contraction FLOPs of the dual form."""
+    es = 2 if w.io == "bf16" else 4
+    per_tok_bytes = 3 * w.d * es + 4 + w.d * es
+    if w.variant == "linear":
+        per_tok_flops = 6 * w.d * w.d + 4 * w.b * w.d
+    else:
+        h = w.hidden
+        per_tok_flops = 14 * w.d * h + 4 * w.b * (w.d + h)
+    return per_tok_bytes * w.tokens, per_tok_flops * w.tokens
+
+
+# ---------------------------------------------------------------- clocks (NVML, during the timed region)
+
+class ClockSampler:
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+    }
+
+    def __init__(self, index: int, period_s: float = 0.01):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons = [], 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._t = None
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t:
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"],
+                    "samples": 0}
+        rs = [n for bit, n in sorted(self.REASONS.items()) if self.reasons & bit]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": rs, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def oracle_sample(w, n_chains: int, T: int, nthreads: int = 0):
+    """Run the fp64 oracle on the first ``n_chains`` chains, first ``T`` tokens.
+    Returns (seconds, tokens processed, threads used)."""
+    import oracle
+    sel = list(range(n_chains))
+    inp = make_inputs(w.with_(T=T), chains=sel)
+    f = lambda t: t.detach().double().numpy()
+    th = nthreads or oracle.max_threads()
+    t0 = time.perf_counter()
+    if w.variant == "linear":
+        oracle.ttt_linear(f(inp["Q"]), f(inp["K"]), f(inp["V"]), f(inp["eta"]), f(inp["W0"]),
+                          f(inp["c0"]), f(inp["ln_g"]), f(inp["ln_b"]), b=w.b, eps=w.eps,
+                          nthreads=th)
+    else:
+        oracle.ttt_mlp(f(inp["Q"]), f(inp["K"]), f(inp["V"]), f(inp["eta"]), f(inp["W1"]), f(inp["c1"]),
+                       f(inp["W2"]), f(inp["c2"]), f(inp["ln_g"]), f(inp["ln_b"]), b=w.b, eps=w.eps,
+                       nthreads=th)
+    dt = time.perf_counter() - t0
+    return dt, n_chains * T, th
+
+
+def _sample_shape(w, cpu_s: float, threads: int):
+    """Pick (chains, T') so one oracle call costs about ``cpu_s`` core-seconds
+    spread over ``threads`` threads (calibrated on one short chain)."""
+    Tc = max(w.b, min(w.T, (256 // w.b) * w.b or w.b))
+    dt, toks, _ = oracle_sample(w, 1, Tc, nthreads=1)
+    per_tok = dt / toks                                   # single-thread seconds per token-head
+    tokens_budget = cpu_s / per_tok
+    chains = int(min(w.chains, max(1, tokens_budget // w.T)))
+    if chains >= threads or chains == w.chains:
+        return chains, w.T
+    chains = min(w.chains, threads)
+    T = int(max(w.b, (tokens_budget / chains) // w.b * w.b))
+    return chains, min(T, w.T)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend)
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def _barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def _max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_gpu(args):
+    import test_weight_sequence_ttt_b300 as ttt
+
+    dist, rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    w = WORKLOADS[args.workload]
+    # weak scaling: every rank runs its own full workload (independent chains)
+    inp = make_inputs(w.with_(seed=w.seed + 7919 * rank))
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    stream = torch.cuda.current_stream()
+    B, H, T, d = dev["Q"].shape
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = {}
+
+    if w.variant == "linear":
+        call = lambda o: ttt.ttt_linear_forward(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W0"], dev["c0"],
+                                                dev["ln_g"], dev["ln_b"], mb=w.b, eps=w.eps, out=o,
+                                                status=st, stream=stream)
+        kind = ttt.linear_kernel_kind(ttt.BF16 if w.io == "bf16" else ttt.F32, w.d, w.b)
+    else:
+        call = lambda o: ttt.ttt_mlp_forward(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W1"], dev["c1"],
+                                             dev["W2"], dev["c2"], dev["ln_g"], dev["ln_b"], mb=w.b, eps=w.eps,
+                                             out=o, status=st, stream=stream)
+        kind = ttt.mlp_kernel_kind(ttt.BF16 if w.io == "bf16" else ttt.F32, w.d, w.hidden, w.b)
+    out = call(out)                       # allocates outputs once
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        call(out)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError("device status %d after warm-up" % int(st.item()))
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    _barrier(dist)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with sampler:
+        for e0, e1 in evs:
+            flush.fill_(1.0)              # evict L2 (inputs are < 126 MB L2) -- outside the events
+            e0.record(stream)
+            call(out)
+            e1.record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    _barrier(dist)
+    times_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.mean(times_ms)
+    ms_max = _max_over_ranks(dist, ms)
+    if int(st.item()) != 0:
+        raise RuntimeError("device status %d in timed region" % int(st.item()))
+
+    # ---- e2e: pinned host buffers through the C ABI, copies inside the timed region
+    host_in = {k: inp[k].pin_memory() for k in ("Q", "K", "V", "eta")}
+    host_Z = torch.empty(inp["Q"].shape, dtype=inp["Q"].dtype).pin_memory()
+    host_L = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_Z.numel() * host_Z.element_size() + host_L.numel() * 4
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for k, t in host_in.items():
+            dev[k].copy_(t, non_blocking=True)
+        call(out)
+        host_Z.copy_(out["Z"], non_blocking=True)
+        host_L.copy_(out["loss"], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+        torch.cuda.synchronize()          # the result is on the host before the next step
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = _max_over_ranks(dist, e2e_s)
+
+    if rank != 0:
+        return None
+    peaks = _peaks()
+    bytes_launch, flops_launch = algorithmic_cost(w)
+    tokens = w.tokens * world
+    value = tokens / (ms_max / 1e3)
+    if w.variant == "linear":
+        bound, achieved, peak, unit = "hbm", bytes_launch / (ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        bound, achieved, peak, unit = "tensor", flops_launch / (ms / 1e3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    t_roof = max(bytes_launch / (peaks["hbm_gbs"] * 1e9), flops_launch / (peaks["bf16_tflops"] * 1e12))
+    line = {
+        "metric": "TTT inner-loop tokens/sec (B·T·H/s) and % of roofline on 1 B300",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.io,
+        "precision": "bf16 I/O; fp16 tensor-core operands; fp32 accumulation, LayerNorm and weight state"
+        if kind == 2 else "fp32 FFMA",
+        "data": "synthetic (seeded Gaussian Q/K/V, sigmoid-gated eta, N(0,0.02^2) W0)",
+        "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
+                   "mb": w.b, "hidden": w.hidden or None, "io": w.io, "kernel_kind": kind,
+                   "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": None,
+                     "roofline_frac": t_roof / (ms / 1e3),
+                     "peak_source": peaks["source"] + " (burst)",
+                     "algorithmic_bytes_per_launch": bytes_launch, "algorithmic_flops_per_launch": flops_launch},
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+        "ms_per_step_min": min(times_ms), "ms_per_step_median": statistics.median(times_ms),
+        "timed_wall_s": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        threads = __import__("oracle").max_threads()
+        chains, Ts = _sample_shape(w, args.cpu_budget_s, threads)
+        dt, toks, th = oracle_sample(w, chains, Ts, nthreads=threads)
+        line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
+                                "sample": "%d of %d chains x %d tokens (fp64 primal token loop, C, OpenMP)"
+                                          % (chains, w.chains, Ts),
+                                "seconds": dt, "cpu_count": os.cpu_count()}
+    return line
+
+
+# ---------------------------------------------------------------- reference arm: the oracle
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    w = WORKLOADS[args.workload]
+    threads = oracle.max_threads()
+    per_step_wall = max(0.05, args.ref_budget_s / max(1, args.steps + args.warmup))
+    chains, Ts = _sample_shape(w, per_step_wall * threads, threads)
+    for _ in range(args.warmup):
+        oracle_sample(w, chains, Ts, nthreads=threads)
+    secs, toks = 0.0, 0
+    for _ in range(args.steps):
+        dt, n, _ = oracle_sample(w, chains, Ts, nthreads=threads)
+        secs += dt
+        toks += n
+    value = toks / secs
+    return {
+        "impl": "reference",
+        "metric": "TTT inner-loop tokens/sec (B·T·H/s) and % of roofline on 1 B300",
+        "value": value, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator)",
+        "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
+                   "mb": w.b, "hidden": w.hidden or None},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": "%d of %d chains x %d tokens per step" % (chains, w.chains, Ts)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=20.0, help="core-seconds of the oracle sample")
+    ap.add_argument("--ref-budget-s", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

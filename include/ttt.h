@@ -1,0 +1,150 @@
+/*
+ * ttt.h -- C ABI of the test-time-training (TTT) inner-loop library for one
+ * NVIDIA B300 (sm_103a).
+ *
+ * What the calls compute
+ * ----------------------
+ * For every chain (sequence beta, head h) independently, a fast weight is
+ * trained on the chain's own tokens by mini-batch gradient descent and read
+ * out after every token:
+ *
+ *   loss   (Eq. 4, "TTT layer" section of the survey page "Test-Time
+ *           Training(TTT)과 LLM 메모리"):   l_t(W) = || f(k_t; W) - v_t ||^2
+ *   update (Eq. 2 of the same section, mini-batched as in Eq. 5 of the
+ *           "End-to-End Test-Time Training for Long Context" review, 2.3):
+ *           W_i = W_{i-1} - (1/b) sum_{t in batch i} eta_t grad l_t(W_{i-1})
+ *   output (Eq. 5 of the survey section):   z_t = f(q_t; W_t), where W_t is
+ *           W_{i-1} minus the (1/b) eta_s grad l_s(W_{i-1}) terms of the
+ *           tokens s <= t of batch i (the in-batch prefix).
+ *   f(x; W) = x + LN(f_res(x; W))  (residual form, survey section
+ *           "재현성과 공개 구현"), LN with frozen gamma/beta, biased variance,
+ *           eps inside the square root.
+ *   TTT-Linear: f_res(x) = W x + c,                      W [d][d], c [d]
+ *   TTT-MLP:    f_res(x) = W2 gelu_tanh(W1 x + c1) + c2,  W1 [h][d], W2 [d][h]
+ *   Per-token reconstruction loss L_t = || z_t - v_t ||^2 ("SR-TTT:
+ *           Surprisal-Aware Residual Test-Time Training", section 2).
+ * The biases c (c1, c2) are fast weights updated like W.
+ *
+ * Conventions
+ * -----------
+ * Memory:    every pointer is device memory owned by the caller; the library
+ *            allocates nothing and keeps no state between calls.
+ * Layout:    all tensors contiguous, row-major, chain-major:
+ *              Q, K, V, Z            [B][H][T][d]  (element type `io`)
+ *              eta, loss, inner_loss [B][H][T]     fp32
+ *              ln_g, ln_b            [H][d]        fp32
+ *            initial weights [B or 1][H][...] fp32 with a batch stride in
+ *            elements (0 = one set shared by every sequence, a learned W_0).
+ *            Final weights [B][H][...] fp32.
+ * Alignment: every pointer 16-byte aligned.
+ * Aliasing:  outputs must not overlap inputs or each other.
+ * Execution: asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *            Host-side validation runs first and returns before any launch.
+ * Errors:    a non-TTT_OK return means nothing was launched (validation) or
+ *            the launch failed (TTT_ERR_CUDA). Problems found on the device
+ *            (a bounded wait that gave up, a non-finite final state, an input
+ *            outside the fp16 operand range) are written to *status_dev (if
+ *            given; must hold 0 on entry) and are read by the caller after
+ *            synchronising.
+ * Threads:   calls on distinct streams with distinct buffers may run
+ *            concurrently.
+ */
+#ifndef TTT_B300_H
+#define TTT_B300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TTT_ABI_VERSION 1
+
+typedef enum {
+    TTT_OK = 0,
+    TTT_ERR_NULL = 1,            /* a required pointer is NULL                       */
+    TTT_ERR_SHAPE = 2,           /* B,H,T,d,mb,hidden out of range or T % mb != 0    */
+    TTT_ERR_UNSUPPORTED = 3,     /* valid shape, no kernel for (io, d, mb, hidden)   */
+    TTT_ERR_ALIGN = 4,           /* a pointer is not 16-byte aligned                 */
+    TTT_ERR_NOT_DEVICE_PTR = 5,  /* a pointer is not device-accessible memory        */
+    TTT_ERR_CUDA = 6,            /* a CUDA runtime call or launch failed             */
+    TTT_ERR_TIMEOUT = 7,         /* device: a bounded wait gave up, chain abandoned  */
+    TTT_ERR_NONFINITE = 8,       /* device: non-finite value in the final state      */
+    TTT_ERR_ALIAS = 9,           /* an output overlaps an input or another output    */
+    TTT_ERR_RANGE = 10           /* device: an input exceeds the fp16 operand range  */
+} ttt_status;
+
+typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
+
+/* ---------------------------------------------------------------------- */
+/* TTT-Linear                                                              */
+/* ---------------------------------------------------------------------- */
+typedef struct {
+    int32_t B, H, T, d;      /* sequences, heads, tokens per chain, head dim   */
+    int32_t mb;              /* mini-batch size b; T % mb == 0                 */
+    int32_t io;              /* ttt_dtype of Q, K, V and Z                     */
+    float ln_eps;            /* LayerNorm epsilon (1e-6 on the pages' configs) */
+    const void *Q, *K, *V;   /* [B][H][T][d] io: test / training / label views */
+    const float *eta;        /* [B][H][T] per-token learning rate (> 0)        */
+    const float *W0;         /* [B|1][H][d][d] initial W (f_res = W x + c)     */
+    const float *c0;         /* [B|1][H][d] initial bias                       */
+    int64_t w0_bstride;      /* elements between sequences in W0 (0 = shared)  */
+    int64_t c0_bstride;      /* elements between sequences in c0 (0 = shared)  */
+    const float *ln_g;       /* [H][d] LayerNorm gamma                         */
+    const float *ln_b;       /* [H][d] LayerNorm beta                          */
+    void *Z;                 /* [B][H][T][d] io out: z_t = f(q_t; W_t)         */
+    float *W_out;            /* [B][H][d][d] final W, or NULL                  */
+    float *c_out;            /* [B][H][d] final c, or NULL                     */
+    float *loss;             /* [B][H][T] L_t = ||z_t - v_t||^2, or NULL       */
+    float *inner_loss;       /* [B][H][T] l_t(W_{i-1}) at the anchor, or NULL  */
+    int32_t *status_dev;     /* device int32 (0 on entry), or NULL             */
+} ttt_linear_args;
+
+/* Supported: io = TTT_F32 or TTT_BF16 with 1 <= d <= 128, 1 <= mb <= 64 and
+ *            d(d+1) + d + 4 mb d + mb^2 + mb floats <= 227 KB
+ *            (fp32 FFMA kernel; kind 1);
+ *            io = TTT_BF16 with d in {64, 128}, mb in {1, 2, 4, 8, 16}
+ *            (tensor-core kernel, kind 2: fp16 MMA operands, fp32
+ *            accumulation, fp32 weight state); kind 2 wins where both apply.
+ *            ttt_linear_kernel_kind() reports the choice. */
+ttt_status ttt_linear_forward(const ttt_linear_args *args, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* TTT-MLP                                                                 */
+/* ---------------------------------------------------------------------- */
+typedef struct {
+    int32_t B, H, T, d, hidden; /* hidden = MLP width h (4d on the pages)       */
+    int32_t mb;
+    int32_t io;
+    float ln_eps;
+    const void *Q, *K, *V;
+    const float *eta;
+    const float *W1_0;       /* [B|1][H][hidden][d] */
+    const float *c1_0;       /* [B|1][H][hidden]    */
+    const float *W2_0;       /* [B|1][H][d][hidden] */
+    const float *c2_0;       /* [B|1][H][d]         */
+    int64_t w_bstride;       /* elements between sequences in W1_0 and W2_0 (0 = shared) */
+    int64_t c1_bstride, c2_bstride;
+    const float *ln_g, *ln_b;
+    void *Z;
+    float *W1_out, *c1_out, *W2_out, *c2_out; /* [B][H][...] or NULL */
+    float *loss, *inner_loss;
+    int32_t *status_dev;
+} ttt_mlp_args;
+
+ttt_status ttt_mlp_forward(const ttt_mlp_args *args, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Introspection                                                           */
+/* ---------------------------------------------------------------------- */
+const char *ttt_status_string(ttt_status s);   /* static string, never NULL */
+int ttt_abi_version(void);                     /* == TTT_ABI_VERSION        */
+/* Which kernel a call with these sizes would launch: 0 = none (unsupported),
+ * 1 = fp32 FFMA kernel, 2 = tensor-core kernel. No CUDA call is made. */
+int ttt_linear_kernel_kind(int32_t io, int32_t d, int32_t mb);
+int ttt_mlp_kernel_kind(int32_t io, int32_t d, int32_t hidden, int32_t mb);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TTT_B300_H */

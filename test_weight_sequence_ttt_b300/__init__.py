@@ -1,0 +1,242 @@
+"""TTT inner loop (TTT-Linear / TTT-MLP) on one NVIDIA B300.
+
+Thin binding over the C ABI of ``include/ttt.h`` (``libttt_b300.so``, built by
+``python -m test_weight_sequence_ttt_b300.build``). This module only marshals
+arguments: every step of the inner loop runs in the library's CUDA kernels.
+PyTorch supplies device memory and streams.
+
+    from test_weight_sequence_ttt_b300 import ttt_linear_forward
+    out = ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, mb=16)
+    out["Z"], out["W"], out["c"], out["loss"], out["inner_loss"]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+__all__ = [
+    "TTTError", "lib", "lib_path", "ttt_linear_forward", "ttt_mlp_forward", "status_string",
+    "abi_version", "linear_kernel_kind", "mlp_kernel_kind", "LinearArgs", "MlpArgs",
+    "STATUS", "F32", "BF16",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_HERE, "libttt_b300.so")
+
+F32, BF16 = 0, 1
+STATUS = {
+    0: "TTT_OK", 1: "TTT_ERR_NULL", 2: "TTT_ERR_SHAPE", 3: "TTT_ERR_UNSUPPORTED", 4: "TTT_ERR_ALIGN",
+    5: "TTT_ERR_NOT_DEVICE_PTR", 6: "TTT_ERR_CUDA", 7: "TTT_ERR_TIMEOUT", 8: "TTT_ERR_NONFINITE",
+    9: "TTT_ERR_ALIAS", 10: "TTT_ERR_RANGE",
+}
+
+_vp = ctypes.c_void_p
+
+
+class LinearArgs(ctypes.Structure):
+    """Mirror of ``ttt_linear_args``."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("T", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("mb", ctypes.c_int32), ("io", ctypes.c_int32), ("ln_eps", ctypes.c_float),
+        ("Q", _vp), ("K", _vp), ("V", _vp), ("eta", _vp), ("W0", _vp), ("c0", _vp),
+        ("w0_bstride", ctypes.c_int64), ("c0_bstride", ctypes.c_int64),
+        ("ln_g", _vp), ("ln_b", _vp), ("Z", _vp), ("W_out", _vp), ("c_out", _vp),
+        ("loss", _vp), ("inner_loss", _vp), ("status_dev", _vp),
+    ]
+
+
+class MlpArgs(ctypes.Structure):
+    """Mirror of ``ttt_mlp_args``."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("T", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("hidden", ctypes.c_int32), ("mb", ctypes.c_int32), ("io", ctypes.c_int32),
+        ("ln_eps", ctypes.c_float),
+        ("Q", _vp), ("K", _vp), ("V", _vp), ("eta", _vp),
+        ("W1_0", _vp), ("c1_0", _vp), ("W2_0", _vp), ("c2_0", _vp),
+        ("w_bstride", ctypes.c_int64), ("c1_bstride", ctypes.c_int64), ("c2_bstride", ctypes.c_int64),
+        ("ln_g", _vp), ("ln_b", _vp), ("Z", _vp),
+        ("W1_out", _vp), ("c1_out", _vp), ("W2_out", _vp), ("c2_out", _vp),
+        ("loss", _vp), ("inner_loss", _vp), ("status_dev", _vp),
+    ]
+
+
+class TTTError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        msg = "%s (%d): %s" % (STATUS.get(code, "?"), code, status_string(code))
+        super().__init__(msg + (" [%s]" % what if what else ""))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libttt_b300.so``. Raises if it has not been built: there is no
+    fallback path."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(lib_path):
+                raise RuntimeError(
+                    "libttt_b300.so is missing; build it with "
+                    "`python -m test_weight_sequence_ttt_b300.build`")
+            L = ctypes.CDLL(lib_path)
+            L.ttt_linear_forward.restype = ctypes.c_int
+            L.ttt_linear_forward.argtypes = [ctypes.POINTER(LinearArgs), _vp]
+            L.ttt_mlp_forward.restype = ctypes.c_int
+            L.ttt_mlp_forward.argtypes = [ctypes.POINTER(MlpArgs), _vp]
+            L.ttt_status_string.restype = ctypes.c_char_p
+            L.ttt_status_string.argtypes = [ctypes.c_int]
+            L.ttt_abi_version.restype = ctypes.c_int
+            L.ttt_abi_version.argtypes = []
+            L.ttt_linear_kernel_kind.restype = ctypes.c_int
+            L.ttt_linear_kernel_kind.argtypes = [ctypes.c_int32] * 3
+            L.ttt_mlp_kernel_kind.restype = ctypes.c_int
+            L.ttt_mlp_kernel_kind.argtypes = [ctypes.c_int32] * 4
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().ttt_status_string(int(code)).decode()
+
+
+def abi_version() -> int:
+    return lib().ttt_abi_version()
+
+
+def linear_kernel_kind(io: int, d: int, mb: int) -> int:
+    return lib().ttt_linear_kernel_kind(io, d, mb)
+
+
+def mlp_kernel_kind(io: int, d: int, hidden: int, mb: int) -> int:
+    return lib().ttt_mlp_kernel_kind(io, d, hidden, mb)
+
+
+# ---------------------------------------------------------------- marshalling helpers
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _io_code(dtype) -> int:
+    import torch
+    if dtype == torch.float32:
+        return F32
+    if dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("Q/K/V must be float32 or bfloat16, got %s" % dtype)
+
+
+def _check_cuda(name, t):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _bstride(t, B: int, per: int) -> int:
+    if t.shape[0] == 1:
+        return 0 if B > 1 else per
+    if t.shape[0] != B:
+        raise ValueError("initial weights need a leading dim of B or 1")
+    return per
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float = 1e-6,
+                       out: Optional[dict] = None, want_state: bool = True,
+                       want_loss: bool = True, want_inner_loss: bool = True,
+                       status=None, stream=None) -> dict:
+    """Run the TTT-Linear inner loop through ``ttt_linear_forward``.
+
+    Q, K, V [B,H,T,d] (float32 or bfloat16, CUDA, contiguous); eta [B,H,T] fp32;
+    W0 [B|1,H,d,d], c0 [B|1,H,d], ln_g/ln_b [H,d] fp32. ``out`` may pass
+    preallocated outputs (keys Z, W, c, loss, inner_loss); missing ones are
+    allocated with torch. ``status`` is an optional int32 CUDA tensor of one
+    element (0 on entry) that receives device-side errors. Asynchronous on
+    ``stream`` (default: torch's current stream)."""
+    import torch
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("eta", eta), ("W0", W0), ("c0", c0),
+                 ("ln_g", ln_g), ("ln_b", ln_b), ("status", status)):
+        _check_cuda(n, t)
+    B, H, T, d = Q.shape
+    out = dict(out or {})
+    dev = Q.device
+    if "Z" not in out:
+        out["Z"] = torch.empty_like(Q)
+    if want_state:
+        out.setdefault("W", torch.empty(B, H, d, d, device=dev, dtype=torch.float32))
+        out.setdefault("c", torch.empty(B, H, d, device=dev, dtype=torch.float32))
+    if want_loss:
+        out.setdefault("loss", torch.empty(B, H, T, device=dev, dtype=torch.float32))
+    if want_inner_loss:
+        out.setdefault("inner_loss", torch.empty(B, H, T, device=dev, dtype=torch.float32))
+    a = LinearArgs(
+        B=B, H=H, T=T, d=d, mb=mb, io=_io_code(Q.dtype), ln_eps=eps,
+        Q=_ptr(Q), K=_ptr(K), V=_ptr(V), eta=_ptr(eta), W0=_ptr(W0), c0=_ptr(c0),
+        w0_bstride=_bstride(W0, B, H * d * d), c0_bstride=_bstride(c0, B, H * d),
+        ln_g=_ptr(ln_g), ln_b=_ptr(ln_b), Z=_ptr(out["Z"]), W_out=_ptr(out.get("W")),
+        c_out=_ptr(out.get("c")), loss=_ptr(out.get("loss")),
+        inner_loss=_ptr(out.get("inner_loss")), status_dev=_ptr(status),
+    )
+    rc = lib().ttt_linear_forward(ctypes.byref(a), _stream_handle(stream))
+    if rc != 0:
+        raise TTTError(rc, "ttt_linear_forward")
+    return out
+
+
+def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: float = 1e-6,
+                    out: Optional[dict] = None, want_state: bool = True,
+                    want_loss: bool = True, want_inner_loss: bool = True,
+                    status=None, stream=None) -> dict:
+    """Run the TTT-MLP inner loop through ``ttt_mlp_forward``.
+
+    W1 [B|1,H,h,d], c1 [B|1,H,h], W2 [B|1,H,d,h], c2 [B|1,H,d] fp32; other
+    arguments as for ``ttt_linear_forward``. Outputs: Z, W1, c1, W2, c2, loss,
+    inner_loss."""
+    import torch
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("eta", eta), ("W1", W1), ("c1", c1), ("W2", W2),
+                 ("c2", c2), ("ln_g", ln_g), ("ln_b", ln_b), ("status", status)):
+        _check_cuda(n, t)
+    B, H, T, d = Q.shape
+    h = W1.shape[-2]
+    out = dict(out or {})
+    dev = Q.device
+    if "Z" not in out:
+        out["Z"] = torch.empty_like(Q)
+    if want_state:
+        out.setdefault("W1", torch.empty(B, H, h, d, device=dev, dtype=torch.float32))
+        out.setdefault("c1", torch.empty(B, H, h, device=dev, dtype=torch.float32))
+        out.setdefault("W2", torch.empty(B, H, d, h, device=dev, dtype=torch.float32))
+        out.setdefault("c2", torch.empty(B, H, d, device=dev, dtype=torch.float32))
+    if want_loss:
+        out.setdefault("loss", torch.empty(B, H, T, device=dev, dtype=torch.float32))
+    if want_inner_loss:
+        out.setdefault("inner_loss", torch.empty(B, H, T, device=dev, dtype=torch.float32))
+    a = MlpArgs(
+        B=B, H=H, T=T, d=d, hidden=h, mb=mb, io=_io_code(Q.dtype), ln_eps=eps,
+        Q=_ptr(Q), K=_ptr(K), V=_ptr(V), eta=_ptr(eta),
+        W1_0=_ptr(W1), c1_0=_ptr(c1), W2_0=_ptr(W2), c2_0=_ptr(c2),
+        w_bstride=_bstride(W1, B, H * h * d), c1_bstride=_bstride(c1, B, H * h),
+        c2_bstride=_bstride(c2, B, H * d),
+        ln_g=_ptr(ln_g), ln_b=_ptr(ln_b), Z=_ptr(out["Z"]),
+        W1_out=_ptr(out.get("W1")), c1_out=_ptr(out.get("c1")), W2_out=_ptr(out.get("W2")),
+        c2_out=_ptr(out.get("c2")), loss=_ptr(out.get("loss")),
+        inner_loss=_ptr(out.get("inner_loss")), status_dev=_ptr(status),
+    )
+    rc = lib().ttt_mlp_forward(ctypes.byref(a), _stream_handle(stream))
+    if rc != 0:
+        raise TTTError(rc, "ttt_mlp_forward")
+    return out

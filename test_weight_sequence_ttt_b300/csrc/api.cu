@@ -1,0 +1,239 @@
+// api.cu -- the C ABI declared in include/ttt.h: host-side validation,
+// dispatch to a kernel, launch. No allocation, no state between calls.
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "ttt_internal.h"
+
+namespace {
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range span(const void *p, size_t bytes)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Range{a, a + bytes};
+}
+
+bool overlap(const Range &a, const Range &b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_device_ptr(const void *p)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // clear the sticky-free error of a failed query
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// Bytes spanned by an initial-weight array [B|1][H][per] with a batch stride.
+size_t init_bytes(int B, int H, size_t per, int64_t bstride)
+{
+    return ((size_t)(B - 1) * (size_t)bstride + (size_t)H * per) * sizeof(float);
+}
+
+bool dims_ok(int B, int H, int T, int d, int mb)
+{
+    if (B < 1 || H < 1 || T < 1 || d < 1 || mb < 1) return false;
+    if ((int64_t)B * H > INT32_MAX) return false;
+    if (T > (1 << 30) || d > 4096) return false;
+    return T % mb == 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ttt_status_string(ttt_status s)
+{
+    switch (s) {
+    case TTT_OK: return "ok";
+    case TTT_ERR_NULL: return "a required pointer is NULL";
+    case TTT_ERR_SHAPE: return "sizes out of range or T not a multiple of the mini-batch size";
+    case TTT_ERR_UNSUPPORTED: return "no kernel for this (io dtype, d, mini-batch, hidden)";
+    case TTT_ERR_ALIGN: return "a pointer or batch stride is not 16-byte aligned";
+    case TTT_ERR_NOT_DEVICE_PTR: return "a pointer is not device memory";
+    case TTT_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case TTT_ERR_TIMEOUT: return "a bounded device wait gave up; outputs are incomplete";
+    case TTT_ERR_NONFINITE: return "the final fast-weight state is not finite";
+    case TTT_ERR_ALIAS: return "an output overlaps an input or another output";
+    case TTT_ERR_RANGE: return "an input is outside the fp16 operand range of the tensor-core kernel";
+    }
+    return "unknown status";
+}
+
+int ttt_abi_version(void) { return TTT_ABI_VERSION; }
+
+int ttt_linear_kernel_kind(int32_t io, int32_t d, int32_t mb)
+{
+    if (ttt::linear_tc_supported(io, d, mb)) return 2;
+    if (ttt::linear_f32_supported(io, d, mb)) return 1;
+    return 0;
+}
+
+int ttt_mlp_kernel_kind(int32_t io, int32_t d, int32_t hidden, int32_t mb)
+{
+    if (ttt::mlp_f32_supported(io, d, hidden, mb)) return 1;
+    return 0;
+}
+
+ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
+{
+    if (!a) return TTT_ERR_NULL;
+    if (!a->Q || !a->K || !a->V || !a->eta || !a->W0 || !a->c0 || !a->ln_g || !a->ln_b || !a->Z)
+        return TTT_ERR_NULL;
+    if (!dims_ok(a->B, a->H, a->T, a->d, a->mb)) return TTT_ERR_SHAPE;
+    if (a->io != TTT_F32 && a->io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
+    if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
+    if (a->w0_bstride < 0 || a->c0_bstride < 0) return TTT_ERR_SHAPE;
+    const int kind = ttt_linear_kernel_kind(a->io, a->d, a->mb);
+    if (kind == 0) return TTT_ERR_UNSUPPORTED;
+
+    const void *in[] = {a->Q, a->K, a->V, a->eta, a->W0, a->c0, a->ln_g, a->ln_b};
+    const void *out[] = {a->Z, a->W_out, a->c_out, a->loss, a->inner_loss, a->status_dev};
+    for (const void *p : in)
+        if (!aligned16(p)) return TTT_ERR_ALIGN;
+    for (const void *p : out)
+        if (p && !aligned16(p) && p != a->status_dev) return TTT_ERR_ALIGN;
+    if ((a->w0_bstride & 3) || (a->c0_bstride & 3)) return TTT_ERR_ALIGN;
+
+    const size_t B = a->B, H = a->H, T = a->T, d = a->d;
+    const size_t es = a->io == TTT_BF16 ? 2 : 4;
+    const size_t tok = B * H * T;
+    const Range rin[] = {span(a->Q, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
+                         span(a->eta, tok * 4), span(a->W0, init_bytes(a->B, a->H, d * d, a->w0_bstride)),
+                         span(a->c0, init_bytes(a->B, a->H, d, a->c0_bstride)), span(a->ln_g, H * d * 4),
+                         span(a->ln_b, H * d * 4)};
+    const Range rout[] = {span(a->Z, tok * d * es), span(a->W_out, a->W_out ? B * H * d * d * 4 : 0),
+                          span(a->c_out, a->c_out ? B * H * d * 4 : 0), span(a->loss, a->loss ? tok * 4 : 0),
+                          span(a->inner_loss, a->inner_loss ? tok * 4 : 0),
+                          span(a->status_dev, a->status_dev ? 4 : 0)};
+    for (size_t i = 0; i < sizeof(rout) / sizeof(rout[0]); ++i) {
+        if (rout[i].hi == rout[i].lo) continue;
+        for (const Range &r : rin)
+            if (overlap(rout[i], r)) return TTT_ERR_ALIAS;
+        for (size_t j = i + 1; j < sizeof(rout) / sizeof(rout[0]); ++j)
+            if (rout[j].hi != rout[j].lo && overlap(rout[i], rout[j])) return TTT_ERR_ALIAS;
+    }
+    for (const void *p : in)
+        if (!is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+    for (const void *p : out)
+        if (p && !is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+
+    ttt::LinearParams p;
+    p.H = a->H;
+    p.T = a->T;
+    p.d = a->d;
+    p.mb = a->mb;
+    p.eps = a->ln_eps;
+    p.Q = a->Q;
+    p.K = a->K;
+    p.V = a->V;
+    p.eta = a->eta;
+    p.W0 = a->W0;
+    p.c0 = a->c0;
+    p.w0_bstride = a->w0_bstride;
+    p.c0_bstride = a->c0_bstride;
+    p.ln_g = a->ln_g;
+    p.ln_b = a->ln_b;
+    p.Z = a->Z;
+    p.W_out = a->W_out;
+    p.c_out = a->c_out;
+    p.loss = a->loss;
+    p.inner_loss = a->inner_loss;
+    p.status = a->status_dev;
+    const int chains = a->B * a->H;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = kind == 2 ? ttt::launch_linear_tc(p, chains, s) : ttt::launch_linear_f32(p, a->io, chains, s);
+    return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
+{
+    if (!a) return TTT_ERR_NULL;
+    if (!a->Q || !a->K || !a->V || !a->eta || !a->W1_0 || !a->c1_0 || !a->W2_0 || !a->c2_0 || !a->ln_g ||
+        !a->ln_b || !a->Z)
+        return TTT_ERR_NULL;
+    if (!dims_ok(a->B, a->H, a->T, a->d, a->mb) || a->hidden < 1 || a->hidden > 4096) return TTT_ERR_SHAPE;
+    if (a->io != TTT_F32 && a->io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
+    if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
+    if (a->w_bstride < 0 || a->c1_bstride < 0 || a->c2_bstride < 0) return TTT_ERR_SHAPE;
+    const int kind = ttt_mlp_kernel_kind(a->io, a->d, a->hidden, a->mb);
+    if (kind == 0) return TTT_ERR_UNSUPPORTED;
+
+    const void *in[] = {a->Q, a->K, a->V, a->eta, a->W1_0, a->c1_0, a->W2_0, a->c2_0, a->ln_g, a->ln_b};
+    const void *out[] = {a->Z, a->W1_out, a->c1_out, a->W2_out, a->c2_out, a->loss, a->inner_loss, a->status_dev};
+    for (const void *p : in)
+        if (!aligned16(p)) return TTT_ERR_ALIGN;
+    for (const void *p : out)
+        if (p && !aligned16(p) && p != a->status_dev) return TTT_ERR_ALIGN;
+    if ((a->w_bstride & 3) || (a->c1_bstride & 3) || (a->c2_bstride & 3)) return TTT_ERR_ALIGN;
+
+    const size_t B = a->B, H = a->H, T = a->T, d = a->d, h = a->hidden;
+    const size_t es = a->io == TTT_BF16 ? 2 : 4;
+    const size_t tok = B * H * T;
+    const Range rin[] = {span(a->Q, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
+                         span(a->eta, tok * 4), span(a->W1_0, init_bytes(a->B, a->H, h * d, a->w_bstride)),
+                         span(a->c1_0, init_bytes(a->B, a->H, h, a->c1_bstride)),
+                         span(a->W2_0, init_bytes(a->B, a->H, h * d, a->w_bstride)),
+                         span(a->c2_0, init_bytes(a->B, a->H, d, a->c2_bstride)), span(a->ln_g, H * d * 4),
+                         span(a->ln_b, H * d * 4)};
+    const Range rout[] = {span(a->Z, tok * d * es),
+                          span(a->W1_out, a->W1_out ? B * H * h * d * 4 : 0),
+                          span(a->c1_out, a->c1_out ? B * H * h * 4 : 0),
+                          span(a->W2_out, a->W2_out ? B * H * h * d * 4 : 0),
+                          span(a->c2_out, a->c2_out ? B * H * d * 4 : 0),
+                          span(a->loss, a->loss ? tok * 4 : 0),
+                          span(a->inner_loss, a->inner_loss ? tok * 4 : 0),
+                          span(a->status_dev, a->status_dev ? 4 : 0)};
+    for (size_t i = 0; i < sizeof(rout) / sizeof(rout[0]); ++i) {
+        if (rout[i].hi == rout[i].lo) continue;
+        for (const Range &r : rin)
+            if (overlap(rout[i], r)) return TTT_ERR_ALIAS;
+        for (size_t j = i + 1; j < sizeof(rout) / sizeof(rout[0]); ++j)
+            if (rout[j].hi != rout[j].lo && overlap(rout[i], rout[j])) return TTT_ERR_ALIAS;
+    }
+    for (const void *p : in)
+        if (!is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+    for (const void *p : out)
+        if (p && !is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+
+    ttt::MlpParams p;
+    p.H = a->H;
+    p.T = a->T;
+    p.d = a->d;
+    p.hidden = a->hidden;
+    p.mb = a->mb;
+    p.eps = a->ln_eps;
+    p.Q = a->Q;
+    p.K = a->K;
+    p.V = a->V;
+    p.eta = a->eta;
+    p.W1 = a->W1_0;
+    p.c1 = a->c1_0;
+    p.W2 = a->W2_0;
+    p.c2 = a->c2_0;
+    p.w_bstride = a->w_bstride;
+    p.c1_bstride = a->c1_bstride;
+    p.c2_bstride = a->c2_bstride;
+    p.ln_g = a->ln_g;
+    p.ln_b = a->ln_b;
+    p.Z = a->Z;
+    p.W1_out = a->W1_out;
+    p.c1_out = a->c1_out;
+    p.W2_out = a->W2_out;
+    p.c2_out = a->c2_out;
+    p.loss = a->loss;
+    p.inner_loss = a->inner_loss;
+    p.status = a->status_dev;
+    const cudaError_t e = ttt::launch_mlp_f32(p, a->io, a->B * a->H, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,140 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launch).
+
+* the library loads and exports every function include/ttt.h declares;
+* the ctypes mirrors of the argument structs match the C layout (offsets
+  printed by a tiny C program compiled with gcc against the header);
+* validation returns the documented status codes before any CUDA work.
+"""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+import test_weight_sequence_ttt_b300 as ttt
+from test_weight_sequence_ttt_b300 import LinearArgs, MlpArgs
+from test_weight_sequence_ttt_b300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ttt.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return ttt.lib()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ttt_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert "ttt_linear_forward" in names and "ttt_mlp_forward" in names
+    for n in names:
+        assert hasattr(L, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", ttt.lib_path], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (ttt_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_version_and_strings(L):
+    assert ttt.abi_version() == 1
+    for code in ttt.STATUS:
+        assert len(ttt.status_string(code)) > 0
+    assert ttt.status_string(999) == "unknown status"
+
+
+def _c_offsets(struct_name, fields):
+    prog = ["#include <stdio.h>", "#include <stddef.h>", '#include "%s"' % HEADER, "int main(void){"]
+    prog.append('printf("%%zu\\n", sizeof(%s));' % struct_name)
+    for f in fields:
+        prog.append('printf("%%zu\\n", offsetof(%s, %s));' % (struct_name, f))
+    prog.append("return 0;}")
+    with tempfile.TemporaryDirectory() as td:
+        c = os.path.join(td, "o.c")
+        exe = os.path.join(td, "o")
+        open(c, "w").write("\n".join(prog))
+        subprocess.check_call(["gcc", "-std=c99", "-o", exe, c])
+        vals = [int(x) for x in subprocess.check_output([exe]).split()]
+    return vals[0], vals[1:]
+
+
+@pytest.mark.parametrize("cls,cname", [(LinearArgs, "ttt_linear_args"), (MlpArgs, "ttt_mlp_args")])
+def test_struct_layout_matches_header(cls, cname):
+    fields = [f[0] for f in cls._fields_]
+    size, offs = _c_offsets(cname, fields)
+    assert ctypes.sizeof(cls) == size
+    assert [getattr(cls, f).offset for f in fields] == offs
+
+
+def test_kernel_kind_table(L):
+    assert ttt.linear_kernel_kind(ttt.BF16, 64, 16) == 2
+    assert ttt.linear_kernel_kind(ttt.BF16, 128, 1) == 2
+    assert ttt.linear_kernel_kind(ttt.BF16, 128, 64) == 1     # fp32 kernel for now
+    assert ttt.linear_kernel_kind(ttt.F32, 16, 16) == 1
+    assert ttt.linear_kernel_kind(ttt.F32, 256, 16) == 0
+    assert ttt.linear_kernel_kind(7, 64, 16) == 0
+    assert ttt.mlp_kernel_kind(ttt.BF16, 64, 256, 16) >= 1
+
+
+def _linear(**kw):
+    """Well-formed argument struct with fake, 16-byte aligned, disjoint pointers."""
+    B, H, T, d = kw.pop("B", 2), kw.pop("H", 3), kw.pop("T", 32), kw.pop("d", 64)
+    base = 1 << 40
+    step = 1 << 32
+    ptrs = {n: base + i * step for i, n in enumerate(
+        ["Q", "K", "V", "eta", "W0", "c0", "ln_g", "ln_b", "Z", "W_out", "c_out", "loss",
+         "inner_loss", "status_dev"])}
+    a = dict(B=B, H=H, T=T, d=d, mb=16, io=ttt.BF16, ln_eps=1e-6, w0_bstride=0, c0_bstride=0, **ptrs)
+    a.update(kw)
+    return LinearArgs(**a)
+
+
+def _call(L, a):
+    return L.ttt_linear_forward(ctypes.byref(a), None)
+
+
+def test_validation_codes(L):
+    assert L.ttt_linear_forward(None, None) == 1
+    assert _call(L, _linear(Q=None)) == 1
+    assert _call(L, _linear(Z=None)) == 1
+    assert _call(L, _linear(T=30)) == 2                   # T % mb
+    assert _call(L, _linear(B=0)) == 2
+    assert _call(L, _linear(ln_eps=-1.0)) == 2
+    assert _call(L, _linear(w0_bstride=-4)) == 2
+    assert _call(L, _linear(io=5)) == 3
+    assert _call(L, _linear(d=256)) == 3
+    assert _call(L, _linear(K=(1 << 40) + 3)) == 4        # misaligned
+    assert _call(L, _linear(w0_bstride=6)) == 4           # stride not 16-byte multiple
+    assert _call(L, _linear(Z=(1 << 40) + (1 << 32) * 1)) == 9   # Z over K
+    assert _call(L, _linear(loss=(1 << 40) + (1 << 32) * 12)) == 9  # loss over inner_loss
+    # well-formed, but the pointers are not device memory (no device here)
+    assert _call(L, _linear()) == 5
+
+
+def test_validation_codes_mlp(L):
+    base = 1 << 40
+    step = 1 << 32
+    names = ["Q", "K", "V", "eta", "W1_0", "c1_0", "W2_0", "c2_0", "ln_g", "ln_b", "Z", "W1_out",
+             "c1_out", "W2_out", "c2_out", "loss", "inner_loss", "status_dev"]
+    ptrs = {n: base + i * step for i, n in enumerate(names)}
+
+    def call(**kw):
+        a = dict(B=1, H=2, T=32, d=64, hidden=256, mb=16, io=ttt.BF16, ln_eps=1e-6, w_bstride=0,
+                 c1_bstride=0, c2_bstride=0, **ptrs)
+        a.update(kw)
+        return L.ttt_mlp_forward(ctypes.byref(MlpArgs(**a)), None)
+
+    assert call(W2_0=None) == 1
+    assert call(T=33) == 2
+    assert call(hidden=0) == 2
+    assert call(io=3) == 3
+    assert call(c2_0=base + 7 * step + 4) == 4
+    assert call(W1_out=base + 5 * step) == 9
+    assert call() == 5

@@ -1,0 +1,202 @@
+"""TTT-Linear: CUDA kernels vs the fp64 oracle (GPU).
+
+Small cases compare every output element; the full-size workloads run every
+chain on the GPU in the configuration the benchmark times and compare sampled
+chains against the oracle. Tolerances (max |err| / RMS of the oracle tensor):
+1e-4 for the fp32 path, 2e-2 for the bf16-io tensor-core path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import test_weight_sequence_ttt_b300 as ttt
+from test_weight_sequence_ttt_b300.inputs import WORKLOADS, make_inputs
+
+from _util import TOL, compare, oracle_linear, rel_err, rms, run_linear, to_np
+
+pytestmark = pytest.mark.gpu
+KEYS = ("Z", "W", "c", "loss", "inner_loss")
+
+
+def _small(d, b, T, B=2, H=3, io="bf16", seed=77):
+    w = WORKLOADS["linear_b8h12_d64_t2k"].with_(B=B, H=H, T=T, d=d, b=b, io=io, seed=seed)
+    return make_inputs(w)
+
+
+def _check(inp, tol, keys=KEYS):
+    got = run_linear(inp)
+    assert int(got["status"].item()) == 0
+    ref = oracle_linear(inp)
+    return compare(got, ref, keys, tol)
+
+
+# ---------------------------------------------------------------- fp32 path
+
+def test_f32_tiny_workload():
+    inp = make_inputs(WORKLOADS["linear_f32_tiny"])
+    assert ttt.linear_kernel_kind(ttt.F32, 16, 16) == 1
+    _check(inp, TOL["f32"])
+
+
+@pytest.mark.parametrize("d,b,T", [(16, 1, 20), (16, 16, 64), (32, 4, 36), (64, 16, 48), (128, 8, 40),
+                                   (128, 32, 64), (24, 3, 27)])
+def test_f32_shapes(d, b, T):
+    _check(_small(d, b, T, io="f32"), TOL["f32"])
+
+
+# ---------------------------------------------------------------- tensor-core path
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("b", [1, 2, 4, 8, 16])
+def test_tc_small(d, b):
+    assert ttt.linear_kernel_kind(ttt.BF16, d, b) == 2
+    T = 48 if b == 16 else 40      # several super-steps, ragged last one for b < 16
+    _check(_small(d, b, T), TOL["bf16"])
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 15, 17])
+def test_tc_tiny_T(T):
+    _check(_small(64, 1, T, B=1, H=2), TOL["bf16"])
+
+
+def test_tc_single_superstep():
+    _check(_small(128, 16, 16, B=1, H=1), TOL["bf16"])
+
+
+def test_bf16_fp32_kernel_shapes():
+    # bf16 io on shapes the tensor-core kernel does not take (fp32 FFMA kernel)
+    assert ttt.linear_kernel_kind(ttt.BF16, 32, 16) == 1
+    _check(_small(32, 16, 48), TOL["bf16"])
+    assert ttt.linear_kernel_kind(ttt.BF16, 128, 64) == 1
+    _check(_small(128, 64, 128, B=1, H=2), TOL["bf16"])
+
+
+def test_per_sequence_initial_weights():
+    inp = _small(64, 16, 64, B=3, H=2)
+    g = torch.Generator().manual_seed(5)
+    inp["W0"] = torch.randn(3, 2, 64, 64, generator=g) * 0.05
+    inp["c0"] = torch.randn(3, 2, 64, generator=g) * 0.1
+    inp["ln_g"] = 1.0 + 0.2 * torch.randn(2, 64, generator=g)
+    inp["ln_b"] = 0.1 * torch.randn(2, 64, generator=g)
+    _check(inp, TOL["bf16"])
+
+
+# ---------------------------------------------------------------- full-size workloads (sampled chains)
+
+FULL = ["linear_b8h12_d64_t2k", "linear_b1h32_d64_t128k", "linear_b16h16_d128_t4k_mb1",
+        "linear_b16h16_d128_t4k_mb4", "linear_b16h16_d128_t4k_mb16", "linear_b16h16_d128_t4k_mb64"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_chains(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    got = run_linear(inp)
+    assert int(got["status"].item()) == 0
+    sel = sorted({0, w.chains - 1, (w.chains * 7) // 13})
+    ref = oracle_linear(make_inputs(w, chains=sel))
+    idx = (np.array([c // w.H for c in sel]), np.array([c % w.H for c in sel]))
+    errs = {}
+    for k in KEYS:
+        g = to_np(got[k])[idx]
+        errs[k] = rel_err(g, ref[k].reshape(g.shape))
+    print(name, errs)
+    assert errs["Z"] <= TOL["bf16"], errs
+    for k in ("W", "c", "loss", "inner_loss"):
+        assert errs[k] <= 5 * TOL["bf16"], errs
+    # every output was written
+    for k in KEYS:
+        assert torch.isfinite(got[k]).all(), k
+
+
+# ---------------------------------------------------------------- invariants (no oracle)
+
+def test_layernorm_statistics_of_output():
+    inp = make_inputs(WORKLOADS["linear_b8h12_d64_t2k"].with_(B=2, T=512))
+    got = run_linear(inp)
+    D = to_np(got["Z"]) - to_np(inp["Q"])
+    assert np.abs(D.mean(-1)).max() < 2e-2
+    ms = (D ** 2).mean(-1)
+    assert ms.max() < 1.02 and ms.min() > 0.95
+
+
+def test_causality_bit_exact():
+    inp = _small(64, 4, 96, B=1, H=2)
+    base = run_linear(inp)
+    t = 53
+    for key in ("Q", "K", "V"):
+        pert = dict(inp)
+        pert[key] = inp[key].clone()
+        pert[key][0, 1, t] += 0.5
+        r = run_linear(pert)
+        assert torch.equal(r["Z"][:, :, :t], base["Z"][:, :, :t]), key
+        assert torch.equal(r["loss"][:, :, :t], base["loss"][:, :, :t]), key
+        assert torch.equal(r["Z"][:, 0], base["Z"][:, 0]), key      # other chain untouched
+        assert not torch.equal(r["Z"][0, 1, t:], base["Z"][0, 1, t:]), key
+
+
+def test_chain_permutation():
+    inp = _small(128, 16, 64, B=4, H=2)
+    base = run_linear(inp)
+    perm = torch.tensor([2, 0, 3, 1])
+    pinp = dict(inp)
+    for k in ("Q", "K", "V", "eta"):
+        pinp[k] = inp[k][perm].contiguous()
+    r = run_linear(pinp)
+    for k in ("Z", "W", "c", "loss", "inner_loss"):
+        assert torch.equal(r[k], base[k][perm]), k
+
+
+def test_resume_two_calls():
+    inp = _small(64, 16, 128, B=1, H=2)
+    full = run_linear(inp)
+    T1 = 64
+    a = dict(inp)
+    for k in ("Q", "K", "V", "eta"):
+        a[k] = inp[k][:, :, :T1].contiguous()
+    ra = run_linear(a)
+    bb = dict(inp)
+    for k in ("Q", "K", "V", "eta"):
+        bb[k] = inp[k][:, :, T1:].contiguous()
+    bb["W0"] = ra["W"].cpu()
+    bb["c0"] = ra["c"].cpu()
+    rb = run_linear(bb)
+    z = torch.cat([ra["Z"], rb["Z"]], 2)
+    assert rel_err(to_np(z), to_np(full["Z"])) < 1e-2
+    assert rel_err(to_np(rb["W"]), to_np(full["W"])) < 1e-2
+
+
+def test_outputs_fully_written_and_optional_outputs():
+    inp = _small(64, 8, 40, B=2, H=2)
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = {"Z": torch.full_like(dev["Q"], float("nan")),
+           "W": torch.full((2, 2, 64, 64), float("nan"), device="cuda"),
+           "c": torch.full((2, 2, 64), float("nan"), device="cuda"),
+           "loss": torch.full((2, 2, 40), float("nan"), device="cuda"),
+           "inner_loss": torch.full((2, 2, 40), float("nan"), device="cuda")}
+    r = run_linear(inp, out=out)
+    for k in out:
+        assert torch.isfinite(r[k]).all(), k
+    # Z only
+    z = ttt.ttt_linear_forward(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W0"], dev["c0"],
+                               dev["ln_g"], dev["ln_b"], mb=8, want_state=False, want_loss=False,
+                               want_inner_loss=False)["Z"]
+    torch.cuda.synchronize()
+    assert torch.equal(z, r["Z"])
+
+
+def test_range_error_reported():
+    inp = _small(64, 16, 32, B=1, H=1)
+    inp["K"] = inp["K"].clone()
+    inp["K"][0, 0, 5, 3] = 1.0e5
+    got = run_linear(inp)
+    assert int(got["status"].item()) == 10   # TTT_ERR_RANGE
+
+
+def test_host_pointer_rejected():
+    inp = _small(64, 16, 32, B=1, H=1)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    with pytest.raises(ttt.TTTError) as e:
+        ttt.ttt_linear_forward(d["Q"], d["K"], d["V"], d["eta"], d["W0"], d["c0"], d["ln_g"], d["ln_b"],
+                               mb=16, out={"Z": torch.empty_like(inp["Q"]).pin_memory()})
+    assert e.value.code in (5,)
