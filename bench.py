@@ -52,11 +52,11 @@ def _peaks():
     return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
 
 
-def algorithmic_cost(w):
-    """Per-launch algorithmic bytes (Q/K/V/Z in the io dtype, eta fp32) and
-    dense-contraction FLOPs of the dual form."""
+def algorithmic_cost(w, z_bytes: int = 4):
+    """Per-launch algorithmic bytes (Q/K/V in the io dtype, eta fp32, Z in its
+    output dtype) and dense-contraction FLOPs of the dual form."""
     es = 2 if w.io == "bf16" else 4
-    per_tok_bytes = 3 * w.d * es + 4 + w.d * es
+    per_tok_bytes = 3 * w.d * es + 4 + w.d * z_bytes
     if w.variant == "linear":
         per_tok_flops = 6 * w.d * w.d + 4 * w.b * w.d
     else:
@@ -68,57 +68,87 @@ def algorithmic_cost(w):
 # ---------------------------------------------------------------- clocks (NVML, during the timed region)
 
 class ClockSampler:
+    """Samples SM clock and clock-event (throttle) reasons of this process's GPU
+    while the timed region runs: NVML (matched by PCI bus id) every 10 ms, else
+    ``nvidia-smi -lms 100``."""
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
         0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
         0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
     }
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.active"]
 
-    def __init__(self, index: int, period_s: float = 0.01):
-        self.index, self.period = index, period_s
-        self.samples, self.reasons = [], 0
-        self.max_mhz = None
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        self.period = period_s
+        self.samples, self.reasons, self.max_mhz = [], 0, None
         self._stop = threading.Event()
         self._t = None
-        self.ok = False
+        self._proc = None
+        self.mode, self.error = None, None
+        props = torch.cuda.get_device_properties(device_index)
+        self.bus_id = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                            props.pci_device_id)
         try:
             import pynvml
             pynvml.nvmlInit()
             self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self._h = pynvml.nvmlDeviceGetHandleByPciBusId(self.bus_id.encode())
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
-            self.ok = False
+            self.mode = "nvml"
+        except Exception as e:  # noqa: BLE001
+            self.error = "nvml: %s" % e
+            self.mode = "smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self._nv
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
                 self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-            except Exception:
-                pass
+            except Exception as e:  # noqa: BLE001
+                self.error = "nvml sample: %s" % e
             time.sleep(self.period)
 
     def __enter__(self):
-        if self.ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
             self._t.start()
+        else:
+            import subprocess
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "--id=" + self.bus_id, "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+            except Exception as e:  # noqa: BLE001
+                self.error = (self.error or "") + "; smi: %s" % e
         return self
 
     def __exit__(self, *a):
         self._stop.set()
         if self._t:
             self._t.join()
+        if self._proc:
+            self._proc.terminate()
+            out, err = self._proc.communicate(timeout=10)
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                    self.reasons |= int(f[2], 16)
+                except (ValueError, IndexError):
+                    continue
+            if not self.samples and err:
+                self.error = (self.error or "") + "; smi: %s" % err.strip()[:200]
 
     def summary(self):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"],
-                    "samples": 0}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "samples": 0,
+                    "error": self.error}
         rs = [n for bit, n in sorted(self.REASONS.items()) if self.reasons & bit]
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": rs, "samples": len(self.samples)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": rs,
+                "samples": len(self.samples), "source": self.mode}
 
 
 # ---------------------------------------------------------------- oracle timing
@@ -198,7 +228,8 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     B, H, T, d = dev["Q"].shape
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = {}
+    zdt = torch.float32 if args.z_dtype == "f32" else torch.bfloat16
+    out = {"Z": torch.empty(dev["Q"].shape, dtype=zdt, device="cuda")}
 
     if w.variant == "linear":
         call = lambda o: ttt.ttt_linear_forward(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W0"], dev["c0"],
@@ -242,7 +273,7 @@ def run_gpu(args):
 
     # ---- e2e: pinned host buffers through the C ABI, copies inside the timed region
     host_in = {k: inp[k].pin_memory() for k in ("Q", "K", "V", "eta")}
-    host_Z = torch.empty(inp["Q"].shape, dtype=inp["Q"].dtype).pin_memory()
+    host_Z = torch.empty(inp["Q"].shape, dtype=zdt).pin_memory()
     host_L = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = host_Z.numel() * host_Z.element_size() + host_L.numel() * 4
@@ -269,7 +300,7 @@ def run_gpu(args):
     if rank != 0:
         return None
     peaks = _peaks()
-    bytes_launch, flops_launch = algorithmic_cost(w)
+    bytes_launch, flops_launch = algorithmic_cost(w, 4 if args.z_dtype == "f32" else 2)
     tokens = w.tokens * world
     value = tokens / (ms_max / 1e3)
     if w.variant == "linear":
@@ -293,7 +324,8 @@ def run_gpu(args):
         if kind == 2 else "fp32 FFMA",
         "data": "synthetic (seeded Gaussian Q/K/V, sigmoid-gated eta, N(0,0.02^2) W0)",
         "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
-                   "mb": w.b, "hidden": w.hidden or None, "io": w.io, "kernel_kind": kind,
+                   "mb": w.b, "hidden": w.hidden or None, "io": w.io, "z_dtype": args.z_dtype,
+                   "kernel_kind": kind,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": None,
@@ -354,10 +386,12 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--z-dtype", default="f32", choices=["f32", "bf16"],
+                    help="element type of Z (fp32 keeps the tolerance gate on the arithmetic)")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0, help="core-seconds of the oracle sample")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

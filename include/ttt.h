@@ -30,7 +30,8 @@
  * Memory:    every pointer is device memory owned by the caller; the library
  *            allocates nothing and keeps no state between calls.
  * Layout:    all tensors contiguous, row-major, chain-major:
- *              Q, K, V, Z            [B][H][T][d]  (element type `io`)
+ *              Q, K, V               [B][H][T][d]  (element type `io`)
+ *              Z                     [B][H][T][d]  (element type `z_io`)
  *              eta, loss, inner_loss [B][H][T]     fp32
  *              ln_g, ln_b            [H][d]        fp32
  *            initial weights [B or 1][H][...] fp32 with a batch stride in
@@ -48,6 +49,8 @@
  *            synchronising.
  * Threads:   calls on distinct streams with distinct buffers may run
  *            concurrently.
+ * Z dtype:   bf16 Z rounds every output to 8 significant bits (relative error
+ *            up to 2^-8 |z|); fp32 Z returns the kernel's result unrounded.
  */
 #ifndef TTT_B300_H
 #define TTT_B300_H
@@ -82,7 +85,8 @@ typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
 typedef struct {
     int32_t B, H, T, d;      /* sequences, heads, tokens per chain, head dim   */
     int32_t mb;              /* mini-batch size b; T % mb == 0                 */
-    int32_t io;              /* ttt_dtype of Q, K, V and Z                     */
+    int32_t io;              /* ttt_dtype of Q, K and V                        */
+    int32_t z_io;            /* ttt_dtype of Z (TTT_F32 or TTT_BF16)           */
     float ln_eps;            /* LayerNorm epsilon (1e-6 on the pages' configs) */
     const void *Q, *K, *V;   /* [B][H][T][d] io: test / training / label views */
     const float *eta;        /* [B][H][T] per-token learning rate (> 0)        */
@@ -92,7 +96,7 @@ typedef struct {
     int64_t c0_bstride;      /* elements between sequences in c0 (0 = shared)  */
     const float *ln_g;       /* [H][d] LayerNorm gamma                         */
     const float *ln_b;       /* [H][d] LayerNorm beta                          */
-    void *Z;                 /* [B][H][T][d] io out: z_t = f(q_t; W_t)         */
+    void *Z;                 /* [B][H][T][d] z_io out: z_t = f(q_t; W_t)       */
     float *W_out;            /* [B][H][d][d] final W, or NULL                  */
     float *c_out;            /* [B][H][d] final c, or NULL                     */
     float *loss;             /* [B][H][T] L_t = ||z_t - v_t||^2, or NULL       */
@@ -115,7 +119,7 @@ ttt_status ttt_linear_forward(const ttt_linear_args *args, void *stream);
 typedef struct {
     int32_t B, H, T, d, hidden; /* hidden = MLP width h (4d on the pages)       */
     int32_t mb;
-    int32_t io;
+    int32_t io, z_io;        /* dtypes of Q/K/V and of Z, as for TTT-Linear   */
     float ln_eps;
     const void *Q, *K, *V;
     const float *eta;

@@ -39,7 +39,8 @@ class LinearArgs(ctypes.Structure):
     """Mirror of ``ttt_linear_args``."""
     _fields_ = [
         ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("T", ctypes.c_int32), ("d", ctypes.c_int32),
-        ("mb", ctypes.c_int32), ("io", ctypes.c_int32), ("ln_eps", ctypes.c_float),
+        ("mb", ctypes.c_int32), ("io", ctypes.c_int32), ("z_io", ctypes.c_int32),
+        ("ln_eps", ctypes.c_float),
         ("Q", _vp), ("K", _vp), ("V", _vp), ("eta", _vp), ("W0", _vp), ("c0", _vp),
         ("w0_bstride", ctypes.c_int64), ("c0_bstride", ctypes.c_int64),
         ("ln_g", _vp), ("ln_b", _vp), ("Z", _vp), ("W_out", _vp), ("c_out", _vp),
@@ -52,7 +53,7 @@ class MlpArgs(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("T", ctypes.c_int32), ("d", ctypes.c_int32),
         ("hidden", ctypes.c_int32), ("mb", ctypes.c_int32), ("io", ctypes.c_int32),
-        ("ln_eps", ctypes.c_float),
+        ("z_io", ctypes.c_int32), ("ln_eps", ctypes.c_float),
         ("Q", _vp), ("K", _vp), ("V", _vp), ("eta", _vp),
         ("W1_0", _vp), ("c1_0", _vp), ("W2_0", _vp), ("c2_0", _vp),
         ("w_bstride", ctypes.c_int64), ("c1_bstride", ctypes.c_int64), ("c2_bstride", ctypes.c_int64),
@@ -156,7 +157,7 @@ def _stream_handle(stream) -> Optional[int]:
 
 
 def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float = 1e-6,
-                       out: Optional[dict] = None, want_state: bool = True,
+                       z_dtype=None, out: Optional[dict] = None, want_state: bool = True,
                        want_loss: bool = True, want_inner_loss: bool = True,
                        status=None, stream=None) -> dict:
     """Run the TTT-Linear inner loop through ``ttt_linear_forward``.
@@ -164,7 +165,8 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
     Q, K, V [B,H,T,d] (float32 or bfloat16, CUDA, contiguous); eta [B,H,T] fp32;
     W0 [B|1,H,d,d], c0 [B|1,H,d], ln_g/ln_b [H,d] fp32. ``out`` may pass
     preallocated outputs (keys Z, W, c, loss, inner_loss); missing ones are
-    allocated with torch. ``status`` is an optional int32 CUDA tensor of one
+    allocated with torch. ``z_dtype`` (torch.float32 by default, or
+    torch.bfloat16) is the element type of Z; a preallocated Z sets it. ``status`` is an optional int32 CUDA tensor of one
     element (0 on entry) that receives device-side errors. Asynchronous on
     ``stream`` (default: torch's current stream)."""
     import torch
@@ -175,7 +177,7 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
     out = dict(out or {})
     dev = Q.device
     if "Z" not in out:
-        out["Z"] = torch.empty_like(Q)
+        out["Z"] = torch.empty(Q.shape, device=dev, dtype=z_dtype or torch.float32)
     if want_state:
         out.setdefault("W", torch.empty(B, H, d, d, device=dev, dtype=torch.float32))
         out.setdefault("c", torch.empty(B, H, d, device=dev, dtype=torch.float32))
@@ -184,7 +186,7 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
     if want_inner_loss:
         out.setdefault("inner_loss", torch.empty(B, H, T, device=dev, dtype=torch.float32))
     a = LinearArgs(
-        B=B, H=H, T=T, d=d, mb=mb, io=_io_code(Q.dtype), ln_eps=eps,
+        B=B, H=H, T=T, d=d, mb=mb, io=_io_code(Q.dtype), z_io=_io_code(out["Z"].dtype), ln_eps=eps,
         Q=_ptr(Q), K=_ptr(K), V=_ptr(V), eta=_ptr(eta), W0=_ptr(W0), c0=_ptr(c0),
         w0_bstride=_bstride(W0, B, H * d * d), c0_bstride=_bstride(c0, B, H * d),
         ln_g=_ptr(ln_g), ln_b=_ptr(ln_b), Z=_ptr(out["Z"]), W_out=_ptr(out.get("W")),
@@ -198,7 +200,7 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
 
 
 def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: float = 1e-6,
-                    out: Optional[dict] = None, want_state: bool = True,
+                    z_dtype=None, out: Optional[dict] = None, want_state: bool = True,
                     want_loss: bool = True, want_inner_loss: bool = True,
                     status=None, stream=None) -> dict:
     """Run the TTT-MLP inner loop through ``ttt_mlp_forward``.
@@ -215,7 +217,7 @@ def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: f
     out = dict(out or {})
     dev = Q.device
     if "Z" not in out:
-        out["Z"] = torch.empty_like(Q)
+        out["Z"] = torch.empty(Q.shape, device=dev, dtype=z_dtype or torch.float32)
     if want_state:
         out.setdefault("W1", torch.empty(B, H, h, d, device=dev, dtype=torch.float32))
         out.setdefault("c1", torch.empty(B, H, h, device=dev, dtype=torch.float32))
@@ -226,7 +228,8 @@ def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: f
     if want_inner_loss:
         out.setdefault("inner_loss", torch.empty(B, H, T, device=dev, dtype=torch.float32))
     a = MlpArgs(
-        B=B, H=H, T=T, d=d, hidden=h, mb=mb, io=_io_code(Q.dtype), ln_eps=eps,
+        B=B, H=H, T=T, d=d, hidden=h, mb=mb, io=_io_code(Q.dtype), z_io=_io_code(out["Z"].dtype),
+        ln_eps=eps,
         Q=_ptr(Q), K=_ptr(K), V=_ptr(V), eta=_ptr(eta),
         W1_0=_ptr(W1), c1_0=_ptr(c1), W2_0=_ptr(W2), c2_0=_ptr(c2),
         w_bstride=_bstride(W1, B, H * h * d), c1_bstride=_bstride(c1, B, H * h),

@@ -46,9 +46,18 @@ bool dims_ok(int B, int H, int T, int d, int mb)
     return T % mb == 0;
 }
 
+#ifdef TTT_TRACE
+unsigned long long *g_trace = nullptr;
+#endif
+
 }  // namespace
 
 extern "C" {
+
+#ifdef TTT_TRACE
+// Diagnostic builds only: device buffer that receives phase timestamps.
+void ttt_debug_set_trace(unsigned long long *buf) { g_trace = buf; }
+#endif
 
 const char *ttt_status_string(ttt_status s)
 {
@@ -90,6 +99,7 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
         return TTT_ERR_NULL;
     if (!dims_ok(a->B, a->H, a->T, a->d, a->mb)) return TTT_ERR_SHAPE;
     if (a->io != TTT_F32 && a->io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
+    if (a->z_io != TTT_F32 && a->z_io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
     if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
     if (a->w0_bstride < 0 || a->c0_bstride < 0) return TTT_ERR_SHAPE;
     const int kind = ttt_linear_kernel_kind(a->io, a->d, a->mb);
@@ -105,12 +115,13 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
 
     const size_t B = a->B, H = a->H, T = a->T, d = a->d;
     const size_t es = a->io == TTT_BF16 ? 2 : 4;
+    const size_t zs = a->z_io == TTT_BF16 ? 2 : 4;
     const size_t tok = B * H * T;
     const Range rin[] = {span(a->Q, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
                          span(a->eta, tok * 4), span(a->W0, init_bytes(a->B, a->H, d * d, a->w0_bstride)),
                          span(a->c0, init_bytes(a->B, a->H, d, a->c0_bstride)), span(a->ln_g, H * d * 4),
                          span(a->ln_b, H * d * 4)};
-    const Range rout[] = {span(a->Z, tok * d * es), span(a->W_out, a->W_out ? B * H * d * d * 4 : 0),
+    const Range rout[] = {span(a->Z, tok * d * zs), span(a->W_out, a->W_out ? B * H * d * d * 4 : 0),
                           span(a->c_out, a->c_out ? B * H * d * 4 : 0), span(a->loss, a->loss ? tok * 4 : 0),
                           span(a->inner_loss, a->inner_loss ? tok * 4 : 0),
                           span(a->status_dev, a->status_dev ? 4 : 0)};
@@ -131,6 +142,7 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     p.T = a->T;
     p.d = a->d;
     p.mb = a->mb;
+    p.z_f32 = a->z_io == TTT_F32;
     p.eps = a->ln_eps;
     p.Q = a->Q;
     p.K = a->K;
@@ -148,6 +160,11 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     p.loss = a->loss;
     p.inner_loss = a->inner_loss;
     p.status = a->status_dev;
+#ifdef TTT_TRACE
+    p.trace = g_trace;
+#else
+    p.trace = nullptr;
+#endif
     const int chains = a->B * a->H;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = kind == 2 ? ttt::launch_linear_tc(p, chains, s) : ttt::launch_linear_f32(p, a->io, chains, s);
@@ -162,6 +179,7 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
         return TTT_ERR_NULL;
     if (!dims_ok(a->B, a->H, a->T, a->d, a->mb) || a->hidden < 1 || a->hidden > 4096) return TTT_ERR_SHAPE;
     if (a->io != TTT_F32 && a->io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
+    if (a->z_io != TTT_F32 && a->z_io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
     if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
     if (a->w_bstride < 0 || a->c1_bstride < 0 || a->c2_bstride < 0) return TTT_ERR_SHAPE;
     const int kind = ttt_mlp_kernel_kind(a->io, a->d, a->hidden, a->mb);
@@ -177,6 +195,7 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
 
     const size_t B = a->B, H = a->H, T = a->T, d = a->d, h = a->hidden;
     const size_t es = a->io == TTT_BF16 ? 2 : 4;
+    const size_t zs = a->z_io == TTT_BF16 ? 2 : 4;
     const size_t tok = B * H * T;
     const Range rin[] = {span(a->Q, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
                          span(a->eta, tok * 4), span(a->W1_0, init_bytes(a->B, a->H, h * d, a->w_bstride)),
@@ -184,7 +203,7 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
                          span(a->W2_0, init_bytes(a->B, a->H, h * d, a->w_bstride)),
                          span(a->c2_0, init_bytes(a->B, a->H, d, a->c2_bstride)), span(a->ln_g, H * d * 4),
                          span(a->ln_b, H * d * 4)};
-    const Range rout[] = {span(a->Z, tok * d * es),
+    const Range rout[] = {span(a->Z, tok * d * zs),
                           span(a->W1_out, a->W1_out ? B * H * h * d * 4 : 0),
                           span(a->c1_out, a->c1_out ? B * H * h * 4 : 0),
                           span(a->W2_out, a->W2_out ? B * H * h * d * 4 : 0),
@@ -210,6 +229,7 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     p.d = a->d;
     p.hidden = a->hidden;
     p.mb = a->mb;
+    p.z_f32 = a->z_io == TTT_F32;
     p.eps = a->ln_eps;
     p.Q = a->Q;
     p.K = a->K;

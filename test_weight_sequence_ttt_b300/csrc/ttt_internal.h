@@ -11,6 +11,7 @@ namespace ttt {
 // Chain-level parameters shared by the TTT-Linear kernels (device pointers).
 struct LinearParams {
     int H, T, d, mb;
+    int z_f32;  // Z element type: 1 = fp32, 0 = bf16
     float eps;
     const void *Q, *K, *V;
     const float *eta;
@@ -20,10 +21,12 @@ struct LinearParams {
     void *Z;
     float *W_out, *c_out, *loss, *inner_loss;
     int *status;
+    unsigned long long *trace;  // phase timestamps (TTT_TRACE builds only), else NULL
 };
 
 struct MlpParams {
     int H, T, d, hidden, mb;
+    int z_f32;
     float eps;
     const void *Q, *K, *V;
     const float *eta;
@@ -34,6 +37,23 @@ struct MlpParams {
     float *W1_out, *c1_out, *W2_out, *c2_out, *loss, *inner_loss;
     int *status;
 };
+
+// Phase-timestamp hook for performance diagnosis. Compiled in only with
+// -DTTT_TRACE; records clock64() of CTA 0 at role phase boundaries for steps
+// [kTraceFirst, kTraceFirst + kTraceSteps) into trace[(step - first) * 16 + slot].
+constexpr int kTraceFirst = 16, kTraceSteps = 32, kTraceSlots = 16;
+#ifdef TTT_TRACE
+#define TTT_TRACE_AT(p, step, slot)                                                                   \
+    do {                                                                                              \
+        if ((p).trace && blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (step) >= kTraceFirst &&       \
+            (step) < kTraceFirst + kTraceSteps)                                                       \
+            (p).trace[((step)-kTraceFirst) * kTraceSlots + (slot)] = clock64();                       \
+    } while (0)
+#else
+#define TTT_TRACE_AT(p, step, slot) \
+    do {                            \
+    } while (0)
+#endif
 
 // fp32 FFMA kernels (io f32 or bf16), any d <= 128, mb <= 64, mb*d <= 4096.
 bool linear_f32_supported(int io, int d, int mb);

@@ -48,7 +48,7 @@ __device__ __forceinline__ void set_status(int *status, int code)
     if (status) atomicCAS(status, 0, code);
 }
 
-template <typename IO>
+template <typename IO, typename ZT>
 __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
 {
     extern __shared__ float sm[];
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
     const IO *Qg = static_cast<const IO *>(p.Q) + tok0 * d;
     const IO *Kg = static_cast<const IO *>(p.K) + tok0 * d;
     const IO *Vg = static_cast<const IO *>(p.V) + tok0 * d;
-    IO *Zg = static_cast<IO *>(p.Z) + tok0 * d;
+    ZT *Zg = static_cast<ZT *>(p.Z) + tok0 * d;
     const float *eg = p.eta + tok0;
     const float inv_b = 1.0f / (float)b, inv_d = 1.0f / (float)d;
 
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
             float L = 0.f;
             for (int j = lane; j < d; j += 32) {
                 const float z = Qt[t * d + j] + lg[j] * (y[j] - mu) * rstd + lb[j];
-                st_io<IO>(Zg + (size_t)(t0 + t) * d + j, z);
+                st_io<ZT>(Zg + (size_t)(t0 + t) * d + j, z);
                 const float v = ld_io<IO>(Vg + (size_t)(t0 + t) * d + j);
                 L += (z - v) * (z - v);
             }
@@ -211,22 +211,22 @@ bool linear_f32_supported(int io, int d, int mb)
            linear_f32_smem(d, mb) <= 227 * 1024;
 }
 
-cudaError_t launch_linear_f32(const LinearParams &p, int io, int chains, cudaStream_t s)
+template <typename IO, typename ZT>
+cudaError_t launch_linear_f32_t(const LinearParams &p, int chains, cudaStream_t s)
 {
     const size_t smem = linear_f32_smem(p.d, p.mb);
-    cudaError_t e;
-    if (io == TTT_F32) {
-        e = cudaFuncSetAttribute(linear_f32_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        linear_f32_kernel<float><<<chains, kThreads, smem, s>>>(p);
-    } else {
-        e = cudaFuncSetAttribute(linear_f32_kernel<__nv_bfloat16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        linear_f32_kernel<__nv_bfloat16><<<chains, kThreads, smem, s>>>(p);
-    }
+    cudaError_t e = cudaFuncSetAttribute(linear_f32_kernel<IO, ZT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    linear_f32_kernel<IO, ZT><<<chains, kThreads, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_linear_f32(const LinearParams &p, int io, int chains, cudaStream_t s)
+{
+    if (io == TTT_F32)
+        return p.z_f32 ? launch_linear_f32_t<float, float>(p, chains, s) : launch_linear_f32_t<float, __nv_bfloat16>(p, chains, s);
+    return p.z_f32 ? launch_linear_f32_t<__nv_bfloat16, float>(p, chains, s)
+                   : launch_linear_f32_t<__nv_bfloat16, __nv_bfloat16>(p, chains, s);
 }
 
 }  // namespace ttt

@@ -181,6 +181,7 @@ __device__ void role_loader(const CUtensorMap *tmQ, const CUtensorMap *tmK, cons
             abort_chain(R.flags, p.status);
             break;
         }
+        TTT_TRACE_AT(p, i, 14);
         uint8_t *stg = stage_ptr<D>(sm, st);
         const int t0 = i * kSS;
         float *se = reinterpret_cast<float *>(stg + C::kOffEta);
@@ -227,6 +228,7 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
             abort_chain(R.flags, p.status);
             return;
         }
+        TTT_TRACE_AT(p, i, 12);
         uint8_t *stg = stage_ptr<D>(sm, st);
         // (1) K - V + beta in the chain warp's accumulator order (from bf16).
         float4 *kvd = reinterpret_cast<float4 *>(stg + C::kOffKVD);
@@ -309,6 +311,7 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
                     gs[(8 * j + 2 * c4 + (r & 1)) * 16 + g + 8 * (r >> 1)] = dk[j][r] + 1.f;
         }
         warp_arrive(&R.prep[st], lane);
+        TTT_TRACE_AT(p, i, 13);
         if (has_prev) {
             fence_proxy_async();  // in-place generic writes before the next TMA refill
             warp_arrive(&R.empty[(i + kStages - 1) % kStages], lane);
@@ -350,6 +353,7 @@ __device__ void role_chain(const LinearParams &p, uint8_t *sm, const Ring &R, in
             abort_chain(R.flags, p.status);
             return;
         }
+        TTT_TRACE_AT(p, i, 0);
         // y = W_{i-2} K_i^T + c_{i-2}  (+ A~_{i-1} (K_{i-1} K_i^T + 1) below)
         float y[MT][2][4];
         const float4 *S = reinterpret_cast<const float4 *>(sm + C::kOffS + slot * C::kFragF32);
@@ -487,6 +491,7 @@ __device__ void role_chain(const LinearParams &p, uint8_t *sm, const Ring &R, in
                 }
             }
         }
+        TTT_TRACE_AT(p, i, 1);
         // Publish A~_i (fp16 A-fragments: rows f, columns s).
         if (!wait_bar(&R.aempty[slot], parity_of(i >> 1) ^ 1u, R.flags)) {
             abort_chain(R.flags, p.status);
@@ -498,6 +503,7 @@ __device__ void role_chain(const LinearParams &p, uint8_t *sm, const Ring &R, in
             Ab[mt * 32 + lane] = make_uint4(pack_h2(y[mt][0][0], y[mt][0][1]), pack_h2(y[mt][0][2], y[mt][0][3]),
                                             pack_h2(y[mt][1][0], y[mt][1][1]), pack_h2(y[mt][1][2], y[mt][1][3]));
         warp_arrive(&R.afull[slot], lane);
+        TTT_TRACE_AT(p, i, 2);
         if (p.inner_loss && g == 0) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -575,6 +581,7 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
         const int st = i % kStages, slot = i & 1;
         const bool has_next = i + 1 < nsteps;
         uint8_t *stg = stage_ptr<D>(sm, st);
+        if (w == 0) TTT_TRACE_AT(p, i, 3);
         bool ok = true;
         if (has_next) {
             ok = wait_bar(&R.prep[(i + 1) % kStages], parity_of((i + 1) / kStages), R.flags) &&
@@ -585,6 +592,7 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
             abort_chain(R.flags, p.status);
             return;
         }
+        if (w == 0) TTT_TRACE_AT(p, i, 4);
         pack_w();  // W_{start of i} as fp16 A-fragments
         if (has_next)
             rgemm(smem_u32(stage_ptr<D>(sm, (i + 1) % kStages) + C::kOffK),
@@ -595,11 +603,13 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
             if (has_next) mbar_arrive(&R.sfull[slot ^ 1]);
             mbar_arrive(&R.qfull[slot]);
         }
+        if (w == 0) TTT_TRACE_AT(p, i, 5);
         // W += A~_i K_i, c += A~_i 1
         if (!wait_bar(&R.afull[slot], parity_of(i >> 1), R.flags)) {
             abort_chain(R.flags, p.status);
             return;
         }
+        if (w == 0) TTT_TRACE_AT(p, i, 6);
         const uint4 a = reinterpret_cast<const uint4 *>(sm + C::kOffA + slot * C::kFragA)[w * 32 + lane];
         warp_arrive(&R.aempty[slot], lane);
         const uint32_t at[4] = {a.x, a.y, a.z, a.w};
@@ -619,6 +629,7 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
         s1 += __shfl_xor_sync(kFull, s1, 2);
         cb0 += s0;
         cb1 += s1;
+        if (w == 0) TTT_TRACE_AT(p, i, 7);
         warp_arrive(&R.empty[st], lane);
     }
     bool bad = !isfinite(cb0) || !isfinite(cb1);
@@ -664,6 +675,7 @@ __device__ void role_output(const CUtensorMap *tmZ, const LinearParams &p, uint8
         const int slot = i & 1, st = i % kStages;
         uint8_t *stg = stage_ptr<D>(sm, st);
         float yq[MT][NTO][4];
+        if (o == 0) TTT_TRACE_AT(p, i, 8);
         if (!wait_bar(&R.qfull[slot], parity_of(i >> 1), R.flags)) {
             abort_chain(R.flags, p.status);
             break;
@@ -680,6 +692,7 @@ __device__ void role_output(const CUtensorMap *tmZ, const LinearParams &p, uint8
                 yq[mt][k][3] = v.w;
             }
         warp_arrive(&R.qempty[slot], lane);
+        if (o == 0) TTT_TRACE_AT(p, i, 9);
         if (!wait_bar(&R.afull[slot], parity_of(i >> 1), R.flags) ||
             !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags) ||
             !wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
@@ -701,6 +714,7 @@ __device__ void role_output(const CUtensorMap *tmZ, const LinearParams &p, uint8
             }
         }
         warp_arrive(&R.aempty[slot], lane);
+        if (o == 0) TTT_TRACE_AT(p, i, 10);
         // z = q + LN(yq); L_t = ||z_t - v_t||^2
         float L[NTO][2];
 #pragma unroll
@@ -734,37 +748,55 @@ __device__ void role_output(const CUtensorMap *tmZ, const LinearParams &p, uint8
                     }
                 L[k][e] = col_sum(l);
             }
-        // Z tile -> staging (bf16, transposed by stmatrix) -> TMA store.
-        uint8_t *zb = sm + C::kOffZ + slot * C::kZStage;
-        if (lane == 0) bulk_wait_read<1>();
-        __syncwarp();
+        if (p.z_f32) {
+            // fp32 Z: each group of 8 lanes writes 8 consecutive features (one
+            // 32-byte sector) of a token.
+            float *Zf = static_cast<float *>(p.Z) + tok0 * D;
 #pragma unroll
-        for (int k = 0; k < NTO; ++k) {
-            const int nt = o * NTO + k;
+            for (int k = 0; k < NTO; ++k)
 #pragma unroll
-            for (int mp = 0; mp < MT; mp += 2) {
-                const int jm = lane >> 3;
-                const int t = 8 * nt + (lane & 7);
-                const int chunk = 2 * (mp + (jm >> 1)) + (jm & 1);
-                stsm_x4_t(smem_u32(zb + zswz<D>(t, chunk)),
-                          pack_bf2(yq[mp][k][0], yq[mp][k][1]), pack_bf2(yq[mp][k][2], yq[mp][k][3]),
-                          pack_bf2(yq[mp + 1][k][0], yq[mp + 1][k][1]),
-                          pack_bf2(yq[mp + 1][k][2], yq[mp + 1][k][3]));
-            }
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) {
+                for (int e = 0; e < 2; ++e) {
+                    const int t = i * kSS + 8 * (o * NTO + k) + 2 * c4 + e;
+                    if (t < T) {
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) Zf[(size_t)t * D + 16 * mt + g + 8 * u] = yq[mt][k][e + 2 * u];
+                    }
+                }
+        } else {
+            // bf16 Z tile -> staging (transposed by stmatrix) -> TMA store.
+            uint8_t *zb = sm + C::kOffZ + slot * C::kZStage;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
 #pragma unroll
             for (int k = 0; k < NTO; ++k) {
                 const int nt = o * NTO + k;
-                if (i * kSS + 8 * nt < T) {
 #pragma unroll
-                    for (int h = 0; h < D / 64; ++h)
-                        tma_store_3d(tmZ, zb + (nt * (D / 64) + h) * 1024, h * 64, i * kSS + 8 * nt, chain);
+                for (int mp = 0; mp < MT; mp += 2) {
+                    const int jm = lane >> 3;
+                    const int t = 8 * nt + (lane & 7);
+                    const int chunk = 2 * (mp + (jm >> 1)) + (jm & 1);
+                    stsm_x4_t(smem_u32(zb + zswz<D>(t, chunk)),
+                              pack_bf2(yq[mp][k][0], yq[mp][k][1]), pack_bf2(yq[mp][k][2], yq[mp][k][3]),
+                              pack_bf2(yq[mp + 1][k][0], yq[mp + 1][k][1]),
+                              pack_bf2(yq[mp + 1][k][2], yq[mp + 1][k][3]));
                 }
             }
-            bulk_commit();
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < NTO; ++k) {
+                    const int nt = o * NTO + k;
+                    if (i * kSS + 8 * nt < T) {
+#pragma unroll
+                        for (int h = 0; h < D / 64; ++h)
+                            tma_store_3d(tmZ, zb + (nt * (D / 64) + h) * 1024, h * 64, i * kSS + 8 * nt, chain);
+                    }
+                }
+                bulk_commit();
+            }
         }
         if (p.loss && g == 0) {
 #pragma unroll
@@ -775,6 +807,7 @@ __device__ void role_output(const CUtensorMap *tmZ, const LinearParams &p, uint8
                     if (t < T) p.loss[tok0 + t] = L[k][e];
                 }
         }
+        if (o == 0) TTT_TRACE_AT(p, i, 11);
         warp_arrive(&R.empty[st], lane);
     }
     if (lane == 0) bulk_wait<0>();
@@ -880,7 +913,11 @@ cudaError_t launch_dsub(const LinearParams &p, int chains, cudaStream_t s)
 {
     CUtensorMap mQ, mK, mV, mZ;
     if (!make_map(&mQ, p.Q, D, p.T, chains, 16) || !make_map(&mK, p.K, D, p.T, chains, 16) ||
-        !make_map(&mV, p.V, D, p.T, chains, 16) || !make_map(&mZ, p.Z, D, p.T, chains, 8))
+        !make_map(&mV, p.V, D, p.T, chains, 16))
+        return cudaErrorInvalidValue;
+    if (p.z_f32)
+        mZ = mQ;  // not used: fp32 Z is written with plain stores
+    else if (!make_map(&mZ, p.Z, D, p.T, chains, 8))
         return cudaErrorInvalidValue;
     constexpr int smem = Cfg<D>::kSmemAlloc;
     cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<D, SUBB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -71,7 +71,7 @@ __device__ __forceinline__ void row_stats(const float *y, int d, float eps, int 
     rstd = rsqrtf(warp_sum(v) / (float)d + eps);
 }
 
-template <typename IO>
+template <typename IO, typename ZT>
 __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
 {
     extern __shared__ float sm[];
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
     const IO *Qg = static_cast<const IO *>(p.Q) + tok0 * d;
     const IO *Kg = static_cast<const IO *>(p.K) + tok0 * d;
     const IO *Vg = static_cast<const IO *>(p.V) + tok0 * d;
-    IO *Zg = static_cast<IO *>(p.Z) + tok0 * d;
+    ZT *Zg = static_cast<ZT *>(p.Z) + tok0 * d;
     const float *eg = p.eta + tok0;
     const float inv_b = 1.f / (float)b, inv_d = 1.f / (float)d;
 
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
             float L = 0.f;
             for (int j = lane; j < d; j += 32) {
                 const float z = Qt[t * d + j] + lg[j] * (y[j] - mu) * rstd + lb[j];
-                st_io<IO>(Zg + (size_t)(t0 + t) * d + j, z);
+                st_io<ZT>(Zg + (size_t)(t0 + t) * d + j, z);
                 L += (z - Vt[t * d + j]) * (z - Vt[t * d + j]);
             }
             L = warp_sum(L);
@@ -285,21 +285,22 @@ bool mlp_f32_supported(int io, int d, int hidden, int mb)
            mb >= 1 && mb <= 64 && mlp_f32_floats(d, hidden, mb) * sizeof(float) <= kMaxSmem;
 }
 
-cudaError_t launch_mlp_f32(const MlpParams &p, int io, int chains, cudaStream_t s)
+template <typename IO, typename ZT>
+cudaError_t launch_mlp_f32_t(const MlpParams &p, int chains, cudaStream_t s)
 {
     const size_t smem = mlp_f32_floats(p.d, p.hidden, p.mb) * sizeof(float);
-    cudaError_t e;
-    if (io == TTT_F32) {
-        e = cudaFuncSetAttribute(mlp_f32_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        mlp_f32_kernel<float><<<chains, kThreads, smem, s>>>(p);
-    } else {
-        e = cudaFuncSetAttribute(mlp_f32_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess) return e;
-        mlp_f32_kernel<__nv_bfloat16><<<chains, kThreads, smem, s>>>(p);
-    }
+    cudaError_t e = cudaFuncSetAttribute(mlp_f32_kernel<IO, ZT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    mlp_f32_kernel<IO, ZT><<<chains, kThreads, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_mlp_f32(const MlpParams &p, int io, int chains, cudaStream_t s)
+{
+    if (io == TTT_F32)
+        return p.z_f32 ? launch_mlp_f32_t<float, float>(p, chains, s) : launch_mlp_f32_t<float, __nv_bfloat16>(p, chains, s);
+    return p.z_f32 ? launch_mlp_f32_t<__nv_bfloat16, float>(p, chains, s)
+                   : launch_mlp_f32_t<__nv_bfloat16, __nv_bfloat16>(p, chains, s);
 }
 
 }  // namespace ttt

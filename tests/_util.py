@@ -32,21 +32,21 @@ def dev(inp: dict) -> dict:
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def run_linear(inp: dict, *, status=True, out=None):
+def run_linear(inp: dict, *, status=True, out=None, z_dtype=torch.float32):
     d = dev(inp)
     st = torch.zeros(1, dtype=torch.int32, device="cuda") if status else None
     o = ttt.ttt_linear_forward(d["Q"], d["K"], d["V"], d["eta"], d["W0"], d["c0"], d["ln_g"], d["ln_b"],
-                               mb=inp["b"], eps=inp["eps"], status=st, out=out)
+                               mb=inp["b"], eps=inp["eps"], status=st, out=out, z_dtype=z_dtype)
     torch.cuda.synchronize()
     o["status"] = st
     return o
 
 
-def run_mlp(inp: dict, *, status=True):
+def run_mlp(inp: dict, *, status=True, z_dtype=torch.float32):
     d = dev(inp)
     st = torch.zeros(1, dtype=torch.int32, device="cuda") if status else None
     o = ttt.ttt_mlp_forward(d["Q"], d["K"], d["V"], d["eta"], d["W1"], d["c1"], d["W2"], d["c2"],
-                            d["ln_g"], d["ln_b"], mb=inp["b"], eps=inp["eps"], status=st)
+                            d["ln_g"], d["ln_b"], mb=inp["b"], eps=inp["eps"], status=st, z_dtype=z_dtype)
     torch.cuda.synchronize()
     o["status"] = st
     return o
@@ -77,3 +77,18 @@ def compare(got: dict, ref: dict, keys, tol: float, sel=None) -> dict:
     bad = {k: e for k, e in errs.items() if not e <= tol}
     assert not bad, "max|err|/RMS above %.1e: %s (all: %s)" % (tol, bad, errs)
     return errs
+
+
+BF16_HALF_ULP = 2.0 ** -8   # largest relative rounding error of a bf16 value
+
+
+def check_bf16_z(z_got, z_ref, tol: float) -> float:
+    """bf16 Z: every element within tol * RMS(Z) of the oracle plus the bf16
+    format's own rounding bound 2^-8 |z|. Returns the arithmetic part of the
+    worst error, max(|err| - 2^-8 |z_ref|) / RMS(Z)."""
+    g = np.asarray(to_np(z_got) if isinstance(z_got, torch.Tensor) else z_got, np.float64)
+    r = np.asarray(z_ref, np.float64).reshape(g.shape)
+    R = rms(r)
+    excess = (np.abs(g - r) - BF16_HALF_ULP * np.abs(r)).max() / R
+    assert excess <= tol, "bf16 Z: arithmetic error %.3e * RMS(Z) above %.1e" % (excess, tol)
+    return float(excess)

@@ -12,7 +12,7 @@ import torch
 import test_weight_sequence_ttt_b300 as ttt
 from test_weight_sequence_ttt_b300.inputs import WORKLOADS, make_inputs
 
-from _util import TOL, compare, oracle_linear, rel_err, rms, run_linear, to_np
+from _util import TOL, check_bf16_z, compare, oracle_linear, rel_err, rms, run_linear, to_np
 
 pytestmark = pytest.mark.gpu
 KEYS = ("Z", "W", "c", "loss", "inner_loss")
@@ -69,6 +69,26 @@ def test_bf16_fp32_kernel_shapes():
     _check(_small(32, 16, 48), TOL["bf16"])
     assert ttt.linear_kernel_kind(ttt.BF16, 128, 64) == 1
     _check(_small(128, 64, 128, B=1, H=2), TOL["bf16"])
+
+
+@pytest.mark.parametrize("d,b", [(64, 16), (128, 4), (64, 1)])
+def test_tc_bf16_z_output(d, b):
+    """Z stored as bf16 (TMA store path): the oracle within 2e-2 RMS(Z) plus
+    the bf16 rounding of each element."""
+    inp = _small(d, b, 64)
+    got = run_linear(inp, z_dtype=torch.bfloat16)
+    assert got["Z"].dtype == torch.bfloat16 and int(got["status"].item()) == 0
+    ref = oracle_linear(inp)
+    check_bf16_z(got["Z"], ref["Z"], TOL["bf16"])
+    f32 = run_linear(inp)
+    assert torch.equal(got["Z"], f32["Z"].to(torch.bfloat16))
+    assert torch.equal(got["W"], f32["W"]) and torch.equal(got["loss"], f32["loss"])
+
+
+def test_f32_kernel_bf16_z_output():
+    inp = _small(32, 8, 32, io="f32")
+    got = run_linear(inp, z_dtype=torch.bfloat16)
+    check_bf16_z(got["Z"], oracle_linear(inp)["Z"], TOL["f32"])
 
 
 def test_per_sequence_initial_weights():
@@ -169,7 +189,7 @@ def test_resume_two_calls():
 def test_outputs_fully_written_and_optional_outputs():
     inp = _small(64, 8, 40, B=2, H=2)
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    out = {"Z": torch.full_like(dev["Q"], float("nan")),
+    out = {"Z": torch.full(dev["Q"].shape, float("nan"), device="cuda"),
            "W": torch.full((2, 2, 64, 64), float("nan"), device="cuda"),
            "c": torch.full((2, 2, 64), float("nan"), device="cuda"),
            "loss": torch.full((2, 2, 40), float("nan"), device="cuda"),
@@ -198,5 +218,5 @@ def test_host_pointer_rejected():
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     with pytest.raises(ttt.TTTError) as e:
         ttt.ttt_linear_forward(d["Q"], d["K"], d["V"], d["eta"], d["W0"], d["c0"], d["ln_g"], d["ln_b"],
-                               mb=16, out={"Z": torch.empty_like(inp["Q"]).pin_memory()})
+                               mb=16, out={"Z": torch.empty(inp["Q"].shape).pin_memory()})
     assert e.value.code in (5,)

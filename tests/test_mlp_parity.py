@@ -5,7 +5,9 @@ import pytest
 import test_weight_sequence_ttt_b300 as ttt
 from test_weight_sequence_ttt_b300.inputs import WORKLOADS, make_inputs
 
-from _util import TOL, compare, oracle_mlp, rel_err, run_mlp, to_np
+import torch
+
+from _util import TOL, check_bf16_z, compare, oracle_mlp, rel_err, run_mlp, to_np
 
 pytestmark = pytest.mark.gpu
 KEYS = ("Z", "W1", "c1", "W2", "c2", "loss", "inner_loss")
@@ -30,6 +32,12 @@ def test_mlp_bf16(d, h, b, T):
     got = run_mlp(inp)
     assert int(got["status"].item()) == 0
     compare(got, oracle_mlp(inp), KEYS, TOL["bf16"])
+
+
+def test_mlp_bf16_z_output():
+    inp = _small(64, 256, 16, 32)
+    got = run_mlp(inp, z_dtype=torch.bfloat16)
+    check_bf16_z(got["Z"], oracle_mlp(inp)["Z"], TOL["bf16"])
 
 
 def test_mlp_full_size_sampled_chains():
