@@ -136,6 +136,14 @@ typedef struct {
     int32_t *status_dev;
 } ttt_mlp_args;
 
+/* Supported: io = TTT_F32 or TTT_BF16 with d <= 256, hidden <= 1024,
+ *            mb <= 64 and the per-chain state in 227 KB of shared memory
+ *            (fp32 FFMA kernel; kind 1);
+ *            io = TTT_BF16 with d = 64, hidden = 256, mb = 16 (tensor-core
+ *            kernel, kind 2: fp16 MMA operands, fp32 accumulation, fp32 W1 in
+ *            registers and fp32 W2 in tensor memory, tanh-approximation GELU);
+ *            kind 2 wins where both apply. ttt_mlp_kernel_kind() reports the
+ *            choice. */
 ttt_status ttt_mlp_forward(const ttt_mlp_args *args, void *stream);
 
 /* ---------------------------------------------------------------------- */

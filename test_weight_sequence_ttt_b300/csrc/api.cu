@@ -88,6 +88,7 @@ int ttt_linear_kernel_kind(int32_t io, int32_t d, int32_t mb)
 
 int ttt_mlp_kernel_kind(int32_t io, int32_t d, int32_t hidden, int32_t mb)
 {
+    if (ttt::mlp_tc_supported(io, d, hidden, mb)) return 2;
     if (ttt::mlp_f32_supported(io, d, hidden, mb)) return 1;
     return 0;
 }
@@ -252,7 +253,9 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     p.loss = a->loss;
     p.inner_loss = a->inner_loss;
     p.status = a->status_dev;
-    const cudaError_t e = ttt::launch_mlp_f32(p, a->io, a->B * a->H, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        kind == 2 ? ttt::launch_mlp_tc(p, a->B * a->H, s) : ttt::launch_mlp_f32(p, a->io, a->B * a->H, s);
     return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 

@@ -13,22 +13,30 @@
 // consecutive mini-batches when b < 16). Warp roles:
 //   L (1 warp)  TMA loader: Q/K/V tiles [16 tok x d] bf16 (128B-swizzled) and
 //               eta into a ring of kStages stages.
-//   P (1 warp)  prep: fp16 copies of the K/Q tiles; Gram fragments: causal
-//               Q K^T + 1 and (b < 16) K K^T + 1.
+//   P (1 warp)  prep: fp16 copies of the K/Q tiles; Gram fragments (causal
+//               Q_i K_i^T + 1, K_{i-1} K_i^T + 1 and, for b < 16, K_i K_i^T + 1);
+//               per token: the LayerNorm shift u0.k + mean(c0) and the sums
+//               sum_f gamma_f kv_f, sum_f kv_f^2 with kv = k - v + beta.
 //   W (d/16)    warp w owns rows 16w..16w+15 of W and c as fp32 mma
 //               accumulators in registers for the whole sequence, and runs the
-//               serial chain for those rows:
-//                 Y^T = W K^T + c,  Rq^T = W Q^T + c        (mma, fp16 operands)
-//                 LayerNorm statistics of every token's column of Y^T, summed
-//                 over the W warps through shared memory + a named barrier
-//                 G = dl/dY (LN backward, a second barrier round)
-//                 A~ = -(eta/b) G^T (its own rows), then W += A~ K, c += A~ 1
-//                 Yq^T = Rq^T + A~ Mq   (Mq = causal Q K^T + 1: in-batch prefix)
+//               serial chain for those rows.
 //   O (2)       output: Z = Q + LN(Yq), L_t = ||z_t - v_t||^2, Z stores.
 //
-// Per super-step the W warps synchronise with each other twice per mini-batch
-// (LayerNorm forward statistics, then backward sums); everything else moves
-// through mbarriers between roles, all of them bounded waits.
+// The serial chain of one super-step i (W warps) is
+//   LayerNorm forward + backward of Y_i^T (one cross-warp reduction round per
+//   mini-batch) -> A~_i = -(eta/b) G_i^T -> Y_{i+1}^T = S_{i+1} + A~_i Kx_i
+// where S_{i+1} = W_{i-1} K_{i+1}^T + c_{i-1} and Rq_i = W_{i-1} Q_i^T + c_{i-1}
+// are computed while the reduction round is in flight, and Kx_i = K_i K_{i+1}^T
+// + 1. Exact in real arithmetic (W_i = W_{i-1} + A~_i K_i); it reorders rounding
+// only. Off the chain: W += A~_i K_i, c += A~_i 1, Yq_i^T = Rq_i + A~_i Mq_i.
+//
+// One reduction round. The feature mean of Y is invariant under the update
+// (the LayerNorm gradient sums to zero over features, so the column sums of W
+// and the sum of c never change), so sh_t = u0.k_t + mean(c0), with u0 the
+// feature mean of W_0's rows, is the token's LN mean up to rounding drift. Each
+// W warp sums, over its rows, d = y - sh: d, d^2, gamma^2 d, gamma^2 d^2 and
+// gamma kv d; the five sums of the W warps add up (split-phase mbarrier) and give
+// the mean, variance and the two LayerNorm-backward means in closed form.
 //
 // Precision. MMA operands are fp16 (10-bit mantissa) with fp32 accumulation;
 // W, c, LayerNorm statistics and gradients stay fp32. Inputs and W must stay
@@ -38,17 +46,13 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
-#include "ptx.cuh"
-#include "ttt_internal.h"
+#include "tc_common.cuh"
 
 namespace ttt {
 namespace {
 
-constexpr int kSS = 16;       // tokens per super-step
+using namespace tc;
 constexpr int kStages = 6;    // input ring depth
-constexpr unsigned kFull = 0xffffffffu;
-constexpr int kBarStats = 1;  // named barrier ids (0 is __syncthreads)
-constexpr int kBarBwd = 2;
 
 template <int D>
 struct Cfg {
@@ -65,17 +69,22 @@ struct Cfg {
     static constexpr int kTile = 32 * D;             // 16 rows x D x 2 B
     static constexpr int kOffK = 0, kOffQ = kTile, kOffV = 2 * kTile;  // bf16, as loaded
     static constexpr int kOffKh = 3 * kTile, kOffQh = 4 * kTile;      // fp16 copies (same layout)
-    static constexpr int kOffMq = 5 * kTile;
+    static constexpr int kOffMq = 5 * kTile;         // fp16 B fragments, 32 lanes x 16 B each
     static constexpr int kOffGk = kOffMq + 512;
-    static constexpr int kOffEta = kOffGk + 512;     // 16 floats
-    static constexpr int kStageBytes = ((kOffEta + 64 + 1023) / 1024) * 1024;
+    static constexpr int kOffKx = kOffGk + 512;
+    static constexpr int kOffEta = kOffKx + 512;     // 16 floats each:
+    static constexpr int kOffSh = kOffEta + 64;      //   LayerNorm shift
+    static constexpr int kOffPk = kOffSh + 64;       //   sum_f gamma_f kv_f
+    static constexpr int kOffQk = kOffPk + 64;       //   sum_f kv_f^2
+    static constexpr int kStageBytes = ((kOffQk + 64 + 1023) / 1024) * 1024;
     static constexpr int YS = D + 4;                 // row stride (floats) of the Yq^T hand-off
     static constexpr int kOffStages = 0;
     static constexpr int kOffY = kStages * kStageBytes;            // 2 slots x [16][YS] fp32
-    static constexpr int kOffRedA = kOffY + 2 * kSS * YS * 4;     // [MT][16] float2
-    static constexpr int kOffRedB = kOffRedA + MT * kSS * 8;      // [MT][16] float4
-    static constexpr int kOffBar = kOffRedB + MT * kSS * 16;
-    static constexpr int kNumBars = 3 * kStages + 4;
+    static constexpr int kOffRedX = kOffY + 2 * kSS * YS * 4;     // 2 bufs x [MT][16] float4
+    static constexpr int kOffRedY = kOffRedX + 2 * MT * kSS * 16; // 2 bufs x [MT][16] float
+    static constexpr int kOffCst = kOffRedY + 2 * MT * kSS * 4;   // u0, gamma, beta: 3 x D floats
+    static constexpr int kOffBar = kOffCst + 3 * D * 4;
+    static constexpr int kNumBars = 3 * kStages + 6;
     static constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
     static constexpr int kSmemAlloc = kSmem + 1024;                // slack for alignment
     static_assert(FPL % 4 == 0, "output lanes hold whole 4-feature chunks");
@@ -83,63 +92,14 @@ struct Cfg {
 
 // Barrier map (all in shared memory):
 //   full[s]   TMA Q/K/V + cp.async eta landed in stage s      (L -> P, W, O)
-//   prep[s]   P finished stage s (fp16 tiles, Grams)           (P -> W, O)
+//   prep[s]   P finished stage s (fp16 tiles, Grams, sums)     (P -> W, O)
 //   empty[s]  every consumer is done with stage s              (P, W, O -> L)
 //   yfull/yempty[2]  Yq^T hand-off                            (W <-> O)
+//   red[2]    the W warps' partial LayerNorm sums of one round (W -> W)
 struct Ring {
-    uint64_t *full, *prep, *empty, *yfull, *yempty;
+    uint64_t *full, *prep, *empty, *yfull, *yempty, *red;
     volatile int *flags;  // [0] abort, [1] fp16 range violation seen
 };
-
-__device__ __forceinline__ uint32_t parity_of(int use) { return (uint32_t)(use & 1); }
-
-// Byte offset of the 16-byte chunk (row r, chunk j) of a [16 x D] 2-byte tile
-// loaded by TMA with 128-byte swizzle as D/64 boxes of 64 columns.
-__device__ __forceinline__ uint32_t swz(int r, int j)
-{
-    return (uint32_t)((j >> 3) * 2048 + r * 128 + (((j & 7) ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ void record(int *status, int code)
-{
-    if (status) atomicCAS(status, 0, code);
-}
-
-// Bounded wait that also gives up as soon as another warp has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *flags)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (flags[0]) return false;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-__device__ __forceinline__ void abort_chain(volatile int *flags, int *status)
-{
-    flags[0] = 1;
-    record(status, TTT_ERR_TIMEOUT);
-}
-
-__device__ __forceinline__ void warp_arrive(uint64_t *bar, int lane)
-{
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar);
-}
-
-// Sum over the 8 lanes that share (lane & 3): the row axis of an mma
-// accumulator tile, i.e. the feature axis of a transposed activation.
-__device__ __forceinline__ float col_sum(float v)
-{
-    v += __shfl_xor_sync(kFull, v, 4);
-    v += __shfl_xor_sync(kFull, v, 8);
-    v += __shfl_xor_sync(kFull, v, 16);
-    return v;
-}
-
-__device__ __forceinline__ float round_h(float v) { return __half2float(__float2half_rn(v)); }
 
 template <int D>
 __device__ __forceinline__ uint8_t *stage_ptr(uint8_t *sm, int st)
@@ -147,67 +107,37 @@ __device__ __forceinline__ uint8_t *stage_ptr(uint8_t *sm, int st)
     return sm + Cfg<D>::kOffStages + st * Cfg<D>::kStageBytes;
 }
 
-// ------------------------------------------------------------------ L: loader
-template <int D>
-__device__ void role_loader(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
-                            const LinearParams &p, uint8_t *sm, const Ring &R, int chain, int lane,
-                            int nsteps)
-{
-    using C = Cfg<D>;
-    const int T = p.T;
-    const float *eta = p.eta + (size_t)chain * T;
-    if (lane == 0) {
-        prefetch_tmap(tmQ);
-        prefetch_tmap(tmK);
-        prefetch_tmap(tmV);
-    }
-    int issued = 0;
-    for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kStages;
-        if (!wait_bar(&R.empty[st], parity_of(i / kStages) ^ 1u, R.flags)) {
-            abort_chain(R.flags, p.status);
-            break;
-        }
-        TTT_TRACE_AT(p, i, 14);
-        uint8_t *stg = stage_ptr<D>(sm, st);
-        const int t0 = i * kSS;
-        float *se = reinterpret_cast<float *>(stg + C::kOffEta);
-        if (lane < kSS) {
-            const int t = t0 + lane;
-            cp_async_4(se + lane, eta + (t < T ? t : 0), t < T ? 4u : 0u);  // zero-fill past T
-        }
-        cp_async_mbar_arrive_noinc(&R.full[st]);
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&R.full[st], 3 * C::kTile);
-#pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-                tma_load_3d(stg + C::kOffK + h * 2048, tmK, &R.full[st], h * 64, t0, chain);
-                tma_load_3d(stg + C::kOffQ + h * 2048, tmQ, &R.full[st], h * 64, t0, chain);
-                tma_load_3d(stg + C::kOffV + h * 2048, tmV, &R.full[st], h * 64, t0, chain);
-            }
-        }
-        issued = i + 1;
-    }
-    // Never leave while a copy issued here may still be landing in shared memory.
-    for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        (void)mbar_wait(&R.full[i % kStages], parity_of(i / kStages));
-}
-
 // ------------------------------------------------------------------ P: prep
-// Two bf16 values (one 32-bit word) -> fp16x2, round to nearest even.
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w)
-{
-    return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
 template <int D, int SUBB>
-__device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int lane, int nsteps)
+__device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int bi, int hi, int lane, int nsteps)
 {
     using C = Cfg<D>;
     const int g = lane >> 2, c4 = lane & 3;
+    // Constants of the chain: u0 = feature mean of W_0's rows, mean(c0), gamma, beta.
+    float *cu = reinterpret_cast<float *>(sm + C::kOffCst), *cg = cu + D, *cbt = cg + D;
+    {
+        const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
+        for (int j = lane; j < D; j += 32) {
+            float s = 0.f;
+            for (int f = 0; f < D; ++f) s += W0[f * D + j];
+            cu[j] = s * (1.f / (float)D);
+            cg[j] = p.ln_g[hi * D + j];
+            cbt[j] = p.ln_b[hi * D + j];
+        }
+    }
+    float cmean = 0.f;
+    {
+        const float *c0 = p.c0 + bi * p.c0_bstride + (long long)hi * D;
+        for (int j = lane; j < D; j += 32) cmean += c0[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cmean += __shfl_xor_sync(kFull, cmean, o);
+        cmean *= 1.f / (float)D;
+    }
+    __syncwarp();
     uint32_t mag = 0;  // per-halfword max of |bf16 bits|: >= 0x4780 means |x| >= 2^16 (or inf/nan)
     const int ra = (lane & 7) + ((lane >> 3) & 1) * 8;  // A-fragment row (ldmatrix x4)
     const int rb = (lane & 7) + (lane >> 4) * 8;        // B-fragment row
+    const int tt = lane & 15, half = lane >> 4;         // per-token sums: token, half of the features
     for (int i = 0; i < nsteps; ++i) {
         const int st = i % kStages;
         if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
@@ -229,25 +159,69 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
                 dst[ch] = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
             }
         }
+        // (2) per-token LayerNorm shift and kv sums (bf16 inputs, fp32 sums).
+        {
+            float shs = 0.f, ps = 0.f, qs = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < D / 16; ++ch) {
+                const int j = half * (D / 16) + ch;  // 16-byte chunk (8 features)
+                const uint4 kb = *reinterpret_cast<const uint4 *>(stg + C::kOffK + swz(tt, j));
+                const uint4 vb = *reinterpret_cast<const uint4 *>(stg + C::kOffV + swz(tt, j));
+                const uint32_t kw[4] = {kb.x, kb.y, kb.z, kb.w}, vw[4] = {vb.x, vb.y, vb.z, vb.w};
+                const float4 *u4 = reinterpret_cast<const float4 *>(cu + 8 * j);
+                const float4 *g4 = reinterpret_cast<const float4 *>(cg + 8 * j);
+                const float4 *b4 = reinterpret_cast<const float4 *>(cbt + 8 * j);
+                const float4 uu[2] = {u4[0], u4[1]}, gg[2] = {g4[0], g4[1]}, bb[2] = {b4[0], b4[1]};
+                const float uf[8] = {uu[0].x, uu[0].y, uu[0].z, uu[0].w, uu[1].x, uu[1].y, uu[1].z, uu[1].w};
+                const float gf[8] = {gg[0].x, gg[0].y, gg[0].z, gg[0].w, gg[1].x, gg[1].y, gg[1].z, gg[1].w};
+                const float bf[8] = {bb[0].x, bb[0].y, bb[0].z, bb[0].w, bb[1].x, bb[1].y, bb[1].z, bb[1].w};
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t kbits = q & 1 ? kw[q >> 1] >> 16 : kw[q >> 1] & 0xffffu;
+                    const uint32_t vbits = q & 1 ? vw[q >> 1] >> 16 : vw[q >> 1] & 0xffffu;
+                    const float kf = bf16_bits_to_f32(kbits), vf = bf16_bits_to_f32(vbits);
+                    const float kv = kf - vf + bf[q];
+                    shs = fmaf(uf[q], kf, shs);
+                    ps = fmaf(gf[q], kv, ps);
+                    qs = fmaf(kv, kv, qs);
+                }
+            }
+            shs += __shfl_xor_sync(kFull, shs, 16);
+            ps += __shfl_xor_sync(kFull, ps, 16);
+            qs += __shfl_xor_sync(kFull, qs, 16);
+            if (half == 0) {
+                reinterpret_cast<float *>(stg + C::kOffSh)[tt] = shs + cmean;
+                reinterpret_cast<float *>(stg + C::kOffPk)[tt] = ps;
+                reinterpret_cast<float *>(stg + C::kOffQk)[tt] = qs;
+            }
+        }
         __syncwarp();
-        // (2) Gram fragments. d*[j][r] holds (t = g + 8(r>>1), s = 8j + 2c4 + (r&1)).
+        // (3) Gram fragments. d*[j][r] holds (t = g + 8(r>>1), s = 8j + 2c4 + (r&1)):
+        //     dq = Q_i K_i^T, dk = K_i K_i^T, dx = K_i K_{i-1}^T (t in step i, s in step i-1).
         const uint32_t sK = smem_u32(stg + C::kOffKh), sQ = smem_u32(stg + C::kOffQh);
-        float dq[2][4] = {}, dk[2][4] = {};
+        const uint32_t sKp = smem_u32(stage_ptr<D>(sm, (i + kStages - 1) % kStages) + C::kOffKh);
+        const bool has_prev = i > 0;
+        float dq[2][4] = {}, dk[2][4] = {}, dx[2][4] = {};
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            uint32_t aq[4], bk[4];
+            uint32_t aq[4], ak[4], bk[4];
             ldsm_x4(aq, sQ + swz(ra, 2 * ks + (lane >> 4)));
             ldsm_x4(bk, sK + swz(rb, 2 * ks + ((lane >> 3) & 1)));
             mma16816(dq[0], aq, bk[0], bk[1]);
             mma16816(dq[1], aq, bk[2], bk[3]);
+            if (SUBB < 16 || has_prev) ldsm_x4(ak, sK + swz(ra, 2 * ks + (lane >> 4)));
             if (SUBB < 16) {
-                uint32_t ak[4];
-                ldsm_x4(ak, sK + swz(ra, 2 * ks + (lane >> 4)));
                 mma16816(dk[0], ak, bk[0], bk[1]);
                 mma16816(dk[1], ak, bk[2], bk[3]);
             }
+            if (has_prev) {
+                uint32_t bp[4];
+                ldsm_x4(bp, sKp + swz(rb, 2 * ks + ((lane >> 3) & 1)));
+                mma16816(dx[0], ak, bp[0], bp[1]);
+                mma16816(dx[1], ak, bp[2], bp[3]);
+            }
         }
-        // Causal Q K^T + 1 as B fragments (k = s, n = t) for the W warps.
+        // As B fragments (k = s, n = t) for the W warps.
         auto mq = [&](int j, int r) {
             const int t = g + 8 * (r >> 1), s = 8 * j + 2 * c4 + (r & 1);
             return s <= t ? dq[j][r] + 1.f : 0.f;
@@ -260,10 +234,16 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
                 pack_h2(dk[0][0] + 1.f, dk[0][1] + 1.f), pack_h2(dk[1][0] + 1.f, dk[1][1] + 1.f),
                 pack_h2(dk[0][2] + 1.f, dk[0][3] + 1.f), pack_h2(dk[1][2] + 1.f, dk[1][3] + 1.f));
         }
+        if (has_prev) {
+            reinterpret_cast<uint4 *>(stg + C::kOffKx)[lane] = make_uint4(
+                pack_h2(dx[0][0] + 1.f, dx[0][1] + 1.f), pack_h2(dx[1][0] + 1.f, dx[1][1] + 1.f),
+                pack_h2(dx[0][2] + 1.f, dx[0][3] + 1.f), pack_h2(dx[1][2] + 1.f, dx[1][3] + 1.f));
+        }
         warp_arrive(&R.prep[st], lane);
         TTT_TRACE_AT(p, i, 13);
-        if (lane == 0) mbar_arrive(&R.empty[st]);
+        if (has_prev && lane == 0) mbar_arrive(&R.empty[(i + kStages - 1) % kStages]);  // K_{i-1} no longer read
     }
+    if (nsteps > 0 && lane == 0) mbar_arrive(&R.empty[(nsteps - 1) % kStages]);
     const bool range_bad = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
     if (__any_sync(kFull, range_bad) && lane == 0) {
         R.flags[1] = 1;
@@ -272,13 +252,34 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
 }
 
 // ------------------------------------------------------------------ W: weight + chain warps
+// acc (this warp's 16 rows x 16 tokens) = c + W tile^T, W packed to fp16 on the fly.
+template <int D>
+__device__ __forceinline__ void rows_gemm(const float (&Wa)[D / 8][4], const float (&cb)[2], uint32_t tile, int lane,
+                                          float (&acc)[2][4])
+{
+    const int rb = (lane & 7) + (lane >> 4) * 8, cb16 = (lane >> 3) & 1;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[nt][r] = cb[r >> 1];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint32_t af[4] = {pack_h2(Wa[2 * ks][0], Wa[2 * ks][1]), pack_h2(Wa[2 * ks][2], Wa[2 * ks][3]),
+                                pack_h2(Wa[2 * ks + 1][0], Wa[2 * ks + 1][1]),
+                                pack_h2(Wa[2 * ks + 1][2], Wa[2 * ks + 1][3])};
+        uint32_t bk[4];
+        ldsm_x4(bk, tile + swz(rb, 2 * ks + cb16));
+        mma16816(acc[0], af, bk[0], bk[1]);
+        mma16816(acc[1], af, bk[2], bk[3]);
+    }
+}
+
 template <int D, int SUBB>
 __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int chain, int bi,
                              int hi, size_t tok0, int lane, int nsteps)
 {
     using C = Cfg<D>;
     constexpr int MT = C::MT, NTW = D / 8, NSUB = kSS / SUBB;
-    constexpr int kNThr = MT * 32;
     const int g = lane >> 2, c4 = lane & 3;
     const int r0 = 16 * w + g, r1 = r0 + 8;
     const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
@@ -296,53 +297,40 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
     float cb[2] = {c0[r0], c0[r1]};
     const float gam[2] = {p.ln_g[hi * D + r0], p.ln_g[hi * D + r1]};
     const float bet[2] = {p.ln_b[hi * D + r0], p.ln_b[hi * D + r1]};
+    float gam2all = 0.f;  // sum of gamma^2 over all features
+    for (int f = 0; f < D; ++f) gam2all = fmaf(p.ln_g[hi * D + f], p.ln_g[hi * D + f], gam2all);
     const int rb = (lane & 7) + (lane >> 4) * 8;        // ldmatrix row, non-transposed B
     const int cb16 = (lane >> 3) & 1;
     const int rt = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row, transposed B
     const int ct = lane >> 4;
     const float invD = 1.f / (float)D, eps = p.eps;
-    float2 *redA = reinterpret_cast<float2 *>(sm + C::kOffRedA);
-    float4 *redB = reinterpret_cast<float4 *>(sm + C::kOffRedB);
     const int T = p.T;
 
+    // Prologue: Y_0^T = W_0 K_0^T + c_0.
+    float yk[2][4];
+    if (!wait_bar(&R.full[0], 0u, R.flags) || !wait_bar(&R.prep[0], 0u, R.flags)) {
+        abort_chain(R.flags, p.status);
+        return;
+    }
+    rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, 0) + C::kOffKh), lane, yk);
+
+    int rnd = 0;  // reduction rounds so far (buffer rnd & 1, phase (rnd >> 1) & 1)
     for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kStages, slot = i & 1;
+        const int st = i % kStages, slot = i & 1, stn = (i + 1) % kStages;
+        const bool has_next = i + 1 < nsteps;
         uint8_t *stg = stage_ptr<D>(sm, st);
+        uint8_t *stgn = stage_ptr<D>(sm, stn);
         if (w == 0) TTT_TRACE_AT(p, i, 0);
-        bool bad = !wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
-                   !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags) ||
-                   !wait_bar(&R.yempty[slot], parity_of(i >> 1) ^ 1u, R.flags);
-        if (bad) abort_chain(R.flags, p.status);
-        if (w == 0) TTT_TRACE_AT(p, i, 1);
-        // Y^T = W_{i-1} K_i^T + c and Rq^T = W_{i-1} Q_i^T + c (this warp's 16 rows).
-        float yk[2][4], yq[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) yk[nt][r] = yq[nt][r] = cb[r >> 1];
-        if (!bad) {
-            const uint32_t sK = smem_u32(stg + C::kOffKh), sQ = smem_u32(stg + C::kOffQh);
-#pragma unroll
-            for (int ks = 0; ks < MT; ++ks) {
-                const uint32_t af[4] = {pack_h2(Wa[2 * ks][0], Wa[2 * ks][1]), pack_h2(Wa[2 * ks][2], Wa[2 * ks][3]),
-                                        pack_h2(Wa[2 * ks + 1][0], Wa[2 * ks + 1][1]),
-                                        pack_h2(Wa[2 * ks + 1][2], Wa[2 * ks + 1][3])};
-                uint32_t bk[4], bq[4];
-                ldsm_x4(bk, sK + swz(rb, 2 * ks + cb16));
-                ldsm_x4(bq, sQ + swz(rb, 2 * ks + cb16));
-                mma16816(yk[0], af, bk[0], bk[1]);
-                mma16816(yk[1], af, bk[2], bk[3]);
-                mma16816(yq[0], af, bq[0], bq[1]);
-                mma16816(yq[1], af, bq[2], bq[3]);
-            }
+        bool ok = true;  // stage i's full/prep were waited for as "next" (or in the prologue)
+        if (has_next)
+            ok = ok && wait_bar(&R.full[stn], parity_of((i + 1) / kStages), R.flags) &&
+                 wait_bar(&R.prep[stn], parity_of((i + 1) / kStages), R.flags);
+        ok = ok && wait_bar(&R.yempty[slot], parity_of(i >> 1) ^ 1u, R.flags);
+        if (!ok) {
+            abort_chain(R.flags, p.status);
+            return;
         }
-        if (w == 0) TTT_TRACE_AT(p, i, 2);
-        const float *se = reinterpret_cast<const float *>(stg + C::kOffEta);
-        float escale[2][2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) escale[nt][e] = -se[8 * nt + 2 * c4 + e] * (1.f / (float)SUBB);
+        if (w == 0) TTT_TRACE_AT(p, i, 1);
         // K - V + beta in this warp's accumulator order: ldmatrix.trans of the
         // bf16 tiles hands each lane tokens (2c4, 2c4+1) of features g, g+8.
         float kv[2][4];
@@ -359,104 +347,126 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
                     kv[nt][2 * u + 1] = bf16_bits_to_f32(a >> 16) - bf16_bits_to_f32(b >> 16) + bet[u];
                 }
         }
+        // Per-column (token) scalars of this lane's four columns t = 8nt + 2c4 + e.
+        const float *ssh = reinterpret_cast<const float *>(stg + C::kOffSh);
+        float escale[2][2], shv[2][2];
+        {
+            const float *se = reinterpret_cast<const float *>(stg + C::kOffEta);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float2 e2 = *reinterpret_cast<const float2 *>(se + 8 * nt + 2 * c4);
+                const float2 s2 = *reinterpret_cast<const float2 *>(ssh + 8 * nt + 2 * c4);
+                escale[nt][0] = -e2.x * (1.f / (float)SUBB);
+                escale[nt][1] = -e2.y * (1.f / (float)SUBB);
+                shv[nt][0] = s2.x;
+                shv[nt][1] = s2.y;
+            }
+        }
+        // The column this lane combines across the W warps (lanes g and g + 4
+        // duplicate); its results reach the lanes that hold it by shuffles.
+        const int tc = 8 * (g & 1) + 2 * c4 + ((g >> 1) & 1);
+        const float sh_c = ssh[tc];
+        const float pk_c = reinterpret_cast<const float *>(stg + C::kOffPk)[tc];
+        const float qk_c = reinterpret_cast<const float *>(stg + C::kOffQk)[tc];
         float at[2][4] = {};   // A~ = -(eta/b) G, fp16-rounded, every column once set
         float lin[2][2] = {};  // inner loss of each column
+        float Sn[2][4], Rq[2][4];
 #pragma unroll
         for (int m = 0; m < NSUB; ++m) {
-            // --- LayerNorm statistics: this warp's 16 rows, then all W warps (parallel variance).
-            float mw[2][2], m2w[2][2];
+            // --- this warp's shifted sums over its 16 rows, for every column.
+            float s1[2][2], s2[2][2], sb[2][2], sc[2][2], sd[2][2];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const float mloc = col_sum(yk[nt][e] + yk[nt][e + 2]) * (1.f / 16.f);
-                    const float a = yk[nt][e] - mloc, b2 = yk[nt][e + 2] - mloc;
-                    mw[nt][e] = mloc;
-                    m2w[nt][e] = col_sum(a * a + b2 * b2);
-                }
-            if (g == 0) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) redA[w * kSS + 8 * nt + 2 * c4 + e] = make_float2(mw[nt][e], m2w[nt][e]);
-            }
-            if (named_bar_or(kBarStats, kNThr, bad || R.flags[0] != 0)) {
-                abort_chain(R.flags, p.status);
-                return;  // every W warp takes this branch together
-            }
-            float mu[2][2], rs[2][2];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = 8 * nt + 2 * c4 + e;
-                    float2 part[MT];
-                    float s = 0.f;
-#pragma unroll
-                    for (int u = 0; u < MT; ++u) {
-                        part[u] = redA[u * kSS + t];
-                        s += part[u].x;
-                    }
-                    const float mean = s * (1.f / (float)MT);
-                    float m2 = 0.f;
-#pragma unroll
-                    for (int u = 0; u < MT; ++u) {
-                        const float dm = part[u].x - mean;
-                        m2 += part[u].y + 16.f * dm * dm;
-                    }
-                    mu[nt][e] = mean;
-                    rs[nt][e] = rsqrtf(m2 * invD + eps);
-                }
-            // --- LayerNorm backward sums: m1 = sum dh, m2 = sum dh*yh, l = sum E^2, dh = 2 gamma E.
-            float s1[2][2], s2[2][2], sl[2][2];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float a1 = 0.f, a2 = 0.f, al = 0.f;
+                    float a1 = 0.f, a2 = 0.f, ab = 0.f, ac = 0.f, ad = 0.f;
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const float yh = (yk[nt][e + 2 * u] - mu[nt][e]) * rs[nt][e];
-                        const float E = gam[u] * yh + kv[nt][e + 2 * u];
-                        const float dh = 2.f * gam[u] * E;
-                        a1 += dh;
-                        a2 += dh * yh;
-                        al += E * E;
+                        const float dv = yk[nt][e + 2 * u] - shv[nt][e];
+                        const float g2d = gam[u] * gam[u] * dv;
+                        a1 += dv;
+                        a2 = fmaf(dv, dv, a2);
+                        ab += g2d;
+                        ac = fmaf(g2d, dv, ac);
+                        ad = fmaf(gam[u] * kv[nt][e + 2 * u], dv, ad);
                     }
                     s1[nt][e] = col_sum(a1);
                     s2[nt][e] = col_sum(a2);
-                    sl[nt][e] = col_sum(al);
+                    sb[nt][e] = col_sum(ab);
+                    sc[nt][e] = col_sum(ac);
+                    sd[nt][e] = col_sum(ad);
                 }
+            if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 5);
+            const int buf = rnd & 1;
+            float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
+            float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
             if (g == 0) {
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        redB[w * kSS + 8 * nt + 2 * c4 + e] = make_float4(s1[nt][e], s2[nt][e], sl[nt][e], 0.f);
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = 8 * nt + 2 * c4 + e;
+                        redX[w * kSS + t] = make_float4(s1[nt][e], s2[nt][e], sb[nt][e], sc[nt][e]);
+                        redY[w * kSS + t] = sd[nt][e];
+                    }
             }
-            named_bar_sync(kBarBwd, kNThr);
+            warp_arrive(&R.red[buf], lane);
+            if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 6);
+            if (m == 0) {
+                // Independent tensor-core work while the other W warps finish their sums:
+                // S_{i+1} = W_{i-1} K_{i+1}^T + c_{i-1}, Rq_i = W_{i-1} Q_i^T + c_{i-1}.
+                if (has_next) rows_gemm<D>(Wa, cb, smem_u32(stgn + C::kOffKh), lane, Sn);
+                rows_gemm<D>(Wa, cb, smem_u32(stg + C::kOffQh), lane, Rq);
+                if (w == 0) TTT_TRACE_AT(p, i, 2);
+            }
+            if (!wait_bar(&R.red[buf], parity_of(rnd >> 1), R.flags)) {
+                abort_chain(R.flags, p.status);
+                return;
+            }
+            ++rnd;
+            if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 7);
+            // Combine column tc over the W warps: moments about mu = sh + ee.
+            float mu_c, rs_c, M1_c, M2_c, LE_c;
+            {
+                float S1 = 0.f, S2 = 0.f, SB = 0.f, SC = 0.f, SD = 0.f;
+#pragma unroll
+                for (int u = 0; u < MT; ++u) {
+                    const float4 x = redX[u * kSS + tc];
+                    S1 += x.x;
+                    S2 += x.y;
+                    SB += x.z;
+                    SC += x.w;
+                    SD += redY[u * kSS + tc];
+                }
+                const float ee = S1 * invD;
+                const float syy = fmaxf(fmaf(-ee, S1, S2), 0.f);                    // sum (y - mu)^2
+                rs_c = rsqrtf(syy * invD + eps);
+                const float sg1 = fmaf(-ee, gam2all, SB);                             // sum g^2 (y - mu)
+                const float sg2 = fmaf(ee * ee, gam2all, fmaf(-2.f * ee, SB, SC));   // sum g^2 (y - mu)^2
+                const float sgk = fmaf(-ee, pk_c, SD);                                // sum g kv (y - mu)
+                M1_c = 2.f * invD * fmaf(rs_c, sg1, pk_c);                            // mean of dh
+                M2_c = 2.f * invD * rs_c * fmaf(rs_c, sg2, sgk);                      // mean of dh * yh
+                LE_c = fmaf(rs_c, fmaf(rs_c, sg2, 2.f * sgk), qk_c);                 // sum E^2
+                mu_c = sh_c + ee;
+            }
             float ad[2][4];  // this mini-batch's A~ columns (zero elsewhere)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int t = 8 * nt + 2 * c4 + e;
-                    float M1 = 0.f, M2 = 0.f, LE = 0.f;
-#pragma unroll
-                    for (int u = 0; u < MT; ++u) {
-                        const float4 q = redB[u * kSS + t];
-                        M1 += q.x;
-                        M2 += q.y;
-                        LE += q.z;
-                    }
-                    M1 *= invD;
-                    M2 *= invD;
+                    const int src = (nt + 2 * e) * 4 + c4;
+                    const float mu = __shfl_sync(kFull, mu_c, src);
+                    const float rs = __shfl_sync(kFull, rs_c, src);
+                    const float M1 = __shfl_sync(kFull, M1_c, src);
+                    const float M2 = __shfl_sync(kFull, M2_c, src);
+                    const float LE = __shfl_sync(kFull, LE_c, src);
                     const bool in_m = NSUB == 1 || t / SUBB == m;
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const float yh = (yk[nt][e + 2 * u] - mu[nt][e]) * rs[nt][e];
-                        const float E = gam[u] * yh + kv[nt][e + 2 * u];
-                        const float G = rs[nt][e] * (2.f * gam[u] * E - M1 - yh * M2);
+                        const float yh = (yk[nt][e + 2 * u] - mu) * rs;
+                        const float E = fmaf(gam[u], yh, kv[nt][e + 2 * u]);
+                        const float G = rs * (2.f * gam[u] * E - M1 - yh * M2);
                         const float a = round_h(escale[nt][e] * G);
                         ad[nt][e + 2 * u] = in_m ? a : 0.f;
                         if (in_m) at[nt][e + 2 * u] = a;
@@ -475,9 +485,19 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
             }
         }
         if (w == 0) TTT_TRACE_AT(p, i, 3);
-        // W += A~ K_i, c += A~ 1   (W_{i-1} -> W_i for this warp's rows)
         const uint32_t af[4] = {pack_h2(at[0][0], at[0][1]), pack_h2(at[0][2], at[0][3]),
                                 pack_h2(at[1][0], at[1][1]), pack_h2(at[1][2], at[1][3])};
+        // The chain: Y_{i+1}^T = S_{i+1} + A~_i (K_i K_{i+1}^T + 1).
+        if (has_next) {
+            const uint4 kx = reinterpret_cast<const uint4 *>(stgn + C::kOffKx)[lane];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) yk[nt][r] = Sn[nt][r];
+            mma16816(yk[0], af, kx.x, kx.y);
+            mma16816(yk[1], af, kx.z, kx.w);
+        }
+        // W += A~ K_i, c += A~ 1   (W_{i-1} -> W_i for this warp's rows)
         {
             const uint32_t sK = smem_u32(stg + C::kOffKh);
 #pragma unroll
@@ -499,15 +519,16 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
         // Yq^T = Rq^T + A~ Mq (in-batch prefix of every query) -> output warps.
         {
             const uint4 mq = reinterpret_cast<const uint4 *>(stg + C::kOffMq)[lane];
-            mma16816(yq[0], af, mq.x, mq.y);
-            mma16816(yq[1], af, mq.z, mq.w);
+            mma16816(Rq[0], af, mq.x, mq.y);
+            mma16816(Rq[1], af, mq.z, mq.w);
         }
+        if (w == 0) TTT_TRACE_AT(p, i, 11);
         float *ys = reinterpret_cast<float *>(sm + C::kOffY + slot * kSS * C::YS * 4);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int r = 0; r < 4; ++r)
-                ys[(8 * nt + 2 * c4 + (r & 1)) * C::YS + 16 * w + g + 8 * (r >> 1)] = yq[nt][r];
+                ys[(8 * nt + 2 * c4 + (r & 1)) * C::YS + 16 * w + g + 8 * (r >> 1)] = Rq[nt][r];
         warp_arrive(&R.yfull[slot], lane);
         if (w == 0) TTT_TRACE_AT(p, i, 4);
         if (p.inner_loss && w == 0 && g == 0) {
@@ -664,6 +685,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     R.empty = bar + 2 * kStages;
     R.yfull = bar + 3 * kStages;
     R.yempty = R.yfull + 2;
+    R.red = R.yfull + 4;
     R.flags = reinterpret_cast<volatile int *>(bar + C::kNumBars);
 
     if (threadIdx.x == 0) {
@@ -675,6 +697,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         for (int j = 0; j < 2; ++j) {
             mbar_init(&R.yfull[j], C::MT);
             mbar_init(&R.yempty[j], C::NO);
+            mbar_init(&R.red[j], C::MT);
         }
         R.flags[0] = 0;
         R.flags[1] = 0;
@@ -684,9 +707,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (nsteps == 0) return;
 
     if (warp == C::kWarpL) {
-        role_loader<D>(&tmQ, &tmK, &tmV, p, sm, R, chain, lane, nsteps);
+        const StageGeom geom{kStages, C::kStageBytes, C::kOffK, C::kOffQ, C::kOffV, C::kOffEta};
+        role_loader<D>(&tmQ, &tmK, &tmV, p.eta + (size_t)chain * p.T, p.T, p.status, sm + C::kOffStages, geom,
+                       R.full, R.empty, R.flags, chain, lane, nsteps);
     } else if (warp == C::kWarpP) {
-        role_prep<D, SUBB>(p, sm, R, lane, nsteps);
+        role_prep<D, SUBB>(p, sm, R, bi, hi, lane, nsteps);
     } else if (warp < C::kWarpO) {
         role_weights<D, SUBB>(p, sm, R, warp - C::kWarpW, chain, bi, hi, tok0, lane, nsteps);
     } else {
@@ -695,36 +720,6 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void *ptr = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-// [chains][T][D] bf16 viewed as a 3-D tensor; box {64, rows, 1}, 128B swizzle.
-bool make_map(CUtensorMap *m, const void *base, int D, int T, int chains, int rows)
-{
-    auto enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)chains};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 template <int D, int SUBB>
 cudaError_t launch_dsub(const LinearParams &p, int chains, cudaStream_t s)
 {

@@ -1,0 +1,855 @@
+// ttt_mlp_tc.cu -- TTT-MLP inner loop on tensor cores (sm_103a): d = 64,
+// hidden = 256 (4d), mini-batch b = 16, bf16 Q/K/V.
+//
+// Method: the TTT-MLP of the "TTT layer" section of the "Test-Time
+// Training(TTT)과 LLM 메모리" survey page (f_res(x) = W2 gelu_tanh(W1 x + c1)
+// + c2, f(x) = x + LN(f_res(x)), Eq. 2 update, Eq. 4 loss, Eq. 5 output),
+// trained by the mini-batch rule of Eq. 5 of the "End-to-End Test-Time Training
+// for Long Context" review (section 2.3): every gradient of mini-batch i at the
+// anchor (W1, W2) = (W1_{i-1}, W2_{i-1}), weight 1/b, and z_t read with the
+// in-batch prefix of the updates. Per mini-batch (K, Q, V: 16 x d):
+//   Z1 = K W1^T + c1, X2 = gelu(Z1), Y = X2 W2^T + c2               (anchor)
+//   G = dl/dY through x + LN(y);  G1 = (G W2) * gelu'(Z1)
+//   Z1q = Q W1^T + c1 + A~1^T Mq1,   A~1 = -(eta/b) G1, Mq1 = causal q.k + 1
+//   Yq = gelu(Z1q) W2^T + c2 + A~2^T Mq2, A~2 = -(eta/b) G, Mq2 = causal x2q.x2k + 1
+//   Z = Q + LN(Yq);  W1 += A~1^T K, c1 += A~1^T 1;  W2 += A~2^T X2, c2 += A~2^T 1
+//
+// One CTA per (sequence, head) chain. Warp roles:
+//   L (1)  TMA loader of the Q/K/V tiles and eta (shared with TTT-Linear).
+//   P (1)  fp16 copies of the K/Q tiles; causal Q K^T + 1 fragments.
+//   H (8)  warp w owns hidden units 32w..32w+31: W1 rows and c1 in registers
+//          (fp32 mma accumulators), W2 columns as an fp32 master in tensor
+//          memory (tcgen05.ld / tcgen05.st around each update) plus the fp16
+//          copy of W2 in shared memory that every product reads. Computes Z1,
+//          gelu, G1, Z1q and the W1 / W2 updates.
+//   Y (2)  warp y owns output features 32y..32y+31 and c2: Y, the LayerNorm
+//          forward/backward (both Y warps, through shared memory), G, the
+//          X2q X2k^T Gram, Yq and the output Z = Q + LN(Yq), L_t.
+// H and Y hand activations over through shared memory with named barriers
+// (producer bar.arrive, consumer bar.sync). No warp leaves early: after a
+// failed wait a warp keeps running in step with the others (its results are
+// discarded, the status word says why), so every barrier is always met.
+//
+// Precision: fp16 MMA operands (W1, W2, K, Q, X2, G, A~) with fp32
+// accumulation; W1, W2, c1, c2, LayerNorm statistics and gradients fp32. GELU
+// uses the hardware tanh approximation.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tc_common.cuh"
+
+namespace ttt {
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 64, kHid = 256, kB = 16;
+constexpr int kNH = 8;  // H warps, 32 hidden units each
+constexpr int kNY = 2;  // Y warps, 32 output features each
+constexpr int kWarpL = 0, kWarpP = 1, kWarpH = 2, kWarpY = kWarpH + kNH;
+constexpr int kWarps = kWarpY + kNY;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 4;
+// stage layout (bytes)
+constexpr int kTile = 32 * kD;
+constexpr int kOffK = 0, kOffQ = kTile, kOffV = 2 * kTile;  // bf16, as loaded
+constexpr int kOffKh = 3 * kTile, kOffQh = 4 * kTile;      // fp16 copies (same swizzled layout)
+constexpr int kOffMq = 5 * kTile;                          // causal q.k + 1, fp16 B fragments
+constexpr int kOffEta = kOffMq + 512;
+constexpr int kStageBytes = ((kOffEta + 64 + 1023) / 1024) * 1024;
+// fp16 activation / weight buffers, rows padded by 16 bytes (conflict-free ldmatrix)
+constexpr int kHS = kHid + 8;  // halves per row of a [*][hidden] buffer
+constexpr int kFS = kD + 8;    // halves per row of a [16][d] buffer
+constexpr int kOffStages = 0;
+constexpr int kOffW2h = kStages * kStageBytes;          // 2 x [d][kHS]: W2_{i-1} and W2_i
+constexpr int kOffX2k = kOffW2h + 2 * kD * kHS * 2;     // [16][kHS] gelu(Z1) of the keys
+constexpr int kOffX2q = kOffX2k + kB * kHS * 2;         // [16][kHS] gelu(Z1q)
+constexpr int kOffGh = kOffX2q + kB * kHS * 2;          // [16][kFS] G
+constexpr int kOffGt = kOffGh + kB * kFS * 2;           // [16][kFS] A~2 = -(eta/b) G
+constexpr int kOffRed = kOffGt + kB * kFS * 2;          // 2 bufs x [2 Y warps][16] float4
+constexpr int kOffTmem = kOffRed + 2 * kNY * kB * 16;
+constexpr int kOffBar = kOffTmem + 16;
+constexpr int kNumBars = 3 * kStages;
+constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
+constexpr int kSmemAlloc = kSmem + 1024;
+constexpr uint32_t kTmemCols = 128;  // two H warps per lane quarter x 64 columns
+// named barriers: H <-> Y hand-offs (all 320 H and Y threads), Y-internal rounds
+constexpr int kBarX2k = 1, kBarG = 2, kBarX2q = 3, kBarYdone = 4, kBarW2 = 5, kBarYln = 6;
+constexpr int kHY = (kNH + kNY) * 32;
+constexpr float kGeluA = 0.7978845608028654f;  // sqrt(2/pi)
+constexpr float kGeluC = 0.044715f;
+
+struct Ring {
+    uint64_t *full, *prep, *empty;
+    volatile int *flags;  // [0] abort, [1] fp16 range violation seen
+};
+
+__device__ __forceinline__ uint8_t *stage_ptr(uint8_t *sm, int st) { return sm + kOffStages + st * kStageBytes; }
+
+// gelu_tanh(u) and its derivative.
+__device__ __forceinline__ void gelu2(float u, float &g, float &gp)
+{
+    const float th = tanh_fast(kGeluA * fmaf(kGeluC * u * u, u, u));
+    g = 0.5f * u * (1.f + th);
+    gp = 0.5f * (1.f + th) + 0.5f * u * (1.f - th * th) * kGeluA * fmaf(3.f * kGeluC, u * u, 1.f);
+}
+
+__device__ __forceinline__ float gelu1(float u)
+{
+    const float th = tanh_fast(kGeluA * fmaf(kGeluC * u * u, u, u));
+    return 0.5f * u * (1.f + th);
+}
+
+// ------------------------------------------------------------------ P: prep
+__device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int lane, int nsteps)
+{
+    const int g = lane >> 2, c4 = lane & 3;
+    uint32_t mag = 0;  // per-halfword max of |bf16 bits|: >= 0x4780 means |x| >= 2^16 (or inf/nan)
+    const int ra = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int rb = (lane & 7) + (lane >> 4) * 8;
+    for (int i = 0; i < nsteps; ++i) {
+        const int st = i % kStages;
+        if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
+            abort_chain(R.flags, p.status);
+            break;
+        }
+        uint8_t *stg = stage_ptr(sm, st);
+#pragma unroll
+        for (int tile = 0; tile < 2; ++tile) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(stg + (tile == 0 ? kOffK : kOffQ));
+            uint4 *dst = reinterpret_cast<uint4 *>(stg + (tile == 0 ? kOffKh : kOffQh));
+#pragma unroll
+            for (int ch = lane; ch < 2 * kD; ch += 32) {
+                const uint4 x = src[ch];
+                mag = __vmaxu2(mag, __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
+                                             __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu)));
+                dst[ch] = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
+            }
+        }
+        __syncwarp();
+        // dq[j][r] = q_t . k_s with t = g + 8(r>>1), s = 8j + 2c4 + (r&1)
+        const uint32_t sK = smem_u32(stg + kOffKh), sQ = smem_u32(stg + kOffQh);
+        float dq[2][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            uint32_t aq[4], bk[4];
+            ldsm_x4(aq, sQ + swz(ra, 2 * ks + (lane >> 4)));
+            ldsm_x4(bk, sK + swz(rb, 2 * ks + ((lane >> 3) & 1)));
+            mma16816(dq[0], aq, bk[0], bk[1]);
+            mma16816(dq[1], aq, bk[2], bk[3]);
+        }
+        auto mq = [&](int j, int r) {
+            const int t = g + 8 * (r >> 1), s = 8 * j + 2 * c4 + (r & 1);
+            return s <= t ? dq[j][r] + 1.f : 0.f;
+        };
+        reinterpret_cast<uint4 *>(stg + kOffMq)[lane] =
+            make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)),
+                       pack_h2(mq(0, 2), mq(0, 3)), pack_h2(mq(1, 2), mq(1, 3)));
+        warp_arrive(&R.prep[st], lane);
+        if (lane == 0) mbar_arrive(&R.empty[st]);
+    }
+    const bool range_bad = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
+    if (__any_sync(kFull, range_bad) && lane == 0) {
+        R.flags[1] = 1;
+        record(p.status, TTT_ERR_RANGE);
+    }
+}
+
+// Shared-memory byte address of element (row, col) of a padded fp16 buffer.
+__device__ __forceinline__ uint32_t hb(uint32_t base, int row, int col, int stride)
+{
+    return base + (uint32_t)((row * stride + col) * 2);
+}
+
+// H warps, before the main loop: W2 columns h0 + 8nt + 2c4 (+1) of rows
+// 16mf + g (+8) into this warp's tensor-memory columns (fp32 master) and into
+// fp16 buffer 1 (the copy step 0 reads as W2_{-1+1} = W2_0).
+__device__ void hidden_init_w2(const MlpParams &p, uint8_t *sm, int w, int warp, int bi, int hi, uint32_t tmem,
+                               int lane)
+{
+    const int g = lane >> 2, c4 = lane & 3;
+    const int h0 = 32 * w;
+    const float *W20 = p.W2 + bi * p.w_bstride + (long long)hi * kD * kHid;
+    const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(w >= 4 ? 64 : 0);
+    uint32_t v[2][32];
+#pragma unroll
+    for (int mf = 0; mf < 4; ++mf)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int f0 = 16 * mf + g, hc = h0 + 8 * nt + 2 * c4;
+            const float2 a = *reinterpret_cast<const float2 *>(W20 + f0 * kHid + hc);
+            const float2 b = *reinterpret_cast<const float2 *>(W20 + (f0 + 8) * kHid + hc);
+            const int idx = (mf * 4 + nt) * 4;
+            v[idx >> 5][(idx & 31) + 0] = __float_as_uint(a.x);
+            v[idx >> 5][(idx & 31) + 1] = __float_as_uint(a.y);
+            v[idx >> 5][(idx & 31) + 2] = __float_as_uint(b.x);
+            v[idx >> 5][(idx & 31) + 3] = __float_as_uint(b.y);
+            uint8_t *w2 = sm + kOffW2h + kD * kHS * 2;
+            *reinterpret_cast<uint32_t *>(w2 + (f0 * kHS + hc) * 2) = pack_h2(a.x, a.y);
+            *reinterpret_cast<uint32_t *>(w2 + ((f0 + 8) * kHS + hc) * 2) = pack_h2(b.x, b.y);
+        }
+    tmem_st32(taddr, v[0]);
+    tmem_st32(taddr + 32, v[1]);
+    tmem_wait_st();
+}
+
+// ------------------------------------------------------------------ H: hidden-unit warps
+__device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int w, int warp, int chain, int bi,
+                            int hi, uint32_t tmem, int lane, int nsteps)
+{
+    const int g = lane >> 2, c4 = lane & 3;
+    const int h0 = 32 * w;  // first hidden unit of this warp
+    const float *W10 = p.W1 + bi * p.w_bstride + (long long)hi * kHid * kD;
+    const float *c10 = p.c1 + bi * p.c1_bstride + (long long)hi * kHid;
+    // W1 rows h0 + 16m + g (+8), columns 8nt + 2c4 (+1)
+    float W1a[2][8][4];
+    float c1v[2][2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const int r0 = h0 + 16 * m + g;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const float2 a = *reinterpret_cast<const float2 *>(W10 + r0 * kD + 8 * nt + 2 * c4);
+            const float2 b = *reinterpret_cast<const float2 *>(W10 + (r0 + 8) * kD + 8 * nt + 2 * c4);
+            W1a[m][nt][0] = a.x;
+            W1a[m][nt][1] = a.y;
+            W1a[m][nt][2] = b.x;
+            W1a[m][nt][3] = b.y;
+        }
+        c1v[m][0] = c10[r0];
+        c1v[m][1] = c10[r0 + 8];
+    }
+    // This warp's 64 tensor-memory columns: lanes of its quarter, columns 0 or 64.
+    const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(w >= 4 ? 64 : 0);
+    const uint32_t sW2h = smem_u32(sm + kOffW2h), sX2k = smem_u32(sm + kOffX2k), sX2q = smem_u32(sm + kOffX2q);
+    const uint32_t sGh = smem_u32(sm + kOffGh), sGt = smem_u32(sm + kOffGt);
+    const int rb = (lane & 7) + (lane >> 4) * 8, cb16 = (lane >> 3) & 1;  // non-transposed B fragment rows
+    const int rt = (lane & 7) + ((lane >> 3) & 1) * 8, ct = lane >> 4;   // transposed B fragment rows
+    const int srow = (lane & 7) + 8 * (lane >> 4), scol = 8 * ((lane >> 3) & 1);  // stmatrix / trans-A rows
+    for (int i = 0; i < nsteps; ++i) {
+        const int st = i % kStages;
+        uint8_t *stg = stage_ptr(sm, st);
+        if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
+            !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags))
+            abort_chain(R.flags, p.status);  // keep going in step with the other warps
+        const uint32_t sK = smem_u32(stg + kOffKh), sQ = smem_u32(stg + kOffQh);
+        // Z1^T = W1 K^T + c1 and Rq1^T = W1 Q^T + c1 for this warp's 32 hidden units.
+        float z1[2][2][4], rq[2][2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) z1[m][n][r] = rq[m][n][r] = c1v[m][r >> 1];
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            uint32_t bk[4], bq[4];
+            ldsm_x4(bk, sK + swz(rb, 2 * ks + cb16));
+            ldsm_x4(bq, sQ + swz(rb, 2 * ks + cb16));
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const uint32_t af[4] = {pack_h2(W1a[m][2 * ks][0], W1a[m][2 * ks][1]),
+                                        pack_h2(W1a[m][2 * ks][2], W1a[m][2 * ks][3]),
+                                        pack_h2(W1a[m][2 * ks + 1][0], W1a[m][2 * ks + 1][1]),
+                                        pack_h2(W1a[m][2 * ks + 1][2], W1a[m][2 * ks + 1][3])};
+                mma16816(z1[m][0], af, bk[0], bk[1]);
+                mma16816(z1[m][1], af, bk[2], bk[3]);
+                mma16816(rq[m][0], af, bq[0], bq[1]);
+                mma16816(rq[m][1], af, bq[2], bq[3]);
+            }
+        }
+        // X2 = gelu(Z1) (kept in z1), gelu'(Z1) for the backward.
+        float gp[2][2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) gelu2(z1[m][n][r], z1[m][n][r], gp[m][n][r]);
+        if (i > 0) named_bar_sync(kBarYdone, kHY);  // Y is done with X2k / X2q of step i-1
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+            stsm_x4_t(hb(sX2k, srow, h0 + 16 * m + scol, kHS), pack_h2(z1[m][0][0], z1[m][0][1]),
+                      pack_h2(z1[m][0][2], z1[m][0][3]), pack_h2(z1[m][1][0], z1[m][1][1]),
+                      pack_h2(z1[m][1][2], z1[m][1][3]));
+        named_bar_arrive(kBarX2k, kHY);
+        named_bar_sync(kBarG, kHY);  // G and A~2 of step i are in shared memory
+        // G1pre^T = W2^T G^T (W2_{i-1}, buffer (i+1)&1); A operand = W2 columns, transposed.
+        const uint32_t sW2p = sW2h + (uint32_t)(((i + 1) & 1) * kD * kHS * 2);
+        float gg[2][2][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+            uint32_t bg[4];
+            ldsm_x4(bg, hb(sGh, rb, 16 * ks + 8 * cb16, kFS));
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                uint32_t aw[4];
+                ldsm_x4_t(aw, hb(sW2p, 16 * ks + srow, h0 + 16 * m + scol, kHS));
+                mma16816(gg[m][0], aw, bg[0], bg[1]);
+                mma16816(gg[m][1], aw, bg[2], bg[3]);
+            }
+        }
+        // A~1 = -(eta/b) G1 with G1 = G1pre * gelu'(Z1), fp16 A fragments (rows h, columns t).
+        const float *se = reinterpret_cast<const float *>(stg + kOffEta);
+        float es[2][2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const float2 e2 = *reinterpret_cast<const float2 *>(se + 8 * n + 2 * c4);
+            es[n][0] = -e2.x * (1.f / (float)kB);
+            es[n][1] = -e2.y * (1.f / (float)kB);
+        }
+        float a1[2][2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) a1[m][n][r] = round_h(es[n][r & 1] * gg[m][n][r] * gp[m][n][r]);
+        uint32_t af1[2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            af1[m][0] = pack_h2(a1[m][0][0], a1[m][0][1]);
+            af1[m][1] = pack_h2(a1[m][0][2], a1[m][0][3]);
+            af1[m][2] = pack_h2(a1[m][1][0], a1[m][1][1]);
+            af1[m][3] = pack_h2(a1[m][1][2], a1[m][1][3]);
+        }
+        // Z1q^T = Rq1^T + A~1 Mq1 (in-batch prefix), X2q = gelu(Z1q) -> shared memory.
+        {
+            const uint4 mq = reinterpret_cast<const uint4 *>(stg + kOffMq)[lane];
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                mma16816(rq[m][0], af1[m], mq.x, mq.y);
+                mma16816(rq[m][1], af1[m], mq.z, mq.w);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) rq[m][n][r] = gelu1(rq[m][n][r]);
+            stsm_x4_t(hb(sX2q, srow, h0 + 16 * m + scol, kHS), pack_h2(rq[m][0][0], rq[m][0][1]),
+                      pack_h2(rq[m][0][2], rq[m][0][3]), pack_h2(rq[m][1][0], rq[m][1][1]),
+                      pack_h2(rq[m][1][2], rq[m][1][3]));
+        }
+        named_bar_arrive(kBarX2q, kHY);
+        // W1 += A~1 K, c1 += A~1 1.
+#pragma unroll
+        for (int j = 0; j < kD / 16; ++j) {
+            uint32_t bt[4];
+            ldsm_x4_t(bt, sK + swz(rt, 2 * j + ct));
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                mma16816(W1a[m][2 * j], af1[m], bt[0], bt[1]);
+                mma16816(W1a[m][2 * j + 1], af1[m], bt[2], bt[3]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            float s0 = a1[m][0][0] + a1[m][0][1] + a1[m][1][0] + a1[m][1][1];
+            float s1 = a1[m][0][2] + a1[m][0][3] + a1[m][1][2] + a1[m][1][3];
+            s0 += __shfl_xor_sync(kFull, s0, 1);
+            s0 += __shfl_xor_sync(kFull, s0, 2);
+            s1 += __shfl_xor_sync(kFull, s1, 1);
+            s1 += __shfl_xor_sync(kFull, s1, 2);
+            c1v[m][0] += s0;
+            c1v[m][1] += s1;
+        }
+        // W2 columns += A~2^T X2 (rows f, this warp's hidden columns); the fp32
+        // master goes through tensor memory, the fp16 copy to buffer i&1.
+        {
+            uint32_t v[2][32];
+            tmem_ld32(taddr, v[0]);
+            tmem_ld32(taddr + 32, v[1]);
+            uint32_t bx[2][4];  // B = X2k (k = t, n = h), two pairs of n-tiles
+#pragma unroll
+            for (int q = 0; q < 2; ++q) ldsm_x4_t(bx[q], hb(sX2k, rt, h0 + 16 * q + 8 * ct, kHS));
+            tmem_wait_ld();
+            uint8_t *w2 = sm + kOffW2h + (i & 1) * kD * kHS * 2;
+#pragma unroll
+            for (int mf = 0; mf < 4; ++mf) {
+                uint32_t ag[4];  // A = A~2 (rows f, columns t) from Gt[t][f], transposed
+                ldsm_x4_t(ag, hb(sGt, srow, 16 * mf + scol, kFS));
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int idx = (mf * 4 + nt) * 4;
+                    uint32_t *vv = &v[idx >> 5][idx & 31];
+                    float acc[4] = {__uint_as_float(vv[0]), __uint_as_float(vv[1]), __uint_as_float(vv[2]),
+                                    __uint_as_float(vv[3])};
+                    mma16816(acc, ag, bx[nt >> 1][2 * (nt & 1)], bx[nt >> 1][2 * (nt & 1) + 1]);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) vv[r] = __float_as_uint(acc[r]);
+                    const int f0 = 16 * mf + g, hc = h0 + 8 * nt + 2 * c4;
+                    *reinterpret_cast<uint32_t *>(w2 + (f0 * kHS + hc) * 2) = pack_h2(acc[0], acc[1]);
+                    *reinterpret_cast<uint32_t *>(w2 + ((f0 + 8) * kHS + hc) * 2) = pack_h2(acc[2], acc[3]);
+                }
+            }
+            tmem_st32(taddr, v[0]);
+            tmem_st32(taddr + 32, v[1]);
+            tmem_wait_st();
+        }
+        named_bar_arrive(kBarW2, kHY);
+        warp_arrive(&R.empty[st], lane);
+    }
+    if (nsteps > 0) named_bar_sync(kBarYdone, kHY);  // matches the Y warps' last arrival
+    // Final state.
+    bool bad = false;
+    const size_t ch = (size_t)chain;
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const int r0 = h0 + 16 * m + g;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) bad |= !isfinite(W1a[m][nt][r]);
+        bad |= !isfinite(c1v[m][0]) || !isfinite(c1v[m][1]);
+        if (p.W1_out) {
+            float *Wo = p.W1_out + ch * kHid * kD;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                *reinterpret_cast<float2 *>(Wo + r0 * kD + 8 * nt + 2 * c4) = make_float2(W1a[m][nt][0], W1a[m][nt][1]);
+                *reinterpret_cast<float2 *>(Wo + (r0 + 8) * kD + 8 * nt + 2 * c4) =
+                    make_float2(W1a[m][nt][2], W1a[m][nt][3]);
+            }
+        }
+        if (p.c1_out && c4 == 0) {
+            p.c1_out[ch * kHid + r0] = c1v[m][0];
+            p.c1_out[ch * kHid + r0 + 8] = c1v[m][1];
+        }
+    }
+    {
+        uint32_t v[2][32];
+        tmem_ld32(taddr, v[0]);
+        tmem_ld32(taddr + 32, v[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int mf = 0; mf < 4; ++mf)
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int idx = (mf * 4 + nt) * 4;
+                const float a0 = __uint_as_float(v[idx >> 5][idx & 31]), a1v = __uint_as_float(v[idx >> 5][(idx & 31) + 1]);
+                const float b0 = __uint_as_float(v[idx >> 5][(idx & 31) + 2]), b1 = __uint_as_float(v[idx >> 5][(idx & 31) + 3]);
+                bad |= !isfinite(a0) || !isfinite(a1v) || !isfinite(b0) || !isfinite(b1);
+                if (p.W2_out) {
+                    float *Wo = p.W2_out + ch * kD * kHid;
+                    const int f0 = 16 * mf + g, hc = h0 + 8 * nt + 2 * c4;
+                    *reinterpret_cast<float2 *>(Wo + f0 * kHid + hc) = make_float2(a0, a1v);
+                    *reinterpret_cast<float2 *>(Wo + (f0 + 8) * kHid + hc) = make_float2(b0, b1);
+                }
+            }
+    }
+    if (__any_sync(kFull, bad) && lane == 0) record(p.status, TTT_ERR_NONFINITE);
+}
+
+// ------------------------------------------------------------------ Y: output-feature warps
+// LayerNorm statistics of the 16 token columns over the 64 features held by
+// the two Y warps (32 rows each): local (mean, M2) per column, combined across
+// the two warps by the parallel-variance formula. Returns mean and 1/std of
+// the lane's four columns (8n + 2c4 + e).
+__device__ __forceinline__ void y_ln_stats(const float (&x)[2][2][4], float4 *red, int &rnd, int y, int g, int c4,
+                                           float eps, float (&mu)[2][2], float (&rs)[2][2])
+{
+    float ml[2][2], m2l[2][2];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float s = col_sum(x[0][n][e] + x[0][n][e + 2] + x[1][n][e] + x[1][n][e + 2]) * (1.f / 32.f);
+            float q = 0.f;
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const float d = x[m][n][e + 2 * u] - s;
+                    q = fmaf(d, d, q);
+                }
+            ml[n][e] = s;
+            m2l[n][e] = col_sum(q);
+        }
+    float4 *rb = red + (rnd & 1) * kNY * kB;
+    if (g == 0) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) rb[y * kB + 8 * n + 2 * c4 + e] = make_float4(ml[n][e], m2l[n][e], 0.f, 0.f);
+    }
+    named_bar_sync(kBarYln, kNY * 32);
+    ++rnd;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = 8 * n + 2 * c4 + e;
+            const float4 a = rb[t], b = rb[kB + t];
+            const float mean = 0.5f * (a.x + b.x);
+            const float m2 = a.y + b.y + 32.f * ((a.x - mean) * (a.x - mean) + (b.x - mean) * (b.x - mean));
+            mu[n][e] = mean;
+            rs[n][e] = rsqrtf(m2 * (1.f / (float)kD) + eps);
+        }
+}
+
+// Sums over the 64 features of up to three per-element quantities per column.
+__device__ __forceinline__ void y_sum3(float (&a)[2][2], float (&b)[2][2], float (&c)[2][2], float4 *red, int &rnd,
+                                       int y, int g, int c4)
+{
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            a[n][e] = col_sum(a[n][e]);
+            b[n][e] = col_sum(b[n][e]);
+            c[n][e] = col_sum(c[n][e]);
+        }
+    float4 *rb = red + (rnd & 1) * kNY * kB;
+    if (g == 0) {
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) rb[y * kB + 8 * n + 2 * c4 + e] = make_float4(a[n][e], b[n][e], c[n][e], 0.f);
+    }
+    named_bar_sync(kBarYln, kNY * 32);
+    ++rnd;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = 8 * n + 2 * c4 + e;
+            const float4 u = rb[t], v = rb[kB + t];
+            a[n][e] = u.x + v.x;
+            b[n][e] = u.y + v.y;
+            c[n][e] = u.z + v.z;
+        }
+}
+
+// Y^T (rows f0..f0+31, 16 token columns) += W2 (fp16 buffer) X^T over all hidden units.
+__device__ __forceinline__ void y_gemm(uint32_t sW2, uint32_t sX, int f0, int lane, float (&acc)[2][2][4])
+{
+    const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);   // A rows (non-transposed)
+    const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);   // B rows (non-transposed)
+#pragma unroll 4
+    for (int ks = 0; ks < kHid / 16; ++ks) {
+        uint32_t bx[4];
+        ldsm_x4(bx, hb(sX, rb, 16 * ks + cb, kHS));
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            uint32_t aw[4];
+            ldsm_x4(aw, hb(sW2, f0 + 16 * m + ra, 16 * ks + ca, kHS));
+            mma16816(acc[m][0], aw, bx[0], bx[1]);
+            mma16816(acc[m][1], aw, bx[2], bx[3]);
+        }
+    }
+}
+
+__device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, int chain, int bi, int hi, size_t tok0,
+                       int lane, int nsteps)
+{
+    const int g = lane >> 2, c4 = lane & 3;
+    const int f0 = 32 * y;  // first output feature of this warp
+    const float *c20 = p.c2 + bi * p.c2_bstride + (long long)hi * kD;
+    float c2v[2][2], gam[2][2], bet[2][2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int f = f0 + 16 * m + g + 8 * u;
+            c2v[m][u] = c20[f];
+            gam[m][u] = p.ln_g[hi * kD + f];
+            bet[m][u] = p.ln_b[hi * kD + f];
+        }
+    const uint32_t sW2h = smem_u32(sm + kOffW2h), sX2k = smem_u32(sm + kOffX2k), sX2q = smem_u32(sm + kOffX2q);
+    const uint32_t sGh = smem_u32(sm + kOffGh), sGt = smem_u32(sm + kOffGt);
+    float4 *red = reinterpret_cast<float4 *>(sm + kOffRed);
+    int rnd = 0;
+    const int rbt = (lane & 7) + (lane >> 4) * 8, cbt = (lane >> 3) & 1;        // ldmatrix.trans of a tile
+    const int srow = (lane & 7) + 8 * (lane >> 4), scol = 8 * ((lane >> 3) & 1);  // stmatrix rows
+    const float eps = p.eps, invD = 1.f / (float)kD;
+    const int T = p.T;
+    for (int i = 0; i < nsteps; ++i) {
+        const int st = i % kStages;
+        uint8_t *stg = stage_ptr(sm, st);
+        if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
+            !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags))
+            abort_chain(R.flags, p.status);
+        // k - v + beta, q and v at this lane's (feature, token) positions: ldmatrix.trans of the bf16 tiles.
+        float kv[2][2][4], qv[2][2][4], vv[2][2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int chunk = 2 * (2 * y + m) + cbt;
+            uint32_t kr[4], vr[4], qr[4];
+            ldsm_x4_t(kr, smem_u32(stg + kOffK) + swz(rbt, chunk));
+            ldsm_x4_t(vr, smem_u32(stg + kOffV) + swz(rbt, chunk));
+            ldsm_x4_t(qr, smem_u32(stg + kOffQ) + swz(rbt, chunk));
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t a = kr[2 * n + u], b = vr[2 * n + u], q = qr[2 * n + u];
+                    vv[m][n][2 * u] = bf16_bits_to_f32(b & 0xffffu);
+                    vv[m][n][2 * u + 1] = bf16_bits_to_f32(b >> 16);
+                    kv[m][n][2 * u] = bf16_bits_to_f32(a & 0xffffu) - vv[m][n][2 * u] + bet[m][u];
+                    kv[m][n][2 * u + 1] = bf16_bits_to_f32(a >> 16) - vv[m][n][2 * u + 1] + bet[m][u];
+                    qv[m][n][2 * u] = bf16_bits_to_f32(q & 0xffffu);
+                    qv[m][n][2 * u + 1] = bf16_bits_to_f32(q >> 16);
+                }
+        }
+        float es[2][2];
+        {
+            const float *se = reinterpret_cast<const float *>(stg + kOffEta);
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const float2 e2 = *reinterpret_cast<const float2 *>(se + 8 * n + 2 * c4);
+                es[n][0] = -e2.x * (1.f / (float)kB);
+                es[n][1] = -e2.y * (1.f / (float)kB);
+            }
+        }
+        if (i > 0) named_bar_sync(kBarW2, kHY);  // W2_{i-1} copy complete
+        const uint32_t sW2p = sW2h + (uint32_t)(((i + 1) & 1) * kD * kHS * 2);
+        named_bar_sync(kBarX2k, kHY);
+        // Y^T = W2_{i-1} X2k^T + c2
+        float yk[2][2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) yk[m][n][r] = c2v[m][r >> 1];
+        y_gemm(sW2p, sX2k, f0, lane, yk);
+        // LayerNorm forward + backward: G = dl/dY, inner loss.
+        float mu[2][2], rs[2][2];
+        y_ln_stats(yk, red, rnd, y, g, c4, eps, mu, rs);
+        float s1[2][2] = {}, s2[2][2] = {}, sl[2][2] = {};
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int e = r & 1, u = r >> 1;
+                    const float yh = (yk[m][n][r] - mu[n][e]) * rs[n][e];
+                    const float E = fmaf(gam[m][u], yh, kv[m][n][r]);
+                    const float dh = 2.f * gam[m][u] * E;
+                    s1[n][e] += dh;
+                    s2[n][e] = fmaf(dh, yh, s2[n][e]);
+                    sl[n][e] = fmaf(E, E, sl[n][e]);
+                }
+        y_sum3(s1, s2, sl, red, rnd, y, g, c4);
+        float gh[2][2][4], a2[2][2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int e = r & 1, u = r >> 1;
+                    const float yh = (yk[m][n][r] - mu[n][e]) * rs[n][e];
+                    const float E = fmaf(gam[m][u], yh, kv[m][n][r]);
+                    const float G = rs[n][e] * (2.f * gam[m][u] * E - s1[n][e] * invD - yh * s2[n][e] * invD);
+                    gh[m][n][r] = G;
+                    a2[m][n][r] = round_h(es[n][e] * G);
+                }
+        if (p.inner_loss && y == 0 && g == 0) {
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = i * kB + 8 * n + 2 * c4 + e;
+                    if (t < T) p.inner_loss[tok0 + t] = sl[n][e];
+                }
+        }
+        // G and A~2 to shared memory as [t][f] (the H warps' operands).
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            stsm_x4_t(hb(sGh, srow, f0 + 16 * m + scol, kFS), pack_h2(gh[m][0][0], gh[m][0][1]),
+                      pack_h2(gh[m][0][2], gh[m][0][3]), pack_h2(gh[m][1][0], gh[m][1][1]),
+                      pack_h2(gh[m][1][2], gh[m][1][3]));
+            stsm_x4_t(hb(sGt, srow, f0 + 16 * m + scol, kFS), pack_h2(a2[m][0][0], a2[m][0][1]),
+                      pack_h2(a2[m][0][2], a2[m][0][3]), pack_h2(a2[m][1][0], a2[m][1][1]),
+                      pack_h2(a2[m][1][2], a2[m][1][3]));
+        }
+        named_bar_arrive(kBarG, kHY);
+        float c2o[2][2];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            float s0 = a2[m][0][0] + a2[m][0][1] + a2[m][1][0] + a2[m][1][1];
+            float s1r = a2[m][0][2] + a2[m][0][3] + a2[m][1][2] + a2[m][1][3];
+            s0 += __shfl_xor_sync(kFull, s0, 1);
+            s0 += __shfl_xor_sync(kFull, s0, 2);
+            s1r += __shfl_xor_sync(kFull, s1r, 1);
+            s1r += __shfl_xor_sync(kFull, s1r, 2);
+            c2o[m][0] = c2v[m][0];
+            c2o[m][1] = c2v[m][1];
+            c2v[m][0] += s0;
+            c2v[m][1] += s1r;
+        }
+        named_bar_sync(kBarX2q, kHY);
+        // Mq2 = causal gelu(Z1q_t) . gelu(Z1k_s) + 1 as B fragments; Yq^T = W2_{i-1} X2q^T + c2 + A~2 Mq2.
+        uint4 mq2;
+        {
+            const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);
+            const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);
+            float dq[2][4] = {};
+#pragma unroll 4
+            for (int ks = 0; ks < kHid / 16; ++ks) {
+                uint32_t aq[4], bk[4];
+                ldsm_x4(aq, hb(sX2q, ra, 16 * ks + ca, kHS));
+                ldsm_x4(bk, hb(sX2k, rb, 16 * ks + cb, kHS));
+                mma16816(dq[0], aq, bk[0], bk[1]);
+                mma16816(dq[1], aq, bk[2], bk[3]);
+            }
+            auto mq = [&](int j, int r) {
+                const int t = g + 8 * (r >> 1), s = 8 * j + 2 * c4 + (r & 1);
+                return s <= t ? dq[j][r] + 1.f : 0.f;
+            };
+            mq2 = make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)), pack_h2(mq(0, 2), mq(0, 3)),
+                             pack_h2(mq(1, 2), mq(1, 3)));
+        }
+        float yq[2][2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) yq[m][n][r] = c2o[m][r >> 1];
+        y_gemm(sW2p, sX2q, f0, lane, yq);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const uint32_t af[4] = {pack_h2(a2[m][0][0], a2[m][0][1]), pack_h2(a2[m][0][2], a2[m][0][3]),
+                                    pack_h2(a2[m][1][0], a2[m][1][1]), pack_h2(a2[m][1][2], a2[m][1][3])};
+            mma16816(yq[m][0], af, mq2.x, mq2.y);
+            mma16816(yq[m][1], af, mq2.z, mq2.w);
+        }
+        named_bar_arrive(kBarYdone, kHY);
+        // z = q + LN(yq); L_t = ||z_t - v_t||^2
+        y_ln_stats(yq, red, rnd, y, g, c4, eps, mu, rs);
+        float sz[2][2] = {}, d0[2][2] = {}, d1[2][2] = {};
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int e = r & 1, u = r >> 1;
+                    const float z = qv[m][n][r] + fmaf(gam[m][u], (yq[m][n][r] - mu[n][e]) * rs[n][e], bet[m][u]);
+                    yq[m][n][r] = z;
+                    const float dz = z - vv[m][n][r];
+                    sz[n][e] = fmaf(dz, dz, sz[n][e]);
+                }
+        y_sum3(sz, d0, d1, red, rnd, y, g, c4);
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = i * kB + 8 * n + 2 * c4 + e;
+                if (t >= T) continue;
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int f = f0 + 16 * m + g + 8 * u;
+                        const float z = yq[m][n][e + 2 * u];
+                        if (p.z_f32)
+                            static_cast<float *>(p.Z)[(tok0 + t) * kD + f] = z;
+                        else
+                            static_cast<__nv_bfloat16 *>(p.Z)[(tok0 + t) * kD + f] = __float2bfloat16_rn(z);
+                    }
+                if (p.loss && y == 0 && g == 0) p.loss[tok0 + t] = sz[n][e];
+            }
+        warp_arrive(&R.empty[st], lane);
+    }
+    if (nsteps > 0) named_bar_sync(kBarW2, kHY);  // matches the H warps' last arrival
+    bool bad = false;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            bad |= !isfinite(c2v[m][u]);
+            if (p.c2_out && c4 == 0) p.c2_out[(size_t)chain * kD + f0 + 16 * m + g + 8 * u] = c2v[m][u];
+        }
+    if (__any_sync(kFull, bad) && lane == 0) record(p.status, TTT_ERR_NONFINITE);
+}
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1)
+mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const MlpParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int chain = blockIdx.x;
+    const int bi = chain / p.H, hi = chain % p.H;
+    const int nsteps = p.T / kB;
+    const size_t tok0 = (size_t)chain * p.T;
+
+    Ring R;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kOffBar);
+    R.full = bar;
+    R.prep = bar + kStages;
+    R.empty = bar + 2 * kStages;
+    R.flags = reinterpret_cast<volatile int *>(bar + kNumBars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffTmem);
+
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&R.full[s], 33);               // expect_tx arrive + 32 cp.async arrivals
+            mbar_init(&R.prep[s], 1);
+            mbar_init(&R.empty[s], kNH + kNY + 1);  // H warps, Y warps, P
+        }
+        R.flags[0] = 0;
+        R.flags[1] = 0;
+        fence_mbar_init();
+    }
+    tmem_fence_before_sync();
+    __syncthreads();  // (0) barriers and the tensor-memory address
+    tmem_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= kWarpH && warp < kWarpY) hidden_init_w2(p, sm, warp - kWarpH, warp, bi, hi, tmem, lane);
+    tmem_fence_before_sync();
+    __syncthreads();  // (1) initial W2 copies visible; tensor-memory stores complete
+    tmem_fence_after_sync();
+
+    if (warp == kWarpL) {
+        const StageGeom geom{kStages, kStageBytes, kOffK, kOffQ, kOffV, kOffEta};
+        role_loader<kD>(&tmQ, &tmK, &tmV, p.eta + tok0, p.T, p.status, sm + kOffStages, geom, R.full, R.empty,
+                        R.flags, chain, lane, nsteps);
+    } else if (warp == kWarpP) {
+        role_prep(p, sm, R, lane, nsteps);
+    } else if (warp < kWarpY) {
+        role_hidden(p, sm, R, warp - kWarpH, warp, chain, bi, hi, tmem, lane, nsteps);
+    } else {
+        role_y(p, sm, R, warp - kWarpY, chain, bi, hi, tok0, lane, nsteps);
+    }
+    tmem_fence_before_sync();
+    __syncthreads();  // (2) every tensor-memory access is complete
+    if (warp == 0) {
+        tmem_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+bool mlp_tc_supported(int io, int d, int hidden, int mb)
+{
+    return io == TTT_BF16 && d == kD && hidden == kHid && mb == kB;
+}
+
+cudaError_t launch_mlp_tc(const MlpParams &p, int chains, cudaStream_t s)
+{
+    CUtensorMap mQ, mK, mV;
+    if (!make_map(&mQ, p.Q, kD, p.T, chains, 16) || !make_map(&mK, p.K, kD, p.T, chains, 16) ||
+        !make_map(&mV, p.V, kD, p.T, chains, 16))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(mlp_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    mlp_tc_kernel<<<chains, kThreads, kSmemAlloc, s>>>(mQ, mK, mV, p);
+    return cudaGetLastError();
+}
+
+}  // namespace ttt
