@@ -40,6 +40,35 @@ from test_weight_sequence_ttt_b300.inputs import WORKLOADS, make_inputs  # noqa:
 
 DEFAULT_WORKLOAD = "linear_b8h12_d64_t2k"
 L2_FLUSH_BYTES = 256 << 20
+CSRC = os.path.join(ROOT, "test_weight_sequence_ttt_b300", "csrc")
+TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def sources_sha1() -> str:
+    """sha1 over the CUDA sources of the library (kernels + headers)."""
+    import glob
+    import hashlib
+    h = hashlib.sha1()
+    for f in sorted(glob.glob(os.path.join(CSRC, "*"))):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(f, "rb") as fh:
+                h.update(os.path.basename(f).encode())
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, z_dtype: str):
+    """DRAM bytes per launch of the workload's kernel from the last ncu capture
+    (profiles/traffic.json), or None when the sources changed since."""
+    try:
+        with open(TRAFFIC) as f:
+            j = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = j.get("%s/z_%s" % (workload, z_dtype))
+    if not e or e.get("sources_sha1") != sources_sha1():
+        return None
+    return e.get("dram_bytes_per_launch")
 
 
 def _peaks():
@@ -118,7 +147,7 @@ class ClockSampler:
             try:
                 self._proc = subprocess.Popen(
                     ["nvidia-smi", "--id=" + self.bus_id, "--query-gpu=" + ",".join(self.SMI_FIELDS),
-                     "--format=csv,noheader,nounits", "-lms", "100"],
+                     "--format=csv,noheader,nounits", "-lms", "50"],
                     stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
             except Exception as e:  # noqa: BLE001
                 self.error = (self.error or "") + "; smi: %s" % e
@@ -319,16 +348,16 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.io,
-        "precision": "bf16 I/O; fp16 tensor-core operands; fp32 accumulation, LayerNorm and weight state"
-        if kind == 2 else "fp32 FFMA",
+        "dtype": "f16-mma/f32" if kind == 2 else "f32",
+        "precision": "bf16 Q/K/V; fp16 tensor-core operands with fp32 accumulation; fp32 LayerNorm, "
+                     "gradients and weight state" if kind == 2 else "fp32 FFMA",
         "data": "synthetic (seeded Gaussian Q/K/V, sigmoid-gated eta, N(0,0.02^2) W0)",
         "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
                    "mb": w.b, "hidden": w.hidden or None, "io": w.io, "z_dtype": args.z_dtype,
                    "kernel_kind": kind,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": measured_traffic(w.name, args.z_dtype),
                      "roofline_frac": t_roof / (ms / 1e3),
                      "peak_source": peaks["source"] + " (burst)",
                      "algorithmic_bytes_per_launch": bytes_launch, "algorithmic_flops_per_launch": flops_launch},
@@ -390,8 +419,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--z-dtype", default="f32", choices=["f32", "bf16"],
-                    help="element type of Z (fp32 keeps the tolerance gate on the arithmetic)")
+    ap.add_argument("--z-dtype", default="bf16", choices=["f32", "bf16"],
+                    help="element type of Z (bf16 = the I/O type of the workloads)")
     ap.add_argument("--cpu-budget-s", type=float, default=20.0, help="core-seconds of the oracle sample")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -253,6 +253,11 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     p.loss = a->loss;
     p.inner_loss = a->inner_loss;
     p.status = a->status_dev;
+#ifdef TTT_TRACE
+    p.trace = g_trace;
+#else
+    p.trace = nullptr;
+#endif
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e =
         kind == 2 ? ttt::launch_mlp_tc(p, a->B * a->H, s) : ttt::launch_mlp_f32(p, a->io, a->B * a->H, s);

@@ -36,6 +36,7 @@ struct MlpParams {
     void *Z;
     float *W1_out, *c1_out, *W2_out, *c2_out, *loss, *inner_loss;
     int *status;
+    unsigned long long *trace;  // phase timestamps (TTT_TRACE builds only), else NULL
 };
 
 // Phase-timestamp hook for performance diagnosis. Compiled in only with

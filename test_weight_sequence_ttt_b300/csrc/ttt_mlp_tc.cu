@@ -230,6 +230,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
     for (int i = 0; i < nsteps; ++i) {
         const int st = i % kStages;
         uint8_t *stg = stage_ptr(sm, st);
+        if (w == 0) TTT_TRACE_AT(p, i, 0);
         if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
             !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags))
             abort_chain(R.flags, p.status);  // keep going in step with the other warps
@@ -267,6 +268,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             for (int n = 0; n < 2; ++n)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) gelu2(z1[m][n][r], z1[m][n][r], gp[m][n][r]);
+        if (w == 0) TTT_TRACE_AT(p, i, 1);
         if (i > 0) named_bar_sync(kBarYdone, kHY);  // Y is done with X2k / X2q of step i-1
 #pragma unroll
         for (int m = 0; m < 2; ++m)
@@ -274,7 +276,9 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
                       pack_h2(z1[m][0][2], z1[m][0][3]), pack_h2(z1[m][1][0], z1[m][1][1]),
                       pack_h2(z1[m][1][2], z1[m][1][3]));
         named_bar_arrive(kBarX2k, kHY);
+        if (w == 0) TTT_TRACE_AT(p, i, 2);
         named_bar_sync(kBarG, kHY);  // G and A~2 of step i are in shared memory
+        if (w == 0) TTT_TRACE_AT(p, i, 3);
         // G1pre^T = W2^T G^T (W2_{i-1}, buffer (i+1)&1); A operand = W2 columns, transposed.
         const uint32_t sW2p = sW2h + (uint32_t)(((i + 1) & 1) * kD * kHS * 2);
         float gg[2][2][4] = {};
@@ -334,6 +338,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
                       pack_h2(rq[m][1][2], rq[m][1][3]));
         }
         named_bar_arrive(kBarX2q, kHY);
+        if (w == 0) TTT_TRACE_AT(p, i, 4);
         // W1 += A~1 K, c1 += A~1 1.
 #pragma unroll
         for (int j = 0; j < kD / 16; ++j) {
@@ -356,6 +361,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             c1v[m][0] += s0;
             c1v[m][1] += s1;
         }
+        if (w == 0) TTT_TRACE_AT(p, i, 5);
         // W2 columns += A~2^T X2 (rows f, this warp's hidden columns); the fp32
         // master goes through tensor memory, the fp16 copy to buffer i&1.
         {
@@ -390,6 +396,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             tmem_wait_st();
         }
         named_bar_arrive(kBarW2, kHY);
+        if (w == 0) TTT_TRACE_AT(p, i, 6);
         warp_arrive(&R.empty[st], lane);
     }
     if (nsteps > 0) named_bar_sync(kBarYdone, kHY);  // matches the Y warps' last arrival
@@ -603,9 +610,11 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
                 es[n][1] = -e2.y * (1.f / (float)kB);
             }
         }
+        if (y == 0) TTT_TRACE_AT(p, i, 8);
         if (i > 0) named_bar_sync(kBarW2, kHY);  // W2_{i-1} copy complete
         const uint32_t sW2p = sW2h + (uint32_t)(((i + 1) & 1) * kD * kHS * 2);
         named_bar_sync(kBarX2k, kHY);
+        if (y == 0) TTT_TRACE_AT(p, i, 9);
         // Y^T = W2_{i-1} X2k^T + c2
         float yk[2][2][4];
 #pragma unroll
@@ -615,6 +624,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
 #pragma unroll
                 for (int r = 0; r < 4; ++r) yk[m][n][r] = c2v[m][r >> 1];
         y_gemm(sW2p, sX2k, f0, lane, yk);
+        if (y == 0) TTT_TRACE_AT(p, i, 10);
         // LayerNorm forward + backward: G = dl/dY, inner loss.
         float mu[2][2], rs[2][2];
         y_ln_stats(yk, red, rnd, y, g, c4, eps, mu, rs);
@@ -668,6 +678,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
                       pack_h2(a2[m][1][2], a2[m][1][3]));
         }
         named_bar_arrive(kBarG, kHY);
+        if (y == 0) TTT_TRACE_AT(p, i, 11);
         float c2o[2][2];
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
@@ -683,6 +694,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
             c2v[m][1] += s1r;
         }
         named_bar_sync(kBarX2q, kHY);
+        if (y == 0) TTT_TRACE_AT(p, i, 12);
         // Mq2 = causal gelu(Z1q_t) . gelu(Z1k_s) + 1 as B fragments; Yq^T = W2_{i-1} X2q^T + c2 + A~2 Mq2.
         uint4 mq2;
         {
@@ -720,6 +732,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
             mma16816(yq[m][1], af, mq2.z, mq2.w);
         }
         named_bar_arrive(kBarYdone, kHY);
+        if (y == 0) TTT_TRACE_AT(p, i, 13);
         // z = q + LN(yq); L_t = ||z_t - v_t||^2
         y_ln_stats(yq, red, rnd, y, g, c4, eps, mu, rs);
         float sz[2][2] = {}, d0[2][2] = {}, d1[2][2] = {};
@@ -755,6 +768,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
                     }
                 if (p.loss && y == 0 && g == 0) p.loss[tok0 + t] = sz[n][e];
             }
+        if (y == 0) TTT_TRACE_AT(p, i, 14);
         warp_arrive(&R.empty[st], lane);
     }
     if (nsteps > 0) named_bar_sync(kBarW2, kHY);  // matches the H warps' last arrival
