@@ -13,10 +13,11 @@
 // consecutive mini-batches when b < 16). Warp roles:
 //   L (1 warp)  TMA loader: Q/K/V tiles [16 tok x d] bf16 (128B-swizzled) and
 //               eta into a ring of kStages stages.
-//   P (1 warp)  prep: fp16 copies of the K/Q tiles; Gram fragments (causal
-//               Q_i K_i^T + 1, K_{i-1} K_i^T + 1 and, for b < 16, K_i K_i^T + 1);
-//               per token: the LayerNorm shift u0.k + mean(c0) and the sums
+//               Two stages behind its loads it also writes the per-token
+//               scalars: the LayerNorm shift u0.k + mean(c0) and the sums
 //               sum_f gamma_f kv_f, sum_f kv_f^2 with kv = k - v + beta.
+//   P (1 warp)  prep: fp16 copies of the K/Q tiles; Gram fragments (causal
+//               Q_i K_i^T + 1, K_{i-1} K_i^T + 1 and, for b < 16, K_i K_i^T + 1).
 //   W (d/16)    warp w owns rows 16w..16w+15 of W and c as fp32 mma
 //               accumulators in registers for the whole sequence, and runs the
 //               serial chain for those rows.
@@ -37,6 +38,16 @@
 // W warp sums, over its rows, d = y - sh: d, d^2, gamma^2 d, gamma^2 d^2 and
 // gamma kv d; the five sums of the W warps add up (split-phase mbarrier) and give
 // the mean, variance and the two LayerNorm-backward means in closed form.
+//
+// Chain/weight split (d = 64). The chain above runs on its own warps (C, d/16
+// of them, rows 16w..16w+15 of Y^T) that do nothing else: partial sums, one
+// named-barrier reduction round, G and A~, the 16-wide correction. Separate
+// weight warps (T) hold W and c, apply W += A~ K, and compute S_{i+2},
+// Rq_{i+1} and Yq_i. A~ and S cross between the two groups through shared
+// memory and alternating producer/consumer named barriers, so the chain warps
+// never wait on an mbarrier. No warp of either group leaves early: after a
+// failed wait a T warp keeps running in step (results discarded, status set).
+// For d = 128 the W warps do both jobs (register budget of 20 warps).
 //
 // Precision. MMA operands are fp16 (10-bit mantissa) with fp32 accumulation;
 // W, c, LayerNorm statistics and gradients stay fp32. Inputs and W must stay
@@ -83,7 +94,13 @@ struct Cfg {
     static constexpr int kOffRedX = kOffY + 2 * kSS * YS * 4;     // 2 bufs x [MT][16] float4
     static constexpr int kOffRedY = kOffRedX + 2 * MT * kSS * 16; // 2 bufs x [MT][16] float
     static constexpr int kOffCst = kOffRedY + 2 * MT * kSS * 4;   // u0, gamma, beta: 3 x D floats
-    static constexpr int kOffBar = kOffCst + 3 * D * 4;
+    // chain/weight split (D = 64): hand-off rings between the chain (C) and weight (T) warps
+    static constexpr int kOffAR = kOffCst + 3 * D * 4;            // 2 slots x [MT][32 lanes] A~ fragments
+    static constexpr int kOffSR = kOffAR + 2 * MT * 512;          // 2 slots x [MT][2][32 lanes] S fragments
+    static constexpr int kOffBar = kOffSR + 2 * MT * 1024;
+    static constexpr int kSplitWarpC = 2, kSplitWarpT = 2 + MT, kSplitWarpO = 2 + 2 * MT;
+    static constexpr int kSplitWarps = kSplitWarpO + NO;
+    static constexpr int kSplitThreads = kSplitWarps * 32;
     static constexpr int kNumBars = 3 * kStages + 6;
     static constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
     static constexpr int kSmemAlloc = kSmem + 1024;                // slack for alignment
@@ -107,37 +124,161 @@ __device__ __forceinline__ uint8_t *stage_ptr(uint8_t *sm, int st)
     return sm + Cfg<D>::kOffStages + st * Cfg<D>::kStageBytes;
 }
 
+// ------------------------------------------------------------------ per-token LayerNorm scalars
+// For d = 64 the loader warp computes them (two stages behind its loads);
+// for d = 128 the prep warp does, because a loader with 64 features per lane
+// to sum would fall behind on the loads.
+template <int D>
+constexpr bool kSumsInLoader = D == 64;
+
+// Chain constants into shared memory: u0 = feature mean of W_0's rows, gamma,
+// beta; returns mean(c0) (all lanes).
+template <int D>
+__device__ float chain_consts(const LinearParams &p, uint8_t *sm, int bi, int hi, int lane)
+{
+    using C = Cfg<D>;
+    float *cu = reinterpret_cast<float *>(sm + C::kOffCst), *cg = cu + D, *cbt = cg + D;
+    const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
+    const float *c0 = p.c0 + bi * p.c0_bstride + (long long)hi * D;
+    float cmean = 0.f;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+        const int j = lane + 32 * q;
+        float s[8] = {};
+#pragma unroll 8
+        for (int f = 0; f < D; ++f) s[f & 7] += W0[f * D + j];
+        cu[j] = ((s[0] + s[1]) + (s[2] + s[3]) + ((s[4] + s[5]) + (s[6] + s[7]))) * (1.f / (float)D);
+        cg[j] = p.ln_g[hi * D + j];
+        cbt[j] = p.ln_b[hi * D + j];
+        cmean += c0[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cmean += __shfl_xor_sync(kFull, cmean, o);
+    __syncwarp();
+    return cmean * (1.f / (float)D);
+}
+
+// Per-token scalars of one stage (16 tokens; lane pair per token, half the
+// features each): the LayerNorm shift sh_t = u0 . k_t + mean(c0),
+// sum_f gamma_f kv_f and sum_f kv_f^2 with kv = k - v + beta.
+template <int D>
+__device__ void token_sums(uint8_t *stg, const uint8_t *sm, float cmean, int lane)
+{
+    using C = Cfg<D>;
+    const float *cu = reinterpret_cast<const float *>(sm + C::kOffCst), *cg = cu + D, *cbt = cg + D;
+    const int tt = lane & 15, half = lane >> 4;
+    float shs = 0.f, ps = 0.f, qs = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < D / 16; ++ch) {
+        const int jj = half * (D / 16) + ch;  // 16-byte chunk (8 features)
+        const uint4 kb = *reinterpret_cast<const uint4 *>(stg + C::kOffK + swz(tt, jj));
+        const uint4 vb = *reinterpret_cast<const uint4 *>(stg + C::kOffV + swz(tt, jj));
+        const uint32_t kw[4] = {kb.x, kb.y, kb.z, kb.w}, vw[4] = {vb.x, vb.y, vb.z, vb.w};
+        const float4 *u4 = reinterpret_cast<const float4 *>(cu + 8 * jj);
+        const float4 *g4 = reinterpret_cast<const float4 *>(cg + 8 * jj);
+        const float4 *b4 = reinterpret_cast<const float4 *>(cbt + 8 * jj);
+        const float4 uu[2] = {u4[0], u4[1]}, gg[2] = {g4[0], g4[1]}, bb[2] = {b4[0], b4[1]};
+        const float uf[8] = {uu[0].x, uu[0].y, uu[0].z, uu[0].w, uu[1].x, uu[1].y, uu[1].z, uu[1].w};
+        const float gf[8] = {gg[0].x, gg[0].y, gg[0].z, gg[0].w, gg[1].x, gg[1].y, gg[1].z, gg[1].w};
+        const float bf[8] = {bb[0].x, bb[0].y, bb[0].z, bb[0].w, bb[1].x, bb[1].y, bb[1].z, bb[1].w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t kbits = q & 1 ? kw[q >> 1] >> 16 : kw[q >> 1] & 0xffffu;
+            const uint32_t vbits = q & 1 ? vw[q >> 1] >> 16 : vw[q >> 1] & 0xffffu;
+            const float kf = bf16_bits_to_f32(kbits), vf = bf16_bits_to_f32(vbits);
+            const float kv = kf - vf + bf[q];
+            shs = fmaf(uf[q], kf, shs);
+            ps = fmaf(gf[q], kv, ps);
+            qs = fmaf(kv, kv, qs);
+        }
+    }
+    shs += __shfl_xor_sync(kFull, shs, 16);
+    ps += __shfl_xor_sync(kFull, ps, 16);
+    qs += __shfl_xor_sync(kFull, qs, 16);
+    if (half == 0) {
+        reinterpret_cast<float *>(stg + C::kOffSh)[tt] = shs + cmean;
+        reinterpret_cast<float *>(stg + C::kOffPk)[tt] = ps;
+        reinterpret_cast<float *>(stg + C::kOffQk)[tt] = qs;
+    }
+}
+
+// ------------------------------------------------------------------ L: loader + per-token sums
+// The loader warp issues the TMA loads of stage i, and kLag stages behind,
+// once stage j has landed, writes the per-token scalars of the LayerNorm
+// reduction into it: the shift sh_t = u0 . k_t + mean(c0) (u0 = feature mean
+// of W_0's rows), sum_f gamma_f kv_f and sum_f kv_f^2 (kv = k - v + beta). Its
+// arrival on prep[j] joins the prep warp's.
+constexpr int kLag = 2;
+
+template <int D>
+__device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                 const LinearParams &p, uint8_t *sm, const Ring &R, int chain, int bi, int hi, int lane,
+                                 int nsteps)
+{
+    using C = Cfg<D>;
+    const int T = p.T;
+    const float *eta = p.eta + (size_t)chain * T;
+    const float cmean = kSumsInLoader<D> ? chain_consts<D>(p, sm, bi, hi, lane) : 0.f;
+    if (lane == 0) {
+        prefetch_tmap(tmQ);
+        prefetch_tmap(tmK);
+        prefetch_tmap(tmV);
+    }
+    int issued = 0;
+    const int lag = kSumsInLoader<D> ? kLag : 0;
+    for (int i = 0; i < nsteps + lag; ++i) {
+        if (i < nsteps) {
+            const int st = i % kStages;
+            if (!wait_bar(&R.empty[st], parity_of(i / kStages) ^ 1u, R.flags)) {
+                abort_chain(R.flags, p.status);
+                break;
+            }
+            TTT_TRACE_AT(p, i, 14);
+            uint8_t *stg = stage_ptr<D>(sm, st);
+            const int t0 = i * kSS;
+            float *se = reinterpret_cast<float *>(stg + C::kOffEta);
+            if (lane < kSS) {
+                const int t = t0 + lane;
+                cp_async_4(se + lane, eta + (t < T ? t : 0), t < T ? 4u : 0u);  // zero-fill past T
+            }
+            cp_async_mbar_arrive_noinc(&R.full[st]);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&R.full[st], 3 * C::kTile);
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {
+                    tma_load_3d(stg + C::kOffK + h * 2048, tmK, &R.full[st], h * 64, t0, chain);
+                    tma_load_3d(stg + C::kOffQ + h * 2048, tmQ, &R.full[st], h * 64, t0, chain);
+                    tma_load_3d(stg + C::kOffV + h * 2048, tmV, &R.full[st], h * 64, t0, chain);
+                }
+            }
+            issued = i + 1;
+        }
+        if (!kSumsInLoader<D>) continue;
+        const int j = i - kLag;
+        if (j < 0) continue;
+        const int sj = j % kStages;
+        if (!wait_bar(&R.full[sj], parity_of(j / kStages), R.flags)) {
+            abort_chain(R.flags, p.status);
+            break;
+        }
+        token_sums<D>(stage_ptr<D>(sm, sj), sm, cmean, lane);
+        warp_arrive(&R.prep[sj], lane);
+    }
+    // Never leave while a copy issued here may still be landing in shared memory.
+    for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+        (void)mbar_wait(&R.full[i % kStages], parity_of(i / kStages));
+}
+
 // ------------------------------------------------------------------ P: prep
 template <int D, int SUBB>
 __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int bi, int hi, int lane, int nsteps)
 {
     using C = Cfg<D>;
     const int g = lane >> 2, c4 = lane & 3;
-    // Constants of the chain: u0 = feature mean of W_0's rows, mean(c0), gamma, beta.
-    float *cu = reinterpret_cast<float *>(sm + C::kOffCst), *cg = cu + D, *cbt = cg + D;
-    {
-        const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
-        for (int j = lane; j < D; j += 32) {
-            float s = 0.f;
-            for (int f = 0; f < D; ++f) s += W0[f * D + j];
-            cu[j] = s * (1.f / (float)D);
-            cg[j] = p.ln_g[hi * D + j];
-            cbt[j] = p.ln_b[hi * D + j];
-        }
-    }
-    float cmean = 0.f;
-    {
-        const float *c0 = p.c0 + bi * p.c0_bstride + (long long)hi * D;
-        for (int j = lane; j < D; j += 32) cmean += c0[j];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cmean += __shfl_xor_sync(kFull, cmean, o);
-        cmean *= 1.f / (float)D;
-    }
-    __syncwarp();
     uint32_t mag = 0;  // per-halfword max of |bf16 bits|: >= 0x4780 means |x| >= 2^16 (or inf/nan)
     const int ra = (lane & 7) + ((lane >> 3) & 1) * 8;  // A-fragment row (ldmatrix x4)
     const int rb = (lane & 7) + (lane >> 4) * 8;        // B-fragment row
-    const int tt = lane & 15, half = lane >> 4;         // per-token sums: token, half of the features
+    const float cmean = kSumsInLoader<D> ? 0.f : chain_consts<D>(p, sm, bi, hi, lane);
     for (int i = 0; i < nsteps; ++i) {
         const int st = i % kStages;
         if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
@@ -159,42 +300,7 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
                 dst[ch] = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
             }
         }
-        // (2) per-token LayerNorm shift and kv sums (bf16 inputs, fp32 sums).
-        {
-            float shs = 0.f, ps = 0.f, qs = 0.f;
-#pragma unroll
-            for (int ch = 0; ch < D / 16; ++ch) {
-                const int j = half * (D / 16) + ch;  // 16-byte chunk (8 features)
-                const uint4 kb = *reinterpret_cast<const uint4 *>(stg + C::kOffK + swz(tt, j));
-                const uint4 vb = *reinterpret_cast<const uint4 *>(stg + C::kOffV + swz(tt, j));
-                const uint32_t kw[4] = {kb.x, kb.y, kb.z, kb.w}, vw[4] = {vb.x, vb.y, vb.z, vb.w};
-                const float4 *u4 = reinterpret_cast<const float4 *>(cu + 8 * j);
-                const float4 *g4 = reinterpret_cast<const float4 *>(cg + 8 * j);
-                const float4 *b4 = reinterpret_cast<const float4 *>(cbt + 8 * j);
-                const float4 uu[2] = {u4[0], u4[1]}, gg[2] = {g4[0], g4[1]}, bb[2] = {b4[0], b4[1]};
-                const float uf[8] = {uu[0].x, uu[0].y, uu[0].z, uu[0].w, uu[1].x, uu[1].y, uu[1].z, uu[1].w};
-                const float gf[8] = {gg[0].x, gg[0].y, gg[0].z, gg[0].w, gg[1].x, gg[1].y, gg[1].z, gg[1].w};
-                const float bf[8] = {bb[0].x, bb[0].y, bb[0].z, bb[0].w, bb[1].x, bb[1].y, bb[1].z, bb[1].w};
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t kbits = q & 1 ? kw[q >> 1] >> 16 : kw[q >> 1] & 0xffffu;
-                    const uint32_t vbits = q & 1 ? vw[q >> 1] >> 16 : vw[q >> 1] & 0xffffu;
-                    const float kf = bf16_bits_to_f32(kbits), vf = bf16_bits_to_f32(vbits);
-                    const float kv = kf - vf + bf[q];
-                    shs = fmaf(uf[q], kf, shs);
-                    ps = fmaf(gf[q], kv, ps);
-                    qs = fmaf(kv, kv, qs);
-                }
-            }
-            shs += __shfl_xor_sync(kFull, shs, 16);
-            ps += __shfl_xor_sync(kFull, ps, 16);
-            qs += __shfl_xor_sync(kFull, qs, 16);
-            if (half == 0) {
-                reinterpret_cast<float *>(stg + C::kOffSh)[tt] = shs + cmean;
-                reinterpret_cast<float *>(stg + C::kOffPk)[tt] = ps;
-                reinterpret_cast<float *>(stg + C::kOffQk)[tt] = qs;
-            }
-        }
+        if (!kSumsInLoader<D>) token_sums<D>(stg, sm, cmean, lane);
         __syncwarp();
         // (3) Gram fragments. d*[j][r] holds (t = g + 8(r>>1), s = 8j + 2c4 + (r&1)):
         //     dq = Q_i K_i^T, dk = K_i K_i^T, dx = K_i K_{i-1}^T (t in step i, s in step i-1).
@@ -298,7 +404,10 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
     const float gam[2] = {p.ln_g[hi * D + r0], p.ln_g[hi * D + r1]};
     const float bet[2] = {p.ln_b[hi * D + r0], p.ln_b[hi * D + r1]};
     float gam2all = 0.f;  // sum of gamma^2 over all features
-    for (int f = 0; f < D; ++f) gam2all = fmaf(p.ln_g[hi * D + f], p.ln_g[hi * D + f], gam2all);
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) gam2all = fmaf(p.ln_g[hi * D + lane + 32 * q], p.ln_g[hi * D + lane + 32 * q], gam2all);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gam2all += __shfl_xor_sync(kFull, gam2all, o);
     const int rb = (lane & 7) + (lane >> 4) * 8;        // ldmatrix row, non-transposed B
     const int cb16 = (lane >> 3) & 1;
     const int rt = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row, transposed B
@@ -663,6 +772,388 @@ __device__ void role_output(const LinearParams &p, uint8_t *sm, const Ring &R, i
     }
 }
 
+// ------------------------------------------------------------------ chain/weight split (D = 64)
+constexpr int kBarRed = 1;  // C warps: one reduction round
+constexpr int kBarA0 = 2;   // A~_i ready (C -> T), ids 2 and 3 by i & 1
+constexpr int kBarS0 = 4;   // S_k ready (T -> C), ids 4 and 5 by k & 1
+
+template <int D, int SUBB>
+__device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int hi, size_t tok0,
+                                 int lane, int nsteps)
+{
+    using C = Cfg<D>;
+    constexpr int MT = C::MT, NSUB = kSS / SUBB;
+    constexpr int kNAS = 2 * MT * 32;
+    const int g = lane >> 2, c4 = lane & 3;
+    const int r0 = 16 * w + g, r1 = r0 + 8;
+    const float gam[2] = {p.ln_g[hi * D + r0], p.ln_g[hi * D + r1]};
+    const float bet[2] = {p.ln_b[hi * D + r0], p.ln_b[hi * D + r1]};
+    float gam2all = 0.f;  // sum of gamma^2 over all features
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) gam2all = fmaf(p.ln_g[hi * D + lane + 32 * q], p.ln_g[hi * D + lane + 32 * q], gam2all);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gam2all += __shfl_xor_sync(kFull, gam2all, o);
+    const int rb = (lane & 7) + (lane >> 4) * 8, cb16 = (lane >> 3) & 1;
+    const float invD = 1.f / (float)D, eps = p.eps;
+    const int T = p.T;
+    const float4 *SR = reinterpret_cast<const float4 *>(sm + C::kOffSR);
+    uint4 *AR = reinterpret_cast<uint4 *>(sm + C::kOffAR);
+    int rnd = 0;
+    float yk[2][4];
+    named_bar_sync(kBarS0, kNAS);  // Y_0 = W_0 K_0^T + c_0 from the T warps
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const float4 v = SR[w * 64 + nt * 32 + lane];
+        yk[nt][0] = v.x;
+        yk[nt][1] = v.y;
+        yk[nt][2] = v.z;
+        yk[nt][3] = v.w;
+    }
+    for (int i = 0; i < nsteps; ++i) {
+        const int st = i % kStages, stn = (i + 1) % kStages;
+        const bool has_next = i + 1 < nsteps;
+        uint8_t *stg = stage_ptr<D>(sm, st);
+        uint8_t *stgn = stage_ptr<D>(sm, stn);
+        if (w == 0) TTT_TRACE_AT(p, i, 0);
+        // Stage i was waited for by the T warps before they published S_i; the
+        // named barrier that handed S_i over orders those reads after the loads.
+        float kv[2][4];
+        {
+            uint32_t kr[4], vr[4];
+            ldsm_x4_t(kr, smem_u32(stg + C::kOffK) + swz(rb, 2 * w + cb16));
+            ldsm_x4_t(vr, smem_u32(stg + C::kOffV) + swz(rb, 2 * w + cb16));
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t a = kr[2 * nt + u], b = vr[2 * nt + u];
+                    kv[nt][2 * u] = bf16_bits_to_f32(a & 0xffffu) - bf16_bits_to_f32(b & 0xffffu) + bet[u];
+                    kv[nt][2 * u + 1] = bf16_bits_to_f32(a >> 16) - bf16_bits_to_f32(b >> 16) + bet[u];
+                }
+        }
+        const float *ssh = reinterpret_cast<const float *>(stg + C::kOffSh);
+        float escale[2][2], shv[2][2];
+        {
+            const float *se = reinterpret_cast<const float *>(stg + C::kOffEta);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float2 e2 = *reinterpret_cast<const float2 *>(se + 8 * nt + 2 * c4);
+                const float2 s2 = *reinterpret_cast<const float2 *>(ssh + 8 * nt + 2 * c4);
+                escale[nt][0] = -e2.x * (1.f / (float)SUBB);
+                escale[nt][1] = -e2.y * (1.f / (float)SUBB);
+                shv[nt][0] = s2.x;
+                shv[nt][1] = s2.y;
+            }
+        }
+        const int tc = 8 * (g & 1) + 2 * c4 + ((g >> 1) & 1);
+        const float sh_c = ssh[tc];
+        const float pk_c = reinterpret_cast<const float *>(stg + C::kOffPk)[tc];
+        const float qk_c = reinterpret_cast<const float *>(stg + C::kOffQk)[tc];
+        float at[2][4] = {}, lin[2][2] = {};
+#pragma unroll
+        for (int m = 0; m < NSUB; ++m) {
+            float s1[2][2], s2[2][2], sb[2][2], sc[2][2], sd[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float a1 = 0.f, a2 = 0.f, ab = 0.f, ac = 0.f, ad = 0.f;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float dv = yk[nt][e + 2 * u] - shv[nt][e];
+                        const float g2d = gam[u] * gam[u] * dv;
+                        a1 += dv;
+                        a2 = fmaf(dv, dv, a2);
+                        ab += g2d;
+                        ac = fmaf(g2d, dv, ac);
+                        ad = fmaf(gam[u] * kv[nt][e + 2 * u], dv, ad);
+                    }
+                    s1[nt][e] = col_sum(a1);
+                    s2[nt][e] = col_sum(a2);
+                    sb[nt][e] = col_sum(ab);
+                    sc[nt][e] = col_sum(ac);
+                    sd[nt][e] = col_sum(ad);
+                }
+            const int buf = rnd & 1;
+            float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
+            float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
+            if (g == 0) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = 8 * nt + 2 * c4 + e;
+                        redX[w * kSS + t] = make_float4(s1[nt][e], s2[nt][e], sb[nt][e], sc[nt][e]);
+                        redY[w * kSS + t] = sd[nt][e];
+                    }
+            }
+            if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 1);
+            named_bar_sync(kBarRed, MT * 32);
+            ++rnd;
+            if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 2);
+            float mu_c, rs_c, M1_c, M2_c, LE_c;
+            {
+                float S1 = 0.f, S2 = 0.f, SB = 0.f, SC = 0.f, SD = 0.f;
+#pragma unroll
+                for (int u = 0; u < MT; ++u) {
+                    const float4 x = redX[u * kSS + tc];
+                    S1 += x.x;
+                    S2 += x.y;
+                    SB += x.z;
+                    SC += x.w;
+                    SD += redY[u * kSS + tc];
+                }
+                const float ee = S1 * invD;
+                const float syy = fmaxf(fmaf(-ee, S1, S2), 0.f);
+                rs_c = rsqrtf(syy * invD + eps);
+                const float sg1 = fmaf(-ee, gam2all, SB);
+                const float sg2 = fmaf(ee * ee, gam2all, fmaf(-2.f * ee, SB, SC));
+                const float sgk = fmaf(-ee, pk_c, SD);
+                M1_c = 2.f * invD * fmaf(rs_c, sg1, pk_c);
+                M2_c = 2.f * invD * rs_c * fmaf(rs_c, sg2, sgk);
+                LE_c = fmaf(rs_c, fmaf(rs_c, sg2, 2.f * sgk), qk_c);
+                mu_c = sh_c + ee;
+            }
+            float ad[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = 8 * nt + 2 * c4 + e;
+                    const int src = (nt + 2 * e) * 4 + c4;
+                    const float mu = __shfl_sync(kFull, mu_c, src);
+                    const float rs = __shfl_sync(kFull, rs_c, src);
+                    const float M1 = __shfl_sync(kFull, M1_c, src);
+                    const float M2 = __shfl_sync(kFull, M2_c, src);
+                    const float LE = __shfl_sync(kFull, LE_c, src);
+                    const bool in_m = NSUB == 1 || t / SUBB == m;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float yh = (yk[nt][e + 2 * u] - mu) * rs;
+                        const float E = fmaf(gam[u], yh, kv[nt][e + 2 * u]);
+                        const float G = rs * (2.f * gam[u] * E - M1 - yh * M2);
+                        const float a = round_h(escale[nt][e] * G);
+                        ad[nt][e + 2 * u] = in_m ? a : 0.f;
+                        if (in_m) at[nt][e + 2 * u] = a;
+                    }
+                    if (in_m) lin[nt][e] = LE;
+                }
+            if (NSUB > 1 && m + 1 < NSUB) {
+                const uint4 gk = reinterpret_cast<const uint4 *>(stg + C::kOffGk)[lane];
+                const uint32_t adf[4] = {pack_h2(ad[0][0], ad[0][1]), pack_h2(ad[0][2], ad[0][3]),
+                                         pack_h2(ad[1][0], ad[1][1]), pack_h2(ad[1][2], ad[1][3])};
+                mma16816(yk[0], adf, gk.x, gk.y);
+                mma16816(yk[1], adf, gk.z, gk.w);
+            }
+        }
+        const uint32_t af[4] = {pack_h2(at[0][0], at[0][1]), pack_h2(at[0][2], at[0][3]),
+                                pack_h2(at[1][0], at[1][1]), pack_h2(at[1][2], at[1][3])};
+        AR[((i & 1) * MT + w) * 32 + lane] = make_uint4(af[0], af[1], af[2], af[3]);
+        named_bar_arrive(kBarA0 + (i & 1), kNAS);
+        if (w == 0) TTT_TRACE_AT(p, i, 3);
+        if (p.inner_loss && w == 0 && g == 0) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = i * kSS + 8 * nt + 2 * c4 + e;
+                    if (t < T) p.inner_loss[tok0 + t] = lin[nt][e];
+                }
+        }
+        warp_arrive(&R.empty[st], lane);
+        if (has_next) {
+            // Y_{i+1}^T = S_{i+1} + A~_i (K_i K_{i+1}^T + 1)
+            named_bar_sync(kBarS0 + ((i + 1) & 1), kNAS);
+            const uint4 kx = reinterpret_cast<const uint4 *>(stgn + C::kOffKx)[lane];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float4 v = SR[(((i + 1) & 1) * MT + w) * 64 + nt * 32 + lane];
+                yk[nt][0] = v.x;
+                yk[nt][1] = v.y;
+                yk[nt][2] = v.z;
+                yk[nt][3] = v.w;
+            }
+            mma16816(yk[0], af, kx.x, kx.y);
+            mma16816(yk[1], af, kx.z, kx.w);
+            if (w == 0) TTT_TRACE_AT(p, i, 4);
+        }
+    }
+}
+
+template <int D>
+__device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int chain, int bi, int hi,
+                                   int lane, int nsteps)
+{
+    using C = Cfg<D>;
+    constexpr int MT = C::MT, NTW = D / 8;
+    constexpr int kNAS = 2 * MT * 32;
+    const int g = lane >> 2, c4 = lane & 3;
+    const int r0 = 16 * w + g, r1 = r0 + 8;
+    const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
+    const float *c0 = p.c0 + bi * p.c0_bstride + (long long)hi * D;
+    float Wa[NTW][4];
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) {
+        const float2 a = *reinterpret_cast<const float2 *>(W0 + r0 * D + 8 * nt + 2 * c4);
+        const float2 b = *reinterpret_cast<const float2 *>(W0 + r1 * D + 8 * nt + 2 * c4);
+        Wa[nt][0] = a.x;
+        Wa[nt][1] = a.y;
+        Wa[nt][2] = b.x;
+        Wa[nt][3] = b.y;
+    }
+    float cb[2] = {c0[r0], c0[r1]};
+    const int rt = (lane & 7) + ((lane >> 3) & 1) * 8, ct = lane >> 4;
+    float4 *SR = reinterpret_cast<float4 *>(sm + C::kOffSR);
+    const uint4 *AR = reinterpret_cast<const uint4 *>(sm + C::kOffAR);
+    auto wait_stage = [&](int k) {
+        if (!wait_bar(&R.full[k % kStages], parity_of(k / kStages), R.flags) ||
+            !wait_bar(&R.prep[k % kStages], parity_of(k / kStages), R.flags))
+            abort_chain(R.flags, p.status);  // keep going in step with the chain warps
+    };
+    auto publish_s = [&](int k) {  // S_k = W K_k^T + c (this warp's rows) -> the chain warps
+        float acc[2][4];
+        rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, k % kStages) + C::kOffKh), lane, acc);
+        float4 *dst = SR + ((k & 1) * MT + w) * 64;
+        dst[lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+        dst[32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+        named_bar_arrive(kBarS0 + (k & 1), kNAS);
+    };
+    wait_stage(0);
+    publish_s(0);
+    if (nsteps > 1) {
+        wait_stage(1);
+        publish_s(1);
+    }
+    float Rq[2][4];
+    rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, 0) + C::kOffQh), lane, Rq);
+    for (int j = 0; j < nsteps; ++j) {
+        const int st = j % kStages, slot = j & 1;
+        uint8_t *stg = stage_ptr<D>(sm, st);
+        named_bar_sync(kBarA0 + slot, kNAS);
+        if (w == 0) TTT_TRACE_AT(p, j, 5);
+        const uint4 a = AR[(slot * MT + w) * 32 + lane];
+        const uint32_t af[4] = {a.x, a.y, a.z, a.w};
+        // W_{j-1} -> W_j, c_{j-1} -> c_j
+        {
+            const uint32_t sK = smem_u32(stg + C::kOffKh);
+#pragma unroll
+            for (int jj = 0; jj < MT; ++jj) {
+                uint32_t bt[4];
+                ldsm_x4_t(bt, sK + swz(rt, 2 * jj + ct));
+                mma16816(Wa[2 * jj], af, bt[0], bt[1]);
+                mma16816(Wa[2 * jj + 1], af, bt[2], bt[3]);
+            }
+        }
+        auto hsum = [](uint32_t v) {
+            return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu))) +
+                   __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+        };
+        float s0 = hsum(a.x) + hsum(a.z), s1 = hsum(a.y) + hsum(a.w);
+        s0 += __shfl_xor_sync(kFull, s0, 1);
+        s0 += __shfl_xor_sync(kFull, s0, 2);
+        s1 += __shfl_xor_sync(kFull, s1, 1);
+        s1 += __shfl_xor_sync(kFull, s1, 2);
+        cb[0] += s0;
+        cb[1] += s1;
+        // Yq_j^T = Rq_j^T + A~_j Mq_j -> output warps
+        {
+            const uint4 mq = reinterpret_cast<const uint4 *>(stg + C::kOffMq)[lane];
+            mma16816(Rq[0], af, mq.x, mq.y);
+            mma16816(Rq[1], af, mq.z, mq.w);
+        }
+        if (!wait_bar(&R.yempty[slot], parity_of(j >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
+        float *ys = reinterpret_cast<float *>(sm + C::kOffY + slot * kSS * C::YS * 4);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                ys[(8 * nt + 2 * c4 + (r & 1)) * C::YS + 16 * w + g + 8 * (r >> 1)] = Rq[nt][r];
+        warp_arrive(&R.yfull[slot], lane);
+        if (w == 0) TTT_TRACE_AT(p, j, 6);
+        if (j + 2 < nsteps) {
+            wait_stage(j + 2);
+            publish_s(j + 2);  // S_{j+2} = W_j K_{j+2}^T + c_j
+        }
+        if (w == 0) TTT_TRACE_AT(p, j, 7);
+        if (j + 1 < nsteps)  // Rq_{j+1} = W_j Q_{j+1}^T + c_j (stage j+1 waited for above, one step earlier)
+            rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % kStages) + C::kOffQh), lane, Rq);
+        warp_arrive(&R.empty[st], lane);
+    }
+    bool badv = !isfinite(cb[0]) || !isfinite(cb[1]);
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) badv |= !isfinite(Wa[nt][r]);
+    if (p.W_out) {
+        float *Wo = p.W_out + (size_t)chain * D * D;
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt) {
+            *reinterpret_cast<float2 *>(Wo + r0 * D + 8 * nt + 2 * c4) = make_float2(Wa[nt][0], Wa[nt][1]);
+            *reinterpret_cast<float2 *>(Wo + r1 * D + 8 * nt + 2 * c4) = make_float2(Wa[nt][2], Wa[nt][3]);
+        }
+    }
+    if (p.c_out && c4 == 0) {
+        p.c_out[(size_t)chain * D + r0] = cb[0];
+        p.c_out[(size_t)chain * D + r1] = cb[1];
+    }
+    if (__any_sync(kFull, badv) && lane == 0) record(p.status, TTT_ERR_NONFINITE);
+}
+
+template <int D, int SUBB>
+__global__ void __launch_bounds__(Cfg<D>::kSplitThreads, 1)
+linear_tc_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const LinearParams p)
+{
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int chain = blockIdx.x;
+    const int bi = chain / p.H, hi = chain % p.H;
+    const int nsteps = (p.T + kSS - 1) / kSS;
+    const size_t tok0 = (size_t)chain * p.T;
+
+    Ring R;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::kOffBar);
+    R.full = bar;
+    R.prep = bar + kStages;
+    R.empty = bar + 2 * kStages;
+    R.yfull = bar + 3 * kStages;
+    R.yempty = R.yfull + 2;
+    R.red = R.yfull + 4;
+    R.flags = reinterpret_cast<volatile int *>(bar + C::kNumBars);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&R.full[s], 33);                      // expect_tx arrive + 32 cp.async arrivals
+            mbar_init(&R.prep[s], kSumsInLoader<D> ? 2 : 1);  // P (and L)
+            mbar_init(&R.empty[s], 2 * C::MT + C::NO + 1);  // C warps, T warps, O warps, P
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&R.yfull[j], C::MT);
+            mbar_init(&R.yempty[j], C::NO);
+            mbar_init(&R.red[j], C::MT);
+        }
+        R.flags[0] = 0;
+        R.flags[1] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (nsteps == 0) return;
+
+    if (warp == C::kWarpL) {
+        role_loader_sums<D>(&tmQ, &tmK, &tmV, p, sm, R, chain, bi, hi, lane, nsteps);
+    } else if (warp == C::kWarpP) {
+        role_prep<D, SUBB>(p, sm, R, bi, hi, lane, nsteps);
+    } else if (warp < C::kSplitWarpT) {
+        role_chain_split<D, SUBB>(p, sm, R, warp - C::kSplitWarpC, hi, tok0, lane, nsteps);
+    } else if (warp < C::kSplitWarpO) {
+        role_weights_split<D>(p, sm, R, warp - C::kSplitWarpT, chain, bi, hi, lane, nsteps);
+    } else {
+        role_output<D>(p, sm, R, warp - C::kSplitWarpO, chain, hi, tok0, lane, nsteps);
+    }
+}
+
 // ------------------------------------------------------------------ kernel
 template <int D, int SUBB>
 __global__ void __launch_bounds__(Cfg<D>::kThreads, 1)
@@ -691,7 +1182,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&R.full[s], 33);                  // expect_tx arrive + 32 cp.async arrivals
-            mbar_init(&R.prep[s], 1);
+            mbar_init(&R.prep[s], kSumsInLoader<D> ? 2 : 1);  // P (and L)
             mbar_init(&R.empty[s], C::MT + C::NO + 1);  // W warps, O warps, P
         }
         for (int j = 0; j < 2; ++j) {
@@ -707,9 +1198,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (nsteps == 0) return;
 
     if (warp == C::kWarpL) {
-        const StageGeom geom{kStages, C::kStageBytes, C::kOffK, C::kOffQ, C::kOffV, C::kOffEta};
-        role_loader<D>(&tmQ, &tmK, &tmV, p.eta + (size_t)chain * p.T, p.T, p.status, sm + C::kOffStages, geom,
-                       R.full, R.empty, R.flags, chain, lane, nsteps);
+        role_loader_sums<D>(&tmQ, &tmK, &tmV, p, sm, R, chain, bi, hi, lane, nsteps);
     } else if (warp == C::kWarpP) {
         role_prep<D, SUBB>(p, sm, R, bi, hi, lane, nsteps);
     } else if (warp < C::kWarpO) {
@@ -728,9 +1217,17 @@ cudaError_t launch_dsub(const LinearParams &p, int chains, cudaStream_t s)
         !make_map(&mV, p.V, D, p.T, chains, 16))
         return cudaErrorInvalidValue;
     constexpr int smem = Cfg<D>::kSmemAlloc;
-    cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel<D, SUBB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    linear_tc_kernel<D, SUBB><<<chains, Cfg<D>::kThreads, smem, s>>>(mQ, mK, mV, p);
+    if constexpr (D == 64) {
+        cudaError_t e =
+            cudaFuncSetAttribute(linear_tc_split_kernel<D, SUBB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        linear_tc_split_kernel<D, SUBB><<<chains, Cfg<D>::kSplitThreads, smem, s>>>(mQ, mK, mV, p);
+    } else {
+        cudaError_t e =
+            cudaFuncSetAttribute(linear_tc_kernel<D, SUBB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        linear_tc_kernel<D, SUBB><<<chains, Cfg<D>::kThreads, smem, s>>>(mQ, mK, mV, p);
+    }
     return cudaGetLastError();
 }
 

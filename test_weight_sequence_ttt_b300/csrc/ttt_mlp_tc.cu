@@ -16,15 +16,17 @@
 //
 // One CTA per (sequence, head) chain. Warp roles:
 //   L (1)  TMA loader of the Q/K/V tiles and eta (shared with TTT-Linear).
-//   P (1)  fp16 copies of the K/Q tiles; causal Q K^T + 1 fragments.
+//   P (1)  fp16 copies of the K/Q tiles; causal Q K^T + 1 fragments; one step
+//          behind, the output side: the X2q X2k^T Gram (causal + 1 fragments
+//          for the Y warps) and Z = Q + LN(Yq), L_t with the Z stores.
 //   H (8)  warp w owns hidden units 32w..32w+31: W1 rows and c1 in registers
 //          (fp32 mma accumulators), W2 columns as an fp32 master in tensor
 //          memory (tcgen05.ld / tcgen05.st around each update) plus the fp16
 //          copy of W2 in shared memory that every product reads. Computes Z1,
 //          gelu, G1, Z1q and the W1 / W2 updates.
 //   Y (2)  warp y owns output features 32y..32y+31 and c2: Y, the LayerNorm
-//          forward/backward (both Y warps, through shared memory), G, the
-//          X2q X2k^T Gram, Yq and the output Z = Q + LN(Yq), L_t.
+//          forward/backward (both Y warps, through shared memory), G and
+//          Yq = X2q W2^T + c2 + A~2^T Mq2, handed to P.
 // H and Y hand activations over through shared memory with named barriers
 // (producer bar.arrive, consumer bar.sync). No warp leaves early: after a
 // failed wait a warp keeps running in step with the others (its results are
@@ -68,9 +70,12 @@ constexpr int kOffX2q = kOffX2k + kB * kHS * 2;         // [16][kHS] gelu(Z1q)
 constexpr int kOffGh = kOffX2q + kB * kHS * 2;          // [16][kFS] G
 constexpr int kOffGt = kOffGh + kB * kFS * 2;           // [16][kFS] A~2 = -(eta/b) G
 constexpr int kOffRed = kOffGt + kB * kFS * 2;          // 2 bufs x [2 Y warps][16] float4
-constexpr int kOffTmem = kOffRed + 2 * kNY * kB * 16;
+constexpr int kYS = kD + 4;                              // floats per row of the Yq hand-off
+constexpr int kOffYq = kOffRed + 2 * kNY * kB * 16;      // 2 slots x [16][kYS] fp32 Yq (Y -> P)
+constexpr int kOffMq2 = kOffYq + 2 * kB * kYS * 4;       // causal x2q.x2k + 1 fragments (P -> Y)
+constexpr int kOffTmem = kOffMq2 + 512;
 constexpr int kOffBar = kOffTmem + 16;
-constexpr int kNumBars = 3 * kStages;
+constexpr int kNumBars = 3 * kStages + 6;
 constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
 constexpr int kSmemAlloc = kSmem + 1024;
 constexpr uint32_t kTmemCols = 128;  // two H warps per lane quarter x 64 columns
@@ -80,8 +85,10 @@ constexpr int kHY = (kNH + kNY) * 32;
 constexpr float kGeluA = 0.7978845608028654f;  // sqrt(2/pi)
 constexpr float kGeluC = 0.044715f;
 
+// mbarriers: full/prep/empty (stage ring), hq (H -> P: X2q of the step is
+// written), mq2 (P -> Y: Gram fragments), yqfull/yqempty[2] (Yq hand-off Y <-> P).
 struct Ring {
-    uint64_t *full, *prep, *empty;
+    uint64_t *full, *prep, *empty, *hq, *mq2, *yqfull, *yqempty;
     volatile int *flags;  // [0] abort, [1] fp16 range violation seen
 };
 
@@ -101,53 +108,162 @@ __device__ __forceinline__ float gelu1(float u)
     return 0.5f * u * (1.f + th);
 }
 
-// ------------------------------------------------------------------ P: prep
-__device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int lane, int nsteps)
+// ------------------------------------------------------------------ P: prep and output
+__device__ __forceinline__ uint32_t hb(uint32_t base, int row, int col, int stride);
+
+// Step i's input side: fp16 copies of the K/Q tiles and causal Q K^T + 1 fragments.
+__device__ __forceinline__ void prep_stage(uint8_t *stg, int lane, uint32_t &mag)
+{
+    const int g = lane >> 2, c4 = lane & 3;
+    const int ra = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int rb = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+    for (int tile = 0; tile < 2; ++tile) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(stg + (tile == 0 ? kOffK : kOffQ));
+        uint4 *dst = reinterpret_cast<uint4 *>(stg + (tile == 0 ? kOffKh : kOffQh));
+#pragma unroll
+        for (int ch = lane; ch < 2 * kD; ch += 32) {
+            const uint4 x = src[ch];
+            mag = __vmaxu2(mag, __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
+                                         __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu)));
+            dst[ch] = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
+        }
+    }
+    __syncwarp();
+    // dq[j][r] = q_t . k_s with t = g + 8(r>>1), s = 8j + 2c4 + (r&1)
+    const uint32_t sK = smem_u32(stg + kOffKh), sQ = smem_u32(stg + kOffQh);
+    float dq[2][4] = {};
+#pragma unroll
+    for (int ks = 0; ks < kD / 16; ++ks) {
+        uint32_t aq[4], bk[4];
+        ldsm_x4(aq, sQ + swz(ra, 2 * ks + (lane >> 4)));
+        ldsm_x4(bk, sK + swz(rb, 2 * ks + ((lane >> 3) & 1)));
+        mma16816(dq[0], aq, bk[0], bk[1]);
+        mma16816(dq[1], aq, bk[2], bk[3]);
+    }
+    auto mq = [&](int j, int r) {
+        const int t = g + 8 * (r >> 1), s = 8 * j + 2 * c4 + (r & 1);
+        return s <= t ? dq[j][r] + 1.f : 0.f;
+    };
+    reinterpret_cast<uint4 *>(stg + kOffMq)[lane] =
+        make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)), pack_h2(mq(0, 2), mq(0, 3)),
+                   pack_h2(mq(1, 2), mq(1, 3)));
+}
+
+// P runs the input side one step ahead of the output side: iteration i preps
+// stage i, then finishes step i - 1 (the X2q X2k^T Gram for the Y warps, and
+// Z = Q + LN(Yq), L_t once the Y warps hand Yq over).
+__device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi, size_t tok0, int lane, int nsteps)
 {
     const int g = lane >> 2, c4 = lane & 3;
     uint32_t mag = 0;  // per-halfword max of |bf16 bits|: >= 0x4780 means |x| >= 2^16 (or inf/nan)
-    const int ra = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int rb = (lane & 7) + (lane >> 4) * 8;
-    for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kStages;
-        if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
+    const int tl = lane >> 1, half = lane & 1;  // output side: token and half of the features
+    float gam[32], bet[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        gam[k] = p.ln_g[hi * kD + 32 * half + k];
+        bet[k] = p.ln_b[hi * kD + 32 * half + k];
+    }
+    const uint32_t sX2k = smem_u32(sm + kOffX2k), sX2q = smem_u32(sm + kOffX2q);
+    const float invD = 1.f / (float)kD, eps = p.eps;
+    bool ok = true;
+    for (int i = 0; i <= nsteps && ok; ++i) {
+        if (i < nsteps) {
+            const int st = i % kStages;
+            if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
+                abort_chain(R.flags, p.status);
+                break;
+            }
+            prep_stage(stage_ptr(sm, st), lane, mag);
+            warp_arrive(&R.prep[st], lane);
+        }
+        if (i == 0) continue;
+        const int j = i - 1, stj = j % kStages, slot = j & 1;
+        uint8_t *stg = stage_ptr(sm, stj);
+        // Gram of step j: Mq2[s][t] = (s <= t)(x2q_t . x2k_s + 1) as B fragments (k = s, n = t).
+        if (!wait_bar(R.hq, parity_of(j), R.flags)) {
             abort_chain(R.flags, p.status);
             break;
         }
-        uint8_t *stg = stage_ptr(sm, st);
+        {
+            const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);
+            const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);
+            float dq[2][4] = {};
+#pragma unroll 4
+            for (int ks = 0; ks < kHid / 16; ++ks) {
+                uint32_t aq[4], bk[4];
+                ldsm_x4(aq, hb(sX2q, ra, 16 * ks + ca, kHS));
+                ldsm_x4(bk, hb(sX2k, rb, 16 * ks + cb, kHS));
+                mma16816(dq[0], aq, bk[0], bk[1]);
+                mma16816(dq[1], aq, bk[2], bk[3]);
+            }
+            auto mq = [&](int jj, int r) {
+                const int t = g + 8 * (r >> 1), s = 8 * jj + 2 * c4 + (r & 1);
+                return s <= t ? dq[jj][r] + 1.f : 0.f;
+            };
+            reinterpret_cast<uint4 *>(sm + kOffMq2)[lane] =
+                make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)), pack_h2(mq(0, 2), mq(0, 3)),
+                           pack_h2(mq(1, 2), mq(1, 3)));
+        }
+        warp_arrive(R.mq2, lane);
+        // Output of step j: z = q + LN(yq), L_t = ||z_t - v_t||^2; lane pair per token.
+        if (!wait_bar(&R.yqfull[slot], parity_of(j >> 1), R.flags)) {
+            abort_chain(R.flags, p.status);
+            break;
+        }
+        const float *ys = reinterpret_cast<const float *>(sm + kOffYq) + slot * kB * kYS + tl * kYS + 32 * half;
+        float yv[32];
 #pragma unroll
-        for (int tile = 0; tile < 2; ++tile) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(stg + (tile == 0 ? kOffK : kOffQ));
-            uint4 *dst = reinterpret_cast<uint4 *>(stg + (tile == 0 ? kOffKh : kOffQh));
+        for (int k = 0; k < 8; ++k) {
+            const float4 v = *reinterpret_cast<const float4 *>(ys + 4 * k);
+            yv[4 * k] = v.x;
+            yv[4 * k + 1] = v.y;
+            yv[4 * k + 2] = v.z;
+            yv[4 * k + 3] = v.w;
+        }
+        warp_arrive(&R.yqempty[slot], lane);
+        float s = 0.f;
 #pragma unroll
-            for (int ch = lane; ch < 2 * kD; ch += 32) {
-                const uint4 x = src[ch];
-                mag = __vmaxu2(mag, __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
-                                             __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu)));
-                dst[ch] = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
+        for (int k = 0; k < 32; ++k) s += yv[k];
+        s += __shfl_xor_sync(kFull, s, 1);
+        const float mu = s * invD;
+        float v2 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v2 = fmaf(yv[k] - mu, yv[k] - mu, v2);
+        v2 += __shfl_xor_sync(kFull, v2, 1);
+        const float rs = rsqrtf(v2 * invD + eps);
+        float l = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int chunk = 4 * half + c;  // 8 features per 16-byte chunk
+            const uint4 qb = *reinterpret_cast<const uint4 *>(stg + kOffQ + swz(tl, chunk));
+            const uint4 vb = *reinterpret_cast<const uint4 *>(stg + kOffV + swz(tl, chunk));
+            const uint32_t qw[4] = {qb.x, qb.y, qb.z, qb.w}, vw[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int k = 8 * c + q;
+                const float qf = bf16_bits_to_f32(q & 1 ? qw[q >> 1] >> 16 : qw[q >> 1] & 0xffffu);
+                const float vf = bf16_bits_to_f32(q & 1 ? vw[q >> 1] >> 16 : vw[q >> 1] & 0xffffu);
+                const float z = qf + fmaf(gam[k], (yv[k] - mu) * rs, bet[k]);
+                yv[k] = z;
+                l = fmaf(z - vf, z - vf, l);
             }
         }
-        __syncwarp();
-        // dq[j][r] = q_t . k_s with t = g + 8(r>>1), s = 8j + 2c4 + (r&1)
-        const uint32_t sK = smem_u32(stg + kOffKh), sQ = smem_u32(stg + kOffQh);
-        float dq[2][4] = {};
+        l += __shfl_xor_sync(kFull, l, 1);
+        const size_t row = tok0 + (size_t)j * kB + tl;
+        if (p.z_f32) {
+            float4 *Zr = reinterpret_cast<float4 *>(static_cast<float *>(p.Z) + row * kD + 32 * half);
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-            uint32_t aq[4], bk[4];
-            ldsm_x4(aq, sQ + swz(ra, 2 * ks + (lane >> 4)));
-            ldsm_x4(bk, sK + swz(rb, 2 * ks + ((lane >> 3) & 1)));
-            mma16816(dq[0], aq, bk[0], bk[1]);
-            mma16816(dq[1], aq, bk[2], bk[3]);
+            for (int k = 0; k < 8; ++k) Zr[k] = make_float4(yv[4 * k], yv[4 * k + 1], yv[4 * k + 2], yv[4 * k + 3]);
+        } else {
+            uint4 *Zr = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Z) + row * kD + 32 * half);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                Zr[k] = make_uint4(pack_bf2(yv[8 * k], yv[8 * k + 1]), pack_bf2(yv[8 * k + 2], yv[8 * k + 3]),
+                                   pack_bf2(yv[8 * k + 4], yv[8 * k + 5]), pack_bf2(yv[8 * k + 6], yv[8 * k + 7]));
         }
-        auto mq = [&](int j, int r) {
-            const int t = g + 8 * (r >> 1), s = 8 * j + 2 * c4 + (r & 1);
-            return s <= t ? dq[j][r] + 1.f : 0.f;
-        };
-        reinterpret_cast<uint4 *>(stg + kOffMq)[lane] =
-            make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)),
-                       pack_h2(mq(0, 2), mq(0, 3)), pack_h2(mq(1, 2), mq(1, 3)));
-        warp_arrive(&R.prep[st], lane);
-        if (lane == 0) mbar_arrive(&R.empty[st]);
+        if (p.loss && half == 0) p.loss[row] = l;
+        warp_arrive(&R.empty[stj], lane);
     }
     const bool range_bad = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
     if (__any_sync(kFull, range_bad) && lane == 0) {
@@ -338,6 +454,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
                       pack_h2(rq[m][1][2], rq[m][1][3]));
         }
         named_bar_arrive(kBarX2q, kHY);
+        warp_arrive(R.hq, lane);
         if (w == 0) TTT_TRACE_AT(p, i, 4);
         // W1 += A~1 K, c1 += A~1 1.
 #pragma unroll
@@ -578,26 +695,21 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
         if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
             !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags))
             abort_chain(R.flags, p.status);
-        // k - v + beta, q and v at this lane's (feature, token) positions: ldmatrix.trans of the bf16 tiles.
-        float kv[2][2][4], qv[2][2][4], vv[2][2][4];
+        // k - v + beta at this lane's (feature, token) positions: ldmatrix.trans of the bf16 tiles.
+        float kv[2][2][4];
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
             const int chunk = 2 * (2 * y + m) + cbt;
-            uint32_t kr[4], vr[4], qr[4];
+            uint32_t kr[4], vr[4];
             ldsm_x4_t(kr, smem_u32(stg + kOffK) + swz(rbt, chunk));
             ldsm_x4_t(vr, smem_u32(stg + kOffV) + swz(rbt, chunk));
-            ldsm_x4_t(qr, smem_u32(stg + kOffQ) + swz(rbt, chunk));
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const uint32_t a = kr[2 * n + u], b = vr[2 * n + u], q = qr[2 * n + u];
-                    vv[m][n][2 * u] = bf16_bits_to_f32(b & 0xffffu);
-                    vv[m][n][2 * u + 1] = bf16_bits_to_f32(b >> 16);
-                    kv[m][n][2 * u] = bf16_bits_to_f32(a & 0xffffu) - vv[m][n][2 * u] + bet[m][u];
-                    kv[m][n][2 * u + 1] = bf16_bits_to_f32(a >> 16) - vv[m][n][2 * u + 1] + bet[m][u];
-                    qv[m][n][2 * u] = bf16_bits_to_f32(q & 0xffffu);
-                    qv[m][n][2 * u + 1] = bf16_bits_to_f32(q >> 16);
+                    const uint32_t a = kr[2 * n + u], b = vr[2 * n + u];
+                    kv[m][n][2 * u] = bf16_bits_to_f32(a & 0xffffu) - bf16_bits_to_f32(b & 0xffffu) + bet[m][u];
+                    kv[m][n][2 * u + 1] = bf16_bits_to_f32(a >> 16) - bf16_bits_to_f32(b >> 16) + bet[m][u];
                 }
         }
         float es[2][2];
@@ -695,27 +807,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
         }
         named_bar_sync(kBarX2q, kHY);
         if (y == 0) TTT_TRACE_AT(p, i, 12);
-        // Mq2 = causal gelu(Z1q_t) . gelu(Z1k_s) + 1 as B fragments; Yq^T = W2_{i-1} X2q^T + c2 + A~2 Mq2.
-        uint4 mq2;
-        {
-            const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);
-            const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);
-            float dq[2][4] = {};
-#pragma unroll 4
-            for (int ks = 0; ks < kHid / 16; ++ks) {
-                uint32_t aq[4], bk[4];
-                ldsm_x4(aq, hb(sX2q, ra, 16 * ks + ca, kHS));
-                ldsm_x4(bk, hb(sX2k, rb, 16 * ks + cb, kHS));
-                mma16816(dq[0], aq, bk[0], bk[1]);
-                mma16816(dq[1], aq, bk[2], bk[3]);
-            }
-            auto mq = [&](int j, int r) {
-                const int t = g + 8 * (r >> 1), s = 8 * j + 2 * c4 + (r & 1);
-                return s <= t ? dq[j][r] + 1.f : 0.f;
-            };
-            mq2 = make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)), pack_h2(mq(0, 2), mq(0, 3)),
-                             pack_h2(mq(1, 2), mq(1, 3)));
-        }
+        // Yq^T = W2_{i-1} X2q^T + c2 + A~2 Mq2, Mq2 (causal x2q.x2k + 1) from P.
         float yq[2][2][4];
 #pragma unroll
         for (int m = 0; m < 2; ++m)
@@ -724,50 +816,30 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
 #pragma unroll
                 for (int r = 0; r < 4; ++r) yq[m][n][r] = c2o[m][r >> 1];
         y_gemm(sW2p, sX2q, f0, lane, yq);
+        if (!wait_bar(R.mq2, parity_of(i), R.flags)) abort_chain(R.flags, p.status);
+        {
+            const uint4 mq2 = reinterpret_cast<const uint4 *>(sm + kOffMq2)[lane];
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const uint32_t af[4] = {pack_h2(a2[m][0][0], a2[m][0][1]), pack_h2(a2[m][0][2], a2[m][0][3]),
-                                    pack_h2(a2[m][1][0], a2[m][1][1]), pack_h2(a2[m][1][2], a2[m][1][3])};
-            mma16816(yq[m][0], af, mq2.x, mq2.y);
-            mma16816(yq[m][1], af, mq2.z, mq2.w);
+            for (int m = 0; m < 2; ++m) {
+                const uint32_t af[4] = {pack_h2(a2[m][0][0], a2[m][0][1]), pack_h2(a2[m][0][2], a2[m][0][3]),
+                                        pack_h2(a2[m][1][0], a2[m][1][1]), pack_h2(a2[m][1][2], a2[m][1][3])};
+                mma16816(yq[m][0], af, mq2.x, mq2.y);
+                mma16816(yq[m][1], af, mq2.z, mq2.w);
+            }
         }
-        named_bar_arrive(kBarYdone, kHY);
+        named_bar_arrive(kBarYdone, kHY);  // X2k, X2q and the Gram fragments of step i are consumed
         if (y == 0) TTT_TRACE_AT(p, i, 13);
-        // z = q + LN(yq); L_t = ||z_t - v_t||^2
-        y_ln_stats(yq, red, rnd, y, g, c4, eps, mu, rs);
-        float sz[2][2] = {}, d0[2][2] = {}, d1[2][2] = {};
+        const int slot = i & 1;
+        if (!wait_bar(&R.yqempty[slot], parity_of(i >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
+        float *ys = reinterpret_cast<float *>(sm + kOffYq) + slot * kB * kYS;
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int e = r & 1, u = r >> 1;
-                    const float z = qv[m][n][r] + fmaf(gam[m][u], (yq[m][n][r] - mu[n][e]) * rs[n][e], bet[m][u]);
-                    yq[m][n][r] = z;
-                    const float dz = z - vv[m][n][r];
-                    sz[n][e] = fmaf(dz, dz, sz[n][e]);
-                }
-        y_sum3(sz, d0, d1, red, rnd, y, g, c4);
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int t = i * kB + 8 * n + 2 * c4 + e;
-                if (t >= T) continue;
-#pragma unroll
-                for (int m = 0; m < 2; ++m)
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int f = f0 + 16 * m + g + 8 * u;
-                        const float z = yq[m][n][e + 2 * u];
-                        if (p.z_f32)
-                            static_cast<float *>(p.Z)[(tok0 + t) * kD + f] = z;
-                        else
-                            static_cast<__nv_bfloat16 *>(p.Z)[(tok0 + t) * kD + f] = __float2bfloat16_rn(z);
-                    }
-                if (p.loss && y == 0 && g == 0) p.loss[tok0 + t] = sz[n][e];
-            }
+                for (int r = 0; r < 4; ++r)
+                    ys[(8 * n + 2 * c4 + (r & 1)) * kYS + f0 + 16 * m + g + 8 * (r >> 1)] = yq[m][n][r];
+        warp_arrive(&R.yqfull[slot], lane);
         if (y == 0) TTT_TRACE_AT(p, i, 14);
         warp_arrive(&R.empty[st], lane);
     }
@@ -801,6 +873,10 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     R.full = bar;
     R.prep = bar + kStages;
     R.empty = bar + 2 * kStages;
+    R.hq = bar + 3 * kStages;
+    R.mq2 = R.hq + 1;
+    R.yqfull = R.hq + 2;
+    R.yqempty = R.hq + 4;
     R.flags = reinterpret_cast<volatile int *>(bar + kNumBars);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffTmem);
 
@@ -813,6 +889,12 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(&R.full[s], 33);               // expect_tx arrive + 32 cp.async arrivals
             mbar_init(&R.prep[s], 1);
             mbar_init(&R.empty[s], kNH + kNY + 1);  // H warps, Y warps, P
+        }
+        mbar_init(R.hq, kNH);
+        mbar_init(R.mq2, 1);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&R.yqfull[j], kNY);
+            mbar_init(&R.yqempty[j], 1);
         }
         R.flags[0] = 0;
         R.flags[1] = 0;
@@ -833,7 +915,7 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         role_loader<kD>(&tmQ, &tmK, &tmV, p.eta + tok0, p.T, p.status, sm + kOffStages, geom, R.full, R.empty,
                         R.flags, chain, lane, nsteps);
     } else if (warp == kWarpP) {
-        role_prep(p, sm, R, lane, nsteps);
+        role_prep(p, sm, R, hi, tok0, lane, nsteps);
     } else if (warp < kWarpY) {
         role_hidden(p, sm, R, warp - kWarpH, warp, chain, bi, hi, tmem, lane, nsteps);
     } else {
