@@ -220,34 +220,12 @@ def _sample_shape(w, cpu_s: float, threads: int):
 
 # ---------------------------------------------------------------- GPU arm
 
-def _dist():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    if ws > 1:
-        import torch.distributed as dist
-        if not dist.is_initialized():
-            backend = "nccl" if torch.cuda.is_available() else "gloo"
-            dist.init_process_group(backend)
-        return dist, dist.get_rank(), ws
-    return None, 0, 1
-
-
-def _barrier(dist):
-    if dist is not None:
-        dist.barrier()
-
-
-def _max_over_ranks(dist, x: float) -> float:
-    if dist is None:
-        return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
 def run_gpu(args):
     import test_weight_sequence_ttt_b300 as ttt
+    from test_weight_sequence_ttt_b300 import shard
 
-    dist, rank, world = _dist()
+    dist = shard.init()
+    rank, world = shard.world()
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     w = WORKLOADS[args.workload]
@@ -282,7 +260,7 @@ def run_gpu(args):
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device())
-    _barrier(dist)
+    shard.barrier(dist)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     with sampler:
@@ -293,10 +271,10 @@ def run_gpu(args):
             e1.record(stream)
         torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    _barrier(dist)
+    shard.barrier(dist)
     times_ms = [a.elapsed_time(b) for a, b in evs]
     ms = statistics.mean(times_ms)
-    ms_max = _max_over_ranks(dist, ms)
+    ms_max = shard.max_over_ranks(dist, ms)
     if int(st.item()) != 0:
         raise RuntimeError("device status %d in timed region" % int(st.item()))
 
@@ -318,19 +296,19 @@ def run_gpu(args):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    _barrier(dist)
+    shard.barrier(dist)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         e2e_step()
         torch.cuda.synchronize()          # the result is on the host before the next step
     e2e_s = (time.perf_counter() - t0) / e2e_steps
-    e2e_s = _max_over_ranks(dist, e2e_s)
+    e2e_s = shard.max_over_ranks(dist, e2e_s)
+    tokens = shard.sum_over_ranks(dist, w.tokens)  # every rank ran its own full workload (weak scaling)
 
     if rank != 0:
         return None
     peaks = _peaks()
     bytes_launch, flops_launch = algorithmic_cost(w, 4 if args.z_dtype == "f32" else 2)
-    tokens = w.tokens * world
     value = tokens / (ms_max / 1e3)
     if w.variant == "linear":
         bound, achieved, peak, unit = "hbm", bytes_launch / (ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"

@@ -66,7 +66,7 @@ cudaError_t launch_mlp_f32(const MlpParams &p, int io, int chains, cudaStream_t 
 bool mlp_tc_supported(int io, int d, int hidden, int mb);
 cudaError_t launch_mlp_tc(const MlpParams &p, int chains, cudaStream_t s);
 
-// Tensor-core kernel (io bf16, d in {64,128}, mb in {1,2,4,8,16}).
+// Tensor-core kernel (io bf16, d in {64,128}, mb in {1,2,4,8,16,32,64}).
 bool linear_tc_supported(int io, int d, int mb);
 // Returns cudaSuccess or the failing error; tensor maps are built inside.
 cudaError_t launch_linear_tc(const LinearParams &p, int chains, cudaStream_t s);

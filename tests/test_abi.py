@@ -76,7 +76,10 @@ def test_struct_layout_matches_header(cls, cname):
 def test_kernel_kind_table(L):
     assert ttt.linear_kernel_kind(ttt.BF16, 64, 16) == 2
     assert ttt.linear_kernel_kind(ttt.BF16, 128, 1) == 2
-    assert ttt.linear_kernel_kind(ttt.BF16, 128, 64) == 1     # fp32 kernel for now
+    assert ttt.linear_kernel_kind(ttt.BF16, 128, 64) == 2
+    assert ttt.linear_kernel_kind(ttt.BF16, 64, 32) == 2
+    assert ttt.linear_kernel_kind(ttt.BF16, 128, 128) == 0    # no kernel for b > 64
+    assert ttt.linear_kernel_kind(ttt.BF16, 64, 3) == 1       # fp32 kernel
     assert ttt.linear_kernel_kind(ttt.F32, 16, 16) == 1
     assert ttt.linear_kernel_kind(ttt.F32, 256, 16) == 0
     assert ttt.linear_kernel_kind(7, 64, 16) == 0

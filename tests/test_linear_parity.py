@@ -47,10 +47,11 @@ def test_f32_shapes(d, b, T):
 # ---------------------------------------------------------------- tensor-core path
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("b", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("b", [1, 2, 4, 8, 16, 32, 64])
 def test_tc_small(d, b):
     assert ttt.linear_kernel_kind(ttt.BF16, d, b) == 2
-    T = 48 if b == 16 else 40      # several super-steps, ragged last one for b < 16
+    # several super-steps; a ragged last one for b < 16; several mini-batches for b > 16
+    T = {16: 48, 32: 96, 64: 192}.get(b, 40)
     _check(_small(d, b, T), TOL["bf16"])
 
 
@@ -67,8 +68,8 @@ def test_bf16_fp32_kernel_shapes():
     # bf16 io on shapes the tensor-core kernel does not take (fp32 FFMA kernel)
     assert ttt.linear_kernel_kind(ttt.BF16, 32, 16) == 1
     _check(_small(32, 16, 48), TOL["bf16"])
-    assert ttt.linear_kernel_kind(ttt.BF16, 128, 64) == 1
-    _check(_small(128, 64, 128, B=1, H=2), TOL["bf16"])
+    assert ttt.linear_kernel_kind(ttt.BF16, 96, 8) == 1
+    _check(_small(96, 8, 40, B=1, H=2), TOL["bf16"])
 
 
 @pytest.mark.parametrize("d,b", [(64, 16), (128, 4), (64, 1)])

@@ -51,3 +51,97 @@ def test_mlp_full_size_sampled_chains():
     errs = {k: rel_err(to_np(got[k])[idx], ref[k].reshape(to_np(got[k])[idx].shape)) for k in KEYS}
     print(errs)
     assert errs["Z"] <= TOL["bf16"], errs
+
+
+# ---------------------------------------------------------------- tensor-core MLP kernel (d=64, h=256, b=16)
+
+def _tc(T=64, B=2, H=2, seed=91):
+    w = WORKLOADS["mlp_b4h12_d64_t8k"].with_(B=B, H=H, T=T, seed=seed)
+    return make_inputs(w)
+
+
+def test_mlp_tc_kernel_kind():
+    assert ttt.mlp_kernel_kind(ttt.BF16, 64, 256, 16) == 2
+    assert ttt.mlp_kernel_kind(ttt.BF16, 64, 256, 4) == 1
+    assert ttt.mlp_kernel_kind(ttt.F32, 64, 256, 16) == 1
+
+
+@pytest.mark.parametrize("T", [16, 32, 160])
+def test_mlp_tc_lengths(T):
+    inp = _tc(T=T, B=1, H=3)
+    got = run_mlp(inp)
+    assert int(got["status"].item()) == 0
+    compare(got, oracle_mlp(inp), KEYS, TOL["bf16"])
+
+
+def test_mlp_tc_per_sequence_weights_and_ln_params():
+    inp = _tc(T=48, B=3, H=2)
+    g = torch.Generator().manual_seed(11)
+    inp["W1"] = torch.randn(3, 2, 256, 64, generator=g) * 0.05
+    inp["W2"] = torch.randn(3, 2, 64, 256, generator=g) * 0.05
+    inp["c1"] = torch.randn(3, 2, 256, generator=g) * 0.1
+    inp["c2"] = torch.randn(3, 2, 64, generator=g) * 0.1
+    inp["ln_g"] = 1.0 + 0.2 * torch.randn(2, 64, generator=g)
+    inp["ln_b"] = 0.1 * torch.randn(2, 64, generator=g)
+    got = run_mlp(inp)
+    assert int(got["status"].item()) == 0
+    compare(got, oracle_mlp(inp), KEYS, TOL["bf16"])
+
+
+def test_mlp_tc_causality_bit_exact():
+    inp = _tc(T=64, B=1, H=2)
+    base = run_mlp(inp)
+    t = 37
+    for key in ("Q", "K", "V"):
+        pert = dict(inp)
+        pert[key] = inp[key].clone()
+        pert[key][0, 1, t] += 0.5
+        r = run_mlp(pert)
+        assert torch.equal(r["Z"][:, :, :t], base["Z"][:, :, :t]), key
+        assert torch.equal(r["loss"][:, :, :t], base["loss"][:, :, :t]), key
+        assert torch.equal(r["Z"][:, 0], base["Z"][:, 0]), key
+        assert not torch.equal(r["Z"][0, 1, t:], base["Z"][0, 1, t:]), key
+
+
+def test_mlp_tc_chain_permutation():
+    inp = _tc(T=32, B=3, H=2)
+    base = run_mlp(inp)
+    perm = torch.tensor([2, 0, 1])
+    pinp = dict(inp)
+    for k in ("Q", "K", "V", "eta"):
+        pinp[k] = inp[k][perm].contiguous()
+    r = run_mlp(pinp)
+    for k in KEYS:
+        assert torch.equal(r[k], base[k][perm]), k
+
+
+def test_mlp_tc_resume_two_calls():
+    inp = _tc(T=96, B=1, H=2)
+    full = run_mlp(inp)
+    T1 = 48
+    a, bb = dict(inp), dict(inp)
+    for k in ("Q", "K", "V", "eta"):
+        a[k] = inp[k][:, :, :T1].contiguous()
+        bb[k] = inp[k][:, :, T1:].contiguous()
+    ra = run_mlp(a)
+    for k in ("W1", "c1", "W2", "c2"):
+        bb[k] = ra[k].cpu()
+    rb = run_mlp(bb)
+    z = torch.cat([ra["Z"], rb["Z"]], 2)
+    assert rel_err(to_np(z), to_np(full["Z"])) < 1e-2
+    assert rel_err(to_np(rb["W2"]), to_np(full["W2"])) < 1e-2
+
+
+def test_mlp_tc_outputs_fully_written():
+    inp = _tc(T=32, B=2, H=2)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    nan = lambda *s: torch.full(s, float("nan"), device="cuda")
+    out = {"Z": nan(2, 2, 32, 64), "W1": nan(2, 2, 256, 64), "c1": nan(2, 2, 256), "W2": nan(2, 2, 64, 256),
+           "c2": nan(2, 2, 64), "loss": nan(2, 2, 32), "inner_loss": nan(2, 2, 32)}
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = ttt.ttt_mlp_forward(d["Q"], d["K"], d["V"], d["eta"], d["W1"], d["c1"], d["W2"], d["c2"], d["ln_g"],
+                            d["ln_b"], mb=16, out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for k in out:
+        assert torch.isfinite(r[k]).all(), k
