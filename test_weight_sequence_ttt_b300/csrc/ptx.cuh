@@ -245,6 +245,14 @@ __device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r
                  : "memory");
 }
 
+// Transpose of an 8x8 b16 matrix held one row pair per thread (mma fragment order).
+__device__ __forceinline__ uint32_t movm_t(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // ------------------------------------------------------------------ mma (legacy warp-level)
 // D[16x8] += A[16x16] * B[16x8], fp16 operands, fp32 accumulate.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)

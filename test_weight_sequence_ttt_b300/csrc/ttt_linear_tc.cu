@@ -88,7 +88,9 @@ struct Cfg {
     static constexpr int kOffSh = kOffEta + 64;      //   LayerNorm shift
     static constexpr int kOffPk = kOffSh + 64;       //   sum_f gamma_f kv_f
     static constexpr int kOffQk = kOffPk + 64;       //   sum_f kv_f^2
-    static constexpr int kStageBytes = ((kOffQk + 64 + 1023) / 1024) * 1024;
+    static constexpr int kOffKxA = kOffQk + 64;      // K_{i-1} K_i^T + 1 and K_i K_i^T + 1 as fp16
+    static constexpr int kOffGkA = kOffKxA + 512;    //   A fragments (rows t of step i)
+    static constexpr int kStageBytes = ((kOffGkA + 512 + 1023) / 1024) * 1024;
     static constexpr int YS = D + 4;                 // row stride (floats) of the Yq^T hand-off
     static constexpr int kOffStages = 0;
     static constexpr int kOffY = kStages * kStageBytes;            // 2 slots x [16][YS] fp32
@@ -97,8 +99,9 @@ struct Cfg {
     static constexpr int kOffCst = kOffRedY + 2 * MT * kSS * 4;   // u0, gamma, beta: 3 x D floats
     // chain/weight split (D = 64): hand-off rings between the chain (C) and weight (T) warps
     static constexpr int kOffAR = kOffCst + 3 * D * 4;            // 2 slots x [MT][32 lanes] A~ fragments
-    static constexpr int kOffSR = kOffAR + 2 * MT * 512;          // 2 slots x [MT][2][32 lanes] S fragments
-    static constexpr int kOffBar = kOffSR + 2 * MT * 1024;
+    static constexpr int SRS = 20;                                // row stride (floats) of an S block [16 t][16 f]
+    static constexpr int kOffSR = kOffAR + 2 * MT * 512;          // 2 slots x [MT][16][SRS] S blocks
+    static constexpr int kOffBar = kOffSR + 2 * MT * 16 * SRS * 4;
     static constexpr int kSplitWarpC = 2, kSplitWarpT = 2 + MT, kSplitWarpO = 2 + 2 * MT;
     static constexpr int kSplitWarps = kSplitWarpO + NO;
     static constexpr int kSplitThreads = kSplitWarps * 32;
@@ -133,22 +136,44 @@ template <int D>
 constexpr bool kSumsInLoader = D == 64;
 
 // Chain constants into shared memory: u0 = feature mean of W_0's rows, gamma,
-// beta; returns mean(c0) (all lanes).
+// beta; returns mean(c0) (all lanes). W_0 is read row-contiguously in float4s
+// with every load of a lane independent, so the whole matrix is in flight at
+// once instead of one dependent round trip per row.
 template <int D>
 __device__ float chain_consts(const LinearParams &p, uint8_t *sm, int bi, int hi, int lane)
 {
     using C = Cfg<D>;
+    constexpr int Q4 = D / 4;              // float4s per row
+    constexpr int RSTEP = 32 / Q4;         // rows covered by one pass of the warp (2 for d = 64, 1 for 128)
     float *cu = reinterpret_cast<float *>(sm + C::kOffCst), *cg = cu + D, *cbt = cg + D;
-    const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
+    const float4 *W4 = reinterpret_cast<const float4 *>(p.W0 + bi * p.w0_bstride + (long long)hi * D * D);
     const float *c0 = p.c0 + bi * p.c0_bstride + (long long)hi * D;
+    const int q = lane % Q4, r0 = lane / Q4;  // this lane's column group and first row
+    float4 acc[4] = {};
+#pragma unroll 16
+    for (int f = r0, k = 0; f < D; f += RSTEP, ++k) {
+        const float4 v = W4[f * Q4 + q];
+        acc[k & 3].x += v.x;
+        acc[k & 3].y += v.y;
+        acc[k & 3].z += v.z;
+        acc[k & 3].w += v.w;
+    }
+    float4 t = make_float4((acc[0].x + acc[1].x) + (acc[2].x + acc[3].x), (acc[0].y + acc[1].y) + (acc[2].y + acc[3].y),
+                           (acc[0].z + acc[1].z) + (acc[2].z + acc[3].z), (acc[0].w + acc[1].w) + (acc[2].w + acc[3].w));
+    if (RSTEP == 2) {  // lanes q and q + 16 summed alternate rows
+        t.x += __shfl_xor_sync(kFull, t.x, 16);
+        t.y += __shfl_xor_sync(kFull, t.y, 16);
+        t.z += __shfl_xor_sync(kFull, t.z, 16);
+        t.w += __shfl_xor_sync(kFull, t.w, 16);
+    }
+    if (r0 == 0) {
+        const float s = 1.f / (float)D;
+        reinterpret_cast<float4 *>(cu)[q] = make_float4(t.x * s, t.y * s, t.z * s, t.w * s);
+    }
     float cmean = 0.f;
 #pragma unroll
-    for (int q = 0; q < D / 32; ++q) {
-        const int j = lane + 32 * q;
-        float s[8] = {};
-#pragma unroll 8
-        for (int f = 0; f < D; ++f) s[f & 7] += W0[f * D + j];
-        cu[j] = ((s[0] + s[1]) + (s[2] + s[3]) + ((s[4] + s[5]) + (s[6] + s[7]))) * (1.f / (float)D);
+    for (int qq = 0; qq < D / 32; ++qq) {
+        const int j = lane + 32 * qq;
         cg[j] = p.ln_g[hi * D + j];
         cbt[j] = p.ln_b[hi * D + j];
         cmean += c0[j];
@@ -337,14 +362,16 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
             make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)),
                        pack_h2(mq(0, 2), mq(0, 3)), pack_h2(mq(1, 2), mq(1, 3)));
         if (SUBB < 16) {
-            reinterpret_cast<uint4 *>(stg + C::kOffGk)[lane] = make_uint4(
-                pack_h2(dk[0][0] + 1.f, dk[0][1] + 1.f), pack_h2(dk[1][0] + 1.f, dk[1][1] + 1.f),
-                pack_h2(dk[0][2] + 1.f, dk[0][3] + 1.f), pack_h2(dk[1][2] + 1.f, dk[1][3] + 1.f));
+            const uint32_t k0 = pack_h2(dk[0][0] + 1.f, dk[0][1] + 1.f), k1 = pack_h2(dk[1][0] + 1.f, dk[1][1] + 1.f);
+            const uint32_t k2 = pack_h2(dk[0][2] + 1.f, dk[0][3] + 1.f), k3 = pack_h2(dk[1][2] + 1.f, dk[1][3] + 1.f);
+            reinterpret_cast<uint4 *>(stg + C::kOffGk)[lane] = make_uint4(k0, k1, k2, k3);   // B (k = s, n = t)
+            reinterpret_cast<uint4 *>(stg + C::kOffGkA)[lane] = make_uint4(k0, k2, k1, k3);  // A (m = t, k = s)
         }
         if (has_prev) {
-            reinterpret_cast<uint4 *>(stg + C::kOffKx)[lane] = make_uint4(
-                pack_h2(dx[0][0] + 1.f, dx[0][1] + 1.f), pack_h2(dx[1][0] + 1.f, dx[1][1] + 1.f),
-                pack_h2(dx[0][2] + 1.f, dx[0][3] + 1.f), pack_h2(dx[1][2] + 1.f, dx[1][3] + 1.f));
+            const uint32_t x0 = pack_h2(dx[0][0] + 1.f, dx[0][1] + 1.f), x1 = pack_h2(dx[1][0] + 1.f, dx[1][1] + 1.f);
+            const uint32_t x2 = pack_h2(dx[0][2] + 1.f, dx[0][3] + 1.f), x3 = pack_h2(dx[1][2] + 1.f, dx[1][3] + 1.f);
+            reinterpret_cast<uint4 *>(stg + C::kOffKx)[lane] = make_uint4(x0, x1, x2, x3);   // B (k = s_{i-1}, n = t_i)
+            reinterpret_cast<uint4 *>(stg + C::kOffKxA)[lane] = make_uint4(x0, x2, x1, x3);  // A (m = t_i, k = s_{i-1})
         }
         warp_arrive(&R.prep[st], lane);
         TTT_TRACE_AT(p, i, 13);
@@ -1026,6 +1053,10 @@ constexpr int kBarRed = 1;  // C warps: one reduction round
 constexpr int kBarA0 = 2;   // A~_i ready (C -> T), ids 2 and 3 by i & 1
 constexpr int kBarS0 = 4;   // S_k ready (T -> C), ids 4 and 5 by k & 1
 
+// C warp w holds Y_i for output features f0..f0+15 (f0 = 16w) with the tokens
+// on the mma M axis: lane (g, c4) has tokens g, g+8 and features
+// f0 + 8nt + 2c4 + e, so a token's sums over the warp's 16 features need four
+// in-register terms and two shuffle levels.
 template <int D, int SUBB>
 __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int hi, size_t tok0,
                                  int lane, int nsteps)
@@ -1034,30 +1065,42 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
     constexpr int MT = C::MT, NSUB = kSS / SUBB;
     constexpr int kNAS = 2 * MT * 32;
     const int g = lane >> 2, c4 = lane & 3;
-    const int r0 = 16 * w + g, r1 = r0 + 8;
-    const float gam[2] = {p.ln_g[hi * D + r0], p.ln_g[hi * D + r1]};
-    const float bet[2] = {p.ln_b[hi * D + r0], p.ln_b[hi * D + r1]};
+    const int f0 = 16 * w;
+    float gam[2][2], bet[2][2], gg2[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int f = f0 + 8 * nt + 2 * c4 + e;
+            gam[nt][e] = p.ln_g[hi * D + f];
+            bet[nt][e] = p.ln_b[hi * D + f];
+            gg2[nt][e] = gam[nt][e] * gam[nt][e];
+        }
     float gam2all = 0.f;  // sum of gamma^2 over all features
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) gam2all = fmaf(p.ln_g[hi * D + lane + 32 * q], p.ln_g[hi * D + lane + 32 * q], gam2all);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) gam2all += __shfl_xor_sync(kFull, gam2all, o);
-    const int rb = (lane & 7) + (lane >> 4) * 8, cb16 = (lane >> 3) & 1;
     const float invD = 1.f / (float)D, eps = p.eps;
     const int T = p.T;
-    const float4 *SR = reinterpret_cast<const float4 *>(sm + C::kOffSR);
+    const float *SR = reinterpret_cast<const float *>(sm + C::kOffSR);
     uint4 *AR = reinterpret_cast<uint4 *>(sm + C::kOffAR);
+    const int tcomb = g + 8 * (c4 & 1);  // the token this lane combines across the C warps
     int rnd = 0;
-    float yk[2][4];
-    named_bar_sync(kBarS0, kNAS);  // Y_0 = W_0 K_0^T + c_0 from the T warps
+    float yk[2][4];  // [nt][r]: token g + 8(r>>1), feature f0 + 8nt + 2c4 + (r&1)
+    auto load_s = [&](int slot) {
+        const float *blk = SR + (slot * MT + w) * 16 * C::SRS;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const float4 v = SR[w * 64 + nt * 32 + lane];
-        yk[nt][0] = v.x;
-        yk[nt][1] = v.y;
-        yk[nt][2] = v.z;
-        yk[nt][3] = v.w;
-    }
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float2 v = *reinterpret_cast<const float2 *>(blk + (g + 8 * u) * C::SRS + 8 * nt + 2 * c4);
+                yk[nt][2 * u] = v.x;
+                yk[nt][2 * u + 1] = v.y;
+            }
+    };
+    named_bar_sync(kBarS0, kNAS);  // Y_0 = W_0 K_0^T + c_0 from the T warps
+    load_s(0);
     for (int i = 0; i < nsteps; ++i) {
         const int st = i % kStages, stn = (i + 1) % kStages;
         const bool has_next = i + 1 < nsteps;
@@ -1065,76 +1108,68 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
         uint8_t *stgn = stage_ptr<D>(sm, stn);
         if (w == 0) TTT_TRACE_AT(p, i, 0);
         // Stage i was waited for by the T warps before they published S_i; the
-        // named barrier that handed S_i over orders those reads after the loads.
+        // named barrier that handed S_i over orders these reads after the loads.
         float kv[2][4];
-        {
-            uint32_t kr[4], vr[4];
-            ldsm_x4_t(kr, smem_u32(stg + C::kOffK) + swz(rb, 2 * w + cb16));
-            ldsm_x4_t(vr, smem_u32(stg + C::kOffV) + swz(rb, 2 * w + cb16));
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const uint32_t a = kr[2 * nt + u], b = vr[2 * nt + u];
-                    kv[nt][2 * u] = bf16_bits_to_f32(a & 0xffffu) - bf16_bits_to_f32(b & 0xffffu) + bet[u];
-                    kv[nt][2 * u + 1] = bf16_bits_to_f32(a >> 16) - bf16_bits_to_f32(b >> 16) + bet[u];
-                }
-        }
-        const float *ssh = reinterpret_cast<const float *>(stg + C::kOffSh);
-        float escale[2][2], shv[2][2];
-        {
-            const float *se = reinterpret_cast<const float *>(stg + C::kOffEta);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float2 e2 = *reinterpret_cast<const float2 *>(se + 8 * nt + 2 * c4);
-                const float2 s2 = *reinterpret_cast<const float2 *>(ssh + 8 * nt + 2 * c4);
-                escale[nt][0] = -e2.x * (1.f / (float)SUBB);
-                escale[nt][1] = -e2.y * (1.f / (float)SUBB);
-                shv[nt][0] = s2.x;
-                shv[nt][1] = s2.y;
+            for (int u = 0; u < 2; ++u) {
+                const int t = g + 8 * u, f = f0 + 8 * nt + 2 * c4;
+                const uint32_t off = swz(t, f >> 3) + (f & 7) * 2;
+                const uint32_t kb = *reinterpret_cast<const uint32_t *>(stg + C::kOffK + off);
+                const uint32_t vb = *reinterpret_cast<const uint32_t *>(stg + C::kOffV + off);
+                kv[nt][2 * u] = bf16_bits_to_f32(kb & 0xffffu) - bf16_bits_to_f32(vb & 0xffffu) + bet[nt][0];
+                kv[nt][2 * u + 1] = bf16_bits_to_f32(kb >> 16) - bf16_bits_to_f32(vb >> 16) + bet[nt][1];
             }
-        }
-        const int tc = 8 * (g & 1) + 2 * c4 + ((g >> 1) & 1);
-        const float sh_c = ssh[tc];
-        const float pk_c = reinterpret_cast<const float *>(stg + C::kOffPk)[tc];
-        const float qk_c = reinterpret_cast<const float *>(stg + C::kOffQk)[tc];
-        float at[2][4] = {}, lin[2][2] = {};
+        const float *ssh = reinterpret_cast<const float *>(stg + C::kOffSh);
+        const float *se = reinterpret_cast<const float *>(stg + C::kOffEta);
+        const float escale[2] = {-se[g] * (1.f / (float)SUBB), -se[g + 8] * (1.f / (float)SUBB)};
+        const float shv[2] = {ssh[g], ssh[g + 8]};
+        const float sh_c = ssh[tcomb];
+        const float pk_c = reinterpret_cast<const float *>(stg + C::kOffPk)[tcomb];
+        const float qk_c = reinterpret_cast<const float *>(stg + C::kOffQk)[tcomb];
+        float at[2][4] = {}, lin[2] = {};
 #pragma unroll
         for (int m = 0; m < NSUB; ++m) {
-            float s1[2][2], s2[2][2], sb[2][2], sc[2][2], sd[2][2];
+            // this warp's shifted sums over its 16 features, per token (u)
+            float q[2][5];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float a1 = 0.f, a2 = 0.f, ab = 0.f, ac = 0.f, ad = 0.f;
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const float dv = yk[nt][e + 2 * u] - shv[nt][e];
-                        const float g2d = gam[u] * gam[u] * dv;
-                        a1 += dv;
-                        a2 = fmaf(dv, dv, a2);
-                        ab += g2d;
-                        ac = fmaf(g2d, dv, ac);
-                        ad = fmaf(gam[u] * kv[nt][e + 2 * u], dv, ad);
-                    }
-                    s1[nt][e] = col_sum(a1);
-                    s2[nt][e] = col_sum(a2);
-                    sb[nt][e] = col_sum(ab);
-                    sc[nt][e] = col_sum(ac);
-                    sd[nt][e] = col_sum(ad);
-                }
-            const int buf = rnd & 1;
-            float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
-            float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
-            if (g == 0) {
+            for (int u = 0; u < 2; ++u) {
+                float a1 = 0.f, a2 = 0.f, ab = 0.f, ac = 0.f, ad = 0.f;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int t = 8 * nt + 2 * c4 + e;
-                        redX[w * kSS + t] = make_float4(s1[nt][e], s2[nt][e], sb[nt][e], sc[nt][e]);
-                        redY[w * kSS + t] = sd[nt][e];
+                        const float dv = yk[nt][2 * u + e] - shv[u];
+                        const float g2d = gg2[nt][e] * dv;
+                        a1 += dv;
+                        a2 = fmaf(dv, dv, a2);
+                        ab += g2d;
+                        ac = fmaf(g2d, dv, ac);
+                        ad = fmaf(gam[nt][e] * kv[nt][2 * u + e], dv, ad);
                     }
+                q[u][0] = a1;
+                q[u][1] = a2;
+                q[u][2] = ab;
+                q[u][3] = ac;
+                q[u][4] = ad;
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int k = 0; k < 5; ++k) {
+                    q[u][k] += __shfl_xor_sync(kFull, q[u][k], 1);
+                    q[u][k] += __shfl_xor_sync(kFull, q[u][k], 2);
+                }
+            const int buf = rnd & 1;
+            float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
+            float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
+            if (c4 == 0) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    redX[w * kSS + g + 8 * u] = make_float4(q[u][0], q[u][1], q[u][2], q[u][3]);
+                    redY[w * kSS + g + 8 * u] = q[u][4];
+                }
             }
             if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 1);
             named_bar_sync(kBarRed, MT * 32);
@@ -1145,12 +1180,12 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
                 float S1 = 0.f, S2 = 0.f, SB = 0.f, SC = 0.f, SD = 0.f;
 #pragma unroll
                 for (int u = 0; u < MT; ++u) {
-                    const float4 x = redX[u * kSS + tc];
+                    const float4 x = redX[u * kSS + tcomb];
                     S1 += x.x;
                     S2 += x.y;
                     SB += x.z;
                     SC += x.w;
-                    SD += redY[u * kSS + tc];
+                    SD += redY[u * kSS + tcomb];
                 }
                 const float ee = S1 * invD;
                 const float syy = fmaxf(fmaf(-ee, S1, S2), 0.f);
@@ -1165,65 +1200,61 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
             }
             float ad[2][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+            for (int u = 0; u < 2; ++u) {
+                const int src = g * 4 + u;  // lane (g, u) combined token g + 8u
+                const float mu = __shfl_sync(kFull, mu_c, src);
+                const float rs = __shfl_sync(kFull, rs_c, src);
+                const float M1 = __shfl_sync(kFull, M1_c, src);
+                const float M2 = __shfl_sync(kFull, M2_c, src);
+                const float LE = __shfl_sync(kFull, LE_c, src);
+                const bool in_m = NSUB == 1 || (g + 8 * u) / SUBB == m;
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = 8 * nt + 2 * c4 + e;
-                    const int src = (nt + 2 * e) * 4 + c4;
-                    const float mu = __shfl_sync(kFull, mu_c, src);
-                    const float rs = __shfl_sync(kFull, rs_c, src);
-                    const float M1 = __shfl_sync(kFull, M1_c, src);
-                    const float M2 = __shfl_sync(kFull, M2_c, src);
-                    const float LE = __shfl_sync(kFull, LE_c, src);
-                    const bool in_m = NSUB == 1 || t / SUBB == m;
+                for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const float yh = (yk[nt][e + 2 * u] - mu) * rs;
-                        const float E = fmaf(gam[u], yh, kv[nt][e + 2 * u]);
-                        const float G = rs * (2.f * gam[u] * E - M1 - yh * M2);
-                        const float a = round_h(escale[nt][e] * G);
-                        ad[nt][e + 2 * u] = in_m ? a : 0.f;
-                        if (in_m) at[nt][e + 2 * u] = a;
+                    for (int e = 0; e < 2; ++e) {
+                        const int r = 2 * u + e;
+                        const float yh = (yk[nt][r] - mu) * rs;
+                        const float E = fmaf(gam[nt][e], yh, kv[nt][r]);
+                        const float G = rs * (2.f * gam[nt][e] * E - M1 - yh * M2);
+                        const float a = round_h(escale[u] * G);
+                        ad[nt][r] = in_m ? a : 0.f;
+                        if (in_m) at[nt][r] = a;
                     }
-                    if (in_m) lin[nt][e] = LE;
-                }
+                if (in_m) lin[u] = LE;
+            }
             if (NSUB > 1 && m + 1 < NSUB) {
-                const uint4 gk = reinterpret_cast<const uint4 *>(stg + C::kOffGk)[lane];
-                const uint32_t adf[4] = {pack_h2(ad[0][0], ad[0][1]), pack_h2(ad[0][2], ad[0][3]),
-                                         pack_h2(ad[1][0], ad[1][1]), pack_h2(ad[1][2], ad[1][3])};
-                mma16816(yk[0], adf, gk.x, gk.y);
-                mma16816(yk[1], adf, gk.z, gk.w);
+                // Later mini-batches of this super-step see this one's update:
+                // Y[t][f] += sum_{s in mini-batch m} (k_s . k_t + 1) A~[f][s].
+                const uint4 gk = reinterpret_cast<const uint4 *>(stg + C::kOffGkA)[lane];
+                const uint32_t ga[4] = {gk.x, gk.y, gk.z, gk.w};
+                const uint32_t d00 = movm_t(pack_h2(ad[0][0], ad[0][1])), d01 = movm_t(pack_h2(ad[0][2], ad[0][3]));
+                const uint32_t d10 = movm_t(pack_h2(ad[1][0], ad[1][1])), d11 = movm_t(pack_h2(ad[1][2], ad[1][3]));
+                mma16816(yk[0], ga, d00, d01);
+                mma16816(yk[1], ga, d10, d11);
             }
         }
-        const uint32_t af[4] = {pack_h2(at[0][0], at[0][1]), pack_h2(at[0][2], at[0][3]),
-                                pack_h2(at[1][0], at[1][1]), pack_h2(at[1][2], at[1][3])};
+        // A~ in the T warps' layout (rows f, columns t): four 8x8 transposes.
+        const uint32_t af[4] = {movm_t(pack_h2(at[0][0], at[0][1])), movm_t(pack_h2(at[1][0], at[1][1])),
+                                movm_t(pack_h2(at[0][2], at[0][3])), movm_t(pack_h2(at[1][2], at[1][3]))};
         AR[((i & 1) * MT + w) * 32 + lane] = make_uint4(af[0], af[1], af[2], af[3]);
         named_bar_arrive(kBarA0 + (i & 1), kNAS);
         if (w == 0) TTT_TRACE_AT(p, i, 3);
-        if (p.inner_loss && w == 0 && g == 0) {
+        if (p.inner_loss && w == 0 && c4 == 0) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = i * kSS + 8 * nt + 2 * c4 + e;
-                    if (t < T) p.inner_loss[tok0 + t] = lin[nt][e];
-                }
+            for (int u = 0; u < 2; ++u) {
+                const int t = i * kSS + g + 8 * u;
+                if (t < T) p.inner_loss[tok0 + t] = lin[u];
+            }
         }
         warp_arrive(&R.empty[st], lane);
         if (has_next) {
-            // Y_{i+1}^T = S_{i+1} + A~_i (K_i K_{i+1}^T + 1)
+            // Y_{i+1} = S_{i+1} + (K_{i+1} K_i^T + 1) A~_i^T
             named_bar_sync(kBarS0 + ((i + 1) & 1), kNAS);
-            const uint4 kx = reinterpret_cast<const uint4 *>(stgn + C::kOffKx)[lane];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float4 v = SR[(((i + 1) & 1) * MT + w) * 64 + nt * 32 + lane];
-                yk[nt][0] = v.x;
-                yk[nt][1] = v.y;
-                yk[nt][2] = v.z;
-                yk[nt][3] = v.w;
-            }
-            mma16816(yk[0], af, kx.x, kx.y);
-            mma16816(yk[1], af, kx.z, kx.w);
+            load_s((i + 1) & 1);
+            const uint4 kx = reinterpret_cast<const uint4 *>(stgn + C::kOffKxA)[lane];
+            const uint32_t xa[4] = {kx.x, kx.y, kx.z, kx.w};
+            mma16816(yk[0], xa, af[0], af[2]);
+            mma16816(yk[1], xa, af[1], af[3]);
             if (w == 0) TTT_TRACE_AT(p, i, 4);
         }
     }
@@ -1252,7 +1283,7 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
     }
     float cb[2] = {c0[r0], c0[r1]};
     const int rt = (lane & 7) + ((lane >> 3) & 1) * 8, ct = lane >> 4;
-    float4 *SR = reinterpret_cast<float4 *>(sm + C::kOffSR);
+    float *SR = reinterpret_cast<float *>(sm + C::kOffSR);
     const uint4 *AR = reinterpret_cast<const uint4 *>(sm + C::kOffAR);
     auto wait_stage = [&](int k) {
         if (!wait_bar(&R.full[k % kStages], parity_of(k / kStages), R.flags) ||
@@ -1262,9 +1293,11 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
     auto publish_s = [&](int k) {  // S_k = W K_k^T + c (this warp's rows) -> the chain warps
         float acc[2][4];
         rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, k % kStages) + C::kOffKh), lane, acc);
-        float4 *dst = SR + ((k & 1) * MT + w) * 64;
-        dst[lane] = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-        dst[32 + lane] = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+        float *blk = SR + ((k & 1) * MT + w) * 16 * C::SRS;  // [t][f - 16w], the chain warps' order
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) blk[(8 * nt + 2 * c4 + (r & 1)) * C::SRS + g + 8 * (r >> 1)] = acc[nt][r];
         named_bar_arrive(kBarS0 + (k & 1), kNAS);
     };
     wait_stage(0);
