@@ -1,12 +1,33 @@
 // ttt_internal.h -- launch interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/ttt.h"
 
 namespace ttt {
+
+// Raise kernel Kern's dynamic shared-memory limit to `bytes` on the current
+// device unless an earlier call already did (the attribute lasts for the
+// process), so the per-call cost is one cudaGetDevice.
+template <auto Kern>
+cudaError_t ensure_smem(int bytes)
+{
+    static std::atomic<int> done[64];  // per device: the largest limit set so far
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) {
+        int cur = done[dev].load(std::memory_order_relaxed);
+        while (cur < bytes && !done[dev].compare_exchange_weak(cur, bytes, std::memory_order_acq_rel)) {
+        }
+    }
+    return e;
+}
 
 // Chain-level parameters shared by the TTT-Linear kernels (device pointers).
 struct LinearParams {

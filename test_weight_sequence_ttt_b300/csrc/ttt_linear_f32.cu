@@ -215,7 +215,7 @@ template <typename IO, typename ZT>
 cudaError_t launch_linear_f32_t(const LinearParams &p, int chains, cudaStream_t s)
 {
     const size_t smem = linear_f32_smem(p.d, p.mb);
-    cudaError_t e = cudaFuncSetAttribute(linear_f32_kernel<IO, ZT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem<linear_f32_kernel<IO, ZT>>((int)smem);
     if (e != cudaSuccess) return e;
     linear_f32_kernel<IO, ZT><<<chains, kThreads, smem, s>>>(p);
     return cudaGetLastError();

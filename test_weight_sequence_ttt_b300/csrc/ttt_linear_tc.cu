@@ -1239,6 +1239,7 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
         AR[((i & 1) * MT + w) * 32 + lane] = make_uint4(af[0], af[1], af[2], af[3]);
         named_bar_arrive(kBarA0 + (i & 1), kNAS);
         if (w == 0) TTT_TRACE_AT(p, i, 3);
+        warp_arrive(&R.empty[st], lane);  // before the global stores: a release need not wait for them
         if (p.inner_loss && w == 0 && c4 == 0) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -1246,7 +1247,6 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
                 if (t < T) p.inner_loss[tok0 + t] = lin[u];
             }
         }
-        warp_arrive(&R.empty[st], lane);
         if (has_next) {
             // Y_{i+1} = S_{i+1} + (K_{i+1} K_i^T + 1) A~_i^T
             named_bar_sync(kBarS0 + ((i + 1) & 1), kNAS);
@@ -1503,13 +1503,11 @@ cudaError_t launch_dsub(const LinearParams &p, int chains, cudaStream_t s)
         return cudaErrorInvalidValue;
     constexpr int smem = Cfg<D>::kSmemAlloc;
     if constexpr (D == 64 && SUBB <= kSS) {
-        cudaError_t e =
-            cudaFuncSetAttribute(linear_tc_split_kernel<D, SUBB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = ensure_smem<linear_tc_split_kernel<D, SUBB>>(smem);
         if (e != cudaSuccess) return e;
         linear_tc_split_kernel<D, SUBB><<<chains, Cfg<D>::kSplitThreads, smem, s>>>(mQ, mK, mV, p);
     } else {
-        cudaError_t e =
-            cudaFuncSetAttribute(linear_tc_kernel<D, SUBB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = ensure_smem<linear_tc_kernel<D, SUBB>>(smem);
         if (e != cudaSuccess) return e;
         linear_tc_kernel<D, SUBB><<<chains, Cfg<D>::kThreads, smem, s>>>(mQ, mK, mV, p);
     }

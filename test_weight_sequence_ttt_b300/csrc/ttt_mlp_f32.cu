@@ -289,7 +289,7 @@ template <typename IO, typename ZT>
 cudaError_t launch_mlp_f32_t(const MlpParams &p, int chains, cudaStream_t s)
 {
     const size_t smem = mlp_f32_floats(p.d, p.hidden, p.mb) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(mlp_f32_kernel<IO, ZT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem<mlp_f32_kernel<IO, ZT>>((int)smem);
     if (e != cudaSuccess) return e;
     mlp_f32_kernel<IO, ZT><<<chains, kThreads, smem, s>>>(p);
     return cudaGetLastError();

@@ -942,7 +942,7 @@ cudaError_t launch_mlp_tc(const MlpParams &p, int chains, cudaStream_t s)
     if (!make_map(&mQ, p.Q, kD, p.T, chains, 16) || !make_map(&mK, p.K, kD, p.T, chains, 16) ||
         !make_map(&mV, p.V, kD, p.T, chains, 16))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(mlp_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    cudaError_t e = ensure_smem<mlp_tc_kernel>(kSmemAlloc);
     if (e != cudaSuccess) return e;
     mlp_tc_kernel<<<chains, kThreads, kSmemAlloc, s>>>(mQ, mK, mV, p);
     return cudaGetLastError();
