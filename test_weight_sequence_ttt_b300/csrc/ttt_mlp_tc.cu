@@ -27,6 +27,14 @@
 //   Y (2)  warp y owns output features 32y..32y+31 and c2: Y, the LayerNorm
 //          forward/backward (both Y warps, through shared memory), G and
 //          Yq = X2q W2^T + c2 + A~2^T Mq2, handed to P.
+// Look-ahead. The recurrence of one step is A~1_i -> Z1 of step i+1 ->
+// gelu -> Y of step i+1 -> LayerNorm backward -> G -> A~1_{i+1}. Neither
+// weight update sits on it:
+//   Z1_{i+1}^T = (W1_{i-1} K_{i+1}^T + c1_{i-1}) + A~1_i (K_i K_{i+1}^T + 1)
+//   Y_{i+1}^T  = (W2_{i-1} X2_{i+1}^T + c2_{i-1}) + A~2_i (X2_i X2_{i+1}^T + 1)
+// (exact in real arithmetic), so the H warps apply W1 += A~1 K and the
+// tensor-memory W2 update while the Y warps already work on the next step;
+// three fp16 copies of W2 (W2_j in buffer j % 3) keep every reader's version.
 // H and Y hand activations over through shared memory with named barriers
 // (producer bar.arrive, consumer bar.sync). No warp leaves early: after a
 // failed wait a warp keeps running in step with the others (its results are
@@ -52,24 +60,28 @@ constexpr int kNY = 2;  // Y warps, 32 output features each
 constexpr int kWarpL = 0, kWarpP = 1, kWarpH = 2, kWarpY = kWarpH + kNH;
 constexpr int kWarps = kWarpY + kNY;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 // stage layout (bytes)
 constexpr int kTile = 32 * kD;
 constexpr int kOffK = 0, kOffQ = kTile, kOffV = 2 * kTile;  // bf16, as loaded
 constexpr int kOffKh = 3 * kTile, kOffQh = 4 * kTile;      // fp16 copies (same swizzled layout)
 constexpr int kOffMq = 5 * kTile;                          // causal q.k + 1, fp16 B fragments
-constexpr int kOffEta = kOffMq + 512;
+constexpr int kOffKx = kOffMq + 512;                       // k_{i-1}.k_i + 1, fp16 B fragments
+constexpr int kOffEta = kOffKx + 512;
 constexpr int kStageBytes = ((kOffEta + 64 + 1023) / 1024) * 1024;
 // fp16 activation / weight buffers, rows padded by 16 bytes (conflict-free ldmatrix)
 constexpr int kHS = kHid + 8;  // halves per row of a [*][hidden] buffer
 constexpr int kFS = kD + 8;    // halves per row of a [16][d] buffer
 constexpr int kOffStages = 0;
-constexpr int kOffW2h = kStages * kStageBytes;          // 2 x [d][kHS]: W2_{i-1} and W2_i
-constexpr int kOffX2k = kOffW2h + 2 * kD * kHS * 2;     // [16][kHS] gelu(Z1) of the keys
-constexpr int kOffX2q = kOffX2k + kB * kHS * 2;         // [16][kHS] gelu(Z1q)
-constexpr int kOffGh = kOffX2q + kB * kHS * 2;          // [16][kFS] G
-constexpr int kOffGt = kOffGh + kB * kFS * 2;           // [16][kFS] A~2 = -(eta/b) G
-constexpr int kOffRed = kOffGt + kB * kFS * 2;          // 2 bufs x [2 Y warps][16] float4
+constexpr int kW2hBytes = kD * kHS * 2;                  // one fp16 copy of W2, [d][kHS]
+constexpr int kOffW2h = kStages * kStageBytes;          // 3 copies: W2_j in buffer j % 3
+constexpr int kX2Bytes = kB * kHS * 2;                  // one [16][kHS] fp16 activation tile
+constexpr int kOffX2k = kOffW2h + 3 * kW2hBytes;        // 3 x gelu(Z1) of the keys, step j in j % 3
+constexpr int kOffX2q = kOffX2k + 3 * kX2Bytes;         // 2 x gelu(Z1q), step j in j & 1
+constexpr int kGBytes = kB * kFS * 2;
+constexpr int kOffGh = kOffX2q + 2 * kX2Bytes;          // 2 x [16][kFS] G, step j in j & 1
+constexpr int kOffGt = kOffGh + 2 * kGBytes;            // 2 x [16][kFS] A~2 = -(eta/b) G
+constexpr int kOffRed = kOffGt + 2 * kGBytes;           // 2 bufs x [2 Y warps][16] float4
 constexpr int kYS = kD + 4;                              // floats per row of the Yq hand-off
 constexpr int kOffYq = kOffRed + 2 * kNY * kB * 16;      // 2 slots x [16][kYS] fp32 Yq (Y -> P)
 constexpr int kOffMq2 = kOffYq + 2 * kB * kYS * 4;       // causal x2q.x2k + 1 fragments (P -> Y)
@@ -80,7 +92,7 @@ constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
 constexpr int kSmemAlloc = kSmem + 1024;
 constexpr uint32_t kTmemCols = 128;  // two H warps per lane quarter x 64 columns
 // named barriers: H <-> Y hand-offs (all 320 H and Y threads), Y-internal rounds
-constexpr int kBarX2k = 1, kBarG = 2, kBarX2q = 3, kBarYdone = 4, kBarW2 = 5, kBarYln = 6;
+constexpr int kBarX2k = 1, kBarG = 2, kBarX2q = 3 /* and 4, by step parity */, kBarYln = 5;
 constexpr int kHY = (kNH + kNY) * 32;
 constexpr float kGeluA = 0.7978845608028654f;  // sqrt(2/pi)
 constexpr float kGeluC = 0.044715f;
@@ -111,8 +123,9 @@ __device__ __forceinline__ float gelu1(float u)
 // ------------------------------------------------------------------ P: prep and output
 __device__ __forceinline__ uint32_t hb(uint32_t base, int row, int col, int stride);
 
-// Step i's input side: fp16 copies of the K/Q tiles and causal Q K^T + 1 fragments.
-__device__ __forceinline__ void prep_stage(uint8_t *stg, int lane, uint32_t &mag)
+// Step i's input side: fp16 copies of the K/Q tiles, causal Q K^T + 1
+// fragments and (i > 0) K_{i-1} K_i^T + 1 fragments for the Z1 look-ahead.
+__device__ __forceinline__ void prep_stage(uint8_t *stg, const uint8_t *stg_prev, int lane, uint32_t &mag)
 {
     const int g = lane >> 2, c4 = lane & 3;
     const int ra = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -132,7 +145,7 @@ __device__ __forceinline__ void prep_stage(uint8_t *stg, int lane, uint32_t &mag
     __syncwarp();
     // dq[j][r] = q_t . k_s with t = g + 8(r>>1), s = 8j + 2c4 + (r&1)
     const uint32_t sK = smem_u32(stg + kOffKh), sQ = smem_u32(stg + kOffQh);
-    float dq[2][4] = {};
+    float dq[2][4] = {}, dx[2][4] = {};  // dx[j][r] = k_t . k'_s, t in step i, s in step i-1
 #pragma unroll
     for (int ks = 0; ks < kD / 16; ++ks) {
         uint32_t aq[4], bk[4];
@@ -140,7 +153,18 @@ __device__ __forceinline__ void prep_stage(uint8_t *stg, int lane, uint32_t &mag
         ldsm_x4(bk, sK + swz(rb, 2 * ks + ((lane >> 3) & 1)));
         mma16816(dq[0], aq, bk[0], bk[1]);
         mma16816(dq[1], aq, bk[2], bk[3]);
+        if (stg_prev) {
+            uint32_t ak[4], bp[4];
+            ldsm_x4(ak, sK + swz(ra, 2 * ks + (lane >> 4)));
+            ldsm_x4(bp, smem_u32(stg_prev + kOffKh) + swz(rb, 2 * ks + ((lane >> 3) & 1)));
+            mma16816(dx[0], ak, bp[0], bp[1]);
+            mma16816(dx[1], ak, bp[2], bp[3]);
+        }
     }
+    if (stg_prev)  // B fragments (k = s of step i-1, n = t of step i)
+        reinterpret_cast<uint4 *>(stg + kOffKx)[lane] =
+            make_uint4(pack_h2(dx[0][0] + 1.f, dx[0][1] + 1.f), pack_h2(dx[1][0] + 1.f, dx[1][1] + 1.f),
+                       pack_h2(dx[0][2] + 1.f, dx[0][3] + 1.f), pack_h2(dx[1][2] + 1.f, dx[1][3] + 1.f));
     auto mq = [&](int j, int r) {
         const int t = g + 8 * (r >> 1), s = 8 * j + 2 * c4 + (r & 1);
         return s <= t ? dq[j][r] + 1.f : 0.f;
@@ -150,9 +174,10 @@ __device__ __forceinline__ void prep_stage(uint8_t *stg, int lane, uint32_t &mag
                    pack_h2(mq(1, 2), mq(1, 3)));
 }
 
-// P runs the input side one step ahead of the output side: iteration i preps
-// stage i, then finishes step i - 1 (the X2q X2k^T Gram for the Y warps, and
+// P runs the input side two steps ahead of the output side: iteration i preps
+// stage i, then finishes step i - 2 (the X2q X2k^T Gram for the Y warps, and
 // Z = Q + LN(Yq), L_t once the Y warps hand Yq over).
+constexpr int kPrepLead = 2;
 __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi, size_t tok0, int lane, int nsteps)
 {
     const int g = lane >> 2, c4 = lane & 3;
@@ -167,18 +192,18 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
     const uint32_t sX2k = smem_u32(sm + kOffX2k), sX2q = smem_u32(sm + kOffX2q);
     const float invD = 1.f / (float)kD, eps = p.eps;
     bool ok = true;
-    for (int i = 0; i <= nsteps && ok; ++i) {
+    for (int i = 0; i < nsteps + kPrepLead && ok; ++i) {
         if (i < nsteps) {
             const int st = i % kStages;
             if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
                 abort_chain(R.flags, p.status);
                 break;
             }
-            prep_stage(stage_ptr(sm, st), lane, mag);
+            prep_stage(stage_ptr(sm, st), i > 0 ? stage_ptr(sm, (i + kStages - 1) % kStages) : nullptr, lane, mag);
             warp_arrive(&R.prep[st], lane);
         }
-        if (i == 0) continue;
-        const int j = i - 1, stj = j % kStages, slot = j & 1;
+        if (i < kPrepLead) continue;
+        const int j = i - kPrepLead, stj = j % kStages, slot = j & 1;
         uint8_t *stg = stage_ptr(sm, stj);
         // Gram of step j: Mq2[s][t] = (s <= t)(x2q_t . x2k_s + 1) as B fragments (k = s, n = t).
         if (!wait_bar(R.hq, parity_of(j), R.flags)) {
@@ -188,15 +213,22 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
         {
             const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);
             const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);
-            float dq[2][4] = {};
-#pragma unroll 4
+            // four k-slices of independent accumulators (the mma latency, not its rate, bounds this)
+            float dq4[4][2][4] = {};
+            const uint32_t sQj = sX2q + (uint32_t)((j & 1) * kX2Bytes), sKj = sX2k + (uint32_t)((j % 3) * kX2Bytes);
+#pragma unroll
             for (int ks = 0; ks < kHid / 16; ++ks) {
                 uint32_t aq[4], bk[4];
-                ldsm_x4(aq, hb(sX2q, ra, 16 * ks + ca, kHS));
-                ldsm_x4(bk, hb(sX2k, rb, 16 * ks + cb, kHS));
-                mma16816(dq[0], aq, bk[0], bk[1]);
-                mma16816(dq[1], aq, bk[2], bk[3]);
+                ldsm_x4(aq, hb(sQj, ra, 16 * ks + ca, kHS));
+                ldsm_x4(bk, hb(sKj, rb, 16 * ks + cb, kHS));
+                mma16816(dq4[ks & 3][0], aq, bk[0], bk[1]);
+                mma16816(dq4[ks & 3][1], aq, bk[2], bk[3]);
             }
+            float dq[2][4];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) dq[jj][r] = (dq4[0][jj][r] + dq4[1][jj][r]) + (dq4[2][jj][r] + dq4[3][jj][r]);
             auto mq = [&](int jj, int r) {
                 const int t = g + 8 * (r >> 1), s = 8 * jj + 2 * c4 + (r & 1);
                 return s <= t ? dq[jj][r] + 1.f : 0.f;
@@ -280,7 +312,7 @@ __device__ __forceinline__ uint32_t hb(uint32_t base, int row, int col, int stri
 
 // H warps, before the main loop: W2 columns h0 + 8nt + 2c4 (+1) of rows
 // 16mf + g (+8) into this warp's tensor-memory columns (fp32 master) and into
-// fp16 buffer 1 (the copy step 0 reads as W2_{-1+1} = W2_0).
+// fp16 buffers 1 and 2 (the copies steps 0 and 1 read as W2_{-2}, W2_{-1}).
 __device__ void hidden_init_w2(const MlpParams &p, uint8_t *sm, int w, int warp, int bi, int hi, uint32_t tmem,
                                int lane)
 {
@@ -301,9 +333,12 @@ __device__ void hidden_init_w2(const MlpParams &p, uint8_t *sm, int w, int warp,
             v[idx >> 5][(idx & 31) + 1] = __float_as_uint(a.y);
             v[idx >> 5][(idx & 31) + 2] = __float_as_uint(b.x);
             v[idx >> 5][(idx & 31) + 3] = __float_as_uint(b.y);
-            uint8_t *w2 = sm + kOffW2h + kD * kHS * 2;
-            *reinterpret_cast<uint32_t *>(w2 + (f0 * kHS + hc) * 2) = pack_h2(a.x, a.y);
-            *reinterpret_cast<uint32_t *>(w2 + ((f0 + 8) * kHS + hc) * 2) = pack_h2(b.x, b.y);
+#pragma unroll
+            for (int buf = 1; buf <= 2; ++buf) {  // W2_{-2} = W2_{-1} = W2_0 (buffers 1 and 2)
+                uint8_t *w2 = sm + kOffW2h + buf * kW2hBytes;
+                *reinterpret_cast<uint32_t *>(w2 + (f0 * kHS + hc) * 2) = pack_h2(a.x, a.y);
+                *reinterpret_cast<uint32_t *>(w2 + ((f0 + 8) * kHS + hc) * 2) = pack_h2(b.x, b.y);
+            }
         }
     tmem_st32(taddr, v[0]);
     tmem_st32(taddr + 32, v[1]);
@@ -343,74 +378,107 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
     const int rb = (lane & 7) + (lane >> 4) * 8, cb16 = (lane >> 3) & 1;  // non-transposed B fragment rows
     const int rt = (lane & 7) + ((lane >> 3) & 1) * 8, ct = lane >> 4;   // transposed B fragment rows
     const int srow = (lane & 7) + 8 * (lane >> 4), scol = 8 * ((lane >> 3) & 1);  // stmatrix / trans-A rows
-    for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kStages;
-        uint8_t *stg = stage_ptr(sm, st);
-        if (w == 0) TTT_TRACE_AT(p, i, 0);
-        if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
-            !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags))
+    auto wait_stage = [&](int k) {
+        if (!wait_bar(&R.full[k % kStages], parity_of(k / kStages), R.flags) ||
+            !wait_bar(&R.prep[k % kStages], parity_of(k / kStages), R.flags))
             abort_chain(R.flags, p.status);  // keep going in step with the other warps
-        const uint32_t sK = smem_u32(stg + kOffKh), sQ = smem_u32(stg + kOffQh);
-        // Z1^T = W1 K^T + c1 and Rq1^T = W1 Q^T + c1 for this warp's 32 hidden units.
-        float z1[2][2][4], rq[2][2][4];
+    };
+    // acc = c1 + W1 tile^T for this warp's 32 hidden units, for one or two tiles at
+    // once (W1 packed to fp16 on the fly, once for both).
+    auto w1_gemm2 = [&](uint32_t tile0, float (&acc0)[2][2][4], uint32_t tile1, float (&acc1)[2][2][4],
+                        bool two) {
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) z1[m][n][r] = rq[m][n][r] = c1v[m][r >> 1];
+                for (int r = 0; r < 4; ++r) acc0[m][n][r] = acc1[m][n][r] = c1v[m][r >> 1];
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             uint32_t bk[4], bq[4];
-            ldsm_x4(bk, sK + swz(rb, 2 * ks + cb16));
-            ldsm_x4(bq, sQ + swz(rb, 2 * ks + cb16));
+            ldsm_x4(bk, tile0 + swz(rb, 2 * ks + cb16));
+            if (two) ldsm_x4(bq, tile1 + swz(rb, 2 * ks + cb16));
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 const uint32_t af[4] = {pack_h2(W1a[m][2 * ks][0], W1a[m][2 * ks][1]),
                                         pack_h2(W1a[m][2 * ks][2], W1a[m][2 * ks][3]),
                                         pack_h2(W1a[m][2 * ks + 1][0], W1a[m][2 * ks + 1][1]),
                                         pack_h2(W1a[m][2 * ks + 1][2], W1a[m][2 * ks + 1][3])};
-                mma16816(z1[m][0], af, bk[0], bk[1]);
-                mma16816(z1[m][1], af, bk[2], bk[3]);
-                mma16816(rq[m][0], af, bq[0], bq[1]);
-                mma16816(rq[m][1], af, bq[2], bq[3]);
+                mma16816(acc0[m][0], af, bk[0], bk[1]);
+                mma16816(acc0[m][1], af, bk[2], bk[3]);
+                if (two) {
+                    mma16816(acc1[m][0], af, bq[0], bq[1]);
+                    mma16816(acc1[m][1], af, bq[2], bq[3]);
+                }
             }
         }
-        // X2 = gelu(Z1) (kept in z1), gelu'(Z1) for the backward.
-        float gp[2][2][4];
+    };
+    // this warp's hidden columns of an activation tile [16 t][hidden] (fp16)
+    auto write_x = [&](uint32_t base, const float (&x)[2][2][4]) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+            stsm_x4_t(hb(base, srow, h0 + 16 * m + scol, kHS), pack_h2(x[m][0][0], x[m][0][1]),
+                      pack_h2(x[m][0][2], x[m][0][3]), pack_h2(x[m][1][0], x[m][1][1]),
+                      pack_h2(x[m][1][2], x[m][1][3]));
+    };
+    // Prologue: Z1_0 = W1_0 K_0^T + c1_0, Rq1_0, and S1_1 = W1_0 K_1^T + c1_0.
+    float z1[2][2][4], s1[2][2][4], rq[2][2][4];
+    __half2 gp[2][2][2];  // gelu'(Z1) of the next step, fp16 pairs (it only scales an fp16-rounded value)
+    auto gelu_x = [&](float (&x)[2][2][4]) {  // x <- gelu(x), gp <- gelu'(x)
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) gelu2(z1[m][n][r], z1[m][n][r], gp[m][n][r]);
-        if (w == 0) TTT_TRACE_AT(p, i, 1);
-        if (i > 0) named_bar_sync(kBarYdone, kHY);  // Y is done with X2k / X2q of step i-1
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-            stsm_x4_t(hb(sX2k, srow, h0 + 16 * m + scol, kHS), pack_h2(z1[m][0][0], z1[m][0][1]),
-                      pack_h2(z1[m][0][2], z1[m][0][3]), pack_h2(z1[m][1][0], z1[m][1][1]),
-                      pack_h2(z1[m][1][2], z1[m][1][3]));
+                for (int u = 0; u < 2; ++u) {
+                    float d0, d1;
+                    gelu2(x[m][n][2 * u], x[m][n][2 * u], d0);
+                    gelu2(x[m][n][2 * u + 1], x[m][n][2 * u + 1], d1);
+                    gp[m][n][u] = __floats2half2_rn(d0, d1);
+                }
+    };
+    if (nsteps > 0) {
+        wait_stage(0);
+        w1_gemm2(smem_u32(stage_ptr(sm, 0) + kOffKh), z1, smem_u32(stage_ptr(sm, 0) + kOffQh), rq, true);
+        gelu_x(z1);
+        write_x(sX2k, z1);
         named_bar_arrive(kBarX2k, kHY);
-        if (w == 0) TTT_TRACE_AT(p, i, 2);
-        named_bar_sync(kBarG, kHY);  // G and A~2 of step i are in shared memory
+    }
+    if (nsteps > 1) {
+        wait_stage(1);
+        w1_gemm2(smem_u32(stage_ptr(sm, 1) + kOffKh), s1, 0u, s1, false);
+    }
+    for (int i = 0; i < nsteps; ++i) {
+        const int st = i % kStages;
+        uint8_t *stg = stage_ptr(sm, st);
+        const uint32_t sK = smem_u32(stg + kOffKh);
+        if (w == 0) TTT_TRACE_AT(p, i, 0);
+        named_bar_sync(kBarG, kHY);  // G_i and A~2_i (slot i & 1) are in shared memory
         if (w == 0) TTT_TRACE_AT(p, i, 3);
-        // G1pre^T = W2^T G^T (W2_{i-1}, buffer (i+1)&1); A operand = W2 columns, transposed.
-        const uint32_t sW2p = sW2h + (uint32_t)(((i + 1) & 1) * kD * kHS * 2);
-        float gg[2][2][4] = {};
+        // G1pre^T = W2_{i-1}^T G_i^T (W2 columns of buffer (i+2) % 3, transposed as the A operand).
+        const uint32_t sW2p = sW2h + (uint32_t)(((i + 2) % 3) * kW2hBytes);
+        const uint32_t sG = sGh + (uint32_t)((i & 1) * kGBytes);
+        float gg[2][2][4] = {}, gg2[2][2][4] = {};  // even / odd k-steps: two independent chains each
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             uint32_t bg[4];
-            ldsm_x4(bg, hb(sGh, rb, 16 * ks + 8 * cb16, kFS));
+            ldsm_x4(bg, hb(sG, rb, 16 * ks + 8 * cb16, kFS));
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 uint32_t aw[4];
                 ldsm_x4_t(aw, hb(sW2p, 16 * ks + srow, h0 + 16 * m + scol, kHS));
-                mma16816(gg[m][0], aw, bg[0], bg[1]);
-                mma16816(gg[m][1], aw, bg[2], bg[3]);
+                mma16816(ks & 1 ? gg2[m][0] : gg[m][0], aw, bg[0], bg[1]);
+                mma16816(ks & 1 ? gg2[m][1] : gg[m][1], aw, bg[2], bg[3]);
             }
         }
-        // A~1 = -(eta/b) G1 with G1 = G1pre * gelu'(Z1), fp16 A fragments (rows h, columns t).
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) gg[m][n][r] += gg2[m][n][r];
+        if (w == 0) TTT_TRACE_AT(p, i, 2);
+        // A~1 = -(eta/b) G1 with G1 = G1pre * gelu'(Z1), fp16 A fragments (rows h, columns t); c1 += A~1 1.
         const float *se = reinterpret_cast<const float *>(stg + kOffEta);
         float es[2][2];
 #pragma unroll
@@ -419,22 +487,48 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             es[n][0] = -e2.x * (1.f / (float)kB);
             es[n][1] = -e2.y * (1.f / (float)kB);
         }
-        float a1[2][2][4];
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) a1[m][n][r] = round_h(es[n][r & 1] * gg[m][n][r] * gp[m][n][r]);
         uint32_t af1[2][4];
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-            af1[m][0] = pack_h2(a1[m][0][0], a1[m][0][1]);
-            af1[m][1] = pack_h2(a1[m][0][2], a1[m][0][3]);
-            af1[m][2] = pack_h2(a1[m][1][0], a1[m][1][1]);
-            af1[m][3] = pack_h2(a1[m][1][2], a1[m][1][3]);
+            float a[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const __half2 d = gp[m][n][r >> 1];
+                    a[n][r] = round_h(es[n][r & 1] * gg[m][n][r] * __half2float(r & 1 ? __high2half(d) : __low2half(d)));
+                }
+            af1[m][0] = pack_h2(a[0][0], a[0][1]);
+            af1[m][1] = pack_h2(a[0][2], a[0][3]);
+            af1[m][2] = pack_h2(a[1][0], a[1][1]);
+            af1[m][3] = pack_h2(a[1][2], a[1][3]);
+            float sr0 = a[0][0] + a[0][1] + a[1][0] + a[1][1];
+            float sr1 = a[0][2] + a[0][3] + a[1][2] + a[1][3];
+            sr0 += __shfl_xor_sync(kFull, sr0, 1);
+            sr0 += __shfl_xor_sync(kFull, sr0, 2);
+            sr1 += __shfl_xor_sync(kFull, sr1, 1);
+            sr1 += __shfl_xor_sync(kFull, sr1, 2);
+            c1v[m][0] += sr0;
+            c1v[m][1] += sr1;
         }
-        // Z1q^T = Rq1^T + A~1 Mq1 (in-batch prefix), X2q = gelu(Z1q) -> shared memory.
+        if (i + 1 < nsteps) {
+            // The chain: Z1_{i+1}^T = S1_{i+1} + A~1_i (K_i K_{i+1}^T + 1), X2k_{i+1} -> Y warps.
+            const uint4 kx = reinterpret_cast<const uint4 *>(stage_ptr(sm, (i + 1) % kStages) + kOffKx)[lane];
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) z1[m][n][r] = s1[m][n][r];
+                mma16816(z1[m][0], af1[m], kx.x, kx.y);
+                mma16816(z1[m][1], af1[m], kx.z, kx.w);
+            }
+            gelu_x(z1);
+            write_x(sX2k + (uint32_t)(((i + 1) % 3) * kX2Bytes), z1);
+            named_bar_arrive(kBarX2k, kHY);
+        }
+        if (w == 0) TTT_TRACE_AT(p, i, 1);
+        // Output side: Z1q_i^T = Rq1_i^T + A~1_i Mq1_i, X2q = gelu(Z1q) -> shared memory.
         {
             const uint4 mq = reinterpret_cast<const uint4 *>(stg + kOffMq)[lane];
 #pragma unroll
@@ -444,19 +538,16 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             }
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
+        for (int m = 0; m < 2; ++m)
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) rq[m][n][r] = gelu1(rq[m][n][r]);
-            stsm_x4_t(hb(sX2q, srow, h0 + 16 * m + scol, kHS), pack_h2(rq[m][0][0], rq[m][0][1]),
-                      pack_h2(rq[m][0][2], rq[m][0][3]), pack_h2(rq[m][1][0], rq[m][1][1]),
-                      pack_h2(rq[m][1][2], rq[m][1][3]));
-        }
-        named_bar_arrive(kBarX2q, kHY);
+        write_x(sX2q + (uint32_t)((i & 1) * kX2Bytes), rq);
+        named_bar_arrive(kBarX2q + (i & 1), kHY);  // also orders W2_{i-1} before the Y warps' Yq_i
         warp_arrive(R.hq, lane);
         if (w == 0) TTT_TRACE_AT(p, i, 4);
-        // W1 += A~1 K, c1 += A~1 1.
+        // W1_i = W1_{i-1} + A~1_i K_i.
 #pragma unroll
         for (int j = 0; j < kD / 16; ++j) {
             uint32_t bt[4];
@@ -467,56 +558,55 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
                 mma16816(W1a[m][2 * j + 1], af1[m], bt[2], bt[3]);
             }
         }
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            float s0 = a1[m][0][0] + a1[m][0][1] + a1[m][1][0] + a1[m][1][1];
-            float s1 = a1[m][0][2] + a1[m][0][3] + a1[m][1][2] + a1[m][1][3];
-            s0 += __shfl_xor_sync(kFull, s0, 1);
-            s0 += __shfl_xor_sync(kFull, s0, 2);
-            s1 += __shfl_xor_sync(kFull, s1, 1);
-            s1 += __shfl_xor_sync(kFull, s1, 2);
-            c1v[m][0] += s0;
-            c1v[m][1] += s1;
-        }
         if (w == 0) TTT_TRACE_AT(p, i, 5);
-        // W2 columns += A~2^T X2 (rows f, this warp's hidden columns); the fp32
-        // master goes through tensor memory, the fp16 copy to buffer i&1.
+        // W2_i = W2_{i-1} + A~2_i^T X2k_i (rows f, this warp's hidden columns): the fp32
+        // master goes through tensor memory (two halves of 32 columns: features 0-31,
+        // 32-63), the fp16 copy to buffer i % 3.
         {
-            uint32_t v[2][32];
-            tmem_ld32(taddr, v[0]);
-            tmem_ld32(taddr + 32, v[1]);
-            uint32_t bx[2][4];  // B = X2k (k = t, n = h), two pairs of n-tiles
+            uint32_t bx[2][4];  // B = X2k_i (k = t, n = h), two pairs of n-tiles
+            const uint32_t sXk = sX2k + (uint32_t)((i % 3) * kX2Bytes);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) ldsm_x4_t(bx[q], hb(sX2k, rt, h0 + 16 * q + 8 * ct, kHS));
-            tmem_wait_ld();
-            uint8_t *w2 = sm + kOffW2h + (i & 1) * kD * kHS * 2;
+            for (int q = 0; q < 2; ++q) ldsm_x4_t(bx[q], hb(sXk, rt, h0 + 16 * q + 8 * ct, kHS));
+            uint8_t *w2 = sm + kOffW2h + (i % 3) * kW2hBytes;
+            const uint32_t sGa = sGt + (uint32_t)((i & 1) * kGBytes);
 #pragma unroll
-            for (int mf = 0; mf < 4; ++mf) {
-                uint32_t ag[4];  // A = A~2 (rows f, columns t) from Gt[t][f], transposed
-                ldsm_x4_t(ag, hb(sGt, srow, 16 * mf + scol, kFS));
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v[32];
+                tmem_ld32(taddr + 32 * hf, v);
+                tmem_wait_ld();
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    const int idx = (mf * 4 + nt) * 4;
-                    uint32_t *vv = &v[idx >> 5][idx & 31];
-                    float acc[4] = {__uint_as_float(vv[0]), __uint_as_float(vv[1]), __uint_as_float(vv[2]),
-                                    __uint_as_float(vv[3])};
-                    mma16816(acc, ag, bx[nt >> 1][2 * (nt & 1)], bx[nt >> 1][2 * (nt & 1) + 1]);
+                for (int mh = 0; mh < 2; ++mh) {
+                    const int mf = 2 * hf + mh;
+                    uint32_t ag[4];  // A = A~2 (rows f, columns t) from Gt[t][f], transposed
+                    ldsm_x4_t(ag, hb(sGa, srow, 16 * mf + scol, kFS));
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) vv[r] = __float_as_uint(acc[r]);
-                    const int f0 = 16 * mf + g, hc = h0 + 8 * nt + 2 * c4;
-                    *reinterpret_cast<uint32_t *>(w2 + (f0 * kHS + hc) * 2) = pack_h2(acc[0], acc[1]);
-                    *reinterpret_cast<uint32_t *>(w2 + ((f0 + 8) * kHS + hc) * 2) = pack_h2(acc[2], acc[3]);
+                    for (int nt = 0; nt < 4; ++nt) {
+                        uint32_t *vv = &v[(mh * 4 + nt) * 4];
+                        float acc[4] = {__uint_as_float(vv[0]), __uint_as_float(vv[1]), __uint_as_float(vv[2]),
+                                        __uint_as_float(vv[3])};
+                        mma16816(acc, ag, bx[nt >> 1][2 * (nt & 1)], bx[nt >> 1][2 * (nt & 1) + 1]);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) vv[r] = __float_as_uint(acc[r]);
+                        const int f0 = 16 * mf + g, hc = h0 + 8 * nt + 2 * c4;
+                        *reinterpret_cast<uint32_t *>(w2 + (f0 * kHS + hc) * 2) = pack_h2(acc[0], acc[1]);
+                        *reinterpret_cast<uint32_t *>(w2 + ((f0 + 8) * kHS + hc) * 2) = pack_h2(acc[2], acc[3]);
+                    }
                 }
+                tmem_st32(taddr + 32 * hf, v);
+                tmem_wait_st();
             }
-            tmem_st32(taddr, v[0]);
-            tmem_st32(taddr + 32, v[1]);
-            tmem_wait_st();
         }
-        named_bar_arrive(kBarW2, kHY);
         if (w == 0) TTT_TRACE_AT(p, i, 6);
+        // Look-ahead products from W1_i: Rq1_{i+1} and S1_{i+2} (fp16 W1 packed once for both).
+        if (i + 1 < nsteps) {
+            const bool two = i + 2 < nsteps;
+            if (two) wait_stage(i + 2);
+            w1_gemm2(smem_u32(stage_ptr(sm, (i + 1) % kStages) + kOffQh), rq,
+                     smem_u32(stage_ptr(sm, (i + 2) % kStages) + kOffKh), s1, two);
+        }
+        if (w == 0) TTT_TRACE_AT(p, i, 7);
         warp_arrive(&R.empty[st], lane);
     }
-    if (nsteps > 0) named_bar_sync(kBarYdone, kHY);  // matches the Y warps' last arrival
     // Final state.
     bool bad = false;
     const size_t ch = (size_t)chain;
@@ -646,38 +736,53 @@ __device__ __forceinline__ void y_sum3(float (&a)[2][2], float (&b)[2][2], float
         }
 }
 
-// Y^T (rows f0..f0+31, 16 token columns) += W2 (fp16 buffer) X^T over all hidden units.
+// Y^T (rows f0..f0+31, 16 token columns) += W2 (fp16 buffer) X^T over all hidden
+// units; even and odd k-steps go to separate accumulators (8 independent chains).
 __device__ __forceinline__ void y_gemm(uint32_t sW2, uint32_t sX, int f0, int lane, float (&acc)[2][2][4])
 {
     const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);   // A rows (non-transposed)
     const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);   // B rows (non-transposed)
+    float acc2[2][2][4] = {};
 #pragma unroll 4
-    for (int ks = 0; ks < kHid / 16; ++ks) {
-        uint32_t bx[4];
-        ldsm_x4(bx, hb(sX, rb, 16 * ks + cb, kHS));
+    for (int ks = 0; ks < kHid / 16; ks += 2) {
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            uint32_t aw[4];
-            ldsm_x4(aw, hb(sW2, f0 + 16 * m + ra, 16 * ks + ca, kHS));
-            mma16816(acc[m][0], aw, bx[0], bx[1]);
-            mma16816(acc[m][1], aw, bx[2], bx[3]);
+        for (int u = 0; u < 2; ++u) {
+            uint32_t bx[4];
+            ldsm_x4(bx, hb(sX, rb, 16 * (ks + u) + cb, kHS));
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                uint32_t aw[4];
+                ldsm_x4(aw, hb(sW2, f0 + 16 * m + ra, 16 * (ks + u) + ca, kHS));
+                mma16816(u ? acc2[m][0] : acc[m][0], aw, bx[0], bx[1]);
+                mma16816(u ? acc2[m][1] : acc[m][1], aw, bx[2], bx[3]);
+            }
         }
     }
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[m][n][r] += acc2[m][n][r];
 }
 
+// Y warps. Iteration i first runs step i's part of the recurrence (Y from the
+// look-ahead, LayerNorm backward, G and A~2 to the H warps), then the output
+// product of step i - 1 (Yq = X2q W2^T + c2 + A~2 Mq2, handed to P), which is
+// off the recurrence and overlaps the H warps' work on step i.
 __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, int chain, int bi, int hi, size_t tok0,
                        int lane, int nsteps)
 {
     const int g = lane >> 2, c4 = lane & 3;
     const int f0 = 32 * y;  // first output feature of this warp
     const float *c20 = p.c2 + bi * p.c2_bstride + (long long)hi * kD;
-    float c2v[2][2], gam[2][2], bet[2][2];
+    float c2v[2][2], c2p[2][2], gam[2][2], bet[2][2];  // c2_{i-1} and c2_{i-2} at the top of iteration i
 #pragma unroll
     for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int f = f0 + 16 * m + g + 8 * u;
-            c2v[m][u] = c20[f];
+            c2v[m][u] = c2p[m][u] = c20[f];
             gam[m][u] = p.ln_g[hi * kD + f];
             bet[m][u] = p.ln_b[hi * kD + f];
         }
@@ -687,163 +792,210 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
     int rnd = 0;
     const int rbt = (lane & 7) + (lane >> 4) * 8, cbt = (lane >> 3) & 1;        // ldmatrix.trans of a tile
     const int srow = (lane & 7) + 8 * (lane >> 4), scol = 8 * ((lane >> 3) & 1);  // stmatrix rows
+    const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);     // A rows (non-transposed)
+    const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);     // B rows (non-transposed)
+    uint32_t a2f[2][4] = {};  // A~2_{i-1} as fp16 A fragments (rows f, columns t)
     const float eps = p.eps, invD = 1.f / (float)kD;
     const int T = p.T;
-    for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kStages;
-        uint8_t *stg = stage_ptr(sm, st);
-        if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
-            !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags))
-            abort_chain(R.flags, p.status);
-        // k - v + beta at this lane's (feature, token) positions: ldmatrix.trans of the bf16 tiles.
-        float kv[2][2][4];
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int chunk = 2 * (2 * y + m) + cbt;
-            uint32_t kr[4], vr[4];
-            ldsm_x4_t(kr, smem_u32(stg + kOffK) + swz(rbt, chunk));
-            ldsm_x4_t(vr, smem_u32(stg + kOffV) + swz(rbt, chunk));
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const uint32_t a = kr[2 * n + u], b = vr[2 * n + u];
-                    kv[m][n][2 * u] = bf16_bits_to_f32(a & 0xffffu) - bf16_bits_to_f32(b & 0xffffu) + bet[m][u];
-                    kv[m][n][2 * u + 1] = bf16_bits_to_f32(a >> 16) - bf16_bits_to_f32(b >> 16) + bet[m][u];
-                }
-        }
-        float es[2][2];
-        {
-            const float *se = reinterpret_cast<const float *>(stg + kOffEta);
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                const float2 e2 = *reinterpret_cast<const float2 *>(se + 8 * n + 2 * c4);
-                es[n][0] = -e2.x * (1.f / (float)kB);
-                es[n][1] = -e2.y * (1.f / (float)kB);
-            }
-        }
-        if (y == 0) TTT_TRACE_AT(p, i, 8);
-        if (i > 0) named_bar_sync(kBarW2, kHY);  // W2_{i-1} copy complete
-        const uint32_t sW2p = sW2h + (uint32_t)(((i + 1) & 1) * kD * kHS * 2);
-        named_bar_sync(kBarX2k, kHY);
-        if (y == 0) TTT_TRACE_AT(p, i, 9);
-        // Y^T = W2_{i-1} X2k^T + c2
-        float yk[2][2][4];
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) yk[m][n][r] = c2v[m][r >> 1];
-        y_gemm(sW2p, sX2k, f0, lane, yk);
-        if (y == 0) TTT_TRACE_AT(p, i, 10);
-        // LayerNorm forward + backward: G = dl/dY, inner loss.
-        float mu[2][2], rs[2][2];
-        y_ln_stats(yk, red, rnd, y, g, c4, eps, mu, rs);
-        float s1[2][2] = {}, s2[2][2] = {}, sl[2][2] = {};
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int e = r & 1, u = r >> 1;
-                    const float yh = (yk[m][n][r] - mu[n][e]) * rs[n][e];
-                    const float E = fmaf(gam[m][u], yh, kv[m][n][r]);
-                    const float dh = 2.f * gam[m][u] * E;
-                    s1[n][e] += dh;
-                    s2[n][e] = fmaf(dh, yh, s2[n][e]);
-                    sl[n][e] = fmaf(E, E, sl[n][e]);
-                }
-        y_sum3(s1, s2, sl, red, rnd, y, g, c4);
-        float gh[2][2][4], a2[2][2][4];
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int e = r & 1, u = r >> 1;
-                    const float yh = (yk[m][n][r] - mu[n][e]) * rs[n][e];
-                    const float E = fmaf(gam[m][u], yh, kv[m][n][r]);
-                    const float G = rs[n][e] * (2.f * gam[m][u] * E - s1[n][e] * invD - yh * s2[n][e] * invD);
-                    gh[m][n][r] = G;
-                    a2[m][n][r] = round_h(es[n][e] * G);
-                }
-        if (p.inner_loss && y == 0 && g == 0) {
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = i * kB + 8 * n + 2 * c4 + e;
-                    if (t < T) p.inner_loss[tok0 + t] = sl[n][e];
-                }
-        }
-        // G and A~2 to shared memory as [t][f] (the H warps' operands).
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            stsm_x4_t(hb(sGh, srow, f0 + 16 * m + scol, kFS), pack_h2(gh[m][0][0], gh[m][0][1]),
-                      pack_h2(gh[m][0][2], gh[m][0][3]), pack_h2(gh[m][1][0], gh[m][1][1]),
-                      pack_h2(gh[m][1][2], gh[m][1][3]));
-            stsm_x4_t(hb(sGt, srow, f0 + 16 * m + scol, kFS), pack_h2(a2[m][0][0], a2[m][0][1]),
-                      pack_h2(a2[m][0][2], a2[m][0][3]), pack_h2(a2[m][1][0], a2[m][1][1]),
-                      pack_h2(a2[m][1][2], a2[m][1][3]));
-        }
-        named_bar_arrive(kBarG, kHY);
-        if (y == 0) TTT_TRACE_AT(p, i, 11);
-        float c2o[2][2];
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            float s0 = a2[m][0][0] + a2[m][0][1] + a2[m][1][0] + a2[m][1][1];
-            float s1r = a2[m][0][2] + a2[m][0][3] + a2[m][1][2] + a2[m][1][3];
-            s0 += __shfl_xor_sync(kFull, s0, 1);
-            s0 += __shfl_xor_sync(kFull, s0, 2);
-            s1r += __shfl_xor_sync(kFull, s1r, 1);
-            s1r += __shfl_xor_sync(kFull, s1r, 2);
-            c2o[m][0] = c2v[m][0];
-            c2o[m][1] = c2v[m][1];
-            c2v[m][0] += s0;
-            c2v[m][1] += s1r;
-        }
-        named_bar_sync(kBarX2q, kHY);
-        if (y == 0) TTT_TRACE_AT(p, i, 12);
-        // Yq^T = W2_{i-1} X2q^T + c2 + A~2 Mq2, Mq2 (causal x2q.x2k + 1) from P.
-        float yq[2][2][4];
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) yq[m][n][r] = c2o[m][r >> 1];
-        y_gemm(sW2p, sX2q, f0, lane, yq);
-        if (!wait_bar(R.mq2, parity_of(i), R.flags)) abort_chain(R.flags, p.status);
-        {
-            const uint4 mq2 = reinterpret_cast<const uint4 *>(sm + kOffMq2)[lane];
+    for (int i = 0; i <= nsteps; ++i) {
+        uint32_t a2n[2][4];
+        float c2n[2][2];
+        if (i < nsteps) {
+            const int st = i % kStages;
+            uint8_t *stg = stage_ptr(sm, st);
+            if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
+                !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags))
+                abort_chain(R.flags, p.status);
+            // k - v + beta at this lane's (feature, token) positions: ldmatrix.trans of the bf16 tiles.
+            float kv[2][2][4];
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
-                const uint32_t af[4] = {pack_h2(a2[m][0][0], a2[m][0][1]), pack_h2(a2[m][0][2], a2[m][0][3]),
-                                        pack_h2(a2[m][1][0], a2[m][1][1]), pack_h2(a2[m][1][2], a2[m][1][3])};
-                mma16816(yq[m][0], af, mq2.x, mq2.y);
-                mma16816(yq[m][1], af, mq2.z, mq2.w);
+                const int chunk = 2 * (2 * y + m) + cbt;
+                uint32_t kr[4], vr[4];
+                ldsm_x4_t(kr, smem_u32(stg + kOffK) + swz(rbt, chunk));
+                ldsm_x4_t(vr, smem_u32(stg + kOffV) + swz(rbt, chunk));
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t a = kr[2 * n + u], b = vr[2 * n + u];
+                        kv[m][n][2 * u] = bf16_bits_to_f32(a & 0xffffu) - bf16_bits_to_f32(b & 0xffffu) + bet[m][u];
+                        kv[m][n][2 * u + 1] = bf16_bits_to_f32(a >> 16) - bf16_bits_to_f32(b >> 16) + bet[m][u];
+                    }
+            }
+            float es[2][2];
+            {
+                const float *se = reinterpret_cast<const float *>(stg + kOffEta);
+#pragma unroll
+                for (int n = 0; n < 2; ++n) {
+                    const float2 e2 = *reinterpret_cast<const float2 *>(se + 8 * n + 2 * c4);
+                    es[n][0] = -e2.x * (1.f / (float)kB);
+                    es[n][1] = -e2.y * (1.f / (float)kB);
+                }
+            }
+            if (y == 0) TTT_TRACE_AT(p, i, 8);
+            named_bar_sync(kBarX2k, kHY);  // X2k_i written (and with it every W2 update up to step i-2)
+            if (y == 0) TTT_TRACE_AT(p, i, 9);
+            // Y^T = W2_{i-1} X2k^T + c2_{i-1}, read as W2_{i-2} X2k^T + c2_{i-1} + A~2_{i-1} (X2k_{i-1} X2k^T)
+            // so that the W2 update of step i-1 is off this path.
+            const uint32_t sXk = sX2k + (uint32_t)((i % 3) * kX2Bytes);
+            float yk[2][2][4];
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) yk[m][n][r] = c2v[m][r >> 1];
+            y_gemm(sW2h + (uint32_t)(((i + 1) % 3) * kW2hBytes), sXk, f0, lane, yk);
+            if (i > 0) {
+                // dx[j][r] = x2_t . x2'_s, t in step i (rows), s in step i-1; four k-slices
+                const uint32_t sXp = sX2k + (uint32_t)(((i + 2) % 3) * kX2Bytes);
+                float dx4[4][2][4] = {};
+#pragma unroll
+                for (int ks = 0; ks < kHid / 16; ++ks) {
+                    uint32_t ax[4], bp[4];
+                    ldsm_x4(ax, hb(sXk, ra, 16 * ks + ca, kHS));
+                    ldsm_x4(bp, hb(sXp, rb, 16 * ks + cb, kHS));
+                    mma16816(dx4[ks & 3][0], ax, bp[0], bp[1]);
+                    mma16816(dx4[ks & 3][1], ax, bp[2], bp[3]);
+                }
+                float dx[2][4];
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        dx[jj][r] = (dx4[0][jj][r] + dx4[1][jj][r]) + (dx4[2][jj][r] + dx4[3][jj][r]);
+                const uint32_t bx[4] = {pack_h2(dx[0][0], dx[0][1]), pack_h2(dx[1][0], dx[1][1]),
+                                        pack_h2(dx[0][2], dx[0][3]), pack_h2(dx[1][2], dx[1][3])};
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    mma16816(yk[m][0], a2f[m], bx[0], bx[1]);
+                    mma16816(yk[m][1], a2f[m], bx[2], bx[3]);
+                }
+            }
+            if (y == 0) TTT_TRACE_AT(p, i, 10);
+            // LayerNorm forward + backward: G = dl/dY, inner loss.
+            float mu[2][2], rs[2][2];
+            y_ln_stats(yk, red, rnd, y, g, c4, eps, mu, rs);
+            float s1[2][2] = {}, s2[2][2] = {}, sl[2][2] = {};
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int e = r & 1, u = r >> 1;
+                        const float yh = (yk[m][n][r] - mu[n][e]) * rs[n][e];
+                        const float E = fmaf(gam[m][u], yh, kv[m][n][r]);
+                        const float dh = 2.f * gam[m][u] * E;
+                        s1[n][e] += dh;
+                        s2[n][e] = fmaf(dh, yh, s2[n][e]);
+                        sl[n][e] = fmaf(E, E, sl[n][e]);
+                    }
+            y_sum3(s1, s2, sl, red, rnd, y, g, c4);
+            float gh[2][2][4], a2[2][2][4];
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int e = r & 1, u = r >> 1;
+                        const float yh = (yk[m][n][r] - mu[n][e]) * rs[n][e];
+                        const float E = fmaf(gam[m][u], yh, kv[m][n][r]);
+                        const float G = rs[n][e] * (2.f * gam[m][u] * E - s1[n][e] * invD - yh * s2[n][e] * invD);
+                        gh[m][n][r] = G;
+                        a2[m][n][r] = round_h(es[n][e] * G);
+                    }
+            // G and A~2 to shared memory as [t][f] (the H warps' operands), slot i & 1.
+            const uint32_t sG = sGh + (uint32_t)((i & 1) * kGBytes), sA = sGt + (uint32_t)((i & 1) * kGBytes);
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                stsm_x4_t(hb(sG, srow, f0 + 16 * m + scol, kFS), pack_h2(gh[m][0][0], gh[m][0][1]),
+                          pack_h2(gh[m][0][2], gh[m][0][3]), pack_h2(gh[m][1][0], gh[m][1][1]),
+                          pack_h2(gh[m][1][2], gh[m][1][3]));
+                stsm_x4_t(hb(sA, srow, f0 + 16 * m + scol, kFS), pack_h2(a2[m][0][0], a2[m][0][1]),
+                          pack_h2(a2[m][0][2], a2[m][0][3]), pack_h2(a2[m][1][0], a2[m][1][1]),
+                          pack_h2(a2[m][1][2], a2[m][1][3]));
+            }
+            named_bar_arrive(kBarG, kHY);
+            if (y == 0) TTT_TRACE_AT(p, i, 11);
+            if (p.inner_loss && y == 0 && g == 0) {
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = i * kB + 8 * n + 2 * c4 + e;
+                        if (t < T) p.inner_loss[tok0 + t] = sl[n][e];
+                    }
+            }
+            // c2_i = c2_{i-1} + A~2_i 1, and A~2_i as A fragments for the next step.
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                float s0 = a2[m][0][0] + a2[m][0][1] + a2[m][1][0] + a2[m][1][1];
+                float s1r = a2[m][0][2] + a2[m][0][3] + a2[m][1][2] + a2[m][1][3];
+                s0 += __shfl_xor_sync(kFull, s0, 1);
+                s0 += __shfl_xor_sync(kFull, s0, 2);
+                s1r += __shfl_xor_sync(kFull, s1r, 1);
+                s1r += __shfl_xor_sync(kFull, s1r, 2);
+                c2n[m][0] = c2v[m][0] + s0;
+                c2n[m][1] = c2v[m][1] + s1r;
+                a2n[m][0] = pack_h2(a2[m][0][0], a2[m][0][1]);
+                a2n[m][1] = pack_h2(a2[m][0][2], a2[m][0][3]);
+                a2n[m][2] = pack_h2(a2[m][1][0], a2[m][1][1]);
+                a2n[m][3] = pack_h2(a2[m][1][2], a2[m][1][3]);
+            }
+            warp_arrive(&R.empty[st], lane);
+        }
+        if (i > 0) {
+            // Output of step j = i - 1: Yq^T = W2_{j-1} X2q^T + c2_{j-1} + A~2_j Mq2, Mq2 (causal x2q.x2k + 1) from P.
+            const int j = i - 1;
+            named_bar_sync(kBarX2q + (j & 1), kHY);  // X2q_j written (and W2_{j-1} before it)
+            if (y == 0) TTT_TRACE_AT(p, j, 12);
+            float yq[2][2][4];
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) yq[m][n][r] = c2p[m][r >> 1];
+            y_gemm(sW2h + (uint32_t)(((j + 2) % 3) * kW2hBytes), sX2q + (uint32_t)((j & 1) * kX2Bytes), f0, lane, yq);
+            if (!wait_bar(R.mq2, parity_of(j), R.flags)) abort_chain(R.flags, p.status);
+            {
+                const uint4 mq2 = reinterpret_cast<const uint4 *>(sm + kOffMq2)[lane];
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    mma16816(yq[m][0], a2f[m], mq2.x, mq2.y);
+                    mma16816(yq[m][1], a2f[m], mq2.z, mq2.w);
+                }
+            }
+            if (y == 0) TTT_TRACE_AT(p, j, 13);
+            const int slot = j & 1;
+            if (!wait_bar(&R.yqempty[slot], parity_of(j >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
+            float *ys = reinterpret_cast<float *>(sm + kOffYq) + slot * kB * kYS;
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        ys[(8 * n + 2 * c4 + (r & 1)) * kYS + f0 + 16 * m + g + 8 * (r >> 1)] = yq[m][n][r];
+            warp_arrive(&R.yqfull[slot], lane);
+            if (y == 0) TTT_TRACE_AT(p, j, 14);
+        }
+        if (i < nsteps) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    c2p[m][u] = c2v[m][u];
+                    c2v[m][u] = c2n[m][u];
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) a2f[m][q] = a2n[m][q];
             }
         }
-        named_bar_arrive(kBarYdone, kHY);  // X2k, X2q and the Gram fragments of step i are consumed
-        if (y == 0) TTT_TRACE_AT(p, i, 13);
-        const int slot = i & 1;
-        if (!wait_bar(&R.yqempty[slot], parity_of(i >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
-        float *ys = reinterpret_cast<float *>(sm + kOffYq) + slot * kB * kYS;
-#pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    ys[(8 * n + 2 * c4 + (r & 1)) * kYS + f0 + 16 * m + g + 8 * (r >> 1)] = yq[m][n][r];
-        warp_arrive(&R.yqfull[slot], lane);
-        if (y == 0) TTT_TRACE_AT(p, i, 14);
-        warp_arrive(&R.empty[st], lane);
     }
-    if (nsteps > 0) named_bar_sync(kBarW2, kHY);  // matches the H warps' last arrival
     bool bad = false;
 #pragma unroll
     for (int m = 0; m < 2; ++m)
