@@ -21,6 +21,11 @@ learning rates eta (b) and anchor (W, c) = (W_{i-1}, c_{i-1}):
 For TTT-MLP the same holds per layer: layer 1 sees the keys/queries, layer 2
 sees the GELU activations X2 of keys (anchor weights) and queries (prefix
 weights).
+
+Output rules: "prefix" is the form above. "anchor" (every prediction of a
+mini-batch made with the weights before it, review section 2.3) drops A:
+Yq = Q W^T + 1 c^T. "key" (the review's simplified output rule, Eq. 9) is the
+anchor rule with the keys as queries, so Yq = Y and Z - V = E.
 """
 from __future__ import annotations
 
@@ -75,7 +80,14 @@ def _broadcast_init(a, B):
     return np.broadcast_to(a, (B,) + a.shape[1:]) if a.shape[0] == 1 else a
 
 
-def ttt_linear_dual(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True):
+def _queries(Q, K, rule):
+    if rule not in ("prefix", "anchor", "key"):
+        raise ValueError(rule)
+    return K if rule == "key" else Q
+
+
+def ttt_linear_dual(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, rule="prefix"):
+    Q = _queries(Q, K, rule)
     Q, K, V, eta = (np.asarray(a, np.float64) for a in (Q, K, V, eta))
     B, H, T, d = Q.shape
     W0 = _broadcast_init(W0, B)
@@ -85,7 +97,7 @@ def ttt_linear_dual(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=Tru
     cf = np.empty((B, H, d))
     loss = np.empty((B, H, T))
     inner = np.empty((B, H, T))
-    mask = np.tril(np.ones((b, b)))
+    mask = np.tril(np.ones((b, b))) if rule == "prefix" else np.zeros((b, b))
     for bi in range(B):
         for hi in range(H):
             W = W0[bi, hi].copy()
@@ -108,7 +120,8 @@ def ttt_linear_dual(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=Tru
     return dict(Z=Z, W=Wf, c=cf, loss=loss, inner_loss=inner)
 
 
-def ttt_mlp_dual(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_res=True):
+def ttt_mlp_dual(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, rule="prefix"):
+    Q = _queries(Q, K, rule)
     Q, K, V, eta = (np.asarray(a, np.float64) for a in (Q, K, V, eta))
     B, H, T, d = Q.shape
     W1, c1, W2, c2 = (_broadcast_init(a, B) for a in (W1, c1, W2, c2))
@@ -118,7 +131,7 @@ def ttt_mlp_dual(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_re
                W2=np.empty((B, H, d, h)), c2=np.empty((B, H, d)))
     loss = np.empty((B, H, T))
     inner = np.empty((B, H, T))
-    mask = np.tril(np.ones((b, b)))
+    mask = np.tril(np.ones((b, b))) if rule == "prefix" else np.zeros((b, b))
     for bi in range(B):
         for hi in range(H):
             w1, b1 = W1[bi, hi].copy(), c1[bi, hi].copy()

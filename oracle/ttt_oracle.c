@@ -35,6 +35,15 @@
  *   - The loss is the squared L2 sum (no 1/d).
  *   - GELU is the tanh form.
  *
+ * Output rules (argument `rule`; the weight trajectory does not depend on it):
+ *   0  prefix: z_t = f(q_t; W_t), the in-batch prefix above ([TTT-survey] Eq. 5).
+ *   1  anchor: z_t = f(q_t; W_{i-1}) for every token of batch i: [E2E-review]
+ *      section 2.3, where every prediction of a mini-batch is made with the
+ *      weights before it.
+ *   2  key: z_t = f(k_t; W_{i-1}): the simplified output rule of [E2E-review]
+ *      section 2.4.2, Eq. 9 (the inner loss's own prediction is the output; its
+ *      W_{t-1} is the anchor under mini-batch updates, and exactly W_{t-1} at b = 1).
+ *
  * Everything is double precision, plain loops, one (sequence, head) chain at a
  * time; chains are independent and run on OpenMP threads.
  *
@@ -212,7 +221,7 @@ double oracle_mlp_token_grad(int d, int h, int ln_res, const double *W1, const d
 /* ------------------------------------------------------------------ */
 /* TTT-Linear inner loop, primal token form.                            */
 /* ------------------------------------------------------------------ */
-static void linear_chain(int T, int d, int b, int ln_res, const double *Q, const double *K,
+static void linear_chain(int T, int d, int b, int ln_res, int rule, const double *Q, const double *K,
                          const double *V, const double *eta, const double *W0,
                          const double *c0, const double *lg, const double *lb, double eps,
                          double *Z, double *W_out, double *c_out, double *loss,
@@ -245,9 +254,13 @@ static void linear_chain(int T, int d, int b, int ln_res, const double *Q, const
                 for (int j = 0; j < d; ++j) W[(size_t)r * d + j] -= s * g[r] * k[j];
                 c[r] -= s * g[r];
             }
-            /* Eq. 5: z_t = f(q_t; W_t). */
-            affine(d, d, W, c, q, y);
-            output_rule(d, ln_res, q, y, lg, lb, eps, z, work);
+            /* Output: Eq. 5 z_t = f(q_t; W_t), or f(q_t; W_{i-1}) / f(k_t; W_{i-1}). */
+            const double *x = rule == 2 ? k : q;
+            if (rule == 0)
+                affine(d, d, W, c, x, y);
+            else
+                affine(d, d, Wa, ca, x, y);
+            output_rule(d, ln_res, x, y, lg, lb, eps, z, work);
             double L = 0.0;
             for (int j = 0; j < d; ++j) {
                 Z[(size_t)(t0 + t) * d + j] = z[j];
@@ -262,7 +275,7 @@ static void linear_chain(int T, int d, int b, int ln_res, const double *Q, const
     free(W);
 }
 
-void oracle_ttt_linear(int B, int H, int T, int d, int b, int ln_res, const double *Q,
+void oracle_ttt_linear(int B, int H, int T, int d, int b, int ln_res, int rule, const double *Q,
                        const double *K, const double *V, const double *eta, const double *W0,
                        const double *c0, long w0_bstride, long c0_bstride, const double *ln_g,
                        const double *ln_b, double eps, double *Z, double *W_out, double *c_out,
@@ -276,7 +289,7 @@ void oracle_ttt_linear(int B, int H, int T, int d, int b, int ln_res, const doub
     for (long ch = 0; ch < chains; ++ch) {
         const long bi = ch / H, hi = ch % H;
         const size_t tok = (size_t)ch * T;
-        linear_chain(T, d, b, ln_res, Q + tok * d, K + tok * d, V + tok * d, eta + tok,
+        linear_chain(T, d, b, ln_res, rule, Q + tok * d, K + tok * d, V + tok * d, eta + tok,
                      W0 + bi * w0_bstride + hi * (size_t)d * d, c0 + bi * c0_bstride + hi * (size_t)d,
                      ln_g + hi * (size_t)d, ln_b + hi * (size_t)d, eps, Z + tok * d,
                      W_out ? W_out + (size_t)ch * d * d : NULL, c_out ? c_out + (size_t)ch * d : NULL,
@@ -288,7 +301,7 @@ void oracle_ttt_linear(int B, int H, int T, int d, int b, int ln_res, const doub
 /* TTT-MLP inner loop, primal token form.                               */
 /* f_res(x) = W2 gelu(W1 x + c1) + c2, W1 [h][d], W2 [d][h].            */
 /* ------------------------------------------------------------------ */
-static void mlp_chain(int T, int d, int h, int b, int ln_res, const double *Q, const double *K,
+static void mlp_chain(int T, int d, int h, int b, int ln_res, int rule, const double *Q, const double *K,
                       const double *V, const double *eta, const double *W10, const double *c10,
                       const double *W20, const double *c20, const double *lg, const double *lb,
                       double eps, double *Z, double *W1o, double *c1o, double *W2o, double *c2o,
@@ -341,10 +354,12 @@ static void mlp_chain(int T, int d, int h, int b, int ln_res, const double *Q, c
                 for (int r = 0; r < d; ++r) W1[(size_t)j * d + r] -= s * dz[j] * k[r];
                 c1[j] -= s * dz[j];
             }
-            affine(h, d, W1, c1, q, z1);
+            /* Output at W_t (prefix rule) or at the anchor (anchor and key rules). */
+            const double *x = rule == 2 ? k : q;
+            affine(h, d, rule == 0 ? W1 : W1a, rule == 0 ? c1 : c1a, x, z1);
             for (int j = 0; j < h; ++j) x2[j] = gelu(z1[j]);
-            affine(d, h, W2, c2, x2, y);
-            output_rule(d, ln_res, q, y, lg, lb, eps, z, work);
+            affine(d, h, rule == 0 ? W2 : W2a, rule == 0 ? c2 : c2a, x2, y);
+            output_rule(d, ln_res, x, y, lg, lb, eps, z, work);
             double L = 0.0;
             for (int j = 0; j < d; ++j) {
                 Z[(size_t)(t0 + t) * d + j] = z[j];
@@ -361,7 +376,7 @@ static void mlp_chain(int T, int d, int h, int b, int ln_res, const double *Q, c
     free(W1);
 }
 
-void oracle_ttt_mlp(int B, int H, int T, int d, int h, int b, int ln_res, const double *Q,
+void oracle_ttt_mlp(int B, int H, int T, int d, int h, int b, int ln_res, int rule, const double *Q,
                     const double *K, const double *V, const double *eta, const double *W10,
                     const double *c10, const double *W20, const double *c20, long w_bstride,
                     long c1_bstride, long c2_bstride, const double *ln_g, const double *ln_b,
@@ -377,7 +392,7 @@ void oracle_ttt_mlp(int B, int H, int T, int d, int h, int b, int ln_res, const 
     for (long ch = 0; ch < chains; ++ch) {
         const long bi = ch / H, hi = ch % H;
         const size_t tok = (size_t)ch * T;
-        mlp_chain(T, d, h, b, ln_res, Q + tok * d, K + tok * d, V + tok * d, eta + tok,
+        mlp_chain(T, d, h, b, ln_res, rule, Q + tok * d, K + tok * d, V + tok * d, eta + tok,
                   W10 + bi * w_bstride + hi * hd, c10 + bi * c1_bstride + hi * (size_t)h,
                   W20 + bi * w_bstride + hi * hd, c20 + bi * c2_bstride + hi * (size_t)d,
                   ln_g + hi * (size_t)d, ln_b + hi * (size_t)d, eps, Z + tok * d,

@@ -381,3 +381,106 @@ def test_rejects_ragged_T():
     args = _rand_linear(rng, T=30)
     with pytest.raises(ValueError):
         oracle.ttt_linear(*args, b=4)
+
+
+# ---------------------------------------------------------------- output rules
+# The anchor rule (every prediction of mini-batch i made with W_{i-1}, the E2E
+# review's section 2.3) and the key rule (the review's simplified output rule,
+# Eq. 9: z_t = f(k_t; W_{i-1})) change only the output. Pins: the weight
+# trajectory and inner loss are bit-identical under every rule; each output is
+# the library LayerNorm / tanh-GELU forward at the anchor W_{i-1} (taken from
+# the prefix-rule state after the first i batches, itself pinned above); under
+# the key rule the output minus v is the inner residual, so loss == inner_loss.
+
+def _anchor_states_linear(Q, K, V, eta, W0, c0, g, bt, b):
+    """W_{i-1}, c_{i-1} for every batch i from prefix-rule runs over the first i batches."""
+    T = Q.shape[2]
+    out = []
+    for i in range(T // b):
+        if i == 0:
+            out.append((np.broadcast_to(W0, (Q.shape[0],) + W0.shape[1:]),
+                        np.broadcast_to(c0, (Q.shape[0],) + c0.shape[1:])))
+        else:
+            r = oracle.ttt_linear(Q[:, :, :i * b], K[:, :, :i * b], V[:, :, :i * b], eta[:, :, :i * b],
+                                  W0, c0, g, bt, b=b)
+            out.append((r["W"], r["c"]))
+    return out
+
+
+@pytest.mark.parametrize("rule", ["anchor", "key"])
+@pytest.mark.parametrize("b", [1, 4])
+def test_output_rule_is_library_forward_at_anchor_linear(rule, b):
+    rng = np.random.default_rng(40 + b)
+    Q, K, V, eta, W0, c0, g, bt = _rand_linear(rng, B=2, H=2, T=16, d=6)
+    r = oracle.ttt_linear(Q, K, V, eta, W0, c0, g, bt, b=b, rule=rule)
+    X = K if rule == "key" else Q
+    for i, (Wa, ca) in enumerate(_anchor_states_linear(Q, K, V, eta, W0, c0, g, bt, b)):
+        for bi in range(2):
+            for hi in range(2):
+                for t in range(i * b, (i + 1) * b):
+                    z = _torch_f_linear(torch.tensor(Wa[bi, hi]), torch.tensor(ca[bi, hi]),
+                                        torch.tensor(X[bi, hi, t]), torch.tensor(g[hi]), torch.tensor(bt[hi]),
+                                        1e-6, True).numpy()
+                    np.testing.assert_allclose(r["Z"][bi, hi, t], z, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("rule", ["anchor", "key"])
+def test_output_rule_is_library_forward_at_anchor_mlp(rule):
+    rng = np.random.default_rng(44)
+    Q, K, V, eta, W1, c1, W2, c2, g, bt = _rand_mlp(rng, T=12)
+    b = 4
+    r = oracle.ttt_mlp(Q, K, V, eta, W1, c1, W2, c2, g, bt, b=b, rule=rule)
+    X = K if rule == "key" else Q
+    for i in range(3):
+        if i == 0:
+            st = dict(W1=W1, c1=c1, W2=W2, c2=c2)
+        else:
+            sl = slice(0, i * b)
+            st = oracle.ttt_mlp(Q[:, :, sl], K[:, :, sl], V[:, :, sl], eta[:, :, sl], W1, c1, W2, c2, g, bt, b=b)
+        for hi in range(2):
+            for t in range(i * b, (i + 1) * b):
+                z = _torch_f_mlp(*(torch.tensor(st[n][0, hi]) for n in ("W1", "c1", "W2", "c2")),
+                                 torch.tensor(X[0, hi, t]), torch.tensor(g[hi]), torch.tensor(bt[hi]), 1e-6,
+                                 True).numpy()
+                np.testing.assert_allclose(r["Z"][0, hi, t], z, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("rule", ["anchor", "key"])
+def test_output_rule_leaves_trajectory_unchanged(rule):
+    rng = np.random.default_rng(46)
+    Q, K, V, eta, W0, c0, g, bt = _rand_linear(rng, T=32, d=8)
+    p = oracle.ttt_linear(Q, K, V, eta, W0, c0, g, bt, b=8)
+    r = oracle.ttt_linear(Q, K, V, eta, W0, c0, g, bt, b=8, rule=rule)
+    for f in ("W", "c", "inner_loss"):
+        np.testing.assert_array_equal(r[f], p[f])
+    assert np.abs(r["Z"] - p["Z"]).max() > 1e-3   # the outputs do differ
+    args = _rand_mlp(rng, T=8)
+    pm = oracle.ttt_mlp(*args, b=4)
+    rm = oracle.ttt_mlp(*args, b=4, rule=rule)
+    for f in ("W1", "c1", "W2", "c2", "inner_loss"):
+        np.testing.assert_array_equal(rm[f], pm[f])
+
+
+def test_key_rule_output_is_inner_prediction():
+    rng = np.random.default_rng(47)
+    Q, K, V, eta, W0, c0, g, bt = _rand_linear(rng, T=32, d=8)
+    r = oracle.ttt_linear(None, K, V, eta, W0, c0, g, bt, b=8, rule="key")
+    np.testing.assert_allclose(r["loss"], r["inner_loss"], rtol=1e-12, atol=0)
+    rm = oracle.ttt_mlp(None, *(_rand_mlp(rng, T=8)[1:]), b=4, rule="key")
+    np.testing.assert_allclose(rm["loss"], rm["inner_loss"], rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("rule", ["anchor", "key"])
+@pytest.mark.parametrize("b", [1, 4, 16])
+def test_primal_equals_dual_output_rules(rule, b):
+    rng = np.random.default_rng(48 + b)
+    Q, K, V, eta, W0, c0, g, bt = _rand_linear(rng, T=32, d=8)
+    p = oracle.ttt_linear(Q, K, V, eta, W0, c0, g, bt, b=b, rule=rule)
+    dd = dual.ttt_linear_dual(Q, K, V, eta, W0, c0, g, bt, b=b, rule=rule)
+    for f in p:
+        np.testing.assert_allclose(dd[f], p[f], rtol=1e-11, atol=1e-11)
+    args = _rand_mlp(rng, T=8)
+    pm = oracle.ttt_mlp(*args, b=4, rule=rule)
+    dm = dual.ttt_mlp_dual(*args, b=4, rule=rule)
+    for f in pm:
+        np.testing.assert_allclose(dm[f], pm[f], rtol=1e-11, atol=1e-11)
