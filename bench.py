@@ -81,11 +81,12 @@ def _peaks():
     return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
 
 
-def algorithmic_cost(w, z_bytes: int = 4):
+def algorithmic_cost(w, z_bytes: int = 4, out_rule: str = "prefix"):
     """Per-launch algorithmic bytes (Q/K/V in the io dtype, eta fp32, Z in its
-    output dtype) and dense-contraction FLOPs of the dual form."""
+    output dtype; the key output rule reads no Q) and dense-contraction FLOPs
+    of the dual form."""
     es = 2 if w.io == "bf16" else 4
-    per_tok_bytes = 3 * w.d * es + 4 + w.d * z_bytes
+    per_tok_bytes = (2 if out_rule == "key" else 3) * w.d * es + 4 + w.d * z_bytes
     if w.variant == "linear":
         per_tok_flops = 6 * w.d * w.d + 4 * w.b * w.d
     else:
@@ -182,7 +183,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- oracle timing
 
-def oracle_sample(w, n_chains: int, T: int, nthreads: int = 0):
+def oracle_sample(w, n_chains: int, T: int, nthreads: int = 0, rule: str = "prefix"):
     """Run the fp64 oracle on the first ``n_chains`` chains, first ``T`` tokens.
     Returns (seconds, tokens processed, threads used)."""
     import oracle
@@ -194,11 +195,11 @@ def oracle_sample(w, n_chains: int, T: int, nthreads: int = 0):
     if w.variant == "linear":
         oracle.ttt_linear(f(inp["Q"]), f(inp["K"]), f(inp["V"]), f(inp["eta"]), f(inp["W0"]),
                           f(inp["c0"]), f(inp["ln_g"]), f(inp["ln_b"]), b=w.b, eps=w.eps,
-                          nthreads=th)
+                          nthreads=th, rule=rule)
     else:
         oracle.ttt_mlp(f(inp["Q"]), f(inp["K"]), f(inp["V"]), f(inp["eta"]), f(inp["W1"]), f(inp["c1"]),
                        f(inp["W2"]), f(inp["c2"]), f(inp["ln_g"]), f(inp["ln_b"]), b=w.b, eps=w.eps,
-                       nthreads=th)
+                       nthreads=th, rule=rule)
     dt = time.perf_counter() - t0
     return dt, n_chains * T, th
 
@@ -238,15 +239,17 @@ def run_gpu(args):
     zdt = torch.float32 if args.z_dtype == "f32" else torch.bfloat16
     out = {"Z": torch.empty(dev["Q"].shape, dtype=zdt, device="cuda")}
 
+    rule = args.out_rule
+    q_in = None if rule == "key" else dev["Q"]    # the key rule reads no queries
     if w.variant == "linear":
-        call = lambda o: ttt.ttt_linear_forward(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W0"], dev["c0"],
+        call = lambda o: ttt.ttt_linear_forward(q_in, dev["K"], dev["V"], dev["eta"], dev["W0"], dev["c0"],
                                                 dev["ln_g"], dev["ln_b"], mb=w.b, eps=w.eps, out=o,
-                                                status=st, stream=stream)
+                                                status=st, stream=stream, out_rule=rule)
         kind = ttt.linear_kernel_kind(ttt.BF16 if w.io == "bf16" else ttt.F32, w.d, w.b)
     else:
-        call = lambda o: ttt.ttt_mlp_forward(dev["Q"], dev["K"], dev["V"], dev["eta"], dev["W1"], dev["c1"],
+        call = lambda o: ttt.ttt_mlp_forward(q_in, dev["K"], dev["V"], dev["eta"], dev["W1"], dev["c1"],
                                              dev["W2"], dev["c2"], dev["ln_g"], dev["ln_b"], mb=w.b, eps=w.eps,
-                                             out=o, status=st, stream=stream)
+                                             out=o, status=st, stream=stream, out_rule=rule)
         kind = ttt.mlp_kernel_kind(ttt.BF16 if w.io == "bf16" else ttt.F32, w.d, w.hidden, w.b)
     out = call(out)                       # allocates outputs once
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -279,7 +282,7 @@ def run_gpu(args):
         raise RuntimeError("device status %d in timed region" % int(st.item()))
 
     # ---- e2e: pinned host buffers through the C ABI, copies inside the timed region
-    host_in = {k: inp[k].pin_memory() for k in ("Q", "K", "V", "eta")}
+    host_in = {k: inp[k].pin_memory() for k in (("K", "V", "eta") if rule == "key" else ("Q", "K", "V", "eta"))}
     host_Z = torch.empty(inp["Q"].shape, dtype=zdt).pin_memory()
     host_L = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -308,7 +311,7 @@ def run_gpu(args):
     if rank != 0:
         return None
     peaks = _peaks()
-    bytes_launch, flops_launch = algorithmic_cost(w, 4 if args.z_dtype == "f32" else 2)
+    bytes_launch, flops_launch = algorithmic_cost(w, 4 if args.z_dtype == "f32" else 2, rule)
     value = tokens / (ms_max / 1e3)
     if w.variant == "linear":
         bound, achieved, peak, unit = "hbm", bytes_launch / (ms / 1e3) / 1e9, peaks["hbm_gbs"], "GB/s"
@@ -332,10 +335,11 @@ def run_gpu(args):
         "data": "synthetic (seeded Gaussian Q/K/V, sigmoid-gated eta, N(0,0.02^2) W0)",
         "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
                    "mb": w.b, "hidden": w.hidden or None, "io": w.io, "z_dtype": args.z_dtype,
-                   "kernel_kind": kind,
+                   "out_rule": rule, "kernel_kind": kind,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": measured_traffic(w.name, args.z_dtype),
+                     "frac": achieved / peak,
+                     "traffic": measured_traffic(w.name, args.z_dtype) if rule == "prefix" else None,
                      "roofline_frac": t_roof / (ms / 1e3),
                      "peak_source": peaks["source"] + " (burst)",
                      "algorithmic_bytes_per_launch": bytes_launch, "algorithmic_flops_per_launch": flops_launch},
@@ -349,7 +353,7 @@ def run_gpu(args):
     if world == 1 and not args.no_cpu_baseline:
         threads = __import__("oracle").max_threads()
         chains, Ts = _sample_shape(w, args.cpu_budget_s, threads)
-        dt, toks, th = oracle_sample(w, chains, Ts, nthreads=threads)
+        dt, toks, th = oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule)
         line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
                                 "sample": "%d of %d chains x %d tokens (fp64 primal token loop, C, OpenMP)"
                                           % (chains, w.chains, Ts),
@@ -369,10 +373,10 @@ def run_reference(args):
     per_step_wall = max(0.05, args.ref_budget_s / max(1, args.steps + args.warmup))
     chains, Ts = _sample_shape(w, per_step_wall * threads, threads)
     for _ in range(args.warmup):
-        oracle_sample(w, chains, Ts, nthreads=threads)
+        oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule)
     secs, toks = 0.0, 0
     for _ in range(args.steps):
-        dt, n, _ = oracle_sample(w, chains, Ts, nthreads=threads)
+        dt, n, _ = oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule)
         secs += dt
         toks += n
     value = toks / secs
@@ -383,7 +387,7 @@ def run_reference(args):
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator)",
         "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
-                   "mb": w.b, "hidden": w.hidden or None},
+                   "mb": w.b, "hidden": w.hidden or None, "out_rule": args.out_rule},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": "%d of %d chains x %d tokens per step" % (chains, w.chains, Ts)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -402,6 +406,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=20.0, help="core-seconds of the oracle sample")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out-rule", default="prefix", choices=["prefix", "anchor", "key"],
+                    help="output rule: z_t = f(q_t; W_t) (prefix), f(q_t; W_{i-1}) (anchor), f(k_t; W_{i-1}) (key)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -15,7 +15,9 @@
  *           W_i = W_{i-1} - (1/b) sum_{t in batch i} eta_t grad l_t(W_{i-1})
  *   output (Eq. 5 of the survey section):   z_t = f(q_t; W_t), where W_t is
  *           W_{i-1} minus the (1/b) eta_s grad l_s(W_{i-1}) terms of the
- *           tokens s <= t of batch i (the in-batch prefix).
+ *           tokens s <= t of batch i (the in-batch prefix). Two other output
+ *           rules the pages discuss are selectable (`out_rule`, below); the
+ *           weight trajectory, W_out, c_out and inner_loss do not depend on it.
  *   f(x; W) = x + LN(f_res(x; W))  (residual form, survey section
  *           "재현성과 공개 구현"), LN with frozen gamma/beta, biased variance,
  *           eps inside the square root.
@@ -61,13 +63,13 @@
 extern "C" {
 #endif
 
-#define TTT_ABI_VERSION 1
+#define TTT_ABI_VERSION 2
 
 typedef enum {
     TTT_OK = 0,
     TTT_ERR_NULL = 1,            /* a required pointer is NULL                       */
     TTT_ERR_SHAPE = 2,           /* B,H,T,d,mb,hidden out of range or T % mb != 0    */
-    TTT_ERR_UNSUPPORTED = 3,     /* valid shape, no kernel for (io, d, mb, hidden)   */
+    TTT_ERR_UNSUPPORTED = 3,     /* no kernel for (io, d, mb, hidden), or bad rule   */
     TTT_ERR_ALIGN = 4,           /* a pointer is not 16-byte aligned                 */
     TTT_ERR_NOT_DEVICE_PTR = 5,  /* a pointer is not device-accessible memory        */
     TTT_ERR_CUDA = 6,            /* a CUDA runtime call or launch failed             */
@@ -78,6 +80,23 @@ typedef enum {
 } ttt_status;
 
 typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
+
+/* Output rule: which weights and which input produce z_t for token t of
+ * mini-batch i (the weight trajectory is the same under every rule).
+ *  TTT_OUT_PREFIX  z_t = f(q_t; W_t), W_t = W_{i-1} plus the updates of the
+ *                  tokens s <= t of batch i: Eq. 5 of the "TTT layer" section
+ *                  of the survey page, Eq. 8 of the review's section 2.4.1.
+ *  TTT_OUT_ANCHOR  z_t = f(q_t; W_{i-1}) for every token of the batch: the
+ *                  mini-batch TTT of the "End-to-End Test-Time Training for
+ *                  Long Context" review, section 2.3 (every prediction of a
+ *                  batch is made with the weights before it).
+ *  TTT_OUT_KEY     z_t = f(k_t; W_{i-1}): the simplified output rule, Eq. 9
+ *                  of the review's section 2.4.2 (the inner loss's own
+ *                  prediction reused as the output; Q is not read and may be
+ *                  NULL). Then z_t - v_t is the inner residual, so
+ *                  loss == inner_loss. With mb = 1 the anchor W_{i-1} is
+ *                  W_{t-1}, exactly as Eq. 9 writes it. */
+typedef enum { TTT_OUT_PREFIX = 0, TTT_OUT_ANCHOR = 1, TTT_OUT_KEY = 2 } ttt_out_rule;
 
 /* ---------------------------------------------------------------------- */
 /* TTT-Linear                                                              */
@@ -96,12 +115,13 @@ typedef struct {
     int64_t c0_bstride;      /* elements between sequences in c0 (0 = shared)  */
     const float *ln_g;       /* [H][d] LayerNorm gamma                         */
     const float *ln_b;       /* [H][d] LayerNorm beta                          */
-    void *Z;                 /* [B][H][T][d] z_io out: z_t = f(q_t; W_t)       */
+    void *Z;                 /* [B][H][T][d] z_io out (see out_rule)           */
     float *W_out;            /* [B][H][d][d] final W, or NULL                  */
     float *c_out;            /* [B][H][d] final c, or NULL                     */
     float *loss;             /* [B][H][T] L_t = ||z_t - v_t||^2, or NULL       */
     float *inner_loss;       /* [B][H][T] l_t(W_{i-1}) at the anchor, or NULL  */
     int32_t *status_dev;     /* device int32 (0 on entry), or NULL             */
+    int32_t out_rule;        /* ttt_out_rule; 0 = TTT_OUT_PREFIX               */
 } ttt_linear_args;
 
 /* Supported: io = TTT_F32 or TTT_BF16 with 1 <= d <= 128, 1 <= mb <= 64 and
@@ -134,6 +154,7 @@ typedef struct {
     float *W1_out, *c1_out, *W2_out, *c2_out; /* [B][H][...] or NULL */
     float *loss, *inner_loss;
     int32_t *status_dev;
+    int32_t out_rule;        /* ttt_out_rule, as for TTT-Linear               */
 } ttt_mlp_args;
 
 /* Supported: io = TTT_F32 or TTT_BF16 with d <= 256, hidden <= 1024,

@@ -19,13 +19,15 @@ from typing import Optional
 __all__ = [
     "TTTError", "lib", "lib_path", "ttt_linear_forward", "ttt_mlp_forward", "status_string",
     "abi_version", "linear_kernel_kind", "mlp_kernel_kind", "LinearArgs", "MlpArgs",
-    "STATUS", "F32", "BF16",
+    "STATUS", "F32", "BF16", "OUT_RULES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 lib_path = os.path.join(_HERE, "libttt_b300.so")
 
 F32, BF16 = 0, 1
+# ttt_out_rule: which weights / input produce z_t (see include/ttt.h)
+OUT_RULES = {"prefix": 0, "anchor": 1, "key": 2}
 STATUS = {
     0: "TTT_OK", 1: "TTT_ERR_NULL", 2: "TTT_ERR_SHAPE", 3: "TTT_ERR_UNSUPPORTED", 4: "TTT_ERR_ALIGN",
     5: "TTT_ERR_NOT_DEVICE_PTR", 6: "TTT_ERR_CUDA", 7: "TTT_ERR_TIMEOUT", 8: "TTT_ERR_NONFINITE",
@@ -44,7 +46,7 @@ class LinearArgs(ctypes.Structure):
         ("Q", _vp), ("K", _vp), ("V", _vp), ("eta", _vp), ("W0", _vp), ("c0", _vp),
         ("w0_bstride", ctypes.c_int64), ("c0_bstride", ctypes.c_int64),
         ("ln_g", _vp), ("ln_b", _vp), ("Z", _vp), ("W_out", _vp), ("c_out", _vp),
-        ("loss", _vp), ("inner_loss", _vp), ("status_dev", _vp),
+        ("loss", _vp), ("inner_loss", _vp), ("status_dev", _vp), ("out_rule", ctypes.c_int32),
     ]
 
 
@@ -59,8 +61,16 @@ class MlpArgs(ctypes.Structure):
         ("w_bstride", ctypes.c_int64), ("c1_bstride", ctypes.c_int64), ("c2_bstride", ctypes.c_int64),
         ("ln_g", _vp), ("ln_b", _vp), ("Z", _vp),
         ("W1_out", _vp), ("c1_out", _vp), ("W2_out", _vp), ("c2_out", _vp),
-        ("loss", _vp), ("inner_loss", _vp), ("status_dev", _vp),
+        ("loss", _vp), ("inner_loss", _vp), ("status_dev", _vp), ("out_rule", ctypes.c_int32),
     ]
+
+
+def _rule_code(rule) -> int:
+    if isinstance(rule, str):
+        if rule not in OUT_RULES:
+            raise ValueError("out_rule must be one of %s" % sorted(OUT_RULES))
+        return OUT_RULES[rule]
+    return int(rule)
 
 
 class TTTError(RuntimeError):
@@ -159,7 +169,7 @@ def _stream_handle(stream) -> Optional[int]:
 def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float = 1e-6,
                        z_dtype=None, out: Optional[dict] = None, want_state: bool = True,
                        want_loss: bool = True, want_inner_loss: bool = True,
-                       status=None, stream=None) -> dict:
+                       status=None, stream=None, out_rule="prefix") -> dict:
     """Run the TTT-Linear inner loop through ``ttt_linear_forward``.
 
     Q, K, V [B,H,T,d] (float32 or bfloat16, CUDA, contiguous); eta [B,H,T] fp32;
@@ -168,16 +178,19 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
     allocated with torch. ``z_dtype`` (torch.float32 by default, or
     torch.bfloat16) is the element type of Z; a preallocated Z sets it. ``status`` is an optional int32 CUDA tensor of one
     element (0 on entry) that receives device-side errors. Asynchronous on
-    ``stream`` (default: torch's current stream)."""
+    ``stream`` (default: torch's current stream). ``out_rule`` is "prefix"
+    (z_t = f(q_t; W_t)), "anchor" (z_t = f(q_t; W_{i-1})) or "key"
+    (z_t = f(k_t; W_{i-1}); Q may be None)."""
     import torch
+    rule = _rule_code(out_rule)
     for n, t in (("Q", Q), ("K", K), ("V", V), ("eta", eta), ("W0", W0), ("c0", c0),
                  ("ln_g", ln_g), ("ln_b", ln_b), ("status", status)):
         _check_cuda(n, t)
-    B, H, T, d = Q.shape
+    B, H, T, d = K.shape
     out = dict(out or {})
-    dev = Q.device
+    dev = K.device
     if "Z" not in out:
-        out["Z"] = torch.empty(Q.shape, device=dev, dtype=z_dtype or torch.float32)
+        out["Z"] = torch.empty(K.shape, device=dev, dtype=z_dtype or torch.float32)
     if want_state:
         out.setdefault("W", torch.empty(B, H, d, d, device=dev, dtype=torch.float32))
         out.setdefault("c", torch.empty(B, H, d, device=dev, dtype=torch.float32))
@@ -186,12 +199,12 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
     if want_inner_loss:
         out.setdefault("inner_loss", torch.empty(B, H, T, device=dev, dtype=torch.float32))
     a = LinearArgs(
-        B=B, H=H, T=T, d=d, mb=mb, io=_io_code(Q.dtype), z_io=_io_code(out["Z"].dtype), ln_eps=eps,
+        B=B, H=H, T=T, d=d, mb=mb, io=_io_code(K.dtype), z_io=_io_code(out["Z"].dtype), ln_eps=eps,
         Q=_ptr(Q), K=_ptr(K), V=_ptr(V), eta=_ptr(eta), W0=_ptr(W0), c0=_ptr(c0),
         w0_bstride=_bstride(W0, B, H * d * d), c0_bstride=_bstride(c0, B, H * d),
         ln_g=_ptr(ln_g), ln_b=_ptr(ln_b), Z=_ptr(out["Z"]), W_out=_ptr(out.get("W")),
         c_out=_ptr(out.get("c")), loss=_ptr(out.get("loss")),
-        inner_loss=_ptr(out.get("inner_loss")), status_dev=_ptr(status),
+        inner_loss=_ptr(out.get("inner_loss")), status_dev=_ptr(status), out_rule=rule,
     )
     rc = lib().ttt_linear_forward(ctypes.byref(a), _stream_handle(stream))
     if rc != 0:
@@ -202,22 +215,23 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
 def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: float = 1e-6,
                     z_dtype=None, out: Optional[dict] = None, want_state: bool = True,
                     want_loss: bool = True, want_inner_loss: bool = True,
-                    status=None, stream=None) -> dict:
+                    status=None, stream=None, out_rule="prefix") -> dict:
     """Run the TTT-MLP inner loop through ``ttt_mlp_forward``.
 
     W1 [B|1,H,h,d], c1 [B|1,H,h], W2 [B|1,H,d,h], c2 [B|1,H,d] fp32; other
     arguments as for ``ttt_linear_forward``. Outputs: Z, W1, c1, W2, c2, loss,
     inner_loss."""
     import torch
+    rule = _rule_code(out_rule)
     for n, t in (("Q", Q), ("K", K), ("V", V), ("eta", eta), ("W1", W1), ("c1", c1), ("W2", W2),
                  ("c2", c2), ("ln_g", ln_g), ("ln_b", ln_b), ("status", status)):
         _check_cuda(n, t)
-    B, H, T, d = Q.shape
+    B, H, T, d = K.shape
     h = W1.shape[-2]
     out = dict(out or {})
-    dev = Q.device
+    dev = K.device
     if "Z" not in out:
-        out["Z"] = torch.empty(Q.shape, device=dev, dtype=z_dtype or torch.float32)
+        out["Z"] = torch.empty(K.shape, device=dev, dtype=z_dtype or torch.float32)
     if want_state:
         out.setdefault("W1", torch.empty(B, H, h, d, device=dev, dtype=torch.float32))
         out.setdefault("c1", torch.empty(B, H, h, device=dev, dtype=torch.float32))
@@ -228,7 +242,7 @@ def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: f
     if want_inner_loss:
         out.setdefault("inner_loss", torch.empty(B, H, T, device=dev, dtype=torch.float32))
     a = MlpArgs(
-        B=B, H=H, T=T, d=d, hidden=h, mb=mb, io=_io_code(Q.dtype), z_io=_io_code(out["Z"].dtype),
+        B=B, H=H, T=T, d=d, hidden=h, mb=mb, io=_io_code(K.dtype), z_io=_io_code(out["Z"].dtype),
         ln_eps=eps,
         Q=_ptr(Q), K=_ptr(K), V=_ptr(V), eta=_ptr(eta),
         W1_0=_ptr(W1), c1_0=_ptr(c1), W2_0=_ptr(W2), c2_0=_ptr(c2),
@@ -237,7 +251,7 @@ def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: f
         ln_g=_ptr(ln_g), ln_b=_ptr(ln_b), Z=_ptr(out["Z"]),
         W1_out=_ptr(out.get("W1")), c1_out=_ptr(out.get("c1")), W2_out=_ptr(out.get("W2")),
         c2_out=_ptr(out.get("c2")), loss=_ptr(out.get("loss")),
-        inner_loss=_ptr(out.get("inner_loss")), status_dev=_ptr(status),
+        inner_loss=_ptr(out.get("inner_loss")), status_dev=_ptr(status), out_rule=rule,
     )
     rc = lib().ttt_mlp_forward(ctypes.byref(a), _stream_handle(stream))
     if rc != 0:

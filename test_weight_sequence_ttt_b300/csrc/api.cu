@@ -96,7 +96,10 @@ int ttt_mlp_kernel_kind(int32_t io, int32_t d, int32_t hidden, int32_t mb)
 ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
 {
     if (!a) return TTT_ERR_NULL;
-    if (!a->Q || !a->K || !a->V || !a->eta || !a->W0 || !a->c0 || !a->ln_g || !a->ln_b || !a->Z)
+    if (a->out_rule < TTT_OUT_PREFIX || a->out_rule > TTT_OUT_KEY) return TTT_ERR_UNSUPPORTED;
+    // Under the key rule the queries are the keys (Q is not read).
+    const void *Qe = a->out_rule == TTT_OUT_KEY ? a->K : a->Q;
+    if (!Qe || !a->K || !a->V || !a->eta || !a->W0 || !a->c0 || !a->ln_g || !a->ln_b || !a->Z)
         return TTT_ERR_NULL;
     if (!dims_ok(a->B, a->H, a->T, a->d, a->mb)) return TTT_ERR_SHAPE;
     if (a->io != TTT_F32 && a->io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
@@ -106,7 +109,7 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     const int kind = ttt_linear_kernel_kind(a->io, a->d, a->mb);
     if (kind == 0) return TTT_ERR_UNSUPPORTED;
 
-    const void *in[] = {a->Q, a->K, a->V, a->eta, a->W0, a->c0, a->ln_g, a->ln_b};
+    const void *in[] = {Qe, a->K, a->V, a->eta, a->W0, a->c0, a->ln_g, a->ln_b};
     const void *out[] = {a->Z, a->W_out, a->c_out, a->loss, a->inner_loss, a->status_dev};
     for (const void *p : in)
         if (!aligned16(p)) return TTT_ERR_ALIGN;
@@ -118,7 +121,7 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     const size_t es = a->io == TTT_BF16 ? 2 : 4;
     const size_t zs = a->z_io == TTT_BF16 ? 2 : 4;
     const size_t tok = B * H * T;
-    const Range rin[] = {span(a->Q, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
+    const Range rin[] = {span(Qe, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
                          span(a->eta, tok * 4), span(a->W0, init_bytes(a->B, a->H, d * d, a->w0_bstride)),
                          span(a->c0, init_bytes(a->B, a->H, d, a->c0_bstride)), span(a->ln_g, H * d * 4),
                          span(a->ln_b, H * d * 4)};
@@ -145,7 +148,9 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     p.mb = a->mb;
     p.z_f32 = a->z_io == TTT_F32;
     p.eps = a->ln_eps;
-    p.Q = a->Q;
+    p.prefix = a->out_rule == TTT_OUT_PREFIX;
+    p.q_is_k = a->out_rule == TTT_OUT_KEY;
+    p.Q = Qe;
     p.K = a->K;
     p.V = a->V;
     p.eta = a->eta;
@@ -175,7 +180,9 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
 ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
 {
     if (!a) return TTT_ERR_NULL;
-    if (!a->Q || !a->K || !a->V || !a->eta || !a->W1_0 || !a->c1_0 || !a->W2_0 || !a->c2_0 || !a->ln_g ||
+    if (a->out_rule < TTT_OUT_PREFIX || a->out_rule > TTT_OUT_KEY) return TTT_ERR_UNSUPPORTED;
+    const void *Qe = a->out_rule == TTT_OUT_KEY ? a->K : a->Q;
+    if (!Qe || !a->K || !a->V || !a->eta || !a->W1_0 || !a->c1_0 || !a->W2_0 || !a->c2_0 || !a->ln_g ||
         !a->ln_b || !a->Z)
         return TTT_ERR_NULL;
     if (!dims_ok(a->B, a->H, a->T, a->d, a->mb) || a->hidden < 1 || a->hidden > 4096) return TTT_ERR_SHAPE;
@@ -186,7 +193,7 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     const int kind = ttt_mlp_kernel_kind(a->io, a->d, a->hidden, a->mb);
     if (kind == 0) return TTT_ERR_UNSUPPORTED;
 
-    const void *in[] = {a->Q, a->K, a->V, a->eta, a->W1_0, a->c1_0, a->W2_0, a->c2_0, a->ln_g, a->ln_b};
+    const void *in[] = {Qe, a->K, a->V, a->eta, a->W1_0, a->c1_0, a->W2_0, a->c2_0, a->ln_g, a->ln_b};
     const void *out[] = {a->Z, a->W1_out, a->c1_out, a->W2_out, a->c2_out, a->loss, a->inner_loss, a->status_dev};
     for (const void *p : in)
         if (!aligned16(p)) return TTT_ERR_ALIGN;
@@ -198,7 +205,7 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     const size_t es = a->io == TTT_BF16 ? 2 : 4;
     const size_t zs = a->z_io == TTT_BF16 ? 2 : 4;
     const size_t tok = B * H * T;
-    const Range rin[] = {span(a->Q, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
+    const Range rin[] = {span(Qe, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
                          span(a->eta, tok * 4), span(a->W1_0, init_bytes(a->B, a->H, h * d, a->w_bstride)),
                          span(a->c1_0, init_bytes(a->B, a->H, h, a->c1_bstride)),
                          span(a->W2_0, init_bytes(a->B, a->H, h * d, a->w_bstride)),
@@ -232,7 +239,9 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     p.mb = a->mb;
     p.z_f32 = a->z_io == TTT_F32;
     p.eps = a->ln_eps;
-    p.Q = a->Q;
+    p.prefix = a->out_rule == TTT_OUT_PREFIX;
+    p.q_is_k = a->out_rule == TTT_OUT_KEY;
+    p.Q = Qe;
     p.K = a->K;
     p.V = a->V;
     p.eta = a->eta;

@@ -73,7 +73,8 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w)
 }
 
 // Geometry of one input stage: bf16 K/Q/V tiles [16 x D] at the given byte
-// offsets (1024-aligned) and 16 fp32 learning rates.
+// offsets (1024-aligned; off_q < 0: no query tile is loaded) and 16 fp32
+// learning rates.
 struct StageGeom {
     int stages, stage_bytes, off_k, off_q, off_v, off_eta;
 };
@@ -107,11 +108,11 @@ __device__ void role_loader(const CUtensorMap *tmQ, const CUtensorMap *tmK, cons
         }
         cp_async_mbar_arrive_noinc(&full[st]);
         if (lane == 0) {
-            mbar_arrive_expect_tx(&full[st], 3 * 32 * D);
+            mbar_arrive_expect_tx(&full[st], (g.off_q < 0 ? 2 : 3) * 32 * D);
 #pragma unroll
             for (int h = 0; h < D / 64; ++h) {
                 tma_load_3d(stg + g.off_k + h * 2048, tmK, &full[st], h * 64, t0, chain);
-                tma_load_3d(stg + g.off_q + h * 2048, tmQ, &full[st], h * 64, t0, chain);
+                if (g.off_q >= 0) tma_load_3d(stg + g.off_q + h * 2048, tmQ, &full[st], h * 64, t0, chain);
                 tma_load_3d(stg + g.off_v + h * 2048, tmV, &full[st], h * 64, t0, chain);
             }
         }

@@ -32,7 +32,9 @@ cudaError_t ensure_smem(int bytes)
 // Chain-level parameters shared by the TTT-Linear kernels (device pointers).
 struct LinearParams {
     int H, T, d, mb;
-    int z_f32;  // Z element type: 1 = fp32, 0 = bf16
+    int z_f32;   // Z element type: 1 = fp32, 0 = bf16
+    int prefix;  // 1: z_t with the in-batch prefix W_t; 0: with the anchor W_{i-1}
+    int q_is_k;  // 1: the queries are the keys (no query tile is loaded)
     float eps;
     const void *Q, *K, *V;
     const float *eta;
@@ -48,6 +50,8 @@ struct LinearParams {
 struct MlpParams {
     int H, T, d, hidden, mb;
     int z_f32;
+    int prefix;  // as for LinearParams
+    int q_is_k;
     float eps;
     const void *Q, *K, *V;
     const float *eta;

@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
         for (int idx = tid; idx < b * b; idx += kThreads) {
             const int t = idx / b, s = idx - t * b;
             float v = 0.f;
-            if (s <= t) {
+            if (p.prefix && s <= t) {  // the anchor rule sees no update of the batch
                 const float *q = Qt + t * d, *k = Kt + s * d;
                 float acc = 1.f;
                 for (int i = 0; i < d; ++i) acc = fmaf(q[i], k[i], acc);

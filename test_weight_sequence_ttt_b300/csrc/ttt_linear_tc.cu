@@ -81,6 +81,9 @@ struct Cfg {
     static constexpr int kTile = 32 * D;             // 16 rows x D x 2 B
     static constexpr int kOffK = 0, kOffQ = kTile, kOffV = 2 * kTile;  // bf16, as loaded
     static constexpr int kOffKh = 3 * kTile, kOffQh = 4 * kTile;      // fp16 copies (same layout)
+    // The query tiles; the key tiles stand in for them when the queries are the keys.
+    __device__ static int offQ(const LinearParams &p) { return p.q_is_k ? kOffK : kOffQ; }
+    __device__ static int offQh(const LinearParams &p) { return p.q_is_k ? kOffKh : kOffQh; }
     static constexpr int kOffMq = 5 * kTile;         // fp16 B fragments, 32 lanes x 16 B each
     static constexpr int kOffGk = kOffMq + 512;
     static constexpr int kOffKx = kOffGk + 512;
@@ -269,11 +272,11 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
             }
             cp_async_mbar_arrive_noinc(&R.full[st]);
             if (lane == 0) {
-                mbar_arrive_expect_tx(&R.full[st], 3 * C::kTile);
+                mbar_arrive_expect_tx(&R.full[st], (p.q_is_k ? 2 : 3) * C::kTile);
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {
                     tma_load_3d(stg + C::kOffK + h * 2048, tmK, &R.full[st], h * 64, t0, chain);
-                    tma_load_3d(stg + C::kOffQ + h * 2048, tmQ, &R.full[st], h * 64, t0, chain);
+                    if (!p.q_is_k) tma_load_3d(stg + C::kOffQ + h * 2048, tmQ, &R.full[st], h * 64, t0, chain);
                     tma_load_3d(stg + C::kOffV + h * 2048, tmV, &R.full[st], h * 64, t0, chain);
                 }
             }
@@ -301,6 +304,7 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
 {
     using C = Cfg<D>;
     const int g = lane >> 2, c4 = lane & 3;
+    const bool prefix = p.prefix != 0;
     uint32_t mag = 0;  // per-halfword max of |bf16 bits|: >= 0x4780 means |x| >= 2^16 (or inf/nan)
     const int ra = (lane & 7) + ((lane >> 3) & 1) * 8;  // A-fragment row (ldmatrix x4)
     const int rb = (lane & 7) + (lane >> 4) * 8;        // B-fragment row
@@ -313,9 +317,11 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
         }
         TTT_TRACE_AT(p, i, 12);
         uint8_t *stg = stage_ptr<D>(sm, st);
-        // (1) fp16 copies of the K and Q tiles (same swizzled byte layout).
+        // (1) fp16 copies of the K and Q tiles (same swizzled byte layout; the Q
+        //     tile is the K tile when the queries are the keys).
 #pragma unroll
         for (int tile = 0; tile < 2; ++tile) {
+            if (tile == 1 && p.q_is_k) break;
             const uint4 *src = reinterpret_cast<const uint4 *>(stg + (tile == 0 ? C::kOffK : C::kOffQ));
             uint4 *dst = reinterpret_cast<uint4 *>(stg + (tile == 0 ? C::kOffKh : C::kOffQh));
 #pragma unroll
@@ -330,7 +336,7 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
         __syncwarp();
         // (3) Gram fragments. d*[j][r] holds (t = g + 8(r>>1), s = 8j + 2c4 + (r&1)):
         //     dq = Q_i K_i^T, dk = K_i K_i^T, dx = K_i K_{i-1}^T (t in step i, s in step i-1).
-        const uint32_t sK = smem_u32(stg + C::kOffKh), sQ = smem_u32(stg + C::kOffQh);
+        const uint32_t sK = smem_u32(stg + C::kOffKh), sQ = smem_u32(stg + C::offQh(p));
         const uint32_t sKp = smem_u32(stage_ptr<D>(sm, (i + kStages - 1) % kStages) + C::kOffKh);
         const bool has_prev = i > 0;
         float dq[2][4] = {}, dk[2][4] = {}, dx[2][4] = {};
@@ -353,10 +359,14 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
                 mma16816(dx[1], ak, bp[2], bp[3]);
             }
         }
-        // As B fragments (k = s, n = t) for the W warps.
+        // As B fragments (k = s, n = t) for the W warps. The mask selects which
+        // tokens' updates the output of token t sees: s <= t (in-batch prefix), or
+        // under the anchor rule only the mini-batches before t's own (none when
+        // b >= 16: the outputs use the anchor alone).
         auto mq = [&](int j, int r) {
             const int t = g + 8 * (r >> 1), s = 8 * j + 2 * c4 + (r & 1);
-            return s <= t ? dq[j][r] + 1.f : 0.f;
+            const bool seen = prefix ? s <= t : s / SUBB < t / SUBB;
+            return seen ? dq[j][r] + 1.f : 0.f;
         };
         reinterpret_cast<uint4 *>(stg + C::kOffMq)[lane] =
             make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)),
@@ -553,7 +563,7 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
                 // Independent tensor-core work while the other W warps finish their sums:
                 // S_{i+1} = W_{i-1} K_{i+1}^T + c_{i-1}, Rq_i = W_{i-1} Q_i^T + c_{i-1}.
                 if (has_next) rows_gemm<D>(Wa, cb, smem_u32(stgn + C::kOffKh), lane, Sn);
-                rows_gemm<D>(Wa, cb, smem_u32(stg + C::kOffQh), lane, Rq);
+                rows_gemm<D>(Wa, cb, smem_u32(stg + C::offQh(p)), lane, Rq);
                 if (w == 0) TTT_TRACE_AT(p, i, 2);
             }
             if (!wait_bar(&R.red[buf], parity_of(rnd >> 1), R.flags)) {
@@ -880,29 +890,12 @@ __device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &
                     }
             }
         }
-        // Phase 2: outputs with the running in-batch prefix, then each block's update.
-#pragma unroll
-        for (int pb = 0; pb < NB; ++pb) {
-            const int i = mbi * NB + pb, st = i % kStages, slot = i & 1;
+        // Phase 2: each block's outputs, then its update. With the in-batch prefix the
+        // outputs see the running weights (W_{i-1} plus the earlier blocks' updates);
+        // under the anchor rule every block's outputs come first, all at W_{i-1}.
+        auto block_update = [&](int pb) {
+            const int i = mbi * NB + pb, st = i % kStages;
             uint8_t *stg = stage_ptr<D>(sm, st);
-            float rq[2][4];
-            rows_gemm<D>(Wa, cb, smem_u32(stg + C::kOffQh), lane, rq);
-            {
-                const uint4 mq = reinterpret_cast<const uint4 *>(stg + C::kOffMq)[lane];
-                mma16816(rq[0], afs[pb], mq.x, mq.y);
-                mma16816(rq[1], afs[pb], mq.z, mq.w);
-            }
-            if (!wait_bar(&R.yempty[slot], parity_of(i >> 1) ^ 1u, R.flags)) {
-                abort_chain(R.flags, p.status);
-                return;
-            }
-            float *ys = reinterpret_cast<float *>(sm + C::kOffY + slot * kSS * C::YS * 4);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    ys[(8 * nt + 2 * c4 + (r & 1)) * C::YS + 16 * w + g + 8 * (r >> 1)] = rq[nt][r];
-            warp_arrive(&R.yfull[slot], lane);
             {
                 const uint32_t sK = smem_u32(stg + C::kOffKh);
 #pragma unroll
@@ -925,6 +918,34 @@ __device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &
             cb[0] += s0;
             cb[1] += s1r;
             warp_arrive(&R.empty[st], lane);
+        };
+#pragma unroll
+        for (int pb = 0; pb < NB; ++pb) {
+            const int i = mbi * NB + pb, st = i % kStages, slot = i & 1;
+            uint8_t *stg = stage_ptr<D>(sm, st);
+            float rq[2][4];
+            rows_gemm<D>(Wa, cb, smem_u32(stg + C::offQh(p)), lane, rq);
+            {
+                const uint4 mq = reinterpret_cast<const uint4 *>(stg + C::kOffMq)[lane];
+                mma16816(rq[0], afs[pb], mq.x, mq.y);
+                mma16816(rq[1], afs[pb], mq.z, mq.w);
+            }
+            if (!wait_bar(&R.yempty[slot], parity_of(i >> 1) ^ 1u, R.flags)) {
+                abort_chain(R.flags, p.status);
+                return;
+            }
+            float *ys = reinterpret_cast<float *>(sm + C::kOffY + slot * kSS * C::YS * 4);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    ys[(8 * nt + 2 * c4 + (r & 1)) * C::YS + 16 * w + g + 8 * (r >> 1)] = rq[nt][r];
+            warp_arrive(&R.yfull[slot], lane);
+            if (p.prefix) block_update(pb);
+        }
+        if (!p.prefix) {
+#pragma unroll
+            for (int pb = 0; pb < NB; ++pb) block_update(pb);
         }
     }
     bool badv = !isfinite(cb[0]) || !isfinite(cb[1]);
@@ -1012,7 +1033,7 @@ __device__ void role_output(const LinearParams &p, uint8_t *sm, const Ring &R, i
         for (int k = 0; k < NCH; ++k) {
             const int f = 4 * j + 4 * LPT * k;
             const uint32_t off = swz(tloc, f >> 3) + (f & 7) * 2;
-            const uint2 qb = *reinterpret_cast<const uint2 *>(stg + C::kOffQ + off);  // bf16
+            const uint2 qb = *reinterpret_cast<const uint2 *>(stg + C::offQ(p) + off);  // bf16
             const uint2 vb = *reinterpret_cast<const uint2 *>(stg + C::kOffV + off);  // bf16
             const float qv[4] = {bf16_bits_to_f32(qb.x & 0xffffu), bf16_bits_to_f32(qb.x >> 16),
                                  bf16_bits_to_f32(qb.y & 0xffffu), bf16_bits_to_f32(qb.y >> 16)};
@@ -1307,7 +1328,7 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
         publish_s(1);
     }
     float Rq[2][4];
-    rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, 0) + C::kOffQh), lane, Rq);
+    rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, 0) + C::offQh(p)), lane, Rq);
     for (int j = 0; j < nsteps; ++j) {
         const int st = j % kStages, slot = j & 1;
         uint8_t *stg = stage_ptr<D>(sm, st);
@@ -1358,7 +1379,7 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
         }
         if (w == 0) TTT_TRACE_AT(p, j, 7);
         if (j + 1 < nsteps)  // Rq_{j+1} = W_j Q_{j+1}^T + c_j (stage j+1 waited for above, one step earlier)
-            rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % kStages) + C::kOffQh), lane, Rq);
+            rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % kStages) + C::offQh(p)), lane, Rq);
         warp_arrive(&R.empty[st], lane);
     }
     bool badv = !isfinite(cb[0]) || !isfinite(cb[1]);

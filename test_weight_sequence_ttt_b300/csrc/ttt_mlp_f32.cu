@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
         for (int i = tid; i < b * b; i += kThreads) {
             const int t = i / b, s = i - t * b;
             float v = 0.f;
-            if (s <= t) {
+            if (p.prefix && s <= t) {  // the anchor rule sees no update of the batch
                 float acc = 1.f;
                 for (int u = 0; u < d; ++u) acc = fmaf(Qt[t * d + u], Kt[s * d + u], acc);
                 v = et[s] * inv_b * acc;
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
         for (int i = tid; i < b * b; i += kThreads) {
             const int t = i / b, s = i - t * b;
             float v = 0.f;
-            if (s <= t) {
+            if (p.prefix && s <= t) {  // the anchor rule sees no update of the batch
                 float acc = 1.f;
                 for (int u = 0; u < h; ++u) acc = fmaf(Hq[t * h + u], X2[s * h + u], acc);
                 v = et[s] * inv_b * acc;

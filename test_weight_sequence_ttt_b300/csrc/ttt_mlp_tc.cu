@@ -87,7 +87,7 @@ constexpr int kOffYq = kOffRed + 2 * kNY * kB * 16;      // 2 slots x [16][kYS] 
 constexpr int kOffMq2 = kOffYq + 2 * kB * kYS * 4;       // causal x2q.x2k + 1 fragments (P -> Y)
 constexpr int kOffTmem = kOffMq2 + 512;
 constexpr int kOffBar = kOffTmem + 16;
-constexpr int kNumBars = 3 * kStages + 6;
+constexpr int kNumBars = 3 * kStages + 7;
 constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
 constexpr int kSmemAlloc = kSmem + 1024;
 constexpr uint32_t kTmemCols = 128;  // two H warps per lane quarter x 64 columns
@@ -97,8 +97,11 @@ constexpr int kHY = (kNH + kNY) * 32;
 constexpr float kGeluA = 0.7978845608028654f;  // sqrt(2/pi)
 constexpr float kGeluC = 0.044715f;
 
-// mbarriers: full/prep/empty (stage ring), hq (H -> P: X2q of the step is
-// written), mq2 (P -> Y: Gram fragments), yqfull/yqempty[2] (Yq hand-off Y <-> P).
+// mbarriers: full/prep/empty (stage ring); hq[2] (H -> P: X2q of step j is
+// written; by step parity, because the H warps may arrive for step j + 1
+// before P has waited for step j, never for step j + 2: that needs G_{j+2},
+// which the Y warps hand over only after P's Gram of step j); mq2 (P -> Y:
+// Gram fragments); yqfull/yqempty[2] (Yq hand-off Y <-> P).
 struct Ring {
     uint64_t *full, *prep, *empty, *hq, *mq2, *yqfull, *yqempty;
     volatile int *flags;  // [0] abort, [1] fp16 range violation seen
@@ -125,13 +128,15 @@ __device__ __forceinline__ uint32_t hb(uint32_t base, int row, int col, int stri
 
 // Step i's input side: fp16 copies of the K/Q tiles, causal Q K^T + 1
 // fragments and (i > 0) K_{i-1} K_i^T + 1 fragments for the Z1 look-ahead.
-__device__ __forceinline__ void prep_stage(uint8_t *stg, const uint8_t *stg_prev, int lane, uint32_t &mag)
+__device__ __forceinline__ void prep_stage(uint8_t *stg, const uint8_t *stg_prev, int lane, uint32_t &mag,
+                                           bool prefix, bool q_is_k)
 {
     const int g = lane >> 2, c4 = lane & 3;
     const int ra = (lane & 7) + ((lane >> 3) & 1) * 8;
     const int rb = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
     for (int tile = 0; tile < 2; ++tile) {
+        if (tile == 1 && q_is_k) break;  // the key tile stands in for the query tile
         const uint4 *src = reinterpret_cast<const uint4 *>(stg + (tile == 0 ? kOffK : kOffQ));
         uint4 *dst = reinterpret_cast<uint4 *>(stg + (tile == 0 ? kOffKh : kOffQh));
 #pragma unroll
@@ -144,7 +149,7 @@ __device__ __forceinline__ void prep_stage(uint8_t *stg, const uint8_t *stg_prev
     }
     __syncwarp();
     // dq[j][r] = q_t . k_s with t = g + 8(r>>1), s = 8j + 2c4 + (r&1)
-    const uint32_t sK = smem_u32(stg + kOffKh), sQ = smem_u32(stg + kOffQh);
+    const uint32_t sK = smem_u32(stg + kOffKh), sQ = smem_u32(stg + (q_is_k ? kOffKh : kOffQh));
     float dq[2][4] = {}, dx[2][4] = {};  // dx[j][r] = k_t . k'_s, t in step i, s in step i-1
 #pragma unroll
     for (int ks = 0; ks < kD / 16; ++ks) {
@@ -165,9 +170,9 @@ __device__ __forceinline__ void prep_stage(uint8_t *stg, const uint8_t *stg_prev
         reinterpret_cast<uint4 *>(stg + kOffKx)[lane] =
             make_uint4(pack_h2(dx[0][0] + 1.f, dx[0][1] + 1.f), pack_h2(dx[1][0] + 1.f, dx[1][1] + 1.f),
                        pack_h2(dx[0][2] + 1.f, dx[0][3] + 1.f), pack_h2(dx[1][2] + 1.f, dx[1][3] + 1.f));
-    auto mq = [&](int j, int r) {
+    auto mq = [&](int j, int r) {  // under the anchor rule no update of the batch is seen
         const int t = g + 8 * (r >> 1), s = 8 * j + 2 * c4 + (r & 1);
-        return s <= t ? dq[j][r] + 1.f : 0.f;
+        return prefix && s <= t ? dq[j][r] + 1.f : 0.f;
     };
     reinterpret_cast<uint4 *>(stg + kOffMq)[lane] =
         make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)), pack_h2(mq(0, 2), mq(0, 3)),
@@ -190,6 +195,7 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
         bet[k] = p.ln_b[hi * kD + 32 * half + k];
     }
     const uint32_t sX2k = smem_u32(sm + kOffX2k), sX2q = smem_u32(sm + kOffX2q);
+    const int offQ = p.q_is_k ? kOffK : kOffQ;  // the key tile stands in for the queries
     const float invD = 1.f / (float)kD, eps = p.eps;
     bool ok = true;
     for (int i = 0; i < nsteps + kPrepLead && ok; ++i) {
@@ -199,18 +205,21 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
                 abort_chain(R.flags, p.status);
                 break;
             }
-            prep_stage(stage_ptr(sm, st), i > 0 ? stage_ptr(sm, (i + kStages - 1) % kStages) : nullptr, lane, mag);
+            prep_stage(stage_ptr(sm, st), i > 0 ? stage_ptr(sm, (i + kStages - 1) % kStages) : nullptr, lane, mag,
+                       p.prefix != 0, p.q_is_k != 0);
             warp_arrive(&R.prep[st], lane);
         }
         if (i < kPrepLead) continue;
         const int j = i - kPrepLead, stj = j % kStages, slot = j & 1;
         uint8_t *stg = stage_ptr(sm, stj);
         // Gram of step j: Mq2[s][t] = (s <= t)(x2q_t . x2k_s + 1) as B fragments (k = s, n = t).
-        if (!wait_bar(R.hq, parity_of(j), R.flags)) {
+        if (!wait_bar(&R.hq[j & 1], parity_of(j >> 1), R.flags)) {
             abort_chain(R.flags, p.status);
             break;
         }
-        {
+        if (!p.prefix) {  // anchor rule: Yq sees no update of the batch
+            reinterpret_cast<uint4 *>(sm + kOffMq2)[lane] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
             const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);
             const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);
             // four k-slices of independent accumulators (the mma latency, not its rate, bounds this)
@@ -268,7 +277,7 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const int chunk = 4 * half + c;  // 8 features per 16-byte chunk
-            const uint4 qb = *reinterpret_cast<const uint4 *>(stg + kOffQ + swz(tl, chunk));
+            const uint4 qb = *reinterpret_cast<const uint4 *>(stg + offQ + swz(tl, chunk));
             const uint4 vb = *reinterpret_cast<const uint4 *>(stg + kOffV + swz(tl, chunk));
             const uint32_t qw[4] = {qb.x, qb.y, qb.z, qb.w}, vw[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
@@ -351,6 +360,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
 {
     const int g = lane >> 2, c4 = lane & 3;
     const int h0 = 32 * w;  // first hidden unit of this warp
+    const int offQh = p.q_is_k ? kOffKh : kOffQh;  // the key tile stands in for the queries
     const float *W10 = p.W1 + bi * p.w_bstride + (long long)hi * kHid * kD;
     const float *c10 = p.c1 + bi * p.c1_bstride + (long long)hi * kHid;
     // W1 rows h0 + 16m + g (+8), columns 8nt + 2c4 (+1)
@@ -439,7 +449,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
     };
     if (nsteps > 0) {
         wait_stage(0);
-        w1_gemm2(smem_u32(stage_ptr(sm, 0) + kOffKh), z1, smem_u32(stage_ptr(sm, 0) + kOffQh), rq, true);
+        w1_gemm2(smem_u32(stage_ptr(sm, 0) + kOffKh), z1, smem_u32(stage_ptr(sm, 0) + offQh), rq, true);
         gelu_x(z1);
         write_x(sX2k, z1);
         named_bar_arrive(kBarX2k, kHY);
@@ -545,7 +555,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
                 for (int r = 0; r < 4; ++r) rq[m][n][r] = gelu1(rq[m][n][r]);
         write_x(sX2q + (uint32_t)((i & 1) * kX2Bytes), rq);
         named_bar_arrive(kBarX2q + (i & 1), kHY);  // also orders W2_{i-1} before the Y warps' Yq_i
-        warp_arrive(R.hq, lane);
+        warp_arrive(&R.hq[i & 1], lane);
         if (w == 0) TTT_TRACE_AT(p, i, 4);
         // W1_i = W1_{i-1} + A~1_i K_i.
 #pragma unroll
@@ -601,7 +611,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
         if (i + 1 < nsteps) {
             const bool two = i + 2 < nsteps;
             if (two) wait_stage(i + 2);
-            w1_gemm2(smem_u32(stage_ptr(sm, (i + 1) % kStages) + kOffQh), rq,
+            w1_gemm2(smem_u32(stage_ptr(sm, (i + 1) % kStages) + offQh), rq,
                      smem_u32(stage_ptr(sm, (i + 2) % kStages) + kOffKh), s1, two);
         }
         if (w == 0) TTT_TRACE_AT(p, i, 7);
@@ -1026,9 +1036,9 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     R.prep = bar + kStages;
     R.empty = bar + 2 * kStages;
     R.hq = bar + 3 * kStages;
-    R.mq2 = R.hq + 1;
-    R.yqfull = R.hq + 2;
-    R.yqempty = R.hq + 4;
+    R.mq2 = R.hq + 2;
+    R.yqfull = R.hq + 3;
+    R.yqempty = R.hq + 5;
     R.flags = reinterpret_cast<volatile int *>(bar + kNumBars);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffTmem);
 
@@ -1042,7 +1052,8 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(&R.prep[s], 1);
             mbar_init(&R.empty[s], kNH + kNY + 1);  // H warps, Y warps, P
         }
-        mbar_init(R.hq, kNH);
+        mbar_init(&R.hq[0], kNH);
+        mbar_init(&R.hq[1], kNH);
         mbar_init(R.mq2, 1);
         for (int j = 0; j < 2; ++j) {
             mbar_init(&R.yqfull[j], kNY);
@@ -1063,7 +1074,7 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tmem_fence_after_sync();
 
     if (warp == kWarpL) {
-        const StageGeom geom{kStages, kStageBytes, kOffK, kOffQ, kOffV, kOffEta};
+        const StageGeom geom{kStages, kStageBytes, kOffK, p.q_is_k ? -1 : kOffQ, kOffV, kOffEta};
         role_loader<kD>(&tmQ, &tmK, &tmV, p.eta + tok0, p.T, p.status, sm + kOffStages, geom, R.full, R.empty,
                         R.flags, chain, lane, nsteps);
     } else if (warp == kWarpP) {

@@ -32,37 +32,39 @@ def dev(inp: dict) -> dict:
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def run_linear(inp: dict, *, status=True, out=None, z_dtype=torch.float32):
+def run_linear(inp: dict, *, status=True, out=None, z_dtype=torch.float32, rule="prefix", q_none=False):
     d = dev(inp)
     st = torch.zeros(1, dtype=torch.int32, device="cuda") if status else None
-    o = ttt.ttt_linear_forward(d["Q"], d["K"], d["V"], d["eta"], d["W0"], d["c0"], d["ln_g"], d["ln_b"],
-                               mb=inp["b"], eps=inp["eps"], status=st, out=out, z_dtype=z_dtype)
+    o = ttt.ttt_linear_forward(None if q_none else d["Q"], d["K"], d["V"], d["eta"], d["W0"], d["c0"],
+                               d["ln_g"], d["ln_b"], mb=inp["b"], eps=inp["eps"], status=st, out=out,
+                               z_dtype=z_dtype, out_rule=rule)
     torch.cuda.synchronize()
     o["status"] = st
     return o
 
 
-def run_mlp(inp: dict, *, status=True, z_dtype=torch.float32):
+def run_mlp(inp: dict, *, status=True, z_dtype=torch.float32, rule="prefix", q_none=False):
     d = dev(inp)
     st = torch.zeros(1, dtype=torch.int32, device="cuda") if status else None
-    o = ttt.ttt_mlp_forward(d["Q"], d["K"], d["V"], d["eta"], d["W1"], d["c1"], d["W2"], d["c2"],
-                            d["ln_g"], d["ln_b"], mb=inp["b"], eps=inp["eps"], status=st, z_dtype=z_dtype)
+    o = ttt.ttt_mlp_forward(None if q_none else d["Q"], d["K"], d["V"], d["eta"], d["W1"], d["c1"], d["W2"],
+                            d["c2"], d["ln_g"], d["ln_b"], mb=inp["b"], eps=inp["eps"], status=st,
+                            z_dtype=z_dtype, out_rule=rule)
     torch.cuda.synchronize()
     o["status"] = st
     return o
 
 
-def oracle_linear(inp: dict, nthreads: int = 0) -> dict:
+def oracle_linear(inp: dict, nthreads: int = 0, rule: str = "prefix") -> dict:
     return oracle.ttt_linear(to_np(inp["Q"]), to_np(inp["K"]), to_np(inp["V"]), to_np(inp["eta"]),
                              to_np(inp["W0"]), to_np(inp["c0"]), to_np(inp["ln_g"]), to_np(inp["ln_b"]),
-                             b=inp["b"], eps=inp["eps"], nthreads=nthreads)
+                             b=inp["b"], eps=inp["eps"], nthreads=nthreads, rule=rule)
 
 
-def oracle_mlp(inp: dict, nthreads: int = 0) -> dict:
+def oracle_mlp(inp: dict, nthreads: int = 0, rule: str = "prefix") -> dict:
     return oracle.ttt_mlp(to_np(inp["Q"]), to_np(inp["K"]), to_np(inp["V"]), to_np(inp["eta"]),
                           to_np(inp["W1"]), to_np(inp["c1"]), to_np(inp["W2"]), to_np(inp["c2"]),
                           to_np(inp["ln_g"]), to_np(inp["ln_b"]), b=inp["b"], eps=inp["eps"],
-                          nthreads=nthreads)
+                          nthreads=nthreads, rule=rule)
 
 
 def compare(got: dict, ref: dict, keys, tol: float, sel=None) -> dict:

@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_strings(L):
-    assert ttt.abi_version() == 1
+    assert ttt.abi_version() == 2
     for code in ttt.STATUS:
         assert len(ttt.status_string(code)) > 0
     assert ttt.status_string(999) == "unknown status"
@@ -119,6 +119,11 @@ def test_validation_codes(L):
     assert _call(L, _linear(loss=(1 << 40) + (1 << 32) * 12)) == 9  # loss over inner_loss
     # well-formed, but the pointers are not device memory (no device here)
     assert _call(L, _linear()) == 5
+    # output rule: out of range -> unsupported; Q may be NULL only under the key rule
+    assert _call(L, _linear(out_rule=3)) == 3
+    assert _call(L, _linear(out_rule=-1)) == 3
+    assert _call(L, _linear(Q=None, out_rule=1)) == 1
+    assert _call(L, _linear(Q=None, out_rule=2)) == 5
 
 
 def test_validation_codes_mlp(L):
@@ -141,3 +146,6 @@ def test_validation_codes_mlp(L):
     assert call(c2_0=base + 7 * step + 4) == 4
     assert call(W1_out=base + 5 * step) == 9
     assert call() == 5
+    assert call(out_rule=7) == 3
+    assert call(Q=None, out_rule=0) == 1
+    assert call(Q=None, out_rule=2) == 5
