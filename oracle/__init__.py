@@ -59,12 +59,12 @@ def _load():
             lib = ctypes.CDLL(_LIB)
             lib.oracle_ttt_linear.restype = None
             lib.oracle_ttt_linear.argtypes = (
-                [ctypes.c_int] * 7 + [_dp] * 6 + [ctypes.c_long] * 2 + [_dp] * 2
+                [ctypes.c_int] * 8 + [_dp] * 6 + [ctypes.c_long] * 2 + [_dp] * 2
                 + [ctypes.c_double] + [_dp] * 5 + [ctypes.c_int]
             )
             lib.oracle_ttt_mlp.restype = None
             lib.oracle_ttt_mlp.argtypes = (
-                [ctypes.c_int] * 8 + [_dp] * 8 + [ctypes.c_long] * 3 + [_dp] * 2
+                [ctypes.c_int] * 9 + [_dp] * 8 + [ctypes.c_long] * 3 + [_dp] * 2
                 + [ctypes.c_double] + [_dp] * 7 + [ctypes.c_int]
             )
             lib.oracle_linear_token_grad.restype = ctypes.c_double
@@ -110,7 +110,8 @@ def _init_stride(a, B, per):
     return per
 
 
-def ttt_linear(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nthreads=0, rule="prefix"):
+def ttt_linear(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nthreads=0, rule="prefix",
+               partial_tail=False):
     """TTT-Linear primal token loop in fp64.
 
     Q, K, V [B,H,T,d]; eta [B,H,T]; W0 [B|1,H,d,d] (f_res(x) = W x + c);
@@ -118,12 +119,14 @@ def ttt_linear(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nt
     Returns a dict with Z [B,H,T,d], W, c (final state), loss (L_t =
     ||z_t - v_t||^2) and inner_loss (l_t at the mini-batch anchor W_{i-1}).
     ``rule``: "prefix" z_t = f(q_t; W_t), "anchor" f(q_t; W_{i-1}), "key"
-    f(k_t; W_{i-1}) (Q is then not read and may be None)."""
+    f(k_t; W_{i-1}) (Q is then not read and may be None). With ``partial_tail``
+    T need not be a multiple of b: the last T % b tokens are emitted but not
+    committed (the final state is the one after the last full mini-batch)."""
     if Q is None:
         Q = K
     Q, K, V, eta, W0, c0, ln_g, ln_b = map(_f64, (Q, K, V, eta, W0, c0, ln_g, ln_b))
     B, H, T, d = Q.shape
-    if T % b:
+    if T % b and not partial_tail:
         raise ValueError("T must be a multiple of the mini-batch size b")
     Z = np.empty_like(Q)
     W = np.empty((B, H, d, d))
@@ -131,7 +134,8 @@ def ttt_linear(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nt
     loss = np.empty((B, H, T))
     inner = np.empty((B, H, T))
     _load().oracle_ttt_linear(
-        B, H, T, d, b, int(bool(ln_res)), _rule(rule), _p(Q), _p(K), _p(V), _p(eta), _p(W0), _p(c0),
+        B, H, T, d, b, int(bool(ln_res)), _rule(rule), int(bool(partial_tail)), _p(Q), _p(K), _p(V), _p(eta),
+        _p(W0), _p(c0),
         _init_stride(W0, B, H * d * d), _init_stride(c0, B, H * d), _p(ln_g), _p(ln_b),
         float(eps), _p(Z), _p(W), _p(c), _p(loss), _p(inner), int(nthreads),
     )
@@ -139,7 +143,7 @@ def ttt_linear(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nt
 
 
 def ttt_mlp(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nthreads=0,
-            rule="prefix"):
+            rule="prefix", partial_tail=False):
     """TTT-MLP primal token loop in fp64; f_res(x) = W2 gelu_tanh(W1 x + c1) + c2.
 
     W1 [B|1,H,h,d], c1 [B|1,H,h], W2 [B|1,H,d,h], c2 [B|1,H,d]; ``rule`` as
@@ -149,7 +153,7 @@ def ttt_mlp(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_res=Tru
     Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b = map(_f64, (Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b))
     B, H, T, d = Q.shape
     h = W1.shape[-2]
-    if T % b:
+    if T % b and not partial_tail:
         raise ValueError("T must be a multiple of the mini-batch size b")
     if W1.shape[0] != W2.shape[0]:
         raise ValueError("W1 and W2 must share their leading dim")
@@ -161,7 +165,8 @@ def ttt_mlp(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_res=Tru
     loss = np.empty((B, H, T))
     inner = np.empty((B, H, T))
     _load().oracle_ttt_mlp(
-        B, H, T, d, h, b, int(bool(ln_res)), _rule(rule), _p(Q), _p(K), _p(V), _p(eta), _p(W1), _p(c1),
+        B, H, T, d, h, b, int(bool(ln_res)), _rule(rule), int(bool(partial_tail)), _p(Q), _p(K), _p(V), _p(eta),
+        _p(W1), _p(c1),
         _p(W2), _p(c2), _init_stride(W1, B, H * h * d), _init_stride(c1, B, H * h),
         _init_stride(c2, B, H * d), _p(ln_g), _p(ln_b), float(eps), _p(Z), _p(W1o), _p(c1o),
         _p(W2o), _p(c2o), _p(loss), _p(inner), int(nthreads),

@@ -26,6 +26,9 @@ Output rules: "prefix" is the form above. "anchor" (every prediction of a
 mini-batch made with the weights before it, review section 2.3) drops A:
 Yq = Q W^T + 1 c^T. "key" (the review's simplified output rule, Eq. 9) is the
 anchor rule with the keys as queries, so Yq = Y and Z - V = E.
+
+With ``partial_tail`` the last T % b rows form a shorter batch that uses the
+same 1/b and masks but leaves (W, c) at the anchor: it is emitted, not committed.
 """
 from __future__ import annotations
 
@@ -86,7 +89,8 @@ def _queries(Q, K, rule):
     return K if rule == "key" else Q
 
 
-def ttt_linear_dual(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, rule="prefix"):
+def ttt_linear_dual(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, rule="prefix",
+                    partial_tail=False):
     Q = _queries(Q, K, rule)
     Q, K, V, eta = (np.asarray(a, np.float64) for a in (Q, K, V, eta))
     B, H, T, d = Q.shape
@@ -103,24 +107,27 @@ def ttt_linear_dual(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=Tru
             W = W0[bi, hi].copy()
             c = c0[bi, hi].copy()
             g, bt = np.asarray(ln_g[hi], np.float64), np.asarray(ln_b[hi], np.float64)
-            for i in range(T // b):
-                sl = slice(i * b, (i + 1) * b)
+            for i in range(-(-T // b) if partial_tail else T // b):
+                sl = slice(i * b, min((i + 1) * b, T))
                 k, q, v, e = K[bi, hi, sl], Q[bi, hi, sl], V[bi, hi, sl], eta[bi, hi, sl]
+                nb = k.shape[0]
                 l_in, G = _recon(k, k @ W.T + c, v, g, bt, eps, ln_res)
-                A = mask * (q @ k.T + 1.0) * (e / b)[None, :]
+                A = mask[:nb, :nb] * (q @ k.T + 1.0) * (e / b)[None, :]
                 Yq = q @ W.T + c - A @ G
                 z = _out(q, Yq, g, bt, eps, ln_res)
                 Z[bi, hi, sl] = z
                 loss[bi, hi, sl] = ((z - v) ** 2).sum(-1)
                 inner[bi, hi, sl] = l_in
-                Ge = G * (e / b)[:, None]
-                W = W - Ge.T @ k
-                c = c - Ge.sum(0)
+                if nb == b:
+                    Ge = G * (e / b)[:, None]
+                    W = W - Ge.T @ k
+                    c = c - Ge.sum(0)
             Wf[bi, hi], cf[bi, hi] = W, c
     return dict(Z=Z, W=Wf, c=cf, loss=loss, inner_loss=inner)
 
 
-def ttt_mlp_dual(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, rule="prefix"):
+def ttt_mlp_dual(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, rule="prefix",
+                 partial_tail=False):
     Q = _queries(Q, K, rule)
     Q, K, V, eta = (np.asarray(a, np.float64) for a in (Q, K, V, eta))
     B, H, T, d = Q.shape
@@ -137,28 +144,30 @@ def ttt_mlp_dual(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_re
             w1, b1 = W1[bi, hi].copy(), c1[bi, hi].copy()
             w2, b2 = W2[bi, hi].copy(), c2[bi, hi].copy()
             g, bt = np.asarray(ln_g[hi], np.float64), np.asarray(ln_b[hi], np.float64)
-            for i in range(T // b):
-                sl = slice(i * b, (i + 1) * b)
+            for i in range(-(-T // b) if partial_tail else T // b):
+                sl = slice(i * b, min((i + 1) * b, T))
                 k, q, v, e = K[bi, hi, sl], Q[bi, hi, sl], V[bi, hi, sl], eta[bi, hi, sl]
+                nb = k.shape[0]
                 Z1 = k @ w1.T + b1
                 X2 = _gelu(Z1)
                 l_in, G = _recon(k, X2 @ w2.T + b2, v, g, bt, eps, ln_res)
                 G1 = (G @ w2) * _gelu_prime(Z1)
-                A1 = mask * (q @ k.T + 1.0) * (e / b)[None, :]
+                A1 = mask[:nb, :nb] * (q @ k.T + 1.0) * (e / b)[None, :]
                 Z1q = q @ w1.T + b1 - A1 @ G1
                 X2q = _gelu(Z1q)
-                A2 = mask * (X2q @ X2.T + 1.0) * (e / b)[None, :]
+                A2 = mask[:nb, :nb] * (X2q @ X2.T + 1.0) * (e / b)[None, :]
                 Yq = X2q @ w2.T + b2 - A2 @ G
                 z = _out(q, Yq, g, bt, eps, ln_res)
                 Z[bi, hi, sl] = z
                 loss[bi, hi, sl] = ((z - v) ** 2).sum(-1)
                 inner[bi, hi, sl] = l_in
-                Ge = G * (e / b)[:, None]
-                G1e = G1 * (e / b)[:, None]
-                w2 = w2 - Ge.T @ X2
-                b2 = b2 - Ge.sum(0)
-                w1 = w1 - G1e.T @ k
-                b1 = b1 - G1e.sum(0)
+                if nb == b:
+                    Ge = G * (e / b)[:, None]
+                    G1e = G1 * (e / b)[:, None]
+                    w2 = w2 - Ge.T @ X2
+                    b2 = b2 - Ge.sum(0)
+                    w1 = w1 - G1e.T @ k
+                    b1 = b1 - G1e.sum(0)
             out["W1"][bi, hi], out["c1"][bi, hi] = w1, b1
             out["W2"][bi, hi], out["c2"][bi, hi] = w2, b2
     return dict(Z=Z, loss=loss, inner_loss=inner, **out)

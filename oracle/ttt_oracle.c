@@ -35,6 +35,13 @@
  *   - The loss is the squared L2 sum (no 1/d).
  *   - GELU is the tanh form.
  *
+ * Partial last mini-batch (argument `tail`): with tail = 1, T need not be a
+ * multiple of b. The last T % b tokens form a mini-batch that is emitted but not
+ * committed ([E2E-review] section 2.3.2: a gradient step is taken only once the
+ * decoded tokens fill a whole mini-batch): their inner losses and outputs follow
+ * the same rules (same 1/b, in-batch prefix for the prefix rule), and the final
+ * state is the one after the last full mini-batch.
+ *
  * Output rules (argument `rule`; the weight trajectory does not depend on it):
  *   0  prefix: z_t = f(q_t; W_t), the in-batch prefix above ([TTT-survey] Eq. 5).
  *   1  anchor: z_t = f(q_t; W_{i-1}) for every token of batch i: [E2E-review]
@@ -221,7 +228,7 @@ double oracle_mlp_token_grad(int d, int h, int ln_res, const double *W1, const d
 /* ------------------------------------------------------------------ */
 /* TTT-Linear inner loop, primal token form.                            */
 /* ------------------------------------------------------------------ */
-static void linear_chain(int T, int d, int b, int ln_res, int rule, const double *Q, const double *K,
+static void linear_chain(int T, int d, int b, int ln_res, int rule, int tail, const double *Q, const double *K,
                          const double *V, const double *eta, const double *W0,
                          const double *c0, const double *lg, const double *lb, double eps,
                          double *Z, double *W_out, double *c_out, double *loss,
@@ -233,19 +240,20 @@ static void linear_chain(int T, int d, int b, int ln_res, int rule, const double
     double *y = G + (size_t)b * d, *work = y + d, *z = work + 3 * d, *e = z + d;
     memcpy(W, W0, sizeof(double) * dd);
     memcpy(c, c0, sizeof(double) * d);
-    const int n = T / b;
+    const int n = tail ? (T + b - 1) / b : T / b;
     for (int i = 0; i < n; ++i) {
         const int t0 = i * b;
+        const int nb = T - t0 < b ? T - t0 : b; /* tokens in this mini-batch (< b: the uncommitted tail) */
         /* Anchor W_{i-1}: every gradient of mini-batch i is taken here (Eq. 5 of [E2E-review]). */
         memcpy(Wa, W, sizeof(double) * dd);
         memcpy(ca, c, sizeof(double) * d);
-        for (int s = 0; s < b; ++s) {
+        for (int s = 0; s < nb; ++s) {
             const double *k = K + (size_t)(t0 + s) * d, *v = V + (size_t)(t0 + s) * d;
             affine(d, d, Wa, ca, k, y);                                    /* f_res(k; W_{i-1}) */
             double l = recon_loss_and_grad(d, ln_res, k, y, v, lg, lb, eps, G + (size_t)s * d, work);
             if (inner_loss) inner_loss[t0 + s] = l;                        /* Eq. 4 at W_{i-1} */
         }
-        for (int t = 0; t < b; ++t) {
+        for (int t = 0; t < nb; ++t) {
             const double *k = K + (size_t)(t0 + t) * d, *q = Q + (size_t)(t0 + t) * d;
             const double *v = V + (size_t)(t0 + t) * d, *g = G + (size_t)t * d;
             const double s = eta[t0 + t] / b;
@@ -269,13 +277,17 @@ static void linear_chain(int T, int d, int b, int ln_res, int rule, const double
             }
             if (loss) loss[t0 + t] = L; /* L_t of [SR-TTT] */
         }
+        if (nb < b) { /* the partial mini-batch is not committed */
+            memcpy(W, Wa, sizeof(double) * dd);
+            memcpy(c, ca, sizeof(double) * d);
+        }
     }
     if (W_out) memcpy(W_out, W, sizeof(double) * dd);
     if (c_out) memcpy(c_out, c, sizeof(double) * d);
     free(W);
 }
 
-void oracle_ttt_linear(int B, int H, int T, int d, int b, int ln_res, int rule, const double *Q,
+void oracle_ttt_linear(int B, int H, int T, int d, int b, int ln_res, int rule, int tail, const double *Q,
                        const double *K, const double *V, const double *eta, const double *W0,
                        const double *c0, long w0_bstride, long c0_bstride, const double *ln_g,
                        const double *ln_b, double eps, double *Z, double *W_out, double *c_out,
@@ -289,7 +301,7 @@ void oracle_ttt_linear(int B, int H, int T, int d, int b, int ln_res, int rule, 
     for (long ch = 0; ch < chains; ++ch) {
         const long bi = ch / H, hi = ch % H;
         const size_t tok = (size_t)ch * T;
-        linear_chain(T, d, b, ln_res, rule, Q + tok * d, K + tok * d, V + tok * d, eta + tok,
+        linear_chain(T, d, b, ln_res, rule, tail, Q + tok * d, K + tok * d, V + tok * d, eta + tok,
                      W0 + bi * w0_bstride + hi * (size_t)d * d, c0 + bi * c0_bstride + hi * (size_t)d,
                      ln_g + hi * (size_t)d, ln_b + hi * (size_t)d, eps, Z + tok * d,
                      W_out ? W_out + (size_t)ch * d * d : NULL, c_out ? c_out + (size_t)ch * d : NULL,
@@ -301,7 +313,7 @@ void oracle_ttt_linear(int B, int H, int T, int d, int b, int ln_res, int rule, 
 /* TTT-MLP inner loop, primal token form.                               */
 /* f_res(x) = W2 gelu(W1 x + c1) + c2, W1 [h][d], W2 [d][h].            */
 /* ------------------------------------------------------------------ */
-static void mlp_chain(int T, int d, int h, int b, int ln_res, int rule, const double *Q, const double *K,
+static void mlp_chain(int T, int d, int h, int b, int ln_res, int rule, int tail, const double *Q, const double *K,
                       const double *V, const double *eta, const double *W10, const double *c10,
                       const double *W20, const double *c20, const double *lg, const double *lb,
                       double eps, double *Z, double *W1o, double *c1o, double *W2o, double *c2o,
@@ -319,14 +331,15 @@ static void mlp_chain(int T, int d, int h, int b, int ln_res, int rule, const do
     memcpy(W2, W20, sizeof(double) * hd);
     memcpy(c1, c10, sizeof(double) * h);
     memcpy(c2, c20, sizeof(double) * d);
-    const int n = T / b;
+    const int n = tail ? (T + b - 1) / b : T / b;
     for (int i = 0; i < n; ++i) {
         const int t0 = i * b;
+        const int nb = T - t0 < b ? T - t0 : b; /* < b: the uncommitted tail */
         memcpy(W1a, W1, sizeof(double) * hd);
         memcpy(W2a, W2, sizeof(double) * hd);
         memcpy(c1a, c1, sizeof(double) * h);
         memcpy(c2a, c2, sizeof(double) * d);
-        for (int s = 0; s < b; ++s) {
+        for (int s = 0; s < nb; ++s) {
             const double *k = K + (size_t)(t0 + s) * d, *v = V + (size_t)(t0 + s) * d;
             double *g = G + (size_t)s * d, *xs = X2 + (size_t)s * h, *dz = DZ1 + (size_t)s * h;
             affine(h, d, W1a, c1a, k, z1);
@@ -341,7 +354,7 @@ static void mlp_chain(int T, int d, int h, int b, int ln_res, int rule, const do
                 dz[j] = acc * gelu_prime(z1[j]);
             }
         }
-        for (int t = 0; t < b; ++t) {
+        for (int t = 0; t < nb; ++t) {
             const double *k = K + (size_t)(t0 + t) * d, *q = Q + (size_t)(t0 + t) * d;
             const double *v = V + (size_t)(t0 + t) * d;
             const double *g = G + (size_t)t * d, *xs = X2 + (size_t)t * h, *dz = DZ1 + (size_t)t * h;
@@ -368,6 +381,12 @@ static void mlp_chain(int T, int d, int h, int b, int ln_res, int rule, const do
             }
             if (loss) loss[t0 + t] = L;
         }
+        if (nb < b) { /* the partial mini-batch is not committed */
+            memcpy(W1, W1a, sizeof(double) * hd);
+            memcpy(W2, W2a, sizeof(double) * hd);
+            memcpy(c1, c1a, sizeof(double) * h);
+            memcpy(c2, c2a, sizeof(double) * d);
+        }
     }
     if (W1o) memcpy(W1o, W1, sizeof(double) * hd);
     if (c1o) memcpy(c1o, c1, sizeof(double) * h);
@@ -376,7 +395,7 @@ static void mlp_chain(int T, int d, int h, int b, int ln_res, int rule, const do
     free(W1);
 }
 
-void oracle_ttt_mlp(int B, int H, int T, int d, int h, int b, int ln_res, int rule, const double *Q,
+void oracle_ttt_mlp(int B, int H, int T, int d, int h, int b, int ln_res, int rule, int tail, const double *Q,
                     const double *K, const double *V, const double *eta, const double *W10,
                     const double *c10, const double *W20, const double *c20, long w_bstride,
                     long c1_bstride, long c2_bstride, const double *ln_g, const double *ln_b,
@@ -392,7 +411,7 @@ void oracle_ttt_mlp(int B, int H, int T, int d, int h, int b, int ln_res, int ru
     for (long ch = 0; ch < chains; ++ch) {
         const long bi = ch / H, hi = ch % H;
         const size_t tok = (size_t)ch * T;
-        mlp_chain(T, d, h, b, ln_res, rule, Q + tok * d, K + tok * d, V + tok * d, eta + tok,
+        mlp_chain(T, d, h, b, ln_res, rule, tail, Q + tok * d, K + tok * d, V + tok * d, eta + tok,
                   W10 + bi * w_bstride + hi * hd, c10 + bi * c1_bstride + hi * (size_t)h,
                   W20 + bi * w_bstride + hi * hd, c20 + bi * c2_bstride + hi * (size_t)d,
                   ln_g + hi * (size_t)d, ln_b + hi * (size_t)d, eps, Z + tok * d,

@@ -484,3 +484,70 @@ def test_primal_equals_dual_output_rules(rule, b):
     dm = dual.ttt_mlp_dual(*args, b=4, rule=rule)
     for f in pm:
         np.testing.assert_allclose(dm[f], pm[f], rtol=1e-11, atol=1e-11)
+
+
+# ---------------------------------------------------------------- partial last mini-batch
+# A final mini-batch of T % b < b tokens is emitted but not committed (the E2E
+# review's section 2.3.2: a gradient step only once the decoded tokens fill a
+# mini-batch). Pins: its outputs and losses equal the first rows of the same
+# batch completed later (causality of every rule); the state equals the state
+# of the committed prefix alone; committing later through the resume path gives
+# the single-call result; with T < b the anchor output is the library forward at W_0.
+
+@pytest.mark.parametrize("rule", ["prefix", "anchor", "key"])
+@pytest.mark.parametrize("b,T", [(4, 14), (8, 5), (16, 37)])
+def test_partial_tail_linear(rule, b, T):
+    rng = np.random.default_rng(60 + b + T)
+    Q, K, V, eta, W0, c0, g, bt = _rand_linear(rng, T=-(-T // b) * b, d=8)
+    tc = (T // b) * b
+    full = oracle.ttt_linear(Q, K, V, eta, W0, c0, g, bt, b=b, rule=rule)
+    part = oracle.ttt_linear(Q[:, :, :T], K[:, :, :T], V[:, :, :T], eta[:, :, :T], W0, c0, g, bt, b=b, rule=rule,
+                             partial_tail=True)
+    for f in ("Z", "loss", "inner_loss"):
+        np.testing.assert_array_equal(part[f], full[f][:, :, :T])
+    if tc:
+        pre = oracle.ttt_linear(Q[:, :, :tc], K[:, :, :tc], V[:, :, :tc], eta[:, :, :tc], W0, c0, g, bt, b=b,
+                                rule=rule)
+        np.testing.assert_array_equal(part["W"], pre["W"])
+        np.testing.assert_array_equal(part["c"], pre["c"])
+    else:
+        np.testing.assert_array_equal(part["W"], np.broadcast_to(W0, part["W"].shape))
+    # commit later: resume from the returned state with the completed batch
+    rest = oracle.ttt_linear(Q[:, :, tc:], K[:, :, tc:], V[:, :, tc:], eta[:, :, tc:], part["W"], part["c"], g, bt,
+                             b=b, rule=rule)
+    np.testing.assert_array_equal(rest["W"], full["W"])
+    np.testing.assert_array_equal(rest["Z"], full["Z"][:, :, tc:])
+    d = dual.ttt_linear_dual(Q[:, :, :T], K[:, :, :T], V[:, :, :T], eta[:, :, :T], W0, c0, g, bt, b=b, rule=rule,
+                             partial_tail=True)
+    for f in part:
+        np.testing.assert_allclose(d[f], part[f], rtol=1e-11, atol=1e-11)
+
+
+def test_partial_only_batch_anchor_is_library_forward():
+    rng = np.random.default_rng(70)
+    Q, K, V, eta, W0, c0, g, bt = _rand_linear(rng, B=1, H=2, T=5, d=6)
+    r = oracle.ttt_linear(Q, K, V, eta, W0, c0, g, bt, b=16, rule="anchor", partial_tail=True)
+    for hi in range(2):
+        for t in range(5):
+            z = _torch_f_linear(torch.tensor(W0[0, hi]), torch.tensor(c0[0, hi]), torch.tensor(Q[0, hi, t]),
+                                torch.tensor(g[hi]), torch.tensor(bt[hi]), 1e-6, True).numpy()
+            np.testing.assert_allclose(r["Z"][0, hi, t], z, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(r["W"][0], W0[0])
+
+
+@pytest.mark.parametrize("rule", ["prefix", "anchor"])
+def test_partial_tail_mlp(rule):
+    rng = np.random.default_rng(71)
+    args = list(_rand_mlp(rng, T=12))
+    b, T = 4, 10
+    full = oracle.ttt_mlp(*args, b=b, rule=rule)
+    cut = [a[:, :, :T] for a in args[:4]] + args[4:]
+    part = oracle.ttt_mlp(*cut, b=b, rule=rule, partial_tail=True)
+    for f in ("Z", "loss", "inner_loss"):
+        np.testing.assert_array_equal(part[f], full[f][:, :, :T])
+    pre = oracle.ttt_mlp(*([a[:, :, :8] for a in args[:4]] + args[4:]), b=b, rule=rule)
+    for f in ("W1", "c1", "W2", "c2"):
+        np.testing.assert_array_equal(part[f], pre[f])
+    dm = dual.ttt_mlp_dual(*cut, b=b, rule=rule, partial_tail=True)
+    for f in part:
+        np.testing.assert_allclose(dm[f], part[f], rtol=1e-11, atol=1e-11)
