@@ -195,11 +195,11 @@ def oracle_sample(w, n_chains: int, T: int, nthreads: int = 0, rule: str = "pref
     if w.variant == "linear":
         oracle.ttt_linear(f(inp["Q"]), f(inp["K"]), f(inp["V"]), f(inp["eta"]), f(inp["W0"]),
                           f(inp["c0"]), f(inp["ln_g"]), f(inp["ln_b"]), b=w.b, eps=w.eps,
-                          nthreads=th, rule=rule)
+                          nthreads=th, rule=rule, partial_tail=w.partial_tail)
     else:
         oracle.ttt_mlp(f(inp["Q"]), f(inp["K"]), f(inp["V"]), f(inp["eta"]), f(inp["W1"]), f(inp["c1"]),
                        f(inp["W2"]), f(inp["c2"]), f(inp["ln_g"]), f(inp["ln_b"]), b=w.b, eps=w.eps,
-                       nthreads=th, rule=rule)
+                       nthreads=th, rule=rule, partial_tail=w.partial_tail)
     dt = time.perf_counter() - t0
     return dt, n_chains * T, th
 
@@ -244,12 +244,14 @@ def run_gpu(args):
     if w.variant == "linear":
         call = lambda o: ttt.ttt_linear_forward(q_in, dev["K"], dev["V"], dev["eta"], dev["W0"], dev["c0"],
                                                 dev["ln_g"], dev["ln_b"], mb=w.b, eps=w.eps, out=o,
-                                                status=st, stream=stream, out_rule=rule)
+                                                status=st, stream=stream, out_rule=rule,
+                                                partial_tail=w.partial_tail)
         kind = ttt.linear_kernel_kind(ttt.BF16 if w.io == "bf16" else ttt.F32, w.d, w.b)
     else:
         call = lambda o: ttt.ttt_mlp_forward(q_in, dev["K"], dev["V"], dev["eta"], dev["W1"], dev["c1"],
                                              dev["W2"], dev["c2"], dev["ln_g"], dev["ln_b"], mb=w.b, eps=w.eps,
-                                             out=o, status=st, stream=stream, out_rule=rule)
+                                             out=o, status=st, stream=stream, out_rule=rule,
+                                             partial_tail=w.partial_tail)
         kind = ttt.mlp_kernel_kind(ttt.BF16 if w.io == "bf16" else ttt.F32, w.d, w.hidden, w.b)
     out = call(out)                       # allocates outputs once
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -335,7 +337,7 @@ def run_gpu(args):
         "data": "synthetic (seeded Gaussian Q/K/V, sigmoid-gated eta, N(0,0.02^2) W0)",
         "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
                    "mb": w.b, "hidden": w.hidden or None, "io": w.io, "z_dtype": args.z_dtype,
-                   "out_rule": rule, "kernel_kind": kind,
+                   "out_rule": rule, "partial_tail": w.partial_tail, "kernel_kind": kind,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak,

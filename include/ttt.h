@@ -63,12 +63,13 @@
 extern "C" {
 #endif
 
-#define TTT_ABI_VERSION 2
+#define TTT_ABI_VERSION 3
 
 typedef enum {
     TTT_OK = 0,
     TTT_ERR_NULL = 1,            /* a required pointer is NULL                       */
-    TTT_ERR_SHAPE = 2,           /* B,H,T,d,mb,hidden out of range or T % mb != 0    */
+    TTT_ERR_SHAPE = 2,           /* B,H,T,d,mb,hidden out of range, or T % mb != 0   */
+                                 /* without partial_tail                            */
     TTT_ERR_UNSUPPORTED = 3,     /* no kernel for (io, d, mb, hidden), or bad rule   */
     TTT_ERR_ALIGN = 4,           /* a pointer is not 16-byte aligned                 */
     TTT_ERR_NOT_DEVICE_PTR = 5,  /* a pointer is not device-accessible memory        */
@@ -98,12 +99,23 @@ typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
  *                  W_{t-1}, exactly as Eq. 9 writes it. */
 typedef enum { TTT_OUT_PREFIX = 0, TTT_OUT_ANCHOR = 1, TTT_OUT_KEY = 2 } ttt_out_rule;
 
+/* Partial last mini-batch (decode / chunked prefill). With partial_tail = 0, T
+ * must be a multiple of mb. With partial_tail = 1 it need not be: the last
+ * r = T % mb tokens form a mini-batch that is emitted but not committed, as in
+ * section 2.3.2 of the "End-to-End Test-Time Training for Long Context" review
+ * (a gradient step is taken only once the decoded tokens fill a mini-batch).
+ * Their Z, loss and inner_loss follow out_rule with the same 1/mb and the same
+ * in-batch masks, so they equal the first r rows the completed batch will give
+ * (bit for bit on the tensor-core kernels); W_out/c_out hold the state after
+ * the last full mini-batch. Committing later is a resume: call again from
+ * W_out/c_out with the completed mini-batch. */
+
 /* ---------------------------------------------------------------------- */
 /* TTT-Linear                                                              */
 /* ---------------------------------------------------------------------- */
 typedef struct {
     int32_t B, H, T, d;      /* sequences, heads, tokens per chain, head dim   */
-    int32_t mb;              /* mini-batch size b; T % mb == 0                 */
+    int32_t mb;              /* mini-batch size b (see partial_tail)           */
     int32_t io;              /* ttt_dtype of Q, K and V                        */
     int32_t z_io;            /* ttt_dtype of Z (TTT_F32 or TTT_BF16)           */
     float ln_eps;            /* LayerNorm epsilon (1e-6 on the pages' configs) */
@@ -122,6 +134,7 @@ typedef struct {
     float *inner_loss;       /* [B][H][T] l_t(W_{i-1}) at the anchor, or NULL  */
     int32_t *status_dev;     /* device int32 (0 on entry), or NULL             */
     int32_t out_rule;        /* ttt_out_rule; 0 = TTT_OUT_PREFIX               */
+    int32_t partial_tail;    /* 1: T % mb tokens at the end, not committed     */
 } ttt_linear_args;
 
 /* Supported: io = TTT_F32 or TTT_BF16 with 1 <= d <= 128, 1 <= mb <= 64 and
@@ -155,6 +168,7 @@ typedef struct {
     float *loss, *inner_loss;
     int32_t *status_dev;
     int32_t out_rule;        /* ttt_out_rule, as for TTT-Linear               */
+    int32_t partial_tail;    /* as for TTT-Linear                             */
 } ttt_mlp_args;
 
 /* Supported: io = TTT_F32 or TTT_BF16 with d <= 256, hidden <= 1024,

@@ -38,12 +38,13 @@ size_t init_bytes(int B, int H, size_t per, int64_t bstride)
     return ((size_t)(B - 1) * (size_t)bstride + (size_t)H * per) * sizeof(float);
 }
 
-bool dims_ok(int B, int H, int T, int d, int mb)
+bool dims_ok(int B, int H, int T, int d, int mb, int partial_tail)
 {
     if (B < 1 || H < 1 || T < 1 || d < 1 || mb < 1) return false;
     if ((int64_t)B * H > INT32_MAX) return false;
     if (T > (1 << 30) || d > 4096) return false;
-    return T % mb == 0;
+    if (partial_tail != 0 && partial_tail != 1) return false;
+    return partial_tail || T % mb == 0;
 }
 
 #ifdef TTT_TRACE
@@ -101,7 +102,7 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     const void *Qe = a->out_rule == TTT_OUT_KEY ? a->K : a->Q;
     if (!Qe || !a->K || !a->V || !a->eta || !a->W0 || !a->c0 || !a->ln_g || !a->ln_b || !a->Z)
         return TTT_ERR_NULL;
-    if (!dims_ok(a->B, a->H, a->T, a->d, a->mb)) return TTT_ERR_SHAPE;
+    if (!dims_ok(a->B, a->H, a->T, a->d, a->mb, a->partial_tail)) return TTT_ERR_SHAPE;
     if (a->io != TTT_F32 && a->io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
     if (a->z_io != TTT_F32 && a->z_io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
     if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
@@ -150,6 +151,7 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     p.eps = a->ln_eps;
     p.prefix = a->out_rule == TTT_OUT_PREFIX;
     p.q_is_k = a->out_rule == TTT_OUT_KEY;
+    p.t_commit = a->T - a->T % a->mb;  // tokens whose updates are committed
     p.Q = Qe;
     p.K = a->K;
     p.V = a->V;
@@ -185,7 +187,8 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     if (!Qe || !a->K || !a->V || !a->eta || !a->W1_0 || !a->c1_0 || !a->W2_0 || !a->c2_0 || !a->ln_g ||
         !a->ln_b || !a->Z)
         return TTT_ERR_NULL;
-    if (!dims_ok(a->B, a->H, a->T, a->d, a->mb) || a->hidden < 1 || a->hidden > 4096) return TTT_ERR_SHAPE;
+    if (!dims_ok(a->B, a->H, a->T, a->d, a->mb, a->partial_tail) || a->hidden < 1 || a->hidden > 4096)
+        return TTT_ERR_SHAPE;
     if (a->io != TTT_F32 && a->io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
     if (a->z_io != TTT_F32 && a->z_io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
     if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
@@ -241,6 +244,7 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     p.eps = a->ln_eps;
     p.prefix = a->out_rule == TTT_OUT_PREFIX;
     p.q_is_k = a->out_rule == TTT_OUT_KEY;
+    p.t_commit = a->T - a->T % a->mb;  // tokens whose updates are committed
     p.Q = Qe;
     p.K = a->K;
     p.V = a->V;

@@ -66,6 +66,28 @@ __device__ __forceinline__ float col_sum(float v)
 
 __device__ __forceinline__ float round_h(float v) { return __half2float(__float2half_rn(v)); }
 
+// Tokens of a super-step that are committed: the partial last mini-batch (from
+// token t_commit on) is emitted but its update is not applied.
+__device__ __forceinline__ int committed_in_step(int t_commit, int step)
+{
+    const int n = t_commit - step * kSS;
+    return n < 0 ? 0 : (n > kSS ? kSS : n);
+}
+
+// Zero the token columns t >= tc of an m16n8k16 A fragment whose k axis is the
+// 16 tokens of a super-step (a0/a1: tokens 2c4, 2c4+1; a2/a3: 8 + 2c4, 9 + 2c4).
+__device__ __forceinline__ void mask_tokens(uint32_t (&a)[4], int tc, int lane)
+{
+    if (tc >= kSS) return;
+    const int t = 2 * (lane & 3);
+    const uint32_t lo = (t < tc ? 0x0000ffffu : 0u) | (t + 1 < tc ? 0xffff0000u : 0u);
+    const uint32_t hi = (t + 8 < tc ? 0x0000ffffu : 0u) | (t + 9 < tc ? 0xffff0000u : 0u);
+    a[0] &= lo;
+    a[1] &= lo;
+    a[2] &= hi;
+    a[3] &= hi;
+}
+
 // Two bf16 values (one 32-bit word) -> fp16x2, round to nearest even.
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w)
 {

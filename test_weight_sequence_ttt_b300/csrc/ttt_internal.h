@@ -35,6 +35,7 @@ struct LinearParams {
     int z_f32;   // Z element type: 1 = fp32, 0 = bf16
     int prefix;  // 1: z_t with the in-batch prefix W_t; 0: with the anchor W_{i-1}
     int q_is_k;  // 1: the queries are the keys (no query tile is loaded)
+    int t_commit;  // tokens [0, t_commit) are committed; a partial last mini-batch after them is not
     float eps;
     const void *Q, *K, *V;
     const float *eta;
@@ -52,6 +53,7 @@ struct MlpParams {
     int z_f32;
     int prefix;  // as for LinearParams
     int q_is_k;
+    int t_commit;
     float eps;
     const void *Q, *K, *V;
     const float *eta;

@@ -81,13 +81,16 @@ __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
     for (int j = tid; j < d; j += kThreads) c[j] = c0[j];
 
     for (int t0 = 0; t0 < T; t0 += b) {
+        // nb < b only for a partial last mini-batch: its rows past T are zero
+        // (eta 0: no gradient), its outputs are stored, its update is not applied.
+        const int nb = T - t0 < b ? T - t0 : b;
         __syncthreads();
         for (int idx = tid; idx < b * d; idx += kThreads) {
             const size_t g = (size_t)t0 * d + idx;
-            Kt[idx] = ld_io<IO>(Kg + g);
-            Qt[idx] = ld_io<IO>(Qg + g);
+            Kt[idx] = idx < nb * d ? ld_io<IO>(Kg + g) : 0.f;
+            Qt[idx] = idx < nb * d ? ld_io<IO>(Qg + g) : 0.f;
         }
-        for (int s = tid; s < b; s += kThreads) et[s] = eg[t0 + s];
+        for (int s = tid; s < b; s += kThreads) et[s] = s < nb ? eg[t0 + s] : 0.f;
         __syncthreads();
         // Y = K W^T + c  (keys at the anchor W_{i-1})
         for (int idx = tid; idx < b * d; idx += kThreads) {
@@ -111,7 +114,7 @@ __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
             float l = 0.f, m1 = 0.f, m2 = 0.f;
             for (int j = lane; j < d; j += 32) {
                 const float yh = (y[j] - mu) * rstd;
-                const float e = Kt[s * d + j] + lg[j] * yh + lb[j] - ld_io<IO>(Vg + (size_t)(t0 + s) * d + j);
+                const float e = Kt[s * d + j] + lg[j] * yh + lb[j] - (s < nb ? ld_io<IO>(Vg + (size_t)(t0 + s) * d + j) : 0.f);
                 const float dh = 2.f * e * lg[j];
                 l += e * e;
                 m1 += dh;
@@ -122,11 +125,11 @@ __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
             m2 = warp_sum(m2) * inv_d;
             for (int j = lane; j < d; j += 32) {
                 const float yh = (y[j] - mu) * rstd;
-                const float e = Kt[s * d + j] + lg[j] * yh + lb[j] - ld_io<IO>(Vg + (size_t)(t0 + s) * d + j);
+                const float e = Kt[s * d + j] + lg[j] * yh + lb[j] - (s < nb ? ld_io<IO>(Vg + (size_t)(t0 + s) * d + j) : 0.f);
                 const float dh = 2.f * e * lg[j];
                 G[s * d + j] = rstd * (dh - m1 - yh * m2);
             }
-            if (lane == 0 && p.inner_loss) p.inner_loss[tok0 + t0 + s] = l;
+            if (lane == 0 && p.inner_loss && s < nb) p.inner_loss[tok0 + t0 + s] = l;
         }
         // A[t][s] = (eta_s / b)(q_t . k_s + 1), s <= t
         for (int idx = tid; idx < b * b; idx += kThreads) {
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
         }
         __syncthreads();
         // Z = Q + LN(Yq), L_t = ||z_t - v_t||^2
-        for (int t = warp; t < b; t += kWarps) {
+        for (int t = warp; t < nb; t += kWarps) {
             const float *y = Yq + t * d;
             float mu = 0.f;
             for (int j = lane; j < d; j += 32) mu += y[j];
@@ -172,6 +175,7 @@ __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
             if (lane == 0 && p.loss) p.loss[tok0 + t0 + t] = L;
         }
         // W -= (1/b) G^T diag(eta) K ; c -= (1/b) G^T eta   (W_{i-1} -> W_i)
+        if (nb < b) continue;  // the partial last mini-batch is not committed
         for (int idx = tid; idx < d * d; idx += kThreads) {
             const int j = idx / d, i = idx - j * d;
             float acc = 0.f;

@@ -644,19 +644,24 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
             mma16816(yk[0], af, kx.x, kx.y);
             mma16816(yk[1], af, kx.z, kx.w);
         }
-        // W += A~ K_i, c += A~ 1   (W_{i-1} -> W_i for this warp's rows)
+        // W += A~ K_i, c += A~ 1   (W_{i-1} -> W_i for this warp's rows), over the
+        // committed tokens (all of them unless a partial last mini-batch ends here).
+        const int tcm = committed_in_step(p.t_commit, i);
         {
+            uint32_t au[4] = {af[0], af[1], af[2], af[3]};
+            mask_tokens(au, tcm, lane);
             const uint32_t sK = smem_u32(stg + C::kOffKh);
 #pragma unroll
             for (int j = 0; j < MT; ++j) {
                 uint32_t bt[4];
                 ldsm_x4_t(bt, sK + swz(rt, 2 * j + ct));
-                mma16816(Wa[2 * j], af, bt[0], bt[1]);
-                mma16816(Wa[2 * j + 1], af, bt[2], bt[3]);
+                mma16816(Wa[2 * j], au, bt[0], bt[1]);
+                mma16816(Wa[2 * j + 1], au, bt[2], bt[3]);
             }
         }
-        float s0 = at[0][0] + at[0][1] + at[1][0] + at[1][1];
-        float s1r = at[0][2] + at[0][3] + at[1][2] + at[1][3];
+        auto atc = [&](int nt, int r) { return 8 * nt + 2 * c4 + (r & 1) < tcm ? at[nt][r] : 0.f; };
+        float s0 = atc(0, 0) + atc(0, 1) + atc(1, 0) + atc(1, 1);
+        float s1r = atc(0, 2) + atc(0, 3) + atc(1, 2) + atc(1, 3);
         s0 += __shfl_xor_sync(kFull, s0, 1);
         s0 += __shfl_xor_sync(kFull, s0, 2);
         s1r += __shfl_xor_sync(kFull, s1r, 1);
@@ -747,13 +752,42 @@ __device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &
     const int rt = (lane & 7) + ((lane >> 3) & 1) * 8, ct = lane >> 4;
     const float invD = 1.f / (float)D, eps = p.eps;
     const int T = p.T;
-    const int nmb = nsteps / NB;
+    // Final state: written once, after the last committed mini-batch (a partial
+    // last mini-batch still runs its blocks' updates for its own outputs).
+    auto write_state = [&]() {
+        bool badv = !isfinite(cb[0]) || !isfinite(cb[1]);
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) badv |= !isfinite(Wa[nt][r]);
+        if (p.W_out) {
+            float *Wo = p.W_out + (size_t)chain * D * D;
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt) {
+                *reinterpret_cast<float2 *>(Wo + r0 * D + 8 * nt + 2 * c4) = make_float2(Wa[nt][0], Wa[nt][1]);
+                *reinterpret_cast<float2 *>(Wo + r1 * D + 8 * nt + 2 * c4) = make_float2(Wa[nt][2], Wa[nt][3]);
+            }
+        }
+        if (p.c_out && c4 == 0) {
+            p.c_out[(size_t)chain * D + r0] = cb[0];
+            p.c_out[(size_t)chain * D + r1] = cb[1];
+        }
+        if (__any_sync(kFull, badv) && lane == 0) record(p.status, TTT_ERR_NONFINITE);
+    };
+    bool state_written = false;
+    const int nmb = (nsteps + NB - 1) / NB;
     int rnd = 0;
     for (int mbi = 0; mbi < nmb; ++mbi) {
         uint32_t afs[NB][4];
+        const int nbk = nsteps - mbi * NB < NB ? nsteps - mbi * NB : NB;  // blocks with tokens
+        if ((mbi + 1) * BSZ > p.t_commit && !state_written) {  // the uncommitted partial mini-batch
+            write_state();
+            state_written = true;
+        }
         // Phase 1: every block's A~ at the anchor.
 #pragma unroll 1
         for (int pb = 0; pb < NB; ++pb) {
+            if (pb >= nbk) break;
             const int i = mbi * NB + pb, st = i % kStages;
             uint8_t *stg = stage_ptr<D>(sm, st);
             if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
@@ -921,6 +955,7 @@ __device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &
         };
 #pragma unroll
         for (int pb = 0; pb < NB; ++pb) {
+            if (pb >= nbk) break;
             const int i = mbi * NB + pb, st = i % kStages, slot = i & 1;
             uint8_t *stg = stage_ptr<D>(sm, st);
             float rq[2][4];
@@ -945,27 +980,11 @@ __device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &
         }
         if (!p.prefix) {
 #pragma unroll
-            for (int pb = 0; pb < NB; ++pb) block_update(pb);
+            for (int pb = 0; pb < NB; ++pb)
+                if (pb < nbk) block_update(pb);
         }
     }
-    bool badv = !isfinite(cb[0]) || !isfinite(cb[1]);
-#pragma unroll
-    for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) badv |= !isfinite(Wa[nt][r]);
-    if (p.W_out) {
-        float *Wo = p.W_out + (size_t)chain * D * D;
-#pragma unroll
-        for (int nt = 0; nt < NTW; ++nt) {
-            *reinterpret_cast<float2 *>(Wo + r0 * D + 8 * nt + 2 * c4) = make_float2(Wa[nt][0], Wa[nt][1]);
-            *reinterpret_cast<float2 *>(Wo + r1 * D + 8 * nt + 2 * c4) = make_float2(Wa[nt][2], Wa[nt][3]);
-        }
-    }
-    if (p.c_out && c4 == 0) {
-        p.c_out[(size_t)chain * D + r0] = cb[0];
-        p.c_out[(size_t)chain * D + r1] = cb[1];
-    }
-    if (__any_sync(kFull, badv) && lane == 0) record(p.status, TTT_ERR_NONFINITE);
+    if (!state_written) write_state();
 }
 
 // ------------------------------------------------------------------ O: output warps
@@ -1336,22 +1355,24 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
         if (w == 0) TTT_TRACE_AT(p, j, 5);
         const uint4 a = AR[(slot * MT + w) * 32 + lane];
         const uint32_t af[4] = {a.x, a.y, a.z, a.w};
-        // W_{j-1} -> W_j, c_{j-1} -> c_j
+        // W_{j-1} -> W_j, c_{j-1} -> c_j over the committed tokens of the super-step
+        uint32_t au[4] = {a.x, a.y, a.z, a.w};
+        mask_tokens(au, committed_in_step(p.t_commit, j), lane);
         {
             const uint32_t sK = smem_u32(stg + C::kOffKh);
 #pragma unroll
             for (int jj = 0; jj < MT; ++jj) {
                 uint32_t bt[4];
                 ldsm_x4_t(bt, sK + swz(rt, 2 * jj + ct));
-                mma16816(Wa[2 * jj], af, bt[0], bt[1]);
-                mma16816(Wa[2 * jj + 1], af, bt[2], bt[3]);
+                mma16816(Wa[2 * jj], au, bt[0], bt[1]);
+                mma16816(Wa[2 * jj + 1], au, bt[2], bt[3]);
             }
         }
         auto hsum = [](uint32_t v) {
             return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu))) +
                    __half2float(__ushort_as_half((unsigned short)(v >> 16)));
         };
-        float s0 = hsum(a.x) + hsum(a.z), s1 = hsum(a.y) + hsum(a.w);
+        float s0 = hsum(au[0]) + hsum(au[2]), s1 = hsum(au[1]) + hsum(au[3]);
         s0 += __shfl_xor_sync(kFull, s0, 1);
         s0 += __shfl_xor_sync(kFull, s0, 2);
         s1 += __shfl_xor_sync(kFull, s1, 1);

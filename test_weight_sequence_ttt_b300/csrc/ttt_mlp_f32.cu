@@ -114,14 +114,18 @@ __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
     for (int i = tid; i < d; i += kThreads) c2[i] = c20[i];
 
     for (int t0 = 0; t0 < T; t0 += b) {
+        // nb < b only for a partial last mini-batch (rows past T zero, eta 0;
+        // outputs stored, update not applied).
+        const int nb = T - t0 < b ? T - t0 : b;
         __syncthreads();
         for (int i = tid; i < b * d; i += kThreads) {
             const size_t gi = (size_t)t0 * d + i;
-            Kt[i] = ld_io<IO>(Kg + gi);
-            Qt[i] = ld_io<IO>(Qg + gi);
-            Vt[i] = ld_io<IO>(Vg + gi);
+            const bool in = i < nb * d;
+            Kt[i] = in ? ld_io<IO>(Kg + gi) : 0.f;
+            Qt[i] = in ? ld_io<IO>(Qg + gi) : 0.f;
+            Vt[i] = in ? ld_io<IO>(Vg + gi) : 0.f;
         }
-        for (int s = tid; s < b; s += kThreads) et[s] = eg[t0 + s];
+        for (int s = tid; s < b; s += kThreads) et[s] = s < nb ? eg[t0 + s] : 0.f;
         __syncthreads();
         // Z1 = K W1^T + c1 ; X2 = gelu(Z1)
         for (int i = tid; i < b * h; i += kThreads) {
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
                 const float e = Kt[s * d + j] + lg[j] * yh + lb[j] - Vt[s * d + j];
                 G[s * d + j] = rstd * (2.f * e * lg[j] - m1 - yh * m2);
             }
-            if (lane == 0 && p.inner_loss) p.inner_loss[tok0 + t0 + s] = l;
+            if (lane == 0 && p.inner_loss && s < nb) p.inner_loss[tok0 + t0 + s] = l;
         }
         // A1 = causal (eta_s/b)(q_t.k_s + 1)
         for (int i = tid; i < b * b; i += kThreads) {
@@ -218,8 +222,8 @@ __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
             Yq[i] = acc;
         }
         __syncthreads();
-        // Z = Q + LN(Yq), loss
-        for (int t = warp; t < b; t += kWarps) {
+        // Z = Q + LN(Yq), loss (rows of the batch that exist)
+        for (int t = warp; t < nb; t += kWarps) {
             const float *y = Yq + t * d;
             float mu, rstd;
             row_stats(y, d, p.eps, lane, mu, rstd);
@@ -233,6 +237,7 @@ __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
             if (lane == 0 && p.loss) p.loss[tok0 + t0 + t] = L;
         }
         // W2 -= (1/b) G^T diag(eta) X2 ; c2 -= (1/b) G^T eta
+        if (nb < b) continue;  // the partial last mini-batch is not committed
         for (int i = tid; i < d * h; i += kThreads) {
             const int r = i / h, j = i - r * h;
             float acc = 0.f;

@@ -292,7 +292,9 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
         }
         l += __shfl_xor_sync(kFull, l, 1);
         const size_t row = tok0 + (size_t)j * kB + tl;
-        if (p.z_f32) {
+        const bool valid = j * kB + tl < p.T;  // rows past T (zero-filled tail) are not stored
+        if (!valid) {
+        } else if (p.z_f32) {
             float4 *Zr = reinterpret_cast<float4 *>(static_cast<float *>(p.Z) + row * kD + 32 * half);
 #pragma unroll
             for (int k = 0; k < 8; ++k) Zr[k] = make_float4(yv[4 * k], yv[4 * k + 1], yv[4 * k + 2], yv[4 * k + 3]);
@@ -303,7 +305,7 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
                 Zr[k] = make_uint4(pack_bf2(yv[8 * k], yv[8 * k + 1]), pack_bf2(yv[8 * k + 2], yv[8 * k + 3]),
                                    pack_bf2(yv[8 * k + 4], yv[8 * k + 5]), pack_bf2(yv[8 * k + 6], yv[8 * k + 7]));
         }
-        if (p.loss && half == 0) p.loss[row] = l;
+        if (p.loss && half == 0 && valid) p.loss[row] = l;
         warp_arrive(&R.empty[stj], lane);
     }
     const bool range_bad = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
@@ -462,6 +464,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
         const int st = i % kStages;
         uint8_t *stg = stage_ptr(sm, st);
         const uint32_t sK = smem_u32(stg + kOffKh);
+        const bool commit = (i + 1) * kB <= p.t_commit;  // false only for a partial last step
         if (w == 0) TTT_TRACE_AT(p, i, 0);
         named_bar_sync(kBarG, kHY);  // G_i and A~2_i (slot i & 1) are in shared memory
         if (w == 0) TTT_TRACE_AT(p, i, 3);
@@ -518,8 +521,10 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             sr0 += __shfl_xor_sync(kFull, sr0, 2);
             sr1 += __shfl_xor_sync(kFull, sr1, 1);
             sr1 += __shfl_xor_sync(kFull, sr1, 2);
-            c1v[m][0] += sr0;
-            c1v[m][1] += sr1;
+            if (commit) {
+                c1v[m][0] += sr0;
+                c1v[m][1] += sr1;
+            }
         }
         if (i + 1 < nsteps) {
             // The chain: Z1_{i+1}^T = S1_{i+1} + A~1_i (K_i K_{i+1}^T + 1), X2k_{i+1} -> Y warps.
@@ -557,22 +562,24 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
         named_bar_arrive(kBarX2q + (i & 1), kHY);  // also orders W2_{i-1} before the Y warps' Yq_i
         warp_arrive(&R.hq[i & 1], lane);
         if (w == 0) TTT_TRACE_AT(p, i, 4);
-        // W1_i = W1_{i-1} + A~1_i K_i.
+        // W1_i = W1_{i-1} + A~1_i K_i (both updates skipped for an uncommitted partial step).
+        if (commit) {
 #pragma unroll
-        for (int j = 0; j < kD / 16; ++j) {
-            uint32_t bt[4];
-            ldsm_x4_t(bt, sK + swz(rt, 2 * j + ct));
+            for (int j = 0; j < kD / 16; ++j) {
+                uint32_t bt[4];
+                ldsm_x4_t(bt, sK + swz(rt, 2 * j + ct));
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                mma16816(W1a[m][2 * j], af1[m], bt[0], bt[1]);
-                mma16816(W1a[m][2 * j + 1], af1[m], bt[2], bt[3]);
+                for (int m = 0; m < 2; ++m) {
+                    mma16816(W1a[m][2 * j], af1[m], bt[0], bt[1]);
+                    mma16816(W1a[m][2 * j + 1], af1[m], bt[2], bt[3]);
+                }
             }
         }
         if (w == 0) TTT_TRACE_AT(p, i, 5);
         // W2_i = W2_{i-1} + A~2_i^T X2k_i (rows f, this warp's hidden columns): the fp32
         // master goes through tensor memory (two halves of 32 columns: features 0-31,
         // 32-63), the fp16 copy to buffer i % 3.
-        {
+        if (commit) {
             uint32_t bx[2][4];  // B = X2k_i (k = t, n = h), two pairs of n-tiles
             const uint32_t sXk = sX2k + (uint32_t)((i % 3) * kX2Bytes);
 #pragma unroll
@@ -948,8 +955,9 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
                 s0 += __shfl_xor_sync(kFull, s0, 2);
                 s1r += __shfl_xor_sync(kFull, s1r, 1);
                 s1r += __shfl_xor_sync(kFull, s1r, 2);
-                c2n[m][0] = c2v[m][0] + s0;
-                c2n[m][1] = c2v[m][1] + s1r;
+                const bool commit = (i + 1) * kB <= p.t_commit;  // false only for a partial last step
+                c2n[m][0] = commit ? c2v[m][0] + s0 : c2v[m][0];
+                c2n[m][1] = commit ? c2v[m][1] + s1r : c2v[m][1];
                 a2n[m][0] = pack_h2(a2[m][0][0], a2[m][0][1]);
                 a2n[m][1] = pack_h2(a2[m][0][2], a2[m][0][3]);
                 a2n[m][2] = pack_h2(a2[m][1][0], a2[m][1][1]);
@@ -1027,7 +1035,7 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int chain = blockIdx.x;
     const int bi = chain / p.H, hi = chain % p.H;
-    const int nsteps = p.T / kB;
+    const int nsteps = (p.T + kB - 1) / kB;  // a partial last step (T % 16 tokens) is not committed
     const size_t tok0 = (size_t)chain * p.T;
 
     Ring R;

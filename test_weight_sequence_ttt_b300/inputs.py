@@ -46,6 +46,7 @@ class Workload:
     eta_base: float = 1.0
     w_std: float = 0.02
     eps: float = 1e-6
+    partial_tail: bool = False  # T % b tokens at the end are emitted, not committed
 
     @property
     def chains(self) -> int:
@@ -81,6 +82,12 @@ WORKLOADS = {
                                             4096, 128, 16, "bf16", seed=1005),
     "linear_b16h16_d128_t4k_mb64": Workload("linear_b16h16_d128_t4k_mb64", "linear", 16, 16,
                                             4096, 128, 64, "bf16", seed=1005),
+    # decode step: 15 tokens of an unfilled mini-batch per chain, emitted from the
+    # committed state (the worst case before the 16th token commits the batch)
+    "linear_b8h12_d64_decode15": Workload("linear_b8h12_d64_decode15", "linear", 8, 12, 15, 64, 16,
+                                          "bf16", seed=1006, partial_tail=True),
+    "mlp_b4h12_d64_decode15": Workload("mlp_b4h12_d64_decode15", "mlp", 4, 12, 15, 64, 16, "bf16",
+                                       hidden=256, seed=1007, partial_tail=True),
 }
 
 

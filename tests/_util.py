@@ -54,17 +54,17 @@ def run_mlp(inp: dict, *, status=True, z_dtype=torch.float32, rule="prefix", q_n
     return o
 
 
-def oracle_linear(inp: dict, nthreads: int = 0, rule: str = "prefix") -> dict:
+def oracle_linear(inp: dict, nthreads: int = 0, rule: str = "prefix", partial_tail: bool = False) -> dict:
     return oracle.ttt_linear(to_np(inp["Q"]), to_np(inp["K"]), to_np(inp["V"]), to_np(inp["eta"]),
                              to_np(inp["W0"]), to_np(inp["c0"]), to_np(inp["ln_g"]), to_np(inp["ln_b"]),
-                             b=inp["b"], eps=inp["eps"], nthreads=nthreads, rule=rule)
+                             b=inp["b"], eps=inp["eps"], nthreads=nthreads, rule=rule, partial_tail=partial_tail)
 
 
-def oracle_mlp(inp: dict, nthreads: int = 0, rule: str = "prefix") -> dict:
+def oracle_mlp(inp: dict, nthreads: int = 0, rule: str = "prefix", partial_tail: bool = False) -> dict:
     return oracle.ttt_mlp(to_np(inp["Q"]), to_np(inp["K"]), to_np(inp["V"]), to_np(inp["eta"]),
                           to_np(inp["W1"]), to_np(inp["c1"]), to_np(inp["W2"]), to_np(inp["c2"]),
                           to_np(inp["ln_g"]), to_np(inp["ln_b"]), b=inp["b"], eps=inp["eps"],
-                          nthreads=nthreads, rule=rule)
+                          nthreads=nthreads, rule=rule, partial_tail=partial_tail)
 
 
 def compare(got: dict, ref: dict, keys, tol: float, sel=None) -> dict:

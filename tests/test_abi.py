@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_strings(L):
-    assert ttt.abi_version() == 2
+    assert ttt.abi_version() == 3
     for code in ttt.STATUS:
         assert len(ttt.status_string(code)) > 0
     assert ttt.status_string(999) == "unknown status"
@@ -108,6 +108,8 @@ def test_validation_codes(L):
     assert _call(L, _linear(Q=None)) == 1
     assert _call(L, _linear(Z=None)) == 1
     assert _call(L, _linear(T=30)) == 2                   # T % mb
+    assert _call(L, _linear(T=30, partial_tail=1)) == 5   # allowed with a partial tail
+    assert _call(L, _linear(partial_tail=2)) == 2
     assert _call(L, _linear(B=0)) == 2
     assert _call(L, _linear(ln_eps=-1.0)) == 2
     assert _call(L, _linear(w0_bstride=-4)) == 2
@@ -141,6 +143,7 @@ def test_validation_codes_mlp(L):
 
     assert call(W2_0=None) == 1
     assert call(T=33) == 2
+    assert call(T=33, partial_tail=1) == 5
     assert call(hidden=0) == 2
     assert call(io=3) == 3
     assert call(c2_0=base + 7 * step + 4) == 4
