@@ -191,6 +191,15 @@ int ttt_abi_version(void);                     /* == TTT_ABI_VERSION        */
 int ttt_linear_kernel_kind(int32_t io, int32_t d, int32_t mb);
 int ttt_mlp_kernel_kind(int32_t io, int32_t d, int32_t hidden, int32_t mb);
 
+/* Failure-detection testing hook. In the library built with fault hooks
+ * (libttt_b300_faults.so; never the product library) it makes the loader of
+ * the tensor-core kernels skip the tile loads of super-step `step` (and their
+ * barrier arrivals) in every chain of the following calls, so that the
+ * consumers' bounded waits run out: the call then ends with TTT_ERR_TIMEOUT in
+ * status_dev and the CUDA context stays usable. step = -1 turns it off.
+ * Returns 0 in that library; the product library has no hook and returns -1. */
+int ttt_debug_drop_load(int32_t step);
+
 #ifdef __cplusplus
 }
 #endif

@@ -3,6 +3,10 @@
 Run ``python -m test_weight_sequence_ttt_b300.build`` (or call ``build()``).
 Objects go to ``_build/`` next to this file; the shared library lands in the
 package directory, where the binding loads it. Rebuilds only what changed.
+
+``build_faults()`` builds ``libttt_b300_faults.so``: the same sources with the
+failure-injection hook compiled in (``-DTTT_FAULT_HOOKS``), used only by the
+failure-detection tests.
 """
 from __future__ import annotations
 
@@ -17,6 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT = os.path.join(HERE, "libttt_b300.so")
 BUILD = os.path.join(HERE, "_build")
+OUT_FAULTS = os.path.join(HERE, "libttt_b300_faults.so")
+BUILD_FAULTS = os.path.join(HERE, "_build", "faults")
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
@@ -35,8 +41,8 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src, obj, verbose):
-    cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
+def _compile(src, obj, verbose, extra=()):
+    cmd = [NVCC, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -45,30 +51,36 @@ def _compile(src, obj, verbose):
     return r.stderr
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, *, out: str = OUT, build_dir: str = BUILD,
+          extra=()) -> str:
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdrs = _headers()
     jobs = []
     objs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(build_dir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or _stale(o, [s, *hdrs]):
             jobs.append((s, o))
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
-            for log in ex.map(lambda j: _compile(j[0], j[1], verbose), jobs):
+            for log in ex.map(lambda j: _compile(j[0], j[1], verbose, extra), jobs):
                 if verbose and log:
                     sys.stderr.write(log)
-    if force or jobs or _stale(OUT, objs):
-        tmp = OUT + ".tmp.%d" % os.getpid()
+    if force or jobs or _stale(out, objs):
+        tmp = out + ".tmp.%d" % os.getpid()
         cmd = [NVCC, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-        os.replace(tmp, OUT)
-    return OUT
+        os.replace(tmp, out)
+    return out
+
+
+def build_faults(verbose: bool = False, force: bool = False) -> str:
+    """The library with the failure-injection hook (tests only)."""
+    return build(verbose, force, out=OUT_FAULTS, build_dir=BUILD_FAULTS, extra=("-DTTT_FAULT_HOOKS",))
 
 
 if __name__ == "__main__":

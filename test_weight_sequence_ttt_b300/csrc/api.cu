@@ -47,6 +47,10 @@ bool dims_ok(int B, int H, int T, int d, int mb, int partial_tail)
     return partial_tail || T % mb == 0;
 }
 
+#ifdef TTT_FAULT_HOOKS
+int g_drop_step = -1;
+#endif
+
 #ifdef TTT_TRACE
 unsigned long long *g_trace = nullptr;
 #endif
@@ -79,6 +83,17 @@ const char *ttt_status_string(ttt_status s)
 }
 
 int ttt_abi_version(void) { return TTT_ABI_VERSION; }
+
+int ttt_debug_drop_load(int32_t step)
+{
+#ifdef TTT_FAULT_HOOKS
+    g_drop_step = step < 0 ? -1 : step;
+    return 0;
+#else
+    (void)step;
+    return -1;
+#endif
+}
 
 int ttt_linear_kernel_kind(int32_t io, int32_t d, int32_t mb)
 {
@@ -152,6 +167,11 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     p.prefix = a->out_rule == TTT_OUT_PREFIX;
     p.q_is_k = a->out_rule == TTT_OUT_KEY;
     p.t_commit = a->T - a->T % a->mb;  // tokens whose updates are committed
+#ifdef TTT_FAULT_HOOKS
+    p.drop_step = g_drop_step;
+#else
+    p.drop_step = -1;
+#endif
     p.Q = Qe;
     p.K = a->K;
     p.V = a->V;
@@ -245,6 +265,11 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     p.prefix = a->out_rule == TTT_OUT_PREFIX;
     p.q_is_k = a->out_rule == TTT_OUT_KEY;
     p.t_commit = a->T - a->T % a->mb;  // tokens whose updates are committed
+#ifdef TTT_FAULT_HOOKS
+    p.drop_step = g_drop_step;
+#else
+    p.drop_step = -1;
+#endif
     p.Q = Qe;
     p.K = a->K;
     p.V = a->V;

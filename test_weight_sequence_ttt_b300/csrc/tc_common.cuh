@@ -107,7 +107,8 @@ struct StageGeom {
 template <int D>
 __device__ void role_loader(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
                             const float *eta_chain, int T, int *status, uint8_t *stages, const StageGeom g,
-                            uint64_t *full, uint64_t *empty, volatile int *flags, int chain, int lane, int nsteps)
+                            uint64_t *full, uint64_t *empty, volatile int *flags, int chain, int lane, int nsteps,
+                            int drop_step = -1)
 {
     if (lane == 0) {
         prefetch_tmap(tmQ);
@@ -120,6 +121,10 @@ __device__ void role_loader(const CUtensorMap *tmQ, const CUtensorMap *tmK, cons
         if (!wait_bar(&empty[st], parity_of(i / g.stages) ^ 1u, flags)) {
             abort_chain(flags, status);
             break;
+        }
+        if (i == drop_step) {  // failure-detection tests only (-1 otherwise): this stage never lands
+            issued = i + 1;
+            continue;
         }
         uint8_t *stg = stages + st * g.stage_bytes;
         const int t0 = i * kSS;

@@ -36,6 +36,7 @@ struct LinearParams {
     int prefix;  // 1: z_t with the in-batch prefix W_t; 0: with the anchor W_{i-1}
     int q_is_k;  // 1: the queries are the keys (no query tile is loaded)
     int t_commit;  // tokens [0, t_commit) are committed; a partial last mini-batch after them is not
+    int drop_step;  // fault-hook builds only: the loader skips this super-step (-1: none)
     float eps;
     const void *Q, *K, *V;
     const float *eta;
@@ -54,6 +55,7 @@ struct MlpParams {
     int prefix;  // as for LinearParams
     int q_is_k;
     int t_commit;
+    int drop_step;
     float eps;
     const void *Q, *K, *V;
     const float *eta;

@@ -266,12 +266,17 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
             uint8_t *stg = stage_ptr<D>(sm, st);
             const int t0 = i * kSS;
             float *se = reinterpret_cast<float *>(stg + C::kOffEta);
-            if (lane < kSS) {
+#ifdef TTT_FAULT_HOOKS
+            const bool drop = i == p.drop_step;  // failure-detection tests: this stage never lands
+#else
+            constexpr bool drop = false;
+#endif
+            if (!drop && lane < kSS) {
                 const int t = t0 + lane;
                 cp_async_4(se + lane, eta + (t < T ? t : 0), t < T ? 4u : 0u);  // zero-fill past T
             }
-            cp_async_mbar_arrive_noinc(&R.full[st]);
-            if (lane == 0) {
+            if (!drop) cp_async_mbar_arrive_noinc(&R.full[st]);
+            if (!drop && lane == 0) {
                 mbar_arrive_expect_tx(&R.full[st], (p.q_is_k ? 2 : 3) * C::kTile);
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {
@@ -415,6 +420,32 @@ __device__ __forceinline__ void rows_gemm(const float (&Wa)[D / 8][4], const flo
         ldsm_x4(bk, tile + swz(rb, 2 * ks + cb16));
         mma16816(acc[0], af, bk[0], bk[1]);
         mma16816(acc[1], af, bk[2], bk[3]);
+    }
+}
+
+// Two products of the same rows with one fp16 packing of W: acc0 from tile0 and
+// acc1 from tile1 (four independent accumulator chains).
+template <int D>
+__device__ __forceinline__ void rows_gemm2(const float (&Wa)[D / 8][4], const float (&cb)[2], uint32_t tile0,
+                                           uint32_t tile1, int lane, float (&acc0)[2][4], float (&acc1)[2][4])
+{
+    const int rb = (lane & 7) + (lane >> 4) * 8, cb16 = (lane >> 3) & 1;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc0[nt][r] = acc1[nt][r] = cb[r >> 1];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t b0[4], b1[4];
+        ldsm_x4(b0, tile0 + swz(rb, 2 * ks + cb16));
+        ldsm_x4(b1, tile1 + swz(rb, 2 * ks + cb16));
+        const uint32_t af[4] = {pack_h2(Wa[2 * ks][0], Wa[2 * ks][1]), pack_h2(Wa[2 * ks][2], Wa[2 * ks][3]),
+                                pack_h2(Wa[2 * ks + 1][0], Wa[2 * ks + 1][1]),
+                                pack_h2(Wa[2 * ks + 1][2], Wa[2 * ks + 1][3])};
+        mma16816(acc0[0], af, b0[0], b0[1]);
+        mma16816(acc0[1], af, b0[2], b0[3]);
+        mma16816(acc1[0], af, b1[0], b1[1]);
+        mma16816(acc1[1], af, b1[2], b1[3]);
     }
 }
 
@@ -1169,6 +1200,7 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
         const float pk_c = reinterpret_cast<const float *>(stg + C::kOffPk)[tcomb];
         const float qk_c = reinterpret_cast<const float *>(stg + C::kOffQk)[tcomb];
         float at[2][4] = {}, lin[2] = {};
+        if (w == 0) TTT_TRACE_AT(p, i, 11);
 #pragma unroll
         for (int m = 0; m < NSUB; ++m) {
             // this warp's shifted sums over its 16 features, per token (u)
@@ -1201,6 +1233,7 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
                     q[u][k] += __shfl_xor_sync(kFull, q[u][k], 1);
                     q[u][k] += __shfl_xor_sync(kFull, q[u][k], 2);
                 }
+            if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 15);
             const int buf = rnd & 1;
             float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
             float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
@@ -1330,15 +1363,18 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
             !wait_bar(&R.prep[k % kStages], parity_of(k / kStages), R.flags))
             abort_chain(R.flags, p.status);  // keep going in step with the chain warps
     };
-    auto publish_s = [&](int k) {  // S_k = W K_k^T + c (this warp's rows) -> the chain warps
-        float acc[2][4];
-        rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, k % kStages) + C::kOffKh), lane, acc);
+    auto store_s = [&](int k, const float (&acc)[2][4]) {  // S_k (this warp's rows) -> the chain warps
         float *blk = SR + ((k & 1) * MT + w) * 16 * C::SRS;  // [t][f - 16w], the chain warps' order
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int r = 0; r < 4; ++r) blk[(8 * nt + 2 * c4 + (r & 1)) * C::SRS + g + 8 * (r >> 1)] = acc[nt][r];
         named_bar_arrive(kBarS0 + (k & 1), kNAS);
+    };
+    auto publish_s = [&](int k) {  // S_k = W K_k^T + c
+        float acc[2][4];
+        rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, k % kStages) + C::kOffKh), lane, acc);
+        store_s(k, acc);
     };
     wait_stage(0);
     publish_s(0);
@@ -1394,13 +1430,18 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
                 ys[(8 * nt + 2 * c4 + (r & 1)) * C::YS + 16 * w + g + 8 * (r >> 1)] = Rq[nt][r];
         warp_arrive(&R.yfull[slot], lane);
         if (w == 0) TTT_TRACE_AT(p, j, 6);
+        // S_{j+2} = W_j K_{j+2}^T + c_j and Rq_{j+1} = W_j Q_{j+1}^T + c_j (stage j+1 was
+        // waited for one step earlier), in one pass over W_j.
         if (j + 2 < nsteps) {
             wait_stage(j + 2);
-            publish_s(j + 2);  // S_{j+2} = W_j K_{j+2}^T + c_j
+            float acc[2][4];
+            rows_gemm2<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 2) % kStages) + C::kOffKh),
+                          smem_u32(stage_ptr<D>(sm, (j + 1) % kStages) + C::offQh(p)), lane, acc, Rq);
+            store_s(j + 2, acc);
+        } else if (j + 1 < nsteps) {
+            rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % kStages) + C::offQh(p)), lane, Rq);
         }
         if (w == 0) TTT_TRACE_AT(p, j, 7);
-        if (j + 1 < nsteps)  // Rq_{j+1} = W_j Q_{j+1}^T + c_j (stage j+1 waited for above, one step earlier)
-            rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % kStages) + C::offQh(p)), lane, Rq);
         warp_arrive(&R.empty[st], lane);
     }
     bool badv = !isfinite(cb[0]) || !isfinite(cb[1]);

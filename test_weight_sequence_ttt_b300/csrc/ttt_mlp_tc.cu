@@ -1084,7 +1084,13 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (warp == kWarpL) {
         const StageGeom geom{kStages, kStageBytes, kOffK, p.q_is_k ? -1 : kOffQ, kOffV, kOffEta};
         role_loader<kD>(&tmQ, &tmK, &tmV, p.eta + tok0, p.T, p.status, sm + kOffStages, geom, R.full, R.empty,
-                        R.flags, chain, lane, nsteps);
+                        R.flags, chain, lane, nsteps,
+#ifdef TTT_FAULT_HOOKS
+                        p.drop_step
+#else
+                        -1
+#endif
+        );
     } else if (warp == kWarpP) {
         role_prep(p, sm, R, hi, tok0, lane, nsteps);
     } else if (warp < kWarpY) {
