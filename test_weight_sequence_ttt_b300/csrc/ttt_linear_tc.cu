@@ -137,6 +137,44 @@ __device__ __forceinline__ uint8_t *stage_ptr(uint8_t *sm, int st)
 // to sum would fall behind on the loads.
 template <int D>
 constexpr bool kSumsInLoader = D == 64;
+// For d = 128 the loader makes the fp16 copies of the K/Q tiles instead (two
+// stages behind its loads), and the prep warp forms its Grams from the bf16
+// tiles, which bf16 represents exactly.
+template <int D>
+constexpr bool kCopiesInLoader = D == 128;
+template <int D>
+constexpr bool kLoaderPrep = kSumsInLoader<D> || kCopiesInLoader<D>;  // the loader also arrives on prep[]
+
+// fp16 copies of a stage's K and Q tiles (same swizzled byte layout; no Q copy
+// when the queries are the keys). All loads are issued before any store.
+template <int D>
+__device__ __forceinline__ void fp16_copies(uint8_t *stg, bool q_is_k, int lane, uint32_t &mag)
+{
+    using C = Cfg<D>;
+    constexpr int NCH = 2 * D / 32;  // 16-byte chunks per lane per tile
+    const uint4 *sk = reinterpret_cast<const uint4 *>(stg + C::kOffK);
+    const uint4 *sq = reinterpret_cast<const uint4 *>(stg + C::kOffQ);
+    uint4 xk[NCH], xq[NCH];
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) xk[k] = sk[lane + 32 * k];
+    if (!q_is_k) {
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) xq[k] = sq[lane + 32 * k];
+    }
+    auto conv = [&](const uint4 &x) {
+        mag = __vmaxu2(mag, __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
+                                     __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu)));
+        return make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
+    };
+    uint4 *dk = reinterpret_cast<uint4 *>(stg + C::kOffKh);
+    uint4 *dq = reinterpret_cast<uint4 *>(stg + C::kOffQh);
+#pragma unroll
+    for (int k = 0; k < NCH; ++k) dk[lane + 32 * k] = conv(xk[k]);
+    if (!q_is_k) {
+#pragma unroll
+        for (int k = 0; k < NCH; ++k) dq[lane + 32 * k] = conv(xq[k]);
+    }
+}
 
 // Chain constants into shared memory: u0 = feature mean of W_0's rows, gamma,
 // beta; returns mean(c0) (all lanes). W_0 is read row-contiguously in float4s
@@ -197,7 +235,9 @@ __device__ void token_sums(uint8_t *stg, const uint8_t *sm, float cmean, int lan
     const float *cu = reinterpret_cast<const float *>(sm + C::kOffCst), *cg = cu + D, *cbt = cg + D;
     const int tt = lane & 15, half = lane >> 4;
     float shs = 0.f, ps = 0.f, qs = 0.f;
-#pragma unroll
+    // Partly rolled for d = 128: the kernel's hot code must fit the SM's instruction cache.
+    constexpr int kUnroll = D == 128 ? 2 : D / 16;
+#pragma unroll(kUnroll)
     for (int ch = 0; ch < D / 16; ++ch) {
         const int jj = half * (D / 16) + ch;  // 16-byte chunk (8 features)
         const uint4 kb = *reinterpret_cast<const uint4 *>(stg + C::kOffK + swz(tt, jj));
@@ -248,13 +288,14 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
     const int T = p.T;
     const float *eta = p.eta + (size_t)chain * T;
     const float cmean = kSumsInLoader<D> ? chain_consts<D>(p, sm, bi, hi, lane) : 0.f;
+    uint32_t mag = 0;  // range check of the tiles this warp converts
     if (lane == 0) {
         prefetch_tmap(tmQ);
         prefetch_tmap(tmK);
         prefetch_tmap(tmV);
     }
     int issued = 0;
-    const int lag = kSumsInLoader<D> ? kLag : 0;
+    const int lag = kLoaderPrep<D> ? kLag : 0;
     for (int i = 0; i < nsteps + lag; ++i) {
         if (i < nsteps) {
             const int st = i % kStages;
@@ -287,7 +328,7 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
             }
             issued = i + 1;
         }
-        if (!kSumsInLoader<D>) continue;
+        if (!kLoaderPrep<D>) continue;
         const int j = i - kLag;
         if (j < 0) continue;
         const int sj = j % kStages;
@@ -295,8 +336,16 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
             abort_chain(R.flags, p.status);
             break;
         }
-        token_sums<D>(stage_ptr<D>(sm, sj), sm, cmean, lane);
+        if (kSumsInLoader<D>) token_sums<D>(stage_ptr<D>(sm, sj), sm, cmean, lane);
+        if (kCopiesInLoader<D>) fp16_copies<D>(stage_ptr<D>(sm, sj), p.q_is_k != 0, lane, mag);
         warp_arrive(&R.prep[sj], lane);
+    }
+    if (kCopiesInLoader<D>) {
+        const bool range_bad = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
+        if (__any_sync(kFull, range_bad) && lane == 0) {
+            R.flags[1] = 1;
+            record(p.status, TTT_ERR_RANGE);
+        }
     }
     // Never leave while a copy issued here may still be landing in shared memory.
     for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
@@ -322,27 +371,25 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
         }
         TTT_TRACE_AT(p, i, 12);
         uint8_t *stg = stage_ptr<D>(sm, st);
-        // (1) fp16 copies of the K and Q tiles (same swizzled byte layout; the Q
-        //     tile is the K tile when the queries are the keys).
-#pragma unroll
-        for (int tile = 0; tile < 2; ++tile) {
-            if (tile == 1 && p.q_is_k) break;
-            const uint4 *src = reinterpret_cast<const uint4 *>(stg + (tile == 0 ? C::kOffK : C::kOffQ));
-            uint4 *dst = reinterpret_cast<uint4 *>(stg + (tile == 0 ? C::kOffKh : C::kOffQh));
-#pragma unroll
-            for (int ch = lane; ch < 2 * D; ch += 32) {
-                const uint4 x = src[ch];
-                mag = __vmaxu2(mag, __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
-                                             __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu)));
-                dst[ch] = make_uint4(bf2_to_h2(x.x), bf2_to_h2(x.y), bf2_to_h2(x.z), bf2_to_h2(x.w));
-            }
-        }
+        // (1) fp16 copies of the K and Q tiles (the loader makes them for d = 128).
+        if (!kCopiesInLoader<D>) fp16_copies<D>(stg, p.q_is_k != 0, lane, mag);
+        if (D == 128) TTT_TRACE_AT(p, i, 14);
         if (!kSumsInLoader<D>) token_sums<D>(stg, sm, cmean, lane);
+        if (D == 128) TTT_TRACE_AT(p, i, 15);
         __syncwarp();
         // (3) Gram fragments. d*[j][r] holds (t = g + 8(r>>1), s = 8j + 2c4 + (r&1)):
-        //     dq = Q_i K_i^T, dk = K_i K_i^T, dx = K_i K_{i-1}^T (t in step i, s in step i-1).
-        const uint32_t sK = smem_u32(stg + C::kOffKh), sQ = smem_u32(stg + C::offQh(p));
-        const uint32_t sKp = smem_u32(stage_ptr<D>(sm, (i + kStages - 1) % kStages) + C::kOffKh);
+        //     dq = Q_i K_i^T, dk = K_i K_i^T, dx = K_i K_{i-1}^T (t in step i, s in step i-1),
+        //     from the fp16 copies, or (copies in the loader) from the bf16 tiles.
+        constexpr bool kBf = kCopiesInLoader<D>;
+        auto gmma = [](float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+            if constexpr (kBf)
+                mma16816_bf16(d, a, b0, b1);
+            else
+                mma16816(d, a, b0, b1);
+        };
+        const int offK = kBf ? C::kOffK : C::kOffKh, offQ = kBf ? C::offQ(p) : C::offQh(p);
+        const uint32_t sK = smem_u32(stg + offK), sQ = smem_u32(stg + offQ);
+        const uint32_t sKp = smem_u32(stage_ptr<D>(sm, (i + kStages - 1) % kStages) + offK);
         const bool has_prev = i > 0;
         float dq[2][4] = {}, dk[2][4] = {}, dx[2][4] = {};
 #pragma unroll
@@ -350,18 +397,18 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
             uint32_t aq[4], ak[4], bk[4];
             ldsm_x4(aq, sQ + swz(ra, 2 * ks + (lane >> 4)));
             ldsm_x4(bk, sK + swz(rb, 2 * ks + ((lane >> 3) & 1)));
-            mma16816(dq[0], aq, bk[0], bk[1]);
-            mma16816(dq[1], aq, bk[2], bk[3]);
+            gmma(dq[0], aq, bk[0], bk[1]);
+            gmma(dq[1], aq, bk[2], bk[3]);
             if (SUBB < 16 || has_prev) ldsm_x4(ak, sK + swz(ra, 2 * ks + (lane >> 4)));
             if (SUBB < 16) {
-                mma16816(dk[0], ak, bk[0], bk[1]);
-                mma16816(dk[1], ak, bk[2], bk[3]);
+                gmma(dk[0], ak, bk[0], bk[1]);
+                gmma(dk[1], ak, bk[2], bk[3]);
             }
             if (has_prev) {
                 uint32_t bp[4];
                 ldsm_x4(bp, sKp + swz(rb, 2 * ks + ((lane >> 3) & 1)));
-                mma16816(dx[0], ak, bp[0], bp[1]);
-                mma16816(dx[1], ak, bp[2], bp[3]);
+                gmma(dx[0], ak, bp[0], bp[1]);
+                gmma(dx[1], ak, bp[2], bp[3]);
             }
         }
         // As B fragments (k = s, n = t) for the W warps. The mask selects which
@@ -592,9 +639,10 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
             if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 6);
             if (m == 0) {
                 // Independent tensor-core work while the other W warps finish their sums:
-                // S_{i+1} = W_{i-1} K_{i+1}^T + c_{i-1}, Rq_i = W_{i-1} Q_i^T + c_{i-1}.
-                if (has_next) rows_gemm<D>(Wa, cb, smem_u32(stgn + C::kOffKh), lane, Sn);
-                rows_gemm<D>(Wa, cb, smem_u32(stg + C::offQh(p)), lane, Rq);
+                // S_{i+1} = W_{i-1} K_{i+1}^T + c_{i-1}, Rq_i = W_{i-1} Q_i^T + c_{i-1}, in one
+                // pass (one copy of the code; on the last step the unused S reads the Q tile).
+                const uint32_t sQi = smem_u32(stg + C::offQh(p));
+                rows_gemm2<D>(Wa, cb, has_next ? smem_u32(stgn + C::kOffKh) : sQi, sQi, lane, Sn, Rq);
                 if (w == 0) TTT_TRACE_AT(p, i, 2);
             }
             if (!wait_bar(&R.red[buf], parity_of(rnd >> 1), R.flags)) {
@@ -1491,7 +1539,7 @@ linear_tc_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&R.full[s], 33);                      // expect_tx arrive + 32 cp.async arrivals
-            mbar_init(&R.prep[s], kSumsInLoader<D> ? 2 : 1);  // P (and L)
+            mbar_init(&R.prep[s], kLoaderPrep<D> ? 2 : 1);  // P (and L)
             mbar_init(&R.empty[s], 2 * C::MT + C::NO + 1);  // C warps, T warps, O warps, P
         }
         for (int j = 0; j < 2; ++j) {
@@ -1547,7 +1595,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&R.full[s], 33);                  // expect_tx arrive + 32 cp.async arrivals
-            mbar_init(&R.prep[s], kSumsInLoader<D> ? 2 : 1);  // P (and L)
+            mbar_init(&R.prep[s], kLoaderPrep<D> ? 2 : 1);  // P (and L)
             mbar_init(&R.empty[s], C::MT + C::NO + 1);  // W warps, O warps, P
         }
         for (int j = 0; j < 2; ++j) {
