@@ -140,7 +140,7 @@ typedef struct {
 /* Supported: io = TTT_F32 or TTT_BF16 with 1 <= d <= 128, 1 <= mb <= 64 and
  *            d(d+1) + d + 4 mb d + mb^2 + mb floats <= 227 KB
  *            (fp32 FFMA kernel; kind 1);
- *            io = TTT_BF16 with d in {64, 128}, mb in {1, 2, 4, 8, 16, 32, 64}
+ *            io = TTT_BF16 with d in {64, 128}, mb a power of two in [1, 1024]
  *            (tensor-core kernel, kind 2: fp16 MMA operands, fp32
  *            accumulation, fp32 weight state); kind 2 wins where both apply.
  *            ttt_linear_kernel_kind() reports the choice. */

@@ -470,6 +470,25 @@ __device__ __forceinline__ void rows_gemm(const float (&Wa)[D / 8][4], const flo
     }
 }
 
+// rows_gemm with W already packed as fp16 A fragments (one set per k-step).
+template <int D>
+__device__ __forceinline__ void rows_gemm_h(const uint32_t (&Wh)[D / 16][4], const float (&cb)[2], uint32_t tile,
+                                            int lane, float (&acc)[2][4])
+{
+    const int rb = (lane & 7) + (lane >> 4) * 8, cb16 = (lane >> 3) & 1;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[nt][r] = cb[r >> 1];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t bk[4];
+        ldsm_x4(bk, tile + swz(rb, 2 * ks + cb16));
+        mma16816(acc[0], Wh[ks], bk[0], bk[1]);
+        mma16816(acc[1], Wh[ks], bk[2], bk[3]);
+    }
+}
+
 // Two products of the same rows with one fp16 packing of W: acc0 from tile0 and
 // acc1 from tile1 (four independent accumulator chains).
 template <int D>
@@ -794,15 +813,17 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
 }
 
 // ------------------------------------------------------------------ W: mini-batches of 32 / 64 tokens
-// b = 16 NB: a mini-batch spans NB super-steps that share the anchor W_{i-1},
-// so their gradients have no chain between them. Phase 1 takes Y, the
-// LayerNorm backward and A~ of every block at the anchor; phase 2 emits each
-// block's outputs with the running in-batch prefix (Wa = W_{i-1} + sum of the
-// earlier blocks' A~ K) and applies the block's update, ending at W_i.
+// The two-phase form for NB <= 4 (the mini-batch's stages stay in the ring):
+// phase 1 takes Y, the LayerNorm backward and A~ of every block at the anchor,
+// back to back; phase 2 emits each block's outputs with the running in-batch
+// prefix (Wa = W_{i-1} + sum of the earlier blocks' A~ K) and applies the
+// block's update, ending at W_i. Measured faster than the one-pass form below
+// at b = 64.
 template <int D, int NB>
-__device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int chain, int bi, int hi,
-                                size_t tok0, int lane, int nsteps)
+__device__ void role_weights_mb2(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int chain, int bi, int hi,
+                                 size_t tok0, int lane, int nsteps)
 {
+    static_assert(NB <= 4, "phase 1 keeps every block of the mini-batch in the stage ring");
     using C = Cfg<D>;
     constexpr int MT = C::MT, NTW = D / 8, BSZ = kSS * NB;
     const int g = lane >> 2, c4 = lane & 3;
@@ -1062,6 +1083,280 @@ __device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &
             for (int pb = 0; pb < NB; ++pb)
                 if (pb < nbk) block_update(pb);
         }
+    }
+    if (!state_written) write_state();
+}
+
+// ------------------------------------------------------------------ W: mini-batches of 128 to 1024 tokens
+// b = 16 NB: a mini-batch spans NB super-steps (blocks) that share the anchor
+// W_{i-1}, so their gradients have no chain between them. One pass over the
+// blocks: Y, the LayerNorm backward and A~ of a block come from the anchor (kept
+// as the fp16 A fragments of that product); its outputs come from the running
+// weights Wa = W_{i-1} + the earlier blocks' A~ K (the in-batch prefix) plus the
+// block's own prefix (Mq); then the block's update goes into Wa and its stage is
+// released. At the end of the mini-batch Wa = W_i becomes the next anchor.
+template <int D, int NB>
+__device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int chain, int bi, int hi,
+                                size_t tok0, int lane, int nsteps)
+{
+    using C = Cfg<D>;
+    constexpr int MT = C::MT, NTW = D / 8, BSZ = kSS * NB;
+    const int g = lane >> 2, c4 = lane & 3;
+    const int r0 = 16 * w + g, r1 = r0 + 8;
+    const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
+    const float *c0 = p.c0 + bi * p.c0_bstride + (long long)hi * D;
+    float Wa[NTW][4];
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt) {
+        const float2 a = *reinterpret_cast<const float2 *>(W0 + r0 * D + 8 * nt + 2 * c4);
+        const float2 b = *reinterpret_cast<const float2 *>(W0 + r1 * D + 8 * nt + 2 * c4);
+        Wa[nt][0] = a.x;
+        Wa[nt][1] = a.y;
+        Wa[nt][2] = b.x;
+        Wa[nt][3] = b.y;
+    }
+    float cb[2] = {c0[r0], c0[r1]};
+    uint32_t Wh[D / 16][4];  // the anchor W_{i-1} as fp16 A fragments (what rows_gemm would pack)
+    float ca[2];
+    auto set_anchor = [&]() {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            Wh[ks][0] = pack_h2(Wa[2 * ks][0], Wa[2 * ks][1]);
+            Wh[ks][1] = pack_h2(Wa[2 * ks][2], Wa[2 * ks][3]);
+            Wh[ks][2] = pack_h2(Wa[2 * ks + 1][0], Wa[2 * ks + 1][1]);
+            Wh[ks][3] = pack_h2(Wa[2 * ks + 1][2], Wa[2 * ks + 1][3]);
+        }
+        ca[0] = cb[0];
+        ca[1] = cb[1];
+    };
+    set_anchor();
+    const float gam[2] = {p.ln_g[hi * D + r0], p.ln_g[hi * D + r1]};
+    const float bet[2] = {p.ln_b[hi * D + r0], p.ln_b[hi * D + r1]};
+    float gam2all = 0.f;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) gam2all = fmaf(p.ln_g[hi * D + lane + 32 * q], p.ln_g[hi * D + lane + 32 * q], gam2all);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gam2all += __shfl_xor_sync(kFull, gam2all, o);
+    const int rb = (lane & 7) + (lane >> 4) * 8, cb16 = (lane >> 3) & 1;
+    const int rt = (lane & 7) + ((lane >> 3) & 1) * 8, ct = lane >> 4;
+    const float invD = 1.f / (float)D, eps = p.eps;
+    const int T = p.T;
+    // Final state: written once, after the last committed mini-batch (a partial
+    // last mini-batch still runs its blocks' updates for its own outputs).
+    auto write_state = [&]() {
+        bool badv = !isfinite(cb[0]) || !isfinite(cb[1]);
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) badv |= !isfinite(Wa[nt][r]);
+        if (p.W_out) {
+            float *Wo = p.W_out + (size_t)chain * D * D;
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt) {
+                *reinterpret_cast<float2 *>(Wo + r0 * D + 8 * nt + 2 * c4) = make_float2(Wa[nt][0], Wa[nt][1]);
+                *reinterpret_cast<float2 *>(Wo + r1 * D + 8 * nt + 2 * c4) = make_float2(Wa[nt][2], Wa[nt][3]);
+            }
+        }
+        if (p.c_out && c4 == 0) {
+            p.c_out[(size_t)chain * D + r0] = cb[0];
+            p.c_out[(size_t)chain * D + r1] = cb[1];
+        }
+        if (__any_sync(kFull, badv) && lane == 0) record(p.status, TTT_ERR_NONFINITE);
+    };
+    bool state_written = false;
+    const int nmb = (nsteps + NB - 1) / NB;
+    int rnd = 0;
+    for (int mbi = 0; mbi < nmb; ++mbi) {
+        const int nbk = nsteps - mbi * NB < NB ? nsteps - mbi * NB : NB;  // blocks with tokens
+        if ((mbi + 1) * BSZ > p.t_commit && !state_written) {  // the uncommitted partial mini-batch
+            write_state();
+            state_written = true;
+        }
+#pragma unroll 1
+        for (int pb = 0; pb < NB; ++pb) {
+            if (pb >= nbk) break;
+            const int i = mbi * NB + pb, st = i % kStages;
+            uint8_t *stg = stage_ptr<D>(sm, st);
+            if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
+                !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags)) {
+                abort_chain(R.flags, p.status);
+                return;
+            }
+            float yk[2][4];
+            rows_gemm_h<D>(Wh, ca, smem_u32(stg + C::kOffKh), lane, yk);  // Y at the anchor
+            float kv[2][4];
+            {
+                uint32_t kr[4], vr[4];
+                ldsm_x4_t(kr, smem_u32(stg + C::kOffK) + swz(rb, 2 * w + cb16));
+                ldsm_x4_t(vr, smem_u32(stg + C::kOffV) + swz(rb, 2 * w + cb16));
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t a = kr[2 * nt + u], b = vr[2 * nt + u];
+                        kv[nt][2 * u] = bf16_bits_to_f32(a & 0xffffu) - bf16_bits_to_f32(b & 0xffffu) + bet[u];
+                        kv[nt][2 * u + 1] = bf16_bits_to_f32(a >> 16) - bf16_bits_to_f32(b >> 16) + bet[u];
+                    }
+            }
+            const float *ssh = reinterpret_cast<const float *>(stg + C::kOffSh);
+            const float *se = reinterpret_cast<const float *>(stg + C::kOffEta);
+            float escale[2][2], shv[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float2 e2 = *reinterpret_cast<const float2 *>(se + 8 * nt + 2 * c4);
+                const float2 s2 = *reinterpret_cast<const float2 *>(ssh + 8 * nt + 2 * c4);
+                escale[nt][0] = -e2.x * (1.f / (float)BSZ);
+                escale[nt][1] = -e2.y * (1.f / (float)BSZ);
+                shv[nt][0] = s2.x;
+                shv[nt][1] = s2.y;
+            }
+            const int tc = 8 * (g & 1) + 2 * c4 + ((g >> 1) & 1);
+            const float sh_c = ssh[tc];
+            const float pk_c = reinterpret_cast<const float *>(stg + C::kOffPk)[tc];
+            const float qk_c = reinterpret_cast<const float *>(stg + C::kOffQk)[tc];
+            float s1[2][2], s2[2][2], sb[2][2], sc[2][2], sd[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float a1 = 0.f, a2 = 0.f, ab = 0.f, ac = 0.f, ad = 0.f;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float dv = yk[nt][e + 2 * u] - shv[nt][e];
+                        const float g2d = gam[u] * gam[u] * dv;
+                        a1 += dv;
+                        a2 = fmaf(dv, dv, a2);
+                        ab += g2d;
+                        ac = fmaf(g2d, dv, ac);
+                        ad = fmaf(gam[u] * kv[nt][e + 2 * u], dv, ad);
+                    }
+                    s1[nt][e] = col_sum(a1);
+                    s2[nt][e] = col_sum(a2);
+                    sb[nt][e] = col_sum(ab);
+                    sc[nt][e] = col_sum(ac);
+                    sd[nt][e] = col_sum(ad);
+                }
+            const int buf = rnd & 1;
+            float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
+            float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
+            if (g == 0) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = 8 * nt + 2 * c4 + e;
+                        redX[w * kSS + t] = make_float4(s1[nt][e], s2[nt][e], sb[nt][e], sc[nt][e]);
+                        redY[w * kSS + t] = sd[nt][e];
+                    }
+            }
+            warp_arrive(&R.red[buf], lane);
+            if (!wait_bar(&R.red[buf], parity_of(rnd >> 1), R.flags)) {
+                abort_chain(R.flags, p.status);
+                return;
+            }
+            ++rnd;
+            float mu_c, rs_c, M1_c, M2_c, LE_c;
+            {
+                float S1 = 0.f, S2 = 0.f, SB = 0.f, SC = 0.f, SD = 0.f;
+#pragma unroll
+                for (int u = 0; u < MT; ++u) {
+                    const float4 x = redX[u * kSS + tc];
+                    S1 += x.x;
+                    S2 += x.y;
+                    SB += x.z;
+                    SC += x.w;
+                    SD += redY[u * kSS + tc];
+                }
+                const float ee = S1 * invD;
+                const float syy = fmaxf(fmaf(-ee, S1, S2), 0.f);
+                rs_c = rsqrtf(syy * invD + eps);
+                const float sg1 = fmaf(-ee, gam2all, SB);
+                const float sg2 = fmaf(ee * ee, gam2all, fmaf(-2.f * ee, SB, SC));
+                const float sgk = fmaf(-ee, pk_c, SD);
+                M1_c = 2.f * invD * fmaf(rs_c, sg1, pk_c);
+                M2_c = 2.f * invD * rs_c * fmaf(rs_c, sg2, sgk);
+                LE_c = fmaf(rs_c, fmaf(rs_c, sg2, 2.f * sgk), qk_c);
+                mu_c = sh_c + ee;
+            }
+            float at[2][4], lin[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int src = (nt + 2 * e) * 4 + c4;
+                    const float mu = __shfl_sync(kFull, mu_c, src);
+                    const float rs = __shfl_sync(kFull, rs_c, src);
+                    const float M1 = __shfl_sync(kFull, M1_c, src);
+                    const float M2 = __shfl_sync(kFull, M2_c, src);
+                    lin[nt][e] = __shfl_sync(kFull, LE_c, src);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float yh = (yk[nt][e + 2 * u] - mu) * rs;
+                        const float E = fmaf(gam[u], yh, kv[nt][e + 2 * u]);
+                        const float G = rs * (2.f * gam[u] * E - M1 - yh * M2);
+                        at[nt][e + 2 * u] = round_h(escale[nt][e] * G);
+                    }
+                }
+            const uint32_t af[4] = {pack_h2(at[0][0], at[0][1]), pack_h2(at[0][2], at[0][3]),
+                                    pack_h2(at[1][0], at[1][1]), pack_h2(at[1][2], at[1][3])};
+            if (p.inner_loss && w == 0 && g == 0) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = i * kSS + 8 * nt + 2 * c4 + e;
+                        if (t < T) p.inner_loss[tok0 + t] = lin[nt][e];
+                    }
+            }
+            // Outputs: the running weights (in-batch prefix of the earlier blocks) or,
+            // under the anchor rule, the anchor; plus this block's own prefix (Mq).
+            {
+                const int slot = i & 1;
+                float rq[2][4];
+                if (p.prefix)
+                    rows_gemm<D>(Wa, cb, smem_u32(stg + C::offQh(p)), lane, rq);
+                else
+                    rows_gemm_h<D>(Wh, ca, smem_u32(stg + C::offQh(p)), lane, rq);
+                const uint4 mq = reinterpret_cast<const uint4 *>(stg + C::kOffMq)[lane];
+                mma16816(rq[0], af, mq.x, mq.y);
+                mma16816(rq[1], af, mq.z, mq.w);
+                if (!wait_bar(&R.yempty[slot], parity_of(i >> 1) ^ 1u, R.flags)) {
+                    abort_chain(R.flags, p.status);
+                    return;
+                }
+                float *ys = reinterpret_cast<float *>(sm + C::kOffY + slot * kSS * C::YS * 4);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        ys[(8 * nt + 2 * c4 + (r & 1)) * C::YS + 16 * w + g + 8 * (r >> 1)] = rq[nt][r];
+                warp_arrive(&R.yfull[slot], lane);
+            }
+            // This block's update into the running weights; then the stage is free.
+            {
+                const uint32_t sK = smem_u32(stg + C::kOffKh);
+#pragma unroll
+                for (int j = 0; j < MT; ++j) {
+                    uint32_t bt[4];
+                    ldsm_x4_t(bt, sK + swz(rt, 2 * j + ct));
+                    mma16816(Wa[2 * j], af, bt[0], bt[1]);
+                    mma16816(Wa[2 * j + 1], af, bt[2], bt[3]);
+                }
+                auto hsum = [](uint32_t v) {
+                    return __half2float(__ushort_as_half((unsigned short)(v & 0xffffu))) +
+                           __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+                };
+                float s0 = hsum(af[0]) + hsum(af[2]), s1r = hsum(af[1]) + hsum(af[3]);
+                s0 += __shfl_xor_sync(kFull, s0, 1);
+                s0 += __shfl_xor_sync(kFull, s0, 2);
+                s1r += __shfl_xor_sync(kFull, s1r, 1);
+                s1r += __shfl_xor_sync(kFull, s1r, 2);
+                cb[0] += s0;
+                cb[1] += s1r;
+            }
+            warp_arrive(&R.empty[st], lane);
+        }
+        set_anchor();  // W_i: the next mini-batch's anchor
     }
     if (!state_written) write_state();
 }
@@ -1615,7 +1910,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     } else if (warp == C::kWarpP) {
         role_prep<D, SUBB>(p, sm, R, bi, hi, lane, nsteps);
     } else if (warp < C::kWarpO) {
-        if constexpr (SUBB > kSS)
+        if constexpr (SUBB > kSS && SUBB / kSS <= 4)
+            role_weights_mb2<D, SUBB / kSS>(p, sm, R, warp - C::kWarpW, chain, bi, hi, tok0, lane, nsteps);
+        else if constexpr (SUBB > kSS)
             role_weights_mb<D, SUBB / kSS>(p, sm, R, warp - C::kWarpW, chain, bi, hi, tok0, lane, nsteps);
         else
             role_weights<D, SUBB>(p, sm, R, warp - C::kWarpW, chain, bi, hi, tok0, lane, nsteps);
@@ -1656,6 +1953,10 @@ cudaError_t launch_d(const LinearParams &p, int chains, cudaStream_t s)
     case 16: return launch_dsub<D, 16>(p, chains, s);
     case 32: return launch_dsub<D, 32>(p, chains, s);
     case 64: return launch_dsub<D, 64>(p, chains, s);
+    case 128: return launch_dsub<D, 128>(p, chains, s);
+    case 256: return launch_dsub<D, 256>(p, chains, s);
+    case 512: return launch_dsub<D, 512>(p, chains, s);
+    case 1024: return launch_dsub<D, 1024>(p, chains, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -1664,8 +1965,8 @@ cudaError_t launch_d(const LinearParams &p, int chains, cudaStream_t s)
 
 bool linear_tc_supported(int io, int d, int mb)
 {
-    return io == TTT_BF16 && (d == 64 || d == 128) &&
-           (mb == 1 || mb == 2 || mb == 4 || mb == 8 || mb == 16 || mb == 32 || mb == 64);
+    // b = 1..16 divides the 16-token super-step; b = 32..1024 spans 2..64 of them
+    return io == TTT_BF16 && (d == 64 || d == 128) && mb >= 1 && mb <= 1024 && (mb & (mb - 1)) == 0;
 }
 
 cudaError_t launch_linear_tc(const LinearParams &p, int chains, cudaStream_t s)

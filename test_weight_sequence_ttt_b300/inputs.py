@@ -82,6 +82,9 @@ WORKLOADS = {
                                             4096, 128, 16, "bf16", seed=1005),
     "linear_b16h16_d128_t4k_mb64": Workload("linear_b16h16_d128_t4k_mb64", "linear", 16, 16,
                                             4096, 128, 64, "bf16", seed=1005),
+    # large mini-batch (the E2E review's b = 1K regime): the headline chains, T = 8K, b = 1024
+    "linear_b8h12_d64_t8k_mb1024": Workload("linear_b8h12_d64_t8k_mb1024", "linear", 8, 12, 8192, 64, 1024,
+                                            "bf16", seed=1008),
     # decode step: 15 tokens of an unfilled mini-batch per chain, emitted from the
     # committed state (the worst case before the 16th token commits the batch)
     "linear_b8h12_d64_decode15": Workload("linear_b8h12_d64_decode15", "linear", 8, 12, 15, 64, 16,

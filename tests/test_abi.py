@@ -78,7 +78,10 @@ def test_kernel_kind_table(L):
     assert ttt.linear_kernel_kind(ttt.BF16, 128, 1) == 2
     assert ttt.linear_kernel_kind(ttt.BF16, 128, 64) == 2
     assert ttt.linear_kernel_kind(ttt.BF16, 64, 32) == 2
-    assert ttt.linear_kernel_kind(ttt.BF16, 128, 128) == 0    # no kernel for b > 64
+    assert ttt.linear_kernel_kind(ttt.BF16, 128, 128) == 2    # large mini-batches up to 1024
+    assert ttt.linear_kernel_kind(ttt.BF16, 64, 1024) == 2
+    assert ttt.linear_kernel_kind(ttt.BF16, 64, 2048) == 0    # no kernel past 1024
+    assert ttt.linear_kernel_kind(ttt.BF16, 64, 96) == 0      # not a power of two, past the fp32 kernel's 64
     assert ttt.linear_kernel_kind(ttt.BF16, 64, 3) == 1       # fp32 kernel
     assert ttt.linear_kernel_kind(ttt.F32, 16, 16) == 1
     assert ttt.linear_kernel_kind(ttt.F32, 256, 16) == 0

@@ -47,12 +47,13 @@ def test_f32_shapes(d, b, T):
 # ---------------------------------------------------------------- tensor-core path
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("b", [1, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("b", [1, 2, 4, 8, 16, 32, 64, 128, 256, 1024])
 def test_tc_small(d, b):
     assert ttt.linear_kernel_kind(ttt.BF16, d, b) == 2
     # several super-steps; a ragged last one for b < 16; several mini-batches for b > 16
-    T = {16: 48, 32: 96, 64: 192}.get(b, 40)
-    _check(_small(d, b, T), TOL["bf16"])
+    T = {16: 48, 32: 96, 64: 192, 128: 384, 256: 512, 1024: 2048}.get(b, 40)
+    small = dict(B=1, H=2) if b >= 256 else {}
+    _check(_small(d, b, T, **small), TOL["bf16"])
 
 
 @pytest.mark.parametrize("T", [1, 2, 3, 15, 17])
@@ -105,7 +106,8 @@ def test_per_sequence_initial_weights():
 # ---------------------------------------------------------------- full-size workloads (sampled chains)
 
 FULL = ["linear_b8h12_d64_t2k", "linear_b1h32_d64_t128k", "linear_b16h16_d128_t4k_mb1",
-        "linear_b16h16_d128_t4k_mb4", "linear_b16h16_d128_t4k_mb16", "linear_b16h16_d128_t4k_mb64"]
+        "linear_b16h16_d128_t4k_mb4", "linear_b16h16_d128_t4k_mb16", "linear_b16h16_d128_t4k_mb64",
+        "linear_b8h12_d64_t8k_mb1024"]
 
 
 @pytest.mark.parametrize("name", FULL)

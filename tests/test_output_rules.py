@@ -22,7 +22,7 @@ RULES = ["anchor", "key"]
 # with a ragged last super-step), the merged d = 128 kernel, the b = 64 path,
 # the fp32 kernel with fp32 and with bf16 io.
 LIN_CASES = [(64, 16, 48, "bf16", 2), (64, 4, 40, "bf16", 2), (64, 64, 192, "bf16", 2), (128, 16, 48, "bf16", 2),
-             (128, 2, 36, "bf16", 2), (16, 16, 64, "f32", 1), (32, 16, 48, "bf16", 1)]
+             (128, 2, 36, "bf16", 2), (64, 256, 512, "bf16", 2), (16, 16, 64, "f32", 1), (32, 16, 48, "bf16", 1)]
 
 
 def _lin(d, b, T, io, B=2, H=3, seed=123):

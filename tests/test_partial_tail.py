@@ -21,6 +21,7 @@ pytestmark = pytest.mark.gpu
 # b=64 / b=32 paths (tail of several super-steps; tail only), fp32 kernels.
 LIN = [(64, 16, 37, "bf16", 2), (64, 4, 42, "bf16", 2), (64, 16, 9, "bf16", 2), (128, 16, 23, "bf16", 2),
        (128, 8, 45, "bf16", 2), (64, 64, 100, "bf16", 2), (128, 32, 40, "bf16", 2), (64, 64, 20, "bf16", 2),
+       (64, 256, 600, "bf16", 2), (128, 128, 300, "bf16", 2),
        (16, 16, 21, "f32", 1), (32, 16, 40, "bf16", 1)]
 
 
