@@ -96,6 +96,13 @@ def _p(a):
 RULES = {"prefix": 0, "anchor": 1, "key": 2}
 
 
+def eta_from_gate(logit, eta_base):
+    """The learnable learning-rate gate of the survey's "TTT layer" section,
+    eta = eta_base * sigmoid(theta_lr . x), from the gate logits theta_lr . x (fp64)."""
+    z = np.asarray(logit, np.float64)
+    return float(eta_base) / (1.0 + np.exp(-z))
+
+
 def _rule(rule):
     if rule not in RULES:
         raise ValueError("rule must be one of %s" % sorted(RULES))
@@ -111,7 +118,7 @@ def _init_stride(a, B, per):
 
 
 def ttt_linear(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nthreads=0, rule="prefix",
-               partial_tail=False):
+               partial_tail=False, eta_gate=False, eta_base=1.0):
     """TTT-Linear primal token loop in fp64.
 
     Q, K, V [B,H,T,d]; eta [B,H,T]; W0 [B|1,H,d,d] (f_res(x) = W x + c);
@@ -121,9 +128,13 @@ def ttt_linear(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nt
     ``rule``: "prefix" z_t = f(q_t; W_t), "anchor" f(q_t; W_{i-1}), "key"
     f(k_t; W_{i-1}) (Q is then not read and may be None). With ``partial_tail``
     T need not be a multiple of b: the last T % b tokens are emitted but not
-    committed (the final state is the one after the last full mini-batch)."""
+    committed (the final state is the one after the last full mini-batch).
+    With ``eta_gate``, ``eta`` holds the gate logits and the learning rates are
+    eta_base * sigmoid(logit)."""
     if Q is None:
         Q = K
+    if eta_gate:
+        eta = eta_from_gate(eta, eta_base)
     Q, K, V, eta, W0, c0, ln_g, ln_b = map(_f64, (Q, K, V, eta, W0, c0, ln_g, ln_b))
     B, H, T, d = Q.shape
     if T % b and not partial_tail:
@@ -143,13 +154,15 @@ def ttt_linear(Q, K, V, eta, W0, c0, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nt
 
 
 def ttt_mlp(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, b, eps=1e-6, ln_res=True, nthreads=0,
-            rule="prefix", partial_tail=False):
+            rule="prefix", partial_tail=False, eta_gate=False, eta_base=1.0):
     """TTT-MLP primal token loop in fp64; f_res(x) = W2 gelu_tanh(W1 x + c1) + c2.
 
     W1 [B|1,H,h,d], c1 [B|1,H,h], W2 [B|1,H,d,h], c2 [B|1,H,d]; ``rule`` as
-    for ``ttt_linear``."""
+    for ``ttt_linear`` (so are ``partial_tail``, ``eta_gate`` and ``eta_base``)."""
     if Q is None:
         Q = K
+    if eta_gate:
+        eta = eta_from_gate(eta, eta_base)
     Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b = map(_f64, (Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b))
     B, H, T, d = Q.shape
     h = W1.shape[-2]

@@ -120,7 +120,7 @@ def make_inputs(w: Workload, chains: Optional[Sequence[int]] = None) -> dict:
     d, T, H = w.d, w.T, w.H
     sel = list(range(w.chains)) if chains is None else list(chains)
     dt = _io_dtype(w.io)
-    Qs, Ks, Vs, etas = [], [], [], []
+    Qs, Ks, Vs, etas, logits = [], [], [], [], []
     for ch in sel:
         hh = ch % H
         if w.projected:
@@ -139,6 +139,7 @@ def make_inputs(w: Workload, chains: Optional[Sequence[int]] = None) -> dict:
             thlr = torch.randn(d, generator=_gen(w.seed, hh, "thlr"), dtype=torch.float64) * 0.02
             u = torch.randn(T, generator=_gen(w.seed, ch, "eta"), dtype=torch.float64) * thlr.norm()
         etas.append((w.eta_base * torch.sigmoid(u)).to(torch.float32))
+        logits.append(u.to(torch.float32))
     if chains is None:
         shp = (w.B, H)
         heads = list(range(H))
@@ -150,6 +151,7 @@ def make_inputs(w: Workload, chains: Optional[Sequence[int]] = None) -> dict:
         K=torch.stack(Ks).reshape(*shp, T, d),
         V=torch.stack(Vs).reshape(*shp, T, d),
         eta=torch.stack(etas).reshape(*shp, T),
+        eta_logit=torch.stack(logits).reshape(*shp, T),  # theta_lr . x_t, for the in-kernel gate
         b=w.b, eps=w.eps,
     )
     ln_g = torch.ones(H, d)

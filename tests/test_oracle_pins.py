@@ -551,3 +551,27 @@ def test_partial_tail_mlp(rule):
     dm = dual.ttt_mlp_dual(*cut, b=b, rule=rule, partial_tail=True)
     for f in part:
         np.testing.assert_allclose(dm[f], part[f], rtol=1e-11, atol=1e-11)
+
+
+# ---------------------------------------------------------------- learning-rate gate
+# eta = eta_base * sigmoid(theta_lr . x) from the gate logits: pinned by its closed
+# forms (logit 0 gives eta_base / 2; the gate saturates at eta_base; sigmoid(-z) =
+# 1 - sigmoid(z)) and by the run it must reproduce: the gated oracle equals the
+# oracle given those learning rates directly.
+
+def test_gate_closed_forms():
+    z = np.array([0.0, 40.0, -40.0, 1.3, -1.3])
+    e = oracle.eta_from_gate(z, 0.7)
+    assert e[0] == 0.35
+    np.testing.assert_allclose(e[1], 0.7, rtol=1e-15)
+    assert 0.0 < e[2] < 1e-17
+    np.testing.assert_allclose(e[3] + e[4], 0.7, rtol=1e-15)
+
+
+def test_gate_logit_zero_is_half_base():
+    rng = np.random.default_rng(80)
+    Q, K, V, eta, W0, c0, g, bt = _rand_linear(rng, T=16, d=6)
+    a = oracle.ttt_linear(Q, K, V, np.zeros_like(eta), W0, c0, g, bt, b=4, eta_gate=True, eta_base=0.8)
+    bb = oracle.ttt_linear(Q, K, V, np.full_like(eta, 0.4), W0, c0, g, bt, b=4)
+    for f in a:
+        np.testing.assert_array_equal(a[f], bb[f])
