@@ -241,17 +241,20 @@ def run_gpu(args):
 
     rule = args.out_rule
     q_in = None if rule == "key" else dev["Q"]    # the key rule reads no queries
+    eta_key = "eta_logit" if args.eta_gate else "eta"  # gate logits: the kernels apply the gate
     if w.variant == "linear":
-        call = lambda o: ttt.ttt_linear_forward(q_in, dev["K"], dev["V"], dev["eta"], dev["W0"], dev["c0"],
+        call = lambda o: ttt.ttt_linear_forward(q_in, dev["K"], dev["V"], dev[eta_key], dev["W0"], dev["c0"],
                                                 dev["ln_g"], dev["ln_b"], mb=w.b, eps=w.eps, out=o,
                                                 status=st, stream=stream, out_rule=rule,
-                                                partial_tail=w.partial_tail)
+                                                partial_tail=w.partial_tail, eta_gate=args.eta_gate,
+                                                eta_base=w.eta_base)
         kind = ttt.linear_kernel_kind(ttt.BF16 if w.io == "bf16" else ttt.F32, w.d, w.b)
     else:
-        call = lambda o: ttt.ttt_mlp_forward(q_in, dev["K"], dev["V"], dev["eta"], dev["W1"], dev["c1"],
+        call = lambda o: ttt.ttt_mlp_forward(q_in, dev["K"], dev["V"], dev[eta_key], dev["W1"], dev["c1"],
                                              dev["W2"], dev["c2"], dev["ln_g"], dev["ln_b"], mb=w.b, eps=w.eps,
                                              out=o, status=st, stream=stream, out_rule=rule,
-                                             partial_tail=w.partial_tail)
+                                             partial_tail=w.partial_tail, eta_gate=args.eta_gate,
+                                             eta_base=w.eta_base)
         kind = ttt.mlp_kernel_kind(ttt.BF16 if w.io == "bf16" else ttt.F32, w.d, w.hidden, w.b)
     out = call(out)                       # allocates outputs once
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -284,7 +287,7 @@ def run_gpu(args):
         raise RuntimeError("device status %d in timed region" % int(st.item()))
 
     # ---- e2e: pinned host buffers through the C ABI, copies inside the timed region
-    host_in = {k: inp[k].pin_memory() for k in (("K", "V", "eta") if rule == "key" else ("Q", "K", "V", "eta"))}
+    host_in = {k: inp[k].pin_memory() for k in (("K", "V", eta_key) if rule == "key" else ("Q", "K", "V", eta_key))}
     host_Z = torch.empty(inp["Q"].shape, dtype=zdt).pin_memory()
     host_L = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
@@ -337,7 +340,7 @@ def run_gpu(args):
         "data": "synthetic (seeded Gaussian Q/K/V, sigmoid-gated eta, N(0,0.02^2) W0)",
         "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
                    "mb": w.b, "hidden": w.hidden or None, "io": w.io, "z_dtype": args.z_dtype,
-                   "out_rule": rule, "partial_tail": w.partial_tail, "kernel_kind": kind,
+                   "out_rule": rule, "partial_tail": w.partial_tail, "eta_gate": args.eta_gate, "kernel_kind": kind,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak,
@@ -408,6 +411,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=20.0, help="core-seconds of the oracle sample")
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eta-gate", action="store_true",
+                    help="pass the learning-rate gate logits; the kernels apply eta_base * sigmoid()")
     ap.add_argument("--out-rule", default="prefix", choices=["prefix", "anchor", "key"],
                     help="output rule: z_t = f(q_t; W_t) (prefix), f(q_t; W_{i-1}) (anchor), f(k_t; W_{i-1}) (key)")
     args = ap.parse_args(argv)

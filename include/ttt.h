@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define TTT_ABI_VERSION 3
+#define TTT_ABI_VERSION 4
 
 typedef enum {
     TTT_OK = 0,
@@ -99,6 +99,13 @@ typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
  *                  W_{t-1}, exactly as Eq. 9 writes it. */
 typedef enum { TTT_OUT_PREFIX = 0, TTT_OUT_ANCHOR = 1, TTT_OUT_KEY = 2 } ttt_out_rule;
 
+/* Learning-rate gate. The learnable per-token learning rate of the survey's
+ * "TTT layer" section is eta_t = eta_base * sigmoid(theta_lr . x_t). With
+ * eta_gate = 0, `eta` holds eta_t. With eta_gate = 1 it holds the gate logits
+ * theta_lr . x_t (the gate's projection, computed with the Q/K/V projections
+ * outside the library, like them) and the kernels apply eta_base * sigmoid()
+ * themselves; tokens past T of a partial tail keep eta = 0. */
+
 /* Partial last mini-batch (decode / chunked prefill). With partial_tail = 0, T
  * must be a multiple of mb. With partial_tail = 1 it need not be: the last
  * r = T % mb tokens form a mini-batch that is emitted but not committed, as in
@@ -120,7 +127,7 @@ typedef struct {
     int32_t z_io;            /* ttt_dtype of Z (TTT_F32 or TTT_BF16)           */
     float ln_eps;            /* LayerNorm epsilon (1e-6 on the pages' configs) */
     const void *Q, *K, *V;   /* [B][H][T][d] io: test / training / label views */
-    const float *eta;        /* [B][H][T] per-token learning rate (> 0)        */
+    const float *eta;        /* [B][H][T] learning rate (or gate logit)        */
     const float *W0;         /* [B|1][H][d][d] initial W (f_res = W x + c)     */
     const float *c0;         /* [B|1][H][d] initial bias                       */
     int64_t w0_bstride;      /* elements between sequences in W0 (0 = shared)  */
@@ -135,6 +142,8 @@ typedef struct {
     int32_t *status_dev;     /* device int32 (0 on entry), or NULL             */
     int32_t out_rule;        /* ttt_out_rule; 0 = TTT_OUT_PREFIX               */
     int32_t partial_tail;    /* 1: T % mb tokens at the end, not committed     */
+    int32_t eta_gate;        /* 1: eta holds gate logits (see above)           */
+    float eta_base;          /* gate scale (eta_gate = 1 only), finite, >= 0   */
 } ttt_linear_args;
 
 /* Supported: io = TTT_F32 or TTT_BF16 with 1 <= d <= 128, 1 <= mb <= 64 and
@@ -169,6 +178,8 @@ typedef struct {
     int32_t *status_dev;
     int32_t out_rule;        /* ttt_out_rule, as for TTT-Linear               */
     int32_t partial_tail;    /* as for TTT-Linear                             */
+    int32_t eta_gate;        /* as for TTT-Linear                             */
+    float eta_base;
 } ttt_mlp_args;
 
 /* Supported: io = TTT_F32 or TTT_BF16 with d <= 256, hidden <= 1024,

@@ -47,7 +47,7 @@ class LinearArgs(ctypes.Structure):
         ("w0_bstride", ctypes.c_int64), ("c0_bstride", ctypes.c_int64),
         ("ln_g", _vp), ("ln_b", _vp), ("Z", _vp), ("W_out", _vp), ("c_out", _vp),
         ("loss", _vp), ("inner_loss", _vp), ("status_dev", _vp), ("out_rule", ctypes.c_int32),
-        ("partial_tail", ctypes.c_int32),
+        ("partial_tail", ctypes.c_int32), ("eta_gate", ctypes.c_int32), ("eta_base", ctypes.c_float),
     ]
 
 
@@ -63,7 +63,7 @@ class MlpArgs(ctypes.Structure):
         ("ln_g", _vp), ("ln_b", _vp), ("Z", _vp),
         ("W1_out", _vp), ("c1_out", _vp), ("W2_out", _vp), ("c2_out", _vp),
         ("loss", _vp), ("inner_loss", _vp), ("status_dev", _vp), ("out_rule", ctypes.c_int32),
-        ("partial_tail", ctypes.c_int32),
+        ("partial_tail", ctypes.c_int32), ("eta_gate", ctypes.c_int32), ("eta_base", ctypes.c_float),
     ]
 
 
@@ -171,7 +171,8 @@ def _stream_handle(stream) -> Optional[int]:
 def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float = 1e-6,
                        z_dtype=None, out: Optional[dict] = None, want_state: bool = True,
                        want_loss: bool = True, want_inner_loss: bool = True,
-                       status=None, stream=None, out_rule="prefix", partial_tail: bool = False) -> dict:
+                       status=None, stream=None, out_rule="prefix", partial_tail: bool = False,
+                       eta_gate: bool = False, eta_base: float = 1.0) -> dict:
     """Run the TTT-Linear inner loop through ``ttt_linear_forward``.
 
     Q, K, V [B,H,T,d] (float32 or bfloat16, CUDA, contiguous); eta [B,H,T] fp32;
@@ -184,7 +185,9 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
     (z_t = f(q_t; W_t)), "anchor" (z_t = f(q_t; W_{i-1})) or "key"
     (z_t = f(k_t; W_{i-1}); Q may be None). ``partial_tail`` lets T % mb != 0:
     the last T % mb tokens are emitted but not committed (W, c stay at the
-    state after the last full mini-batch)."""
+    state after the last full mini-batch). With ``eta_gate`` the ``eta``
+    argument holds the gate logits theta_lr . x and the kernels compute
+    eta = eta_base * sigmoid(logit)."""
     import torch
     rule = _rule_code(out_rule)
     for n, t in (("Q", Q), ("K", K), ("V", V), ("eta", eta), ("W0", W0), ("c0", c0),
@@ -209,7 +212,7 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
         ln_g=_ptr(ln_g), ln_b=_ptr(ln_b), Z=_ptr(out["Z"]), W_out=_ptr(out.get("W")),
         c_out=_ptr(out.get("c")), loss=_ptr(out.get("loss")),
         inner_loss=_ptr(out.get("inner_loss")), status_dev=_ptr(status), out_rule=rule,
-        partial_tail=int(bool(partial_tail)),
+        partial_tail=int(bool(partial_tail)), eta_gate=int(bool(eta_gate)), eta_base=float(eta_base),
     )
     rc = lib().ttt_linear_forward(ctypes.byref(a), _stream_handle(stream))
     if rc != 0:
@@ -220,7 +223,8 @@ def ttt_linear_forward(Q, K, V, eta, W0, c0, ln_g, ln_b, *, mb: int, eps: float 
 def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: float = 1e-6,
                     z_dtype=None, out: Optional[dict] = None, want_state: bool = True,
                     want_loss: bool = True, want_inner_loss: bool = True,
-                    status=None, stream=None, out_rule="prefix", partial_tail: bool = False) -> dict:
+                    status=None, stream=None, out_rule="prefix", partial_tail: bool = False,
+                    eta_gate: bool = False, eta_base: float = 1.0) -> dict:
     """Run the TTT-MLP inner loop through ``ttt_mlp_forward``.
 
     W1 [B|1,H,h,d], c1 [B|1,H,h], W2 [B|1,H,d,h], c2 [B|1,H,d] fp32; other
@@ -257,7 +261,7 @@ def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: f
         W1_out=_ptr(out.get("W1")), c1_out=_ptr(out.get("c1")), W2_out=_ptr(out.get("W2")),
         c2_out=_ptr(out.get("c2")), loss=_ptr(out.get("loss")),
         inner_loss=_ptr(out.get("inner_loss")), status_dev=_ptr(status), out_rule=rule,
-        partial_tail=int(bool(partial_tail)),
+        partial_tail=int(bool(partial_tail)), eta_gate=int(bool(eta_gate)), eta_base=float(eta_base),
     )
     rc = lib().ttt_mlp_forward(ctypes.byref(a), _stream_handle(stream))
     if rc != 0:

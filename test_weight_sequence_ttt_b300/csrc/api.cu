@@ -38,6 +38,12 @@ size_t init_bytes(int B, int H, size_t per, int64_t bstride)
     return ((size_t)(B - 1) * (size_t)bstride + (size_t)H * per) * sizeof(float);
 }
 
+bool gate_ok(int eta_gate, float eta_base)
+{
+    if (eta_gate == 0) return true;
+    return eta_gate == 1 && eta_base >= 0.f && eta_base <= 3.0e38f;  // finite, not NaN
+}
+
 bool dims_ok(int B, int H, int T, int d, int mb, int partial_tail)
 {
     if (B < 1 || H < 1 || T < 1 || d < 1 || mb < 1) return false;
@@ -122,6 +128,7 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     if (a->z_io != TTT_F32 && a->z_io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
     if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
     if (a->w0_bstride < 0 || a->c0_bstride < 0) return TTT_ERR_SHAPE;
+    if (!gate_ok(a->eta_gate, a->eta_base)) return TTT_ERR_SHAPE;
     const int kind = ttt_linear_kernel_kind(a->io, a->d, a->mb);
     if (kind == 0) return TTT_ERR_UNSUPPORTED;
 
@@ -167,6 +174,8 @@ ttt_status ttt_linear_forward(const ttt_linear_args *a, void *stream)
     p.prefix = a->out_rule == TTT_OUT_PREFIX;
     p.q_is_k = a->out_rule == TTT_OUT_KEY;
     p.t_commit = a->T - a->T % a->mb;  // tokens whose updates are committed
+    p.eta_gate = a->eta_gate;
+    p.eta_base = a->eta_base;
 #ifdef TTT_FAULT_HOOKS
     p.drop_step = g_drop_step;
 #else
@@ -213,6 +222,7 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     if (a->z_io != TTT_F32 && a->z_io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
     if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
     if (a->w_bstride < 0 || a->c1_bstride < 0 || a->c2_bstride < 0) return TTT_ERR_SHAPE;
+    if (!gate_ok(a->eta_gate, a->eta_base)) return TTT_ERR_SHAPE;
     const int kind = ttt_mlp_kernel_kind(a->io, a->d, a->hidden, a->mb);
     if (kind == 0) return TTT_ERR_UNSUPPORTED;
 
@@ -265,6 +275,8 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     p.prefix = a->out_rule == TTT_OUT_PREFIX;
     p.q_is_k = a->out_rule == TTT_OUT_KEY;
     p.t_commit = a->T - a->T % a->mb;  // tokens whose updates are committed
+    p.eta_gate = a->eta_gate;
+    p.eta_base = a->eta_base;
 #ifdef TTT_FAULT_HOOKS
     p.drop_step = g_drop_step;
 #else

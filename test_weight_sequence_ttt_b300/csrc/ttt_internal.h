@@ -37,6 +37,8 @@ struct LinearParams {
     int q_is_k;  // 1: the queries are the keys (no query tile is loaded)
     int t_commit;  // tokens [0, t_commit) are committed; a partial last mini-batch after them is not
     int drop_step;  // fault-hook builds only: the loader skips this super-step (-1: none)
+    int eta_gate;   // 1: eta holds gate logits, eta_t = eta_base * sigmoid(logit)
+    float eta_base;
     float eps;
     const void *Q, *K, *V;
     const float *eta;
@@ -56,6 +58,8 @@ struct MlpParams {
     int q_is_k;
     int t_commit;
     int drop_step;
+    int eta_gate;
+    float eta_base;
     float eps;
     const void *Q, *K, *V;
     const float *eta;

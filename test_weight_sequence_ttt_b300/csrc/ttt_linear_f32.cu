@@ -90,7 +90,10 @@ __global__ void __launch_bounds__(kThreads) linear_f32_kernel(LinearParams p)
             Kt[idx] = idx < nb * d ? ld_io<IO>(Kg + g) : 0.f;
             Qt[idx] = idx < nb * d ? ld_io<IO>(Qg + g) : 0.f;
         }
-        for (int s = tid; s < b; s += kThreads) et[s] = s < nb ? eg[t0 + s] : 0.f;
+        for (int s = tid; s < b; s += kThreads) {
+            const float e = s < nb ? eg[t0 + s] : 0.f;  // eta, or the gate logit
+            et[s] = s >= nb ? 0.f : p.eta_gate ? p.eta_base / (1.f + __expf(-e)) : e;
+        }
         __syncthreads();
         // Y = K W^T + c  (keys at the anchor W_{i-1})
         for (int idx = tid; idx < b * d; idx += kThreads) {

@@ -13,7 +13,7 @@
 // consecutive mini-batches when b < 16, a share of one mini-batch when b is
 // 32 or 64: see role_weights_mb). Warp roles:
 //   L (1 warp)  TMA loader: Q/K/V tiles [16 tok x d] bf16 (128B-swizzled) and
-//               eta into a ring of kStages stages.
+//               eta into a ring of C::kStages stages.
 //               Two stages behind its loads it also writes the per-token
 //               scalars: the LayerNorm shift u0.k + mean(c0) and the sums
 //               sum_f gamma_f kv_f, sum_f kv_f^2 with kv = k - v + beta.
@@ -64,10 +64,10 @@ namespace ttt {
 namespace {
 
 using namespace tc;
-constexpr int kStages = 6;    // input ring depth
 
 template <int D>
 struct Cfg {
+    static constexpr int kStages = 6;  // input ring depth (eight measured slower at d = 64)
     static constexpr int MT = D / 16;                // W warps (16 rows each)
     static constexpr int NO = 2;                     // output warps
     static constexpr int TPO = kSS / NO;             // tokens per output warp
@@ -144,6 +144,7 @@ template <int D>
 constexpr bool kCopiesInLoader = D == 128;
 template <int D>
 constexpr bool kLoaderPrep = kSumsInLoader<D> || kCopiesInLoader<D>;  // the loader also arrives on prep[]
+static_assert(kLoaderPrep<64> && kLoaderPrep<128>, "the loader applies the learning-rate gate");
 
 // fp16 copies of a stage's K and Q tiles (same swizzled byte layout; no Q copy
 // when the queries are the keys). All loads are issued before any store.
@@ -297,9 +298,28 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
     int issued = 0;
     const int lag = kLoaderPrep<D> ? kLag : 0;
     for (int i = 0; i < nsteps + lag; ++i) {
+        // The lagged work on stage i - kLag first: it needs only that stage's own
+        // loads, while the load of stage i waits for the consumers to release it
+        // (about two super-steps behind the chain); done the other way round, the
+        // weight warps would wait for this work.
+        if (kLoaderPrep<D> && i >= kLag) {
+            const int j = i - kLag, sj = j % C::kStages;
+            if (!wait_bar(&R.full[sj], parity_of(j / C::kStages), R.flags)) {
+                abort_chain(R.flags, p.status);
+                break;
+            }
+            if (p.eta_gate && lane < kSS) {  // eta = eta_base * sigmoid(logit) in place; 0 past T
+                float *se = reinterpret_cast<float *>(stage_ptr<D>(sm, sj) + C::kOffEta);
+                const int t = j * kSS + lane;
+                se[lane] = t < T ? __fdividef(p.eta_base, 1.f + __expf(-se[lane])) : 0.f;
+            }
+            if (kSumsInLoader<D>) token_sums<D>(stage_ptr<D>(sm, sj), sm, cmean, lane);
+            if (kCopiesInLoader<D>) fp16_copies<D>(stage_ptr<D>(sm, sj), p.q_is_k != 0, lane, mag);
+            warp_arrive(&R.prep[sj], lane);
+        }
         if (i < nsteps) {
-            const int st = i % kStages;
-            if (!wait_bar(&R.empty[st], parity_of(i / kStages) ^ 1u, R.flags)) {
+            const int st = i % C::kStages;
+            if (!wait_bar(&R.empty[st], parity_of(i / C::kStages) ^ 1u, R.flags)) {
                 abort_chain(R.flags, p.status);
                 break;
             }
@@ -328,17 +348,6 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
             }
             issued = i + 1;
         }
-        if (!kLoaderPrep<D>) continue;
-        const int j = i - kLag;
-        if (j < 0) continue;
-        const int sj = j % kStages;
-        if (!wait_bar(&R.full[sj], parity_of(j / kStages), R.flags)) {
-            abort_chain(R.flags, p.status);
-            break;
-        }
-        if (kSumsInLoader<D>) token_sums<D>(stage_ptr<D>(sm, sj), sm, cmean, lane);
-        if (kCopiesInLoader<D>) fp16_copies<D>(stage_ptr<D>(sm, sj), p.q_is_k != 0, lane, mag);
-        warp_arrive(&R.prep[sj], lane);
     }
     if (kCopiesInLoader<D>) {
         const bool range_bad = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
@@ -348,8 +357,8 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
         }
     }
     // Never leave while a copy issued here may still be landing in shared memory.
-    for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-        (void)mbar_wait(&R.full[i % kStages], parity_of(i / kStages));
+    for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+        (void)mbar_wait(&R.full[i % C::kStages], parity_of(i / C::kStages));
 }
 
 // ------------------------------------------------------------------ P: prep
@@ -364,8 +373,8 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
     const int rb = (lane & 7) + (lane >> 4) * 8;        // B-fragment row
     const float cmean = kSumsInLoader<D> ? 0.f : chain_consts<D>(p, sm, bi, hi, lane);
     for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kStages;
-        if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
+        const int st = i % C::kStages;
+        if (!wait_bar(&R.full[st], parity_of(i / C::kStages), R.flags)) {
             abort_chain(R.flags, p.status);
             return;
         }
@@ -389,7 +398,7 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
         };
         const int offK = kBf ? C::kOffK : C::kOffKh, offQ = kBf ? C::offQ(p) : C::offQh(p);
         const uint32_t sK = smem_u32(stg + offK), sQ = smem_u32(stg + offQ);
-        const uint32_t sKp = smem_u32(stage_ptr<D>(sm, (i + kStages - 1) % kStages) + offK);
+        const uint32_t sKp = smem_u32(stage_ptr<D>(sm, (i + C::kStages - 1) % C::kStages) + offK);
         const bool has_prev = i > 0;
         float dq[2][4] = {}, dk[2][4] = {}, dx[2][4] = {};
 #pragma unroll
@@ -437,9 +446,9 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
         }
         warp_arrive(&R.prep[st], lane);
         TTT_TRACE_AT(p, i, 13);
-        if (has_prev && lane == 0) mbar_arrive(&R.empty[(i + kStages - 1) % kStages]);  // K_{i-1} no longer read
+        if (has_prev && lane == 0) mbar_arrive(&R.empty[(i + C::kStages - 1) % C::kStages]);  // K_{i-1} no longer read
     }
-    if (nsteps > 0 && lane == 0) mbar_arrive(&R.empty[(nsteps - 1) % kStages]);
+    if (nsteps > 0 && lane == 0) mbar_arrive(&R.empty[(nsteps - 1) % C::kStages]);
     const bool range_bad = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
     if (__any_sync(kFull, range_bad) && lane == 0) {
         R.flags[1] = 1;
@@ -560,15 +569,15 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
 
     int rnd = 0;  // reduction rounds so far (buffer rnd & 1, phase (rnd >> 1) & 1)
     for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kStages, slot = i & 1, stn = (i + 1) % kStages;
+        const int st = i % C::kStages, slot = i & 1, stn = (i + 1) % C::kStages;
         const bool has_next = i + 1 < nsteps;
         uint8_t *stg = stage_ptr<D>(sm, st);
         uint8_t *stgn = stage_ptr<D>(sm, stn);
         if (w == 0) TTT_TRACE_AT(p, i, 0);
         bool ok = true;  // stage i's full/prep were waited for as "next" (or in the prologue)
         if (has_next)
-            ok = ok && wait_bar(&R.full[stn], parity_of((i + 1) / kStages), R.flags) &&
-                 wait_bar(&R.prep[stn], parity_of((i + 1) / kStages), R.flags);
+            ok = ok && wait_bar(&R.full[stn], parity_of((i + 1) / C::kStages), R.flags) &&
+                 wait_bar(&R.prep[stn], parity_of((i + 1) / C::kStages), R.flags);
         ok = ok && wait_bar(&R.yempty[slot], parity_of(i >> 1) ^ 1u, R.flags);
         if (!ok) {
             abort_chain(R.flags, p.status);
@@ -888,10 +897,10 @@ __device__ void role_weights_mb2(const LinearParams &p, uint8_t *sm, const Ring 
 #pragma unroll 1
         for (int pb = 0; pb < NB; ++pb) {
             if (pb >= nbk) break;
-            const int i = mbi * NB + pb, st = i % kStages;
+            const int i = mbi * NB + pb, st = i % C::kStages;
             uint8_t *stg = stage_ptr<D>(sm, st);
-            if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
-                !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags)) {
+            if (!wait_bar(&R.full[st], parity_of(i / C::kStages), R.flags) ||
+                !wait_bar(&R.prep[st], parity_of(i / C::kStages), R.flags)) {
                 abort_chain(R.flags, p.status);
                 return;
             }
@@ -1028,7 +1037,7 @@ __device__ void role_weights_mb2(const LinearParams &p, uint8_t *sm, const Ring 
         // outputs see the running weights (W_{i-1} plus the earlier blocks' updates);
         // under the anchor rule every block's outputs come first, all at W_{i-1}.
         auto block_update = [&](int pb) {
-            const int i = mbi * NB + pb, st = i % kStages;
+            const int i = mbi * NB + pb, st = i % C::kStages;
             uint8_t *stg = stage_ptr<D>(sm, st);
             {
                 const uint32_t sK = smem_u32(stg + C::kOffKh);
@@ -1056,7 +1065,7 @@ __device__ void role_weights_mb2(const LinearParams &p, uint8_t *sm, const Ring 
 #pragma unroll
         for (int pb = 0; pb < NB; ++pb) {
             if (pb >= nbk) break;
-            const int i = mbi * NB + pb, st = i % kStages, slot = i & 1;
+            const int i = mbi * NB + pb, st = i % C::kStages, slot = i & 1;
             uint8_t *stg = stage_ptr<D>(sm, st);
             float rq[2][4];
             rows_gemm<D>(Wa, cb, smem_u32(stg + C::offQh(p)), lane, rq);
@@ -1175,10 +1184,10 @@ __device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &
 #pragma unroll 1
         for (int pb = 0; pb < NB; ++pb) {
             if (pb >= nbk) break;
-            const int i = mbi * NB + pb, st = i % kStages;
+            const int i = mbi * NB + pb, st = i % C::kStages;
             uint8_t *stg = stage_ptr<D>(sm, st);
-            if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
-                !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags)) {
+            if (!wait_bar(&R.full[st], parity_of(i / C::kStages), R.flags) ||
+                !wait_bar(&R.prep[st], parity_of(i / C::kStages), R.flags)) {
                 abort_chain(R.flags, p.status);
                 return;
             }
@@ -1382,12 +1391,12 @@ __device__ void role_output(const LinearParams &p, uint8_t *sm, const Ring &R, i
             bet[k][q] = p.ln_b[hi * D + f];
         }
     for (int i = 0; i < nsteps; ++i) {
-        const int slot = i & 1, st = i % kStages;
+        const int slot = i & 1, st = i % C::kStages;
         uint8_t *stg = stage_ptr<D>(sm, st);
         if (o == 0) TTT_TRACE_AT(p, i, 8);
         if (!wait_bar(&R.yfull[slot], parity_of(i >> 1), R.flags) ||
-            !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags) ||
-            !wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
+            !wait_bar(&R.prep[st], parity_of(i / C::kStages), R.flags) ||
+            !wait_bar(&R.full[st], parity_of(i / C::kStages), R.flags)) {
             abort_chain(R.flags, p.status);
             break;
         }
@@ -1516,7 +1525,7 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
     named_bar_sync(kBarS0, kNAS);  // Y_0 = W_0 K_0^T + c_0 from the T warps
     load_s(0);
     for (int i = 0; i < nsteps; ++i) {
-        const int st = i % kStages, stn = (i + 1) % kStages;
+        const int st = i % C::kStages, stn = (i + 1) % C::kStages;
         const bool has_next = i + 1 < nsteps;
         uint8_t *stg = stage_ptr<D>(sm, st);
         uint8_t *stgn = stage_ptr<D>(sm, stn);
@@ -1702,8 +1711,8 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
     float *SR = reinterpret_cast<float *>(sm + C::kOffSR);
     const uint4 *AR = reinterpret_cast<const uint4 *>(sm + C::kOffAR);
     auto wait_stage = [&](int k) {
-        if (!wait_bar(&R.full[k % kStages], parity_of(k / kStages), R.flags) ||
-            !wait_bar(&R.prep[k % kStages], parity_of(k / kStages), R.flags))
+        if (!wait_bar(&R.full[k % C::kStages], parity_of(k / C::kStages), R.flags) ||
+            !wait_bar(&R.prep[k % C::kStages], parity_of(k / C::kStages), R.flags))
             abort_chain(R.flags, p.status);  // keep going in step with the chain warps
     };
     auto store_s = [&](int k, const float (&acc)[2][4]) {  // S_k (this warp's rows) -> the chain warps
@@ -1716,7 +1725,7 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
     };
     auto publish_s = [&](int k) {  // S_k = W K_k^T + c
         float acc[2][4];
-        rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, k % kStages) + C::kOffKh), lane, acc);
+        rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, k % C::kStages) + C::kOffKh), lane, acc);
         store_s(k, acc);
     };
     wait_stage(0);
@@ -1728,7 +1737,7 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
     float Rq[2][4];
     rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, 0) + C::offQh(p)), lane, Rq);
     for (int j = 0; j < nsteps; ++j) {
-        const int st = j % kStages, slot = j & 1;
+        const int st = j % C::kStages, slot = j & 1;
         uint8_t *stg = stage_ptr<D>(sm, st);
         named_bar_sync(kBarA0 + slot, kNAS);
         if (w == 0) TTT_TRACE_AT(p, j, 5);
@@ -1778,11 +1787,11 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
         if (j + 2 < nsteps) {
             wait_stage(j + 2);
             float acc[2][4];
-            rows_gemm2<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 2) % kStages) + C::kOffKh),
-                          smem_u32(stage_ptr<D>(sm, (j + 1) % kStages) + C::offQh(p)), lane, acc, Rq);
+            rows_gemm2<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 2) % C::kStages) + C::kOffKh),
+                          smem_u32(stage_ptr<D>(sm, (j + 1) % C::kStages) + C::offQh(p)), lane, acc, Rq);
             store_s(j + 2, acc);
         } else if (j + 1 < nsteps) {
-            rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % kStages) + C::offQh(p)), lane, Rq);
+            rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % C::kStages) + C::offQh(p)), lane, Rq);
         }
         if (w == 0) TTT_TRACE_AT(p, j, 7);
         warp_arrive(&R.empty[st], lane);
@@ -1824,15 +1833,15 @@ linear_tc_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
     Ring R;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::kOffBar);
     R.full = bar;
-    R.prep = bar + kStages;
-    R.empty = bar + 2 * kStages;
-    R.yfull = bar + 3 * kStages;
+    R.prep = bar + C::kStages;
+    R.empty = bar + 2 * C::kStages;
+    R.yfull = bar + 3 * C::kStages;
     R.yempty = R.yfull + 2;
     R.red = R.yfull + 4;
     R.flags = reinterpret_cast<volatile int *>(bar + C::kNumBars);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&R.full[s], 33);                      // expect_tx arrive + 32 cp.async arrivals
             mbar_init(&R.prep[s], kLoaderPrep<D> ? 2 : 1);  // P (and L)
             mbar_init(&R.empty[s], 2 * C::MT + C::NO + 1);  // C warps, T warps, O warps, P
@@ -1880,15 +1889,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     Ring R;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::kOffBar);
     R.full = bar;
-    R.prep = bar + kStages;
-    R.empty = bar + 2 * kStages;
-    R.yfull = bar + 3 * kStages;
+    R.prep = bar + C::kStages;
+    R.empty = bar + 2 * C::kStages;
+    R.yfull = bar + 3 * C::kStages;
     R.yempty = R.yfull + 2;
     R.red = R.yfull + 4;
     R.flags = reinterpret_cast<volatile int *>(bar + C::kNumBars);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&R.full[s], 33);                  // expect_tx arrive + 32 cp.async arrivals
             mbar_init(&R.prep[s], kLoaderPrep<D> ? 2 : 1);  // P (and L)
             mbar_init(&R.empty[s], C::MT + C::NO + 1);  // W warps, O warps, P

@@ -125,7 +125,10 @@ __global__ void __launch_bounds__(kThreads) mlp_f32_kernel(MlpParams p)
             Qt[i] = in ? ld_io<IO>(Qg + gi) : 0.f;
             Vt[i] = in ? ld_io<IO>(Vg + gi) : 0.f;
         }
-        for (int s = tid; s < b; s += kThreads) et[s] = s < nb ? eg[t0 + s] : 0.f;
+        for (int s = tid; s < b; s += kThreads) {
+            const float e = s < nb ? eg[t0 + s] : 0.f;  // eta, or the gate logit
+            et[s] = s >= nb ? 0.f : p.eta_gate ? p.eta_base / (1.f + __expf(-e)) : e;
+        }
         __syncthreads();
         // Z1 = K W1^T + c1 ; X2 = gelu(Z1)
         for (int i = tid; i < b * h; i += kThreads) {

@@ -205,6 +205,11 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
                 abort_chain(R.flags, p.status);
                 break;
             }
+            if (p.eta_gate && lane < kB) {  // eta = eta_base * sigmoid(logit); 0 past T
+                float *se = reinterpret_cast<float *>(stage_ptr(sm, st) + kOffEta);
+                const int t = i * kB + lane;
+                se[lane] = t < p.T ? __fdividef(p.eta_base, 1.f + __expf(-se[lane])) : 0.f;
+            }
             prep_stage(stage_ptr(sm, st), i > 0 ? stage_ptr(sm, (i + kStages - 1) % kStages) : nullptr, lane, mag,
                        p.prefix != 0, p.q_is_k != 0);
             warp_arrive(&R.prep[st], lane);

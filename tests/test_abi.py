@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_strings(L):
-    assert ttt.abi_version() == 3
+    assert ttt.abi_version() == 4
     for code in ttt.STATUS:
         assert len(ttt.status_string(code)) > 0
     assert ttt.status_string(999) == "unknown status"
@@ -113,6 +113,10 @@ def test_validation_codes(L):
     assert _call(L, _linear(T=30)) == 2                   # T % mb
     assert _call(L, _linear(T=30, partial_tail=1)) == 5   # allowed with a partial tail
     assert _call(L, _linear(partial_tail=2)) == 2
+    assert _call(L, _linear(eta_gate=1, eta_base=-1.0)) == 2   # gate scale must be >= 0
+    assert _call(L, _linear(eta_gate=1, eta_base=float("nan"))) == 2
+    assert _call(L, _linear(eta_gate=2)) == 2
+    assert _call(L, _linear(eta_gate=1, eta_base=0.5)) == 5
     assert _call(L, _linear(B=0)) == 2
     assert _call(L, _linear(ln_eps=-1.0)) == 2
     assert _call(L, _linear(w0_bstride=-4)) == 2
