@@ -11,14 +11,17 @@
 // Work decomposition. One CTA runs one (sequence, head) chain through all its
 // tokens in "super-steps" of 16 tokens (one mini-batch when b = 16, 16/b
 // consecutive mini-batches when b < 16, a share of one mini-batch when b is
-// 32 or 64: see role_weights_mb). Warp roles:
+// 32 to 1024: see role_weights_mb2 / role_weights_mb). Warp roles:
 //   L (1 warp)  TMA loader: Q/K/V tiles [16 tok x d] bf16 (128B-swizzled) and
-//               eta into a ring of C::kStages stages.
-//               Two stages behind its loads it also writes the per-token
-//               scalars: the LayerNorm shift u0.k + mean(c0) and the sums
-//               sum_f gamma_f kv_f, sum_f kv_f^2 with kv = k - v + beta.
-//   P (1 warp)  prep: fp16 copies of the K/Q tiles; Gram fragments (causal
-//               Q_i K_i^T + 1, K_{i-1} K_i^T + 1 and, for b < 16, K_i K_i^T + 1).
+//               eta into a ring of 6 stages.
+//               Two stages behind its loads it also applies the learning-rate
+//               gate (eta_gate) and writes, for d = 64, the per-token scalars
+//               (the LayerNorm shift u0.k + mean(c0) and the sums
+//               sum_f gamma_f kv_f, sum_f kv_f^2 with kv = k - v + beta), for
+//               d = 128 the fp16 copies of the K/Q tiles.
+//   P (1 warp)  prep: for d = 64 the fp16 copies of the K/Q tiles, for d = 128
+//               the per-token scalars; Gram fragments (causal Q_i K_i^T + 1,
+//               K_{i-1} K_i^T + 1 and, for b < 16, K_i K_i^T + 1).
 //   W (d/16)    warp w owns rows 16w..16w+15 of W and c as fp32 mma
 //               accumulators in registers for the whole sequence, and runs the
 //               serial chain for those rows.
@@ -48,7 +51,8 @@
 // memory and alternating producer/consumer named barriers, so the chain warps
 // never wait on an mbarrier. No warp of either group leaves early: after a
 // failed wait a T warp keeps running in step (results discarded, status set).
-// For d = 128 the W warps do both jobs (register budget of 20 warps).
+// For d = 128 the W warps do both jobs (20 warps of the split form would not
+// fit the register file).
 //
 // Precision. MMA operands are fp16 (10-bit mantissa) with fp32 accumulation;
 // W, c, LayerNorm statistics and gradients stay fp32. Inputs and W must stay

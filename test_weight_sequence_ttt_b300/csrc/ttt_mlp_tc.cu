@@ -16,17 +16,18 @@
 //
 // One CTA per (sequence, head) chain. Warp roles:
 //   L (1)  TMA loader of the Q/K/V tiles and eta (shared with TTT-Linear).
-//   P (1)  fp16 copies of the K/Q tiles; causal Q K^T + 1 fragments; one step
-//          behind, the output side: the X2q X2k^T Gram (causal + 1 fragments
-//          for the Y warps) and Z = Q + LN(Yq), L_t with the Z stores.
+//   P (1)  the learning-rate gate (eta_gate); fp16 copies of the K/Q tiles;
+//          causal Q K^T + 1 and K_{i-1} K_i^T + 1 fragments; two steps behind,
+//          the output side: the X2q X2k^T Gram (causal + 1 fragments for the Y
+//          warps) and Z = Q + LN(Yq), L_t with the Z stores.
 //   H (8)  warp w owns hidden units 32w..32w+31: W1 rows and c1 in registers
 //          (fp32 mma accumulators), W2 columns as an fp32 master in tensor
 //          memory (tcgen05.ld / tcgen05.st around each update) plus the fp16
 //          copy of W2 in shared memory that every product reads. Computes Z1,
 //          gelu, G1, Z1q and the W1 / W2 updates.
 //   Y (2)  warp y owns output features 32y..32y+31 and c2: Y, the LayerNorm
-//          forward/backward (both Y warps, through shared memory), G and
-//          Yq = X2q W2^T + c2 + A~2^T Mq2, handed to P.
+//          forward/backward (both Y warps, through shared memory), G and, one
+//          step later, Yq = X2q W2^T + c2 + A~2^T Mq2, handed to P.
 // Look-ahead. The recurrence of one step is A~1_i -> Z1 of step i+1 ->
 // gelu -> Y of step i+1 -> LayerNorm backward -> G -> A~1_{i+1}. Neither
 // weight update sits on it:
