@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define TTT_ABI_VERSION 4
+#define TTT_ABI_VERSION 5
 
 typedef enum {
     TTT_OK = 0,
@@ -191,6 +191,60 @@ typedef struct {
  *            kind 2 wins where both apply. ttt_mlp_kernel_kind() reports the
  *            choice. */
 ttt_status ttt_mlp_forward(const ttt_mlp_args *args, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* TTT-Linear backward (outer-loop training)                               */
+/* ---------------------------------------------------------------------- */
+/* Gradients of the TTT-Linear inner loop with respect to its inputs, for
+ * training the outer parameters by backpropagation through the inner loop
+ * (section 2.2 of the "End-to-End Test-Time Training for Long Context" review:
+ * the update itself contains a gradient, so this differentiates a gradient).
+ * For the prefix output rule (TTT_OUT_PREFIX) and T a multiple of mb, with
+ * upstream gradients dZ and optional seeds dW_n, dc_n on the final state, the
+ * call returns the gradients of
+ *     J = sum(dZ * Z) + sum(dW_n * W_n) + sum(dc_n * c_n)
+ * with respect to Q, K, V, eta (the gate logits when eta_gate = 1), W0, c0,
+ * ln_g and ln_b, where Z, W_n and c_n are what ttt_linear_forward returns for
+ * the same inputs. Gradients of W0, c0, ln_g and ln_b come back per chain
+ * ([B][H][...]); a W0 shared by the sequences (w0_bstride = 0) or the [H][d]
+ * LayerNorm parameters take the sum over B.
+ * Workspace: the call recomputes the forward and keeps every mini-batch's
+ * starting state (W_{i-1}, c_{i-1}) in `workspace`, caller-allocated device
+ * memory of at least ttt_linear_backward_workspace_bytes() bytes
+ * (B H (T/mb)(d^2 + d) floats), 16-byte aligned; its contents on entry are
+ * ignored and on return are unspecified. Device problems (non-finite
+ * gradients of the initial state or LayerNorm) go to *status_dev. */
+typedef struct {
+    int32_t B, H, T, d, mb;
+    int32_t io;              /* ttt_dtype of Q, K, V and dZ                    */
+    float ln_eps;
+    const void *Q, *K, *V;   /* [B][H][T][d] io, as for the forward            */
+    const float *eta;        /* [B][H][T] learning rate (or gate logit)        */
+    const float *W0, *c0;    /* [B|1][H][d][d], [B|1][H][d]                    */
+    int64_t w0_bstride, c0_bstride;
+    const float *ln_g, *ln_b;/* [H][d]                                         */
+    const void *dZ;          /* [B][H][T][d] io: dJ/dZ                         */
+    const float *dW_n;       /* [B][H][d][d] dJ/dW_n, or NULL (zero)           */
+    const float *dc_n;       /* [B][H][d] dJ/dc_n, or NULL (zero)              */
+    float *dQ, *dK, *dV;     /* [B][H][T][d] fp32 out                          */
+    float *deta;             /* [B][H][T] fp32 out                             */
+    float *dW0;              /* [B][H][d][d] fp32 out, per chain               */
+    float *dc0;              /* [B][H][d] fp32 out, per chain                  */
+    float *dln_g, *dln_b;    /* [B][H][d] fp32 out, per chain                  */
+    void *workspace;         /* device scratch (see above)                     */
+    uint64_t workspace_bytes;/* its size in bytes                              */
+    int32_t *status_dev;     /* device int32 (0 on entry), or NULL             */
+    int32_t eta_gate;        /* as for the forward                             */
+    float eta_base;
+} ttt_linear_bwd_args;
+
+/* Supported: io = TTT_F32 or TTT_BF16 with 1 <= d <= 128, 1 <= mb <= 64 and
+ *            2d(d+1) + 6d + 11 mb d + 2 mb^2 + 4 mb floats <= 227 KB (fp32
+ *            FFMA kernel, one CTA per chain). TTT_ERR_SHAPE if T % mb != 0 or
+ *            workspace_bytes is too small; every output is required. */
+ttt_status ttt_linear_backward(const ttt_linear_bwd_args *args, void *stream);
+/* Workspace size for ttt_linear_backward (0 if the sizes are invalid). */
+uint64_t ttt_linear_backward_workspace_bytes(int32_t B, int32_t H, int32_t T, int32_t d, int32_t mb);
 
 /* ---------------------------------------------------------------------- */
 /* Introspection                                                           */

@@ -17,9 +17,9 @@ import threading
 from typing import Optional
 
 __all__ = [
-    "TTTError", "lib", "lib_path", "ttt_linear_forward", "ttt_mlp_forward", "status_string",
-    "abi_version", "linear_kernel_kind", "mlp_kernel_kind", "LinearArgs", "MlpArgs",
-    "STATUS", "F32", "BF16", "OUT_RULES",
+    "TTTError", "lib", "lib_path", "ttt_linear_forward", "ttt_mlp_forward", "ttt_linear_backward",
+    "linear_backward_workspace_bytes", "status_string", "abi_version", "linear_kernel_kind",
+    "mlp_kernel_kind", "LinearArgs", "MlpArgs", "LinearBwdArgs", "STATUS", "F32", "BF16", "OUT_RULES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -67,6 +67,20 @@ class MlpArgs(ctypes.Structure):
     ]
 
 
+class LinearBwdArgs(ctypes.Structure):
+    """Mirror of ``ttt_linear_bwd_args``."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("T", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("mb", ctypes.c_int32), ("io", ctypes.c_int32), ("ln_eps", ctypes.c_float),
+        ("Q", _vp), ("K", _vp), ("V", _vp), ("eta", _vp), ("W0", _vp), ("c0", _vp),
+        ("w0_bstride", ctypes.c_int64), ("c0_bstride", ctypes.c_int64),
+        ("ln_g", _vp), ("ln_b", _vp), ("dZ", _vp), ("dW_n", _vp), ("dc_n", _vp),
+        ("dQ", _vp), ("dK", _vp), ("dV", _vp), ("deta", _vp), ("dW0", _vp), ("dc0", _vp),
+        ("dln_g", _vp), ("dln_b", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_uint64),
+        ("status_dev", _vp), ("eta_gate", ctypes.c_int32), ("eta_base", ctypes.c_float),
+    ]
+
+
 def _rule_code(rule) -> int:
     if isinstance(rule, str):
         if rule not in OUT_RULES:
@@ -109,6 +123,10 @@ def lib() -> ctypes.CDLL:
             L.ttt_linear_kernel_kind.argtypes = [ctypes.c_int32] * 3
             L.ttt_mlp_kernel_kind.restype = ctypes.c_int
             L.ttt_mlp_kernel_kind.argtypes = [ctypes.c_int32] * 4
+            L.ttt_linear_backward.restype = ctypes.c_int
+            L.ttt_linear_backward.argtypes = [ctypes.POINTER(LinearBwdArgs), _vp]
+            L.ttt_linear_backward_workspace_bytes.restype = ctypes.c_uint64
+            L.ttt_linear_backward_workspace_bytes.argtypes = [ctypes.c_int32] * 5
             _lib = L
     return _lib
 
@@ -266,4 +284,55 @@ def ttt_mlp_forward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, *, mb: int, eps: f
     rc = lib().ttt_mlp_forward(ctypes.byref(a), _stream_handle(stream))
     if rc != 0:
         raise TTTError(rc, "ttt_mlp_forward")
+    return out
+
+
+def linear_backward_workspace_bytes(B: int, H: int, T: int, d: int, mb: int) -> int:
+    """Device scratch ``ttt_linear_backward`` needs (0 for invalid sizes)."""
+    return int(lib().ttt_linear_backward_workspace_bytes(B, H, T, d, mb))
+
+
+def ttt_linear_backward(Q, K, V, eta, W0, c0, ln_g, ln_b, dZ, *, mb: int, dW_n=None, dc_n=None,
+                        eps: float = 1e-6, out: Optional[dict] = None, workspace=None, status=None,
+                        stream=None, eta_gate: bool = False, eta_base: float = 1.0) -> dict:
+    """Gradients of the TTT-Linear inner loop through ``ttt_linear_backward``.
+
+    Inputs as for ``ttt_linear_forward`` (prefix rule, T a multiple of mb)
+    plus dZ [B,H,T,d] in the dtype of Q/K/V and optional final-state seeds
+    dW_n [B,H,d,d], dc_n [B,H,d] fp32. Returns fp32 dQ, dK, dV [B,H,T,d], deta
+    [B,H,T] (w.r.t. the gate logits with ``eta_gate``) and per-chain dW0
+    [B,H,d,d], dc0, dln_g, dln_b [B,H,d] (sum over B for parameters shared by
+    the sequences). ``workspace`` is an optional uint8 CUDA tensor of at least
+    ``linear_backward_workspace_bytes`` bytes; one is allocated otherwise."""
+    import torch
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("eta", eta), ("W0", W0), ("c0", c0), ("ln_g", ln_g),
+                 ("ln_b", ln_b), ("dZ", dZ), ("dW_n", dW_n), ("dc_n", dc_n), ("workspace", workspace),
+                 ("status", status)):
+        _check_cuda(n, t)
+    if dZ.dtype != K.dtype:
+        raise TypeError("dZ must have the dtype of Q/K/V")
+    B, H, T, d = K.shape
+    dev = K.device
+    out = dict(out or {})
+    f32 = dict(device=dev, dtype=torch.float32)
+    for k, shape in (("dQ", (B, H, T, d)), ("dK", (B, H, T, d)), ("dV", (B, H, T, d)), ("deta", (B, H, T)),
+                     ("dW0", (B, H, d, d)), ("dc0", (B, H, d)), ("dln_g", (B, H, d)), ("dln_b", (B, H, d))):
+        if k not in out:
+            out[k] = torch.empty(shape, **f32)
+    need = linear_backward_workspace_bytes(B, H, T, d, mb)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+    a = LinearBwdArgs(
+        B=B, H=H, T=T, d=d, mb=mb, io=_io_code(K.dtype), ln_eps=eps,
+        Q=_ptr(Q), K=_ptr(K), V=_ptr(V), eta=_ptr(eta), W0=_ptr(W0), c0=_ptr(c0),
+        w0_bstride=_bstride(W0, B, H * d * d), c0_bstride=_bstride(c0, B, H * d),
+        ln_g=_ptr(ln_g), ln_b=_ptr(ln_b), dZ=_ptr(dZ), dW_n=_ptr(dW_n), dc_n=_ptr(dc_n),
+        dQ=_ptr(out["dQ"]), dK=_ptr(out["dK"]), dV=_ptr(out["dV"]), deta=_ptr(out["deta"]),
+        dW0=_ptr(out["dW0"]), dc0=_ptr(out["dc0"]), dln_g=_ptr(out["dln_g"]), dln_b=_ptr(out["dln_b"]),
+        workspace=_ptr(workspace), workspace_bytes=workspace.numel() * workspace.element_size(),
+        status_dev=_ptr(status), eta_gate=int(bool(eta_gate)), eta_base=float(eta_base),
+    )
+    rc = lib().ttt_linear_backward(ctypes.byref(a), _stream_handle(stream))
+    if rc != 0:
+        raise TTTError(rc, "ttt_linear_backward")
     return out

@@ -314,4 +314,99 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *a, void *stream)
     return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
+uint64_t ttt_linear_backward_workspace_bytes(int32_t B, int32_t H, int32_t T, int32_t d, int32_t mb)
+{
+    if (!dims_ok(B, H, T, d, mb, 0)) return 0;
+    return ttt::linear_bwd_workspace_bytes(B, H, T, d, mb);
+}
+
+ttt_status ttt_linear_backward(const ttt_linear_bwd_args *a, void *stream)
+{
+    if (!a) return TTT_ERR_NULL;
+    if (!a->Q || !a->K || !a->V || !a->eta || !a->W0 || !a->c0 || !a->ln_g || !a->ln_b || !a->dZ || !a->dQ ||
+        !a->dK || !a->dV || !a->deta || !a->dW0 || !a->dc0 || !a->dln_g || !a->dln_b || !a->workspace)
+        return TTT_ERR_NULL;
+    if (!dims_ok(a->B, a->H, a->T, a->d, a->mb, 0)) return TTT_ERR_SHAPE;
+    if (a->io != TTT_F32 && a->io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
+    if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
+    if (a->w0_bstride < 0 || a->c0_bstride < 0) return TTT_ERR_SHAPE;
+    if (!gate_ok(a->eta_gate, a->eta_base)) return TTT_ERR_SHAPE;
+    if (!ttt::linear_bwd_supported(a->io, a->d, a->mb)) return TTT_ERR_UNSUPPORTED;
+    const size_t wsb = ttt::linear_bwd_workspace_bytes(a->B, a->H, a->T, a->d, a->mb);
+    if (a->workspace_bytes < wsb) return TTT_ERR_SHAPE;
+
+    const void *in[] = {a->Q, a->K, a->V, a->eta, a->W0, a->c0, a->ln_g, a->ln_b, a->dZ};
+    const void *opt_in[] = {a->dW_n, a->dc_n};
+    const void *out[] = {a->dQ, a->dK, a->dV, a->deta, a->dW0, a->dc0, a->dln_g, a->dln_b, a->workspace};
+    for (const void *p : in)
+        if (!aligned16(p)) return TTT_ERR_ALIGN;
+    for (const void *p : opt_in)
+        if (p && !aligned16(p)) return TTT_ERR_ALIGN;
+    for (const void *p : out)
+        if (!aligned16(p)) return TTT_ERR_ALIGN;
+    if ((a->w0_bstride & 3) || (a->c0_bstride & 3)) return TTT_ERR_ALIGN;
+
+    const size_t B = a->B, H = a->H, T = a->T, d = a->d;
+    const size_t es = a->io == TTT_BF16 ? 2 : 4;
+    const size_t tok = B * H * T;
+    const Range rin[] = {span(a->Q, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
+                         span(a->eta, tok * 4), span(a->W0, init_bytes(a->B, a->H, d * d, a->w0_bstride)),
+                         span(a->c0, init_bytes(a->B, a->H, d, a->c0_bstride)), span(a->ln_g, H * d * 4),
+                         span(a->ln_b, H * d * 4), span(a->dZ, tok * d * es),
+                         span(a->dW_n, a->dW_n ? B * H * d * d * 4 : 0), span(a->dc_n, a->dc_n ? B * H * d * 4 : 0)};
+    const Range rout[] = {span(a->dQ, tok * d * 4),       span(a->dK, tok * d * 4),
+                          span(a->dV, tok * d * 4),       span(a->deta, tok * 4),
+                          span(a->dW0, B * H * d * d * 4), span(a->dc0, B * H * d * 4),
+                          span(a->dln_g, B * H * d * 4),  span(a->dln_b, B * H * d * 4),
+                          span(a->workspace, wsb),        span(a->status_dev, a->status_dev ? 4 : 0)};
+    for (size_t i = 0; i < sizeof(rout) / sizeof(rout[0]); ++i) {
+        if (rout[i].hi == rout[i].lo) continue;
+        for (const Range &r : rin)
+            if (r.hi != r.lo && overlap(rout[i], r)) return TTT_ERR_ALIAS;
+        for (size_t j = i + 1; j < sizeof(rout) / sizeof(rout[0]); ++j)
+            if (rout[j].hi != rout[j].lo && overlap(rout[i], rout[j])) return TTT_ERR_ALIAS;
+    }
+    for (const void *p : in)
+        if (!is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+    for (const void *p : opt_in)
+        if (p && !is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+    for (const void *p : out)
+        if (!is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+    if (a->status_dev && !is_device_ptr(a->status_dev)) return TTT_ERR_NOT_DEVICE_PTR;
+
+    ttt::LinearBwdParams p;
+    p.H = a->H;
+    p.T = a->T;
+    p.d = a->d;
+    p.mb = a->mb;
+    p.eta_gate = a->eta_gate;
+    p.eta_base = a->eta_base;
+    p.eps = a->ln_eps;
+    p.Q = a->Q;
+    p.K = a->K;
+    p.V = a->V;
+    p.dZ = a->dZ;
+    p.eta = a->eta;
+    p.W0 = a->W0;
+    p.c0 = a->c0;
+    p.w0_bstride = a->w0_bstride;
+    p.c0_bstride = a->c0_bstride;
+    p.ln_g = a->ln_g;
+    p.ln_b = a->ln_b;
+    p.dW_n = a->dW_n;
+    p.dc_n = a->dc_n;
+    p.dQ = a->dQ;
+    p.dK = a->dK;
+    p.dV = a->dV;
+    p.deta = a->deta;
+    p.dW0 = a->dW0;
+    p.dc0 = a->dc0;
+    p.dln_g = a->dln_g;
+    p.dln_b = a->dln_b;
+    p.ws = static_cast<float *>(a->workspace);
+    p.status = a->status_dev;
+    const cudaError_t e = ttt::launch_linear_bwd(p, a->io, a->B * a->H, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -72,6 +72,23 @@ struct MlpParams {
     unsigned long long *trace;  // phase timestamps (TTT_TRACE builds only), else NULL
 };
 
+// Gradients of the TTT-Linear inner loop (prefix rule, T a multiple of mb).
+struct LinearBwdParams {
+    int H, T, d, mb;
+    int eta_gate;
+    float eta_base;
+    float eps;
+    const void *Q, *K, *V, *dZ;  // io element type
+    const float *eta;
+    const float *W0, *c0;
+    long long w0_bstride, c0_bstride;
+    const float *ln_g, *ln_b;
+    const float *dW_n, *dc_n;  // seeds on the final state, or NULL
+    float *dQ, *dK, *dV, *deta, *dW0, *dc0, *dln_g, *dln_b;
+    float *ws;  // T/mb anchors (W, c) per chain
+    int *status;
+};
+
 // Phase-timestamp hook for performance diagnosis. Compiled in only with
 // -DTTT_TRACE; records clock64() of CTA 0 at role phase boundaries for steps
 // [kTraceFirst, kTraceFirst + kTraceSteps) into trace[(step - first) * 16 + slot].
@@ -99,7 +116,12 @@ cudaError_t launch_mlp_f32(const MlpParams &p, int io, int chains, cudaStream_t 
 bool mlp_tc_supported(int io, int d, int hidden, int mb);
 cudaError_t launch_mlp_tc(const MlpParams &p, int chains, cudaStream_t s);
 
-// Tensor-core kernel (io bf16, d in {64,128}, mb in {1,2,4,8,16,32,64}).
+// fp32 FFMA backward kernel (io f32 or bf16), d <= 128, mb <= 64.
+bool linear_bwd_supported(int io, int d, int mb);
+size_t linear_bwd_workspace_bytes(int B, int H, int T, int d, int mb);
+cudaError_t launch_linear_bwd(const LinearBwdParams &p, int io, int chains, cudaStream_t s);
+
+// Tensor-core kernel (io bf16, d in {64,128}, mb a power of two up to 1024).
 bool linear_tc_supported(int io, int d, int mb);
 // Returns cudaSuccess or the failing error; tensor maps are built inside.
 cudaError_t launch_linear_tc(const LinearParams &p, int chains, cudaStream_t s);

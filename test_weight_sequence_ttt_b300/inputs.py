@@ -17,6 +17,8 @@ Distributions (per workload, see ``WORKLOADS``):
     N(0, ||theta_lr||^2): the same distribution without d extra draws per token.
   * Initial fast weights ~ N(0, 0.02^2), one set per head shared by all sequences
     (a learned W_0); biases 0; LayerNorm gamma = 1, beta = 0, eps = 1e-6.
+  * Backward (``make_cotangents``): upstream gradients dZ ~ N(0, 1) rounded to
+    the io dtype, final-state seeds dW_n, dc_n ~ N(0, 0.1^2) fp32.
 """
 from __future__ import annotations
 
@@ -27,7 +29,7 @@ from typing import Optional, Sequence
 import torch
 
 _TAGS = {"Q": 1, "K": 2, "V": 3, "eta": 4, "x": 5, "W0": 6, "W1": 7, "W2": 8,
-         "thK": 9, "thV": 10, "thQ": 11, "thlr": 12}
+         "thK": 9, "thV": 10, "thQ": 11, "thlr": 12, "dZ": 13, "dWn": 14, "dcn": 15}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -180,3 +182,17 @@ def make_inputs(w: Workload, chains: Optional[Sequence[int]] = None) -> dict:
             out.update(W1=W1[:, None], c1=c1[:, None], W2=W2[:, None], c2=c2[:, None],
                        ln_g=ln_g[:1], ln_b=ln_b[:1])
     return out
+
+
+def make_cotangents(w: Workload, chains: Optional[Sequence[int]] = None) -> dict:
+    """Upstream gradients for the backward of workload ``w`` (CPU tensors):
+    dZ [B,H,T,d] in the io dtype, dW_n [B,H,d,d] and dc_n [B,H,d] fp32, one
+    generator per chain as in ``make_inputs`` (same ``chains`` subset form)."""
+    d, T = w.d, w.T
+    sel = list(range(w.chains)) if chains is None else list(chains)
+    shp = (w.B, w.H) if chains is None else (len(sel), 1)
+    dt = _io_dtype(w.io)
+    dZ = torch.stack([torch.randn(T, d, generator=_gen(w.seed, ch, "dZ")).to(dt) for ch in sel])
+    dWn = torch.stack([torch.randn(d, d, generator=_gen(w.seed, ch, "dWn")) * 0.1 for ch in sel])
+    dcn = torch.stack([torch.randn(d, generator=_gen(w.seed, ch, "dcn")) * 0.1 for ch in sel])
+    return dict(dZ=dZ.reshape(*shp, T, d), dW_n=dWn.reshape(*shp, d, d), dc_n=dcn.reshape(*shp, d))

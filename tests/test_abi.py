@@ -14,7 +14,7 @@ import tempfile
 import pytest
 
 import test_weight_sequence_ttt_b300 as ttt
-from test_weight_sequence_ttt_b300 import LinearArgs, MlpArgs
+from test_weight_sequence_ttt_b300 import LinearArgs, LinearBwdArgs, MlpArgs
 from test_weight_sequence_ttt_b300.build import build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_strings(L):
-    assert ttt.abi_version() == 4
+    assert ttt.abi_version() == 5
     for code in ttt.STATUS:
         assert len(ttt.status_string(code)) > 0
     assert ttt.status_string(999) == "unknown status"
@@ -65,7 +65,8 @@ def _c_offsets(struct_name, fields):
     return vals[0], vals[1:]
 
 
-@pytest.mark.parametrize("cls,cname", [(LinearArgs, "ttt_linear_args"), (MlpArgs, "ttt_mlp_args")])
+@pytest.mark.parametrize("cls,cname", [(LinearArgs, "ttt_linear_args"), (MlpArgs, "ttt_mlp_args"),
+                                       (LinearBwdArgs, "ttt_linear_bwd_args")])
 def test_struct_layout_matches_header(cls, cname):
     fields = [f[0] for f in cls._fields_]
     size, offs = _c_offsets(cname, fields)
@@ -159,3 +160,42 @@ def test_validation_codes_mlp(L):
     assert call(out_rule=7) == 3
     assert call(Q=None, out_rule=0) == 1
     assert call(Q=None, out_rule=2) == 5
+
+
+def test_backward_workspace_bytes(L):
+    # one (W, c) anchor per mini-batch and chain, fp32
+    assert ttt.linear_backward_workspace_bytes(8, 12, 2048, 64, 16) == 8 * 12 * 128 * (64 * 64 + 64) * 4
+    assert ttt.linear_backward_workspace_bytes(1, 1, 16, 16, 16) == (256 + 16) * 4
+    assert ttt.linear_backward_workspace_bytes(1, 1, 30, 16, 16) == 0   # T % mb
+    assert ttt.linear_backward_workspace_bytes(0, 1, 16, 16, 16) == 0
+
+
+def test_validation_codes_backward(L):
+    base = 1 << 40
+    step = 1 << 32
+    names = ["Q", "K", "V", "eta", "W0", "c0", "ln_g", "ln_b", "dZ", "dW_n", "dc_n", "dQ", "dK", "dV",
+             "deta", "dW0", "dc0", "dln_g", "dln_b", "workspace", "status_dev"]
+    ptrs = {n: base + i * step for i, n in enumerate(names)}
+    ws = ttt.linear_backward_workspace_bytes(2, 3, 32, 64, 16)
+
+    def call(**kw):
+        a = dict(B=2, H=3, T=32, d=64, mb=16, io=ttt.BF16, ln_eps=1e-6, w0_bstride=0, c0_bstride=0,
+                 workspace_bytes=ws, **ptrs)
+        a.update(kw)
+        return L.ttt_linear_backward(ctypes.byref(LinearBwdArgs(**a)), None)
+
+    assert L.ttt_linear_backward(None, None) == 1
+    assert call(dZ=None) == 1
+    assert call(dK=None) == 1
+    assert call(workspace=None) == 1
+    assert call(dW_n=None, dc_n=None) == 5       # seeds are optional
+    assert call(T=30) == 2                       # T % mb
+    assert call(workspace_bytes=ws - 4) == 2     # workspace too small
+    assert call(eta_gate=1, eta_base=-2.0) == 2
+    assert call(io=4) == 3
+    assert call(d=256) == 3
+    assert call(mb=128, T=256) == 3
+    assert call(dQ=base + 11 * step + 8) == 4    # misaligned
+    assert call(dQ=base + 1 * step) == 9         # dQ over K
+    assert call(workspace=base + 18 * step) == 9   # workspace over dln_b
+    assert call() == 5                           # well formed; not device memory here
