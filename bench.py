@@ -18,6 +18,12 @@ fp64 CPU oracle on a bounded sample of the same workload.
 
 ``--impl reference`` runs the reference arm: the fp64 CPU oracle as it stands,
 one bounded sample of the workload per step, on the host cores.
+
+``--backward`` (TTT-Linear) times the outer-loop gradient instead: one step is
+one ``ttt_linear_backward`` call over the workload (forward recompute with
+every mini-batch's starting state kept, then the reverse sweep), with seeded
+upstream gradients dZ and final-state seeds. Its roofline is the fp32 FMA
+rate, since the kernel does its contractions on the CUDA cores.
 """
 from __future__ import annotations
 
@@ -36,12 +42,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from test_weight_sequence_ttt_b300.inputs import WORKLOADS, make_inputs  # noqa: E402
+from test_weight_sequence_ttt_b300.inputs import WORKLOADS, make_cotangents, make_inputs  # noqa: E402
 
 DEFAULT_WORKLOAD = "linear_b8h12_d64_t2k"
 L2_FLUSH_BYTES = 256 << 20
 CSRC = os.path.join(ROOT, "test_weight_sequence_ttt_b300", "csrc")
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+# fp32 FFMA peak of one B300: 148 SMs x 128 FP32 lanes x 2 FLOP x 2.032 GHz (maximum SM clock)
+FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 
 
 def sources_sha1() -> str:
@@ -57,7 +65,7 @@ def sources_sha1() -> str:
     return h.hexdigest()
 
 
-def measured_traffic(workload: str, z_dtype: str):
+def measured_traffic(workload: str, z_dtype: str, key: str = None):
     """DRAM bytes per launch of the workload's kernel from the last ncu capture
     (profiles/traffic.json), or None when the sources changed since."""
     try:
@@ -65,7 +73,7 @@ def measured_traffic(workload: str, z_dtype: str):
             j = json.load(f)
     except (OSError, ValueError):
         return None
-    e = j.get("%s/z_%s" % (workload, z_dtype))
+    e = j.get(key or "%s/z_%s" % (workload, z_dtype))
     if not e or e.get("sources_sha1") != sources_sha1():
         return None
     return e.get("dram_bytes_per_launch")
@@ -93,6 +101,22 @@ def algorithmic_cost(w, z_bytes: int = 4, out_rule: str = "prefix"):
         h = w.hidden
         per_tok_flops = 14 * w.d * h + 4 * w.b * (w.d + h)
     return per_tok_bytes * w.tokens, per_tok_flops * w.tokens
+
+
+def backward_cost(w):
+    """Per-launch algorithmic bytes and FLOPs of ttt_linear_backward.
+
+    Bytes: Q, K, V, dZ read twice (forward sweep reads K, V; reverse reads all
+    four), eta twice, dQ, dK, dV written fp32, deta fp32, plus every mini-batch's
+    (W, c) written once and read once. FLOPs: per mini-batch of b tokens the
+    contractions 10 b d^2 (forward recompute 2, reverse 8) + b^2 d (Q K^T) +
+    5 b(b+1)/2 d (the five causal b x b x d products), times 2."""
+    es = 2 if w.io == "bf16" else 4
+    d, b = w.d, w.b
+    per_tok = (2 * d * es) + (4 * d * es) + 2 * 4 + 3 * d * 4 + 4
+    state = w.chains * (w.T // b) * (d * d + d) * 4 * 2
+    flops_tok = 2 * (10 * d * d + b * d) + 5 * (b + 1) * d
+    return per_tok * w.tokens + state, flops_tok * w.tokens
 
 
 # ---------------------------------------------------------------- clocks (NVML, during the timed region)
@@ -219,7 +243,146 @@ def _sample_shape(w, cpu_s: float, threads: int):
     return chains, min(T, w.T)
 
 
+def oracle_backward_sample(w, n_chains: int, T: int):
+    """Run the fp64 backward oracle (torch autograd through the primal token
+    loop) on the first ``n_chains`` chains, first ``T`` tokens. Returns
+    (seconds, tokens processed, threads used)."""
+    from oracle.backward import ttt_linear_backward
+    sel = list(range(n_chains))
+    inp = make_inputs(w.with_(T=T), chains=sel)
+    cot = make_cotangents(w.with_(T=T), chains=sel)
+    f = lambda t: t.detach().double().numpy()
+    t0 = time.perf_counter()
+    ttt_linear_backward(f(inp["Q"]), f(inp["K"]), f(inp["V"]), f(inp["eta"]), f(inp["W0"]), f(inp["c0"]),
+                        f(inp["ln_g"]), f(inp["ln_b"]), f(cot["dZ"]), f(cot["dW_n"]), f(cot["dc_n"]), b=w.b,
+                        eps=w.eps)
+    return time.perf_counter() - t0, n_chains * T, torch.get_num_threads()
+
+
+def _backward_sample_shape(w, seconds: float):
+    """(chains, T') for about ``seconds`` of backward-oracle time (calibrated on
+    one short chain; the oracle is batched over chains, so chains cost less
+    than linearly and this errs on the short side)."""
+    Tc = max(w.b, min(w.T, (256 // w.b) * w.b or w.b))
+    dt, toks, _ = oracle_backward_sample(w, 1, Tc)
+    T = int(max(w.b, min(w.T, (seconds / (dt / Tc)) // w.b * w.b)))
+    if T < w.T:
+        return 1, T
+    return int(min(w.chains, max(1, seconds / (dt / Tc * w.T)))), w.T
+
+
 # ---------------------------------------------------------------- GPU arm
+
+def run_gpu_backward(args):
+    """The --backward leg: ttt_linear_backward over the whole workload."""
+    import test_weight_sequence_ttt_b300 as ttt
+    from test_weight_sequence_ttt_b300 import shard
+
+    dist = shard.init()
+    rank, world = shard.world()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    w = WORKLOADS[args.workload]
+    if w.variant != "linear" or w.partial_tail or w.T % w.b:
+        raise SystemExit("--backward needs a TTT-Linear workload with T a multiple of mb")
+    wr = w.with_(seed=w.seed + 7919 * rank)
+    inp = dict(make_inputs(wr), **make_cotangents(wr))
+    eta_key = "eta_logit" if args.eta_gate else "eta"
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    stream = torch.cuda.current_stream()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(ttt.linear_backward_workspace_bytes(w.B, w.H, w.T, w.d, w.b), dtype=torch.uint8,
+                     device="cuda")
+    call = lambda o: ttt.ttt_linear_backward(dev["Q"], dev["K"], dev["V"], dev[eta_key], dev["W0"], dev["c0"],
+                                             dev["ln_g"], dev["ln_b"], dev["dZ"], mb=w.b, dW_n=dev["dW_n"],
+                                             dc_n=dev["dc_n"], eps=w.eps, out=o, workspace=ws, status=st,
+                                             stream=stream, eta_gate=args.eta_gate, eta_base=w.eta_base)
+    out = call({})
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        call(out)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError("device status %d after warm-up" % int(st.item()))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    shard.barrier(dist)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with sampler:
+        for e0, e1 in evs:
+            flush.fill_(1.0)
+            e0.record(stream)
+            call(out)
+            e1.record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    shard.barrier(dist)
+    times_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.mean(times_ms)
+    ms_max = shard.max_over_ranks(dist, ms)
+    if int(st.item()) != 0:
+        raise RuntimeError("device status %d in timed region" % int(st.item()))
+
+    # e2e: inputs and upstream gradients from pinned host memory, every gradient back to the host
+    host_in = {k: inp[k].pin_memory() for k in ("Q", "K", "V", eta_key, "dZ", "dW_n", "dc_n")}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        for k, t in host_in.items():
+            dev[k].copy_(t, non_blocking=True)
+        call(out)
+        for k, t in host_out.items():
+            t.copy_(out[k], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    shard.barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+        torch.cuda.synchronize()
+    e2e_s = shard.max_over_ranks(dist, (time.perf_counter() - t0) / e2e_steps)
+    tokens = shard.sum_over_ranks(dist, w.tokens)
+    if rank != 0:
+        return None
+    bytes_launch, flops_launch = backward_cost(w)
+    achieved = flops_launch / (ms / 1e3) / 1e12
+    line = {
+        "metric": "TTT-Linear backward (outer-loop gradient) tokens/sec (B·T·H/s) on 1 B300",
+        "value": tokens / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "precision": "bf16 Q/K/V/dZ inputs; fp32 FFMA arithmetic, fp32 gradients",
+        "data": "synthetic (seeded Gaussian Q/K/V/dZ, sigmoid-gated eta, N(0,0.02^2) W0)",
+        "config": {"workload": w.name, "direction": "backward", "variant": "ttt-linear", "B": w.B, "H": w.H,
+                   "T": w.T, "d": w.d, "mb": w.b, "io": w.io, "eta_gate": args.eta_gate,
+                   "workspace_bytes": ws.numel(), "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": "dp%d" % world},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / FP32_PEAK_TFLOPS,
+                     "traffic": measured_traffic(w.name, "", key="%s/backward" % w.name),
+                     "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 FLOP x 2.032 GHz",
+                     "algorithmic_bytes_per_launch": bytes_launch, "algorithmic_flops_per_launch": flops_launch},
+        "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+        "ms_per_step_min": min(times_ms), "ms_per_step_median": statistics.median(times_ms),
+        "timed_wall_s": wall,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        chains, Ts = _backward_sample_shape(w, args.cpu_budget_s / max(1, torch.get_num_threads()))
+        dt, toks, th = oracle_backward_sample(w, chains, Ts)
+        line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
+                                "sample": "%d of %d chains x %d tokens (fp64 torch autograd through the "
+                                          "primal token loop)" % (chains, w.chains, Ts), "seconds": dt}
+    return line
+
 
 def run_gpu(args):
     import test_weight_sequence_ttt_b300 as ttt
@@ -368,10 +531,38 @@ def run_gpu(args):
 
 # ---------------------------------------------------------------- reference arm: the oracle
 
+def run_reference_backward(args):
+    w = WORKLOADS[args.workload]
+    per_step = max(0.2, args.ref_budget_s / max(1, args.steps + args.warmup))
+    chains, Ts = _backward_sample_shape(w, per_step)
+    for _ in range(args.warmup):
+        oracle_backward_sample(w, chains, Ts)
+    secs, toks, th = 0.0, 0, 1
+    for _ in range(args.steps):
+        dt, n, th = oracle_backward_sample(w, chains, Ts)
+        secs += dt
+        toks += n
+    value = toks / secs
+    return {
+        "impl": "reference",
+        "metric": "TTT-Linear backward (outer-loop gradient) tokens/sec (B·T·H/s) on 1 B300",
+        "value": value, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator)",
+        "config": {"workload": w.name, "direction": "backward", "variant": "ttt-linear", "B": w.B, "H": w.H,
+                   "T": w.T, "d": w.d, "mb": w.b},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": th, "kind": "oracle",
+                         "sample": "%d of %d chains x %d tokens per step" % (chains, w.chains, Ts)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
+    if args.backward:
+        return run_reference_backward(args)
     import oracle
     w = WORKLOADS[args.workload]
     threads = oracle.max_threads()
@@ -413,12 +604,19 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eta-gate", action="store_true",
                     help="pass the learning-rate gate logits; the kernels apply eta_base * sigmoid()")
+    ap.add_argument("--backward", action="store_true",
+                    help="time ttt_linear_backward (gradients through the inner loop) instead of the forward")
     ap.add_argument("--out-rule", default="prefix", choices=["prefix", "anchor", "key"],
                     help="output rule: z_t = f(q_t; W_t) (prefix), f(q_t; W_{i-1}) (anchor), f(k_t; W_{i-1}) (key)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.backward and args.out_rule != "prefix":
+        ap.error("--backward supports the prefix output rule only")
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_gpu_backward(args) if args.backward else run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

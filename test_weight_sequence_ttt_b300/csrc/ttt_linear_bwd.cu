@@ -446,6 +446,673 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(LinearBwdParams p)
     if (bad && p.status) atomicCAS(p.status, 0, TTT_ERR_NONFINITE);
 }
 
+// ------------------------------------------------------------------ tiled kernel (compile-time D, MB)
+//
+// The same steps with the sizes fixed at compile time. Rows of every b x D
+// tile and of W, dW are padded to LD = D + 4 floats: 16-byte rows, so float4
+// loads along a row are free of bank conflicts whichever rows the lanes hold.
+// Each thread keeps RPT accumulators (rows rg, rg + NG, ... of one column) for
+// the b x D products and a TB x TB block (rows / columns 4 (tid / 16) + 64 q + k
+// and 4 (tid % 16) + 64 q + k) for the D x D outer products; the LayerNorm rows
+// of a warp are reduced together. The workspace layout is the general kernel's.
+template <int D, int MB>
+struct Tiled {
+    static constexpr int LD = D + 4;
+    static constexpr int NG = kThreads / D;  // row groups of the b x D products
+    static constexpr int RPT = MB / NG;      // rows per thread
+    static constexpr int TB = D / 16;        // outer-product block edge
+    static constexpr int RW = MB / kWarps;   // LayerNorm rows per warp
+    static constexpr int EL = D / 32;        // row elements per lane
+    static_assert(NG * D == kThreads && RPT * NG == MB && RW * kWarps == MB && EL * 32 == D && TB % 4 == 0,
+                  "tiling");
+    static constexpr size_t kFloats = 2 * (size_t)D * LD + 6 * D + 10 * (size_t)MB * LD + 2 * MB * MB + 4 * MB;
+};
+
+struct SmemT {
+    float *W, *dW, *c, *dc, *gam, *bet, *dgam, *dbet;
+    float *K, *Q, *E, *DZ, *Yh, *P, *G, *DP, *R, *KA;  // R also holds du_s once dg_s is formed
+    float *QK, *DA, *et, *det, *rk, *m2k;
+};
+
+template <int D, int MB>
+__device__ SmemT carve_t(float *sm)
+{
+    using C = Tiled<D, MB>;
+    SmemT s;
+    float *p = sm;
+    auto take = [&](size_t n) { float *q = p; p += n; return q; };
+    s.W = take(D * C::LD);
+    s.dW = take(D * C::LD);
+    s.c = take(D);
+    s.dc = take(D);
+    s.gam = take(D);
+    s.bet = take(D);
+    s.dgam = take(D);
+    s.dbet = take(D);
+    s.K = take(MB * C::LD);
+    s.Q = take(MB * C::LD);
+    s.E = take(MB * C::LD);
+    s.DZ = take(MB * C::LD);
+    s.Yh = take(MB * C::LD);
+    s.P = take(MB * C::LD);
+    s.G = take(MB * C::LD);
+    s.DP = take(MB * C::LD);
+    s.R = take(MB * C::LD);
+    s.KA = take(MB * C::LD);
+    s.QK = take(MB * MB);
+    s.DA = take(MB * MB);
+    s.et = take(MB);
+    s.det = take(MB);
+    s.rk = take(MB);
+    s.m2k = take(MB);
+    return s;
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+template <typename IO>
+__device__ __forceinline__ float4 ldg4(const IO *p);
+template <>
+__device__ __forceinline__ float4 ldg4<float>(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+template <>
+__device__ __forceinline__ float4 ldg4<__nv_bfloat16>(const __nv_bfloat16 *p)
+{
+    const uint2 u = *reinterpret_cast<const uint2 *>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <int N>
+__device__ __forceinline__ void wsum_n(float (&v)[N])
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < N; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
+}
+
+// acc[r] += sum_i X[row r][i] M[c][i] (and acc2 with X2): the "times M^T" products.
+template <int D, int MB, bool TWO>
+__device__ __forceinline__ void prod_mt(float (&acc)[Tiled<D, MB>::RPT], float (&acc2)[Tiled<D, MB>::RPT],
+                                        const float *X, const float *X2, const float *M, int c, int rg)
+{
+    using C = Tiled<D, MB>;
+#pragma unroll 4
+    for (int i = 0; i < D; i += 4) {
+        const float4 m = ld4(M + c * C::LD + i);
+#pragma unroll
+        for (int r = 0; r < C::RPT; ++r) {
+            const float4 x = ld4(X + (rg + C::NG * r) * C::LD + i);
+            acc[r] = fmaf(x.x, m.x, fmaf(x.y, m.y, fmaf(x.z, m.z, fmaf(x.w, m.w, acc[r]))));
+            if (TWO) {
+                const float4 x2 = ld4(X2 + (rg + C::NG * r) * C::LD + i);
+                acc2[r] = fmaf(x2.x, m.x, fmaf(x2.y, m.y, fmaf(x2.z, m.z, fmaf(x2.w, m.w, acc2[r]))));
+            }
+        }
+    }
+}
+
+// acc[r] += sum_j X[row r][j] M[j][c]: the "times M" products.
+template <int D, int MB>
+__device__ __forceinline__ void prod_m(float (&acc)[Tiled<D, MB>::RPT], const float *X, const float *M, int c,
+                                       int rg)
+{
+    using C = Tiled<D, MB>;
+#pragma unroll 2
+    for (int j = 0; j < D; j += 4) {
+        const float m0 = M[j * C::LD + c], m1 = M[(j + 1) * C::LD + c];
+        const float m2 = M[(j + 2) * C::LD + c], m3 = M[(j + 3) * C::LD + c];
+#pragma unroll
+        for (int r = 0; r < C::RPT; ++r) {
+            const float4 x = ld4(X + (rg + C::NG * r) * C::LD + j);
+            acc[r] = fmaf(x.x, m0, fmaf(x.y, m1, fmaf(x.z, m2, fmaf(x.w, m3, acc[r]))));
+        }
+    }
+}
+
+// acc[x][y] += sum_t sc_t A[t][row x] B[t][col y] (sc_t = 1 without a scale),
+// with this thread's block rows / columns.
+template <int D, int MB, bool SCALE>
+__device__ __forceinline__ void outer_acc(float (&acc)[Tiled<D, MB>::TB][Tiled<D, MB>::TB], const float *A,
+                                          const float *Bm, const float *sc, int tid)
+{
+    using C = Tiled<D, MB>;
+    const int r0 = 4 * (tid >> 4), c0 = 4 * (tid & 15);
+#pragma unroll 2
+    for (int t = 0; t < MB; ++t) {
+        float a[C::TB], bb[C::TB];
+#pragma unroll
+        for (int q = 0; q < C::TB / 4; ++q) {
+            const float4 av = ld4(A + t * C::LD + r0 + 64 * q);
+            const float4 bv = ld4(Bm + t * C::LD + c0 + 64 * q);
+            a[4 * q] = av.x, a[4 * q + 1] = av.y, a[4 * q + 2] = av.z, a[4 * q + 3] = av.w;
+            bb[4 * q] = bv.x, bb[4 * q + 1] = bv.y, bb[4 * q + 2] = bv.z, bb[4 * q + 3] = bv.w;
+        }
+        if (SCALE) {
+            const float s = sc[t];
+#pragma unroll
+            for (int x = 0; x < C::TB; ++x) a[x] *= s;
+        }
+#pragma unroll
+        for (int x = 0; x < C::TB; ++x)
+#pragma unroll
+            for (int y = 0; y < C::TB; ++y) acc[x][y] = fmaf(a[x], bb[y], acc[x][y]);
+    }
+}
+
+// M[row x][col y] += f * acc[x][y] for this thread's block.
+template <int D, int MB>
+__device__ __forceinline__ void outer_store(float *M, const float (&acc)[Tiled<D, MB>::TB][Tiled<D, MB>::TB],
+                                            float f, int tid)
+{
+    using C = Tiled<D, MB>;
+    const int r0 = 4 * (tid >> 4), c0 = 4 * (tid & 15);
+#pragma unroll
+    for (int qx = 0; qx < C::TB / 4; ++qx)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int qy = 0; qy < C::TB / 4; ++qy) {
+                float *row = M + (r0 + 64 * qx + k) * C::LD + c0 + 64 * qy;
+                float4 v = ld4(row);
+                const int x = 4 * qx + k, y = 4 * qy;
+                v.x = fmaf(f, acc[x][y], v.x);
+                v.y = fmaf(f, acc[x][y + 1], v.y);
+                v.z = fmaf(f, acc[x][y + 2], v.z);
+                v.w = fmaf(f, acc[x][y + 3], v.w);
+                st4(row, v);
+            }
+}
+
+// Key rows (tiled): Yh holds y_s on entry; leaves yh_s in Yh, e_s in E (v_s on
+// entry), g_s in G, r_s and mean(u_s*yh_s) in rk, m2k.
+template <int D, int MB>
+__device__ __forceinline__ void key_rows_t(const SmemT &S, float eps, int warp, int lane)
+{
+    using C = Tiled<D, MB>;
+    constexpr float inv_d = 1.f / (float)D;
+    float y[C::RW][C::EL], mu[C::RW], var[C::RW], m1[C::RW], m2[C::RW], r_[C::RW];
+#pragma unroll
+    for (int r = 0; r < C::RW; ++r) {
+        mu[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < C::EL; ++e) {
+            y[r][e] = S.Yh[(warp + kWarps * r) * C::LD + lane + 32 * e];
+            mu[r] += y[r][e];
+        }
+    }
+    wsum_n(mu);
+#pragma unroll
+    for (int r = 0; r < C::RW; ++r) {
+        mu[r] *= inv_d;
+        var[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < C::EL; ++e) var[r] = fmaf(y[r][e] - mu[r], y[r][e] - mu[r], var[r]);
+    }
+    wsum_n(var);
+#pragma unroll
+    for (int r = 0; r < C::RW; ++r) {
+        const int s = warp + kWarps * r;
+        r_[r] = rsqrtf(var[r] * inv_d + eps);
+        m1[r] = m2[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < C::EL; ++e) {
+            const int j = lane + 32 * e;
+            const float yh = (y[r][e] - mu[r]) * r_[r];
+            const float ee = S.K[s * C::LD + j] + S.gam[j] * yh + S.bet[j] - S.E[s * C::LD + j];
+            const float u = 2.f * S.gam[j] * ee;
+            y[r][e] = yh;
+            S.Yh[s * C::LD + j] = yh;
+            S.E[s * C::LD + j] = ee;
+            m1[r] += u;
+            m2[r] = fmaf(u, yh, m2[r]);
+        }
+    }
+    wsum_n(m1);
+    wsum_n(m2);
+#pragma unroll
+    for (int r = 0; r < C::RW; ++r) {
+        const int s = warp + kWarps * r;
+        m1[r] *= inv_d;
+        m2[r] *= inv_d;
+#pragma unroll
+        for (int e = 0; e < C::EL; ++e) {
+            const int j = lane + 32 * e;
+            S.G[s * C::LD + j] = r_[r] * (2.f * S.gam[j] * S.E[s * C::LD + j] - m1[r] - y[r][e] * m2[r]);
+        }
+        if (lane == 0) {
+            S.rk[s] = r_[r];
+            S.m2k[s] = m2[r];
+        }
+    }
+}
+
+template <typename IO, int D, int MB>
+__global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwdParams p)
+{
+    using C = Tiled<D, MB>;
+    constexpr int LD = C::LD, NG = C::NG, RPT = C::RPT, TB = C::TB, RW = C::RW, EL = C::EL;
+    constexpr float inv_b = 1.f / (float)MB, inv_d = 1.f / (float)D;
+    extern __shared__ __align__(16) float smt[];
+    const SmemT S = carve_t<D, MB>(smt);
+    const int T = p.T, n = T / MB;
+    const int chain = blockIdx.x;
+    const int bi = chain / p.H, hi = chain % p.H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int col = tid % D, rg = tid / D;  // b x D products: column, row group
+    const size_t tok0 = (size_t)chain * T;
+    const IO *Qg = static_cast<const IO *>(p.Q) + tok0 * D;
+    const IO *Kg = static_cast<const IO *>(p.K) + tok0 * D;
+    const IO *Vg = static_cast<const IO *>(p.V) + tok0 * D;
+    const IO *DZg = static_cast<const IO *>(p.dZ) + tok0 * D;
+    const float *eg = p.eta + tok0;
+    float *ws = p.ws + (size_t)chain * n * ((size_t)D * D + D);
+
+    {
+        const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
+        const float *c0 = p.c0 + bi * p.c0_bstride + (long long)hi * D;
+        for (int q = tid; q < D * D / 4; q += kThreads) {
+            const int j = (4 * q) / D, i = (4 * q) % D;
+            st4(S.W + j * LD + i, ld4(W0 + 4 * q));
+            st4(S.dW + j * LD + i, p.dW_n ? ld4(p.dW_n + (size_t)chain * D * D + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f));
+        }
+        for (int j = tid; j < D; j += kThreads) {
+            S.c[j] = c0[j];
+            S.dc[j] = p.dc_n ? p.dc_n[(size_t)chain * D + j] : 0.f;
+            S.gam[j] = p.ln_g[hi * D + j];
+            S.bet[j] = p.ln_b[hi * D + j];
+            S.dgam[j] = 0.f;
+            S.dbet[j] = 0.f;
+        }
+    }
+    auto load_tile = [&](float *dst, const IO *src) {
+        for (int q = tid; q < MB * D / 4; q += kThreads) {
+            const int s = (4 * q) / D, i = (4 * q) % D;
+            st4(dst + s * LD + i, ldg4<IO>(src + 4 * q));
+        }
+    };
+    auto load_eta = [&](int t0) {
+        for (int s = tid; s < MB; s += kThreads) {
+            const float e = eg[t0 + s];
+            S.et[s] = p.eta_gate ? p.eta_base / (1.f + __expf(-e)) : e;
+        }
+    };
+
+    // ---- forward sweep
+    for (int i = 0; i < n; ++i) {
+        const int t0 = i * MB;
+        __syncthreads();
+        float *wsi = ws + (size_t)i * ((size_t)D * D + D);
+        for (int q = tid; q < D * D / 4; q += kThreads) {
+            const int j = (4 * q) / D, ii = (4 * q) % D;
+            st4(wsi + 4 * q, ld4(S.W + j * LD + ii));
+        }
+        for (int j = tid; j < D; j += kThreads) wsi[D * D + j] = S.c[j];
+        load_tile(S.K, Kg + (size_t)t0 * D);
+        load_tile(S.E, Vg + (size_t)t0 * D);
+        load_eta(t0);
+        __syncthreads();
+        {
+            float a[RPT], dummy[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) a[r] = S.c[col];
+            prod_mt<D, MB, false>(a, dummy, S.K, nullptr, S.W, col, rg);
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) S.Yh[(rg + NG * r) * LD + col] = a[r];
+        }
+        __syncthreads();
+        key_rows_t<D, MB>(S, p.eps, warp, lane);
+        __syncthreads();
+        {
+            float acc[TB][TB] = {};
+            outer_acc<D, MB, true>(acc, S.G, S.K, S.et, tid);
+            outer_store<D, MB>(S.W, acc, -inv_b, tid);
+        }
+        for (int j = tid; j < D; j += kThreads) {
+            float a = 0.f;
+#pragma unroll 4
+            for (int s = 0; s < MB; ++s) a = fmaf(S.et[s], S.G[s * LD + j], a);
+            S.c[j] -= a * inv_b;
+        }
+    }
+
+    // ---- reverse sweep
+    for (int i = n - 1; i >= 0; --i) {
+        const int t0 = i * MB;
+        __syncthreads();
+        const float *wsi = ws + (size_t)i * ((size_t)D * D + D);
+        for (int q = tid; q < D * D / 4; q += kThreads) {
+            const int j = (4 * q) / D, ii = (4 * q) % D;
+            st4(S.W + j * LD + ii, ld4(wsi + 4 * q));
+        }
+        for (int j = tid; j < D; j += kThreads) S.c[j] = wsi[D * D + j];
+        load_tile(S.K, Kg + (size_t)t0 * D);
+        load_tile(S.Q, Qg + (size_t)t0 * D);
+        load_tile(S.E, Vg + (size_t)t0 * D);
+        load_tile(S.DZ, DZg + (size_t)t0 * D);
+        load_eta(t0);
+        __syncthreads();
+        // y_s = W k_s + c, W q_t + c; R_s = dW' k_s + dc'; q_t.k_s + 1
+        {
+            float ak[RPT], aq[RPT], ar[RPT], dummy[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                ak[r] = aq[r] = S.c[col];
+                ar[r] = S.dc[col];
+            }
+            prod_mt<D, MB, true>(ak, aq, S.K, S.Q, S.W, col, rg);
+            prod_mt<D, MB, false>(ar, dummy, S.K, nullptr, S.dW, col, rg);
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int s = rg + NG * r;
+                S.Yh[s * LD + col] = ak[r];
+                S.P[s * LD + col] = aq[r];
+                S.R[s * LD + col] = ar[r];
+            }
+        }
+        for (int idx = tid; idx < MB * MB; idx += kThreads) {
+            const int t = idx / MB, s = idx % MB;
+            float acc = 1.f;
+#pragma unroll 4
+            for (int ii = 0; ii < D; ii += 4) {
+                const float4 q = ld4(S.Q + t * LD + ii), k = ld4(S.K + s * LD + ii);
+                acc = fmaf(q.x, k.x, fmaf(q.y, k.y, fmaf(q.z, k.z, fmaf(q.w, k.w, acc))));
+            }
+            S.QK[idx] = acc;
+        }
+        __syncthreads();
+        key_rows_t<D, MB>(S, p.eps, warp, lane);
+        __syncthreads();
+        // p_t = W q_t + c - sum_{s<=t} A_ts g_s
+        {
+            float a[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) a[r] = S.P[(rg + NG * r) * LD + col];
+            for (int s = 0; s < MB; ++s) {
+                const float g = S.G[s * LD + col] * S.et[s] * inv_b;
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int t = rg + NG * r;
+                    if (s <= t) a[r] = fmaf(-S.QK[t * MB + s], g, a[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) S.P[(rg + NG * r) * LD + col] = a[r];
+        }
+        __syncthreads();
+        // output LayerNorm rows: ph_t into P, dp_t into DP
+        {
+            float y[RW][EL], dz[RW][EL], mu[RW], var[RW], a1[RW], a2[RW], rr[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int t = warp + kWarps * r;
+                mu[r] = 0.f;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) {
+                    y[r][e] = S.P[t * LD + lane + 32 * e];
+                    dz[r][e] = S.DZ[t * LD + lane + 32 * e];
+                    mu[r] += y[r][e];
+                }
+            }
+            wsum_n(mu);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                mu[r] *= inv_d;
+                var[r] = 0.f;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) var[r] = fmaf(y[r][e] - mu[r], y[r][e] - mu[r], var[r]);
+            }
+            wsum_n(var);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int t = warp + kWarps * r;
+                rr[r] = rsqrtf(var[r] * inv_d + p.eps);
+                a1[r] = a2[r] = 0.f;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) {
+                    const int j = lane + 32 * e;
+                    const float ph = (y[r][e] - mu[r]) * rr[r], dh = S.gam[j] * dz[r][e];
+                    y[r][e] = ph;
+                    S.P[t * LD + j] = ph;
+                    a1[r] += dh;
+                    a2[r] = fmaf(dh, ph, a2[r]);
+                }
+            }
+            wsum_n(a1);
+            wsum_n(a2);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int t = warp + kWarps * r;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) {
+                    const int j = lane + 32 * e;
+                    S.DP[t * LD + j] = rr[r] * (S.gam[j] * dz[r][e] - a1[r] * inv_d - y[r][e] * a2[r] * inv_d);
+                }
+            }
+        }
+        __syncthreads();
+        for (int j = tid; j < D; j += kThreads) {
+            float ag = 0.f, ab = 0.f;
+#pragma unroll 4
+            for (int t = 0; t < MB; ++t) {
+                ag = fmaf(S.DZ[t * LD + j], S.P[t * LD + j], ag);
+                ab += S.DZ[t * LD + j];
+            }
+            S.dgam[j] += ag;
+            S.dbet[j] += ab;
+        }
+        for (int idx = tid; idx < MB * MB; idx += kThreads) {
+            const int t = idx / MB, s = idx % MB;
+            float acc = 0.f;
+            if (s <= t) {
+#pragma unroll 4
+                for (int j = 0; j < D; j += 4) {
+                    const float4 x = ld4(S.DP + t * LD + j), g = ld4(S.G + s * LD + j);
+                    acc = fmaf(x.x, g.x, fmaf(x.y, g.y, fmaf(x.z, g.z, fmaf(x.w, g.w, acc))));
+                }
+            }
+            S.DA[idx] = -acc;
+        }
+        __syncthreads();
+        // dq_t; dk_s's q- and dW'-parts (KA); dg_s (into P); deta_s
+        {
+            float a[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) a[r] = S.DZ[(rg + NG * r) * LD + col];
+            prod_m<D, MB>(a, S.DP, S.W, col, rg);
+            for (int s = 0; s < MB; ++s) {
+                const float k = S.K[s * LD + col] * S.et[s] * inv_b;
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int t = rg + NG * r;
+                    if (s <= t) a[r] = fmaf(S.DA[t * MB + s], k, a[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) p.dQ[(tok0 + t0 + rg + NG * r) * D + col] = a[r];
+        }
+        {
+            float a[RPT], mix[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) a[r] = mix[r] = 0.f;
+            prod_m<D, MB>(a, S.G, S.dW, col, rg);
+            for (int t = 0; t < MB; ++t) {
+                const float q = S.Q[t * LD + col];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int s = rg + NG * r;
+                    if (t >= s) mix[r] = fmaf(S.DA[t * MB + s], q, mix[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int s = rg + NG * r;
+                S.KA[s * LD + col] = S.et[s] * inv_b * (mix[r] - a[r]);
+            }
+        }
+        {
+            float a[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) a[r] = 0.f;
+            for (int t = 0; t < MB; ++t) {
+                const float x = S.DP[t * LD + col];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int s = rg + NG * r;
+                    if (t >= s) a[r] = fmaf(S.QK[t * MB + s], x, a[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int s = rg + NG * r;
+                S.P[s * LD + col] = -S.et[s] * inv_b * (a[r] + S.R[s * LD + col]);
+            }
+        }
+        for (int s = warp; s < MB; s += kWarps) {
+            float acc = 0.f;
+            for (int t = s + lane; t < MB; t += 32) acc = fmaf(S.DA[t * MB + s], S.QK[t * MB + s], acc);
+#pragma unroll
+            for (int e = 0; e < EL; ++e) acc = fmaf(-S.G[s * LD + lane + 32 * e], S.R[s * LD + lane + 32 * e], acc);
+            acc = wsum(acc);
+            if (lane == 0) S.det[s] = acc * inv_b;
+        }
+        __syncthreads();
+        // through g_s = r_s P_s u_s and the key LayerNorm: dy_s into P, du_s into R, dv_s
+        {
+            float h[RW][EL], yh[RW][EL], u[RW][EL], dyh[RW][EL];
+            float hm[RW], hy[RW], hg[RW], am[RW], ay[RW];
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int s = warp + kWarps * r;
+                hm[r] = hy[r] = hg[r] = 0.f;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) {
+                    const int j = lane + 32 * e;
+                    h[r][e] = S.P[s * LD + j];
+                    yh[r][e] = S.Yh[s * LD + j];
+                    u[r][e] = 2.f * S.gam[j] * S.E[s * LD + j];
+                    hm[r] += h[r][e];
+                    hy[r] = fmaf(h[r][e], yh[r][e], hy[r]);
+                    hg[r] = fmaf(h[r][e], S.G[s * LD + j], hg[r]);
+                }
+            }
+            wsum_n(hm);
+            wsum_n(hy);
+            wsum_n(hg);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int s = warp + kWarps * r;
+                const float rs = S.rk[s], m2 = S.m2k[s];
+                hm[r] *= inv_d;
+                hy[r] *= inv_d;
+                am[r] = ay[r] = 0.f;
+#pragma unroll
+                for (int e = 0; e < EL; ++e) {
+                    const int j = lane + 32 * e;
+                    const float du = rs * (h[r][e] - hm[r] - yh[r][e] * hy[r]);
+                    const float de = 2.f * S.gam[j] * du;
+                    S.R[s * LD + j] = du;
+                    p.dV[(tok0 + t0 + s) * D + j] = -de;
+                    dyh[r][e] = S.gam[j] * de - rs * (h[r][e] * m2 + hy[r] * u[r][e]);
+                    am[r] += dyh[r][e];
+                    ay[r] = fmaf(dyh[r][e], yh[r][e], ay[r]);
+                }
+            }
+            wsum_n(am);
+            wsum_n(ay);
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const int s = warp + kWarps * r;
+                const float rs = S.rk[s], dsig = -rs * hg[r];
+#pragma unroll
+                for (int e = 0; e < EL; ++e) {
+                    const int j = lane + 32 * e;
+                    S.P[s * LD + j] =
+                        rs * (dyh[r][e] - am[r] * inv_d - yh[r][e] * ay[r] * inv_d) + dsig * yh[r][e] * inv_d;
+                }
+            }
+        }
+        __syncthreads();
+        // dk_s; dW, dc carried to batch i - 1; dgamma, dbeta; deta
+        {
+            float a[RPT];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int s = rg + NG * r;
+                a[r] = S.KA[s * LD + col] + 2.f * S.gam[col] * S.R[s * LD + col];
+            }
+            prod_m<D, MB>(a, S.P, S.W, col, rg);
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) p.dK[(tok0 + t0 + rg + NG * r) * D + col] = a[r];
+        }
+        {
+            float acc[TB][TB] = {};
+            outer_acc<D, MB, false>(acc, S.DP, S.Q, nullptr, tid);
+            outer_acc<D, MB, false>(acc, S.P, S.K, nullptr, tid);
+            outer_store<D, MB>(S.dW, acc, 1.f, tid);
+        }
+        for (int j = tid; j < D; j += kThreads) {
+            float ac = 0.f, ag = 0.f, ab = 0.f;
+#pragma unroll 4
+            for (int s = 0; s < MB; ++s) {
+                const float du = S.R[s * LD + j];
+                ac += S.DP[s * LD + j] + S.P[s * LD + j];
+                ag = fmaf(2.f * du, S.gam[j] * S.Yh[s * LD + j] + S.E[s * LD + j], ag);
+                ab = fmaf(2.f * S.gam[j], du, ab);
+            }
+            S.dc[j] += ac;
+            S.dgam[j] += ag;
+            S.dbet[j] += ab;
+        }
+        for (int s = tid; s < MB; s += kThreads) {
+            float v = S.det[s];
+            if (p.eta_gate) {
+                const float sg = 1.f / (1.f + __expf(-eg[t0 + s]));
+                v *= p.eta_base * sg * (1.f - sg);
+            }
+            p.deta[tok0 + t0 + s] = v;
+        }
+    }
+    __syncthreads();
+    bool bad = false;
+    for (int q = tid; q < D * D / 4; q += kThreads) {
+        const int j = (4 * q) / D, ii = (4 * q) % D;
+        const float4 v = ld4(S.dW + j * LD + ii);
+        bad |= !isfinite(v.x) || !isfinite(v.y) || !isfinite(v.z) || !isfinite(v.w);
+        st4(p.dW0 + (size_t)chain * D * D + 4 * q, v);
+    }
+    for (int j = tid; j < D; j += kThreads) {
+        bad |= !isfinite(S.dc[j]) || !isfinite(S.dgam[j]) || !isfinite(S.dbet[j]);
+        p.dc0[(size_t)chain * D + j] = S.dc[j];
+        p.dln_g[(size_t)chain * D + j] = S.dgam[j];
+        p.dln_b[(size_t)chain * D + j] = S.dbet[j];
+    }
+    if (bad && p.status) atomicCAS(p.status, 0, TTT_ERR_NONFINITE);
+}
+
+template <typename IO, int D, int MB>
+cudaError_t launch_tiled(const LinearBwdParams &p, int chains, cudaStream_t s)
+{
+    const size_t smem = sizeof(float) * Tiled<D, MB>::kFloats;
+    cudaError_t e = ensure_smem<linear_bwd_tiled_kernel<IO, D, MB>>((int)smem);
+    if (e != cudaSuccess) return e;
+    linear_bwd_tiled_kernel<IO, D, MB><<<chains, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_bwd_io(const LinearBwdParams &p, int chains, cudaStream_t s, size_t smem_generic)
+{
+    if (p.d == 64 && p.mb == 16) return launch_tiled<IO, 64, 16>(p, chains, s);
+    if (p.d == 128 && p.mb == 16) return launch_tiled<IO, 128, 16>(p, chains, s);
+    cudaError_t e = ensure_smem<linear_bwd_kernel<IO>>((int)smem_generic);
+    if (e != cudaSuccess) return e;
+    linear_bwd_kernel<IO><<<chains, kThreads, smem_generic, s>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t linear_bwd_smem(int d, int mb) { return sizeof(float) * bwd_smem_floats(d, mb); }
@@ -464,16 +1131,7 @@ size_t linear_bwd_workspace_bytes(int B, int H, int T, int d, int mb)
 cudaError_t launch_linear_bwd(const LinearBwdParams &p, int io, int chains, cudaStream_t s)
 {
     const size_t smem = linear_bwd_smem(p.d, p.mb);
-    if (io == TTT_F32) {
-        cudaError_t e = ensure_smem<linear_bwd_kernel<float>>((int)smem);
-        if (e != cudaSuccess) return e;
-        linear_bwd_kernel<float><<<chains, kThreads, smem, s>>>(p);
-    } else {
-        cudaError_t e = ensure_smem<linear_bwd_kernel<__nv_bfloat16>>((int)smem);
-        if (e != cudaSuccess) return e;
-        linear_bwd_kernel<__nv_bfloat16><<<chains, kThreads, smem, s>>>(p);
-    }
-    return cudaGetLastError();
+    return io == TTT_F32 ? launch_bwd_io<float>(p, chains, s, smem) : launch_bwd_io<__nv_bfloat16>(p, chains, s, smem);
 }
 
 }  // namespace ttt
