@@ -52,16 +52,31 @@ TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 
 
-def sources_sha1() -> str:
-    """sha1 over the CUDA sources of the library (kernels + headers)."""
+# The source files each profiled kernel is built from (its .cu and the headers it includes).
+KERNEL_SOURCES = {
+    "linear_tc": ["ttt_linear_tc.cu", "tc_common.cuh", "ptx.cuh", "ttt_internal.h"],
+    "mlp_tc": ["ttt_mlp_tc.cu", "tc_common.cuh", "ptx.cuh", "ttt_internal.h"],
+    "linear_bwd": ["ttt_linear_bwd.cu", "ttt_internal.h"],
+}
+
+
+def sources_sha1(files=None) -> str:
+    """sha1 over CUDA sources of the library: the named files of csrc/, or all
+    kernels and headers."""
     import glob
     import hashlib
     h = hashlib.sha1()
-    for f in sorted(glob.glob(os.path.join(CSRC, "*"))):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(f, "rb") as fh:
-                h.update(os.path.basename(f).encode())
-                h.update(fh.read())
+    if files is None:
+        paths = [f for f in sorted(glob.glob(os.path.join(CSRC, "*"))) if f.endswith((".cu", ".cuh", ".h"))]
+    else:
+        paths = [os.path.join(CSRC, f) for f in sorted(files)]
+    for f in paths:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    include = os.path.join(ROOT, "include", "ttt.h")
+    with open(include, "rb") as fh:
+        h.update(fh.read())
     return h.hexdigest()
 
 
@@ -74,7 +89,7 @@ def measured_traffic(workload: str, z_dtype: str, key: str = None):
     except (OSError, ValueError):
         return None
     e = j.get(key or "%s/z_%s" % (workload, z_dtype))
-    if not e or e.get("sources_sha1") != sources_sha1():
+    if not e or e.get("sources_sha1") != sources_sha1(e.get("sources")):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -451,19 +451,23 @@ __global__ void __launch_bounds__(kThreads) linear_bwd_kernel(LinearBwdParams p)
 // The same steps with the sizes fixed at compile time. Rows of every b x D
 // tile and of W, dW are padded to LD = D + 4 floats: 16-byte rows, so float4
 // loads along a row are free of bank conflicts whichever rows the lanes hold.
-// Each thread keeps RPT accumulators (rows rg, rg + NG, ... of one column) for
-// the b x D products and a TB x TB block (rows / columns 4 (tid / 16) + 64 q + k
-// and 4 (tid % 16) + 64 q + k) for the D x D outer products; the LayerNorm rows
-// of a warp are reduced together. The workspace layout is the general kernel's.
-template <int D, int MB>
+// NT threads. Each thread keeps RPT accumulators (rows rg, rg + NG, ... of one
+// column) for the b x D products and a TR x TC block (rows tid / 16 + (NT / 16) x,
+// columns 4 (tid % 16) + 64 q + k) for the D x D outer products; the LayerNorm
+// rows of a warp are reduced together. The workspace layout is the general
+// kernel's.
+template <int D, int MB, int NT>
 struct Tiled {
     static constexpr int LD = D + 4;
-    static constexpr int NG = kThreads / D;  // row groups of the b x D products
+    static constexpr int NW = NT / 32;       // warps
+    static constexpr int NG = NT / D;        // row groups of the b x D products
     static constexpr int RPT = MB / NG;      // rows per thread
-    static constexpr int TB = D / 16;        // outer-product block edge
-    static constexpr int RW = MB / kWarps;   // LayerNorm rows per warp
+    static constexpr int TR = D * 16 / NT;   // outer-product rows per thread (strided by NT / 16)
+    static constexpr int TC = D / 16;        // outer-product columns per thread (float4 groups 64 apart)
+    static constexpr int RW = MB / NW;       // LayerNorm rows per warp
     static constexpr int EL = D / 32;        // row elements per lane
-    static_assert(NG * D == kThreads && RPT * NG == MB && RW * kWarps == MB && EL * 32 == D && TB % 4 == 0,
+    static_assert(NG * D == NT && RPT * NG == MB && RW * NW == MB && EL * 32 == D && TC % 4 == 0 &&
+                      TR * (NT / 16) == D,
                   "tiling");
     static constexpr size_t kFloats = 2 * (size_t)D * LD + 6 * D + 10 * (size_t)MB * LD + 2 * MB * MB + 4 * MB;
 };
@@ -474,10 +478,10 @@ struct SmemT {
     float *QK, *DA, *et, *det, *rk, *m2k;
 };
 
-template <int D, int MB>
+template <int D, int MB, int NT>
 __device__ SmemT carve_t(float *sm)
 {
-    using C = Tiled<D, MB>;
+    using C = Tiled<D, MB, NT>;
     SmemT s;
     float *p = sm;
     auto take = [&](size_t n) { float *q = p; p += n; return q; };
@@ -534,11 +538,11 @@ __device__ __forceinline__ void wsum_n(float (&v)[N])
 }
 
 // acc[r] += sum_i X[row r][i] M[c][i] (and acc2 with X2): the "times M^T" products.
-template <int D, int MB, bool TWO>
-__device__ __forceinline__ void prod_mt(float (&acc)[Tiled<D, MB>::RPT], float (&acc2)[Tiled<D, MB>::RPT],
+template <int D, int MB, int NT, bool TWO>
+__device__ __forceinline__ void prod_mt(float (&acc)[Tiled<D, MB, NT>::RPT], float (&acc2)[Tiled<D, MB, NT>::RPT],
                                         const float *X, const float *X2, const float *M, int c, int rg)
 {
-    using C = Tiled<D, MB>;
+    using C = Tiled<D, MB, NT>;
 #pragma unroll 4
     for (int i = 0; i < D; i += 4) {
         const float4 m = ld4(M + c * C::LD + i);
@@ -555,11 +559,11 @@ __device__ __forceinline__ void prod_mt(float (&acc)[Tiled<D, MB>::RPT], float (
 }
 
 // acc[r] += sum_j X[row r][j] M[j][c]: the "times M" products.
-template <int D, int MB>
-__device__ __forceinline__ void prod_m(float (&acc)[Tiled<D, MB>::RPT], const float *X, const float *M, int c,
+template <int D, int MB, int NT>
+__device__ __forceinline__ void prod_m(float (&acc)[Tiled<D, MB, NT>::RPT], const float *X, const float *M, int c,
                                        int rg)
 {
-    using C = Tiled<D, MB>;
+    using C = Tiled<D, MB, NT>;
 #pragma unroll 2
     for (int j = 0; j < D; j += 4) {
         const float m0 = M[j * C::LD + c], m1 = M[(j + 1) * C::LD + c];
@@ -574,64 +578,61 @@ __device__ __forceinline__ void prod_m(float (&acc)[Tiled<D, MB>::RPT], const fl
 
 // acc[x][y] += sum_t sc_t A[t][row x] B[t][col y] (sc_t = 1 without a scale),
 // with this thread's block rows / columns.
-template <int D, int MB, bool SCALE>
-__device__ __forceinline__ void outer_acc(float (&acc)[Tiled<D, MB>::TB][Tiled<D, MB>::TB], const float *A,
-                                          const float *Bm, const float *sc, int tid)
+template <int D, int MB, int NT, bool SCALE>
+__device__ __forceinline__ void outer_acc(float (&acc)[Tiled<D, MB, NT>::TR][Tiled<D, MB, NT>::TC],
+                                          const float *A, const float *Bm, const float *sc, int tid)
 {
-    using C = Tiled<D, MB>;
-    const int r0 = 4 * (tid >> 4), c0 = 4 * (tid & 15);
+    using C = Tiled<D, MB, NT>;
+    const int r0 = tid >> 4, c0 = 4 * (tid & 15);
 #pragma unroll 2
     for (int t = 0; t < MB; ++t) {
-        float a[C::TB], bb[C::TB];
+        float a[C::TR], bb[C::TC];
 #pragma unroll
-        for (int q = 0; q < C::TB / 4; ++q) {
-            const float4 av = ld4(A + t * C::LD + r0 + 64 * q);
+        for (int x = 0; x < C::TR; ++x) a[x] = A[t * C::LD + r0 + (NT / 16) * x];
+#pragma unroll
+        for (int q = 0; q < C::TC / 4; ++q) {
             const float4 bv = ld4(Bm + t * C::LD + c0 + 64 * q);
-            a[4 * q] = av.x, a[4 * q + 1] = av.y, a[4 * q + 2] = av.z, a[4 * q + 3] = av.w;
             bb[4 * q] = bv.x, bb[4 * q + 1] = bv.y, bb[4 * q + 2] = bv.z, bb[4 * q + 3] = bv.w;
         }
         if (SCALE) {
             const float s = sc[t];
 #pragma unroll
-            for (int x = 0; x < C::TB; ++x) a[x] *= s;
+            for (int x = 0; x < C::TR; ++x) a[x] *= s;
         }
 #pragma unroll
-        for (int x = 0; x < C::TB; ++x)
+        for (int x = 0; x < C::TR; ++x)
 #pragma unroll
-            for (int y = 0; y < C::TB; ++y) acc[x][y] = fmaf(a[x], bb[y], acc[x][y]);
+            for (int y = 0; y < C::TC; ++y) acc[x][y] = fmaf(a[x], bb[y], acc[x][y]);
     }
 }
 
 // M[row x][col y] += f * acc[x][y] for this thread's block.
-template <int D, int MB>
-__device__ __forceinline__ void outer_store(float *M, const float (&acc)[Tiled<D, MB>::TB][Tiled<D, MB>::TB],
+template <int D, int MB, int NT>
+__device__ __forceinline__ void outer_store(float *M, const float (&acc)[Tiled<D, MB, NT>::TR][Tiled<D, MB, NT>::TC],
                                             float f, int tid)
 {
-    using C = Tiled<D, MB>;
-    const int r0 = 4 * (tid >> 4), c0 = 4 * (tid & 15);
+    using C = Tiled<D, MB, NT>;
+    const int r0 = tid >> 4, c0 = 4 * (tid & 15);
 #pragma unroll
-    for (int qx = 0; qx < C::TB / 4; ++qx)
+    for (int x = 0; x < C::TR; ++x)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int qy = 0; qy < C::TB / 4; ++qy) {
-                float *row = M + (r0 + 64 * qx + k) * C::LD + c0 + 64 * qy;
-                float4 v = ld4(row);
-                const int x = 4 * qx + k, y = 4 * qy;
-                v.x = fmaf(f, acc[x][y], v.x);
-                v.y = fmaf(f, acc[x][y + 1], v.y);
-                v.z = fmaf(f, acc[x][y + 2], v.z);
-                v.w = fmaf(f, acc[x][y + 3], v.w);
-                st4(row, v);
-            }
+        for (int q = 0; q < C::TC / 4; ++q) {
+            float *row = M + (r0 + (NT / 16) * x) * C::LD + c0 + 64 * q;
+            float4 v = ld4(row);
+            v.x = fmaf(f, acc[x][4 * q], v.x);
+            v.y = fmaf(f, acc[x][4 * q + 1], v.y);
+            v.z = fmaf(f, acc[x][4 * q + 2], v.z);
+            v.w = fmaf(f, acc[x][4 * q + 3], v.w);
+            st4(row, v);
+        }
 }
 
 // Key rows (tiled): Yh holds y_s on entry; leaves yh_s in Yh, e_s in E (v_s on
 // entry), g_s in G, r_s and mean(u_s*yh_s) in rk, m2k.
-template <int D, int MB>
+template <int D, int MB, int NT>
 __device__ __forceinline__ void key_rows_t(const SmemT &S, float eps, int warp, int lane)
 {
-    using C = Tiled<D, MB>;
+    using C = Tiled<D, MB, NT>;
     constexpr float inv_d = 1.f / (float)D;
     float y[C::RW][C::EL], mu[C::RW], var[C::RW], m1[C::RW], m2[C::RW], r_[C::RW];
 #pragma unroll
@@ -639,7 +640,7 @@ __device__ __forceinline__ void key_rows_t(const SmemT &S, float eps, int warp, 
         mu[r] = 0.f;
 #pragma unroll
         for (int e = 0; e < C::EL; ++e) {
-            y[r][e] = S.Yh[(warp + kWarps * r) * C::LD + lane + 32 * e];
+            y[r][e] = S.Yh[(warp + C::NW * r) * C::LD + lane + 32 * e];
             mu[r] += y[r][e];
         }
     }
@@ -654,7 +655,7 @@ __device__ __forceinline__ void key_rows_t(const SmemT &S, float eps, int warp, 
     wsum_n(var);
 #pragma unroll
     for (int r = 0; r < C::RW; ++r) {
-        const int s = warp + kWarps * r;
+        const int s = warp + C::NW * r;
         r_[r] = rsqrtf(var[r] * inv_d + eps);
         m1[r] = m2[r] = 0.f;
 #pragma unroll
@@ -674,7 +675,7 @@ __device__ __forceinline__ void key_rows_t(const SmemT &S, float eps, int warp, 
     wsum_n(m2);
 #pragma unroll
     for (int r = 0; r < C::RW; ++r) {
-        const int s = warp + kWarps * r;
+        const int s = warp + C::NW * r;
         m1[r] *= inv_d;
         m2[r] *= inv_d;
 #pragma unroll
@@ -689,14 +690,14 @@ __device__ __forceinline__ void key_rows_t(const SmemT &S, float eps, int warp, 
     }
 }
 
-template <typename IO, int D, int MB>
-__global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwdParams p)
+template <typename IO, int D, int MB, int NT>
+__global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams p)
 {
-    using C = Tiled<D, MB>;
-    constexpr int LD = C::LD, NG = C::NG, RPT = C::RPT, TB = C::TB, RW = C::RW, EL = C::EL;
+    using C = Tiled<D, MB, NT>;
+    constexpr int LD = C::LD, NG = C::NG, RPT = C::RPT, RW = C::RW, EL = C::EL, NW = C::NW;
     constexpr float inv_b = 1.f / (float)MB, inv_d = 1.f / (float)D;
     extern __shared__ __align__(16) float smt[];
-    const SmemT S = carve_t<D, MB>(smt);
+    const SmemT S = carve_t<D, MB, NT>(smt);
     const int T = p.T, n = T / MB;
     const int chain = blockIdx.x;
     const int bi = chain / p.H, hi = chain % p.H;
@@ -713,12 +714,12 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
     {
         const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
         const float *c0 = p.c0 + bi * p.c0_bstride + (long long)hi * D;
-        for (int q = tid; q < D * D / 4; q += kThreads) {
+        for (int q = tid; q < D * D / 4; q += NT) {
             const int j = (4 * q) / D, i = (4 * q) % D;
             st4(S.W + j * LD + i, ld4(W0 + 4 * q));
             st4(S.dW + j * LD + i, p.dW_n ? ld4(p.dW_n + (size_t)chain * D * D + 4 * q) : make_float4(0.f, 0.f, 0.f, 0.f));
         }
-        for (int j = tid; j < D; j += kThreads) {
+        for (int j = tid; j < D; j += NT) {
             S.c[j] = c0[j];
             S.dc[j] = p.dc_n ? p.dc_n[(size_t)chain * D + j] : 0.f;
             S.gam[j] = p.ln_g[hi * D + j];
@@ -728,13 +729,13 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
         }
     }
     auto load_tile = [&](float *dst, const IO *src) {
-        for (int q = tid; q < MB * D / 4; q += kThreads) {
+        for (int q = tid; q < MB * D / 4; q += NT) {
             const int s = (4 * q) / D, i = (4 * q) % D;
             st4(dst + s * LD + i, ldg4<IO>(src + 4 * q));
         }
     };
     auto load_eta = [&](int t0) {
-        for (int s = tid; s < MB; s += kThreads) {
+        for (int s = tid; s < MB; s += NT) {
             const float e = eg[t0 + s];
             S.et[s] = p.eta_gate ? p.eta_base / (1.f + __expf(-e)) : e;
         }
@@ -745,11 +746,11 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
         const int t0 = i * MB;
         __syncthreads();
         float *wsi = ws + (size_t)i * ((size_t)D * D + D);
-        for (int q = tid; q < D * D / 4; q += kThreads) {
+        for (int q = tid; q < D * D / 4; q += NT) {
             const int j = (4 * q) / D, ii = (4 * q) % D;
             st4(wsi + 4 * q, ld4(S.W + j * LD + ii));
         }
-        for (int j = tid; j < D; j += kThreads) wsi[D * D + j] = S.c[j];
+        for (int j = tid; j < D; j += NT) wsi[D * D + j] = S.c[j];
         load_tile(S.K, Kg + (size_t)t0 * D);
         load_tile(S.E, Vg + (size_t)t0 * D);
         load_eta(t0);
@@ -758,19 +759,19 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             float a[RPT], dummy[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) a[r] = S.c[col];
-            prod_mt<D, MB, false>(a, dummy, S.K, nullptr, S.W, col, rg);
+            prod_mt<D, MB, NT, false>(a, dummy, S.K, nullptr, S.W, col, rg);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) S.Yh[(rg + NG * r) * LD + col] = a[r];
         }
         __syncthreads();
-        key_rows_t<D, MB>(S, p.eps, warp, lane);
+        key_rows_t<D, MB, NT>(S, p.eps, warp, lane);
         __syncthreads();
         {
-            float acc[TB][TB] = {};
-            outer_acc<D, MB, true>(acc, S.G, S.K, S.et, tid);
-            outer_store<D, MB>(S.W, acc, -inv_b, tid);
+            float acc[C::TR][C::TC] = {};
+            outer_acc<D, MB, NT, true>(acc, S.G, S.K, S.et, tid);
+            outer_store<D, MB, NT>(S.W, acc, -inv_b, tid);
         }
-        for (int j = tid; j < D; j += kThreads) {
+        for (int j = tid; j < D; j += NT) {
             float a = 0.f;
 #pragma unroll 4
             for (int s = 0; s < MB; ++s) a = fmaf(S.et[s], S.G[s * LD + j], a);
@@ -783,11 +784,11 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
         const int t0 = i * MB;
         __syncthreads();
         const float *wsi = ws + (size_t)i * ((size_t)D * D + D);
-        for (int q = tid; q < D * D / 4; q += kThreads) {
+        for (int q = tid; q < D * D / 4; q += NT) {
             const int j = (4 * q) / D, ii = (4 * q) % D;
             st4(S.W + j * LD + ii, ld4(wsi + 4 * q));
         }
-        for (int j = tid; j < D; j += kThreads) S.c[j] = wsi[D * D + j];
+        for (int j = tid; j < D; j += NT) S.c[j] = wsi[D * D + j];
         load_tile(S.K, Kg + (size_t)t0 * D);
         load_tile(S.Q, Qg + (size_t)t0 * D);
         load_tile(S.E, Vg + (size_t)t0 * D);
@@ -802,8 +803,8 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
                 ak[r] = aq[r] = S.c[col];
                 ar[r] = S.dc[col];
             }
-            prod_mt<D, MB, true>(ak, aq, S.K, S.Q, S.W, col, rg);
-            prod_mt<D, MB, false>(ar, dummy, S.K, nullptr, S.dW, col, rg);
+            prod_mt<D, MB, NT, true>(ak, aq, S.K, S.Q, S.W, col, rg);
+            prod_mt<D, MB, NT, false>(ar, dummy, S.K, nullptr, S.dW, col, rg);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const int s = rg + NG * r;
@@ -812,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
                 S.R[s * LD + col] = ar[r];
             }
         }
-        for (int idx = tid; idx < MB * MB; idx += kThreads) {
+        for (int idx = tid; idx < MB * MB; idx += NT) {
             const int t = idx / MB, s = idx % MB;
             float acc = 1.f;
 #pragma unroll 4
@@ -823,7 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             S.QK[idx] = acc;
         }
         __syncthreads();
-        key_rows_t<D, MB>(S, p.eps, warp, lane);
+        key_rows_t<D, MB, NT>(S, p.eps, warp, lane);
         __syncthreads();
         // p_t = W q_t + c - sum_{s<=t} A_ts g_s
         {
@@ -847,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             float y[RW][EL], dz[RW][EL], mu[RW], var[RW], a1[RW], a2[RW], rr[RW];
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
-                const int t = warp + kWarps * r;
+                const int t = warp + NW * r;
                 mu[r] = 0.f;
 #pragma unroll
                 for (int e = 0; e < EL; ++e) {
@@ -867,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             wsum_n(var);
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
-                const int t = warp + kWarps * r;
+                const int t = warp + NW * r;
                 rr[r] = rsqrtf(var[r] * inv_d + p.eps);
                 a1[r] = a2[r] = 0.f;
 #pragma unroll
@@ -884,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             wsum_n(a2);
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
-                const int t = warp + kWarps * r;
+                const int t = warp + NW * r;
 #pragma unroll
                 for (int e = 0; e < EL; ++e) {
                     const int j = lane + 32 * e;
@@ -893,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             }
         }
         __syncthreads();
-        for (int j = tid; j < D; j += kThreads) {
+        for (int j = tid; j < D; j += NT) {
             float ag = 0.f, ab = 0.f;
 #pragma unroll 4
             for (int t = 0; t < MB; ++t) {
@@ -903,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             S.dgam[j] += ag;
             S.dbet[j] += ab;
         }
-        for (int idx = tid; idx < MB * MB; idx += kThreads) {
+        for (int idx = tid; idx < MB * MB; idx += NT) {
             const int t = idx / MB, s = idx % MB;
             float acc = 0.f;
             if (s <= t) {
@@ -921,7 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             float a[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) a[r] = S.DZ[(rg + NG * r) * LD + col];
-            prod_m<D, MB>(a, S.DP, S.W, col, rg);
+            prod_m<D, MB, NT>(a, S.DP, S.W, col, rg);
             for (int s = 0; s < MB; ++s) {
                 const float k = S.K[s * LD + col] * S.et[s] * inv_b;
 #pragma unroll
@@ -937,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             float a[RPT], mix[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) a[r] = mix[r] = 0.f;
-            prod_m<D, MB>(a, S.G, S.dW, col, rg);
+            prod_m<D, MB, NT>(a, S.G, S.dW, col, rg);
             for (int t = 0; t < MB; ++t) {
                 const float q = S.Q[t * LD + col];
 #pragma unroll
@@ -970,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
                 S.P[s * LD + col] = -S.et[s] * inv_b * (a[r] + S.R[s * LD + col]);
             }
         }
-        for (int s = warp; s < MB; s += kWarps) {
+        for (int s = warp; s < MB; s += NW) {
             float acc = 0.f;
             for (int t = s + lane; t < MB; t += 32) acc = fmaf(S.DA[t * MB + s], S.QK[t * MB + s], acc);
 #pragma unroll
@@ -985,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             float hm[RW], hy[RW], hg[RW], am[RW], ay[RW];
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
-                const int s = warp + kWarps * r;
+                const int s = warp + NW * r;
                 hm[r] = hy[r] = hg[r] = 0.f;
 #pragma unroll
                 for (int e = 0; e < EL; ++e) {
@@ -1003,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             wsum_n(hg);
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
-                const int s = warp + kWarps * r;
+                const int s = warp + NW * r;
                 const float rs = S.rk[s], m2 = S.m2k[s];
                 hm[r] *= inv_d;
                 hy[r] *= inv_d;
@@ -1024,7 +1025,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             wsum_n(ay);
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
-                const int s = warp + kWarps * r;
+                const int s = warp + NW * r;
                 const float rs = S.rk[s], dsig = -rs * hg[r];
 #pragma unroll
                 for (int e = 0; e < EL; ++e) {
@@ -1043,17 +1044,17 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
                 const int s = rg + NG * r;
                 a[r] = S.KA[s * LD + col] + 2.f * S.gam[col] * S.R[s * LD + col];
             }
-            prod_m<D, MB>(a, S.P, S.W, col, rg);
+            prod_m<D, MB, NT>(a, S.P, S.W, col, rg);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) p.dK[(tok0 + t0 + rg + NG * r) * D + col] = a[r];
         }
         {
-            float acc[TB][TB] = {};
-            outer_acc<D, MB, false>(acc, S.DP, S.Q, nullptr, tid);
-            outer_acc<D, MB, false>(acc, S.P, S.K, nullptr, tid);
-            outer_store<D, MB>(S.dW, acc, 1.f, tid);
+            float acc[C::TR][C::TC] = {};
+            outer_acc<D, MB, NT, false>(acc, S.DP, S.Q, nullptr, tid);
+            outer_acc<D, MB, NT, false>(acc, S.P, S.K, nullptr, tid);
+            outer_store<D, MB, NT>(S.dW, acc, 1.f, tid);
         }
-        for (int j = tid; j < D; j += kThreads) {
+        for (int j = tid; j < D; j += NT) {
             float ac = 0.f, ag = 0.f, ab = 0.f;
 #pragma unroll 4
             for (int s = 0; s < MB; ++s) {
@@ -1066,7 +1067,7 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
             S.dgam[j] += ag;
             S.dbet[j] += ab;
         }
-        for (int s = tid; s < MB; s += kThreads) {
+        for (int s = tid; s < MB; s += NT) {
             float v = S.det[s];
             if (p.eta_gate) {
                 const float sg = 1.f / (1.f + __expf(-eg[t0 + s]));
@@ -1077,13 +1078,13 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
     }
     __syncthreads();
     bool bad = false;
-    for (int q = tid; q < D * D / 4; q += kThreads) {
+    for (int q = tid; q < D * D / 4; q += NT) {
         const int j = (4 * q) / D, ii = (4 * q) % D;
         const float4 v = ld4(S.dW + j * LD + ii);
         bad |= !isfinite(v.x) || !isfinite(v.y) || !isfinite(v.z) || !isfinite(v.w);
         st4(p.dW0 + (size_t)chain * D * D + 4 * q, v);
     }
-    for (int j = tid; j < D; j += kThreads) {
+    for (int j = tid; j < D; j += NT) {
         bad |= !isfinite(S.dc[j]) || !isfinite(S.dgam[j]) || !isfinite(S.dbet[j]);
         p.dc0[(size_t)chain * D + j] = S.dc[j];
         p.dln_g[(size_t)chain * D + j] = S.dgam[j];
@@ -1092,21 +1093,21 @@ __global__ void __launch_bounds__(kThreads, 1) linear_bwd_tiled_kernel(LinearBwd
     if (bad && p.status) atomicCAS(p.status, 0, TTT_ERR_NONFINITE);
 }
 
-template <typename IO, int D, int MB>
+template <typename IO, int D, int MB, int NT>
 cudaError_t launch_tiled(const LinearBwdParams &p, int chains, cudaStream_t s)
 {
-    const size_t smem = sizeof(float) * Tiled<D, MB>::kFloats;
-    cudaError_t e = ensure_smem<linear_bwd_tiled_kernel<IO, D, MB>>((int)smem);
+    const size_t smem = sizeof(float) * Tiled<D, MB, NT>::kFloats;
+    cudaError_t e = ensure_smem<linear_bwd_tiled_kernel<IO, D, MB, NT>>((int)smem);
     if (e != cudaSuccess) return e;
-    linear_bwd_tiled_kernel<IO, D, MB><<<chains, kThreads, smem, s>>>(p);
+    linear_bwd_tiled_kernel<IO, D, MB, NT><<<chains, NT, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 template <typename IO>
 cudaError_t launch_bwd_io(const LinearBwdParams &p, int chains, cudaStream_t s, size_t smem_generic)
 {
-    if (p.d == 64 && p.mb == 16) return launch_tiled<IO, 64, 16>(p, chains, s);
-    if (p.d == 128 && p.mb == 16) return launch_tiled<IO, 128, 16>(p, chains, s);
+    if (p.d == 64 && p.mb == 16) return launch_tiled<IO, 64, 16, 256>(p, chains, s);
+    if (p.d == 128 && p.mb == 16) return launch_tiled<IO, 128, 16, 512>(p, chains, s);
     cudaError_t e = ensure_smem<linear_bwd_kernel<IO>>((int)smem_generic);
     if (e != cudaSuccess) return e;
     linear_bwd_kernel<IO><<<chains, kThreads, smem_generic, s>>>(p);
