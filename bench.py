@@ -19,11 +19,12 @@ fp64 CPU oracle on a bounded sample of the same workload.
 ``--impl reference`` runs the reference arm: the fp64 CPU oracle as it stands,
 one bounded sample of the workload per step, on the host cores.
 
-``--backward`` (TTT-Linear) times the outer-loop gradient instead: one step is
-one ``ttt_linear_backward`` call over the workload (forward recompute with
-every mini-batch's starting state kept, then the reverse sweep), with seeded
-upstream gradients dZ and final-state seeds. Its roofline is the fp32 FMA
-rate, since the kernel does its contractions on the CUDA cores.
+``--backward`` times the outer-loop gradient instead: one step is one
+``ttt_linear_backward`` (or, for a TTT-MLP workload, ``ttt_mlp_backward``) call
+over the workload (forward recompute with every mini-batch's starting state
+kept, then the reverse sweep), with seeded upstream gradients dZ and
+final-state seeds. Its roofline is the fp32 FMA rate, since the kernels do
+their contractions on the CUDA cores.
 """
 from __future__ import annotations
 
@@ -119,18 +120,26 @@ def algorithmic_cost(w, z_bytes: int = 4, out_rule: str = "prefix"):
 
 
 def backward_cost(w):
-    """Per-launch algorithmic bytes and FLOPs of ttt_linear_backward.
+    """Per-launch algorithmic bytes and FLOPs of ttt_linear_backward /
+    ttt_mlp_backward.
 
-    Bytes: Q, K, V, dZ read twice (forward sweep reads K, V; reverse reads all
-    four), eta twice, dQ, dK, dV written fp32, deta fp32, plus every mini-batch's
-    (W, c) written once and read once. FLOPs: per mini-batch of b tokens the
-    contractions 10 b d^2 (forward recompute 2, reverse 8) + b^2 d (Q K^T) +
-    5 b(b+1)/2 d (the five causal b x b x d products), times 2."""
+    Bytes: K, V read by the forward sweep and Q, K, V, dZ by the reverse one
+    (io dtype), eta twice, dQ, dK, dV, deta written fp32, plus every
+    mini-batch's starting state written once and read once. FLOPs, per
+    mini-batch of b tokens, the contractions as executed: TTT-Linear
+    10 b d^2 (forward recompute 2, reverse 8) + b^2 d (Q K^T) + 5 b(b+1)/2 d
+    (the causal b x b x d products); TTT-MLP 25 b h d (forward recompute 5,
+    reverse 20) + b^2 (d + h) (the two Grams) + 5 b(b+1)/2 (d + h); times 2."""
     es = 2 if w.io == "bf16" else 4
     d, b = w.d, w.b
     per_tok = (2 * d * es) + (4 * d * es) + 2 * 4 + 3 * d * 4 + 4
-    state = w.chains * (w.T // b) * (d * d + d) * 4 * 2
-    flops_tok = 2 * (10 * d * d + b * d) + 5 * (b + 1) * d
+    if w.variant == "linear":
+        state = w.chains * (w.T // b) * (d * d + d) * 4 * 2
+        flops_tok = 2 * (10 * d * d + b * d) + 5 * (b + 1) * d
+    else:
+        h = w.hidden
+        state = w.chains * (w.T // b) * (2 * h * d + h + d) * 4 * 2
+        flops_tok = 2 * (25 * h * d + b * (d + h)) + 5 * (b + 1) * (d + h)
     return per_tok * w.tokens + state, flops_tok * w.tokens
 
 
@@ -262,15 +271,20 @@ def oracle_backward_sample(w, n_chains: int, T: int):
     """Run the fp64 backward oracle (torch autograd through the primal token
     loop) on the first ``n_chains`` chains, first ``T`` tokens. Returns
     (seconds, tokens processed, threads used)."""
-    from oracle.backward import ttt_linear_backward
+    from oracle.backward import ttt_linear_backward, ttt_mlp_backward
     sel = list(range(n_chains))
     inp = make_inputs(w.with_(T=T), chains=sel)
     cot = make_cotangents(w.with_(T=T), chains=sel)
     f = lambda t: t.detach().double().numpy()
     t0 = time.perf_counter()
-    ttt_linear_backward(f(inp["Q"]), f(inp["K"]), f(inp["V"]), f(inp["eta"]), f(inp["W0"]), f(inp["c0"]),
-                        f(inp["ln_g"]), f(inp["ln_b"]), f(cot["dZ"]), f(cot["dW_n"]), f(cot["dc_n"]), b=w.b,
-                        eps=w.eps)
+    if w.variant == "linear":
+        ttt_linear_backward(f(inp["Q"]), f(inp["K"]), f(inp["V"]), f(inp["eta"]), f(inp["W0"]), f(inp["c0"]),
+                            f(inp["ln_g"]), f(inp["ln_b"]), f(cot["dZ"]), f(cot["dW_n"]), f(cot["dc_n"]), b=w.b,
+                            eps=w.eps)
+    else:
+        ttt_mlp_backward(*(f(inp[k]) for k in ("Q", "K", "V", "eta", "W1", "c1", "W2", "c2", "ln_g", "ln_b")),
+                         f(cot["dZ"]), *(f(cot[k]) for k in ("dW1_n", "dc1_n", "dW2_n", "dc2_n")), b=w.b,
+                         eps=w.eps)
     return time.perf_counter() - t0, n_chains * T, torch.get_num_threads()
 
 
@@ -289,7 +303,7 @@ def _backward_sample_shape(w, seconds: float):
 # ---------------------------------------------------------------- GPU arm
 
 def run_gpu_backward(args):
-    """The --backward leg: ttt_linear_backward over the whole workload."""
+    """The --backward leg: ttt_linear_backward / ttt_mlp_backward over the whole workload."""
     import test_weight_sequence_ttt_b300 as ttt
     from test_weight_sequence_ttt_b300 import shard
 
@@ -298,20 +312,31 @@ def run_gpu_backward(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     w = WORKLOADS[args.workload]
-    if w.variant != "linear" or w.partial_tail or w.T % w.b:
-        raise SystemExit("--backward needs a TTT-Linear workload with T a multiple of mb")
+    if w.partial_tail or w.T % w.b:
+        raise SystemExit("--backward needs a workload with T a multiple of mb")
     wr = w.with_(seed=w.seed + 7919 * rank)
     inp = dict(make_inputs(wr), **make_cotangents(wr))
     eta_key = "eta_logit" if args.eta_gate else "eta"
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     stream = torch.cuda.current_stream()
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ws = torch.empty(ttt.linear_backward_workspace_bytes(w.B, w.H, w.T, w.d, w.b), dtype=torch.uint8,
-                     device="cuda")
-    call = lambda o: ttt.ttt_linear_backward(dev["Q"], dev["K"], dev["V"], dev[eta_key], dev["W0"], dev["c0"],
-                                             dev["ln_g"], dev["ln_b"], dev["dZ"], mb=w.b, dW_n=dev["dW_n"],
-                                             dc_n=dev["dc_n"], eps=w.eps, out=o, workspace=ws, status=st,
-                                             stream=stream, eta_gate=args.eta_gate, eta_base=w.eta_base)
+    if w.variant == "linear":
+        ws = torch.empty(ttt.linear_backward_workspace_bytes(w.B, w.H, w.T, w.d, w.b), dtype=torch.uint8,
+                         device="cuda")
+        seeds = ("dW_n", "dc_n")
+        call = lambda o: ttt.ttt_linear_backward(dev["Q"], dev["K"], dev["V"], dev[eta_key], dev["W0"], dev["c0"],
+                                                 dev["ln_g"], dev["ln_b"], dev["dZ"], mb=w.b, dW_n=dev["dW_n"],
+                                                 dc_n=dev["dc_n"], eps=w.eps, out=o, workspace=ws, status=st,
+                                                 stream=stream, eta_gate=args.eta_gate, eta_base=w.eta_base)
+    else:
+        ws = torch.empty(ttt.mlp_backward_workspace_bytes(w.B, w.H, w.T, w.d, w.hidden, w.b), dtype=torch.uint8,
+                         device="cuda")
+        seeds = ("dW1_n", "dc1_n", "dW2_n", "dc2_n")
+        call = lambda o: ttt.ttt_mlp_backward(*(dev[k] for k in ("Q", "K", "V")), dev[eta_key],
+                                              *(dev[k] for k in ("W1", "c1", "W2", "c2", "ln_g", "ln_b", "dZ")),
+                                              mb=w.b, eps=w.eps, out=o, workspace=ws, status=st, stream=stream,
+                                              eta_gate=args.eta_gate, eta_base=w.eta_base,
+                                              **{k: dev[k] for k in seeds})
     out = call({})
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     for _ in range(args.warmup):
@@ -341,7 +366,7 @@ def run_gpu_backward(args):
         raise RuntimeError("device status %d in timed region" % int(st.item()))
 
     # e2e: inputs and upstream gradients from pinned host memory, every gradient back to the host
-    host_in = {k: inp[k].pin_memory() for k in ("Q", "K", "V", eta_key, "dZ", "dW_n", "dc_n")}
+    host_in = {k: inp[k].pin_memory() for k in ("Q", "K", "V", eta_key, "dZ") + seeds}
     host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
@@ -369,14 +394,16 @@ def run_gpu_backward(args):
     bytes_launch, flops_launch = backward_cost(w)
     achieved = flops_launch / (ms / 1e3) / 1e12
     line = {
-        "metric": "TTT-Linear backward (outer-loop gradient) tokens/sec (B·T·H/s) on 1 B300",
+        "metric": "TTT-%s backward (outer-loop gradient) tokens/sec (B·T·H/s) on 1 B300"
+                  % ("Linear" if w.variant == "linear" else "MLP"),
         "value": tokens / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32",
         "precision": "bf16 Q/K/V/dZ inputs; fp32 FFMA arithmetic, fp32 gradients",
         "data": "synthetic (seeded Gaussian Q/K/V/dZ, sigmoid-gated eta, N(0,0.02^2) W0)",
-        "config": {"workload": w.name, "direction": "backward", "variant": "ttt-linear", "B": w.B, "H": w.H,
-                   "T": w.T, "d": w.d, "mb": w.b, "io": w.io, "eta_gate": args.eta_gate,
+        "config": {"workload": w.name, "direction": "backward", "variant": "ttt-" + w.variant, "B": w.B,
+                   "H": w.H, "T": w.T, "d": w.d, "mb": w.b, "hidden": w.hidden or None, "io": w.io,
+                   "eta_gate": args.eta_gate,
                    "workspace_bytes": ws.numel(), "l2": "flushed between steps (256 MiB write)",
                    "parallelism": "dp%d" % world},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
@@ -396,6 +423,7 @@ def run_gpu_backward(args):
         line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
                                 "sample": "%d of %d chains x %d tokens (fp64 torch autograd through the "
                                           "primal token loop)" % (chains, w.chains, Ts), "seconds": dt}
+    line["precision"] = "%s Q/K/V/dZ inputs; fp32 FFMA arithmetic, fp32 gradients" % w.io
     return line
 
 
@@ -560,12 +588,13 @@ def run_reference_backward(args):
     value = toks / secs
     return {
         "impl": "reference",
-        "metric": "TTT-Linear backward (outer-loop gradient) tokens/sec (B·T·H/s) on 1 B300",
+        "metric": "TTT-%s backward (outer-loop gradient) tokens/sec (B·T·H/s) on 1 B300"
+                  % ("Linear" if w.variant == "linear" else "MLP"),
         "value": value, "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator)",
-        "config": {"workload": w.name, "direction": "backward", "variant": "ttt-linear", "B": w.B, "H": w.H,
-                   "T": w.T, "d": w.d, "mb": w.b},
+        "config": {"workload": w.name, "direction": "backward", "variant": "ttt-" + w.variant, "B": w.B,
+                   "H": w.H, "T": w.T, "d": w.d, "mb": w.b, "hidden": w.hidden or None},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": th, "kind": "oracle",
                          "sample": "%d of %d chains x %d tokens per step" % (chains, w.chains, Ts)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

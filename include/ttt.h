@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define TTT_ABI_VERSION 5
+#define TTT_ABI_VERSION 6
 
 typedef enum {
     TTT_OK = 0,
@@ -245,6 +245,49 @@ typedef struct {
 ttt_status ttt_linear_backward(const ttt_linear_bwd_args *args, void *stream);
 /* Workspace size for ttt_linear_backward (0 if the sizes are invalid). */
 uint64_t ttt_linear_backward_workspace_bytes(int32_t B, int32_t H, int32_t T, int32_t d, int32_t mb);
+
+/* ---------------------------------------------------------------------- */
+/* TTT-MLP backward (outer-loop training)                                  */
+/* ---------------------------------------------------------------------- */
+/* The TTT-MLP counterpart of ttt_linear_backward: for the prefix rule and T a
+ * multiple of mb, the gradients of
+ *     J = sum(dZ * Z) + sum(dW1_n * W1_n) + sum(dc1_n * c1_n)
+ *                     + sum(dW2_n * W2_n) + sum(dc2_n * c2_n)
+ * with respect to Q, K, V, eta (the gate logits when eta_gate = 1), W1_0, c1_0,
+ * W2_0, c2_0, ln_g and ln_b; weight and LayerNorm gradients per chain, as for
+ * TTT-Linear. Workspace: at least ttt_mlp_backward_workspace_bytes() bytes
+ * (per chain (T/mb)(2 hidden d + hidden + d) + 2 hidden d floats: every
+ * mini-batch's starting state and the weight-gradient accumulators), 16-byte
+ * aligned, contents ignored on entry and unspecified on return. */
+typedef struct {
+    int32_t B, H, T, d, hidden, mb;
+    int32_t io;              /* ttt_dtype of Q, K, V and dZ                    */
+    float ln_eps;
+    const void *Q, *K, *V;   /* [B][H][T][d] io                                */
+    const float *eta;        /* [B][H][T]                                      */
+    const float *W1_0, *c1_0, *W2_0, *c2_0; /* as for ttt_mlp_forward          */
+    int64_t w_bstride, c1_bstride, c2_bstride;
+    const float *ln_g, *ln_b;/* [H][d]                                         */
+    const void *dZ;          /* [B][H][T][d] io                                */
+    const float *dW1_n, *dc1_n, *dW2_n, *dc2_n; /* [B][H][...] seeds, or NULL  */
+    float *dQ, *dK, *dV;     /* [B][H][T][d] fp32 out                          */
+    float *deta;             /* [B][H][T] fp32 out                             */
+    float *dW1, *dc1, *dW2, *dc2; /* [B][H][hidden][d], [B][H][hidden], [B][H][d][hidden], [B][H][d] */
+    float *dln_g, *dln_b;    /* [B][H][d] fp32 out, per chain                  */
+    void *workspace;
+    uint64_t workspace_bytes;
+    int32_t *status_dev;
+    int32_t eta_gate;
+    float eta_base;
+} ttt_mlp_bwd_args;
+
+/* Supported: io = TTT_F32 or TTT_BF16, 4 <= d <= 128 and 4 <= hidden with both
+ *            multiples of 4, mb in {1, 2, 4, 8, 16}, and
+ *            2 hidden + 6 d + 13 mb d + 9 mb hidden + 4 mb^2 + 4 mb floats
+ *            <= 227 KB (fp32 FFMA kernel, one CTA of 512 threads per chain). */
+ttt_status ttt_mlp_backward(const ttt_mlp_bwd_args *args, void *stream);
+uint64_t ttt_mlp_backward_workspace_bytes(int32_t B, int32_t H, int32_t T, int32_t d, int32_t hidden,
+                                          int32_t mb);
 
 /* ---------------------------------------------------------------------- */
 /* Introspection                                                           */

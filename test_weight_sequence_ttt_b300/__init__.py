@@ -18,7 +18,8 @@ from typing import Optional
 
 __all__ = [
     "TTTError", "lib", "lib_path", "ttt_linear_forward", "ttt_mlp_forward", "ttt_linear_backward",
-    "linear_backward_workspace_bytes", "status_string", "abi_version", "linear_kernel_kind",
+    "linear_backward_workspace_bytes", "ttt_mlp_backward", "mlp_backward_workspace_bytes", "MlpBwdArgs",
+    "status_string", "abi_version", "linear_kernel_kind",
     "mlp_kernel_kind", "LinearArgs", "MlpArgs", "LinearBwdArgs", "STATUS", "F32", "BF16", "OUT_RULES",
 ]
 
@@ -81,6 +82,23 @@ class LinearBwdArgs(ctypes.Structure):
     ]
 
 
+class MlpBwdArgs(ctypes.Structure):
+    """Mirror of ``ttt_mlp_bwd_args``."""
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("T", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("hidden", ctypes.c_int32), ("mb", ctypes.c_int32), ("io", ctypes.c_int32), ("ln_eps", ctypes.c_float),
+        ("Q", _vp), ("K", _vp), ("V", _vp), ("eta", _vp),
+        ("W1_0", _vp), ("c1_0", _vp), ("W2_0", _vp), ("c2_0", _vp),
+        ("w_bstride", ctypes.c_int64), ("c1_bstride", ctypes.c_int64), ("c2_bstride", ctypes.c_int64),
+        ("ln_g", _vp), ("ln_b", _vp), ("dZ", _vp),
+        ("dW1_n", _vp), ("dc1_n", _vp), ("dW2_n", _vp), ("dc2_n", _vp),
+        ("dQ", _vp), ("dK", _vp), ("dV", _vp), ("deta", _vp),
+        ("dW1", _vp), ("dc1", _vp), ("dW2", _vp), ("dc2", _vp), ("dln_g", _vp), ("dln_b", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_uint64),
+        ("status_dev", _vp), ("eta_gate", ctypes.c_int32), ("eta_base", ctypes.c_float),
+    ]
+
+
 def _rule_code(rule) -> int:
     if isinstance(rule, str):
         if rule not in OUT_RULES:
@@ -127,6 +145,10 @@ def lib() -> ctypes.CDLL:
             L.ttt_linear_backward.argtypes = [ctypes.POINTER(LinearBwdArgs), _vp]
             L.ttt_linear_backward_workspace_bytes.restype = ctypes.c_uint64
             L.ttt_linear_backward_workspace_bytes.argtypes = [ctypes.c_int32] * 5
+            L.ttt_mlp_backward.restype = ctypes.c_int
+            L.ttt_mlp_backward.argtypes = [ctypes.POINTER(MlpBwdArgs), _vp]
+            L.ttt_mlp_backward_workspace_bytes.restype = ctypes.c_uint64
+            L.ttt_mlp_backward_workspace_bytes.argtypes = [ctypes.c_int32] * 6
             _lib = L
     return _lib
 
@@ -335,4 +357,55 @@ def ttt_linear_backward(Q, K, V, eta, W0, c0, ln_g, ln_b, dZ, *, mb: int, dW_n=N
     rc = lib().ttt_linear_backward(ctypes.byref(a), _stream_handle(stream))
     if rc != 0:
         raise TTTError(rc, "ttt_linear_backward")
+    return out
+
+
+def mlp_backward_workspace_bytes(B: int, H: int, T: int, d: int, hidden: int, mb: int) -> int:
+    """Device scratch ``ttt_mlp_backward`` needs (0 for invalid sizes)."""
+    return int(lib().ttt_mlp_backward_workspace_bytes(B, H, T, d, hidden, mb))
+
+
+def ttt_mlp_backward(Q, K, V, eta, W1, c1, W2, c2, ln_g, ln_b, dZ, *, mb: int, dW1_n=None, dc1_n=None,
+                     dW2_n=None, dc2_n=None, eps: float = 1e-6, out: Optional[dict] = None, workspace=None,
+                     status=None, stream=None, eta_gate: bool = False, eta_base: float = 1.0) -> dict:
+    """Gradients of the TTT-MLP inner loop through ``ttt_mlp_backward``.
+
+    Inputs as for ``ttt_mlp_forward`` (prefix rule, T a multiple of mb) plus dZ
+    in the dtype of Q/K/V and optional fp32 final-state seeds. Returns fp32 dQ,
+    dK, dV, deta and per-chain dW1, dc1, dW2, dc2, dln_g, dln_b."""
+    import torch
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("eta", eta), ("W1", W1), ("c1", c1), ("W2", W2), ("c2", c2),
+                 ("ln_g", ln_g), ("ln_b", ln_b), ("dZ", dZ), ("dW1_n", dW1_n), ("dc1_n", dc1_n),
+                 ("dW2_n", dW2_n), ("dc2_n", dc2_n), ("workspace", workspace), ("status", status)):
+        _check_cuda(n, t)
+    if dZ.dtype != K.dtype:
+        raise TypeError("dZ must have the dtype of Q/K/V")
+    B, H, T, d = K.shape
+    h = W1.shape[-2]
+    dev = K.device
+    out = dict(out or {})
+    f32 = dict(device=dev, dtype=torch.float32)
+    for k, shape in (("dQ", (B, H, T, d)), ("dK", (B, H, T, d)), ("dV", (B, H, T, d)), ("deta", (B, H, T)),
+                     ("dW1", (B, H, h, d)), ("dc1", (B, H, h)), ("dW2", (B, H, d, h)), ("dc2", (B, H, d)),
+                     ("dln_g", (B, H, d)), ("dln_b", (B, H, d))):
+        if k not in out:
+            out[k] = torch.empty(shape, **f32)
+    if workspace is None:
+        workspace = torch.empty(max(mlp_backward_workspace_bytes(B, H, T, d, h, mb), 16), device=dev,
+                                dtype=torch.uint8)
+    a = MlpBwdArgs(
+        B=B, H=H, T=T, d=d, hidden=h, mb=mb, io=_io_code(K.dtype), ln_eps=eps,
+        Q=_ptr(Q), K=_ptr(K), V=_ptr(V), eta=_ptr(eta), W1_0=_ptr(W1), c1_0=_ptr(c1), W2_0=_ptr(W2),
+        c2_0=_ptr(c2), w_bstride=_bstride(W1, B, H * h * d), c1_bstride=_bstride(c1, B, H * h),
+        c2_bstride=_bstride(c2, B, H * d), ln_g=_ptr(ln_g), ln_b=_ptr(ln_b), dZ=_ptr(dZ),
+        dW1_n=_ptr(dW1_n), dc1_n=_ptr(dc1_n), dW2_n=_ptr(dW2_n), dc2_n=_ptr(dc2_n),
+        dQ=_ptr(out["dQ"]), dK=_ptr(out["dK"]), dV=_ptr(out["dV"]), deta=_ptr(out["deta"]),
+        dW1=_ptr(out["dW1"]), dc1=_ptr(out["dc1"]), dW2=_ptr(out["dW2"]), dc2=_ptr(out["dc2"]),
+        dln_g=_ptr(out["dln_g"]), dln_b=_ptr(out["dln_b"]),
+        workspace=_ptr(workspace), workspace_bytes=workspace.numel() * workspace.element_size(),
+        status_dev=_ptr(status), eta_gate=int(bool(eta_gate)), eta_base=float(eta_base),
+    )
+    rc = lib().ttt_mlp_backward(ctypes.byref(a), _stream_handle(stream))
+    if rc != 0:
+        raise TTTError(rc, "ttt_mlp_backward")
     return out

@@ -409,4 +409,113 @@ ttt_status ttt_linear_backward(const ttt_linear_bwd_args *a, void *stream)
     return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
 }
 
+uint64_t ttt_mlp_backward_workspace_bytes(int32_t B, int32_t H, int32_t T, int32_t d, int32_t hidden, int32_t mb)
+{
+    if (!dims_ok(B, H, T, d, mb, 0) || hidden < 1 || hidden > 4096) return 0;
+    return ttt::mlp_bwd_workspace_bytes(B, H, T, d, hidden, mb);
+}
+
+ttt_status ttt_mlp_backward(const ttt_mlp_bwd_args *a, void *stream)
+{
+    if (!a) return TTT_ERR_NULL;
+    if (!a->Q || !a->K || !a->V || !a->eta || !a->W1_0 || !a->c1_0 || !a->W2_0 || !a->c2_0 || !a->ln_g ||
+        !a->ln_b || !a->dZ || !a->dQ || !a->dK || !a->dV || !a->deta || !a->dW1 || !a->dc1 || !a->dW2 ||
+        !a->dc2 || !a->dln_g || !a->dln_b || !a->workspace)
+        return TTT_ERR_NULL;
+    if (!dims_ok(a->B, a->H, a->T, a->d, a->mb, 0) || a->hidden < 1 || a->hidden > 4096) return TTT_ERR_SHAPE;
+    if (a->io != TTT_F32 && a->io != TTT_BF16) return TTT_ERR_UNSUPPORTED;
+    if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
+    if (a->w_bstride < 0 || a->c1_bstride < 0 || a->c2_bstride < 0) return TTT_ERR_SHAPE;
+    if (!gate_ok(a->eta_gate, a->eta_base)) return TTT_ERR_SHAPE;
+    if (!ttt::mlp_bwd_supported(a->io, a->d, a->hidden, a->mb)) return TTT_ERR_UNSUPPORTED;
+    const size_t wsb = ttt::mlp_bwd_workspace_bytes(a->B, a->H, a->T, a->d, a->hidden, a->mb);
+    if (a->workspace_bytes < wsb) return TTT_ERR_SHAPE;
+
+    const void *in[] = {a->Q, a->K, a->V, a->eta, a->W1_0, a->c1_0, a->W2_0, a->c2_0, a->ln_g, a->ln_b, a->dZ};
+    const void *opt_in[] = {a->dW1_n, a->dc1_n, a->dW2_n, a->dc2_n};
+    const void *out[] = {a->dQ, a->dK, a->dV, a->deta, a->dW1, a->dc1, a->dW2, a->dc2, a->dln_g, a->dln_b,
+                         a->workspace};
+    for (const void *p : in)
+        if (!aligned16(p)) return TTT_ERR_ALIGN;
+    for (const void *p : opt_in)
+        if (p && !aligned16(p)) return TTT_ERR_ALIGN;
+    for (const void *p : out)
+        if (!aligned16(p)) return TTT_ERR_ALIGN;
+    if ((a->w_bstride & 3) || (a->c1_bstride & 3) || (a->c2_bstride & 3)) return TTT_ERR_ALIGN;
+
+    const size_t B = a->B, H = a->H, T = a->T, d = a->d, h = a->hidden;
+    const size_t es = a->io == TTT_BF16 ? 2 : 4;
+    const size_t tok = B * H * T;
+    const Range rin[] = {span(a->Q, tok * d * es), span(a->K, tok * d * es), span(a->V, tok * d * es),
+                         span(a->eta, tok * 4), span(a->W1_0, init_bytes(a->B, a->H, h * d, a->w_bstride)),
+                         span(a->c1_0, init_bytes(a->B, a->H, h, a->c1_bstride)),
+                         span(a->W2_0, init_bytes(a->B, a->H, h * d, a->w_bstride)),
+                         span(a->c2_0, init_bytes(a->B, a->H, d, a->c2_bstride)), span(a->ln_g, H * d * 4),
+                         span(a->ln_b, H * d * 4), span(a->dZ, tok * d * es),
+                         span(a->dW1_n, a->dW1_n ? B * H * h * d * 4 : 0), span(a->dc1_n, a->dc1_n ? B * H * h * 4 : 0),
+                         span(a->dW2_n, a->dW2_n ? B * H * h * d * 4 : 0), span(a->dc2_n, a->dc2_n ? B * H * d * 4 : 0)};
+    const Range rout[] = {span(a->dQ, tok * d * 4),        span(a->dK, tok * d * 4),
+                          span(a->dV, tok * d * 4),        span(a->deta, tok * 4),
+                          span(a->dW1, B * H * h * d * 4), span(a->dc1, B * H * h * 4),
+                          span(a->dW2, B * H * h * d * 4), span(a->dc2, B * H * d * 4),
+                          span(a->dln_g, B * H * d * 4),   span(a->dln_b, B * H * d * 4),
+                          span(a->workspace, wsb),         span(a->status_dev, a->status_dev ? 4 : 0)};
+    for (size_t i = 0; i < sizeof(rout) / sizeof(rout[0]); ++i) {
+        if (rout[i].hi == rout[i].lo) continue;
+        for (const Range &r : rin)
+            if (r.hi != r.lo && overlap(rout[i], r)) return TTT_ERR_ALIAS;
+        for (size_t j = i + 1; j < sizeof(rout) / sizeof(rout[0]); ++j)
+            if (rout[j].hi != rout[j].lo && overlap(rout[i], rout[j])) return TTT_ERR_ALIAS;
+    }
+    for (const void *p : in)
+        if (!is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+    for (const void *p : opt_in)
+        if (p && !is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+    for (const void *p : out)
+        if (!is_device_ptr(p)) return TTT_ERR_NOT_DEVICE_PTR;
+    if (a->status_dev && !is_device_ptr(a->status_dev)) return TTT_ERR_NOT_DEVICE_PTR;
+
+    ttt::MlpBwdParams p;
+    p.H = a->H;
+    p.T = a->T;
+    p.d = a->d;
+    p.hidden = a->hidden;
+    p.mb = a->mb;
+    p.eta_gate = a->eta_gate;
+    p.eta_base = a->eta_base;
+    p.eps = a->ln_eps;
+    p.Q = a->Q;
+    p.K = a->K;
+    p.V = a->V;
+    p.dZ = a->dZ;
+    p.eta = a->eta;
+    p.W1 = a->W1_0;
+    p.c1 = a->c1_0;
+    p.W2 = a->W2_0;
+    p.c2 = a->c2_0;
+    p.w_bstride = a->w_bstride;
+    p.c1_bstride = a->c1_bstride;
+    p.c2_bstride = a->c2_bstride;
+    p.ln_g = a->ln_g;
+    p.ln_b = a->ln_b;
+    p.dW1_n = a->dW1_n;
+    p.dc1_n = a->dc1_n;
+    p.dW2_n = a->dW2_n;
+    p.dc2_n = a->dc2_n;
+    p.dQ = a->dQ;
+    p.dK = a->dK;
+    p.dV = a->dV;
+    p.deta = a->deta;
+    p.dW1 = a->dW1;
+    p.dc1 = a->dc1;
+    p.dW2 = a->dW2;
+    p.dc2 = a->dc2;
+    p.dln_g = a->dln_g;
+    p.dln_b = a->dln_b;
+    p.ws = static_cast<float *>(a->workspace);
+    p.status = a->status_dev;
+    const cudaError_t e = ttt::launch_mlp_bwd(p, a->io, a->B * a->H, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
 }  // extern "C"

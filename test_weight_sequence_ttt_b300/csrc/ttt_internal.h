@@ -89,6 +89,23 @@ struct LinearBwdParams {
     int *status;
 };
 
+// Gradients of the TTT-MLP inner loop (prefix rule, T a multiple of mb).
+struct MlpBwdParams {
+    int H, T, d, hidden, mb;
+    int eta_gate;
+    float eta_base;
+    float eps;
+    const void *Q, *K, *V, *dZ;  // io element type
+    const float *eta;
+    const float *W1, *c1, *W2, *c2;
+    long long w_bstride, c1_bstride, c2_bstride;
+    const float *ln_g, *ln_b;
+    const float *dW1_n, *dc1_n, *dW2_n, *dc2_n;  // seeds on the final state, or NULL
+    float *dQ, *dK, *dV, *deta, *dW1, *dc1, *dW2, *dc2, *dln_g, *dln_b;
+    float *ws;  // T/mb starting states (W1, c1, W2, c2) and dW1, dW2 per chain
+    int *status;
+};
+
 // Phase-timestamp hook for performance diagnosis. Compiled in only with
 // -DTTT_TRACE; records clock64() of CTA 0 at role phase boundaries for steps
 // [kTraceFirst, kTraceFirst + kTraceSteps) into trace[(step - first) * 16 + slot].
@@ -120,6 +137,11 @@ cudaError_t launch_mlp_tc(const MlpParams &p, int chains, cudaStream_t s);
 bool linear_bwd_supported(int io, int d, int mb);
 size_t linear_bwd_workspace_bytes(int B, int H, int T, int d, int mb);
 cudaError_t launch_linear_bwd(const LinearBwdParams &p, int io, int chains, cudaStream_t s);
+
+// fp32 FFMA TTT-MLP backward kernel (io f32 or bf16), mb in {1, 2, 4, 8, 16}.
+bool mlp_bwd_supported(int io, int d, int hidden, int mb);
+size_t mlp_bwd_workspace_bytes(int B, int H, int T, int d, int hidden, int mb);
+cudaError_t launch_mlp_bwd(const MlpBwdParams &p, int io, int chains, cudaStream_t s);
 
 // Tensor-core kernel (io bf16, d in {64,128}, mb a power of two up to 1024).
 bool linear_tc_supported(int io, int d, int mb);

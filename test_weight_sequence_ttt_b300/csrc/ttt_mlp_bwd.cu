@@ -1,0 +1,630 @@
+// ttt_mlp_bwd.cu -- gradients of the TTT-MLP inner loop for outer-loop training:
+// reverse mode through the mini-batch rule, fp32 (FFMA).
+//
+// Forward of mini-batch i, anchor (W1, c1, W2, c2) (the prefix-rule matrix form
+// of Eq. 5 of the "End-to-End Test-Time Training for Long Context" review,
+// section 2.3, with the output of Eq. 5 of the survey's "TTT layer" section;
+// f_res(x) = W2 gelu(W1 x + c1) + c2, residual LayerNorm form):
+//   Z1 = K W1^T + c1,  X2 = gelu(Z1),  Y = X2 W2^T + c2
+//   G  = d l / d Y through the key LayerNorm (as for TTT-Linear)
+//   P1 = G W2,  G1 = P1 * gelu'(Z1)                            (= d l / d Z1)
+//   A1 = causal (eta_s/b)(q_t.k_s + 1),     Z1q = Q W1^T + c1 - A1 G1,  X2q = gelu(Z1q)
+//   A2 = causal (eta_s/b)(x2q_t.x2_s + 1),  Yq = X2q W2^T + c2 - A2 G,  Z = Q + LN(Yq)
+//   W1' = W1 - (1/b) G1^T diag(eta) K, c1' = c1 - (1/b) G1^T eta,
+//   W2' = W2 - (1/b) G^T diag(eta) X2,  c2' = c2 - (1/b) G^T eta.
+// The reverse pass, per mini-batch from the last to the first, with the carried
+// gradients (dW1', dc1', dW2', dc2') of the state after it:
+//   dYq  = output LayerNorm backward of dZ;   dW2 += dYq^T X2q, dc2 += sum dYq
+//   DA2  = -dYq G^T (causal);  dZ1q = (dYq W2 + (DA2 eta/b) X2) * gelu'(Z1q)
+//   dG   = -A2^T dYq - (eta/b) R2,  R2 = dW2' x2_s + dc2'
+//   dX2  = (DA2 eta/b)^T X2q - (eta/b) dW2'^T g_s
+//   DA1  = -dZ1q G1^T (causal);  dQ = dZ + dZ1q W1 + (DA1 eta/b) K
+//   dK   = (DA1 eta/b)^T Q - (eta/b) dW1'^T g1_s + ...,   dG1 = -A1^T dZ1q - (eta/b) R1,  R1 = dW1' k_s + dc1'
+//   deta_s = (1/b)(sum_t DA1_ts (q_t.k_s + 1) + DA2_ts (x2q_t.x2_s + 1) - g1_s.R1_s - g_s.R2_s)
+//   dP1  = dG1 * gelu'(Z1),  dZ1 = dG1 * P1 * gelu''(Z1),  dG += dP1 W2^T,  dW2 += G^T dP1
+//   dG -> dY through the key LayerNorm backward once more (second order, as for TTT-Linear),
+//         dV = -de, dK += de
+//   dX2 += dY W2,  dZ1 += dX2 * gelu'(Z1),  dK += dZ1 W1
+//   dW1 += dZ1q^T Q + dZ1^T K,  dW2 += dY^T X2,  dc1 += sum(dZ1q + dZ1),  dc2 += sum dY.
+//
+// One CTA of 512 threads per (sequence, head) chain. The mini-batch tiles live in
+// shared memory; the weights do not fit beside them (W1, W2, dW1, dW2 are 256 KB
+// at d = 64, h = 256), so a forward sweep writes every mini-batch's starting
+// state (W1, c1, W2, c2) to the caller's workspace, the reverse sweep reads the
+// anchors from there (they stay in L2), and dW1, dW2 accumulate in the workspace.
+#include <cuda_bf16.h>
+
+#include "ttt_internal.h"
+
+namespace ttt {
+namespace {
+
+constexpr int kNT = 512;
+constexpr int kNW = kNT / 32;
+constexpr int kMaxPer = 4;  // row elements per lane of the LayerNorm rows (d <= 128)
+
+constexpr float kGeluA = 0.7978845608028654f;  // sqrt(2 / pi)
+constexpr float kGeluC = 0.044715f;
+
+// gelu_tanh and its first and second derivatives.
+__device__ __forceinline__ float gelu0(float u) { return 0.5f * u * (1.f + tanhf(kGeluA * fmaf(kGeluC * u * u, u, u))); }
+__device__ __forceinline__ float gelu1(float u)
+{
+    const float th = tanhf(kGeluA * fmaf(kGeluC * u * u, u, u)), w1 = kGeluA * fmaf(3.f * kGeluC, u * u, 1.f);
+    return 0.5f * (1.f + th) + 0.5f * u * (1.f - th * th) * w1;
+}
+__device__ __forceinline__ float gelu2(float u)
+{
+    const float th = tanhf(kGeluA * fmaf(kGeluC * u * u, u, u)), w1 = kGeluA * fmaf(3.f * kGeluC, u * u, 1.f);
+    const float w2 = 6.f * kGeluA * kGeluC * u;
+    return (1.f - th * th) * (w1 + 0.5f * u * (w2 - 2.f * th * w1 * w1));
+}
+
+template <typename IO>
+__device__ __forceinline__ float ldx(const IO *p);
+template <>
+__device__ __forceinline__ float ldx<float>(const float *p) { return *p; }
+template <>
+__device__ __forceinline__ float ldx<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+__device__ __forceinline__ float wsum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+
+__host__ __device__ inline size_t mlp_bwd_smem_floats(int d, int h, int b)
+{
+    return 2 * (size_t)h + 6 * (size_t)d + 13 * (size_t)b * d + 9 * (size_t)b * h + 4 * (size_t)b * b + 4 * (size_t)b;
+}
+
+struct MSmem {
+    float *c1, *dc1, *c2, *dc2, *gam, *bet, *dgam, *dbet;
+    float *K, *Q, *E, *DZ, *Yh, *P, *G, *DYq, *DG, *R2, *DY, *KA, *DU;  // [b][d]
+    float *Z1, *X2, *P1, *G1, *Z1q, *X2q, *DG1, *DX2, *R1;             // [b][h]
+    float *QK1, *QK2, *DA1, *DA2;                                       // [b][b]
+    float *et, *det, *rk, *m2k;                                          // [b]
+};
+
+__device__ MSmem mcarve(float *sm, int d, int h, int b)
+{
+    MSmem s;
+    float *p = sm;
+    auto take = [&](size_t n) { float *q = p; p += n; return q; };
+    s.c1 = take(h);
+    s.dc1 = take(h);
+    s.c2 = take(d);
+    s.dc2 = take(d);
+    s.gam = take(d);
+    s.bet = take(d);
+    s.dgam = take(d);
+    s.dbet = take(d);
+    float **bd[] = {&s.K, &s.Q, &s.E, &s.DZ, &s.Yh, &s.P, &s.G, &s.DYq, &s.DG, &s.R2, &s.DY, &s.KA, &s.DU};
+    for (float **q : bd) *q = take((size_t)b * d);
+    float **bh[] = {&s.Z1, &s.X2, &s.P1, &s.G1, &s.Z1q, &s.X2q, &s.DG1, &s.DX2, &s.R1};
+    for (float **q : bh) *q = take((size_t)b * h);
+    s.QK1 = take(b * b);
+    s.QK2 = take(b * b);
+    s.DA1 = take(b * b);
+    s.DA2 = take(b * b);
+    s.et = take(b);
+    s.det = take(b);
+    s.rk = take(b);
+    s.m2k = take(b);
+    return s;
+}
+
+// out(s, n) for the MB rows s of A and the N rows n of W (row-major, Kd columns):
+// acc = sum_k A[s][k] W[n][k]; epi(s, n, acc). Each work item is one weight row
+// and RB rows of A, so each weight element is read MB / RB times.
+template <int MB, typename Epi>
+__device__ __forceinline__ void prod_rows(const float *A, const float *W, int N, int Kd, Epi epi)
+{
+    constexpr int RB = MB < 8 ? MB : 8;
+    for (int it = threadIdx.x; it < N * (MB / RB); it += kNT) {
+        const int n = it % N, s0 = (it / N) * RB;
+        float acc[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) acc[r] = 0.f;
+        const float *w = W + (size_t)n * Kd;
+        for (int k = 0; k < Kd; k += 4) {
+            const float4 wv = ld4(w + k);
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                const float4 a = ld4(A + (s0 + r) * Kd + k);
+                acc[r] = fmaf(a.x, wv.x, fmaf(a.y, wv.y, fmaf(a.z, wv.z, fmaf(a.w, wv.w, acc[r]))));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) epi(s0 + r, n, acc[r]);
+    }
+}
+
+// out(s, n) = sum_j A[s][j] W[j][n] (W row-major [Kd][N]); lanes hold consecutive n.
+template <int MB, typename Epi>
+__device__ __forceinline__ void prod_cols(const float *A, const float *W, int N, int Kd, Epi epi)
+{
+    constexpr int RB = MB < 8 ? MB : 8;
+    for (int it = threadIdx.x; it < N * (MB / RB); it += kNT) {
+        const int n = it % N, s0 = (it / N) * RB;
+        float acc[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) acc[r] = 0.f;
+        for (int j = 0; j < Kd; ++j) {
+            const float wv = W[(size_t)j * N + n];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) acc[r] = fmaf(A[(s0 + r) * Kd + j], wv, acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) epi(s0 + r, n, acc[r]);
+    }
+}
+
+// out[t][s] = sum_k X[t][k] Y[s][k] + add for s <= t (causal) else 0; sign applied.
+template <int MB>
+__device__ __forceinline__ void gram(float *out, const float *X, const float *Y, int Kd, float add, float sign,
+                                     bool causal)
+{
+    for (int it = threadIdx.x; it < MB * MB; it += kNT) {
+        const int t = it / MB, s = it % MB;
+        float acc = 0.f;
+        if (!causal || s <= t) {
+            acc = add;
+            for (int k = 0; k < Kd; k += 4) {
+                const float4 x = ld4(X + t * Kd + k), y = ld4(Y + s * Kd + k);
+                acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+            }
+        }
+        out[it] = sign * acc;
+    }
+}
+
+// Key rows: Yh holds y_s on entry; leaves yh_s in Yh, e_s in E (v_s on entry),
+// g_s in G, r_s and mean(u_s*yh_s) in rk, m2k. One warp per row.
+__device__ __forceinline__ void key_rows(const MSmem &S, int d, int b, float eps, int warp, int lane)
+{
+    const float inv_d = 1.f / (float)d;
+    for (int s = warp; s < b; s += kNW) {
+        float *y = S.Yh + s * d, *e = S.E + s * d;
+        float mu = 0.f;
+        for (int j = lane; j < d; j += 32) mu += y[j];
+        mu = wsum(mu) * inv_d;
+        float var = 0.f;
+        for (int j = lane; j < d; j += 32) var += (y[j] - mu) * (y[j] - mu);
+        const float r = rsqrtf(wsum(var) * inv_d + eps);
+        float m1 = 0.f, m2 = 0.f;
+        for (int j = lane; j < d; j += 32) {
+            const float yh = (y[j] - mu) * r;
+            const float ee = S.K[s * d + j] + S.gam[j] * yh + S.bet[j] - e[j];
+            const float u = 2.f * S.gam[j] * ee;
+            y[j] = yh;
+            e[j] = ee;
+            m1 += u;
+            m2 += u * yh;
+        }
+        m1 = wsum(m1) * inv_d;
+        m2 = wsum(m2) * inv_d;
+        for (int j = lane; j < d; j += 32) S.G[s * d + j] = r * (2.f * S.gam[j] * e[j] - m1 - y[j] * m2);
+        if (lane == 0) {
+            S.rk[s] = r;
+            S.m2k[s] = m2;
+        }
+    }
+}
+
+template <typename IO, int MB>
+__global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
+{
+    extern __shared__ __align__(16) float smm[];
+    const int d = p.d, h = p.hidden, T = p.T, n = T / MB;
+    const MSmem S = mcarve(smm, d, h, MB);
+    const int chain = blockIdx.x;
+    const int bi = chain / p.H, hi = chain % p.H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float inv_b = 1.f / (float)MB, inv_d = 1.f / (float)d;
+    const size_t tok0 = (size_t)chain * T;
+    const IO *Qg = static_cast<const IO *>(p.Q) + tok0 * d;
+    const IO *Kg = static_cast<const IO *>(p.K) + tok0 * d;
+    const IO *Vg = static_cast<const IO *>(p.V) + tok0 * d;
+    const IO *DZg = static_cast<const IO *>(p.dZ) + tok0 * d;
+    const float *eg = p.eta + tok0;
+    const size_t hd = (size_t)h * d, slot = 2 * hd + h + d;
+    float *ws = p.ws + (size_t)chain * (n * slot + 2 * hd);
+    float *dW1 = ws + n * slot, *dW2 = dW1 + hd;  // [h][d], [d][h]
+    auto W1s = [&](int i) { return ws + (size_t)i * slot; };
+    auto c1s = [&](int i) { return ws + (size_t)i * slot + hd; };
+    auto W2s = [&](int i) { return ws + (size_t)i * slot + hd + h; };
+    auto c2s = [&](int i) { return ws + (size_t)i * slot + 2 * hd + h; };
+
+    {
+        const float *W1 = p.W1 + bi * p.w_bstride + (long long)hi * hd;
+        const float *W2 = p.W2 + bi * p.w_bstride + (long long)hi * hd;
+        const float *c1 = p.c1 + bi * p.c1_bstride + (long long)hi * h;
+        const float *c2 = p.c2 + bi * p.c2_bstride + (long long)hi * d;
+        for (size_t q = tid; q < hd; q += kNT) {
+            W1s(0)[q] = W1[q];
+            W2s(0)[q] = W2[q];
+            dW1[q] = p.dW1_n ? p.dW1_n[(size_t)chain * hd + q] : 0.f;
+            dW2[q] = p.dW2_n ? p.dW2_n[(size_t)chain * hd + q] : 0.f;
+        }
+        for (int j = tid; j < h; j += kNT) {
+            c1s(0)[j] = c1[j];
+            S.dc1[j] = p.dc1_n ? p.dc1_n[(size_t)chain * h + j] : 0.f;
+        }
+        for (int j = tid; j < d; j += kNT) {
+            c2s(0)[j] = c2[j];
+            S.dc2[j] = p.dc2_n ? p.dc2_n[(size_t)chain * d + j] : 0.f;
+            S.gam[j] = p.ln_g[hi * d + j];
+            S.bet[j] = p.ln_b[hi * d + j];
+            S.dgam[j] = 0.f;
+            S.dbet[j] = 0.f;
+        }
+    }
+    auto load_eta = [&](int t0) {
+        for (int s = tid; s < MB; s += kNT) {
+            const float e = eg[t0 + s];
+            S.et[s] = p.eta_gate ? p.eta_base / (1.f + __expf(-e)) : e;
+        }
+    };
+    // The anchor's key side: Z1, X2 = gelu(Z1), Y -> key LayerNorm -> G, P1 = G W2, G1.
+    auto key_side = [&](const float *W1, const float *W2) {
+        prod_rows<MB>(S.K, W1, h, d, [&](int s, int m, float a) {
+            const float z = a + S.c1[m];
+            S.Z1[s * h + m] = z;
+            S.X2[s * h + m] = gelu0(z);
+        });
+        __syncthreads();
+        prod_rows<MB>(S.X2, W2, d, h, [&](int s, int j, float a) { S.Yh[s * d + j] = a + S.c2[j]; });
+        __syncthreads();
+        key_rows(S, d, MB, p.eps, warp, lane);
+        __syncthreads();
+        prod_cols<MB>(S.G, W2, h, d, [&](int s, int m, float a) {
+            S.P1[s * h + m] = a;
+            S.G1[s * h + m] = a * gelu1(S.Z1[s * h + m]);
+        });
+    };
+
+    // ---- forward sweep: the starting state of every mini-batch into the workspace
+    for (int i = 0; i < n; ++i) {
+        const int t0 = i * MB;
+        __syncthreads();
+        for (int j = tid; j < h; j += kNT) S.c1[j] = c1s(i)[j];
+        for (int j = tid; j < d; j += kNT) S.c2[j] = c2s(i)[j];
+        for (int q = tid; q < MB * d; q += kNT) {
+            S.K[q] = ldx<IO>(Kg + (size_t)t0 * d + q);
+            S.E[q] = ldx<IO>(Vg + (size_t)t0 * d + q);
+        }
+        load_eta(t0);
+        __syncthreads();
+        key_side(W1s(i), W2s(i));
+        __syncthreads();
+        if (i + 1 < n) {
+            const float *W1 = W1s(i), *W2 = W2s(i);
+            float *W1n = W1s(i + 1), *W2n = W2s(i + 1);
+            for (size_t q = tid; q < hd; q += kNT) {
+                const int m = (int)(q / d), k = (int)(q % d);
+                float a = 0.f;
+                for (int s = 0; s < MB; ++s) a = fmaf(S.et[s] * S.G1[s * h + m], S.K[s * d + k], a);
+                W1n[q] = W1[q] - a * inv_b;
+            }
+            for (size_t q = tid; q < hd; q += kNT) {
+                const int j = (int)(q / h), m = (int)(q % h);
+                float a = 0.f;
+                for (int s = 0; s < MB; ++s) a = fmaf(S.et[s] * S.G[s * d + j], S.X2[s * h + m], a);
+                W2n[q] = W2[q] - a * inv_b;
+            }
+            for (int m = tid; m < h; m += kNT) {
+                float a = 0.f;
+                for (int s = 0; s < MB; ++s) a = fmaf(S.et[s], S.G1[s * h + m], a);
+                c1s(i + 1)[m] = S.c1[m] - a * inv_b;
+            }
+            for (int j = tid; j < d; j += kNT) {
+                float a = 0.f;
+                for (int s = 0; s < MB; ++s) a = fmaf(S.et[s], S.G[s * d + j], a);
+                c2s(i + 1)[j] = S.c2[j] - a * inv_b;
+            }
+        }
+    }
+
+    // ---- reverse sweep
+    for (int i = n - 1; i >= 0; --i) {
+        const int t0 = i * MB;
+        const float *W1 = W1s(i), *W2 = W2s(i);
+        __syncthreads();
+        for (int j = tid; j < h; j += kNT) S.c1[j] = c1s(i)[j];
+        for (int j = tid; j < d; j += kNT) S.c2[j] = c2s(i)[j];
+        for (int q = tid; q < MB * d; q += kNT) {
+            const size_t g = (size_t)t0 * d + q;
+            S.K[q] = ldx<IO>(Kg + g);
+            S.Q[q] = ldx<IO>(Qg + g);
+            S.E[q] = ldx<IO>(Vg + g);
+            S.DZ[q] = ldx<IO>(DZg + g);
+        }
+        load_eta(t0);
+        __syncthreads();
+        key_side(W1, W2);
+        prod_rows<MB>(S.Q, W1, h, d, [&](int s, int m, float a) { S.Z1q[s * h + m] = a + S.c1[m]; });
+        gram<MB>(S.QK1, S.Q, S.K, d, 1.f, 1.f, false);
+        __syncthreads();
+        // Z1q = Q W1^T + c1 - A1 G1, X2q = gelu(Z1q)
+        for (int q = tid; q < MB * h; q += kNT) {
+            const int t = q / h, m = q % h;
+            float a = S.Z1q[q];
+            for (int s = 0; s <= t; ++s) a = fmaf(-S.et[s] * inv_b * S.QK1[t * MB + s], S.G1[s * h + m], a);
+            S.Z1q[q] = a;
+            S.X2q[q] = gelu0(a);
+        }
+        __syncthreads();
+        gram<MB>(S.QK2, S.X2q, S.X2, h, 1.f, 1.f, false);
+        prod_rows<MB>(S.X2q, W2, d, h, [&](int s, int j, float a) { S.P[s * d + j] = a + S.c2[j]; });
+        __syncthreads();
+        for (int q = tid; q < MB * d; q += kNT) {
+            const int t = q / d, j = q % d;
+            float a = S.P[q];
+            for (int s = 0; s <= t; ++s) a = fmaf(-S.et[s] * inv_b * S.QK2[t * MB + s], S.G[s * d + j], a);
+            S.P[q] = a;
+        }
+        __syncthreads();
+        // output LayerNorm rows: ph_t into P, dYq_t
+        for (int t = warp; t < MB; t += kNW) {
+            float *y = S.P + t * d;
+            const float *dz = S.DZ + t * d;
+            float mu = 0.f;
+            for (int j = lane; j < d; j += 32) mu += y[j];
+            mu = wsum(mu) * inv_d;
+            float var = 0.f;
+            for (int j = lane; j < d; j += 32) var += (y[j] - mu) * (y[j] - mu);
+            const float r = rsqrtf(wsum(var) * inv_d + p.eps);
+            float a1 = 0.f, a2 = 0.f;
+            for (int j = lane; j < d; j += 32) {
+                const float ph = (y[j] - mu) * r, dh = S.gam[j] * dz[j];
+                y[j] = ph;
+                a1 += dh;
+                a2 += dh * ph;
+            }
+            a1 = wsum(a1) * inv_d;
+            a2 = wsum(a2) * inv_d;
+            for (int j = lane; j < d; j += 32) S.DYq[t * d + j] = r * (S.gam[j] * dz[j] - a1 - y[j] * a2);
+        }
+        __syncthreads();
+        for (int j = tid; j < d; j += kNT) {
+            float ag = 0.f, ab = 0.f;
+            for (int t = 0; t < MB; ++t) {
+                ag = fmaf(S.DZ[t * d + j], S.P[t * d + j], ag);
+                ab += S.DZ[t * d + j];
+            }
+            S.dgam[j] += ag;
+            S.dbet[j] += ab;
+        }
+        gram<MB>(S.DA2, S.DYq, S.G, d, 0.f, -1.f, true);
+        prod_rows<MB>(S.X2, dW2, d, h, [&](int s, int j, float a) { S.R2[s * d + j] = a + S.dc2[j]; });
+        prod_rows<MB>(S.K, dW1, h, d, [&](int s, int m, float a) { S.R1[s * h + m] = a + S.dc1[m]; });
+        __syncthreads();
+        // dZ1q (into Z1q), dG, the q- and dW2'-sides of dX2, deta (layer 2)
+        prod_cols<MB>(S.DYq, W2, h, d, [&](int t, int m, float a) {
+            for (int s = 0; s <= t; ++s) a = fmaf(S.DA2[t * MB + s] * S.et[s] * inv_b, S.X2[s * h + m], a);
+            S.Z1q[t * h + m] = a * gelu1(S.Z1q[t * h + m]);
+        });
+        for (int q = tid; q < MB * d; q += kNT) {
+            const int s = q / d, j = q % d;
+            float a = 0.f;
+            for (int t = s; t < MB; ++t) a = fmaf(S.QK2[t * MB + s], S.DYq[t * d + j], a);
+            S.DG[q] = -S.et[s] * inv_b * (a + S.R2[q]);
+        }
+        prod_cols<MB>(S.G, dW2, h, d, [&](int s, int m, float a) {
+            float mix = 0.f;
+            for (int t = s; t < MB; ++t) mix = fmaf(S.DA2[t * MB + s], S.X2q[t * h + m], mix);
+            S.DX2[s * h + m] = S.et[s] * inv_b * (mix - a);
+        });
+        for (int s = warp; s < MB; s += kNW) {
+            float a = 0.f;
+            for (int t = s + lane; t < MB; t += 32) a = fmaf(S.DA2[t * MB + s], S.QK2[t * MB + s], a);
+            for (int j = lane; j < d; j += 32) a = fmaf(-S.G[s * d + j], S.R2[s * d + j], a);
+            a = wsum(a);
+            if (lane == 0) S.det[s] = a * inv_b;
+        }
+        __syncthreads();
+        gram<MB>(S.DA1, S.Z1q, S.G1, h, 0.f, -1.f, true);
+        __syncthreads();
+        // dq_t; the q- and dW1'-sides of dk_s (KA); dG1; deta (layer 1)
+        prod_cols<MB>(S.Z1q, W1, d, h, [&](int t, int k, float a) {
+            a += S.DZ[t * d + k];
+            for (int s = 0; s <= t; ++s) a = fmaf(S.DA1[t * MB + s] * S.et[s] * inv_b, S.K[s * d + k], a);
+            p.dQ[(tok0 + t0 + t) * d + k] = a;
+        });
+        prod_cols<MB>(S.G1, dW1, d, h, [&](int s, int k, float a) {
+            float mix = 0.f;
+            for (int t = s; t < MB; ++t) mix = fmaf(S.DA1[t * MB + s], S.Q[t * d + k], mix);
+            S.KA[s * d + k] = S.et[s] * inv_b * (mix - a);
+        });
+        for (int q = tid; q < MB * h; q += kNT) {
+            const int s = q / h, m = q % h;
+            float a = 0.f;
+            for (int t = s; t < MB; ++t) a = fmaf(S.QK1[t * MB + s], S.Z1q[t * h + m], a);
+            S.DG1[q] = -S.et[s] * inv_b * (a + S.R1[q]);
+        }
+        for (int s = warp; s < MB; s += kNW) {
+            float a = 0.f;
+            for (int t = s + lane; t < MB; t += 32) a = fmaf(S.DA1[t * MB + s], S.QK1[t * MB + s], a);
+            for (int m = lane; m < h; m += 32) a = fmaf(-S.G1[s * h + m], S.R1[s * h + m], a);
+            a = wsum(a);
+            if (lane == 0) S.det[s] += a * inv_b;
+        }
+        __syncthreads();
+        // through G1 = P1 * gelu'(Z1): dP1 (into DG1), the gelu'' part of dZ1 (into R1)
+        for (int q = tid; q < MB * h; q += kNT) {
+            const float z = S.Z1[q], g1 = S.DG1[q];
+            S.R1[q] = g1 * S.P1[q] * gelu2(z);
+            S.DG1[q] = g1 * gelu1(z);
+        }
+        __syncthreads();
+        prod_rows<MB>(S.DG1, W2, d, h, [&](int s, int j, float a) { S.DG[s * d + j] += a; });
+        __syncthreads();
+        // through G and the key LayerNorm (second order): dY into DY, du into DU, dv
+        for (int s = warp; s < MB; s += kNW) {
+            const float r = S.rk[s], m2 = S.m2k[s];
+            float hv[kMaxPer], yh[kMaxPer], u[kMaxPer], dyh[kMaxPer];
+            float hm = 0.f, hy = 0.f, hg = 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxPer; ++q) {
+                const int j = lane + 32 * q;
+                hv[q] = yh[q] = u[q] = 0.f;
+                if (j < d) {
+                    hv[q] = S.DG[s * d + j];
+                    yh[q] = S.Yh[s * d + j];
+                    u[q] = 2.f * S.gam[j] * S.E[s * d + j];
+                    hm += hv[q];
+                    hy += hv[q] * yh[q];
+                    hg += hv[q] * S.G[s * d + j];
+                }
+            }
+            hm = wsum(hm) * inv_d;
+            hy = wsum(hy) * inv_d;
+            hg = wsum(hg);
+            float am = 0.f, ay = 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxPer; ++q) {
+                const int j = lane + 32 * q;
+                dyh[q] = 0.f;
+                if (j < d) {
+                    const float du = r * (hv[q] - hm - yh[q] * hy);
+                    const float de = 2.f * S.gam[j] * du;
+                    S.DU[s * d + j] = du;
+                    p.dV[(tok0 + t0 + s) * d + j] = -de;
+                    dyh[q] = S.gam[j] * de - r * (hv[q] * m2 + hy * u[q]);
+                    am += dyh[q];
+                    ay += dyh[q] * yh[q];
+                }
+            }
+            am = wsum(am) * inv_d;
+            ay = wsum(ay) * inv_d;
+            const float dsig = -r * hg;
+#pragma unroll
+            for (int q = 0; q < kMaxPer; ++q) {
+                const int j = lane + 32 * q;
+                if (j < d) S.DY[s * d + j] = r * (dyh[q] - am - yh[q] * ay) + dsig * yh[q] * inv_d;
+            }
+        }
+        __syncthreads();
+        // dX2 += dY W2;  dZ1 = (gelu'' part) + dX2 * gelu'(Z1)  (into R1)
+        prod_cols<MB>(S.DY, W2, h, d, [&](int s, int m, float a) {
+            const int q = s * h + m;
+            S.R1[q] += (S.DX2[q] + a) * gelu1(S.Z1[q]);
+        });
+        __syncthreads();
+        // dk_s; dW1, dW2, dc1, dc2 carried to batch i - 1; dgamma, dbeta; deta
+        prod_cols<MB>(S.R1, W1, d, h, [&](int s, int k, float a) {
+            p.dK[(tok0 + t0 + s) * d + k] = a + S.KA[s * d + k] + 2.f * S.gam[k] * S.DU[s * d + k];
+        });
+        for (size_t q = tid; q < hd; q += kNT) {
+            const int m = (int)(q / d), k = (int)(q % d);
+            float a = 0.f;
+            for (int s = 0; s < MB; ++s) {
+                a = fmaf(S.Z1q[s * h + m], S.Q[s * d + k], a);
+                a = fmaf(S.R1[s * h + m], S.K[s * d + k], a);
+            }
+            dW1[q] += a;
+        }
+        for (size_t q = tid; q < hd; q += kNT) {
+            const int j = (int)(q / h), m = (int)(q % h);
+            float a = 0.f;
+            for (int s = 0; s < MB; ++s) {
+                a = fmaf(S.DYq[s * d + j], S.X2q[s * h + m], a);
+                a = fmaf(S.G[s * d + j], S.DG1[s * h + m], a);
+                a = fmaf(S.DY[s * d + j], S.X2[s * h + m], a);
+            }
+            dW2[q] += a;
+        }
+        for (int m = tid; m < h; m += kNT) {
+            float a = 0.f;
+            for (int s = 0; s < MB; ++s) a += S.Z1q[s * h + m] + S.R1[s * h + m];
+            S.dc1[m] += a;
+        }
+        for (int j = tid; j < d; j += kNT) {
+            float ac = 0.f, ag = 0.f, ab = 0.f;
+            for (int s = 0; s < MB; ++s) {
+                const float du = S.DU[s * d + j];
+                ac += S.DYq[s * d + j] + S.DY[s * d + j];
+                ag = fmaf(2.f * du, S.gam[j] * S.Yh[s * d + j] + S.E[s * d + j], ag);
+                ab = fmaf(2.f * S.gam[j], du, ab);
+            }
+            S.dc2[j] += ac;
+            S.dgam[j] += ag;
+            S.dbet[j] += ab;
+        }
+        for (int s = tid; s < MB; s += kNT) {
+            float v = S.det[s];
+            if (p.eta_gate) {
+                const float sg = 1.f / (1.f + __expf(-eg[t0 + s]));
+                v *= p.eta_base * sg * (1.f - sg);
+            }
+            p.deta[tok0 + t0 + s] = v;
+        }
+    }
+    __syncthreads();
+    bool bad = false;
+    for (size_t q = tid; q < hd; q += kNT) {
+        const float a = dW1[q], c = dW2[q];
+        bad |= !isfinite(a) || !isfinite(c);
+        p.dW1[(size_t)chain * hd + q] = a;
+        p.dW2[(size_t)chain * hd + q] = c;
+    }
+    for (int m = tid; m < h; m += kNT) {
+        bad |= !isfinite(S.dc1[m]);
+        p.dc1[(size_t)chain * h + m] = S.dc1[m];
+    }
+    for (int j = tid; j < d; j += kNT) {
+        bad |= !isfinite(S.dc2[j]) || !isfinite(S.dgam[j]) || !isfinite(S.dbet[j]);
+        p.dc2[(size_t)chain * d + j] = S.dc2[j];
+        p.dln_g[(size_t)chain * d + j] = S.dgam[j];
+        p.dln_b[(size_t)chain * d + j] = S.dbet[j];
+    }
+    if (bad && p.status) atomicCAS(p.status, 0, TTT_ERR_NONFINITE);
+}
+
+template <typename IO, int MB>
+cudaError_t launch_mb(const MlpBwdParams &p, int chains, cudaStream_t s)
+{
+    const size_t smem = sizeof(float) * mlp_bwd_smem_floats(p.d, p.hidden, MB);
+    cudaError_t e = ensure_smem<mlp_bwd_kernel<IO, MB>>((int)smem);
+    if (e != cudaSuccess) return e;
+    mlp_bwd_kernel<IO, MB><<<chains, kNT, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_io(const MlpBwdParams &p, int chains, cudaStream_t s)
+{
+    switch (p.mb) {
+    case 1: return launch_mb<IO, 1>(p, chains, s);
+    case 2: return launch_mb<IO, 2>(p, chains, s);
+    case 4: return launch_mb<IO, 4>(p, chains, s);
+    case 8: return launch_mb<IO, 8>(p, chains, s);
+    default: return launch_mb<IO, 16>(p, chains, s);
+    }
+}
+
+}  // namespace
+
+bool mlp_bwd_supported(int io, int d, int hidden, int mb)
+{
+    const bool pow2 = mb == 1 || mb == 2 || mb == 4 || mb == 8 || mb == 16;
+    return (io == TTT_F32 || io == TTT_BF16) && d >= 4 && d <= 32 * kMaxPer && d % 4 == 0 && hidden >= 4 &&
+           hidden % 4 == 0 && pow2 && sizeof(float) * mlp_bwd_smem_floats(d, hidden, mb) <= 227 * 1024;
+}
+
+size_t mlp_bwd_workspace_bytes(int B, int H, int T, int d, int hidden, int mb)
+{
+    const size_t hd = (size_t)hidden * d;
+    return (size_t)B * H * ((size_t)(T / mb) * (2 * hd + hidden + d) + 2 * hd) * sizeof(float);
+}
+
+cudaError_t launch_mlp_bwd(const MlpBwdParams &p, int io, int chains, cudaStream_t s)
+{
+    return io == TTT_F32 ? launch_io<float>(p, chains, s) : launch_io<__nv_bfloat16>(p, chains, s);
+}
+
+}  // namespace ttt

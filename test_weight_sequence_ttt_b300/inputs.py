@@ -29,7 +29,7 @@ from typing import Optional, Sequence
 import torch
 
 _TAGS = {"Q": 1, "K": 2, "V": 3, "eta": 4, "x": 5, "W0": 6, "W1": 7, "W2": 8,
-         "thK": 9, "thV": 10, "thQ": 11, "thlr": 12, "dZ": 13, "dWn": 14, "dcn": 15}
+         "thK": 9, "thV": 10, "thQ": 11, "thlr": 12, "dZ": 13, "dWn": 14, "dcn": 15, "dW2n": 16, "dc2n": 17}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -186,13 +186,25 @@ def make_inputs(w: Workload, chains: Optional[Sequence[int]] = None) -> dict:
 
 def make_cotangents(w: Workload, chains: Optional[Sequence[int]] = None) -> dict:
     """Upstream gradients for the backward of workload ``w`` (CPU tensors):
-    dZ [B,H,T,d] in the io dtype, dW_n [B,H,d,d] and dc_n [B,H,d] fp32, one
-    generator per chain as in ``make_inputs`` (same ``chains`` subset form)."""
+    dZ [B,H,T,d] in the io dtype and fp32 seeds on the final state -- linear:
+    dW_n [B,H,d,d], dc_n [B,H,d]; mlp: dW1_n [B,H,h,d], dc1_n [B,H,h], dW2_n
+    [B,H,d,h], dc2_n [B,H,d] -- one generator per chain as in ``make_inputs``
+    (same ``chains`` subset form)."""
     d, T = w.d, w.T
     sel = list(range(w.chains)) if chains is None else list(chains)
     shp = (w.B, w.H) if chains is None else (len(sel), 1)
     dt = _io_dtype(w.io)
     dZ = torch.stack([torch.randn(T, d, generator=_gen(w.seed, ch, "dZ")).to(dt) for ch in sel])
-    dWn = torch.stack([torch.randn(d, d, generator=_gen(w.seed, ch, "dWn")) * 0.1 for ch in sel])
-    dcn = torch.stack([torch.randn(d, generator=_gen(w.seed, ch, "dcn")) * 0.1 for ch in sel])
-    return dict(dZ=dZ.reshape(*shp, T, d), dW_n=dWn.reshape(*shp, d, d), dc_n=dcn.reshape(*shp, d))
+    out = dict(dZ=dZ.reshape(*shp, T, d))
+
+    def seed(tag, shape):
+        g = [_gen(w.seed, ch, tag) for ch in sel]
+        return torch.stack([torch.randn(*shape, generator=gg) * 0.1 for gg in g]).reshape(*shp, *shape)
+
+    if w.variant == "linear":
+        out.update(dW_n=seed("dWn", (d, d)), dc_n=seed("dcn", (d,)))
+    else:
+        h = w.hidden
+        out.update(dW1_n=seed("dWn", (h, d)), dc1_n=seed("dcn", (h,)), dW2_n=seed("dW2n", (d, h)),
+                   dc2_n=seed("dc2n", (d,)))
+    return out

@@ -14,7 +14,7 @@ import tempfile
 import pytest
 
 import test_weight_sequence_ttt_b300 as ttt
-from test_weight_sequence_ttt_b300 import LinearArgs, LinearBwdArgs, MlpArgs
+from test_weight_sequence_ttt_b300 import LinearArgs, LinearBwdArgs, MlpArgs, MlpBwdArgs
 from test_weight_sequence_ttt_b300.build import build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_strings(L):
-    assert ttt.abi_version() == 5
+    assert ttt.abi_version() == 6
     for code in ttt.STATUS:
         assert len(ttt.status_string(code)) > 0
     assert ttt.status_string(999) == "unknown status"
@@ -66,7 +66,7 @@ def _c_offsets(struct_name, fields):
 
 
 @pytest.mark.parametrize("cls,cname", [(LinearArgs, "ttt_linear_args"), (MlpArgs, "ttt_mlp_args"),
-                                       (LinearBwdArgs, "ttt_linear_bwd_args")])
+                                       (LinearBwdArgs, "ttt_linear_bwd_args"), (MlpBwdArgs, "ttt_mlp_bwd_args")])
 def test_struct_layout_matches_header(cls, cname):
     fields = [f[0] for f in cls._fields_]
     size, offs = _c_offsets(cname, fields)
@@ -199,3 +199,33 @@ def test_validation_codes_backward(L):
     assert call(dQ=base + 1 * step) == 9         # dQ over K
     assert call(workspace=base + 18 * step) == 9   # workspace over dln_b
     assert call() == 5                           # well formed; not device memory here
+
+
+def test_mlp_backward_workspace_and_validation(L):
+    hd = 256 * 64
+    assert ttt.mlp_backward_workspace_bytes(4, 12, 8192, 64, 256, 16) == 48 * (512 * (2 * hd + 256 + 64) + 2 * hd) * 4
+    assert ttt.mlp_backward_workspace_bytes(1, 1, 30, 64, 256, 16) == 0
+    base = 1 << 40
+    step = 1 << 32
+    names = ["Q", "K", "V", "eta", "W1_0", "c1_0", "W2_0", "c2_0", "ln_g", "ln_b", "dZ", "dW1_n", "dc1_n",
+             "dW2_n", "dc2_n", "dQ", "dK", "dV", "deta", "dW1", "dc1", "dW2", "dc2", "dln_g", "dln_b", "workspace",
+             "status_dev"]
+    ptrs = {n: base + i * step for i, n in enumerate(names)}
+    ws = ttt.mlp_backward_workspace_bytes(1, 2, 32, 64, 256, 16)
+
+    def call(**kw):
+        a = dict(B=1, H=2, T=32, d=64, hidden=256, mb=16, io=ttt.BF16, ln_eps=1e-6, w_bstride=0, c1_bstride=0,
+                 c2_bstride=0, workspace_bytes=ws, **ptrs)
+        a.update(kw)
+        return L.ttt_mlp_backward(ctypes.byref(MlpBwdArgs(**a)), None)
+
+    assert L.ttt_mlp_backward(None, None) == 1
+    assert call(dW2=None) == 1
+    assert call(dW1_n=None, dc1_n=None, dW2_n=None, dc2_n=None) == 5
+    assert call(T=33) == 2
+    assert call(workspace_bytes=ws - 16) == 2
+    assert call(mb=32, T=64) == 3          # mini-batches up to 16
+    assert call(d=62) == 3                 # d a multiple of 4
+    assert call(dK=base + 16 * step + 4) == 4
+    assert call(dW1=base + 5 * step) == 9  # dW1 over c1_0
+    assert call() == 5
