@@ -32,6 +32,10 @@
 // at d = 64, h = 256), so a forward sweep writes every mini-batch's starting
 // state (W1, c1, W2, c2) to the caller's workspace, the reverse sweep reads the
 // anchors from there (they stay in L2), and dW1, dW2 accumulate in the workspace.
+// W2 and dW2 are kept there transposed, [h][d] like W1, so that every product
+// with a d-wide output reads a weight column coalesced across the lanes and
+// every product with an h-wide output reads one 16-byte-aligned weight row per
+// thread.
 #include <cuda_bf16.h>
 
 #include "ttt_internal.h"
@@ -120,16 +124,16 @@ __device__ MSmem mcarve(float *sm, int d, int h, int b)
 // out(s, n) for the MB rows s of A and the N rows n of W (row-major, Kd columns):
 // acc = sum_k A[s][k] W[n][k]; epi(s, n, acc). Each work item is one weight row
 // and RB rows of A, so each weight element is read MB / RB times.
-template <int MB, typename Epi>
-__device__ __forceinline__ void prod_rows(const float *A, const float *W, int N, int Kd, Epi epi)
+template <int MB, int RB, typename Epi>
+__device__ __forceinline__ void prod_rows_rb(const float *A, const float *W, int N, int Kd, Epi &epi)
 {
-    constexpr int RB = MB < 8 ? MB : 8;
     for (int it = threadIdx.x; it < N * (MB / RB); it += kNT) {
         const int n = it % N, s0 = (it / N) * RB;
         float acc[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) acc[r] = 0.f;
         const float *w = W + (size_t)n * Kd;
+#pragma unroll 2
         for (int k = 0; k < Kd; k += 4) {
             const float4 wv = ld4(w + k);
 #pragma unroll
@@ -144,22 +148,91 @@ __device__ __forceinline__ void prod_rows(const float *A, const float *W, int N,
 }
 
 // out(s, n) = sum_j A[s][j] W[j][n] (W row-major [Kd][N]); lanes hold consecutive n.
-template <int MB, typename Epi>
-__device__ __forceinline__ void prod_cols(const float *A, const float *W, int N, int Kd, Epi epi)
+template <int MB, int RB, typename Epi>
+__device__ __forceinline__ void prod_cols_rb(const float *A, const float *W, int N, int Kd, Epi &epi)
 {
-    constexpr int RB = MB < 8 ? MB : 8;
     for (int it = threadIdx.x; it < N * (MB / RB); it += kNT) {
         const int n = it % N, s0 = (it / N) * RB;
         float acc[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) acc[r] = 0.f;
-        for (int j = 0; j < Kd; ++j) {
-            const float wv = W[(size_t)j * N + n];
+#pragma unroll 2
+        for (int j = 0; j < Kd; j += 4) {
+            const float w0 = W[(size_t)j * N + n], w1 = W[(size_t)(j + 1) * N + n];
+            const float w2 = W[(size_t)(j + 2) * N + n], w3 = W[(size_t)(j + 3) * N + n];
 #pragma unroll
-            for (int r = 0; r < RB; ++r) acc[r] = fmaf(A[(s0 + r) * Kd + j], wv, acc[r]);
+            for (int r = 0; r < RB; ++r) {
+                const float4 a = ld4(A + (s0 + r) * Kd + j);
+                acc[r] = fmaf(a.x, w0, fmaf(a.y, w1, fmaf(a.z, w2, fmaf(a.w, w3, acc[r]))));
+            }
         }
 #pragma unroll
         for (int r = 0; r < RB; ++r) epi(s0 + r, n, acc[r]);
+    }
+}
+
+// Rows of A per work item: as many as keep every thread busy (at most 8).
+template <int MB>
+__device__ __forceinline__ int rows_per_item(int N)
+{
+    return (MB >= 8 && N * MB >= 8 * kNT) ? 8 : (MB >= 4 && N * MB >= 4 * kNT) ? 4 : (MB >= 2) ? 2 : 1;
+}
+
+template <int MB, typename Epi>
+__device__ __forceinline__ void prod_rows(const float *A, const float *W, int N, int Kd, Epi epi)
+{
+    switch (rows_per_item<MB>(N)) {
+    case 8: prod_rows_rb<MB, (MB >= 8 ? 8 : 1)>(A, W, N, Kd, epi); break;
+    case 4: prod_rows_rb<MB, (MB >= 4 ? 4 : 1)>(A, W, N, Kd, epi); break;
+    case 2: prod_rows_rb<MB, (MB >= 2 ? 2 : 1)>(A, W, N, Kd, epi); break;
+    default: prod_rows_rb<MB, 1>(A, W, N, Kd, epi);
+    }
+}
+
+template <int MB, typename Epi>
+__device__ __forceinline__ void prod_cols(const float *A, const float *W, int N, int Kd, Epi epi)
+{
+    switch (rows_per_item<MB>(N)) {
+    case 8: prod_cols_rb<MB, (MB >= 8 ? 8 : 1)>(A, W, N, Kd, epi); break;
+    case 4: prod_cols_rb<MB, (MB >= 4 ? 4 : 1)>(A, W, N, Kd, epi); break;
+    case 2: prod_cols_rb<MB, (MB >= 2 ? 2 : 1)>(A, W, N, Kd, epi); break;
+    default: prod_cols_rb<MB, 1>(A, W, N, Kd, epi);
+    }
+}
+
+// Outer products over the mini-batch, 4 x 4 blocks per work item: for rows
+// r0 + (R/4) x and columns c0..c0+3, acc[x] = sum_s sc_s A[s][r] B[s][c] summed over
+// up to three (A, B) pairs (A [MB][R], B [MB][C] in shared memory); epi(r, c0, acc).
+template <int MB, typename Epi>
+__device__ __forceinline__ void outer4(int R, int C, const float *A0, const float *B0, const float *A1,
+                                       const float *B1, const float *A2, const float *B2, const float *sc, Epi epi)
+{
+    const int RQ = R / 4, CQ = C / 4;
+    for (int it = threadIdx.x; it < RQ * CQ; it += kNT) {
+        const int r0 = it / CQ, c0 = 4 * (it % CQ);
+        float4 acc[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) acc[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto pair = [&](const float *A, const float *B) {
+#pragma unroll 4
+            for (int s = 0; s < MB; ++s) {
+                const float4 bv = ld4(B + s * C + c0);
+                const float f = sc ? sc[s] : 1.f;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const float a = f * A[s * R + r0 + RQ * x];
+                    acc[x].x = fmaf(a, bv.x, acc[x].x);
+                    acc[x].y = fmaf(a, bv.y, acc[x].y);
+                    acc[x].z = fmaf(a, bv.z, acc[x].z);
+                    acc[x].w = fmaf(a, bv.w, acc[x].w);
+                }
+            }
+        };
+        pair(A0, B0);
+        if (A1) pair(A1, B1);
+        if (A2) pair(A2, B2);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) epi(r0 + RQ * x, c0, acc[x]);
     }
 }
 
@@ -233,10 +306,10 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
     const float *eg = p.eta + tok0;
     const size_t hd = (size_t)h * d, slot = 2 * hd + h + d;
     float *ws = p.ws + (size_t)chain * (n * slot + 2 * hd);
-    float *dW1 = ws + n * slot, *dW2 = dW1 + hd;  // [h][d], [d][h]
+    float *dW1 = ws + n * slot, *dW2 = dW1 + hd;  // [h][d] both (dW2 transposed)
     auto W1s = [&](int i) { return ws + (size_t)i * slot; };
     auto c1s = [&](int i) { return ws + (size_t)i * slot + hd; };
-    auto W2s = [&](int i) { return ws + (size_t)i * slot + hd + h; };
+    auto W2s = [&](int i) { return ws + (size_t)i * slot + hd + h; };  // W2^T [h][d]
     auto c2s = [&](int i) { return ws + (size_t)i * slot + 2 * hd + h; };
 
     {
@@ -245,10 +318,11 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
         const float *c1 = p.c1 + bi * p.c1_bstride + (long long)hi * h;
         const float *c2 = p.c2 + bi * p.c2_bstride + (long long)hi * d;
         for (size_t q = tid; q < hd; q += kNT) {
+            const size_t m = q / d, j = q % d, qt = j * h + m;  // [h][d] index q <- [d][h] index qt
             W1s(0)[q] = W1[q];
-            W2s(0)[q] = W2[q];
+            W2s(0)[q] = W2[qt];
             dW1[q] = p.dW1_n ? p.dW1_n[(size_t)chain * hd + q] : 0.f;
-            dW2[q] = p.dW2_n ? p.dW2_n[(size_t)chain * hd + q] : 0.f;
+            dW2[q] = p.dW2_n ? p.dW2_n[(size_t)chain * hd + qt] : 0.f;
         }
         for (int j = tid; j < h; j += kNT) {
             c1s(0)[j] = c1[j];
@@ -277,11 +351,11 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
             S.X2[s * h + m] = gelu0(z);
         });
         __syncthreads();
-        prod_rows<MB>(S.X2, W2, d, h, [&](int s, int j, float a) { S.Yh[s * d + j] = a + S.c2[j]; });
+        prod_cols<MB>(S.X2, W2, d, h, [&](int s, int j, float a) { S.Yh[s * d + j] = a + S.c2[j]; });
         __syncthreads();
         key_rows(S, d, MB, p.eps, warp, lane);
         __syncthreads();
-        prod_cols<MB>(S.G, W2, h, d, [&](int s, int m, float a) {
+        prod_rows<MB>(S.G, W2, h, d, [&](int s, int m, float a) {
             S.P1[s * h + m] = a;
             S.G1[s * h + m] = a * gelu1(S.Z1[s * h + m]);
         });
@@ -304,18 +378,16 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
         if (i + 1 < n) {
             const float *W1 = W1s(i), *W2 = W2s(i);
             float *W1n = W1s(i + 1), *W2n = W2s(i + 1);
-            for (size_t q = tid; q < hd; q += kNT) {
-                const int m = (int)(q / d), k = (int)(q % d);
-                float a = 0.f;
-                for (int s = 0; s < MB; ++s) a = fmaf(S.et[s] * S.G1[s * h + m], S.K[s * d + k], a);
-                W1n[q] = W1[q] - a * inv_b;
-            }
-            for (size_t q = tid; q < hd; q += kNT) {
-                const int j = (int)(q / h), m = (int)(q % h);
-                float a = 0.f;
-                for (int s = 0; s < MB; ++s) a = fmaf(S.et[s] * S.G[s * d + j], S.X2[s * h + m], a);
-                W2n[q] = W2[q] - a * inv_b;
-            }
+            outer4<MB>(h, d, S.G1, S.K, nullptr, nullptr, nullptr, nullptr, S.et, [&](int m, int k, float4 a) {
+                const float4 w = ld4(W1 + (size_t)m * d + k);
+                *reinterpret_cast<float4 *>(W1n + (size_t)m * d + k) =
+                    make_float4(w.x - a.x * inv_b, w.y - a.y * inv_b, w.z - a.z * inv_b, w.w - a.w * inv_b);
+            });
+            outer4<MB>(h, d, S.X2, S.G, nullptr, nullptr, nullptr, nullptr, S.et, [&](int m, int j, float4 a) {
+                const float4 w = ld4(W2 + (size_t)m * d + j);
+                *reinterpret_cast<float4 *>(W2n + (size_t)m * d + j) =
+                    make_float4(w.x - a.x * inv_b, w.y - a.y * inv_b, w.z - a.z * inv_b, w.w - a.w * inv_b);
+            });
             for (int m = tid; m < h; m += kNT) {
                 float a = 0.f;
                 for (int s = 0; s < MB; ++s) a = fmaf(S.et[s], S.G1[s * h + m], a);
@@ -359,7 +431,7 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
         }
         __syncthreads();
         gram<MB>(S.QK2, S.X2q, S.X2, h, 1.f, 1.f, false);
-        prod_rows<MB>(S.X2q, W2, d, h, [&](int s, int j, float a) { S.P[s * d + j] = a + S.c2[j]; });
+        prod_cols<MB>(S.X2q, W2, d, h, [&](int s, int j, float a) { S.P[s * d + j] = a + S.c2[j]; });
         __syncthreads();
         for (int q = tid; q < MB * d; q += kNT) {
             const int t = q / d, j = q % d;
@@ -400,11 +472,11 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
             S.dbet[j] += ab;
         }
         gram<MB>(S.DA2, S.DYq, S.G, d, 0.f, -1.f, true);
-        prod_rows<MB>(S.X2, dW2, d, h, [&](int s, int j, float a) { S.R2[s * d + j] = a + S.dc2[j]; });
+        prod_cols<MB>(S.X2, dW2, d, h, [&](int s, int j, float a) { S.R2[s * d + j] = a + S.dc2[j]; });
         prod_rows<MB>(S.K, dW1, h, d, [&](int s, int m, float a) { S.R1[s * h + m] = a + S.dc1[m]; });
         __syncthreads();
         // dZ1q (into Z1q), dG, the q- and dW2'-sides of dX2, deta (layer 2)
-        prod_cols<MB>(S.DYq, W2, h, d, [&](int t, int m, float a) {
+        prod_rows<MB>(S.DYq, W2, h, d, [&](int t, int m, float a) {
             for (int s = 0; s <= t; ++s) a = fmaf(S.DA2[t * MB + s] * S.et[s] * inv_b, S.X2[s * h + m], a);
             S.Z1q[t * h + m] = a * gelu1(S.Z1q[t * h + m]);
         });
@@ -414,7 +486,7 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
             for (int t = s; t < MB; ++t) a = fmaf(S.QK2[t * MB + s], S.DYq[t * d + j], a);
             S.DG[q] = -S.et[s] * inv_b * (a + S.R2[q]);
         }
-        prod_cols<MB>(S.G, dW2, h, d, [&](int s, int m, float a) {
+        prod_rows<MB>(S.G, dW2, h, d, [&](int s, int m, float a) {
             float mix = 0.f;
             for (int t = s; t < MB; ++t) mix = fmaf(S.DA2[t * MB + s], S.X2q[t * h + m], mix);
             S.DX2[s * h + m] = S.et[s] * inv_b * (mix - a);
@@ -461,7 +533,7 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
             S.DG1[q] = g1 * gelu1(z);
         }
         __syncthreads();
-        prod_rows<MB>(S.DG1, W2, d, h, [&](int s, int j, float a) { S.DG[s * d + j] += a; });
+        prod_cols<MB>(S.DG1, W2, d, h, [&](int s, int j, float a) { S.DG[s * d + j] += a; });
         __syncthreads();
         // through G and the key LayerNorm (second order): dY into DY, du into DU, dv
         for (int s = warp; s < MB; s += kNW) {
@@ -510,7 +582,7 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
         }
         __syncthreads();
         // dX2 += dY W2;  dZ1 = (gelu'' part) + dX2 * gelu'(Z1)  (into R1)
-        prod_cols<MB>(S.DY, W2, h, d, [&](int s, int m, float a) {
+        prod_rows<MB>(S.DY, W2, h, d, [&](int s, int m, float a) {
             const int q = s * h + m;
             S.R1[q] += (S.DX2[q] + a) * gelu1(S.Z1[q]);
         });
@@ -519,25 +591,16 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
         prod_cols<MB>(S.R1, W1, d, h, [&](int s, int k, float a) {
             p.dK[(tok0 + t0 + s) * d + k] = a + S.KA[s * d + k] + 2.f * S.gam[k] * S.DU[s * d + k];
         });
-        for (size_t q = tid; q < hd; q += kNT) {
-            const int m = (int)(q / d), k = (int)(q % d);
-            float a = 0.f;
-            for (int s = 0; s < MB; ++s) {
-                a = fmaf(S.Z1q[s * h + m], S.Q[s * d + k], a);
-                a = fmaf(S.R1[s * h + m], S.K[s * d + k], a);
-            }
-            dW1[q] += a;
-        }
-        for (size_t q = tid; q < hd; q += kNT) {
-            const int j = (int)(q / h), m = (int)(q % h);
-            float a = 0.f;
-            for (int s = 0; s < MB; ++s) {
-                a = fmaf(S.DYq[s * d + j], S.X2q[s * h + m], a);
-                a = fmaf(S.G[s * d + j], S.DG1[s * h + m], a);
-                a = fmaf(S.DY[s * d + j], S.X2[s * h + m], a);
-            }
-            dW2[q] += a;
-        }
+        outer4<MB>(h, d, S.Z1q, S.Q, S.R1, S.K, nullptr, nullptr, nullptr, [&](int m, int k, float4 a) {
+            float4 *o = reinterpret_cast<float4 *>(dW1 + (size_t)m * d + k);
+            const float4 v = *o;
+            *o = make_float4(v.x + a.x, v.y + a.y, v.z + a.z, v.w + a.w);
+        });
+        outer4<MB>(h, d, S.X2q, S.DYq, S.DG1, S.G, S.X2, S.DY, nullptr, [&](int m, int j, float4 a) {
+            float4 *o = reinterpret_cast<float4 *>(dW2 + (size_t)m * d + j);
+            const float4 v = *o;
+            *o = make_float4(v.x + a.x, v.y + a.y, v.z + a.z, v.w + a.w);
+        });
         for (int m = tid; m < h; m += kNT) {
             float a = 0.f;
             for (int s = 0; s < MB; ++s) a += S.Z1q[s * h + m] + S.R1[s * h + m];
@@ -567,10 +630,11 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
     __syncthreads();
     bool bad = false;
     for (size_t q = tid; q < hd; q += kNT) {
+        const size_t m = q / d, j = q % d;
         const float a = dW1[q], c = dW2[q];
         bad |= !isfinite(a) || !isfinite(c);
         p.dW1[(size_t)chain * hd + q] = a;
-        p.dW2[(size_t)chain * hd + q] = c;
+        p.dW2[(size_t)chain * hd + j * h + m] = c;
     }
     for (int m = tid; m < h; m += kNT) {
         bad |= !isfinite(S.dc1[m]);
