@@ -133,7 +133,7 @@ __device__ __forceinline__ void prod_rows_rb(const float *A, const float *W, int
 #pragma unroll
         for (int r = 0; r < RB; ++r) acc[r] = 0.f;
         const float *w = W + (size_t)n * Kd;
-#pragma unroll 2
+#pragma unroll 8
         for (int k = 0; k < Kd; k += 4) {
             const float4 wv = ld4(w + k);
 #pragma unroll
@@ -156,7 +156,7 @@ __device__ __forceinline__ void prod_cols_rb(const float *A, const float *W, int
         float acc[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) acc[r] = 0.f;
-#pragma unroll 2
+#pragma unroll 4
         for (int j = 0; j < Kd; j += 4) {
             const float w0 = W[(size_t)j * N + n], w1 = W[(size_t)(j + 1) * N + n];
             const float w2 = W[(size_t)(j + 2) * N + n], w3 = W[(size_t)(j + 3) * N + n];
