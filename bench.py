@@ -648,6 +648,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eta-gate", action="store_true",
                     help="pass the learning-rate gate logits; the kernels apply eta_base * sigmoid()")
+    ap.add_argument("--T", type=int, default=0,
+                    help="tokens per chain instead of the workload's (a small case of the same kernel, "
+                         "for profiling; the line's config says so)")
     ap.add_argument("--backward", action="store_true",
                     help="time ttt_linear_backward (gradients through the inner loop) instead of the forward")
     ap.add_argument("--out-rule", default="prefix", choices=["prefix", "anchor", "key"],
@@ -655,6 +658,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.T:
+        name = "%s_T%d" % (args.workload, args.T)
+        WORKLOADS[name] = WORKLOADS[args.workload].with_(name=name, T=args.T)
+        args.workload = name
     if args.backward and args.out_rule != "prefix":
         ap.error("--backward supports the prefix output rule only")
     if args.impl == "reference":
