@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define TTT_ABI_VERSION 6
+#define TTT_ABI_VERSION 7
 
 typedef enum {
     TTT_OK = 0,
@@ -77,7 +77,9 @@ typedef enum {
     TTT_ERR_TIMEOUT = 7,         /* device: a bounded wait gave up, chain abandoned  */
     TTT_ERR_NONFINITE = 8,       /* device: non-finite value in the final state      */
     TTT_ERR_ALIAS = 9,           /* an output overlaps an input or another output    */
-    TTT_ERR_RANGE = 10           /* device: an input exceeds the fp16 operand range  */
+    TTT_ERR_RANGE = 10,          /* device: an input exceeds the fp16 operand range  */
+    TTT_ERR_SCRATCH = 11         /* the call needs more than the library's static    */
+                                 /* scratch (ttt_linear_backward_noalloc)           */
 } ttt_status;
 
 typedef enum { TTT_F32 = 0, TTT_BF16 = 1 } ttt_dtype;
@@ -245,6 +247,26 @@ typedef struct {
 ttt_status ttt_linear_backward(const ttt_linear_bwd_args *args, void *stream);
 /* Workspace size for ttt_linear_backward (0 if the sizes are invalid). */
 uint64_t ttt_linear_backward_workspace_bytes(int32_t B, int32_t H, int32_t T, int32_t d, int32_t mb);
+
+/* TTT-Linear backward without a caller workspace. The paper has no
+ * counterpart of this call; it exists for callers that cannot allocate device
+ * memory at the time of the call (code with no device allocator of its own, or
+ * a host program that must keep a fixed, planned footprint and cannot risk an
+ * allocation failing or synchronising in the middle of its work). It computes
+ * exactly what ttt_linear_backward computes, with the same arguments, but keeps
+ * the per-mini-batch checkpoints in a static array inside the library
+ * (TTT_NOALLOC_SCRATCH_BYTES on every GPU that loads the library, held until
+ * the process exits) instead of `workspace`; args->workspace and
+ * args->workspace_bytes are ignored. It allocates nothing. Calls whose
+ * ttt_linear_backward_workspace_bytes() exceeds TTT_NOALLOC_SCRATCH_BYTES
+ * return TTT_ERR_SCRATCH before any launch. Every call on a GPU shares the one
+ * array, and it keeps the previous call's contents (the kernel overwrites
+ * everything it reads), so calls that overlap on the GPU -- on different
+ * streams, or from different host threads -- race: issue them in order on one
+ * stream. The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture. */
+#define TTT_NOALLOC_SCRATCH_BYTES (32u << 20)
+ttt_status ttt_linear_backward_noalloc(const ttt_linear_bwd_args *args, void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* TTT-MLP backward (outer-loop training)                                  */

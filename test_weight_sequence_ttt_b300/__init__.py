@@ -32,8 +32,10 @@ OUT_RULES = {"prefix": 0, "anchor": 1, "key": 2}
 STATUS = {
     0: "TTT_OK", 1: "TTT_ERR_NULL", 2: "TTT_ERR_SHAPE", 3: "TTT_ERR_UNSUPPORTED", 4: "TTT_ERR_ALIGN",
     5: "TTT_ERR_NOT_DEVICE_PTR", 6: "TTT_ERR_CUDA", 7: "TTT_ERR_TIMEOUT", 8: "TTT_ERR_NONFINITE",
-    9: "TTT_ERR_ALIAS", 10: "TTT_ERR_RANGE",
+    9: "TTT_ERR_ALIAS", 10: "TTT_ERR_RANGE", 11: "TTT_ERR_SCRATCH",
 }
+# bytes of the library's static scratch behind ttt_linear_backward_noalloc (include/ttt.h)
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _vp = ctypes.c_void_p
 
@@ -145,6 +147,8 @@ def lib() -> ctypes.CDLL:
             L.ttt_linear_backward.argtypes = [ctypes.POINTER(LinearBwdArgs), _vp]
             L.ttt_linear_backward_workspace_bytes.restype = ctypes.c_uint64
             L.ttt_linear_backward_workspace_bytes.argtypes = [ctypes.c_int32] * 5
+            L.ttt_linear_backward_noalloc.restype = ctypes.c_int
+            L.ttt_linear_backward_noalloc.argtypes = [ctypes.POINTER(LinearBwdArgs), _vp]
             L.ttt_mlp_backward.restype = ctypes.c_int
             L.ttt_mlp_backward.argtypes = [ctypes.POINTER(MlpBwdArgs), _vp]
             L.ttt_mlp_backward_workspace_bytes.restype = ctypes.c_uint64

@@ -84,6 +84,7 @@ const char *ttt_status_string(ttt_status s)
     case TTT_ERR_NONFINITE: return "the final fast-weight state is not finite";
     case TTT_ERR_ALIAS: return "an output overlaps an input or another output";
     case TTT_ERR_RANGE: return "an input is outside the fp16 operand range of the tensor-core kernel";
+    case TTT_ERR_SCRATCH: return "the call needs more scratch than the library's static array holds";
     }
     return "unknown status";
 }
@@ -407,6 +408,20 @@ ttt_status ttt_linear_backward(const ttt_linear_bwd_args *a, void *stream)
     p.status = a->status_dev;
     const cudaError_t e = ttt::launch_linear_bwd(p, a->io, a->B * a->H, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TTT_OK : TTT_ERR_CUDA;
+}
+
+ttt_status ttt_linear_backward_noalloc(const ttt_linear_bwd_args *a, void *stream)
+{
+    if (!a) return TTT_ERR_NULL;
+    const uint64_t need = ttt_linear_backward_workspace_bytes(a->B, a->H, a->T, a->d, a->mb);
+    if (need == 0) return TTT_ERR_SHAPE;
+    if (need > TTT_NOALLOC_SCRATCH_BYTES) return TTT_ERR_SCRATCH;
+    void *scratch = nullptr;
+    if (ttt::linear_bwd_noalloc_scratch(&scratch) != cudaSuccess) return TTT_ERR_CUDA;
+    ttt_linear_bwd_args b = *a;
+    b.workspace = scratch;
+    b.workspace_bytes = TTT_NOALLOC_SCRATCH_BYTES;
+    return ttt_linear_backward(&b, stream);
 }
 
 uint64_t ttt_mlp_backward_workspace_bytes(int32_t B, int32_t H, int32_t T, int32_t d, int32_t hidden, int32_t mb)

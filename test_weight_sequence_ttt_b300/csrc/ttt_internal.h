@@ -136,6 +136,8 @@ cudaError_t launch_mlp_tc(const MlpParams &p, int chains, cudaStream_t s);
 // fp32 FFMA backward kernel (io f32 or bf16), d <= 128, mb <= 64.
 bool linear_bwd_supported(int io, int d, int mb);
 size_t linear_bwd_workspace_bytes(int B, int H, int T, int d, int mb);
+// Device address of the library's static backward scratch on the current device.
+cudaError_t linear_bwd_noalloc_scratch(void **ptr);
 cudaError_t launch_linear_bwd(const LinearBwdParams &p, int io, int chains, cudaStream_t s);
 
 // fp32 FFMA TTT-MLP backward kernel (io f32 or bf16), mb in {1, 2, 4, 8, 16}.

@@ -36,7 +36,15 @@
 // batch to the first and recomputes the batch's forward from its anchor.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "ttt_internal.h"
+
+// Scratch of ttt_linear_backward_noalloc: the library's own device memory for the
+// per-mini-batch checkpoints, for callers that cannot allocate a workspace.
+// TTT_NOALLOC_SCRATCH_BYTES per GPU that loads the library, held until exit;
+// every call of that entry point on a GPU shares it.
+static __device__ __align__(256) float g_noalloc_scratch[TTT_NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
 namespace ttt {
 namespace {
@@ -1122,6 +1130,28 @@ bool linear_bwd_supported(int io, int d, int mb)
 {
     return (io == TTT_F32 || io == TTT_BF16) && d >= 1 && d <= 32 * kMaxPer && mb >= 1 && mb <= 64 &&
            linear_bwd_smem(d, mb) <= 227 * 1024;
+}
+
+cudaError_t linear_bwd_noalloc_scratch(void **ptr)
+{
+    // In host code g_noalloc_scratch names a host-side stand-in, not device
+    // memory: the device address comes from the runtime, once per device (with
+    // that device current), and is kept for later calls.
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
 }
 
 size_t linear_bwd_workspace_bytes(int B, int H, int T, int d, int mb)
