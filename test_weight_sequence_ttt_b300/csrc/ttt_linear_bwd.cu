@@ -536,6 +536,31 @@ __device__ __forceinline__ float4 ldg4<__nv_bfloat16>(const __nv_bfloat16 *p)
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// One 4-element chunk of an input tile as loaded from global memory, before
+// conversion to fp32 (the register form of the next mini-batch's prefetch).
+template <typename IO>
+struct RawChunk;
+template <>
+struct RawChunk<float> {
+    using T = float4;
+};
+template <>
+struct RawChunk<__nv_bfloat16> {
+    using T = uint2;
+};
+template <typename IO>
+__device__ __forceinline__ typename RawChunk<IO>::T ldraw(const IO *p)
+{
+    return *reinterpret_cast<const typename RawChunk<IO>::T *>(p);
+}
+__device__ __forceinline__ float4 cvt4(const float4 &r) { return r; }
+__device__ __forceinline__ float4 cvt4(const uint2 &u)
+{
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
 template <int N>
 __device__ __forceinline__ void wsum_n(float (&v)[N])
 {
@@ -748,8 +773,67 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             S.et[s] = p.eta_gate ? p.eta_base / (1.f + __expf(-e)) : e;
         }
     };
+    // Register prefetch of the next mini-batch (256-thread kernels, which have
+    // registers to spare): its global loads are issued at the start of the
+    // current mini-batch's last phase and land in shared memory after it.
+    constexpr bool PF = NT == 256;
+    constexpr int CT = (MB * D / 4 + NT - 1) / NT, CW = (D * D / 4 + NT - 1) / NT;
+    using RC = typename RawChunk<IO>::T;
+    RC pk[CT], pq[CT], pv[CT], pz[CT];
+    float4 pw[CW];
+    float pc = 0.f, pe = 0.f;
+    auto issue_tiles = [&](int t0, bool rev) {
+#pragma unroll
+        for (int u = 0; u < CT; ++u) {
+            const int q = tid + u * NT;
+            if (q < MB * D / 4) {
+                const size_t g = (size_t)t0 * D + 4 * q;
+                pk[u] = ldraw<IO>(Kg + g);
+                pv[u] = ldraw<IO>(Vg + g);
+                if (rev) {
+                    pq[u] = ldraw<IO>(Qg + g);
+                    pz[u] = ldraw<IO>(DZg + g);
+                }
+            }
+        }
+        pe = tid < MB ? eg[t0 + tid] : 0.f;
+    };
+    auto commit_tiles = [&](bool rev) {
+#pragma unroll
+        for (int u = 0; u < CT; ++u) {
+            const int q = tid + u * NT;
+            if (q < MB * D / 4) {
+                const int s = (4 * q) / D, ii = (4 * q) % D;
+                st4(S.K + s * LD + ii, cvt4(pk[u]));
+                st4(S.E + s * LD + ii, cvt4(pv[u]));
+                if (rev) {
+                    st4(S.Q + s * LD + ii, cvt4(pq[u]));
+                    st4(S.DZ + s * LD + ii, cvt4(pz[u]));
+                }
+            }
+        }
+        if (tid < MB) S.et[tid] = p.eta_gate ? p.eta_base / (1.f + __expf(-pe)) : pe;
+    };
+    auto issue_anchor = [&](int i) {
+        const float *wsi = ws + (size_t)i * ((size_t)D * D + D);
+#pragma unroll
+        for (int u = 0; u < CW; ++u) {
+            const int q = tid + u * NT;
+            if (q < D * D / 4) pw[u] = ld4(wsi + 4 * q);
+        }
+        pc = tid < D ? wsi[D * D + tid] : 0.f;
+    };
+    auto commit_anchor = [&]() {
+#pragma unroll
+        for (int u = 0; u < CW; ++u) {
+            const int q = tid + u * NT;
+            if (q < D * D / 4) st4(S.W + ((4 * q) / D) * LD + (4 * q) % D, pw[u]);
+        }
+        if (tid < D) S.c[tid] = pc;
+    };
 
     // ---- forward sweep
+    if (PF) issue_tiles(0, false);
     for (int i = 0; i < n; ++i) {
         const int t0 = i * MB;
         __syncthreads();
@@ -759,9 +843,13 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             st4(wsi + 4 * q, ld4(S.W + j * LD + ii));
         }
         for (int j = tid; j < D; j += NT) wsi[D * D + j] = S.c[j];
-        load_tile(S.K, Kg + (size_t)t0 * D);
-        load_tile(S.E, Vg + (size_t)t0 * D);
-        load_eta(t0);
+        if (PF) {
+            commit_tiles(false);
+        } else {
+            load_tile(S.K, Kg + (size_t)t0 * D);
+            load_tile(S.E, Vg + (size_t)t0 * D);
+            load_eta(t0);
+        }
         __syncthreads();
         {
             float a[RPT], dummy[RPT];
@@ -774,6 +862,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         __syncthreads();
         key_rows_t<D, MB, NT>(S, p.eps, warp, lane);
         __syncthreads();
+        if (PF && i + 1 < n) issue_tiles(t0 + MB, false);
         {
             float acc[C::TR][C::TC] = {};
             outer_acc<D, MB, NT, true>(acc, S.G, S.K, S.et, tid);
@@ -788,20 +877,30 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
     }
 
     // ---- reverse sweep
+    if (PF) {
+        __syncthreads();  // the forward sweep's last anchor store is visible
+        issue_tiles((n - 1) * MB, true);
+        issue_anchor(n - 1);
+    }
     for (int i = n - 1; i >= 0; --i) {
         const int t0 = i * MB;
         __syncthreads();
-        const float *wsi = ws + (size_t)i * ((size_t)D * D + D);
-        for (int q = tid; q < D * D / 4; q += NT) {
-            const int j = (4 * q) / D, ii = (4 * q) % D;
-            st4(S.W + j * LD + ii, ld4(wsi + 4 * q));
+        if (PF) {
+            commit_tiles(true);
+            commit_anchor();
+        } else {
+            const float *wsi = ws + (size_t)i * ((size_t)D * D + D);
+            for (int q = tid; q < D * D / 4; q += NT) {
+                const int j = (4 * q) / D, ii = (4 * q) % D;
+                st4(S.W + j * LD + ii, ld4(wsi + 4 * q));
+            }
+            for (int j = tid; j < D; j += NT) S.c[j] = wsi[D * D + j];
+            load_tile(S.K, Kg + (size_t)t0 * D);
+            load_tile(S.Q, Qg + (size_t)t0 * D);
+            load_tile(S.E, Vg + (size_t)t0 * D);
+            load_tile(S.DZ, DZg + (size_t)t0 * D);
+            load_eta(t0);
         }
-        for (int j = tid; j < D; j += NT) S.c[j] = wsi[D * D + j];
-        load_tile(S.K, Kg + (size_t)t0 * D);
-        load_tile(S.Q, Qg + (size_t)t0 * D);
-        load_tile(S.E, Vg + (size_t)t0 * D);
-        load_tile(S.DZ, DZg + (size_t)t0 * D);
-        load_eta(t0);
         __syncthreads();
         // y_s = W k_s + c, W q_t + c; R_s = dW' k_s + dc'; q_t.k_s + 1
         {
@@ -1045,6 +1144,10 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         }
         __syncthreads();
         // dk_s; dW, dc carried to batch i - 1; dgamma, dbeta; deta
+        if (PF && i > 0) {
+            issue_tiles(t0 - MB, true);
+            issue_anchor(i - 1);
+        }
         {
             float a[RPT];
 #pragma unroll
