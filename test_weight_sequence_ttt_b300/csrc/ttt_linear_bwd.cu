@@ -1218,7 +1218,7 @@ template <typename IO>
 cudaError_t launch_bwd_io(const LinearBwdParams &p, int chains, cudaStream_t s, size_t smem_generic)
 {
     if (p.d == 64 && p.mb == 16) return launch_tiled<IO, 64, 16, 256>(p, chains, s);
-    if (p.d == 128 && p.mb == 16) return launch_tiled<IO, 128, 16, 512>(p, chains, s);
+    if (p.d == 128 && p.mb == 16) return launch_tiled<IO, 128, 16, 256>(p, chains, s);
     cudaError_t e = ensure_smem<linear_bwd_kernel<IO>>((int)smem_generic);
     if (e != cudaSuccess) return e;
     linear_bwd_kernel<IO><<<chains, kThreads, smem_generic, s>>>(p);
