@@ -819,10 +819,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         __syncthreads();
         {
             float *w1 = W1s(i), *w2 = W2s(i);
-            for (int x = tid; x < HH * d; x += kNT) {
-                const int m = x / d, j = x % d;
-                w1[x] = W1h[m * LW + j];
-                w2[x] = W2h[m * LW + j];
+            for (int x = tid; x < HH * d / 4; x += kNT) {
+                const int m = (4 * x) / d, j = (4 * x) % d;
+                *reinterpret_cast<float4 *>(w1 + 4 * x) = ld4(W1h + m * LW + j);
+                *reinterpret_cast<float4 *>(w2 + 4 * x) = ld4(W2h + m * LW + j);
             }
             for (int m = tid; m < HH; m += kNT) c1s(i)[m] = c1h[m];
             if (rank == 0)
@@ -868,10 +868,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         __syncthreads();
         {
             const float *w1 = W1s(i), *w2 = W2s(i);
-            for (int x = tid; x < HH * d; x += kNT) {
-                const int m = x / d, j = x % d;
-                W1h[m * LW + j] = w1[x];
-                W2h[m * LW + j] = w2[x];
+            for (int x = tid; x < HH * d / 4; x += kNT) {
+                const int m = (4 * x) / d, j = (4 * x) % d;
+                *reinterpret_cast<float4 *>(W1h + m * LW + j) = ld4(w1 + 4 * x);
+                *reinterpret_cast<float4 *>(W2h + m * LW + j) = ld4(w2 + 4 * x);
             }
             for (int m = tid; m < HH; m += kNT) c1h[m] = c1s(i)[m];
             for (int j = tid; j < d; j += kNT) S.c2[j] = c2s(i)[j];
