@@ -125,7 +125,7 @@ __device__ MSmem mcarve(float *sm, int d, int h, int b)
 // out(s, n) for the MB rows s of A and the N rows n of W (row-major, Kd columns):
 // acc = sum_k A[s][k] W[n][k]; epi(s, n, acc). Each work item is one weight row
 // and RB rows of A, so each weight element is read MB / RB times.
-template <int MB, int RB, typename Epi>
+template <int MB, int RB, int UNR, typename Epi>
 __device__ __forceinline__ void prod_rows_rb(const float *A, const float *W, int ldw, int N, int Kd, Epi &epi)
 {
     for (int it = threadIdx.x; it < N * (MB / RB); it += kNT) {
@@ -134,7 +134,7 @@ __device__ __forceinline__ void prod_rows_rb(const float *A, const float *W, int
 #pragma unroll
         for (int r = 0; r < RB; ++r) acc[r] = 0.f;
         const float *w = W + (size_t)n * ldw;
-#pragma unroll 8
+#pragma unroll UNR
         for (int k = 0; k < Kd; k += 4) {
             const float4 wv = ld4(w + k);
 #pragma unroll
@@ -149,7 +149,7 @@ __device__ __forceinline__ void prod_rows_rb(const float *A, const float *W, int
 }
 
 // out(s, n) = sum_j A[s][j] W[j][n] (W row-major [Kd][N]); lanes hold consecutive n.
-template <int MB, int RB, typename Epi>
+template <int MB, int RB, int UNR, typename Epi>
 __device__ __forceinline__ void prod_cols_rb(const float *A, const float *W, int ldw, int N, int Kd, Epi &epi)
 {
     for (int it = threadIdx.x; it < N * (MB / RB); it += kNT) {
@@ -157,7 +157,7 @@ __device__ __forceinline__ void prod_cols_rb(const float *A, const float *W, int
         float acc[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) acc[r] = 0.f;
-#pragma unroll 4
+#pragma unroll UNR
         for (int j = 0; j < Kd; j += 4) {
             const float w0 = W[(size_t)j * ldw + n], w1 = W[(size_t)(j + 1) * ldw + n];
             const float w2 = W[(size_t)(j + 2) * ldw + n], w3 = W[(size_t)(j + 3) * ldw + n];
@@ -180,39 +180,41 @@ __device__ __forceinline__ int rows_per_item(int N)
 }
 
 // The products with W row-major and rows ldw floats apart (ldw = Kd for
-// prod_rows, N for prod_cols unless the rows are padded).
-template <int MB, typename Epi>
+// prod_rows, N for prod_cols unless the rows are padded). UNR is the unrolling
+// of the weight loop: deep where the weights come from L2 (more loads in
+// flight), shallow where they sit in shared memory (fewer registers).
+template <int MB, int UNR = 8, typename Epi>
 __device__ __forceinline__ void prod_rows_ld(const float *A, const float *W, int ldw, int N, int Kd, Epi epi)
 {
     switch (rows_per_item<MB>(N)) {
-    case 8: prod_rows_rb<MB, (MB >= 8 ? 8 : 1)>(A, W, ldw, N, Kd, epi); break;
-    case 4: prod_rows_rb<MB, (MB >= 4 ? 4 : 1)>(A, W, ldw, N, Kd, epi); break;
-    case 2: prod_rows_rb<MB, (MB >= 2 ? 2 : 1)>(A, W, ldw, N, Kd, epi); break;
-    default: prod_rows_rb<MB, 1>(A, W, ldw, N, Kd, epi);
+    case 8: prod_rows_rb<MB, (MB >= 8 ? 8 : 1), UNR>(A, W, ldw, N, Kd, epi); break;
+    case 4: prod_rows_rb<MB, (MB >= 4 ? 4 : 1), UNR>(A, W, ldw, N, Kd, epi); break;
+    case 2: prod_rows_rb<MB, (MB >= 2 ? 2 : 1), UNR>(A, W, ldw, N, Kd, epi); break;
+    default: prod_rows_rb<MB, 1, UNR>(A, W, ldw, N, Kd, epi);
     }
 }
 
-template <int MB, typename Epi>
+template <int MB, int UNR = 4, typename Epi>
 __device__ __forceinline__ void prod_cols_ld(const float *A, const float *W, int ldw, int N, int Kd, Epi epi)
 {
     switch (rows_per_item<MB>(N)) {
-    case 8: prod_cols_rb<MB, (MB >= 8 ? 8 : 1)>(A, W, ldw, N, Kd, epi); break;
-    case 4: prod_cols_rb<MB, (MB >= 4 ? 4 : 1)>(A, W, ldw, N, Kd, epi); break;
-    case 2: prod_cols_rb<MB, (MB >= 2 ? 2 : 1)>(A, W, ldw, N, Kd, epi); break;
-    default: prod_cols_rb<MB, 1>(A, W, ldw, N, Kd, epi);
+    case 8: prod_cols_rb<MB, (MB >= 8 ? 8 : 1), UNR>(A, W, ldw, N, Kd, epi); break;
+    case 4: prod_cols_rb<MB, (MB >= 4 ? 4 : 1), UNR>(A, W, ldw, N, Kd, epi); break;
+    case 2: prod_cols_rb<MB, (MB >= 2 ? 2 : 1), UNR>(A, W, ldw, N, Kd, epi); break;
+    default: prod_cols_rb<MB, 1, UNR>(A, W, ldw, N, Kd, epi);
     }
 }
 
 template <int MB, typename Epi>
 __device__ __forceinline__ void prod_rows(const float *A, const float *W, int N, int Kd, Epi epi)
 {
-    prod_rows_ld<MB>(A, W, Kd, N, Kd, epi);
+    prod_rows_ld<MB, 8>(A, W, Kd, N, Kd, epi);
 }
 
 template <int MB, typename Epi>
 __device__ __forceinline__ void prod_cols(const float *A, const float *W, int N, int Kd, Epi epi)
 {
-    prod_cols_ld<MB>(A, W, N, N, Kd, epi);
+    prod_cols_ld<MB, 4>(A, W, N, N, Kd, epi);
 }
 
 // Outer products over the mini-batch, 4 x 4 blocks per work item: for rows
@@ -785,7 +787,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
     };
     // Y = X2 W2^T + c2 summed over both halves into Yh (the key side's only exchange).
     auto key_side = [&]() {
-        prod_rows_ld<MB>(S.K, W1h, LW, HH, d, [&](int s, int m, float a) {
+        prod_rows_ld<MB, 2>(S.K, W1h, LW, HH, d, [&](int s, int m, float a) {
             const float z = a + c1h[m];
             S.Z1[s * HH + m] = z;
             S.X2[s * HH + m] = gelu0(z);
@@ -793,7 +795,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         __syncthreads();
         {
             float *rm = remote();
-            prod_cols_ld<MB>(S.X2, W2h, LW, d, HH, [&](int s, int j, float a) {
+            prod_cols_ld<MB, 2>(S.X2, W2h, LW, d, HH, [&](int s, int j, float a) {
                 S.Yh[s * d + j] = a;
                 rm[s * d + j] = a;
             });
@@ -807,7 +809,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         __syncthreads();
         key_rows(S, d, MB, p.eps, warp, lane);
         __syncthreads();
-        prod_rows_ld<MB>(S.G, W2h, LW, HH, d, [&](int s, int m, float a) {
+        prod_rows_ld<MB, 2>(S.G, W2h, LW, HH, d, [&](int s, int m, float a) {
             S.P1[s * HH + m] = a;
             S.G1[s * HH + m] = a * gelu1(S.Z1[s * HH + m]);
         });
@@ -886,7 +888,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         load_eta(t0);
         __syncthreads();
         key_side();
-        prod_rows_ld<MB>(S.Q, W1h, LW, HH, d, [&](int s, int m, float a) { S.Z1q[s * HH + m] = a + c1h[m]; });
+        prod_rows_ld<MB, 2>(S.Q, W1h, LW, HH, d, [&](int s, int m, float a) { S.Z1q[s * HH + m] = a + c1h[m]; });
         gram<MB>(S.QK1, S.Q, S.K, d, 1.f, 1.f, false);
         __syncthreads();
         for (int x = tid; x < MB * HH; x += kNT) {
@@ -910,7 +912,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
                 S.QK2[it] = acc;
                 rm[it] = acc;
             }
-            prod_cols_ld<MB>(S.X2q, W2h, LW, d, HH, [&](int s, int j, float a) {
+            prod_cols_ld<MB, 2>(S.X2q, W2h, LW, d, HH, [&](int s, int j, float a) {
                 S.P[s * d + j] = a;
                 rm[MB * MB + s * d + j] = a;
             });
@@ -978,7 +980,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         }
         __syncthreads();
         // dZ1q (into Z1q), dG, the q- and dW2'-sides of dX2, deta (layer 2)
-        prod_rows_ld<MB>(S.DYq, W2h, LW, HH, d, [&](int t, int m, float a) {
+        prod_rows_ld<MB, 2>(S.DYq, W2h, LW, HH, d, [&](int t, int m, float a) {
             for (int s = 0; s <= t; ++s) a = fmaf(S.DA2[t * MB + s] * S.et[s] * inv_b, S.X2[s * HH + m], a);
             S.Z1q[t * HH + m] = a * gelu1(S.Z1q[t * HH + m]);
         });
@@ -1027,7 +1029,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         // at 2 MB d), each partial over h; dG1 is local
         {
             float *rm = remote();
-            prod_cols_ld<MB>(S.Z1q, W1h, LW, d, HH, [&](int t, int k, float a) {
+            prod_cols_ld<MB, 2>(S.Z1q, W1h, LW, d, HH, [&](int t, int k, float a) {
                 S.DY[t * d + k] = a;  // DY is free until the second-order rows
                 rm[t * d + k] = a;
             });
@@ -1085,7 +1087,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         // exchange: dP1 W2^T (the dP1-part of dG), partial over h
         {
             float *rm = remote();
-            prod_cols_ld<MB>(S.DG1, W2h, LW, d, HH, [&](int s, int j, float a) {
+            prod_cols_ld<MB, 2>(S.DG1, W2h, LW, d, HH, [&](int s, int j, float a) {
                 S.DY[s * d + j] = a;
                 rm[s * d + j] = a;
             });
@@ -1144,7 +1146,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         }
         __syncthreads();
         // dX2 += dY W2;  dZ1 = (gelu'' part) + dX2 * gelu'(Z1)  (into R1)
-        prod_rows_ld<MB>(S.DY, W2h, LW, HH, d, [&](int s, int m, float a) {
+        prod_rows_ld<MB, 2>(S.DY, W2h, LW, HH, d, [&](int s, int m, float a) {
             const int x = s * HH + m;
             S.R1[x] += (S.DX2[x] + a) * gelu1(S.Z1[x]);
         });
@@ -1152,7 +1154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         // exchange: dZ1 W1 (the rest of dK), partial over h
         {
             float *rm = remote();
-            prod_cols_ld<MB>(S.R1, W1h, LW, d, HH, [&](int s, int k, float a) {
+            prod_cols_ld<MB, 2>(S.R1, W1h, LW, d, HH, [&](int s, int k, float a) {
                 S.DG[s * d + k] = a;  // DG is no longer needed
                 rm[s * d + k] = a;
             });
