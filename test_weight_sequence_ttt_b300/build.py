@@ -4,9 +4,10 @@ Run ``python -m test_weight_sequence_ttt_b300.build`` (or call ``build()``).
 Objects go to ``_build/`` next to this file; the shared library lands in the
 package directory, where the binding loads it. Rebuilds only what changed.
 
-``build_faults()`` builds ``libttt_b300_faults.so``: the same sources with the
+``build_faults()`` builds ``libttt_b300_faults.so``: the same library with the
 failure-injection hook compiled in (``-DTTT_FAULT_HOOKS``), used only by the
-failure-detection tests.
+failure-detection tests. Only the sources that mention the hook are compiled
+again; the other objects are the product build's.
 """
 from __future__ import annotations
 
@@ -51,17 +52,26 @@ def _compile(src, obj, verbose, extra=()):
     return r.stderr
 
 
+def _mentions(path, word):
+    with open(path) as f:
+        return word in f.read()
+
+
 def build(verbose: bool = False, force: bool = False, *, out: str = OUT, build_dir: str = BUILD,
-          extra=()) -> str:
+          extra=(), only_with: str = "") -> str:
+    """Compile the stale sources in parallel and link. With ``only_with`` only
+    the sources that mention that word are compiled into ``build_dir``; the
+    others are linked from the product build's objects."""
     os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdrs = _headers()
     jobs = []
     objs = []
     for s in srcs:
-        o = os.path.join(build_dir, os.path.basename(s)[:-3] + ".o")
+        own = not only_with or _mentions(s, only_with)
+        o = os.path.join(build_dir if own else BUILD, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
-        if force or _stale(o, [s, *hdrs]):
+        if own and (force or _stale(o, [s, *hdrs])):
             jobs.append((s, o))
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
@@ -80,7 +90,9 @@ def build(verbose: bool = False, force: bool = False, *, out: str = OUT, build_d
 
 def build_faults(verbose: bool = False, force: bool = False) -> str:
     """The library with the failure-injection hook (tests only)."""
-    return build(verbose, force, out=OUT_FAULTS, build_dir=BUILD_FAULTS, extra=("-DTTT_FAULT_HOOKS",))
+    build(verbose, force)  # the objects it shares with the product library
+    return build(verbose, force, out=OUT_FAULTS, build_dir=BUILD_FAULTS, extra=("-DTTT_FAULT_HOOKS",),
+                 only_with="TTT_FAULT_HOOKS")
 
 
 if __name__ == "__main__":

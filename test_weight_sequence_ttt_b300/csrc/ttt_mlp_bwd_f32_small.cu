@@ -1,0 +1,13 @@
+// ttt_mlp_bwd_f32_small.cu -- instantiations of the TTT-MLP backward kernels (ttt_mlp_bwd.cuh)
+// for fp32 inputs, mini-batch sizes 1, 2, 4.
+#include "ttt_mlp_bwd.cuh"
+
+namespace ttt {
+namespace mlpb {
+
+template cudaError_t launch_mb<float, 1>(const MlpBwdParams &, int, cudaStream_t);
+template cudaError_t launch_mb<float, 2>(const MlpBwdParams &, int, cudaStream_t);
+template cudaError_t launch_mb<float, 4>(const MlpBwdParams &, int, cudaStream_t);
+
+}  // namespace mlpb
+}  // namespace ttt
