@@ -252,12 +252,16 @@ def oracle_sample(w, n_chains: int, T: int, nthreads: int = 0, rule: str = "pref
     return dt, n_chains * T, th
 
 
-def _sample_shape(w, cpu_s: float, threads: int):
+def _sample_shape(w, cpu_s: float, threads: int, calib=None):
     """Pick (chains, T') so one oracle call costs about ``cpu_s`` core-seconds
-    spread over ``threads`` threads (calibrated on one short chain)."""
+    spread over ``threads`` threads (calibrated on one short chain, single
+    threaded; ``calib`` receives the single-thread tokens/s)."""
     Tc = max(w.b, min(w.T, (256 // w.b) * w.b or w.b))
     dt, toks, _ = oracle_sample(w, 1, Tc, nthreads=1)
     per_tok = dt / toks                                   # single-thread seconds per token-head
+    if calib is not None:
+        calib["single_thread_tokens_per_s"] = 1.0 / per_tok
+        calib["single_thread_sample"] = "1 chain x %d tokens" % Tc
     tokens_budget = cpu_s / per_tok
     chains = int(min(w.chains, max(1, tokens_budget // w.T)))
     if chains >= threads or chains == w.chains:
@@ -265,6 +269,17 @@ def _sample_shape(w, cpu_s: float, threads: int):
     chains = min(w.chains, threads)
     T = int(max(w.b, (tokens_budget / chains) // w.b * w.b))
     return chains, min(T, w.T)
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 def oracle_backward_sample(w, n_chains: int, T: int):
@@ -563,12 +578,13 @@ def run_gpu(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         threads = __import__("oracle").max_threads()
-        chains, Ts = _sample_shape(w, args.cpu_budget_s, threads)
+        calib = {}
+        chains, Ts = _sample_shape(w, args.cpu_budget_s, threads, calib)
         dt, toks, th = oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule)
         line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
                                 "sample": "%d of %d chains x %d tokens (fp64 primal token loop, C, OpenMP)"
                                           % (chains, w.chains, Ts),
-                                "seconds": dt, "cpu_count": os.cpu_count()}
+                                "seconds": dt, "cpu_count": os.cpu_count(), "model": cpu_model(), **calib}
     return line
 
 
@@ -629,7 +645,8 @@ def run_reference(args):
         "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
                    "mb": w.b, "hidden": w.hidden or None, "out_rule": args.out_rule},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": "%d of %d chains x %d tokens per step" % (chains, w.chains, Ts)},
+                         "sample": "%d of %d chains x %d tokens per step" % (chains, w.chains, Ts),
+                         "cpu_count": os.cpu_count(), "model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
