@@ -125,7 +125,8 @@ def backward_cost(w):
 
     Bytes: K, V read by the forward sweep and Q, K, V, dZ by the reverse one
     (io dtype), eta twice, dQ, dK, dV, deta written fp32, plus every
-    mini-batch's starting state written once and read once. FLOPs, per
+    mini-batch's starting state (and for TTT-MLP its key-side activations)
+    written once and read once. FLOPs, per
     mini-batch of b tokens, the contractions as executed: TTT-Linear
     10 b d^2 (forward recompute 2, reverse 8) + b^2 d (Q K^T) + 5 b(b+1)/2 d
     (the causal b x b x d products); TTT-MLP 25 b h d (forward recompute 5,
@@ -138,7 +139,7 @@ def backward_cost(w):
         flops_tok = 2 * (10 * d * d + b * d) + 5 * (b + 1) * d
     else:
         h = w.hidden
-        state = w.chains * (w.T // b) * (2 * h * d + h + d) * 4 * 2
+        state = (w.chains * (w.T // b) * (2 * h * d + h + d) + w.tokens * (2 * h + 3 * d + 2)) * 4 * 2
         flops_tok = 2 * (25 * h * d + b * (d + h)) + 5 * (b + 1) * (d + h)
     return per_tok * w.tokens + state, flops_tok * w.tokens
 

@@ -278,9 +278,10 @@ ttt_status ttt_linear_backward_noalloc(const ttt_linear_bwd_args *args, void *st
  * with respect to Q, K, V, eta (the gate logits when eta_gate = 1), W1_0, c1_0,
  * W2_0, c2_0, ln_g and ln_b; weight and LayerNorm gradients per chain, as for
  * TTT-Linear. Workspace: at least ttt_mlp_backward_workspace_bytes() bytes
- * (per chain (T/mb)(2 hidden d + hidden + d) + 2 hidden d floats: every
- * mini-batch's starting state and the weight-gradient accumulators), 16-byte
- * aligned, contents ignored on entry and unspecified on return. */
+ * (per chain (T/mb)(2 hidden d + hidden + d) + 2 hidden d + T (2 hidden + 3 d + 2)
+ * floats: every mini-batch's starting state, the weight-gradient accumulators
+ * and every mini-batch's key-side activations), 16-byte aligned, contents
+ * ignored on entry and unspecified on return. */
 typedef struct {
     int32_t B, H, T, d, hidden, mb;
     int32_t io;              /* ttt_dtype of Q, K, V and dZ                    */

@@ -44,8 +44,10 @@ bool mlp_bwd_supported(int io, int d, int hidden, int mb)
 
 size_t mlp_bwd_workspace_bytes(int B, int H, int T, int d, int hidden, int mb)
 {
-    const size_t hd = (size_t)hidden * d;
-    return (size_t)B * H * ((size_t)(T / mb) * (2 * hd + hidden + d) + 2 * hd) * sizeof(float);
+    // per chain: every mini-batch's starting state, dW1 and dW2, every mini-batch's key side
+    const size_t hd = (size_t)hidden * d, n = (size_t)(T / mb);
+    return (size_t)B * H * (n * (2 * hd + hidden + d) + 2 * hd + n * mlpb::mlp_bwd_saved_floats(d, hidden, mb)) *
+           sizeof(float);
 }
 
 cudaError_t launch_mlp_bwd(const MlpBwdParams &p, int io, int chains, cudaStream_t s)

@@ -85,6 +85,15 @@ __device__ __forceinline__ float wsum(float v)
 }
 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ void st4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+
+// Floats of one mini-batch's saved key side (Z1 and P1 by CTA half, yh, e, g, and the
+// two row statistics): the two-CTA kernel's forward sweep writes it, its reverse
+// sweep reads it back instead of recomputing.
+__host__ __device__ inline size_t mlp_bwd_saved_floats(int d, int h, int b)
+{
+    return 2 * (size_t)b * h + 3 * (size_t)b * d + 2 * (size_t)b;
+}
 
 __host__ __device__ inline size_t mlp_bwd_smem_floats(int d, int h, int b)
 {
@@ -688,7 +697,10 @@ __global__ void __launch_bounds__(kNT, 1) mlp_bwd_kernel(MlpBwdParams p)
 // between exchanges: a slot is written again only after the peer has passed
 // the next barrier, and the peer reads each slot right after the barrier that
 // filled it. CTA 0 writes the token gradients and the d-wide parameter
-// gradients; each CTA writes its halves of dW1, dc1, dW2.
+// gradients; each CTA writes its halves of dW1, dc1, dW2. The forward sweep also
+// keeps each mini-batch's key side (Z1, P1, yh, e, g and the row statistics) in the
+// workspace, so the reverse sweep skips the three products, the exchange and the
+// LayerNorm rows that would recompute it.
 constexpr int kCB = 16;  // mini-batch size of the cluster kernel
 
 __host__ __device__ inline size_t mlp_bwd_cluster_smem_floats(int d, int h)
@@ -751,8 +763,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
     const IO *DZg = static_cast<const IO *>(p.dZ) + tok0 * d;
     const float *eg = p.eta + tok0;
     const size_t hd = (size_t)h * d, slot = 2 * hd + h + d, r0 = (size_t)rank * HH;
-    float *ws = p.ws + (size_t)chain * (n * slot + 2 * hd);
+    const size_t SV = mlp_bwd_saved_floats(d, h, MB);
+    float *ws = p.ws + (size_t)chain * (n * slot + 2 * hd + n * SV);
     float *dW1h = ws + n * slot + r0 * d, *dW2h = ws + n * slot + hd + r0 * d;  // this CTA's rows
+    // saved key side of mini-batch i: Z1 [2][MB][HH] and P1 [2][MB][HH] by CTA, then yh, e, g
+    // [MB][d] and r, mean(u yh) [MB]
+    auto Svs = [&](int i) { return ws + n * slot + 2 * hd + (size_t)i * SV; };
     auto W1s = [&](int i) { return ws + (size_t)i * slot + r0 * d; };
     auto c1s = [&](int i) { return ws + (size_t)i * slot + hd + r0; };
     auto W2s = [&](int i) { return ws + (size_t)i * slot + hd + h + r0 * d; };
@@ -843,6 +859,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         __syncthreads();
         key_side();
         __syncthreads();
+        {
+            float *sv = Svs(i);
+            float *z = sv + (size_t)rank * MB * HH, *pp = sv + (size_t)(2 + rank) * MB * HH;
+            for (int x = tid; x < MB * HH / 4; x += kNT) {
+                st4(z + 4 * x, ld4(S.Z1 + 4 * x));
+                st4(pp + 4 * x, ld4(S.P1 + 4 * x));
+            }
+            if (rank == 0) {
+                float *yd = sv + (size_t)4 * MB * HH;
+                for (int x = tid; x < MB * d / 4; x += kNT) {
+                    st4(yd + 4 * x, ld4(S.Yh + 4 * x));
+                    st4(yd + MB * d + 4 * x, ld4(S.E + 4 * x));
+                    st4(yd + 2 * MB * d + 4 * x, ld4(S.G + 4 * x));
+                }
+                for (int x = tid; x < MB; x += kNT) {
+                    yd[3 * MB * d + x] = S.rk[x];
+                    yd[3 * MB * d + MB + x] = S.m2k[x];
+                }
+            }
+        }
         outer4<MB>(HH, d, S.G1, S.K, nullptr, nullptr, nullptr, nullptr, S.et, [&](int m, int k, float4 a) {
             float *w = W1h + m * LW + k;
             w[0] -= a.x * inv_b;
@@ -887,12 +923,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
             const size_t g = (size_t)t0 * d + x;
             S.K[x] = ldx<IO>(Kg + g);
             S.Q[x] = ldx<IO>(Qg + g);
-            S.E[x] = ldx<IO>(Vg + g);
             S.DZ[x] = ldx<IO>(DZg + g);
         }
         load_eta(t0);
+        {
+            // the key side of this mini-batch, as the forward sweep left it
+            const float *sv = Svs(i);
+            const float *z = sv + (size_t)rank * MB * HH, *pp = sv + (size_t)(2 + rank) * MB * HH;
+            const float *yd = sv + (size_t)4 * MB * HH;
+            for (int x = tid; x < MB * HH / 4; x += kNT) {
+                const float4 zz = ld4(z + 4 * x), pv = ld4(pp + 4 * x);
+                st4(S.Z1 + 4 * x, zz);
+                st4(S.P1 + 4 * x, pv);
+                st4(S.X2 + 4 * x, make_float4(gelu0(zz.x), gelu0(zz.y), gelu0(zz.z), gelu0(zz.w)));
+                st4(S.G1 + 4 * x, make_float4(pv.x * gelu1(zz.x), pv.y * gelu1(zz.y), pv.z * gelu1(zz.z),
+                                              pv.w * gelu1(zz.w)));
+            }
+            for (int x = tid; x < MB * d / 4; x += kNT) {
+                st4(S.Yh + 4 * x, ld4(yd + 4 * x));
+                st4(S.E + 4 * x, ld4(yd + MB * d + 4 * x));
+                st4(S.G + 4 * x, ld4(yd + 2 * MB * d + 4 * x));
+            }
+            for (int x = tid; x < MB; x += kNT) {
+                S.rk[x] = yd[3 * MB * d + x];
+                S.m2k[x] = yd[3 * MB * d + MB + x];
+            }
+        }
         __syncthreads();
-        key_side();
         prod_rows_ld<MB, 2>(S.Q, W1h, LW, HH, d, [&](int s, int m, float a) { S.Z1q[s * HH + m] = a + c1h[m]; });
         gram<MB>(S.QK1, S.Q, S.K, d, 1.f, 1.f, false);
         __syncthreads();

@@ -203,7 +203,8 @@ def test_validation_codes_backward(L):
 
 def test_mlp_backward_workspace_and_validation(L):
     hd = 256 * 64
-    assert ttt.mlp_backward_workspace_bytes(4, 12, 8192, 64, 256, 16) == 48 * (512 * (2 * hd + 256 + 64) + 2 * hd) * 4
+    assert ttt.mlp_backward_workspace_bytes(4, 12, 8192, 64, 256, 16) == \
+        48 * (512 * (2 * hd + 256 + 64) + 2 * hd + 8192 * (2 * 256 + 3 * 64 + 2)) * 4
     assert ttt.mlp_backward_workspace_bytes(1, 1, 30, 64, 256, 16) == 0
     base = 1 << 40
     step = 1 << 32
