@@ -129,8 +129,9 @@ def backward_cost(w):
     written once and read once. FLOPs, per
     mini-batch of b tokens, the contractions as executed: TTT-Linear
     10 b d^2 (forward recompute 2, reverse 8) + b^2 d (Q K^T) + 5 b(b+1)/2 d
-    (the causal b x b x d products); TTT-MLP 25 b h d (forward recompute 5,
-    reverse 20) + b^2 (d + h) (the two Grams) + 5 b(b+1)/2 (d + h); times 2."""
+    (the causal b x b x d products); TTT-MLP 22 b h d (forward recompute 5,
+    reverse 17: the reverse sweep reuses the forward sweep's key side) +
+    b^2 (d + h) (the two Grams) + 5 b(b+1)/2 (d + h); times 2."""
     es = 2 if w.io == "bf16" else 4
     d, b = w.d, w.b
     per_tok = (2 * d * es) + (4 * d * es) + 2 * 4 + 3 * d * 4 + 4
@@ -140,7 +141,7 @@ def backward_cost(w):
     else:
         h = w.hidden
         state = (w.chains * (w.T // b) * (2 * h * d + h + d) + w.tokens * (2 * h + 3 * d + 2)) * 4 * 2
-        flops_tok = 2 * (25 * h * d + b * (d + h)) + 5 * (b + 1) * (d + h)
+        flops_tok = 2 * (22 * h * d + b * (d + h)) + 5 * (b + 1) * (d + h)
     return per_tok * w.tokens + state, flops_tok * w.tokens
 
 

@@ -46,5 +46,5 @@ def test_cost_models():
     assert bb == 1548 * w.tokens + w.chains * (2048 // 16) * (64 * 64 + 64) * 8
     m = WORKLOADS["mlp_b4h12_d64_t8k"]
     _, mf = bench.backward_cost(m)
-    assert mf == (2 * (25 * 256 * 64 + 16 * (64 + 256)) + 5 * 17 * (64 + 256)) * m.tokens  # 856 640
+    assert mf == (2 * (22 * 256 * 64 + 16 * (64 + 256)) + 5 * 17 * (64 + 256)) * m.tokens  # 758 336
     assert abs(bench.FP32_PEAK_TFLOPS - 148 * 128 * 2 * 2.032e-3) < 1e-9   # TFLOP/s
