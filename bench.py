@@ -128,8 +128,9 @@ def backward_cost(w):
     mini-batch's starting state (and for TTT-MLP its key-side activations)
     written once and read once. FLOPs, per
     mini-batch of b tokens, the contractions as executed: TTT-Linear
-    10 b d^2 (forward recompute 2, reverse 8) + b^2 d (Q K^T) + 5 b(b+1)/2 d
-    (the causal b x b x d products); TTT-MLP 22 b h d (forward recompute 5,
+    10 b d^2 (forward recompute 2, reverse 8; 9 where the reverse sweep reuses
+    the forward sweep's key side, d = 64 and b = 16) + b^2 d (Q K^T) +
+    5 b(b+1)/2 d (the causal b x b x d products); TTT-MLP 22 b h d (forward recompute 5,
     reverse 17: the reverse sweep reuses the forward sweep's key side) +
     b^2 (d + h) (the two Grams) + 5 b(b+1)/2 (d + h); times 2."""
     es = 2 if w.io == "bf16" else 4
@@ -137,7 +138,10 @@ def backward_cost(w):
     per_tok = (2 * d * es) + (4 * d * es) + 2 * 4 + 3 * d * 4 + 4
     if w.variant == "linear":
         state = w.chains * (w.T // b) * (d * d + d) * 4 * 2
-        flops_tok = 2 * (10 * d * d + b * d) + 5 * (b + 1) * d
+        saves = d == 64 and b == 16  # the kernel that keeps each mini-batch's key side
+        if saves:
+            state += w.tokens * (3 * d + 2) * 4 * 2
+        flops_tok = 2 * ((9 if saves else 10) * d * d + b * d) + 5 * (b + 1) * d
     else:
         h = w.hidden
         state = (w.chains * (w.T // b) * (2 * h * d + h + d) + w.tokens * (2 * h + 3 * d + 2)) * 4 * 2

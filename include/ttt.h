@@ -211,10 +211,11 @@ ttt_status ttt_mlp_forward(const ttt_mlp_args *args, void *stream);
  * ([B][H][...]); a W0 shared by the sequences (w0_bstride = 0) or the [H][d]
  * LayerNorm parameters take the sum over B.
  * Workspace: the call recomputes the forward and keeps every mini-batch's
- * starting state (W_{i-1}, c_{i-1}) in `workspace`, caller-allocated device
- * memory of at least ttt_linear_backward_workspace_bytes() bytes
- * (B H (T/mb)(d^2 + d) floats), 16-byte aligned; its contents on entry are
- * ignored and on return are unspecified. Device problems (non-finite
+ * starting state (W_{i-1}, c_{i-1}) and key-side activations in `workspace`,
+ * caller-allocated device memory of at least
+ * ttt_linear_backward_workspace_bytes() bytes (B H ((T/mb)(d^2 + d) +
+ * T (3d + 2)) floats), 16-byte aligned; its contents on entry are ignored and
+ * on return are unspecified. Device problems (non-finite
  * gradients of the initial state or LayerNorm) go to *status_dev. */
 typedef struct {
     int32_t B, H, T, d, mb;

@@ -742,7 +742,12 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
     const IO *Vg = static_cast<const IO *>(p.V) + tok0 * D;
     const IO *DZg = static_cast<const IO *>(p.dZ) + tok0 * D;
     const float *eg = p.eta + tok0;
-    float *ws = p.ws + (size_t)chain * n * ((size_t)D * D + D);
+    // workspace of the chain: every mini-batch's starting state (W, c), then (d = 64) every
+    // mini-batch's key side (yh, e, g [MB][D] and r, mean(u yh) [MB]) for the reverse sweep
+    constexpr bool SAVE = D == 64 && NT == 256;  // with the register prefetch (PF), which loads it
+    constexpr size_t SVL = (size_t)MB * (3 * D + 2);
+    float *ws = p.ws + (size_t)chain * (n * ((size_t)D * D + D) + (size_t)T * (3 * D + 2));
+    float *svb = ws + (size_t)n * ((size_t)D * D + D);
 
     {
         const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
@@ -782,6 +787,8 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
     RC pk[CT], pq[CT], pv[CT], pz[CT];
     float4 pw[CW];
     float pc = 0.f, pe = 0.f;
+    float4 sy[CT], se[CT], sg[CT];  // prefetched key side (SAVE)
+    float sr = 0.f, sm2 = 0.f;
     auto issue_tiles = [&](int t0, bool rev) {
 #pragma unroll
         for (int u = 0; u < CT; ++u) {
@@ -789,7 +796,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             if (q < MB * D / 4) {
                 const size_t g = (size_t)t0 * D + 4 * q;
                 pk[u] = ldraw<IO>(Kg + g);
-                pv[u] = ldraw<IO>(Vg + g);
+                if (!(SAVE && rev)) pv[u] = ldraw<IO>(Vg + g);  // the reverse sweep reads e, not v
                 if (rev) {
                     pq[u] = ldraw<IO>(Qg + g);
                     pz[u] = ldraw<IO>(DZg + g);
@@ -805,7 +812,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             if (q < MB * D / 4) {
                 const int s = (4 * q) / D, ii = (4 * q) % D;
                 st4(S.K + s * LD + ii, cvt4(pk[u]));
-                st4(S.E + s * LD + ii, cvt4(pv[u]));
+                if (!(SAVE && rev)) st4(S.E + s * LD + ii, cvt4(pv[u]));
                 if (rev) {
                     st4(S.Q + s * LD + ii, cvt4(pq[u]));
                     st4(S.DZ + s * LD + ii, cvt4(pz[u]));
@@ -813,6 +820,36 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             }
         }
         if (tid < MB) S.et[tid] = p.eta_gate ? p.eta_base / (1.f + __expf(-pe)) : pe;
+    };
+    auto issue_saved = [&](int i) {
+        const float *sv = svb + (size_t)i * SVL;
+#pragma unroll
+        for (int u = 0; u < CT; ++u) {
+            const int q = tid + u * NT;
+            if (q < MB * D / 4) {
+                sy[u] = ld4(sv + 4 * q);
+                se[u] = ld4(sv + MB * D + 4 * q);
+                sg[u] = ld4(sv + 2 * MB * D + 4 * q);
+            }
+        }
+        sr = tid < MB ? sv[3 * MB * D + tid] : 0.f;
+        sm2 = tid < MB ? sv[3 * MB * D + MB + tid] : 0.f;
+    };
+    auto commit_saved = [&]() {
+#pragma unroll
+        for (int u = 0; u < CT; ++u) {
+            const int q = tid + u * NT;
+            if (q < MB * D / 4) {
+                const int s = (4 * q) / D, ii = (4 * q) % D;
+                st4(S.Yh + s * LD + ii, sy[u]);
+                st4(S.E + s * LD + ii, se[u]);
+                st4(S.G + s * LD + ii, sg[u]);
+            }
+        }
+        if (tid < MB) {
+            S.rk[tid] = sr;
+            S.m2k[tid] = sm2;
+        }
     };
     auto issue_anchor = [&](int i) {
         const float *wsi = ws + (size_t)i * ((size_t)D * D + D);
@@ -863,6 +900,19 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         key_rows_t<D, MB, NT>(S, p.eps, warp, lane);
         __syncthreads();
         if (PF && i + 1 < n) issue_tiles(t0 + MB, false);
+        if (SAVE) {
+            float *sv = svb + (size_t)i * SVL;
+            for (int q = tid; q < MB * D / 4; q += NT) {
+                const int s = (4 * q) / D, ii = (4 * q) % D;
+                st4(sv + 4 * q, ld4(S.Yh + s * LD + ii));
+                st4(sv + MB * D + 4 * q, ld4(S.E + s * LD + ii));
+                st4(sv + 2 * MB * D + 4 * q, ld4(S.G + s * LD + ii));
+            }
+            for (int x = tid; x < MB; x += NT) {
+                sv[3 * MB * D + x] = S.rk[x];
+                sv[3 * MB * D + MB + x] = S.m2k[x];
+            }
+        }
         {
             float acc[C::TR][C::TC] = {};
             outer_acc<D, MB, NT, true>(acc, S.G, S.K, S.et, tid);
@@ -881,6 +931,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         __syncthreads();  // the forward sweep's last anchor store is visible
         issue_tiles((n - 1) * MB, true);
         issue_anchor(n - 1);
+        if (SAVE) issue_saved(n - 1);
     }
     for (int i = n - 1; i >= 0; --i) {
         const int t0 = i * MB;
@@ -888,6 +939,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         if (PF) {
             commit_tiles(true);
             commit_anchor();
+            if (SAVE) commit_saved();
         } else {
             const float *wsi = ws + (size_t)i * ((size_t)D * D + D);
             for (int q = tid; q < D * D / 4; q += NT) {
@@ -910,12 +962,16 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
                 ak[r] = aq[r] = S.c[col];
                 ar[r] = S.dc[col];
             }
-            prod_mt<D, MB, NT, true>(ak, aq, S.K, S.Q, S.W, col, rg);
+            if (SAVE) {
+                prod_mt<D, MB, NT, false>(aq, dummy, S.Q, nullptr, S.W, col, rg);  // y_s was saved
+            } else {
+                prod_mt<D, MB, NT, true>(ak, aq, S.K, S.Q, S.W, col, rg);
+            }
             prod_mt<D, MB, NT, false>(ar, dummy, S.K, nullptr, S.dW, col, rg);
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const int s = rg + NG * r;
-                S.Yh[s * LD + col] = ak[r];
+                if (!SAVE) S.Yh[s * LD + col] = ak[r];
                 S.P[s * LD + col] = aq[r];
                 S.R[s * LD + col] = ar[r];
             }
@@ -931,8 +987,10 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             S.QK[idx] = acc;
         }
         __syncthreads();
-        key_rows_t<D, MB, NT>(S, p.eps, warp, lane);
-        __syncthreads();
+        if (!SAVE) {
+            key_rows_t<D, MB, NT>(S, p.eps, warp, lane);
+            __syncthreads();
+        }
         // p_t = W q_t + c - sum_{s<=t} A_ts g_s
         {
             float a[RPT];
@@ -1147,6 +1205,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         if (PF && i > 0) {
             issue_tiles(t0 - MB, true);
             issue_anchor(i - 1);
+            if (SAVE) issue_saved(i - 1);
         }
         {
             float a[RPT];
@@ -1259,7 +1318,9 @@ cudaError_t linear_bwd_noalloc_scratch(void **ptr)
 
 size_t linear_bwd_workspace_bytes(int B, int H, int T, int d, int mb)
 {
-    return (size_t)B * H * (size_t)(T / mb) * ((size_t)d * d + d) * sizeof(float);
+    // per chain: every mini-batch's starting state (W, c), then every token's key side
+    // (yh, e, g and the two row statistics of its mini-batch)
+    return (size_t)B * H * ((size_t)(T / mb) * ((size_t)d * d + d) + (size_t)T * (3 * d + 2)) * sizeof(float);
 }
 
 cudaError_t launch_linear_bwd(const LinearBwdParams &p, int io, int chains, cudaStream_t s)

@@ -164,8 +164,10 @@ def test_validation_codes_mlp(L):
 
 def test_backward_workspace_bytes(L):
     # one (W, c) anchor per mini-batch and chain, fp32
-    assert ttt.linear_backward_workspace_bytes(8, 12, 2048, 64, 16) == 8 * 12 * 128 * (64 * 64 + 64) * 4
-    assert ttt.linear_backward_workspace_bytes(1, 1, 16, 16, 16) == (256 + 16) * 4
+    # one (W, c) starting state per mini-batch and chain, and each token's key side, fp32
+    assert ttt.linear_backward_workspace_bytes(8, 12, 2048, 64, 16) == \
+        8 * 12 * (128 * (64 * 64 + 64) + 2048 * (3 * 64 + 2)) * 4
+    assert ttt.linear_backward_workspace_bytes(1, 1, 16, 16, 16) == (256 + 16 + 16 * (48 + 2)) * 4
     assert ttt.linear_backward_workspace_bytes(1, 1, 30, 16, 16) == 0   # T % mb
     assert ttt.linear_backward_workspace_bytes(0, 1, 16, 16, 16) == 0
 
