@@ -135,10 +135,10 @@ def backward_cost(w):
     b^2 (d + h) (the two Grams) + 5 b(b+1)/2 (d + h); times 2."""
     es = 2 if w.io == "bf16" else 4
     d, b = w.d, w.b
-    per_tok = (2 * d * es) + (4 * d * es) + 2 * 4 + 3 * d * 4 + 4
+    saves = w.variant == "linear" and d == 64 and b == 16  # keeps the key side: no V in the reverse
+    per_tok = (2 * d * es) + ((3 if saves else 4) * d * es) + 2 * 4 + 3 * d * 4 + 4
     if w.variant == "linear":
         state = w.chains * (w.T // b) * (d * d + d) * 4 * 2
-        saves = d == 64 and b == 16  # the kernel that keeps each mini-batch's key side
         if saves:
             state += w.tokens * (3 * d + 2) * 4 * 2
         flops_tok = 2 * ((9 if saves else 10) * d * d + b * d) + 5 * (b + 1) * d

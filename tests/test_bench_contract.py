@@ -43,7 +43,7 @@ def test_cost_models():
     assert nb_key == nbytes - 64 * 2 * w.tokens                     # the key rule reads no queries
     bb, bf = bench.backward_cost(w)
     assert bf == (2 * (9 * 64 * 64 + 16 * 64) + 5 * 17 * 64) * w.tokens    # 81 216 FLOP per token-head
-    assert bb == 1548 * w.tokens + w.chains * (2048 // 16) * (64 * 64 + 64) * 8 + w.tokens * 194 * 8
+    assert bb == 1420 * w.tokens + w.chains * (2048 // 16) * (64 * 64 + 64) * 8 + w.tokens * 194 * 8
     m = WORKLOADS["mlp_b4h12_d64_t8k"]
     _, mf = bench.backward_cost(m)
     assert mf == (2 * (22 * 256 * 64 + 16 * (64 + 256)) + 5 * 17 * (64 + 256)) * m.tokens  # 758 336
