@@ -61,9 +61,17 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: bytes) -> bytes:
+    """The source without its C/C++ comments (so that a comment edit does not
+    mark a measurement stale)."""
+    import re
+    t = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+    return re.sub(rb"//[^\n]*", b"", t)
+
+
 def sources_sha1(files=None) -> str:
-    """sha1 over CUDA sources of the library: the named files of csrc/, or all
-    kernels and headers."""
+    """sha1 over the code (comments removed) of CUDA sources of the library: the
+    named files of csrc/, or all kernels and headers, and include/ttt.h."""
     import glob
     import hashlib
     h = hashlib.sha1()
@@ -74,10 +82,10 @@ def sources_sha1(files=None) -> str:
     for f in paths:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()))
     include = os.path.join(ROOT, "include", "ttt.h")
     with open(include, "rb") as fh:
-        h.update(fh.read())
+        h.update(_code_only(fh.read()))
     return h.hexdigest()
 
 

@@ -33,7 +33,10 @@
 // One CTA per (sequence, head) chain. A forward sweep stores every anchor
 // (W_{i-1}, c_{i-1}) in the caller's workspace (checkpointing every mini-batch:
 // n (d^2 + d) floats per chain); the reverse sweep reloads them from the last
-// batch to the first and recomputes the batch's forward from its anchor.
+// batch to the first and recomputes the batch's forward from its anchor. The
+// tiled kernel at d = 64 also keeps each mini-batch's key side (yh, e, g and the
+// two row statistics, after the checkpoints) and the reverse sweep reads it back
+// instead of recomputing y_s and the key LayerNorm.
 #include <cuda_bf16.h>
 
 #include <mutex>

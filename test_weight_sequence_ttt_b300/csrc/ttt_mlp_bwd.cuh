@@ -27,18 +27,21 @@
 //   dX2 += dY W2,  dZ1 += dX2 * gelu'(Z1),  dK += dZ1 W1
 //   dW1 += dZ1q^T Q + dZ1^T K,  dW2 += dY^T X2,  dc1 += sum(dZ1q + dZ1),  dc2 += sum dY.
 //
-// One CTA of 512 threads per (sequence, head) chain. The mini-batch tiles live in
-// shared memory; the weights do not fit beside them (W1, W2, dW1, dW2 are 256 KB
-// at d = 64, h = 256), so a forward sweep writes every mini-batch's starting
-// state (W1, c1, W2, c2) to the caller's workspace, the reverse sweep reads the
-// anchors from there (they stay in L2), and dW1, dW2 accumulate in the workspace.
+// Two kernels. mlp_bwd_kernel<b> (b in {1, 2, 4, 8}, and 16 where the cluster
+// kernel does not apply): one CTA of 512 threads per (sequence, head) chain. The
+// mini-batch tiles live in shared memory; the weights do not fit beside them
+// (W1, W2, dW1, dW2 are 256 KB at d = 64, h = 256), so a forward sweep writes every
+// mini-batch's starting state (W1, c1, W2, c2) to the caller's workspace, the
+// reverse sweep reads the anchors from there (they stay in L2), and dW1, dW2
+// accumulate in the workspace. W2 and dW2 are kept there transposed, [h][d] like
+// W1, so that every product with a d-wide output reads a weight column coalesced
+// across the lanes and every product with an h-wide output reads one
+// 16-byte-aligned weight row per thread. mlp_bwd_cluster_kernel (b = 16): the same
+// steps with one chain over two CTAs, each holding half of the hidden units' weights
+// in shared memory (see its own comment below).
 //
 // The kernels are instantiated in ttt_mlp_bwd_*.cu (several translation units,
 // so that they compile in parallel) and dispatched from ttt_mlp_bwd.cu.
-// W2 and dW2 are kept there transposed, [h][d] like W1, so that every product
-// with a d-wide output reads a weight column coalesced across the lanes and
-// every product with an h-wide output reads one 16-byte-aligned weight row per
-// thread.
 #pragma once
 
 #include <cooperative_groups.h>
