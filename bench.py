@@ -12,8 +12,11 @@ Prints one JSON line. ``value`` is whole-job throughput (B*T*H tokens per
 second over all ranks) with inputs resident in HBM, timed per step with CUDA
 events on the launching stream and L2 flushed (256 MiB write) between steps.
 ``e2e`` is the same metric through the C ABI with pinned host buffers: the
-host->device copies of the step's inputs and the device->host copy of Z and
-the per-token loss are inside the timed region. ``cpu_baseline`` times the
+host->device copies of the step's inputs and the device->host copies of all
+its outputs (Z, the final state, the per-token losses) are inside the timed
+region, pipelined across steps on
+separate streams (inputs of step k in while step k-1 computes, results of
+step k-1 out while step k computes). ``cpu_baseline`` times the
 fp64 CPU oracle on a bounded sample of the same workload.
 
 ``--impl reference`` runs the reference arm: the fp64 CPU oracle as it stands,
@@ -329,6 +332,56 @@ def _backward_sample_shape(w, seconds: float):
     return int(min(w.chains, max(1, seconds / (dt / Tc * w.T)))), w.T
 
 
+# ---------------------------------------------------------------- end to end
+
+def pipelined_e2e(host_in: dict, dev_like: dict, out_like: dict, run, steps: int, warm: int = 2) -> float:
+    """Seconds per step of ``steps`` end-to-end steps through the public API.
+
+    Every step copies all of its inputs from pinned host memory to the device
+    (``host_in``), runs ``run(dev_in, out, stream)`` and copies all of its
+    results (``out``) back to pinned host memory, inside the timed region. As
+    a user overlapping transfers with compute would, the steps are pipelined
+    on three streams with two sets of buffers: step k's inputs go in while step
+    k-1 computes, and step k-1's results come out while step k computes (PCIe
+    carries both directions at once)."""
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    dev_in = [{k: torch.empty_like(v) for k, v in dev_like.items()} for _ in range(2)]
+    outs = [{k: torch.empty_like(v) for k, v in out_like.items()} for _ in range(2)]
+    host_out = [{k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out_like.items()} for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    torch.cuda.synchronize()
+
+    def step(k):
+        j = k & 1
+        if k >= 2:
+            s_in.wait_event(ev_cmp[j])       # the compute that read dev_in[j] is done
+        with torch.cuda.stream(s_in):
+            for name, t in host_in.items():
+                dev_in[j][name].copy_(t, non_blocking=True)
+        ev_in[j].record(s_in)
+        s_cmp.wait_event(ev_in[j])
+        if k >= 2:
+            s_cmp.wait_event(ev_out[j])      # outs[j] has been read back
+        run(dev_in[j], outs[j], s_cmp)
+        ev_cmp[j].record(s_cmp)
+        s_out.wait_event(ev_cmp[j])
+        with torch.cuda.stream(s_out):
+            for name, t in host_out[j].items():
+                t.copy_(outs[j][name], non_blocking=True)
+        ev_out[j].record(s_out)
+
+    for k in range(warm):
+        step(k)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(steps):
+        step(k)
+    torch.cuda.synchronize()                  # every step's results are on the host
+    return (time.perf_counter() - t0) / steps
+
+
 # ---------------------------------------------------------------- GPU arm
 
 def run_gpu_backward(args):
@@ -396,27 +449,26 @@ def run_gpu_backward(args):
 
     # e2e: inputs and upstream gradients from pinned host memory, every gradient back to the host
     host_in = {k: inp[k].pin_memory() for k in ("Q", "K", "V", eta_key, "dZ") + seeds}
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    d2h = sum(t.numel() * t.element_size() for t in out.values())
     e2e_steps = max(3, min(args.steps, 20))
 
-    def e2e_step():
-        for k, t in host_in.items():
-            dev[k].copy_(t, non_blocking=True)
-        call(out)
-        for k, t in host_out.items():
-            t.copy_(out[k], non_blocking=True)
+    def run_e2e(di, o, strm):
+        x = dict(dev, **di)
+        if w.variant == "linear":
+            ttt.ttt_linear_backward(x["Q"], x["K"], x["V"], x[eta_key], x["W0"], x["c0"], x["ln_g"], x["ln_b"],
+                                    x["dZ"], mb=w.b, dW_n=x["dW_n"], dc_n=x["dc_n"], eps=w.eps, out=o,
+                                    workspace=ws, status=st, stream=strm, eta_gate=args.eta_gate,
+                                    eta_base=w.eta_base)
+        else:
+            ttt.ttt_mlp_backward(*(x[k] for k in ("Q", "K", "V")), x[eta_key],
+                                 *(x[k] for k in ("W1", "c1", "W2", "c2", "ln_g", "ln_b", "dZ")), mb=w.b, eps=w.eps,
+                                 out=o, workspace=ws, status=st, stream=strm, eta_gate=args.eta_gate,
+                                 eta_base=w.eta_base, **{k: x[k] for k in seeds})
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
     shard.barrier(dist)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-        torch.cuda.synchronize()
-    e2e_s = shard.max_over_ranks(dist, (time.perf_counter() - t0) / e2e_steps)
+    e2e_s = pipelined_e2e(host_in, {k: dev[k] for k in host_in}, out, run_e2e, e2e_steps)
+    e2e_s = shard.max_over_ranks(dist, e2e_s)
     tokens = shard.sum_over_ranks(dist, w.tokens)
     if rank != 0:
         return None
@@ -523,28 +575,25 @@ def run_gpu(args):
 
     # ---- e2e: pinned host buffers through the C ABI, copies inside the timed region
     host_in = {k: inp[k].pin_memory() for k in (("K", "V", eta_key) if rule == "key" else ("Q", "K", "V", eta_key))}
-    host_Z = torch.empty(inp["Q"].shape, dtype=zdt).pin_memory()
-    host_L = torch.empty((B, H, T), dtype=torch.float32).pin_memory()
+    res = dict(out)      # every output of the call (Z, final W and c, loss, inner loss) is read back
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_Z.numel() * host_Z.element_size() + host_L.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in res.values())
     e2e_steps = max(3, min(args.steps, 50))
 
-    def e2e_step():
-        for k, t in host_in.items():
-            dev[k].copy_(t, non_blocking=True)
-        call(out)
-        host_Z.copy_(out["Z"], non_blocking=True)
-        host_L.copy_(out["loss"], non_blocking=True)
+    def run_e2e(di, o, strm):
+        x = dict(dev, **di)
+        qx = None if rule == "key" else x["Q"]
+        if w.variant == "linear":
+            ttt.ttt_linear_forward(qx, x["K"], x["V"], x[eta_key], x["W0"], x["c0"], x["ln_g"], x["ln_b"], mb=w.b,
+                                   eps=w.eps, out=o, status=st, stream=strm, out_rule=rule,
+                                   partial_tail=w.partial_tail, eta_gate=args.eta_gate, eta_base=w.eta_base)
+        else:
+            ttt.ttt_mlp_forward(qx, x["K"], x["V"], x[eta_key], x["W1"], x["c1"], x["W2"], x["c2"], x["ln_g"],
+                                x["ln_b"], mb=w.b, eps=w.eps, out=o, status=st, stream=strm, out_rule=rule,
+                                partial_tail=w.partial_tail, eta_gate=args.eta_gate, eta_base=w.eta_base)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
     shard.barrier(dist)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-        torch.cuda.synchronize()          # the result is on the host before the next step
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = pipelined_e2e(host_in, {k: dev[k] for k in host_in}, res, run_e2e, e2e_steps)
     e2e_s = shard.max_over_ranks(dist, e2e_s)
     tokens = shard.sum_over_ranks(dist, w.tokens)  # every rank ran its own full workload (weak scaling)
 
