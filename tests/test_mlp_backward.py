@@ -7,7 +7,9 @@ of the oracle's tensor, the bound of the TTT-Linear backward (fp32 arithmetic
 throughout). Sizes span several mini-batches, b in {1, 4, 16}, widths that are
 not multiples of the warp, bf16 inputs, the learning-rate gate, optional seeds
 and per-sequence initial weights; the benchmark's TTT-MLP workload runs on the
-GPU with one sampled chain checked against the oracle at full length.
+GPU with one sampled chain checked against the oracle at full length. b = 16
+runs the two-CTA cluster kernel where h is a multiple of 8 and the single-CTA
+kernel otherwise; both are covered.
 """
 import numpy as np
 import pytest
@@ -79,6 +81,7 @@ def _compare(got, ref, sel=None):
 @pytest.mark.parametrize("B,H,T,d,h,b,io", [
     (1, 2, 64, 16, 64, 16, "f32"), (1, 2, 64, 64, 256, 16, "f32"), (2, 1, 24, 8, 36, 4, "f32"),
     (1, 1, 12, 12, 20, 1, "f32"), (1, 2, 64, 64, 256, 16, "bf16"), (1, 1, 32, 40, 160, 8, "f32"),
+    (1, 2, 48, 12, 20, 16, "f32"),   # b = 16 with h not a multiple of 8: the single-CTA kernel
 ])
 def test_mlp_backward_matches_oracle(B, H, T, d, h, b, io):
     x = _case(B, H, T, d, h, b, io, seed=B * 100 + T + d + h + b)
