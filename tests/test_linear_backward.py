@@ -83,6 +83,7 @@ def _compare(got, ref, sel=None):
     (2, 2, 48, 64, 1, "f32"), (1, 2, 256, 64, 32, "f32"), (1, 2, 256, 32, 64, "f32"),
     (1, 2, 64, 128, 16, "f32"),
     (2, 2, 128, 64, 16, "bf16"), (1, 1, 16, 8, 16, "f32"),
+    (1, 1, 32, 128, 8, "f32"),       # d = 128 on the general kernel
 ])
 def test_backward_matches_oracle(B, H, T, d, b, io):
     x = _case(B, H, T, d, b, io, seed=B * 1000 + T + d + b)
