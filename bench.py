@@ -140,13 +140,13 @@ def backward_cost(w):
     written once and read once. FLOPs, per
     mini-batch of b tokens, the contractions as executed: TTT-Linear
     10 b d^2 (forward recompute 2, reverse 8; 9 where the reverse sweep reuses
-    the forward sweep's key side, d = 64 and b = 16) + b^2 d (Q K^T) +
+    the forward sweep's key side, d in {64, 128} and b = 16) + b^2 d (Q K^T) +
     5 b(b+1)/2 d (the causal b x b x d products); TTT-MLP 22 b h d (forward recompute 5,
     reverse 17: the reverse sweep reuses the forward sweep's key side) +
     b^2 (d + h) (the two Grams) + 5 b(b+1)/2 (d + h); times 2."""
     es = 2 if w.io == "bf16" else 4
     d, b = w.d, w.b
-    saves = w.variant == "linear" and d == 64 and b == 16  # keeps the key side: no V in the reverse
+    saves = w.variant == "linear" and d in (64, 128) and b == 16  # keeps the key side: no V in the reverse
     per_tok = (2 * d * es) + ((3 if saves else 4) * d * es) + 2 * 4 + 3 * d * 4 + 4
     if w.variant == "linear":
         state = w.chains * (w.T // b) * (d * d + d) * 4 * 2

@@ -34,9 +34,9 @@
 // (W_{i-1}, c_{i-1}) in the caller's workspace (checkpointing every mini-batch:
 // n (d^2 + d) floats per chain); the reverse sweep reloads them from the last
 // batch to the first and recomputes the batch's forward from its anchor. The
-// tiled kernel at d = 64 also keeps each mini-batch's key side (yh, e, g and the
-// two row statistics, after the checkpoints) and the reverse sweep reads it back
-// instead of recomputing y_s and the key LayerNorm.
+// tiled kernel also keeps each mini-batch's key side (yh, e, g and the two row
+// statistics, after the checkpoints) and the reverse sweep reads it back instead
+// of recomputing y_s and the key LayerNorm.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -745,9 +745,12 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
     const IO *Vg = static_cast<const IO *>(p.V) + tok0 * D;
     const IO *DZg = static_cast<const IO *>(p.dZ) + tok0 * D;
     const float *eg = p.eta + tok0;
-    // workspace of the chain: every mini-batch's starting state (W, c), then (d = 64) every
-    // mini-batch's key side (yh, e, g [MB][D] and r, mean(u yh) [MB]) for the reverse sweep
-    constexpr bool SAVE = D == 64 && NT == 256;  // with the register prefetch (PF), which loads it
+    // workspace of the chain: every mini-batch's starting state (W, c), then every
+    // mini-batch's key side (yh, e, g [MB][D] and r, mean(u yh) [MB]) for the reverse sweep.
+    // SAVE goes with the register prefetch (PF, 256 threads); at d = 64 the key side is
+    // prefetched into registers too (PFS), at d = 128 (no registers to spare) it is loaded
+    // at the start of its mini-batch.
+    constexpr bool SAVE = NT == 256, PFS = SAVE && D == 64;
     constexpr size_t SVL = (size_t)MB * (3 * D + 2);
     float *ws = p.ws + (size_t)chain * (n * ((size_t)D * D + D) + (size_t)T * (3 * D + 2));
     float *svb = ws + (size_t)n * ((size_t)D * D + D);
@@ -934,7 +937,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         __syncthreads();  // the forward sweep's last anchor store is visible
         issue_tiles((n - 1) * MB, true);
         issue_anchor(n - 1);
-        if (SAVE) issue_saved(n - 1);
+        if (PFS) issue_saved(n - 1);
     }
     for (int i = n - 1; i >= 0; --i) {
         const int t0 = i * MB;
@@ -942,7 +945,21 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         if (PF) {
             commit_tiles(true);
             commit_anchor();
-            if (SAVE) commit_saved();
+            if (PFS) {
+                commit_saved();
+            } else if (SAVE) {
+                const float *sv = svb + (size_t)i * SVL;
+                for (int q = tid; q < MB * D / 4; q += NT) {
+                    const int s = (4 * q) / D, ii = (4 * q) % D;
+                    st4(S.Yh + s * LD + ii, ld4(sv + 4 * q));
+                    st4(S.E + s * LD + ii, ld4(sv + MB * D + 4 * q));
+                    st4(S.G + s * LD + ii, ld4(sv + 2 * MB * D + 4 * q));
+                }
+                for (int x = tid; x < MB; x += NT) {
+                    S.rk[x] = sv[3 * MB * D + x];
+                    S.m2k[x] = sv[3 * MB * D + MB + x];
+                }
+            }
         } else {
             const float *wsi = ws + (size_t)i * ((size_t)D * D + D);
             for (int q = tid; q < D * D / 4; q += NT) {
@@ -1208,7 +1225,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         if (PF && i > 0) {
             issue_tiles(t0 - MB, true);
             issue_anchor(i - 1);
-            if (SAVE) issue_saved(i - 1);
+            if (PFS) issue_saved(i - 1);
         }
         {
             float a[RPT];
