@@ -308,7 +308,10 @@ typedef struct {
 /* Supported: io = TTT_F32 or TTT_BF16, 4 <= d <= 128 and 4 <= hidden with both
  *            multiples of 4, mb in {1, 2, 4, 8, 16}, and
  *            2 hidden + 6 d + 13 mb d + 9 mb hidden + 4 mb^2 + 4 mb floats
- *            <= 227 KB (fp32 FFMA kernel, one CTA of 512 threads per chain). */
+ *            <= 227 KB (fp32 FFMA kernel, one CTA of 512 threads per chain).
+ *            With mb = 16 and hidden a multiple of 8 (and the half-width
+ *            state fitting 227 KB) each chain runs on a cluster of two CTAs
+ *            instead, each holding half of the hidden units' weights. */
 ttt_status ttt_mlp_backward(const ttt_mlp_bwd_args *args, void *stream);
 uint64_t ttt_mlp_backward_workspace_bytes(int32_t B, int32_t H, int32_t T, int32_t d, int32_t hidden,
                                           int32_t mb);
