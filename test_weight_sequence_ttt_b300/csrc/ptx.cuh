@@ -16,6 +16,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory base rounded up to 1024 bytes (what the 128-byte
+// swizzle of the TMA tiles needs). The offset is added to the shared-memory
+// pointer itself, not to an integer copy of it, so the compiler still knows
+// every access through the result is to shared memory and emits shared-memory
+// loads and stores instead of generic ones.
+__device__ __forceinline__ uint8_t *smem_align1024(uint8_t *base)
+{
+    return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
