@@ -72,7 +72,8 @@ typedef enum {
                                  /* without partial_tail                            */
     TTT_ERR_UNSUPPORTED = 3,     /* no kernel for (io, d, mb, hidden), or bad rule   */
     TTT_ERR_ALIGN = 4,           /* a pointer is not 16-byte aligned                 */
-    TTT_ERR_NOT_DEVICE_PTR = 5,  /* a pointer is not device-accessible memory        */
+    TTT_ERR_NOT_DEVICE_PTR = 5,  /* a pointer is neither device memory of the        */
+                                 /* current device nor managed memory               */
     TTT_ERR_CUDA = 6,            /* a CUDA runtime call or launch failed             */
     TTT_ERR_TIMEOUT = 7,         /* device: a bounded wait gave up, chain abandoned  */
     TTT_ERR_NONFINITE = 8,       /* device: non-finite value in the final state      */
@@ -264,8 +265,11 @@ uint64_t ttt_linear_backward_workspace_bytes(int32_t B, int32_t H, int32_t T, in
  * array, and it keeps the previous call's contents (the kernel overwrites
  * everything it reads), so calls that overlap on the GPU -- on different
  * streams, or from different host threads -- race: issue them in order on one
- * stream. The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture. */
+ * stream. The array belongs to the library's module in the runtime's context
+ * of the current device; every call looks its device address up there
+ * (cudaGetSymbolAddress), so no address outlives a cudaDeviceReset. The first
+ * call on a device, and the first after a cudaDeviceReset, loads the module
+ * into that context: make it before any stream capture. */
 #define TTT_NOALLOC_SCRATCH_BYTES (32u << 20)
 ttt_status ttt_linear_backward_noalloc(const ttt_linear_bwd_args *args, void *stream);
 

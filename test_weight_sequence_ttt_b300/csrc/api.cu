@@ -22,6 +22,9 @@ bool overlap(const Range &a, const Range &b) { return a.lo < b.hi && b.lo < a.hi
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device memory of the current device (the one the kernels launch on), or
+// managed memory. Memory of another GPU is refused: a kernel of this device
+// would otherwise touch it through peer mappings, or fault where none exist.
 bool is_device_ptr(const void *p)
 {
     cudaPointerAttributes at;
@@ -29,7 +32,14 @@ bool is_device_ptr(const void *p)
         (void)cudaGetLastError();  // clear the sticky-free error of a failed query
         return false;
     }
-    return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+    if (at.type == cudaMemoryTypeManaged) return true;
+    if (at.type != cudaMemoryTypeDevice) return false;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return at.device == dev;
 }
 
 // Bytes spanned by an initial-weight array [B|1][H][per] with a batch stride.

@@ -39,7 +39,6 @@
 // of recomputing y_s and the key LayerNorm.
 #include <cuda_bf16.h>
 
-#include <mutex>
 
 #include "ttt_internal.h"
 
@@ -1317,22 +1316,14 @@ bool linear_bwd_supported(int io, int d, int mb)
 cudaError_t linear_bwd_noalloc_scratch(void **ptr)
 {
     // In host code g_noalloc_scratch names a host-side stand-in, not device
-    // memory: the device address comes from the runtime, once per device (with
-    // that device current), and is kept for later calls.
-    static std::mutex mu;
-    static void *addr[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    // memory. The runtime gives its device address in the current device's
+    // context; it is looked up on every call (a cheap table lookup) rather than
+    // cached, so a context that was torn down and made again (cudaDeviceReset)
+    // or another context on the same device never sees a stale address.
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        addr[dev] = p;
-    }
-    *ptr = addr[dev];
+    *ptr = p;
     return cudaSuccess;
 }
 

@@ -25,7 +25,7 @@ def test_reference_arm_line():
         assert k in j, k
     assert j["impl"] == "reference" and j["value"] > 0 and j["unit"] == "tokens/s"
     assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
-    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["config"]["workload"] == "linear_b8h12_d64_t2k"
+    assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["config"]["workload"] == bench.DEFAULT_WORKLOAD
 
 
 def test_reference_arm_backward_line():
@@ -48,3 +48,20 @@ def test_cost_models():
     _, mf = bench.backward_cost(m)
     assert mf == (2 * (22 * 256 * 64 + 16 * (64 + 256)) + 5 * 17 * (64 + 256)) * m.tokens  # 758 336
     assert abs(bench.FP32_PEAK_TFLOPS - 148 * 128 * 2 * 2.032e-3) < 1e-9   # TFLOP/s
+
+
+def test_two_ranks_host_only():
+    """``--gpus 2`` without a torchrun environment starts the two ranks itself;
+    rank 0 alone prints one line, for the whole job, and the ranks' chains are
+    disjoint blocks that cover the job."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--host-only",
+                          "--steps", "2", "--warmup", "3", "--workload", "linear_b8h12_d64_t2k"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    j = json.loads(lines[0])
+    assert j["n_gpus"] == 2 and j["scaling"] == "weak" and j["value"] > 0
+    spans = j["config"]["rank_chains"]
+    n = WORKLOADS["linear_b8h12_d64_t2k"].chains
+    assert spans == [[0, n], [n, 2 * n]]

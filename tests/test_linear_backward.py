@@ -25,7 +25,7 @@ from _util import rel_err, to_np
 
 pytestmark = pytest.mark.gpu
 
-TOL_BWD = 1e-3
+TOL_BWD = 1e-4
 KEYS = ["dQ", "dK", "dV", "deta", "dW0", "dc0", "dln_g", "dln_b"]
 
 

@@ -185,8 +185,14 @@ def test_resume_two_calls():
     bb["c0"] = ra["c"].cpu()
     rb = run_linear(bb)
     z = torch.cat([ra["Z"], rb["Z"]], 2)
-    assert rel_err(to_np(z), to_np(full["Z"])) < 1e-2
-    assert rel_err(to_np(rb["W"]), to_np(full["W"])) < 1e-2
+    ez, ew = rel_err(to_np(z), to_np(full["Z"])), rel_err(to_np(rb["W"]), to_np(full["W"]))
+    print("resume gap: Z %.3e W %.3e" % (ez, ew))
+    # Equal in exact arithmetic. The second call starts its look-ahead afresh
+    # (Y = W K^T + c instead of S + the carried correction) and takes its
+    # LayerNorm shift from the resumed W's feature mean, so the two differ by
+    # one rounding of the fp16 operands (2^-11 relative), carried through a few
+    # mini-batches: measured 5.9e-4 on Z and 1.2e-5 on W.
+    assert ez < 2e-3 and ew < 1e-4
 
 
 def test_outputs_fully_written_and_optional_outputs():
@@ -223,3 +229,19 @@ def test_host_pointer_rejected():
         ttt.ttt_linear_forward(d["Q"], d["K"], d["V"], d["eta"], d["W0"], d["c0"], d["ln_g"], d["ln_b"],
                                mb=16, out={"Z": torch.empty(inp["Q"].shape).pin_memory()})
     assert e.value.code in (5,)
+
+
+@pytest.mark.skipif(torch.cuda.device_count() < 2, reason="needs a second GPU to hold the foreign buffer")
+def test_other_device_pointer_rejected():
+    # every buffer on GPU 1 while GPU 0 is current: refused before any launch,
+    # so the preset output stays as it was
+    inp = _small(64, 16, 32, B=1, H=1)
+    d = {k: (v.to("cuda:1") if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    z = torch.full(inp["Q"].shape, 7.0, device="cuda:1")
+    with torch.cuda.device(0):
+        with pytest.raises(ttt.TTTError) as e:
+            ttt.ttt_linear_forward(d["Q"], d["K"], d["V"], d["eta"], d["W0"], d["c0"], d["ln_g"], d["ln_b"],
+                                   mb=16, out={"Z": z}, stream=torch.cuda.current_stream(0))
+    assert e.value.code == 5
+    torch.cuda.synchronize(1)
+    assert bool((z == 7.0).all())

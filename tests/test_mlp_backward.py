@@ -4,7 +4,11 @@ differences).
 
 Each gradient tensor is compared element by element: max |err| <= TOL_BWD * RMS
 of the oracle's tensor, the bound of the TTT-Linear backward (fp32 arithmetic
-throughout). Sizes span several mini-batches, b in {1, 4, 16}, widths that are
+throughout). The full-length chain (T = 8192: 512 mini-batches whose adjoints
+the reverse sweep accumulates one after the other through the two layers and
+the GELU's second derivative) is held to TOL_BWD_FULL instead: there the fp32
+rounding of the long reverse accumulation reaches about 3e-4 on dK, dV and
+deta (measured), while every shorter case stays under 1e-4. Sizes span several mini-batches, b in {1, 4, 16}, widths that are
 not multiples of the warp, bf16 inputs, the learning-rate gate, optional seeds
 and per-sequence initial weights; the benchmark's TTT-MLP workload runs on the
 GPU with one sampled chain checked against the oracle at full length. b = 16
@@ -23,7 +27,8 @@ from _util import rel_err, to_np
 
 pytestmark = pytest.mark.gpu
 
-TOL_BWD = 1e-3
+TOL_BWD = 1e-4
+TOL_BWD_FULL = 1e-3
 KEYS = ["dQ", "dK", "dV", "deta", "dW1", "dc1", "dW2", "dc2", "dln_g", "dln_b"]
 INS = ["Q", "K", "V", "eta", "W1", "c1", "W2", "c2", "ln_g", "ln_b"]
 SEEDS = ["dW1_n", "dc1_n", "dW2_n", "dc2_n"]
@@ -66,15 +71,16 @@ def _oracle(x, *, gate=False, eta_base=1.0, seeds=True):
                       eta_gate=gate, eta_base=eta_base)
 
 
-def _compare(got, ref, sel=None):
+def _compare(got, ref, sel=None, tol=TOL_BWD):
     errs = {}
     for k in KEYS:
         g = to_np(got[k])
         if sel is not None:
             g = g[sel]
         errs[k] = rel_err(g.reshape(ref[k].shape), ref[k])
-    bad = {k: e for k, e in errs.items() if not e <= TOL_BWD}
-    assert not bad, "max|err|/RMS above %.0e: %s (all: %s)" % (TOL_BWD, bad, errs)
+    print(errs)
+    bad = {k: e for k, e in errs.items() if not e <= tol}
+    assert not bad, "max|err|/RMS above %.0e: %s (all: %s)" % (tol, bad, errs)
     return errs
 
 
@@ -115,4 +121,4 @@ def test_mlp_backward_full_workload_sampled_chain():
     ref = oracle_bwd(*(to_np(si[k]) for k in INS), to_np(sc["dZ"]), *(to_np(sc[k]) for k in SEEDS), b=w.b,
                      eps=w.eps)
     bi, hi = divmod(ch, w.H)
-    _compare(got, ref, sel=(slice(bi, bi + 1), slice(hi, hi + 1)))
+    _compare(got, ref, sel=(slice(bi, bi + 1), slice(hi, hi + 1)), tol=TOL_BWD_FULL)

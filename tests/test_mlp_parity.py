@@ -51,6 +51,8 @@ def test_mlp_full_size_sampled_chains():
     errs = {k: rel_err(to_np(got[k])[idx], ref[k].reshape(to_np(got[k])[idx].shape)) for k in KEYS}
     print(errs)
     assert errs["Z"] <= TOL["bf16"], errs
+    for k in KEYS:
+        assert errs[k] <= 5 * TOL["bf16"], errs
 
 
 # ---------------------------------------------------------------- tensor-core MLP kernel (d=64, h=256, b=16)
