@@ -6,7 +6,18 @@
 A step is one call of the library over the whole workload (every chain, every
 token): the full TTT inner loop -- loads, key forward, LayerNorm
 forward/backward, in-batch mixing, output, weight update, final state.
-Default workload: TTT-Linear, 8 sequences x 12 heads, d=64, T=2048, b=16.
+Default workload: the long-context TTT-Linear prefill scan, 1 sequence x 32
+heads, d=64, T=131072, b=16 (2.16 GB of Q/K/V/eta/Z per call: the largest of
+the workloads that fit one GPU).
+
+``--gpus N`` runs one process per GPU. Without a torchrun environment the
+script starts the N processes itself (torch.distributed.run, 127.0.0.1). Every
+chain is independent, so the scaling is weak: each rank runs its own seeded
+workload of the same shape (its chains are distinct units of one job of N
+times the chains), with no collective on the data path; rank 0 prints the
+whole-job tokens/s over the slowest rank's time. ``--host-only`` replaces the
+GPU step by the CPU oracle on a small slice of each rank's chains (gloo), for
+testing this multi-process logic on a machine without GPUs.
 
 Prints one JSON line. ``value`` is whole-job throughput (B*T*H tokens per
 second over all ranks) with inputs resident in HBM, timed per step with CUDA
@@ -49,7 +60,7 @@ if ROOT not in sys.path:
 
 from test_weight_sequence_ttt_b300.inputs import WORKLOADS, make_cotangents, make_inputs  # noqa: E402
 
-DEFAULT_WORKLOAD = "linear_b8h12_d64_t2k"
+DEFAULT_WORKLOAD = "linear_b1h32_d64_t128k"
 L2_FLUSH_BYTES = 256 << 20
 CSRC = os.path.join(ROOT, "test_weight_sequence_ttt_b300", "csrc")
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
@@ -163,59 +174,119 @@ def backward_cost(w):
 
 # ---------------------------------------------------------------- clocks (NVML, during the timed region)
 
+class _NvmlCtypes:
+    """The few NVML queries the sampler needs, through ctypes on the driver's
+    libnvidia-ml.so.1 (read-only queries; present wherever the driver is)."""
+
+    def __init__(self, bus_id: str):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        rc = self.lib.nvmlInit_v2()
+        if rc != 0:
+            raise RuntimeError("nvmlInit_v2 returned %d" % rc)
+        self.h = ctypes.c_void_p()
+        rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByPciBusId_v2(%s) returned %d" % (bus_id, rc))
+
+    def clock(self, max_clock: bool = False) -> int:
+        v = self.ct.c_uint()
+        fn = self.lib.nvmlDeviceGetMaxClockInfo if max_clock else self.lib.nvmlDeviceGetClockInfo
+        rc = fn(self.h, 1, self.ct.byref(v))  # 1 = NVML_CLOCK_SM
+        if rc != 0:
+            raise RuntimeError("clock query returned %d" % rc)
+        return v.value
+
+    def reasons(self) -> int:
+        v = self.ct.c_ulonglong()
+        rc = self.lib.nvmlDeviceGetCurrentClocksEventReasons(self.h, self.ct.byref(v))
+        if rc != 0:
+            raise RuntimeError("clocks event reasons query returned %d" % rc)
+        return v.value
+
+
 class ClockSampler:
     """Samples SM clock and clock-event (throttle) reasons of this process's GPU
-    while the timed region runs: NVML (matched by PCI bus id) every 10 ms, else
-    ``nvidia-smi -lms 100``."""
+    while the timed region runs: NVML (ctypes on the driver library, else the
+    pynvml module) every 5 ms from a thread, else ``nvidia-smi -lms 50``. The
+    sampler starts before the timed region; ``mark_start``/``mark_end`` bound
+    it, and the summary keeps the samples inside it plus the last one before
+    and the first one after (so a timed region shorter than the sampling period
+    still has samples on both sides)."""
     REASONS = {
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
         0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
         0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
     }
-    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.active"]
+    SMI_FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "clocks_event_reasons.active"]
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
+    def __init__(self, device_index: int, period_s: float = 0.005):
         self.period = period_s
-        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.samples = []            # (time.perf_counter(), sm MHz, reason bits)
+        self.max_mhz = None
+        self.t_start = self.t_end = None
         self._stop = threading.Event()
         self._t = None
         self._proc = None
+        self._q = None
         self.mode, self.error = None, None
         props = torch.cuda.get_device_properties(device_index)
         self.bus_id = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
                                             props.pci_device_id)
+        errs = []
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByPciBusId(self.bus_id.encode())
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self.mode = "nvml"
+            nv = _NvmlCtypes(self.bus_id)
+            self._q = lambda: (nv.clock(), nv.reasons())
+            self.max_mhz = nv.clock(max_clock=True)
+            self.mode = "nvml-ctypes"
         except Exception as e:  # noqa: BLE001
-            self.error = "nvml: %s" % e
+            errs.append("nvml ctypes: %s" % e)
+        if self.mode is None:
+            try:
+                import pynvml
+                pynvml.nvmlInit()
+                h = pynvml.nvmlDeviceGetHandleByPciBusId(self.bus_id.encode())
+                self._q = lambda: (pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM),
+                                   pynvml.nvmlDeviceGetCurrentClocksEventReasons(h))
+                self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+                self.mode = "pynvml"
+            except Exception as e:  # noqa: BLE001
+                errs.append("pynvml: %s" % e)
+        if self.mode is None:
             self.mode = "smi"
+        self.error = "; ".join(errs) or None
 
     def _run_nvml(self):
-        nv = self._nv
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                self.reasons |= nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                mhz, bits = self._q()
+                self.samples.append((time.perf_counter(), float(mhz), int(bits)))
             except Exception as e:  # noqa: BLE001
                 self.error = "nvml sample: %s" % e
             time.sleep(self.period)
 
+    def mark_start(self):
+        self.t_start = time.perf_counter()
+
+    def mark_end(self):
+        self.t_end = time.perf_counter()
+        if self.mode != "smi":
+            time.sleep(3 * self.period)   # one sample after the region
+
     def __enter__(self):
-        if self.mode == "nvml":
+        if self.mode != "smi":
             self._t = threading.Thread(target=self._run_nvml, daemon=True)
             self._t.start()
+            time.sleep(3 * self.period)   # one sample before the region
         else:
             import subprocess
             try:
                 self._proc = subprocess.Popen(
-                    ["nvidia-smi", "--id=" + self.bus_id, "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                    ["nvidia-smi", "--id=" + self.bus_id, "--query-gpu=" + ",".join(self.SMI_FIELDS[1:]),
                      "--format=csv,noheader,nounits", "-lms", "50"],
                     stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+                time.sleep(0.3)           # nvidia-smi takes a moment to print its first line
             except Exception as e:  # noqa: BLE001
                 self.error = (self.error or "") + "; smi: %s" % e
         return self
@@ -225,26 +296,39 @@ class ClockSampler:
         if self._t:
             self._t.join()
         if self._proc:
+            time.sleep(0.1)
             self._proc.terminate()
             out, err = self._proc.communicate(timeout=10)
+            # nvidia-smi lines carry no host timestamp: keep them all (they span the region)
             for line in out.splitlines():
                 f = [x.strip() for x in line.split(",")]
                 try:
-                    self.samples.append(float(f[0]))
+                    self.samples.append((None, float(f[0]), int(f[2], 16)))
                     self.max_mhz = float(f[1])
-                    self.reasons |= int(f[2], 16)
                 except (ValueError, IndexError):
                     continue
             if not self.samples and err:
                 self.error = (self.error or "") + "; smi: %s" % err.strip()[:200]
 
+    def _window(self):
+        if self.t_start is None or self.t_end is None or any(t is None for t, _, _ in self.samples):
+            return list(self.samples)
+        inside = [x for x in self.samples if self.t_start <= x[0] <= self.t_end]
+        before = [x for x in self.samples if x[0] < self.t_start][-1:]
+        after = [x for x in self.samples if x[0] > self.t_end][:1]
+        return before + inside + after
+
     def summary(self):
-        if not self.samples:
+        win = self._window()
+        if not win:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"], "samples": 0,
                     "error": self.error}
-        rs = [n for bit, n in sorted(self.REASONS.items()) if self.reasons & bit]
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": rs,
-                "samples": len(self.samples), "source": self.mode}
+        bits = 0
+        for _, _, b in win:
+            bits |= b
+        rs = [n for bit, n in sorted(self.REASONS.items()) if bits & bit]
+        return {"sm_mhz": statistics.median(m for _, m, _ in win), "sm_max_mhz": self.max_mhz, "reasons": rs,
+                "samples": len(win), "source": self.mode}
 
 
 # ---------------------------------------------------------------- oracle timing
@@ -407,6 +491,7 @@ def run_gpu_backward(args):
     w = WORKLOADS[args.workload]
     if w.partial_tail or w.T % w.b:
         raise SystemExit("--backward needs a workload with T a multiple of mb")
+    rank_chains = _rank_chains(dist, rank, world, w)
     wr = w.with_(seed=w.seed + 7919 * rank)
     inp = dict(make_inputs(wr), **make_cotangents(wr))
     eta_key = "eta_logit" if args.eta_gate else "eta"
@@ -442,15 +527,17 @@ def run_gpu_backward(args):
     sampler = ClockSampler(torch.cuda.current_device())
     shard.barrier(dist)
     torch.cuda.synchronize()
-    wall0 = time.perf_counter()
     with sampler:
+        sampler.mark_start()
+        wall0 = time.perf_counter()
         for e0, e1 in evs:
             flush.fill_(1.0)
             e0.record(stream)
             call(out)
             e1.record(stream)
         torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
+        wall = time.perf_counter() - wall0
+        sampler.mark_end()
     shard.barrier(dist)
     times_ms = [a.elapsed_time(b) for a, b in evs]
     ms = statistics.mean(times_ms)
@@ -497,7 +584,7 @@ def run_gpu_backward(args):
                    "H": w.H, "T": w.T, "d": w.d, "mb": w.b, "hidden": w.hidden or None, "io": w.io,
                    "eta_gate": args.eta_gate,
                    "workspace_bytes": ws.numel(), "l2": "flushed between steps (256 MiB write)",
-                   "parallelism": "dp%d" % world},
+                   "parallelism": "dp%d" % world, "rank_chains": rank_chains},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                      "frac": achieved / FP32_PEAK_TFLOPS,
                      "traffic": measured_traffic(w.name, "", key="%s/backward" % w.name),
@@ -529,6 +616,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     w = WORKLOADS[args.workload]
     # weak scaling: every rank runs its own full workload (independent chains)
+    rank_chains = _rank_chains(dist, rank, world, w)
     inp = make_inputs(w.with_(seed=w.seed + 7919 * rank))
     dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     stream = torch.cuda.current_stream()
@@ -568,15 +656,17 @@ def run_gpu(args):
     sampler = ClockSampler(torch.cuda.current_device())
     shard.barrier(dist)
     torch.cuda.synchronize()
-    wall0 = time.perf_counter()
     with sampler:
+        sampler.mark_start()
+        wall0 = time.perf_counter()
         for e0, e1 in evs:
-            flush.fill_(1.0)              # evict L2 (inputs are < 126 MB L2) -- outside the events
+            flush.fill_(1.0)              # evict L2 (some workloads are smaller than it) -- outside the events
             e0.record(stream)
             call(out)
             e1.record(stream)
         torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
+        wall = time.perf_counter() - wall0
+        sampler.mark_end()
     shard.barrier(dist)
     times_ms = [a.elapsed_time(b) for a, b in evs]
     ms = statistics.mean(times_ms)
@@ -636,7 +726,8 @@ def run_gpu(args):
         "config": {"workload": w.name, "variant": "ttt-" + w.variant, "B": w.B, "H": w.H, "T": w.T, "d": w.d,
                    "mb": w.b, "hidden": w.hidden or None, "io": w.io, "z_dtype": args.z_dtype,
                    "out_rule": rule, "partial_tail": w.partial_tail, "eta_gate": args.eta_gate, "kernel_kind": kind,
-                   "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world},
+                   "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world,
+                   "rank_chains": rank_chains},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak,
                      "traffic": measured_traffic(w.name, args.z_dtype) if rule == "prefix" else None,
@@ -653,20 +744,86 @@ def run_gpu(args):
     if world == 1 and not args.no_cpu_baseline:
         threads = __import__("oracle").max_threads()
         calib = {}
-        chains, Ts = _sample_shape(w, args.cpu_budget_s, threads, calib)
-        dt, toks, th = oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule)
+        chains, Ts = _sample_shape(w, args.cpu_budget_s / 4, threads, calib)
+        oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule)       # warm-up call
+        runs = [oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule) for _ in range(3)]
+        dt = statistics.median(r[0] for r in runs)
+        toks, th = runs[0][1], runs[0][2]
         line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
-                                "sample": "%d of %d chains x %d tokens (fp64 primal token loop, C, OpenMP)"
-                                          % (chains, w.chains, Ts),
+                                "sample": "%d of %d chains x %d tokens (fp64 primal token loop, C, OpenMP); "
+                                          "median of 3 calls after one warm-up call" % (chains, w.chains, Ts),
                                 "seconds": dt, "cpu_count": os.cpu_count(), "model": cpu_model(), **calib}
     return line
+
+
+def _rank_chains(dist, rank: int, world: int, w):
+    """Every rank's [start, stop) range of the job's chains. The job is ``world``
+    workloads of ``w``'s shape (weak scaling); rank r owns the r-th block of
+    w.chains chains, drawn from its own seed."""
+    mine = list(shard_slice(rank, world, world * w.chains))
+    if dist is None:
+        return [mine]
+    got = [None] * world
+    dist.all_gather_object(got, mine)
+    return got
+
+
+def shard_slice(rank, world, n):
+    from test_weight_sequence_ttt_b300 import shard
+    return shard.chain_slice(rank, world, n)
+
+
+def run_host_only(args):
+    """The multi-process logic of the GPU arm on CPU (gloo): each rank's step is
+    the fp64 oracle on a small slice of its own chains; barrier, max over ranks
+    of the step time, sum of tokens, rank 0 prints the line."""
+    from test_weight_sequence_ttt_b300 import shard
+    dist = shard.init("gloo")
+    rank, world = shard.world()
+    w = WORKLOADS[args.workload]
+    rank_chains = _rank_chains(dist, rank, world, w)
+    wr = w.with_(seed=w.seed + 7919 * rank)
+    n, Ts = min(2, w.chains), min(w.T, 2 * w.b)
+    for _ in range(args.warmup):
+        oracle_sample(wr, n, Ts, nthreads=1)
+    shard.barrier(dist)
+    secs = 0.0
+    for _ in range(args.steps):
+        dt, toks, _ = oracle_sample(wr, n, Ts, nthreads=1)
+        secs += dt
+    shard.barrier(dist)
+    ms_max = shard.max_over_ranks(dist, 1e3 * secs / args.steps)
+    tokens = shard.sum_over_ranks(dist, n * Ts)
+    if rank != 0:
+        return None
+    return {"impl": "host-only", "metric": "TTT inner-loop tokens/sec (B·T·H/s) and % of roofline on 1 B300",
+            "value": tokens / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded generator)",
+            "config": {"workload": w.name, "parallelism": "dp%d" % world, "rank_chains": rank_chains,
+                       "sample": "%d chains x %d tokens per rank and step (CPU oracle stands in for the GPU)"
+                                 % (n, Ts)}}
+
+
+def _launch_ranks(args, argv):
+    """Start ``args.gpus`` ranks of this script under torch.distributed.run
+    (one process per GPU, rendezvous on 127.0.0.1) and return their exit code."""
+    import socket
+    import subprocess
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", str(args.gpus),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd, cwd=ROOT)
 
 
 # ---------------------------------------------------------------- reference arm: the oracle
 
 def run_reference_backward(args):
     w = WORKLOADS[args.workload]
-    per_step = max(0.01, args.ref_budget_s / max(1, args.steps + args.warmup))
+    per_step = max(0.2, args.ref_budget_s / max(1, args.steps + args.warmup))
     chains, Ts = _backward_sample_shape(w, per_step)
     for _ in range(args.warmup):
         oracle_backward_sample(w, chains, Ts)
@@ -700,7 +857,9 @@ def run_reference(args):
     import oracle
     w = WORKLOADS[args.workload]
     threads = oracle.max_threads()
-    per_step_wall = max(0.005, args.ref_budget_s / max(1, args.steps + args.warmup))
+    # at least 0.05 s of oracle work per step, so fixed per-call costs (thread
+    # start, state set-up) stay small next to it
+    per_step_wall = max(0.05, args.ref_budget_s / max(1, args.steps + args.warmup))
     chains, Ts = _sample_shape(w, per_step_wall * threads, threads)
     for _ in range(args.warmup):
         oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule)
@@ -728,7 +887,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -745,11 +904,21 @@ def main(argv=None):
                          "for profiling; the line's config says so)")
     ap.add_argument("--backward", action="store_true",
                     help="time ttt_linear_backward (gradients through the inner loop) instead of the forward")
+    ap.add_argument("--host-only", action="store_true",
+                    help="run the multi-rank logic on CPU (gloo) with the oracle standing in for the GPU step")
     ap.add_argument("--out-rule", default="prefix", choices=["prefix", "anchor", "key"],
                     help="output rule: z_t = f(q_t; W_t) (prefix), f(q_t; W_{i-1}) (anchor), f(k_t; W_{i-1}) (key)")
-    args = ap.parse_args(argv)
+    raw = list(sys.argv[1:] if argv is None else argv)
+    args = ap.parse_args(raw)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" in os.environ:
+        if int(os.environ["WORLD_SIZE"]) != args.gpus:
+            ap.error("--gpus %d but WORLD_SIZE=%s" % (args.gpus, os.environ["WORLD_SIZE"]))
+    elif args.gpus > 1:
+        raise SystemExit(_launch_ranks(args, raw))
     if args.T:
         name = "%s_T%d" % (args.workload, args.T)
         WORKLOADS[name] = WORKLOADS[args.workload].with_(name=name, T=args.T)
@@ -758,6 +927,8 @@ def main(argv=None):
         ap.error("--backward supports the prefix output rule only")
     if args.impl == "reference":
         line = run_reference(args)
+    elif args.host_only:
+        line = run_host_only(args)
     else:
         line = run_gpu_backward(args) if args.backward else run_gpu(args)
     if line is not None:
