@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define TTT_ABI_VERSION 7
+#define TTT_ABI_VERSION 8
 
 typedef enum {
     TTT_OK = 0,
@@ -329,6 +329,23 @@ int ttt_abi_version(void);                     /* == TTT_ABI_VERSION        */
  * 1 = fp32 FFMA kernel, 2 = tensor-core kernel. No CUDA call is made. */
 int ttt_linear_kernel_kind(int32_t io, int32_t d, int32_t mb);
 int ttt_mlp_kernel_kind(int32_t io, int32_t d, int32_t hidden, int32_t mb);
+
+/* Form of the tensor-core TTT-Linear kernel for d = 64, mb = 16 (kind 2).
+ * A chain's mini-batch steps are serial ("End-to-End Test-Time Training for
+ * Long Context" review, section 2.3, Eq. 5: each step starts from the weights
+ * the previous one left), so with few (sequence, head) chains most SMs would
+ * idle. The cluster form runs each chain on a cluster of two CTAs (two SMs)
+ * that split the work by role: one SM runs the serial chain and the weight
+ * update W_i = W_{i-1} - (1/b) G_i^T diag(eta) K_i, the other keeps a copy of
+ * the fast weights in step (each step's update matrix -(eta/b) G_i^T crosses
+ * over in distributed shared memory) and computes the outputs z_t. Results
+ * agree with the one-CTA form's to rounding (the chain adds its LayerNorm sums
+ * in another order). On a B300 the one-CTA form measured faster at every chain
+ * count, so it is the default.
+ *   mode 0: never (default); 1: when 2 * B * H <= the device's SM count;
+ *   2: always. Process-wide, for later calls; any other value only returns the
+ *   current mode. */
+int32_t ttt_linear_cluster_mode(int32_t mode);
 
 /* Failure-detection testing hook. In the library built with fault hooks
  * (libttt_b300_faults.so; never the product library) it makes the loader of

@@ -19,7 +19,7 @@ from typing import Optional
 __all__ = [
     "TTTError", "lib", "lib_path", "ttt_linear_forward", "ttt_mlp_forward", "ttt_linear_backward",
     "linear_backward_workspace_bytes", "ttt_mlp_backward", "mlp_backward_workspace_bytes", "MlpBwdArgs",
-    "status_string", "abi_version", "linear_kernel_kind",
+    "status_string", "abi_version", "linear_kernel_kind", "linear_cluster_mode",
     "mlp_kernel_kind", "LinearArgs", "MlpArgs", "LinearBwdArgs", "STATUS", "F32", "BF16", "OUT_RULES",
 ]
 
@@ -138,6 +138,8 @@ def lib() -> ctypes.CDLL:
             L.ttt_status_string.restype = ctypes.c_char_p
             L.ttt_status_string.argtypes = [ctypes.c_int]
             L.ttt_abi_version.restype = ctypes.c_int
+            L.ttt_linear_cluster_mode.restype = ctypes.c_int32
+            L.ttt_linear_cluster_mode.argtypes = [ctypes.c_int32]
             L.ttt_abi_version.argtypes = []
             L.ttt_linear_kernel_kind.restype = ctypes.c_int
             L.ttt_linear_kernel_kind.argtypes = [ctypes.c_int32] * 3
@@ -163,6 +165,14 @@ def status_string(code: int) -> str:
 
 def abi_version() -> int:
     return lib().ttt_abi_version()
+
+
+def linear_cluster_mode(mode: int = -1) -> int:
+    """Set (0 never, the default; 1 when 2 * B * H <= SMs; 2 always) and
+    return the form of the d = 64,
+    mb = 16 TTT-Linear kernel that runs each chain on a two-CTA cluster; any
+    other value only reads the current mode (see include/ttt.h)."""
+    return int(lib().ttt_linear_cluster_mode(int(mode)))
 
 
 def linear_kernel_kind(io: int, d: int, mb: int) -> int:

@@ -42,6 +42,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     }
 }
 
+// wait_bar for phases completed from another CTA of the cluster.
+__device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity, volatile int *flags)
+{
+    if (mbar_try_wait_cluster(bar, parity, 0)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity, kSleepHintNs)) return true;
+        if (flags[0]) return false;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 __device__ __forceinline__ void abort_chain(volatile int *flags, int *status)
 {
     flags[0] = 1;

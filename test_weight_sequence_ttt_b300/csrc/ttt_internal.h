@@ -149,5 +149,8 @@ cudaError_t launch_mlp_bwd(const MlpBwdParams &p, int io, int chains, cudaStream
 bool linear_tc_supported(int io, int d, int mb);
 // Returns cudaSuccess or the failing error; tensor maps are built inside.
 cudaError_t launch_linear_tc(const LinearParams &p, int chains, cudaStream_t s);
+// When d = 64, b = 16 runs as one chain per two-CTA cluster: 0 never, 1 when
+// 2 * chains <= SMs (default), 2 always. A mode outside 0..2 only reads it.
+int linear_cluster_mode(int mode);
 
 }  // namespace ttt

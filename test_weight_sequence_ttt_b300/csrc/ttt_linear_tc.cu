@@ -57,6 +57,8 @@
 // Precision. MMA operands are fp16 (10-bit mantissa) with fp32 accumulation;
 // W, c, LayerNorm statistics and gradients stay fp32. Inputs and W must stay
 // inside the fp16 range (|x| < 65504); an input outside it sets TTT_ERR_RANGE.
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -108,11 +110,14 @@ struct Cfg {
     static constexpr int kOffAR = kOffCst + 3 * D * 4;            // 2 slots x [MT][32 lanes] A~ fragments
     static constexpr int SRS = 20;                                // row stride (floats) of an S block [16 t][16 f]
     static constexpr int kOffSR = kOffAR + 2 * MT * 512;          // 2 slots x [MT][16][SRS] S blocks
-    static constexpr int kOffBar = kOffSR + 2 * MT * 16 * SRS * 4;
+    // cluster kernel: ring of A~ blocks the chain CTA sends to the output CTA
+    static constexpr int kNA = 4;                                 // ring slots
+    static constexpr int kOffAR1 = kOffSR + 2 * MT * 16 * SRS * 4;  // kNA slots x [MT][32 lanes] uint4
+    static constexpr int kOffBar = kOffAR1 + kNA * MT * 512;
     static constexpr int kSplitWarpC = 2, kSplitWarpT = 2 + MT, kSplitWarpO = 2 + 2 * MT;
     static constexpr int kSplitWarps = kSplitWarpO + NO;
     static constexpr int kSplitThreads = kSplitWarps * 32;
-    static constexpr int kNumBars = 3 * kStages + 6;
+    static constexpr int kNumBars = 3 * kStages + 6 + 2 * kNA;  // + afull[kNA], aempty[kNA] (cluster kernel)
     static constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
     static constexpr int kSmemAlloc = kSmem + 1024;                // slack for alignment
     static_assert(FPL % 4 == 0, "output lanes hold whole 4-feature chunks");
@@ -124,8 +129,11 @@ struct Cfg {
 //   empty[s]  every consumer is done with stage s              (P, W, O -> L)
 //   yfull/yempty[2]  Yq^T hand-off                            (W <-> O)
 //   red[2]    the W warps' partial LayerNorm sums of one round (W -> W)
+//   afull[k]  A~ of a step landed in ring slot k (cluster kernel, output CTA)
+//   aempty[k] the output CTA is done with slot k     (cluster kernel, chain CTA)
 struct Ring {
     uint64_t *full, *prep, *empty, *yfull, *yempty, *red;
+    uint64_t *afull, *aempty;
     volatile int *flags;  // [0] abort, [1] fp16 range violation seen
 };
 
@@ -284,15 +292,20 @@ __device__ void token_sums(uint8_t *stg, const uint8_t *sm, float cmean, int lan
 // arrival on prep[j] joins the prep warp's.
 constexpr int kLag = 2;
 
-template <int D>
+// LOADQ: the query tiles are loaded (unless the queries are the keys); SUMS: the
+// per-token scalars of the chain are written (d = 64). The cluster kernel's
+// chain CTA loads no queries, its output CTA forms no per-token scalars.
+template <int D, bool LOADQ = true, bool SUMS = kSumsInLoader<D>>
 __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
                                  const LinearParams &p, uint8_t *sm, const Ring &R, int chain, int bi, int hi, int lane,
                                  int nsteps)
 {
     using C = Cfg<D>;
+    static_assert(!SUMS || kSumsInLoader<D>, "per-token scalars in the loader for d = 64 only");
     const int T = p.T;
     const float *eta = p.eta + (size_t)chain * T;
-    const float cmean = kSumsInLoader<D> ? chain_consts<D>(p, sm, bi, hi, lane) : 0.f;
+    const bool no_q = !LOADQ || p.q_is_k;
+    const float cmean = SUMS ? chain_consts<D>(p, sm, bi, hi, lane) : 0.f;
     uint32_t mag = 0;  // range check of the tiles this warp converts
     if (lane == 0) {
         prefetch_tmap(tmQ);
@@ -317,7 +330,7 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
                 const int t = j * kSS + lane;
                 se[lane] = t < T ? __fdividef(p.eta_base, 1.f + __expf(-se[lane])) : 0.f;
             }
-            if (kSumsInLoader<D>) token_sums<D>(stage_ptr<D>(sm, sj), sm, cmean, lane);
+            if (SUMS) token_sums<D>(stage_ptr<D>(sm, sj), sm, cmean, lane);
             if (kCopiesInLoader<D>) fp16_copies<D>(stage_ptr<D>(sm, sj), p.q_is_k != 0, lane, mag);
             warp_arrive(&R.prep[sj], lane);
         }
@@ -342,11 +355,11 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
             }
             if (!drop) cp_async_mbar_arrive_noinc(&R.full[st]);
             if (!drop && lane == 0) {
-                mbar_arrive_expect_tx(&R.full[st], (p.q_is_k ? 2 : 3) * C::kTile);
+                mbar_arrive_expect_tx(&R.full[st], (no_q ? 2 : 3) * C::kTile);
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {
                     tma_load_3d(stg + C::kOffK + h * 2048, tmK, &R.full[st], h * 64, t0, chain);
-                    if (!p.q_is_k) tma_load_3d(stg + C::kOffQ + h * 2048, tmQ, &R.full[st], h * 64, t0, chain);
+                    if (!no_q) tma_load_3d(stg + C::kOffQ + h * 2048, tmQ, &R.full[st], h * 64, t0, chain);
                     tma_load_3d(stg + C::kOffV + h * 2048, tmV, &R.full[st], h * 64, t0, chain);
                 }
             }
@@ -366,7 +379,12 @@ __device__ void role_loader_sums(const CUtensorMap *tmQ, const CUtensorMap *tmK,
 }
 
 // ------------------------------------------------------------------ P: prep
-template <int D, int SUBB>
+// What the prep warp forms (the one-CTA kernels: all of it; the cluster
+// kernel's chain CTA only the K copy and K_{i-1} K_i^T, its output CTA the K and
+// Q copies and Q K^T).
+constexpr int kPrepQ = 1, kPrepMq = 2, kPrepKx = 4, kPrepAll = 7;
+
+template <int D, int SUBB, int PREP = kPrepAll>
 __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int bi, int hi, int lane, int nsteps)
 {
     using C = Cfg<D>;
@@ -385,7 +403,7 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
         TTT_TRACE_AT(p, i, 12);
         uint8_t *stg = stage_ptr<D>(sm, st);
         // (1) fp16 copies of the K and Q tiles (the loader makes them for d = 128).
-        if (!kCopiesInLoader<D>) fp16_copies<D>(stg, p.q_is_k != 0, lane, mag);
+        if (!kCopiesInLoader<D>) fp16_copies<D>(stg, p.q_is_k != 0 || !(PREP & kPrepQ), lane, mag);
         if (D == 128) TTT_TRACE_AT(p, i, 14);
         if (!kSumsInLoader<D>) token_sums<D>(stg, sm, cmean, lane);
         if (D == 128) TTT_TRACE_AT(p, i, 15);
@@ -403,15 +421,17 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
         const int offK = kBf ? C::kOffK : C::kOffKh, offQ = kBf ? C::offQ(p) : C::offQh(p);
         const uint32_t sK = smem_u32(stg + offK), sQ = smem_u32(stg + offQ);
         const uint32_t sKp = smem_u32(stage_ptr<D>(sm, (i + C::kStages - 1) % C::kStages) + offK);
-        const bool has_prev = i > 0;
+        const bool has_prev = (PREP & kPrepKx) && i > 0;
         float dq[2][4] = {}, dk[2][4] = {}, dx[2][4] = {};
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             uint32_t aq[4], ak[4], bk[4];
-            ldsm_x4(aq, sQ + swz(ra, 2 * ks + (lane >> 4)));
             ldsm_x4(bk, sK + swz(rb, 2 * ks + ((lane >> 3) & 1)));
-            gmma(dq[0], aq, bk[0], bk[1]);
-            gmma(dq[1], aq, bk[2], bk[3]);
+            if (PREP & kPrepMq) {
+                ldsm_x4(aq, sQ + swz(ra, 2 * ks + (lane >> 4)));
+                gmma(dq[0], aq, bk[0], bk[1]);
+                gmma(dq[1], aq, bk[2], bk[3]);
+            }
             if (SUBB < 16 || has_prev) ldsm_x4(ak, sK + swz(ra, 2 * ks + (lane >> 4)));
             if (SUBB < 16) {
                 gmma(dk[0], ak, bk[0], bk[1]);
@@ -433,9 +453,10 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
             const bool seen = prefix ? s <= t : s / SUBB < t / SUBB;
             return seen ? dq[j][r] + 1.f : 0.f;
         };
-        reinterpret_cast<uint4 *>(stg + C::kOffMq)[lane] =
-            make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)),
-                       pack_h2(mq(0, 2), mq(0, 3)), pack_h2(mq(1, 2), mq(1, 3)));
+        if (PREP & kPrepMq)
+            reinterpret_cast<uint4 *>(stg + C::kOffMq)[lane] =
+                make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)),
+                           pack_h2(mq(0, 2), mq(0, 3)), pack_h2(mq(1, 2), mq(1, 3)));
         if (SUBB < 16) {
             const uint32_t k0 = pack_h2(dk[0][0] + 1.f, dk[0][1] + 1.f), k1 = pack_h2(dk[1][0] + 1.f, dk[1][1] + 1.f);
             const uint32_t k2 = pack_h2(dk[0][2] + 1.f, dk[0][3] + 1.f), k3 = pack_h2(dk[1][2] + 1.f, dk[1][3] + 1.f);
@@ -450,9 +471,13 @@ __device__ void role_prep(const LinearParams &p, uint8_t *sm, const Ring &R, int
         }
         warp_arrive(&R.prep[st], lane);
         TTT_TRACE_AT(p, i, 13);
-        if (has_prev && lane == 0) mbar_arrive(&R.empty[(i + C::kStages - 1) % C::kStages]);  // K_{i-1} no longer read
+        if (PREP & kPrepKx) {
+            if (has_prev && lane == 0) mbar_arrive(&R.empty[(i + C::kStages - 1) % C::kStages]);  // K_{i-1} no longer read
+        } else if (lane == 0) {
+            mbar_arrive(&R.empty[st]);  // no Gram reads this stage again
+        }
     }
-    if (nsteps > 0 && lane == 0) mbar_arrive(&R.empty[(nsteps - 1) % C::kStages]);
+    if ((PREP & kPrepKx) && nsteps > 0 && lane == 0) mbar_arrive(&R.empty[(nsteps - 1) % C::kStages]);
     const bool range_bad = (mag & 0xffffu) >= 0x4780u || (mag >> 16) >= 0x4780u;
     if (__any_sync(kFull, range_bad) && lane == 0) {
         R.flags[1] = 1;
@@ -1480,29 +1505,40 @@ constexpr int kBarRed = 1;  // C warps: one reduction round
 constexpr int kBarA0 = 2;   // A~_i ready (C -> T), ids 2 and 3 by i & 1
 constexpr int kBarS0 = 4;   // S_k ready (T -> C), ids 4 and 5 by k & 1
 
-// C warp w holds Y_i for output features f0..f0+15 (f0 = 16w) with the tokens
-// on the mma M axis: lane (g, c4) has tokens g, g+8 and features
-// f0 + 8nt + 2c4 + e, so a token's sums over the warp's 16 features need four
-// in-register terms and two shuffle levels.
-template <int D, int SUBB>
-__device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int hi, size_t tok0,
+// The chain runs on NC warps (4 in the one-CTA kernel, 2 in the chain CTA of
+// the cluster kernel). Chain warp c holds Y_i for output features
+// 16 CB c .. 16 CB (c + 1) - 1 as CB = MT / NC blocks of 16 (block w = CB c + bk
+// in the weight warps' numbering) with the tokens on the mma M axis: lane
+// (g, c4) has tokens g, g+8 and features 16w + 8nt + 2c4 + e, so a token's sums
+// over the warp's features need 4 CB in-register terms and two shuffle levels,
+// and one exchange with the other chain warps through shared memory completes
+// them. Every lane then forms the statistics of both its tokens itself.
+// SEND (cluster kernel): every step's A~ also goes to the output CTA (rank 1)
+// through its ring of kNA slots, each 16-byte piece by st.async completing on
+// that CTA's afull[slot]; a slot is written again only after the output CTA
+// has released it (aempty[slot] here).
+template <int D, int SUBB, int NC, bool SEND = false>
+__device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring &R, int c, int hi, size_t tok0,
                                  int lane, int nsteps)
 {
     using C = Cfg<D>;
     constexpr int MT = C::MT, NSUB = kSS / SUBB;
-    constexpr int kNAS = 2 * MT * 32;
+    constexpr int CB = MT / NC;
+    constexpr int kNAS = (NC + MT) * 32;  // chain and weight warps
+    static_assert(CB * NC == MT, "the chain warps cover the weight warps' row blocks");
     const int g = lane >> 2, c4 = lane & 3;
-    const int f0 = 16 * w;
-    float gam[2][2], bet[2][2], gg2[2][2];
+    float gam[CB][2][2], bet[CB][2][2], gg2[CB][2][2];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int bk = 0; bk < CB; ++bk)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int f = f0 + 8 * nt + 2 * c4 + e;
-            gam[nt][e] = p.ln_g[hi * D + f];
-            bet[nt][e] = p.ln_b[hi * D + f];
-            gg2[nt][e] = gam[nt][e] * gam[nt][e];
-        }
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int f = 16 * (CB * c + bk) + 8 * nt + 2 * c4 + e;
+                gam[bk][nt][e] = p.ln_g[hi * D + f];
+                bet[bk][nt][e] = p.ln_b[hi * D + f];
+                gg2[bk][nt][e] = gam[bk][nt][e] * gam[bk][nt][e];
+            }
     float gam2all = 0.f;  // sum of gamma^2 over all features
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) gam2all = fmaf(p.ln_g[hi * D + lane + 32 * q], p.ln_g[hi * D + lane + 32 * q], gam2all);
@@ -1512,70 +1548,84 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
     const int T = p.T;
     const float *SR = reinterpret_cast<const float *>(sm + C::kOffSR);
     uint4 *AR = reinterpret_cast<uint4 *>(sm + C::kOffAR);
-    const int tcomb = g + 8 * (c4 & 1);  // the token this lane combines across the C warps
-    int rnd = 0;
-    float yk[2][4];  // [nt][r]: token g + 8(r>>1), feature f0 + 8nt + 2c4 + (r&1)
+    float yk[CB][2][4];  // [bk][nt][r]: token g + 8(r>>1), feature 16(CB c + bk) + 8nt + 2c4 + (r&1)
     auto load_s = [&](int slot) {
-        const float *blk = SR + (slot * MT + w) * 16 * C::SRS;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int bk = 0; bk < CB; ++bk) {
+            const float *blk = SR + (slot * MT + CB * c + bk) * 16 * C::SRS;
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const float2 v = *reinterpret_cast<const float2 *>(blk + (g + 8 * u) * C::SRS + 8 * nt + 2 * c4);
-                yk[nt][2 * u] = v.x;
-                yk[nt][2 * u + 1] = v.y;
-            }
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const float2 v = *reinterpret_cast<const float2 *>(blk + (g + 8 * u) * C::SRS + 8 * nt + 2 * c4);
+                    yk[bk][nt][2 * u] = v.x;
+                    yk[bk][nt][2 * u + 1] = v.y;
+                }
+        }
     };
+    // The per-step inputs of the chain (k - v + beta, the learning rates, the
+    // per-token scalars of the loader). Stage i is read only after the weight
+    // warps have handed S_i over (they waited for the stage first), so these
+    // loads for step i + 1 are issued while the chain waits for S_{i+1}.
+    float kv[CB][2][4], escale[2], shv[2], pkv[2], qkv[2];
+    auto load_in = [&](const uint8_t *stg) {
+#pragma unroll
+        for (int bk = 0; bk < CB; ++bk)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int t = g + 8 * u, f = 16 * (CB * c + bk) + 8 * nt + 2 * c4;
+                    const uint32_t off = swz(t, f >> 3) + (f & 7) * 2;
+                    const uint32_t kb = *reinterpret_cast<const uint32_t *>(stg + C::kOffK + off);
+                    const uint32_t vb = *reinterpret_cast<const uint32_t *>(stg + C::kOffV + off);
+                    kv[bk][nt][2 * u] = bf16_bits_to_f32(kb & 0xffffu) - bf16_bits_to_f32(vb & 0xffffu) + bet[bk][nt][0];
+                    kv[bk][nt][2 * u + 1] = bf16_bits_to_f32(kb >> 16) - bf16_bits_to_f32(vb >> 16) + bet[bk][nt][1];
+                }
+        const float *ssh = reinterpret_cast<const float *>(stg + C::kOffSh);
+        const float *se = reinterpret_cast<const float *>(stg + C::kOffEta);
+        const float *spk = reinterpret_cast<const float *>(stg + C::kOffPk);
+        const float *sqk = reinterpret_cast<const float *>(stg + C::kOffQk);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            escale[u] = -se[g + 8 * u] * (1.f / (float)SUBB);
+            shv[u] = ssh[g + 8 * u];
+            pkv[u] = spk[g + 8 * u];
+            qkv[u] = sqk[g + 8 * u];
+        }
+    };
+    int rnd = 0;
     named_bar_sync(kBarS0, kNAS);  // Y_0 = W_0 K_0^T + c_0 from the T warps
     load_s(0);
+    load_in(stage_ptr<D>(sm, 0));
     for (int i = 0; i < nsteps; ++i) {
         const int st = i % C::kStages, stn = (i + 1) % C::kStages;
         const bool has_next = i + 1 < nsteps;
         uint8_t *stg = stage_ptr<D>(sm, st);
         uint8_t *stgn = stage_ptr<D>(sm, stn);
-        if (w == 0) TTT_TRACE_AT(p, i, 0);
-        // Stage i was waited for by the T warps before they published S_i; the
-        // named barrier that handed S_i over orders these reads after the loads.
-        float kv[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int t = g + 8 * u, f = f0 + 8 * nt + 2 * c4;
-                const uint32_t off = swz(t, f >> 3) + (f & 7) * 2;
-                const uint32_t kb = *reinterpret_cast<const uint32_t *>(stg + C::kOffK + off);
-                const uint32_t vb = *reinterpret_cast<const uint32_t *>(stg + C::kOffV + off);
-                kv[nt][2 * u] = bf16_bits_to_f32(kb & 0xffffu) - bf16_bits_to_f32(vb & 0xffffu) + bet[nt][0];
-                kv[nt][2 * u + 1] = bf16_bits_to_f32(kb >> 16) - bf16_bits_to_f32(vb >> 16) + bet[nt][1];
-            }
-        const float *ssh = reinterpret_cast<const float *>(stg + C::kOffSh);
-        const float *se = reinterpret_cast<const float *>(stg + C::kOffEta);
-        const float escale[2] = {-se[g] * (1.f / (float)SUBB), -se[g + 8] * (1.f / (float)SUBB)};
-        const float shv[2] = {ssh[g], ssh[g + 8]};
-        const float sh_c = ssh[tcomb];
-        const float pk_c = reinterpret_cast<const float *>(stg + C::kOffPk)[tcomb];
-        const float qk_c = reinterpret_cast<const float *>(stg + C::kOffQk)[tcomb];
-        float at[2][4] = {}, lin[2] = {};
-        if (w == 0) TTT_TRACE_AT(p, i, 11);
+        if (c == 0) TTT_TRACE_AT(p, i, 0);
+        float at[CB][2][4] = {}, lin[2] = {};
 #pragma unroll
         for (int m = 0; m < NSUB; ++m) {
-            // this warp's shifted sums over its 16 features, per token (u)
+            // this warp's shifted sums over its 32 features, per token (u)
             float q[2][5];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 float a1 = 0.f, a2 = 0.f, ab = 0.f, ac = 0.f, ad = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int bk = 0; bk < CB; ++bk)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float dv = yk[nt][2 * u + e] - shv[u];
-                        const float g2d = gg2[nt][e] * dv;
-                        a1 += dv;
-                        a2 = fmaf(dv, dv, a2);
-                        ab += g2d;
-                        ac = fmaf(g2d, dv, ac);
-                        ad = fmaf(gam[nt][e] * kv[nt][2 * u + e], dv, ad);
-                    }
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float dv = yk[bk][nt][2 * u + e] - shv[u];
+                            const float g2d = gg2[bk][nt][e] * dv;
+                            a1 += dv;
+                            a2 = fmaf(dv, dv, a2);
+                            ab += g2d;
+                            ac = fmaf(g2d, dv, ac);
+                            ad = fmaf(gam[bk][nt][e] * kv[bk][nt][2 * u + e], dv, ad);
+                        }
                 q[u][0] = a1;
                 q[u][1] = a2;
                 q[u][2] = ab;
@@ -1589,87 +1639,110 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
                     q[u][k] += __shfl_xor_sync(kFull, q[u][k], 1);
                     q[u][k] += __shfl_xor_sync(kFull, q[u][k], 2);
                 }
-            if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 15);
+            if (c == 0 && m == 0) TTT_TRACE_AT(p, i, 15);
             const int buf = rnd & 1;
-            float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
-            float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
+            float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * NC * kSS;
+            float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * NC * kSS;
             if (c4 == 0) {
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    redX[w * kSS + g + 8 * u] = make_float4(q[u][0], q[u][1], q[u][2], q[u][3]);
-                    redY[w * kSS + g + 8 * u] = q[u][4];
+                    redX[c * kSS + g + 8 * u] = make_float4(q[u][0], q[u][1], q[u][2], q[u][3]);
+                    redY[c * kSS + g + 8 * u] = q[u][4];
                 }
             }
-            if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 1);
-            named_bar_sync(kBarRed, MT * 32);
+            named_bar_sync(kBarRed, NC * 32);
             ++rnd;
-            if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 2);
-            float mu_c, rs_c, M1_c, M2_c, LE_c;
-            {
-                float S1 = 0.f, S2 = 0.f, SB = 0.f, SC = 0.f, SD = 0.f;
+            if (c == 0 && m == 0) TTT_TRACE_AT(p, i, 2);
+            float mu[2], rsv[2], rsE[2], cst[2], M2v[2];
 #pragma unroll
-                for (int u = 0; u < MT; ++u) {
-                    const float4 x = redX[u * kSS + tcomb];
+            for (int u = 0; u < 2; ++u) {
+                // add the other chain warps' partial sums of this token
+                float S1 = q[u][0], S2 = q[u][1], SB = q[u][2], SC = q[u][3], SD = q[u][4];
+#pragma unroll
+                for (int o = 1; o < NC; ++o) {
+                    const int src = (c + o) % NC;
+                    const float4 x = redX[src * kSS + g + 8 * u];
                     S1 += x.x;
                     S2 += x.y;
                     SB += x.z;
                     SC += x.w;
-                    SD += redY[u * kSS + tcomb];
+                    SD += redY[src * kSS + g + 8 * u];
                 }
                 const float ee = S1 * invD;
                 const float syy = fmaxf(fmaf(-ee, S1, S2), 0.f);
-                rs_c = rsqrtf(syy * invD + eps);
+                const float rs = rsqrtf(syy * invD + eps);
                 const float sg1 = fmaf(-ee, gam2all, SB);
                 const float sg2 = fmaf(ee * ee, gam2all, fmaf(-2.f * ee, SB, SC));
-                const float sgk = fmaf(-ee, pk_c, SD);
-                M1_c = 2.f * invD * fmaf(rs_c, sg1, pk_c);
-                M2_c = 2.f * invD * rs_c * fmaf(rs_c, sg2, sgk);
-                LE_c = fmaf(rs_c, fmaf(rs_c, sg2, 2.f * sgk), qk_c);
-                mu_c = sh_c + ee;
+                const float sgk = fmaf(-ee, pkv[u], SD);
+                const float M1 = 2.f * invD * fmaf(rs, sg1, pkv[u]);
+                M2v[u] = 2.f * invD * rs * fmaf(rs, sg2, sgk);
+                const bool in_m = NSUB == 1 || (g + 8 * u) / SUBB == m;
+                if (in_m) lin[u] = fmaf(rs, fmaf(rs, sg2, 2.f * sgk), qkv[u]);
+                mu[u] = shv[u] + ee;
+                rsv[u] = rs;
+                rsE[u] = rs * escale[u];   // a~ = rs escale (2 gamma E - M1 - yh M2)
+                cst[u] = -rsE[u] * M1;
             }
-            float ad[2][4];
+            float ad[CB][2][4];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const int src = g * 4 + u;  // lane (g, u) combined token g + 8u
-                const float mu = __shfl_sync(kFull, mu_c, src);
-                const float rs = __shfl_sync(kFull, rs_c, src);
-                const float M1 = __shfl_sync(kFull, M1_c, src);
-                const float M2 = __shfl_sync(kFull, M2_c, src);
-                const float LE = __shfl_sync(kFull, LE_c, src);
                 const bool in_m = NSUB == 1 || (g + 8 * u) / SUBB == m;
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
+                for (int bk = 0; bk < CB; ++bk)
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int r = 2 * u + e;
-                        const float yh = (yk[nt][r] - mu) * rs;
-                        const float E = fmaf(gam[nt][e], yh, kv[nt][r]);
-                        const float G = rs * (2.f * gam[nt][e] * E - M1 - yh * M2);
-                        const float a = round_h(escale[u] * G);
-                        ad[nt][r] = in_m ? a : 0.f;
-                        if (in_m) at[nt][r] = a;
-                    }
-                if (in_m) lin[u] = LE;
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int r = 2 * u + e;
+                            const float yh = (yk[bk][nt][r] - mu[u]) * rsv[u];
+                            const float E = fmaf(gam[bk][nt][e], yh, kv[bk][nt][r]);
+                            const float t2 = fmaf(-M2v[u], yh, 2.f * gam[bk][nt][e] * E);
+                            const float a = round_h(fmaf(rsE[u], t2, cst[u]));
+                            ad[bk][nt][r] = in_m ? a : 0.f;
+                            if (in_m) at[bk][nt][r] = a;
+                        }
             }
             if (NSUB > 1 && m + 1 < NSUB) {
                 // Later mini-batches of this super-step see this one's update:
                 // Y[t][f] += sum_{s in mini-batch m} (k_s . k_t + 1) A~[f][s].
                 const uint4 gk = reinterpret_cast<const uint4 *>(stg + C::kOffGkA)[lane];
                 const uint32_t ga[4] = {gk.x, gk.y, gk.z, gk.w};
-                const uint32_t d00 = movm_t(pack_h2(ad[0][0], ad[0][1])), d01 = movm_t(pack_h2(ad[0][2], ad[0][3]));
-                const uint32_t d10 = movm_t(pack_h2(ad[1][0], ad[1][1])), d11 = movm_t(pack_h2(ad[1][2], ad[1][3]));
-                mma16816(yk[0], ga, d00, d01);
-                mma16816(yk[1], ga, d10, d11);
+#pragma unroll
+                for (int bk = 0; bk < CB; ++bk) {
+                    const uint32_t d00 = movm_t(pack_h2(ad[bk][0][0], ad[bk][0][1]));
+                    const uint32_t d01 = movm_t(pack_h2(ad[bk][0][2], ad[bk][0][3]));
+                    const uint32_t d10 = movm_t(pack_h2(ad[bk][1][0], ad[bk][1][1]));
+                    const uint32_t d11 = movm_t(pack_h2(ad[bk][1][2], ad[bk][1][3]));
+                    mma16816(yk[bk][0], ga, d00, d01);
+                    mma16816(yk[bk][1], ga, d10, d11);
+                }
             }
         }
-        // A~ in the T warps' layout (rows f, columns t): four 8x8 transposes.
-        const uint32_t af[4] = {movm_t(pack_h2(at[0][0], at[0][1])), movm_t(pack_h2(at[1][0], at[1][1])),
-                                movm_t(pack_h2(at[0][2], at[0][3])), movm_t(pack_h2(at[1][2], at[1][3]))};
-        AR[((i & 1) * MT + w) * 32 + lane] = make_uint4(af[0], af[1], af[2], af[3]);
+        // A~ in the T warps' layout (rows f, columns t): four 8x8 transposes per block.
+        uint32_t af[CB][4];
+#pragma unroll
+        for (int bk = 0; bk < CB; ++bk) {
+            af[bk][0] = movm_t(pack_h2(at[bk][0][0], at[bk][0][1]));
+            af[bk][1] = movm_t(pack_h2(at[bk][1][0], at[bk][1][1]));
+            af[bk][2] = movm_t(pack_h2(at[bk][0][2], at[bk][0][3]));
+            af[bk][3] = movm_t(pack_h2(at[bk][1][2], at[bk][1][3]));
+            AR[((i & 1) * MT + CB * c + bk) * 32 + lane] = make_uint4(af[bk][0], af[bk][1], af[bk][2], af[bk][3]);
+        }
         named_bar_arrive(kBarA0 + (i & 1), kNAS);
-        if (w == 0) TTT_TRACE_AT(p, i, 3);
+        if constexpr (SEND) {
+            const int k = i % C::kNA;
+            if (i >= C::kNA && !wait_bar_cluster(&R.aempty[k], parity_of(i / C::kNA - 1), R.flags))
+                abort_chain(R.flags, p.status);  // keep going in step (results discarded)
+            const uint4 *ar1 = reinterpret_cast<const uint4 *>(sm + C::kOffAR1);
+            const uint32_t rbar = map_shared(smem_u32(&R.afull[k]), 1);
+#pragma unroll
+            for (int bk = 0; bk < CB; ++bk)
+                st_async_v4(map_shared(smem_u32(ar1 + (k * MT + CB * c + bk) * 32 + lane), 1),
+                            make_uint4(af[bk][0], af[bk][1], af[bk][2], af[bk][3]), rbar);
+        }
+        if (c == 0) TTT_TRACE_AT(p, i, 3);
         warp_arrive(&R.empty[st], lane);  // before the global stores: a release need not wait for them
-        if (p.inner_loss && w == 0 && c4 == 0) {
+        if (p.inner_loss && c == 0 && c4 == 0) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int t = i * kSS + g + 8 * u;
@@ -1679,23 +1752,34 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
         if (has_next) {
             // Y_{i+1} = S_{i+1} + (K_{i+1} K_i^T + 1) A~_i^T
             named_bar_sync(kBarS0 + ((i + 1) & 1), kNAS);
+            load_in(stgn);
             load_s((i + 1) & 1);
             const uint4 kx = reinterpret_cast<const uint4 *>(stgn + C::kOffKxA)[lane];
             const uint32_t xa[4] = {kx.x, kx.y, kx.z, kx.w};
-            mma16816(yk[0], xa, af[0], af[2]);
-            mma16816(yk[1], xa, af[1], af[3]);
-            if (w == 0) TTT_TRACE_AT(p, i, 4);
+#pragma unroll
+            for (int bk = 0; bk < CB; ++bk) {
+                mma16816(yk[bk][0], xa, af[bk][0], af[bk][2]);
+                mma16816(yk[bk][1], xa, af[bk][1], af[bk][3]);
+            }
+            if (c == 0) TTT_TRACE_AT(p, i, 4);
         }
     }
 }
 
-template <int D>
+// MODE kWFull: W, c, S and the output products Rq, Yq (one-CTA kernel).
+// MODE kWChain: W, c and S only (cluster kernel, chain CTA).
+// MODE kWOut: a copy of W, c (the same products on the same operands, so the
+// two copies agree bit for bit) and Rq, Yq, with each step's A~ from the
+// chain CTA's ring (cluster kernel, output CTA); writes no final state.
+constexpr int kWFull = 0, kWChain = 1, kWOut = 2;
+
+template <int D, int NC, int MODE = kWFull>
 __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int chain, int bi, int hi,
                                    int lane, int nsteps)
 {
     using C = Cfg<D>;
     constexpr int MT = C::MT, NTW = D / 8;
-    constexpr int kNAS = 2 * MT * 32;
+    constexpr int kNAS = (NC + MT) * 32;  // chain and weight warps
     const int g = lane >> 2, c4 = lane & 3;
     const int r0 = 16 * w + g, r1 = r0 + 8;
     const float *W0 = p.W0 + bi * p.w0_bstride + (long long)hi * D * D;
@@ -1732,20 +1816,34 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
         rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, k % C::kStages) + C::kOffKh), lane, acc);
         store_s(k, acc);
     };
+    const uint4 *AR1 = reinterpret_cast<const uint4 *>(sm + C::kOffAR1);
     wait_stage(0);
-    publish_s(0);
-    if (nsteps > 1) {
-        wait_stage(1);
-        publish_s(1);
+    if (MODE != kWOut) {
+        publish_s(0);
+        if (nsteps > 1) {
+            wait_stage(1);
+            publish_s(1);
+        }
     }
     float Rq[2][4];
-    rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, 0) + C::offQh(p)), lane, Rq);
+    if (MODE != kWChain) rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, 0) + C::offQh(p)), lane, Rq);
     for (int j = 0; j < nsteps; ++j) {
         const int st = j % C::kStages, slot = j & 1;
         uint8_t *stg = stage_ptr<D>(sm, st);
-        named_bar_sync(kBarA0 + slot, kNAS);
+        uint4 a;
+        if (MODE == kWOut) {
+            // this step's A~ from the chain CTA: 2 KB of st.async into ring slot k
+            const int k = j % C::kNA;
+            if (w == 0 && lane == 0) mbar_arrive_expect_tx(&R.afull[k], C::MT * 512);
+            if (!wait_bar_cluster(&R.afull[k], parity_of(j / C::kNA), R.flags)) abort_chain(R.flags, p.status);
+            a = AR1[(k * MT + w) * 32 + lane];
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(map_shared(smem_u32(&R.aempty[k]), 0));  // slot k read
+        } else {
+            named_bar_sync(kBarA0 + slot, kNAS);
+            a = AR[(slot * MT + w) * 32 + lane];
+        }
         if (w == 0) TTT_TRACE_AT(p, j, 5);
-        const uint4 a = AR[(slot * MT + w) * 32 + lane];
         const uint32_t af[4] = {a.x, a.y, a.z, a.w};
         // W_{j-1} -> W_j, c_{j-1} -> c_j over the committed tokens of the super-step
         uint32_t au[4] = {a.x, a.y, a.z, a.w};
@@ -1771,35 +1869,52 @@ __device__ void role_weights_split(const LinearParams &p, uint8_t *sm, const Rin
         s1 += __shfl_xor_sync(kFull, s1, 2);
         cb[0] += s0;
         cb[1] += s1;
-        // Yq_j^T = Rq_j^T + A~_j Mq_j -> output warps
-        {
-            const uint4 mq = reinterpret_cast<const uint4 *>(stg + C::kOffMq)[lane];
-            mma16816(Rq[0], af, mq.x, mq.y);
-            mma16816(Rq[1], af, mq.z, mq.w);
+        if (MODE != kWChain) {
+            // Yq_j^T = Rq_j^T + A~_j Mq_j -> output warps
+            {
+                const uint4 mq = reinterpret_cast<const uint4 *>(stg + C::kOffMq)[lane];
+                mma16816(Rq[0], af, mq.x, mq.y);
+                mma16816(Rq[1], af, mq.z, mq.w);
+            }
+            if (!wait_bar(&R.yempty[slot], parity_of(j >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
+            float *ys = reinterpret_cast<float *>(sm + C::kOffY + slot * kSS * C::YS * 4);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    ys[(8 * nt + 2 * c4 + (r & 1)) * C::YS + 16 * w + g + 8 * (r >> 1)] = Rq[nt][r];
+            warp_arrive(&R.yfull[slot], lane);
         }
-        if (!wait_bar(&R.yempty[slot], parity_of(j >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
-        float *ys = reinterpret_cast<float *>(sm + C::kOffY + slot * kSS * C::YS * 4);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                ys[(8 * nt + 2 * c4 + (r & 1)) * C::YS + 16 * w + g + 8 * (r >> 1)] = Rq[nt][r];
-        warp_arrive(&R.yfull[slot], lane);
         if (w == 0) TTT_TRACE_AT(p, j, 6);
-        // S_{j+2} = W_j K_{j+2}^T + c_j and Rq_{j+1} = W_j Q_{j+1}^T + c_j (stage j+1 was
-        // waited for one step earlier), in one pass over W_j.
-        if (j + 2 < nsteps) {
-            wait_stage(j + 2);
-            float acc[2][4];
-            rows_gemm2<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 2) % C::kStages) + C::kOffKh),
-                          smem_u32(stage_ptr<D>(sm, (j + 1) % C::kStages) + C::offQh(p)), lane, acc, Rq);
-            store_s(j + 2, acc);
-        } else if (j + 1 < nsteps) {
-            rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % C::kStages) + C::offQh(p)), lane, Rq);
+        if (MODE == kWFull) {
+            // S_{j+2} = W_j K_{j+2}^T + c_j and Rq_{j+1} = W_j Q_{j+1}^T + c_j (stage j+1 was
+            // waited for one step earlier), in one pass over W_j.
+            if (j + 2 < nsteps) {
+                wait_stage(j + 2);
+                float acc[2][4];
+                rows_gemm2<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 2) % C::kStages) + C::kOffKh),
+                              smem_u32(stage_ptr<D>(sm, (j + 1) % C::kStages) + C::offQh(p)), lane, acc, Rq);
+                store_s(j + 2, acc);
+            } else if (j + 1 < nsteps) {
+                rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % C::kStages) + C::offQh(p)), lane, Rq);
+            }
+        } else if (MODE == kWChain) {
+            if (j + 2 < nsteps) {  // S_{j+2} = W_j K_{j+2}^T + c_j
+                wait_stage(j + 2);
+                float acc[2][4];
+                rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 2) % C::kStages) + C::kOffKh), lane, acc);
+                store_s(j + 2, acc);
+            }
+        } else {
+            if (j + 1 < nsteps) {  // Rq_{j+1} = W_j Q_{j+1}^T + c_j
+                wait_stage(j + 1);
+                rows_gemm<D>(Wa, cb, smem_u32(stage_ptr<D>(sm, (j + 1) % C::kStages) + C::offQh(p)), lane, Rq);
+            }
         }
         if (w == 0) TTT_TRACE_AT(p, j, 7);
         warp_arrive(&R.empty[st], lane);
     }
+    if (MODE == kWOut) return;  // the chain CTA writes the final state
     bool badv = !isfinite(cb[0]) || !isfinite(cb[1]);
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
@@ -1867,12 +1982,110 @@ linear_tc_split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
     } else if (warp == C::kWarpP) {
         role_prep<D, SUBB>(p, sm, R, bi, hi, lane, nsteps);
     } else if (warp < C::kSplitWarpT) {
-        role_chain_split<D, SUBB>(p, sm, R, warp - C::kSplitWarpC, hi, tok0, lane, nsteps);
+        role_chain_split<D, SUBB, C::MT>(p, sm, R, warp - C::kSplitWarpC, hi, tok0, lane, nsteps);
     } else if (warp < C::kSplitWarpO) {
-        role_weights_split<D>(p, sm, R, warp - C::kSplitWarpT, chain, bi, hi, lane, nsteps);
+        role_weights_split<D, C::MT>(p, sm, R, warp - C::kSplitWarpT, chain, bi, hi, lane, nsteps);
     } else {
         role_output<D>(p, sm, R, warp - C::kSplitWarpO, chain, hi, tok0, lane, nsteps);
     }
+}
+
+// ------------------------------------------------------------------ cluster kernel (d = 64, b = 16)
+// One chain over a cluster of two CTAs on two SMs, for workloads with fewer
+// chains than half the SMs (few heads, long sequences). The chain's serial
+// loop is latency-bound and slows down whenever other warps compete for its
+// scheduler partitions, so the work is split by role:
+//   rank 0, the chain CTA: the chain (2 warps, alone on partitions 0 and 1),
+//     W and c with S_{i+2} (4 weight warps, partitions 2 and 3), the loader
+//     of K, V, eta with the per-token scalars, and the prep warp (fp16 K copy,
+//     K_{i-1} K_i^T); it writes inner_loss and the final state;
+//   rank 1, the output CTA: a copy of W and c kept in step by each A~_i that
+//     the chain CTA sends through distributed shared memory (one way, ahead of
+//     its use, so off the chain's loop), Rq and Yq, the output LayerNorm,
+//     Z and L_t, with its own loads of Q, K, V, eta and its own Q K^T.
+// Warps 4, 5, 8, 9 of rank 0 and 8..11 of rank 1 have no role.
+template <int D>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<D>::kSplitThreads, 1)
+linear_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const LinearParams p)
+{
+    using C = Cfg<D>;
+    static_assert(C::kSplitWarps == 12, "warp map below");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = smem_align1024(smem_raw);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t rank = cluster_ctarank();
+    const int chain = blockIdx.x >> 1;
+    const int bi = chain / p.H, hi = chain % p.H;
+    const int nsteps = (p.T + kSS - 1) / kSS;
+    const size_t tok0 = (size_t)chain * p.T;
+
+    Ring R;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C::kOffBar);
+    R.full = bar;
+    R.prep = bar + C::kStages;
+    R.empty = bar + 2 * C::kStages;
+    R.yfull = bar + 3 * C::kStages;
+    R.yempty = R.yfull + 2;
+    R.red = R.yfull + 4;
+    R.afull = R.yfull + 6;
+    R.aempty = R.afull + C::kNA;
+    R.flags = reinterpret_cast<volatile int *>(bar + C::kNumBars);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&R.full[s], 33);   // expect_tx arrive + 32 cp.async arrivals
+            mbar_init(&R.prep[s], 2);    // P and L
+            mbar_init(&R.empty[s], rank == 0 ? 2 + C::MT + 1 : C::MT + C::NO + 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&R.yfull[j], C::MT);
+            mbar_init(&R.yempty[j], C::NO);
+            mbar_init(&R.red[j], C::MT);
+        }
+        for (int k = 0; k < C::kNA; ++k) {
+            mbar_init(&R.afull[k], 1);       // the expect_tx arrival; the bytes come from rank 0
+            mbar_init(&R.aempty[k], C::MT);  // the four weight warps of rank 1, remotely
+        }
+        R.flags[0] = 0;
+        R.flags[1] = 0;
+        fence_mbar_init();
+    }
+    cluster_sync();  // both CTAs' barriers exist before either touches the other
+    if (nsteps > 0) {
+        if (rank == 0) {
+            switch (warp) {
+            case 0:
+            case 1: role_chain_split<D, kSS, 2, true>(p, sm, R, warp, hi, tok0, lane, nsteps); break;
+            case 2: role_weights_split<D, 2, kWChain>(p, sm, R, 0, chain, bi, hi, lane, nsteps); break;
+            case 3: role_weights_split<D, 2, kWChain>(p, sm, R, 1, chain, bi, hi, lane, nsteps); break;
+            case 6: role_weights_split<D, 2, kWChain>(p, sm, R, 2, chain, bi, hi, lane, nsteps); break;
+            case 7: role_weights_split<D, 2, kWChain>(p, sm, R, 3, chain, bi, hi, lane, nsteps); break;
+            case 10: role_loader_sums<D, false, true>(&tmQ, &tmK, &tmV, p, sm, R, chain, bi, hi, lane, nsteps); break;
+            case 11: role_prep<D, kSS, kPrepKx>(p, sm, R, bi, hi, lane, nsteps); break;
+            default: break;
+            }
+        } else {
+            LinearParams po = p;  // the chain CTA writes inner_loss and the final state
+            po.inner_loss = nullptr;
+            po.W_out = nullptr;
+            po.c_out = nullptr;
+            switch (warp) {
+            case 0:
+            case 1:
+            case 2:
+            case 3: role_weights_split<D, 2, kWOut>(po, sm, R, warp, chain, bi, hi, lane, nsteps); break;
+            case 4:
+            case 5: role_output<D>(po, sm, R, warp - 4, chain, hi, tok0, lane, nsteps); break;
+            case 6: role_loader_sums<D, true, false>(&tmQ, &tmK, &tmV, po, sm, R, chain, bi, hi, lane, nsteps); break;
+            case 7: role_prep<D, kSS, kPrepQ | kPrepMq>(po, sm, R, bi, hi, lane, nsteps); break;
+            default: break;
+            }
+        }
+    }
+    // Neither CTA leaves while the other may still write into its shared
+    // memory (A~ pieces into rank 1, slot releases into rank 0).
+    cluster_sync();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1935,6 +2148,29 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ host side
+// 0: never (default: measured faster at every chain count), 1: when the
+// chains fit half the SMs, 2: always.
+std::atomic<int> g_cluster_mode{0};
+
+// The two-CTA form of d = 64, b = 16 (mode 1) runs when every chain gets its
+// pair of SMs in one wave (2 * chains <= SMs); otherwise the one-CTA kernel
+// keeps a chain per SM.
+bool use_cluster_form(int chains)
+{
+    const int mode = g_cluster_mode.load(std::memory_order_relaxed);
+    if (mode == 0) return false;
+    if (mode == 2) return true;
+    static std::atomic<int> sms[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    int n = sms[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        sms[dev].store(n, std::memory_order_relaxed);
+    }
+    return 2 * chains <= n;
+}
+
 template <int D, int SUBB>
 cudaError_t launch_dsub(const LinearParams &p, int chains, cudaStream_t s)
 {
@@ -1943,6 +2179,14 @@ cudaError_t launch_dsub(const LinearParams &p, int chains, cudaStream_t s)
         !make_map(&mV, p.V, D, p.T, chains, 16))
         return cudaErrorInvalidValue;
     constexpr int smem = Cfg<D>::kSmemAlloc;
+    if constexpr (D == 64 && SUBB == kSS) {
+        if (use_cluster_form(chains)) {
+            cudaError_t e = ensure_smem<linear_tc_cluster_kernel<D>>(smem);
+            if (e != cudaSuccess) return e;
+            linear_tc_cluster_kernel<D><<<2 * chains, Cfg<D>::kSplitThreads, smem, s>>>(mQ, mK, mV, p);
+            return cudaGetLastError();
+        }
+    }
     if constexpr (D == 64 && SUBB <= kSS) {
         cudaError_t e = ensure_smem<linear_tc_split_kernel<D, SUBB>>(smem);
         if (e != cudaSuccess) return e;
@@ -1980,6 +2224,12 @@ bool linear_tc_supported(int io, int d, int mb)
 {
     // b = 1..16 divides the 16-token super-step; b = 32..1024 spans 2..64 of them
     return io == TTT_BF16 && (d == 64 || d == 128) && mb >= 1 && mb <= 1024 && (mb & (mb - 1)) == 0;
+}
+
+int linear_cluster_mode(int mode)
+{
+    if (mode >= 0 && mode <= 2) g_cluster_mode.store(mode, std::memory_order_relaxed);
+    return g_cluster_mode.load(std::memory_order_relaxed);
 }
 
 cudaError_t launch_linear_tc(const LinearParams &p, int chains, cudaStream_t s)

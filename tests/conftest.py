@@ -28,3 +28,14 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(params=[0, 2], ids=["one_cta", "cluster"])
+def linear_form(request):
+    """Runs a test with each form of the d = 64, mb = 16 TTT-Linear kernel: one
+    CTA per chain (0) and the two-CTA cluster per chain (2); other shapes are
+    unaffected. The default (0) comes back afterwards."""
+    import test_weight_sequence_ttt_b300 as ttt
+    ttt.linear_cluster_mode(request.param)
+    yield request.param
+    ttt.linear_cluster_mode(0)

@@ -20,7 +20,7 @@ LIN = [(64, 16, 48, "bf16"), (64, 4, 40, "bf16"), (128, 16, 48, "bf16"), (64, 64
 
 
 @pytest.mark.parametrize("d,b,T,io", LIN)
-def test_linear_gate(d, b, T, io):
+def test_linear_gate(d, b, T, io, linear_form):
     tail = T % b != 0
     w = WORKLOADS["linear_b8h12_d64_t2k"].with_(B=2, H=2, T=T, d=d, b=b, io=io, seed=600 + T, eta_base=0.8,
                                                 partial_tail=tail)

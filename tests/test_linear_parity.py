@@ -93,7 +93,29 @@ def test_f32_kernel_bf16_z_output():
     check_bf16_z(got["Z"], oracle_linear(inp)["Z"], TOL["f32"])
 
 
-def test_per_sequence_initial_weights():
+@pytest.mark.parametrize("B,H,T", [(1, 1, 16), (2, 3, 48), (1, 4, 160), (3, 2, 64)])
+def test_d64_b16_both_forms(linear_form, B, H, T):
+    """d = 64, b = 16 in the one-CTA and the two-CTA cluster form, every output."""
+    _check(_small(64, 16, T, B=B, H=H), TOL["bf16"])
+
+
+def test_d64_b16_forms_agree():
+    """The two forms agree with each other to rounding: the chain's LayerNorm
+    sums are added in another order (two chain warps instead of four)."""
+    inp = _small(64, 16, 256, B=2, H=2)
+    try:
+        ttt.linear_cluster_mode(0)
+        a = run_linear(inp)
+        ttt.linear_cluster_mode(2)
+        b = run_linear(inp)
+    finally:
+        ttt.linear_cluster_mode(0)
+    assert int(a["status"].item()) == 0 and int(b["status"].item()) == 0
+    errs = {k: rel_err(to_np(b[k]), to_np(a[k])) for k in KEYS}
+    assert all(e < 1e-2 for e in errs.values()), errs
+
+
+def test_per_sequence_initial_weights(linear_form):
     inp = _small(64, 16, 64, B=3, H=2)
     g = torch.Generator().manual_seed(5)
     inp["W0"] = torch.randn(3, 2, 64, 64, generator=g) * 0.05
@@ -130,6 +152,16 @@ def test_full_size_sampled_chains(name):
     # every output was written
     for k in KEYS:
         assert torch.isfinite(got[k]).all(), k
+
+
+def test_full_size_long_context_cluster_form():
+    """The long-context workload (1 x 32 chains, T = 128K) in the two-CTA
+    cluster form, sampled chains against the oracle."""
+    try:
+        ttt.linear_cluster_mode(2)
+        test_full_size_sampled_chains("linear_b1h32_d64_t128k")
+    finally:
+        ttt.linear_cluster_mode(0)
 
 
 # ---------------------------------------------------------------- invariants (no oracle)

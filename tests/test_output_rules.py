@@ -32,7 +32,7 @@ def _lin(d, b, T, io, B=2, H=3, seed=123):
 
 @pytest.mark.parametrize("rule", RULES)
 @pytest.mark.parametrize("d,b,T,io,kind", LIN_CASES)
-def test_linear_rule_vs_oracle(rule, d, b, T, io, kind):
+def test_linear_rule_vs_oracle(rule, d, b, T, io, kind, linear_form):
     assert ttt.linear_kernel_kind(ttt.BF16 if io == "bf16" else ttt.F32, d, b) == kind
     inp = _lin(d, b, T, io)
     got = run_linear(inp, rule=rule, q_none=rule == "key")
@@ -60,14 +60,14 @@ def test_mlp_rule_vs_oracle(rule, d, h, b, T, io, kind):
         assert torch.equal(got[k], base[k]), k
 
 
-def test_key_rule_loss_is_inner_loss():
+def test_key_rule_loss_is_inner_loss(linear_form):
     inp = _lin(64, 16, 64, "bf16")
     got = run_linear(inp, rule="key", q_none=True)
     assert int(got["status"].item()) == 0
     assert rel_err(to_np(got["loss"]), to_np(got["inner_loss"])) <= TOL["bf16"]
 
 
-def test_key_rule_equals_anchor_rule_with_keys_as_queries():
+def test_key_rule_equals_anchor_rule_with_keys_as_queries(linear_form):
     inp = _lin(64, 16, 48, "bf16")
     a = run_linear(inp, rule="key", q_none=True)
     inp2 = dict(inp)

@@ -38,7 +38,7 @@ def _run_lin(inp, T, rule="prefix", tail=True):
 
 @pytest.mark.parametrize("rule", ["prefix", "anchor"])
 @pytest.mark.parametrize("d,b,T,io,kind", LIN)
-def test_linear_partial_tail(rule, d, b, T, io, kind):
+def test_linear_partial_tail(rule, d, b, T, io, kind, linear_form):
     assert ttt.linear_kernel_kind(ttt.BF16 if io == "bf16" else ttt.F32, d, b) == kind
     Tfull = -(-T // b) * b
     w = WORKLOADS["linear_b8h12_d64_t2k"].with_(B=2, H=2, T=Tfull, d=d, b=b, io=io, seed=300 + T)
