@@ -377,6 +377,8 @@ def _sample_shape(w, cpu_s: float, threads: int, calib=None):
         calib["single_thread_sample"] = "1 chain x %d tokens" % Tc
     tokens_budget = cpu_s / per_tok
     chains = int(min(w.chains, max(1, tokens_budget // w.T)))
+    if chains >= threads and chains < w.chains:
+        chains = chains // threads * threads   # whole rounds of the OpenMP threads over chains
     if chains >= threads or chains == w.chains:
         return chains, w.T
     chains = min(w.chains, threads)
@@ -615,6 +617,7 @@ def run_gpu(args):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     w = WORKLOADS[args.workload]
+    ttt.linear_cluster_mode({"one_cta": 0, "auto": 1, "cluster": 2}[args.linear_form])
     # weak scaling: every rank runs its own full workload (independent chains)
     rank_chains = _rank_chains(dist, rank, world, w)
     inp = make_inputs(w.with_(seed=w.seed + 7919 * rank))
@@ -727,7 +730,7 @@ def run_gpu(args):
                    "mb": w.b, "hidden": w.hidden or None, "io": w.io, "z_dtype": args.z_dtype,
                    "out_rule": rule, "partial_tail": w.partial_tail, "eta_gate": args.eta_gate, "kernel_kind": kind,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world,
-                   "rank_chains": rank_chains},
+                   "rank_chains": rank_chains, "linear_form": args.linear_form},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak,
                      "traffic": measured_traffic(w.name, args.z_dtype) if rule == "prefix" else None,
@@ -744,7 +747,7 @@ def run_gpu(args):
     if world == 1 and not args.no_cpu_baseline:
         threads = __import__("oracle").max_threads()
         calib = {}
-        chains, Ts = _sample_shape(w, args.cpu_budget_s / 4, threads, calib)
+        chains, Ts = _sample_shape(w, args.cpu_budget_s, threads, calib)
         oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule)       # warm-up call
         runs = [oracle_sample(w, chains, Ts, nthreads=threads, rule=args.out_rule) for _ in range(3)]
         dt = statistics.median(r[0] for r in runs)
@@ -904,6 +907,9 @@ def main(argv=None):
                          "for profiling; the line's config says so)")
     ap.add_argument("--backward", action="store_true",
                     help="time ttt_linear_backward (gradients through the inner loop) instead of the forward")
+    ap.add_argument("--linear-form", default="one_cta", choices=["one_cta", "cluster", "auto"],
+                    help="d=64, b=16 TTT-Linear kernel form: one CTA per chain (default), a two-CTA cluster per "
+                         "chain, or the cluster when 2*B*H <= SMs (ttt_linear_cluster_mode 0 / 2 / 1)")
     ap.add_argument("--host-only", action="store_true",
                     help="run the multi-rank logic on CPU (gloo) with the oracle standing in for the GPU step")
     ap.add_argument("--out-rule", default="prefix", choices=["prefix", "anchor", "key"],
