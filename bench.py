@@ -66,6 +66,8 @@ CSRC = os.path.join(ROOT, "test_weight_sequence_ttt_b300", "csrc")
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 # fp32 FFMA peak of one B300: 148 SMs x 128 FP32 lanes x 2 FLOP x 2.032 GHz (maximum SM clock)
 FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+# dense tf32 over dense bf16 tensor throughput, nominal (1.1 / 2.25 PFLOP/s)
+TF32_PER_BF16 = 1.1 / 2.25
 
 
 # The source files each profiled kernel is built from (its .cu and the headers it includes).
@@ -507,7 +509,8 @@ def run_gpu_backward(args):
         call = lambda o: ttt.ttt_linear_backward(dev["Q"], dev["K"], dev["V"], dev[eta_key], dev["W0"], dev["c0"],
                                                  dev["ln_g"], dev["ln_b"], dev["dZ"], mb=w.b, dW_n=dev["dW_n"],
                                                  dc_n=dev["dc_n"], eps=w.eps, out=o, workspace=ws, status=st,
-                                                 stream=stream, eta_gate=args.eta_gate, eta_base=w.eta_base)
+                                                 stream=stream, eta_gate=args.eta_gate, eta_base=w.eta_base,
+                                                 math=args.bwd_math)
     else:
         ws = torch.empty(ttt.mlp_backward_workspace_bytes(w.B, w.H, w.T, w.d, w.hidden, w.b), dtype=torch.uint8,
                          device="cuda")
@@ -559,7 +562,7 @@ def run_gpu_backward(args):
             ttt.ttt_linear_backward(x["Q"], x["K"], x["V"], x[eta_key], x["W0"], x["c0"], x["ln_g"], x["ln_b"],
                                     x["dZ"], mb=w.b, dW_n=x["dW_n"], dc_n=x["dc_n"], eps=w.eps, out=o,
                                     workspace=ws, status=st, stream=strm, eta_gate=args.eta_gate,
-                                    eta_base=w.eta_base)
+                                    eta_base=w.eta_base, math=args.bwd_math)
         else:
             ttt.ttt_mlp_backward(*(x[k] for k in ("Q", "K", "V")), x[eta_key],
                                  *(x[k] for k in ("W1", "c1", "W2", "c2", "ln_g", "ln_b", "dZ")), mb=w.b, eps=w.eps,
@@ -574,12 +577,21 @@ def run_gpu_backward(args):
         return None
     bytes_launch, flops_launch = backward_cost(w)
     achieved = flops_launch / (ms / 1e3) / 1e12
+    tc = args.bwd_math == "tf32" and w.variant == "linear" and w.d == 64 and w.b == 16
+    if tc:  # the contractions run on the tensor cores with tf32 operands
+        pk = _peaks()
+        peak, bound = pk["bf16_tflops"] * TF32_PER_BF16, "tensor"
+        peak_src = "%s bf16 burst x %.3f (nominal dense tf32 / bf16, 1.1 / 2.25 PFLOP/s)" % (pk["source"],
+                                                                                              TF32_PER_BF16)
+    else:
+        peak, bound = FP32_PEAK_TFLOPS, "alu"
+        peak_src = "derived: 148 SMs x 128 FP32 lanes x 2 FLOP x 2.032 GHz"
     line = {
         "metric": "TTT-%s backward (outer-loop gradient) tokens/sec (B·T·H/s) on 1 B300"
                   % ("Linear" if w.variant == "linear" else "MLP"),
         "value": tokens / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32",
+        "vs_baseline": None, "dtype": "tf32-mma/f32" if tc else "f32",
         "precision": "bf16 Q/K/V/dZ inputs; fp32 FFMA arithmetic, fp32 gradients",
         "data": "synthetic (seeded Gaussian Q/K/V/dZ, sigmoid-gated eta, N(0,0.02^2) W0)",
         "config": {"workload": w.name, "direction": "backward", "variant": "ttt-" + w.variant, "B": w.B,
@@ -587,10 +599,10 @@ def run_gpu_backward(args):
                    "eta_gate": args.eta_gate,
                    "workspace_bytes": ws.numel(), "l2": "flushed between steps (256 MiB write)",
                    "parallelism": "dp%d" % world, "rank_chains": rank_chains},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / FP32_PEAK_TFLOPS,
-                     "traffic": measured_traffic(w.name, "", key="%s/backward" % w.name),
-                     "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 FLOP x 2.032 GHz",
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "traffic": measured_traffic(w.name, "", key="%s/backward" % w.name) if not tc else None,
+                     "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": bytes_launch, "algorithmic_flops_per_launch": flops_launch},
         "e2e": {"value": tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps,
@@ -604,7 +616,10 @@ def run_gpu_backward(args):
         line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
                                 "sample": "%d of %d chains x %d tokens (fp64 torch autograd through the "
                                           "primal token loop)" % (chains, w.chains, Ts), "seconds": dt}
-    line["precision"] = "%s Q/K/V/dZ inputs; fp32 FFMA arithmetic, fp32 gradients" % w.io
+    line["precision"] = ("%s Q/K/V/dZ inputs; tensor-core products with tf32 operands and fp32 accumulation, "
+                         "fp32 LayerNorm rows and gradients" % w.io) if tc else \
+        "%s Q/K/V/dZ inputs; fp32 FFMA arithmetic, fp32 gradients" % w.io
+    line["config"]["math"] = args.bwd_math
     return line
 
 
@@ -907,6 +922,8 @@ def main(argv=None):
                          "for profiling; the line's config says so)")
     ap.add_argument("--backward", action="store_true",
                     help="time ttt_linear_backward (gradients through the inner loop) instead of the forward")
+    ap.add_argument("--bwd-math", default="fp32", choices=["fp32", "tf32"],
+                    help="TTT-Linear backward: fp32 FFMA products, or tf32 tensor-core products (d=64, b=16)")
     ap.add_argument("--linear-form", default="one_cta", choices=["one_cta", "cluster", "auto"],
                     help="d=64, b=16 TTT-Linear kernel form: one CTA per chain (default), a two-CTA cluster per "
                          "chain, or the cluster when 2*B*H <= SMs (ttt_linear_cluster_mode 0 / 2 / 1)")

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define TTT_ABI_VERSION 8
+#define TTT_ABI_VERSION 9
 
 typedef enum {
     TTT_OK = 0,
@@ -240,7 +240,23 @@ typedef struct {
     int32_t *status_dev;     /* device int32 (0 on entry), or NULL             */
     int32_t eta_gate;        /* as for the forward                             */
     float eta_base;
+    int32_t math;            /* TTT_BWD_FP32 (default) or TTT_BWD_TF32          */
 } ttt_linear_bwd_args;
+
+/* Arithmetic of the backward's contractions (ttt_linear_bwd_args.math).
+ *  TTT_BWD_FP32  fp32-grade products: max|err| <= 1e-4 RMS per gradient tensor
+ *                against an fp64 reference on the tested sizes. For d = 64,
+ *                mb = 16 they run on the tensor cores in split precision (each
+ *                operand as a sum of two tf32 values, three tf32 products with
+ *                fp32 accumulation); other sizes use fp32 FFMA.
+ *  TTT_BWD_TF32  for d = 64, mb = 16: one tf32 product each (operands rounded
+ *                to 10 mantissa bits, fp32 accumulation) in the reverse sweep;
+ *                the forward recompute of the weight trajectory keeps split
+ *                precision. Faster; gradients within 2e-2 RMS per tensor
+ *                (measured up to 1.5e-2 at T = 2048). Other sizes run as
+ *                TTT_BWD_FP32. LayerNorm rows and the other elementwise work
+ *                are fp32 in every mode. */
+typedef enum { TTT_BWD_FP32 = 0, TTT_BWD_TF32 = 1 } ttt_bwd_math;
 
 /* Supported: io = TTT_F32 or TTT_BF16 with 1 <= d <= 128, 1 <= mb <= 64 and
  *            2d(d+1) + 6d + 11 mb d + 2 mb^2 + 4 mb floats <= 227 KB (fp32

@@ -21,6 +21,7 @@ __all__ = [
     "linear_backward_workspace_bytes", "ttt_mlp_backward", "mlp_backward_workspace_bytes", "MlpBwdArgs",
     "status_string", "abi_version", "linear_kernel_kind", "linear_cluster_mode",
     "mlp_kernel_kind", "LinearArgs", "MlpArgs", "LinearBwdArgs", "STATUS", "F32", "BF16", "OUT_RULES",
+    "BWD_MATH",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -29,6 +30,8 @@ lib_path = os.path.join(_HERE, "libttt_b300.so")
 F32, BF16 = 0, 1
 # ttt_out_rule: which weights / input produce z_t (see include/ttt.h)
 OUT_RULES = {"prefix": 0, "anchor": 1, "key": 2}
+# ttt_bwd_math: arithmetic of the backward's contractions (see include/ttt.h)
+BWD_MATH = {"fp32": 0, "tf32": 1}
 STATUS = {
     0: "TTT_OK", 1: "TTT_ERR_NULL", 2: "TTT_ERR_SHAPE", 3: "TTT_ERR_UNSUPPORTED", 4: "TTT_ERR_ALIGN",
     5: "TTT_ERR_NOT_DEVICE_PTR", 6: "TTT_ERR_CUDA", 7: "TTT_ERR_TIMEOUT", 8: "TTT_ERR_NONFINITE",
@@ -81,6 +84,7 @@ class LinearBwdArgs(ctypes.Structure):
         ("dQ", _vp), ("dK", _vp), ("dV", _vp), ("deta", _vp), ("dW0", _vp), ("dc0", _vp),
         ("dln_g", _vp), ("dln_b", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_uint64),
         ("status_dev", _vp), ("eta_gate", ctypes.c_int32), ("eta_base", ctypes.c_float),
+        ("math", ctypes.c_int32),
     ]
 
 
@@ -330,7 +334,7 @@ def linear_backward_workspace_bytes(B: int, H: int, T: int, d: int, mb: int) -> 
 
 def ttt_linear_backward(Q, K, V, eta, W0, c0, ln_g, ln_b, dZ, *, mb: int, dW_n=None, dc_n=None,
                         eps: float = 1e-6, out: Optional[dict] = None, workspace=None, status=None,
-                        stream=None, eta_gate: bool = False, eta_base: float = 1.0) -> dict:
+                        stream=None, eta_gate: bool = False, eta_base: float = 1.0, math: str = "fp32") -> dict:
     """Gradients of the TTT-Linear inner loop through ``ttt_linear_backward``.
 
     Inputs as for ``ttt_linear_forward`` (prefix rule, T a multiple of mb)
@@ -339,8 +343,12 @@ def ttt_linear_backward(Q, K, V, eta, W0, c0, ln_g, ln_b, dZ, *, mb: int, dW_n=N
     [B,H,T] (w.r.t. the gate logits with ``eta_gate``) and per-chain dW0
     [B,H,d,d], dc0, dln_g, dln_b [B,H,d] (sum over B for parameters shared by
     the sequences). ``workspace`` is an optional uint8 CUDA tensor of at least
-    ``linear_backward_workspace_bytes`` bytes; one is allocated otherwise."""
+    ``linear_backward_workspace_bytes`` bytes; one is allocated otherwise.
+    ``math`` is "fp32" (every product in fp32) or "tf32" (for d = 64, mb = 16
+    the products run on the tensor cores with tf32 operands; include/ttt.h)."""
     import torch
+    if math not in BWD_MATH:
+        raise ValueError("math must be one of %s" % sorted(BWD_MATH))
     for n, t in (("Q", Q), ("K", K), ("V", V), ("eta", eta), ("W0", W0), ("c0", c0), ("ln_g", ln_g),
                  ("ln_b", ln_b), ("dZ", dZ), ("dW_n", dW_n), ("dc_n", dc_n), ("workspace", workspace),
                  ("status", status)):
@@ -367,6 +375,7 @@ def ttt_linear_backward(Q, K, V, eta, W0, c0, ln_g, ln_b, dZ, *, mb: int, dW_n=N
         dW0=_ptr(out["dW0"]), dc0=_ptr(out["dc0"]), dln_g=_ptr(out["dln_g"]), dln_b=_ptr(out["dln_b"]),
         workspace=_ptr(workspace), workspace_bytes=workspace.numel() * workspace.element_size(),
         status_dev=_ptr(status), eta_gate=int(bool(eta_gate)), eta_base=float(eta_base),
+        math=BWD_MATH[math],
     )
     rc = lib().ttt_linear_backward(ctypes.byref(a), _stream_handle(stream))
     if rc != 0:

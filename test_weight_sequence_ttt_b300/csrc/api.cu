@@ -344,6 +344,7 @@ ttt_status ttt_linear_backward(const ttt_linear_bwd_args *a, void *stream)
     if (!(a->ln_eps >= 0.f) || a->ln_eps > 1.f) return TTT_ERR_SHAPE;
     if (a->w0_bstride < 0 || a->c0_bstride < 0) return TTT_ERR_SHAPE;
     if (!gate_ok(a->eta_gate, a->eta_base)) return TTT_ERR_SHAPE;
+    if (a->math != TTT_BWD_FP32 && a->math != TTT_BWD_TF32) return TTT_ERR_UNSUPPORTED;
     if (!ttt::linear_bwd_supported(a->io, a->d, a->mb)) return TTT_ERR_UNSUPPORTED;
     const size_t wsb = ttt::linear_bwd_workspace_bytes(a->B, a->H, a->T, a->d, a->mb);
     if (a->workspace_bytes < wsb) return TTT_ERR_SHAPE;
@@ -392,6 +393,7 @@ ttt_status ttt_linear_backward(const ttt_linear_bwd_args *a, void *stream)
     p.T = a->T;
     p.d = a->d;
     p.mb = a->mb;
+    p.tf32 = a->math == TTT_BWD_TF32;
     p.eta_gate = a->eta_gate;
     p.eta_base = a->eta_base;
     p.eps = a->ln_eps;

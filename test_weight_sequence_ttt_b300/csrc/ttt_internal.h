@@ -75,6 +75,7 @@ struct MlpParams {
 // Gradients of the TTT-Linear inner loop (prefix rule, T a multiple of mb).
 struct LinearBwdParams {
     int H, T, d, mb;
+    int tf32;  // 1: contractions on the tensor cores with tf32 operands (d = 64, mb = 16)
     int eta_gate;
     float eta_base;
     float eps;

@@ -725,10 +725,151 @@ __device__ __forceinline__ void key_rows_t(const SmemT &S, float eps, int warp, 
     }
 }
 
-template <typename IO, int D, int MB, int NT>
+// ------------------------------------------------------------------ tensor-core products (tf32)
+// The contractions of the tiled kernel on mma.sync m16n8k8 with tf32 operands
+// (fp32 range, operands rounded to nearest to 10 mantissa bits) and fp32
+// accumulation. Operand elements come from shared-memory tiles through the
+// element functions fa(m, k) and fb(k, n); lane (g, c4) feeds k = k0 + 2 c4 and
+// k0 + 2 c4 + 1 into the fragment slots the instruction defines for k0 + c4 and
+// k0 + c4 + 4: a permutation of the k8 block that A and B share, so the sum is
+// the same. Accumulator element r of a tile is (m0 + g + 8 (r >> 1),
+// n0 + 2 c4 + (r & 1)).
+// An fp32 value as a tf32 mma operand, rounded to nearest: the tensor cores
+// read the top 19 bits of the container (sign, exponent, 10 mantissa bits),
+// so adding half of the dropped part (bit 12) first makes their truncation a
+// rounding (ties away from zero). One integer add instead of a conversion
+// instruction on a slower pipe.
+__device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x) + 0x1000u; }
+
+// The same rounding with the dropped bits cleared: the exact value the
+// tensor cores see, for splitting x into hi + lo.
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u); }
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// X3: split precision. Each operand x is carried as hi = tf32(x) and lo =
+// tf32(x - hi), and the product as hi*hi + hi*lo + lo*hi (three mma): about
+// 21 of the 24 fp32 mantissa bits, for the products whose rounding would
+// otherwise be carried through the inner loop's recurrence.
+template <bool X3 = false, class FA, class FB>
+__device__ __forceinline__ void mma_k8(float (&acc)[4], const FA &fa, const FB &fb, int m0, int n0, int k0, int lane)
+{
+    const int g = lane >> 2, ka = k0 + 2 * (lane & 3);
+    const float a[4] = {fa(m0 + g, ka), fa(m0 + g + 8, ka), fa(m0 + g, ka + 1), fa(m0 + g + 8, ka + 1)};
+    const float b[2] = {fb(ka, n0 + g), fb(ka + 1, n0 + g)};
+    uint32_t ah[4], bh[2];
+    if constexpr (X3) {
+        uint32_t al[4], bl[2];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const float h = tf32_hi(a[r]);
+            ah[r] = __float_as_uint(h);
+            al[r] = to_tf32(a[r] - h);
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const float h = tf32_hi(b[r]);
+            bh[r] = __float_as_uint(h);
+            bl[r] = to_tf32(b[r] - h);
+        }
+        mma_tf32(acc, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+        mma_tf32(acc, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+    } else {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) ah[r] = to_tf32(a[r]);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) bh[r] = to_tf32(b[r]);
+    }
+    mma_tf32(acc, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
+}
+
+// acc += sum over k < K of A(m0 + ., k) B(k, n0 + .), in two independent chains
+// (even and odd k8 blocks) that are added at the end.
+template <int K, bool X3 = false, class FA, class FB>
+__device__ __forceinline__ void mma_run(float (&acc)[4], const FA &fa, const FB &fb, int m0, int n0, int lane)
+{
+    if constexpr (K == 8) {
+        mma_k8<X3>(acc, fa, fb, m0, n0, 0, lane);
+    } else {
+        float odd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k0 = 0; k0 < K; k0 += 16) {
+            mma_k8<X3>(acc, fa, fb, m0, n0, k0, lane);
+            mma_k8<X3>(odd, fa, fb, m0, n0, k0 + 8, lane);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] += odd[r];
+    }
+}
+
+// The 16 x N result R(m, n) = init(m, n) + sum_k A1(m, k) B1(k, n) [+ sum_k A2(m, k) B2(k, n)]:
+// warp w forms the n-tiles w, w + NW, ... and hands every element to out(m, n, v).
+template <int N, int NW, int K1, int K2, bool X3 = false, class FI, class FA1, class FB1, class FA2, class FB2,
+          class FO>
+__device__ __forceinline__ void tc_rows(const FI &init, const FA1 &fa1, const FB1 &fb1, const FA2 &fa2, const FB2 &fb2,
+                                        const FO &out, int warp, int lane)
+{
+    const int g = lane >> 2, c4 = lane & 3;
+#pragma unroll
+    for (int nt = warp; nt < N / 8; nt += NW) {
+        const int n0 = 8 * nt;
+        float acc[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[r] = init(g + 8 * (r >> 1), n0 + 2 * c4 + (r & 1));
+        mma_run<K1, X3>(acc, fa1, fb1, 0, n0, lane);
+        if constexpr (K2 > 0) {
+            float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_run<K2, X3>(acc2, fa2, fb2, 0, n0, lane);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[r] += acc2[r];
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) out(g + 8 * (r >> 1), n0 + 2 * c4 + (r & 1), acc[r]);
+    }
+}
+
+// The D x D result of one or two outer-product sums over the MB tokens,
+// sum_t A1(x, t) B1(t, y) [+ sum_t A2(x, t) B2(t, y)], handed to out(x, y, v);
+// warp w forms the 16 x 8 tiles w, w + NW, ... (D / 16 x D / 8 of them).
+template <int D, int MB, int NW, bool TWO, bool X3 = false, class FA1, class FB1, class FA2, class FB2, class FO>
+__device__ __forceinline__ void tc_outer(const FA1 &fa1, const FB1 &fb1, const FA2 &fa2, const FB2 &fb2, const FO &out,
+                                         int warp, int lane)
+{
+    constexpr int MTL = D / 16, TILES = MTL * (D / 8);
+    static_assert(TILES % NW == 0, "whole tiles per warp");
+    const int g = lane >> 2, c4 = lane & 3;
+#pragma unroll
+    for (int q = 0; q < TILES / NW; ++q) {
+        const int tile = warp + NW * q;
+        const int m0 = 16 * (tile % MTL), n0 = 8 * (tile / MTL);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k0 = 0; k0 < MB; k0 += 8) {
+            mma_k8<X3>(acc, fa1, fb1, m0, n0, k0, lane);
+            if constexpr (TWO) mma_k8<X3>(acc, fa2, fb2, m0, n0, k0, lane);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) out(m0 + g + 8 * (r >> 1), n0 + 2 * c4 + (r & 1), acc[r]);
+    }
+}
+
+// MATH 0: fp32 FFMA throughout. MATH 1: every contraction on the tensor cores
+// in split precision (three tf32 products per product: fp32-grade results).
+// MATH 2: the same with one tf32 product, except in the forward sweep, which
+// recomputes the weight trajectory and keeps split precision.
+template <typename IO, int D, int MB, int NT, int MATH = 0>
 __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams p)
 {
+    constexpr bool TC = MATH != 0, X3 = MATH == 1;
     using C = Tiled<D, MB, NT>;
+    const auto none = [](int, int) { return 0.f; };
     constexpr int LD = C::LD, NG = C::NG, RPT = C::RPT, RW = C::RW, EL = C::EL, NW = C::NW;
     constexpr float inv_b = 1.f / (float)MB, inv_d = 1.f / (float)D;
     extern __shared__ __align__(16) float smt[];
@@ -893,7 +1034,12 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             load_eta(t0);
         }
         __syncthreads();
-        {
+        if constexpr (TC) {  // the forward sweep recomputes the trajectory: split precision
+            tc_rows<D, NW, D, 0, true>([&](int, int n) { return S.c[n]; },
+                                       [&](int m, int k) { return S.K[m * LD + k]; },
+                                       [&](int k, int n) { return S.W[n * LD + k]; }, none, none,
+                                       [&](int m, int n, float v) { S.Yh[m * LD + n] = v; }, warp, lane);
+        } else {
             float a[RPT], dummy[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) a[r] = S.c[col];
@@ -918,7 +1064,12 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
                 sv[3 * MB * D + MB + x] = S.m2k[x];
             }
         }
-        {
+        if constexpr (TC) {
+            tc_outer<D, MB, NW, false, true>([&](int x, int t) { return S.et[t] * S.G[t * LD + x]; },
+                                       [&](int t, int y) { return S.K[t * LD + y]; }, none, none,
+                                       [&](int x, int y, float v) { S.W[x * LD + y] = fmaf(-inv_b, v, S.W[x * LD + y]); },
+                                       warp, lane);
+        } else {
             float acc[C::TR][C::TC] = {};
             outer_acc<D, MB, NT, true>(acc, S.G, S.K, S.et, tid);
             outer_store<D, MB, NT>(S.W, acc, -inv_b, tid);
@@ -974,7 +1125,22 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         }
         __syncthreads();
         // y_s = W k_s + c, W q_t + c; R_s = dW' k_s + dc'; q_t.k_s + 1
-        {
+        if constexpr (TC) {
+            tc_rows<D, NW, D, 0, X3>([&](int, int n) { return S.c[n]; }, [&](int m, int k) { return S.Q[m * LD + k]; },
+                                 [&](int k, int n) { return S.W[n * LD + k]; }, none, none,
+                                 [&](int m, int n, float v) { S.P[m * LD + n] = v; }, warp, lane);
+            tc_rows<D, NW, D, 0, X3>([&](int, int n) { return S.dc[n]; }, [&](int m, int k) { return S.K[m * LD + k]; },
+                                 [&](int k, int n) { return S.dW[n * LD + k]; }, none, none,
+                                 [&](int m, int n, float v) { S.R[m * LD + n] = v; }, warp, lane);
+            if (!SAVE)
+                tc_rows<D, NW, D, 0, X3>([&](int, int n) { return S.c[n]; },
+                                     [&](int m, int k) { return S.K[m * LD + k]; },
+                                     [&](int k, int n) { return S.W[n * LD + k]; }, none, none,
+                                     [&](int m, int n, float v) { S.Yh[m * LD + n] = v; }, warp, lane);
+            tc_rows<MB, NW, D, 0, X3>([](int, int) { return 1.f; }, [&](int t, int k) { return S.Q[t * LD + k]; },
+                                  [&](int k, int sc) { return S.K[sc * LD + k]; }, none, none,
+                                  [&](int t, int sc, float v) { S.QK[t * MB + sc] = v; }, warp, lane);
+        } else {
             float ak[RPT], aq[RPT], ar[RPT], dummy[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
@@ -994,16 +1160,16 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
                 S.P[s * LD + col] = aq[r];
                 S.R[s * LD + col] = ar[r];
             }
-        }
-        for (int idx = tid; idx < MB * MB; idx += NT) {
-            const int t = idx / MB, s = idx % MB;
-            float acc = 1.f;
+            for (int idx = tid; idx < MB * MB; idx += NT) {
+                const int t = idx / MB, s = idx % MB;
+                float acc = 1.f;
 #pragma unroll 4
-            for (int ii = 0; ii < D; ii += 4) {
-                const float4 q = ld4(S.Q + t * LD + ii), k = ld4(S.K + s * LD + ii);
-                acc = fmaf(q.x, k.x, fmaf(q.y, k.y, fmaf(q.z, k.z, fmaf(q.w, k.w, acc))));
+                for (int ii = 0; ii < D; ii += 4) {
+                    const float4 q = ld4(S.Q + t * LD + ii), k = ld4(S.K + s * LD + ii);
+                    acc = fmaf(q.x, k.x, fmaf(q.y, k.y, fmaf(q.z, k.z, fmaf(q.w, k.w, acc))));
+                }
+                S.QK[idx] = acc;
             }
-            S.QK[idx] = acc;
         }
         __syncthreads();
         if (!SAVE) {
@@ -1011,7 +1177,12 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             __syncthreads();
         }
         // p_t = W q_t + c - sum_{s<=t} A_ts g_s
-        {
+        if constexpr (TC) {
+            tc_rows<D, NW, MB, 0, X3>([&](int t, int n) { return S.P[t * LD + n]; },
+                                  [&](int t, int sc) { return sc <= t ? -S.QK[t * MB + sc] * S.et[sc] * inv_b : 0.f; },
+                                  [&](int sc, int n) { return S.G[sc * LD + n]; }, none, none,
+                                  [&](int t, int n, float v) { S.P[t * LD + n] = v; }, warp, lane);
+        } else {
             float a[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) a[r] = S.P[(rg + NG * r) * LD + col];
@@ -1088,21 +1259,46 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             S.dgam[j] += ag;
             S.dbet[j] += ab;
         }
-        for (int idx = tid; idx < MB * MB; idx += NT) {
-            const int t = idx / MB, s = idx % MB;
-            float acc = 0.f;
-            if (s <= t) {
+        if constexpr (TC) {
+            tc_rows<MB, NW, D, 0, X3>([](int, int) { return 0.f; }, [&](int t, int k) { return S.DP[t * LD + k]; },
+                                  [&](int k, int sc) { return S.G[sc * LD + k]; }, none, none,
+                                  [&](int t, int sc, float v) { S.DA[t * MB + sc] = sc <= t ? -v : 0.f; }, warp, lane);
+        } else {
+            for (int idx = tid; idx < MB * MB; idx += NT) {
+                const int t = idx / MB, s = idx % MB;
+                float acc = 0.f;
+                if (s <= t) {
 #pragma unroll 4
-                for (int j = 0; j < D; j += 4) {
-                    const float4 x = ld4(S.DP + t * LD + j), g = ld4(S.G + s * LD + j);
-                    acc = fmaf(x.x, g.x, fmaf(x.y, g.y, fmaf(x.z, g.z, fmaf(x.w, g.w, acc))));
+                    for (int j = 0; j < D; j += 4) {
+                        const float4 x = ld4(S.DP + t * LD + j), g = ld4(S.G + s * LD + j);
+                        acc = fmaf(x.x, g.x, fmaf(x.y, g.y, fmaf(x.z, g.z, fmaf(x.w, g.w, acc))));
+                    }
                 }
+                S.DA[idx] = -acc;
             }
-            S.DA[idx] = -acc;
         }
         __syncthreads();
         // dq_t; dk_s's q- and dW'-parts (KA); dg_s (into P); deta_s
-        {
+        if constexpr (TC) {
+            float *dQc = p.dQ + (tok0 + t0) * D;
+            tc_rows<D, NW, D, MB, X3>([&](int t, int n) { return S.DZ[t * LD + n]; },
+                                  [&](int t, int j) { return S.DP[t * LD + j]; },
+                                  [&](int j, int n) { return S.W[j * LD + n]; },
+                                  [&](int t, int sc) { return sc <= t ? S.DA[t * MB + sc] * S.et[sc] * inv_b : 0.f; },
+                                  [&](int sc, int n) { return S.K[sc * LD + n]; },
+                                  [&](int t, int n, float v) { dQc[t * D + n] = v; }, warp, lane);
+            tc_rows<D, NW, MB, D, X3>([](int, int) { return 0.f; },
+                                  [&](int sc, int t) { return t >= sc ? S.DA[t * MB + sc] : 0.f; },
+                                  [&](int t, int n) { return S.Q[t * LD + n]; },
+                                  [&](int sc, int j) { return -S.G[sc * LD + j]; },
+                                  [&](int j, int n) { return S.dW[j * LD + n]; },
+                                  [&](int sc, int n, float v) { S.KA[sc * LD + n] = S.et[sc] * inv_b * v; }, warp, lane);
+            tc_rows<D, NW, MB, 0, X3>([&](int sc, int n) { return S.R[sc * LD + n]; },
+                                  [&](int sc, int t) { return t >= sc ? S.QK[t * MB + sc] : 0.f; },
+                                  [&](int t, int n) { return S.DP[t * LD + n]; }, none, none,
+                                  [&](int sc, int n, float v) { S.P[sc * LD + n] = -S.et[sc] * inv_b * v; }, warp, lane);
+        }
+        if constexpr (!TC) {
             float a[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) a[r] = S.DZ[(rg + NG * r) * LD + col];
@@ -1118,7 +1314,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
 #pragma unroll
             for (int r = 0; r < RPT; ++r) p.dQ[(tok0 + t0 + rg + NG * r) * D + col] = a[r];
         }
-        {
+        if constexpr (!TC) {
             float a[RPT], mix[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) a[r] = mix[r] = 0.f;
@@ -1137,7 +1333,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
                 S.KA[s * LD + col] = S.et[s] * inv_b * (mix[r] - a[r]);
             }
         }
-        {
+        if constexpr (!TC) {
             float a[RPT];
 #pragma unroll
             for (int r = 0; r < RPT; ++r) a[r] = 0.f;
@@ -1226,18 +1422,29 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             issue_anchor(i - 1);
             if (PFS) issue_saved(i - 1);
         }
-        {
-            float a[RPT];
+        if constexpr (TC) {
+            float *dKc = p.dK + (tok0 + t0) * D;
+            tc_rows<D, NW, D, 0, X3>([&](int sc, int n) { return S.KA[sc * LD + n] + 2.f * S.gam[n] * S.R[sc * LD + n]; },
+                                 [&](int sc, int j) { return S.P[sc * LD + j]; },
+                                 [&](int j, int n) { return S.W[j * LD + n]; }, none, none,
+                                 [&](int sc, int n, float v) { dKc[sc * D + n] = v; }, warp, lane);
+            tc_outer<D, MB, NW, true, X3>([&](int x, int t) { return S.DP[t * LD + x]; },
+                                      [&](int t, int y) { return S.Q[t * LD + y]; },
+                                      [&](int x, int t) { return S.P[t * LD + x]; },
+                                      [&](int t, int y) { return S.K[t * LD + y]; },
+                                      [&](int x, int y, float v) { S.dW[x * LD + y] += v; }, warp, lane);
+        } else {
+            {
+                float a[RPT];
 #pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                const int s = rg + NG * r;
-                a[r] = S.KA[s * LD + col] + 2.f * S.gam[col] * S.R[s * LD + col];
+                for (int r = 0; r < RPT; ++r) {
+                    const int s = rg + NG * r;
+                    a[r] = S.KA[s * LD + col] + 2.f * S.gam[col] * S.R[s * LD + col];
+                }
+                prod_m<D, MB, NT>(a, S.P, S.W, col, rg);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) p.dK[(tok0 + t0 + rg + NG * r) * D + col] = a[r];
             }
-            prod_m<D, MB, NT>(a, S.P, S.W, col, rg);
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) p.dK[(tok0 + t0 + rg + NG * r) * D + col] = a[r];
-        }
-        {
             float acc[C::TR][C::TC] = {};
             outer_acc<D, MB, NT, false>(acc, S.DP, S.Q, nullptr, tid);
             outer_acc<D, MB, NT, false>(acc, S.P, S.K, nullptr, tid);
@@ -1282,20 +1489,22 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
     if (bad && p.status) atomicCAS(p.status, 0, TTT_ERR_NONFINITE);
 }
 
-template <typename IO, int D, int MB, int NT>
+template <typename IO, int D, int MB, int NT, int MATH = 0>
 cudaError_t launch_tiled(const LinearBwdParams &p, int chains, cudaStream_t s)
 {
     const size_t smem = sizeof(float) * Tiled<D, MB, NT>::kFloats;
-    cudaError_t e = ensure_smem<linear_bwd_tiled_kernel<IO, D, MB, NT>>((int)smem);
+    cudaError_t e = ensure_smem<linear_bwd_tiled_kernel<IO, D, MB, NT, MATH>>((int)smem);
     if (e != cudaSuccess) return e;
-    linear_bwd_tiled_kernel<IO, D, MB, NT><<<chains, NT, smem, s>>>(p);
+    linear_bwd_tiled_kernel<IO, D, MB, NT, MATH><<<chains, NT, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 template <typename IO>
 cudaError_t launch_bwd_io(const LinearBwdParams &p, int chains, cudaStream_t s, size_t smem_generic)
 {
-    if (p.d == 64 && p.mb == 16) return launch_tiled<IO, 64, 16, 256>(p, chains, s);
+    // d = 64, b = 16: tensor cores, split precision (fp32-grade) or one tf32 product
+    if (p.d == 64 && p.mb == 16)
+        return p.tf32 ? launch_tiled<IO, 64, 16, 256, 2>(p, chains, s) : launch_tiled<IO, 64, 16, 256, 1>(p, chains, s);
     if (p.d == 128 && p.mb == 16) return launch_tiled<IO, 128, 16, 256>(p, chains, s);
     cudaError_t e = ensure_smem<linear_bwd_kernel<IO>>((int)smem_generic);
     if (e != cudaSuccess) return e;
