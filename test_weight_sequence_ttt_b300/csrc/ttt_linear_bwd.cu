@@ -38,6 +38,7 @@
 // statistics, after the checkpoints) and the reverse sweep reads it back instead
 // of recomputing y_s and the key LayerNorm.
 #include <cuda_bf16.h>
+#include <type_traits>
 
 
 #include "ttt_internal.h"
@@ -728,11 +729,8 @@ __device__ __forceinline__ void key_rows_t(const SmemT &S, float eps, int warp, 
 // ------------------------------------------------------------------ tensor-core products (tf32)
 // The contractions of the tiled kernel on mma.sync m16n8k8 with tf32 operands
 // (fp32 range, operands rounded to nearest to 10 mantissa bits) and fp32
-// accumulation. Operand elements come from shared-memory tiles through the
-// element functions fa(m, k) and fb(k, n); lane (g, c4) feeds k = k0 + 2 c4 and
-// k0 + 2 c4 + 1 into the fragment slots the instruction defines for k0 + c4 and
-// k0 + c4 + 4: a permutation of the k8 block that A and B share, so the sum is
-// the same. Accumulator element r of a tile is (m0 + g + 8 (r >> 1),
+// accumulation, operands from the shared-memory tiles (see the operand sources
+// below). Accumulator element r of a tile is (m0 + g + 8 (r >> 1),
 // n0 + 2 c4 + (r & 1)).
 // An fp32 value as a tf32 mma operand, rounded to nearest: the tensor cores
 // read the top 19 bits of the container (sign, exponent, 10 mantissa bits),
@@ -741,9 +739,10 @@ __device__ __forceinline__ void key_rows_t(const SmemT &S, float eps, int warp, 
 // instruction on a slower pipe.
 __device__ __forceinline__ uint32_t to_tf32(float x) { return __float_as_uint(x) + 0x1000u; }
 
-// The same rounding with the dropped bits cleared: the exact value the
-// tensor cores see, for splitting x into hi + lo.
-__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u); }
+// x with the 13 bits the tensor cores drop cleared: hi of the split x = hi + lo
+// (lo = x - hi is exact, below 2^-10 |x|, and its own tf32 rounding costs
+// 2^-21 |x| at most).
+__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xffffe000u); }
 
 __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1)
@@ -754,38 +753,115 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Operand sources. A fragment (16 x 8, rows m0.., columns k0..): lane (g, c4)
+// holds A(m0 + g, k0 + c4), A(m0 + g + 8, k0 + c4), A(m0 + g, k0 + c4 + 4),
+// A(m0 + g + 8, k0 + c4 + 4); B fragment (8 x 8): B(k0 + c4, n0 + g),
+// B(k0 + c4 + 4, n0 + g). ARows / BRowsT read a row-major fp32 tile with one
+// ldmatrix: viewed as 16-bit pairs, an 8 x 4 block of fp32 is an 8 x 8 b16
+// matrix, and ldmatrix hands lane (g, c4) the 32-bit word (row g, column c4),
+// which is the fragment element. Row starts must be 16-byte aligned. EXACT
+// marks a source whose values tf32 holds exactly (tiles of bf16 inputs: 8
+// mantissa bits), so split precision needs no low part for it.
+template <bool EXACT = false>
+struct ARows {  // A(m, k) = p[m * ld + k]
+    static constexpr bool kExact = EXACT;
+    const float *p;
+    int ld;
+    __device__ __forceinline__ void frag(uint32_t (&a)[4], int m0, int k0, int lane) const
+    {
+        const int row = m0 + (lane & 7) + 8 * ((lane >> 3) & 1), col = k0 + 4 * (lane >> 4);
+        asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                     : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p + row * ld + col))));
+    }
+};
+template <bool EXACT = false>
+struct BRowsT {  // B(k, n) = p[n * ld + k]
+    static constexpr bool kExact = EXACT;
+    const float *p;
+    int ld;
+    __device__ __forceinline__ void frag(uint32_t (&b)[2], int k0, int n0, int lane) const
+    {
+        const int l = lane & 15, row = n0 + (l & 7), col = k0 + 4 * (l >> 3);
+        asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+                     : "=r"(b[0]), "=r"(b[1])
+                     : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p + row * ld + col))));
+    }
+};
+template <class F, bool EXACT = false>
+struct AFn {  // A(m, k) = f(m, k)
+    static constexpr bool kExact = EXACT;
+    F f;
+    __device__ __forceinline__ void frag(uint32_t (&a)[4], int m0, int k0, int lane) const
+    {
+        const int g = lane >> 2, c4 = lane & 3;
+        a[0] = __float_as_uint(f(m0 + g, k0 + c4));
+        a[1] = __float_as_uint(f(m0 + g + 8, k0 + c4));
+        a[2] = __float_as_uint(f(m0 + g, k0 + c4 + 4));
+        a[3] = __float_as_uint(f(m0 + g + 8, k0 + c4 + 4));
+    }
+};
+template <class F, bool EXACT = false>
+struct BFn {  // B(k, n) = f(k, n)
+    static constexpr bool kExact = EXACT;
+    F f;
+    __device__ __forceinline__ void frag(uint32_t (&b)[2], int k0, int n0, int lane) const
+    {
+        const int g = lane >> 2, c4 = lane & 3;
+        b[0] = __float_as_uint(f(k0 + c4, n0 + g));
+        b[1] = __float_as_uint(f(k0 + c4 + 4, n0 + g));
+    }
+};
+template <bool EXACT = false, class F>
+__device__ __forceinline__ AFn<F, EXACT> afn(F f) { return AFn<F, EXACT>{f}; }
+template <bool EXACT = false, class F>
+__device__ __forceinline__ BFn<F, EXACT> bfn(F f) { return BFn<F, EXACT>{f}; }
+struct NoOp {  // an absent second product
+    static constexpr bool kExact = true;
+    __device__ __forceinline__ void frag(uint32_t (&a)[4], int, int, int) const {}
+    __device__ __forceinline__ void frag(uint32_t (&b)[2], int, int, int) const {}
+};
+
 // X3: split precision. Each operand x is carried as hi = tf32(x) and lo =
 // tf32(x - hi), and the product as hi*hi + hi*lo + lo*hi (three mma): about
 // 21 of the 24 fp32 mantissa bits, for the products whose rounding would
 // otherwise be carried through the inner loop's recurrence.
-template <bool X3 = false, class FA, class FB>
-__device__ __forceinline__ void mma_k8(float (&acc)[4], const FA &fa, const FB &fb, int m0, int n0, int k0, int lane)
+template <bool X3 = false, class SA, class SB>
+__device__ __forceinline__ void mma_k8(float (&acc)[4], const SA &sa, const SB &sb, int m0, int n0, int k0, int lane)
 {
-    const int g = lane >> 2, ka = k0 + 2 * (lane & 3);
-    const float a[4] = {fa(m0 + g, ka), fa(m0 + g + 8, ka), fa(m0 + g, ka + 1), fa(m0 + g + 8, ka + 1)};
-    const float b[2] = {fb(ka, n0 + g), fb(ka + 1, n0 + g)};
+    uint32_t a[4], b[2];
+    sa.frag(a, m0, k0, lane);
+    sb.frag(b, k0, n0, lane);
     uint32_t ah[4], bh[2];
     if constexpr (X3) {
         uint32_t al[4], bl[2];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const float h = tf32_hi(a[r]);
-            ah[r] = __float_as_uint(h);
-            al[r] = to_tf32(a[r] - h);
+            if constexpr (SA::kExact) {
+                ah[r] = a[r];
+            } else {
+                const float h = tf32_hi(__uint_as_float(a[r]));
+                ah[r] = __float_as_uint(h);
+                al[r] = to_tf32(__uint_as_float(a[r]) - h);
+            }
         }
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            const float h = tf32_hi(b[r]);
-            bh[r] = __float_as_uint(h);
-            bl[r] = to_tf32(b[r] - h);
+            if constexpr (SB::kExact) {
+                bh[r] = b[r];
+            } else {
+                const float h = tf32_hi(__uint_as_float(b[r]));
+                bh[r] = __float_as_uint(h);
+                bl[r] = to_tf32(__uint_as_float(b[r]) - h);
+            }
         }
-        mma_tf32(acc, al[0], al[1], al[2], al[3], bh[0], bh[1]);
-        mma_tf32(acc, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+        if constexpr (!SA::kExact) mma_tf32(acc, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+        if constexpr (!SB::kExact) mma_tf32(acc, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
     } else {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) ah[r] = to_tf32(a[r]);
+        for (int r = 0; r < 4; ++r) ah[r] = a[r] + 0x1000u;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) bh[r] = to_tf32(b[r]);
+        for (int r = 0; r < 2; ++r) bh[r] = b[r] + 0x1000u;
     }
     mma_tf32(acc, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
 }
@@ -809,8 +885,9 @@ __device__ __forceinline__ void mma_run(float (&acc)[4], const FA &fa, const FB 
     }
 }
 
-// The 16 x N result R(m, n) = init(m, n) + sum_k A1(m, k) B1(k, n) [+ sum_k A2(m, k) B2(k, n)]:
-// warp w forms the n-tiles w, w + NW, ... and hands every element to out(m, n, v).
+// The 16 x N result R(m, n) = init(m, n) + sum_k A1(m, k) B1(k, n) [+ sum_k A2(m, k) B2(k, n)]
+// (operand sources fa*, fb*): warp w forms the n-tiles w, w + NW, ... and hands
+// every element to out(m, n, v).
 template <int N, int NW, int K1, int K2, bool X3 = false, class FI, class FA1, class FB1, class FA2, class FB2,
           class FO>
 __device__ __forceinline__ void tc_rows(const FI &init, const FA1 &fa1, const FB1 &fb1, const FA2 &fa2, const FB2 &fb2,
@@ -836,7 +913,7 @@ __device__ __forceinline__ void tc_rows(const FI &init, const FA1 &fa1, const FB
 }
 
 // The D x D result of one or two outer-product sums over the MB tokens,
-// sum_t A1(x, t) B1(t, y) [+ sum_t A2(x, t) B2(t, y)], handed to out(x, y, v);
+// sum_t A1(x, t) B1(t, y) [+ sum_t A2(x, t) B2(t, y)] (operand sources), handed to out(x, y, v);
 // warp w forms the 16 x 8 tiles w, w + NW, ... (D / 16 x D / 8 of them).
 template <int D, int MB, int NW, bool TWO, bool X3 = false, class FA1, class FB1, class FA2, class FB2, class FO>
 __device__ __forceinline__ void tc_outer(const FA1 &fa1, const FB1 &fb1, const FA2 &fa2, const FB2 &fb2, const FO &out,
@@ -868,8 +945,9 @@ template <typename IO, int D, int MB, int NT, int MATH = 0>
 __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams p)
 {
     constexpr bool TC = MATH != 0, X3 = MATH == 1;
+    constexpr bool QE = std::is_same<IO, __nv_bfloat16>::value;  // K, Q tiles hold bf16 values: exact in tf32
     using C = Tiled<D, MB, NT>;
-    const auto none = [](int, int) { return 0.f; };
+    const NoOp none{};
     constexpr int LD = C::LD, NG = C::NG, RPT = C::RPT, RW = C::RW, EL = C::EL, NW = C::NW;
     constexpr float inv_b = 1.f / (float)MB, inv_d = 1.f / (float)D;
     extern __shared__ __align__(16) float smt[];
@@ -1035,9 +1113,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         }
         __syncthreads();
         if constexpr (TC) {  // the forward sweep recomputes the trajectory: split precision
-            tc_rows<D, NW, D, 0, true>([&](int, int n) { return S.c[n]; },
-                                       [&](int m, int k) { return S.K[m * LD + k]; },
-                                       [&](int k, int n) { return S.W[n * LD + k]; }, none, none,
+            tc_rows<D, NW, D, 0, true>([&](int, int n) { return S.c[n]; }, ARows<QE>{S.K, LD}, BRowsT<>{S.W, LD}, none, none,
                                        [&](int m, int n, float v) { S.Yh[m * LD + n] = v; }, warp, lane);
         } else {
             float a[RPT], dummy[RPT];
@@ -1065,8 +1141,8 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             }
         }
         if constexpr (TC) {
-            tc_outer<D, MB, NW, false, true>([&](int x, int t) { return S.et[t] * S.G[t * LD + x]; },
-                                       [&](int t, int y) { return S.K[t * LD + y]; }, none, none,
+            tc_outer<D, MB, NW, false, true>(afn([&](int x, int t) { return S.et[t] * S.G[t * LD + x]; }),
+                                             bfn<QE>([&](int t, int y) { return S.K[t * LD + y]; }), none, none,
                                        [&](int x, int y, float v) { S.W[x * LD + y] = fmaf(-inv_b, v, S.W[x * LD + y]); },
                                        warp, lane);
         } else {
@@ -1126,19 +1202,15 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         __syncthreads();
         // y_s = W k_s + c, W q_t + c; R_s = dW' k_s + dc'; q_t.k_s + 1
         if constexpr (TC) {
-            tc_rows<D, NW, D, 0, X3>([&](int, int n) { return S.c[n]; }, [&](int m, int k) { return S.Q[m * LD + k]; },
-                                 [&](int k, int n) { return S.W[n * LD + k]; }, none, none,
+            tc_rows<D, NW, D, 0, X3>([&](int, int n) { return S.c[n]; }, ARows<QE>{S.Q, LD}, BRowsT<>{S.W, LD}, none, none,
                                  [&](int m, int n, float v) { S.P[m * LD + n] = v; }, warp, lane);
-            tc_rows<D, NW, D, 0, X3>([&](int, int n) { return S.dc[n]; }, [&](int m, int k) { return S.K[m * LD + k]; },
-                                 [&](int k, int n) { return S.dW[n * LD + k]; }, none, none,
+            tc_rows<D, NW, D, 0, X3>([&](int, int n) { return S.dc[n]; }, ARows<QE>{S.K, LD}, BRowsT<>{S.dW, LD}, none, none,
                                  [&](int m, int n, float v) { S.R[m * LD + n] = v; }, warp, lane);
             if (!SAVE)
-                tc_rows<D, NW, D, 0, X3>([&](int, int n) { return S.c[n]; },
-                                     [&](int m, int k) { return S.K[m * LD + k]; },
-                                     [&](int k, int n) { return S.W[n * LD + k]; }, none, none,
+                tc_rows<D, NW, D, 0, X3>([&](int, int n) { return S.c[n]; }, ARows<QE>{S.K, LD}, BRowsT<>{S.W, LD}, none,
+                                         none,
                                      [&](int m, int n, float v) { S.Yh[m * LD + n] = v; }, warp, lane);
-            tc_rows<MB, NW, D, 0, X3>([](int, int) { return 1.f; }, [&](int t, int k) { return S.Q[t * LD + k]; },
-                                  [&](int k, int sc) { return S.K[sc * LD + k]; }, none, none,
+            tc_rows<MB, NW, D, 0, X3>([](int, int) { return 1.f; }, ARows<QE>{S.Q, LD}, BRowsT<QE>{S.K, LD}, none, none,
                                   [&](int t, int sc, float v) { S.QK[t * MB + sc] = v; }, warp, lane);
         } else {
             float ak[RPT], aq[RPT], ar[RPT], dummy[RPT];
@@ -1179,8 +1251,8 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         // p_t = W q_t + c - sum_{s<=t} A_ts g_s
         if constexpr (TC) {
             tc_rows<D, NW, MB, 0, X3>([&](int t, int n) { return S.P[t * LD + n]; },
-                                  [&](int t, int sc) { return sc <= t ? -S.QK[t * MB + sc] * S.et[sc] * inv_b : 0.f; },
-                                  [&](int sc, int n) { return S.G[sc * LD + n]; }, none, none,
+                                  afn([&](int t, int sc) { return sc <= t ? -S.QK[t * MB + sc] * S.et[sc] * inv_b : 0.f; }),
+                                  bfn([&](int sc, int n) { return S.G[sc * LD + n]; }), none, none,
                                   [&](int t, int n, float v) { S.P[t * LD + n] = v; }, warp, lane);
         } else {
             float a[RPT];
@@ -1260,8 +1332,7 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             S.dbet[j] += ab;
         }
         if constexpr (TC) {
-            tc_rows<MB, NW, D, 0, X3>([](int, int) { return 0.f; }, [&](int t, int k) { return S.DP[t * LD + k]; },
-                                  [&](int k, int sc) { return S.G[sc * LD + k]; }, none, none,
+            tc_rows<MB, NW, D, 0, X3>([](int, int) { return 0.f; }, ARows<>{S.DP, LD}, BRowsT<>{S.G, LD}, none, none,
                                   [&](int t, int sc, float v) { S.DA[t * MB + sc] = sc <= t ? -v : 0.f; }, warp, lane);
         } else {
             for (int idx = tid; idx < MB * MB; idx += NT) {
@@ -1282,20 +1353,18 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         if constexpr (TC) {
             float *dQc = p.dQ + (tok0 + t0) * D;
             tc_rows<D, NW, D, MB, X3>([&](int t, int n) { return S.DZ[t * LD + n]; },
-                                  [&](int t, int j) { return S.DP[t * LD + j]; },
-                                  [&](int j, int n) { return S.W[j * LD + n]; },
-                                  [&](int t, int sc) { return sc <= t ? S.DA[t * MB + sc] * S.et[sc] * inv_b : 0.f; },
-                                  [&](int sc, int n) { return S.K[sc * LD + n]; },
+                                  ARows<>{S.DP, LD}, bfn([&](int j, int n) { return S.W[j * LD + n]; }),
+                                  afn([&](int t, int sc) { return sc <= t ? S.DA[t * MB + sc] * S.et[sc] * inv_b : 0.f; }),
+                                  bfn<QE>([&](int sc, int n) { return S.K[sc * LD + n]; }),
                                   [&](int t, int n, float v) { dQc[t * D + n] = v; }, warp, lane);
             tc_rows<D, NW, MB, D, X3>([](int, int) { return 0.f; },
-                                  [&](int sc, int t) { return t >= sc ? S.DA[t * MB + sc] : 0.f; },
-                                  [&](int t, int n) { return S.Q[t * LD + n]; },
-                                  [&](int sc, int j) { return -S.G[sc * LD + j]; },
-                                  [&](int j, int n) { return S.dW[j * LD + n]; },
+                                  afn([&](int sc, int t) { return t >= sc ? S.DA[t * MB + sc] : 0.f; }),
+                                  bfn<QE>([&](int t, int n) { return S.Q[t * LD + n]; }), ARows<>{S.G, LD},
+                                  bfn([&](int j, int n) { return -S.dW[j * LD + n]; }),
                                   [&](int sc, int n, float v) { S.KA[sc * LD + n] = S.et[sc] * inv_b * v; }, warp, lane);
             tc_rows<D, NW, MB, 0, X3>([&](int sc, int n) { return S.R[sc * LD + n]; },
-                                  [&](int sc, int t) { return t >= sc ? S.QK[t * MB + sc] : 0.f; },
-                                  [&](int t, int n) { return S.DP[t * LD + n]; }, none, none,
+                                  afn([&](int sc, int t) { return t >= sc ? S.QK[t * MB + sc] : 0.f; }),
+                                  bfn([&](int t, int n) { return S.DP[t * LD + n]; }), none, none,
                                   [&](int sc, int n, float v) { S.P[sc * LD + n] = -S.et[sc] * inv_b * v; }, warp, lane);
         }
         if constexpr (!TC) {
@@ -1425,13 +1494,12 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
         if constexpr (TC) {
             float *dKc = p.dK + (tok0 + t0) * D;
             tc_rows<D, NW, D, 0, X3>([&](int sc, int n) { return S.KA[sc * LD + n] + 2.f * S.gam[n] * S.R[sc * LD + n]; },
-                                 [&](int sc, int j) { return S.P[sc * LD + j]; },
-                                 [&](int j, int n) { return S.W[j * LD + n]; }, none, none,
+                                 ARows<>{S.P, LD}, bfn([&](int j, int n) { return S.W[j * LD + n]; }), none, none,
                                  [&](int sc, int n, float v) { dKc[sc * D + n] = v; }, warp, lane);
-            tc_outer<D, MB, NW, true, X3>([&](int x, int t) { return S.DP[t * LD + x]; },
-                                      [&](int t, int y) { return S.Q[t * LD + y]; },
-                                      [&](int x, int t) { return S.P[t * LD + x]; },
-                                      [&](int t, int y) { return S.K[t * LD + y]; },
+            tc_outer<D, MB, NW, true, X3>(afn([&](int x, int t) { return S.DP[t * LD + x]; }),
+                                          bfn<QE>([&](int t, int y) { return S.Q[t * LD + y]; }),
+                                          afn([&](int x, int t) { return S.P[t * LD + x]; }),
+                                          bfn<QE>([&](int t, int y) { return S.K[t * LD + y]; }),
                                       [&](int x, int y, float v) { S.dW[x * LD + y] += v; }, warp, lane);
         } else {
             {
