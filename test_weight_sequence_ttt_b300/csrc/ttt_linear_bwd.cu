@@ -1570,10 +1570,11 @@ cudaError_t launch_tiled(const LinearBwdParams &p, int chains, cudaStream_t s)
 template <typename IO>
 cudaError_t launch_bwd_io(const LinearBwdParams &p, int chains, cudaStream_t s, size_t smem_generic)
 {
-    // d = 64, b = 16: tensor cores, split precision (fp32-grade) or one tf32 product
+    // b = 16, d = 64 or 128: tensor cores, split precision (fp32-grade) or one tf32 product
     if (p.d == 64 && p.mb == 16)
         return p.tf32 ? launch_tiled<IO, 64, 16, 256, 2>(p, chains, s) : launch_tiled<IO, 64, 16, 256, 1>(p, chains, s);
-    if (p.d == 128 && p.mb == 16) return launch_tiled<IO, 128, 16, 256>(p, chains, s);
+    if (p.d == 128 && p.mb == 16)
+        return p.tf32 ? launch_tiled<IO, 128, 16, 256, 2>(p, chains, s) : launch_tiled<IO, 128, 16, 256, 1>(p, chains, s);
     cudaError_t e = ensure_smem<linear_bwd_kernel<IO>>((int)smem_generic);
     if (e != cudaSuccess) return e;
     linear_bwd_kernel<IO><<<chains, kThreads, smem_generic, s>>>(p);

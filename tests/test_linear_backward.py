@@ -86,7 +86,7 @@ def _compare(got, ref, sel=None, tol=TOL_BWD):
 @pytest.mark.parametrize("B,H,T,d,b,io", [
     (2, 2, 64, 16, 16, "f32"), (1, 3, 128, 64, 16, "f32"), (1, 2, 96, 40, 12, "f32"),
     (2, 2, 48, 64, 1, "f32"), (1, 2, 256, 64, 32, "f32"), (1, 2, 256, 32, 64, "f32"),
-    (1, 2, 64, 128, 16, "f32"),
+    (1, 2, 64, 128, 16, "f32"), (1, 2, 256, 128, 16, "bf16"),
     (2, 2, 128, 64, 16, "bf16"), (1, 1, 16, 8, 16, "f32"),
     (1, 1, 32, 128, 8, "f32"),       # d = 128 on the general kernel
 ])
@@ -167,9 +167,10 @@ def test_backward_host_pointer_rejected():
 
 # ---------------------------------------------------------------- tf32 tensor-core kernel (d = 64, b = 16)
 
-@pytest.mark.parametrize("B,H,T,io", [(1, 3, 128, "f32"), (2, 2, 128, "bf16"), (1, 1, 16, "f32"), (2, 1, 512, "bf16")])
-def test_backward_tf32_matches_oracle(B, H, T, io):
-    x = _case(B, H, T, 64, 16, io, seed=B * 1000 + T + 2)
+@pytest.mark.parametrize("B,H,T,d,io", [(1, 3, 128, 64, "f32"), (2, 2, 128, 64, "bf16"), (1, 1, 16, 64, "f32"),
+                                         (2, 1, 512, 64, "bf16"), (1, 2, 256, 128, "bf16"), (1, 1, 64, 128, "f32")])
+def test_backward_tf32_matches_oracle(B, H, T, d, io):
+    x = _case(B, H, T, d, 16, io, seed=B * 1000 + T + 2 + d)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     got = _run(x, status=st, math="tf32")
     assert int(st.item()) == 0
