@@ -633,6 +633,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     w = WORKLOADS[args.workload]
     ttt.linear_cluster_mode({"one_cta": 0, "auto": 1, "cluster": 2}[args.linear_form])
+    ttt.mlp_cluster_mode({"one_cta": 0, "auto": 1, "cluster": 2}[args.mlp_form])
     # weak scaling: every rank runs its own full workload (independent chains)
     rank_chains = _rank_chains(dist, rank, world, w)
     inp = make_inputs(w.with_(seed=w.seed + 7919 * rank))
@@ -745,7 +746,8 @@ def run_gpu(args):
                    "mb": w.b, "hidden": w.hidden or None, "io": w.io, "z_dtype": args.z_dtype,
                    "out_rule": rule, "partial_tail": w.partial_tail, "eta_gate": args.eta_gate, "kernel_kind": kind,
                    "l2": "flushed between steps (256 MiB write)", "parallelism": "dp%d" % world,
-                   "rank_chains": rank_chains, "linear_form": args.linear_form},
+                   "rank_chains": rank_chains, "linear_form": args.linear_form,
+                   "mlp_form": args.mlp_form},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak,
                      "traffic": measured_traffic(w.name, args.z_dtype) if rule == "prefix" else None,
@@ -927,6 +929,9 @@ def main(argv=None):
     ap.add_argument("--linear-form", default="one_cta", choices=["one_cta", "cluster", "auto"],
                     help="d=64, b=16 TTT-Linear kernel form: one CTA per chain (default), a two-CTA cluster per "
                          "chain, or the cluster when 2*B*H <= SMs (ttt_linear_cluster_mode 0 / 2 / 1)")
+    ap.add_argument("--mlp-form", default="auto", choices=["one_cta", "cluster", "auto"],
+                    help="tensor-core TTT-MLP kernel form: one CTA per chain, a two-CTA cluster per chain with the "
+                         "hidden units split, or the cluster when 2*B*H <= SMs (default; ttt_mlp_cluster_mode 0 / 2 / 1)")
     ap.add_argument("--host-only", action="store_true",
                     help="run the multi-rank logic on CPU (gloo) with the oracle standing in for the GPU step")
     ap.add_argument("--out-rule", default="prefix", choices=["prefix", "anchor", "key"],

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define TTT_ABI_VERSION 9
+#define TTT_ABI_VERSION 10
 
 typedef enum {
     TTT_OK = 0,
@@ -362,6 +362,20 @@ int ttt_mlp_kernel_kind(int32_t io, int32_t d, int32_t hidden, int32_t mb);
  *   2: always. Process-wide, for later calls; any other value only returns the
  *   current mode. */
 int32_t ttt_linear_cluster_mode(int32_t mode);
+
+/* Form of the tensor-core TTT-MLP kernel (kind 2 of ttt_mlp_kernel_kind). The
+ * chain is serial as above, and with few chains most SMs would idle. The
+ * cluster form runs each chain on a cluster of two CTAs that split the hidden
+ * units of f_res(x) = W2 gelu(W1 x + c1) + c2 ("TTT layer" section of the
+ * "Test-Time Training(TTT)과 LLM 메모리" survey page): each owns 128 rows of W1
+ * and c1 and 128 columns of W2, and every sum over the hidden units (the key
+ * forward Y, the output forward Yq) adds the two CTAs' partial sums, which
+ * cross over in distributed shared memory. Results agree with the one-CTA
+ * form's to rounding (each sum over the hidden units is taken in two halves).
+ *   mode 0: never; 1: when 2 * B * H <= the device's SM count (default);
+ *   2: always. Process-wide, for later calls; any other value only returns the
+ *   current mode. */
+int32_t ttt_mlp_cluster_mode(int32_t mode);
 
 /* Failure-detection testing hook. In the library built with fault hooks
  * (libttt_b300_faults.so; never the product library) it makes the loader of

@@ -20,6 +20,7 @@ __all__ = [
     "TTTError", "lib", "lib_path", "ttt_linear_forward", "ttt_mlp_forward", "ttt_linear_backward",
     "linear_backward_workspace_bytes", "ttt_mlp_backward", "mlp_backward_workspace_bytes", "MlpBwdArgs",
     "status_string", "abi_version", "linear_kernel_kind", "linear_cluster_mode",
+    "mlp_cluster_mode",
     "mlp_kernel_kind", "LinearArgs", "MlpArgs", "LinearBwdArgs", "STATUS", "F32", "BF16", "OUT_RULES",
     "BWD_MATH",
 ]
@@ -144,6 +145,8 @@ def lib() -> ctypes.CDLL:
             L.ttt_abi_version.restype = ctypes.c_int
             L.ttt_linear_cluster_mode.restype = ctypes.c_int32
             L.ttt_linear_cluster_mode.argtypes = [ctypes.c_int32]
+            L.ttt_mlp_cluster_mode.restype = ctypes.c_int32
+            L.ttt_mlp_cluster_mode.argtypes = [ctypes.c_int32]
             L.ttt_abi_version.argtypes = []
             L.ttt_linear_kernel_kind.restype = ctypes.c_int
             L.ttt_linear_kernel_kind.argtypes = [ctypes.c_int32] * 3
@@ -177,6 +180,14 @@ def linear_cluster_mode(mode: int = -1) -> int:
     mb = 16 TTT-Linear kernel that runs each chain on a two-CTA cluster; any
     other value only reads the current mode (see include/ttt.h)."""
     return int(lib().ttt_linear_cluster_mode(int(mode)))
+
+
+def mlp_cluster_mode(mode: int = -1) -> int:
+    """Set (0 never; 1 when 2 * B * H <= SMs, the default; 2 always) and
+    return the form of the tensor-core TTT-MLP kernel that runs each chain on
+    a two-CTA cluster with the hidden units split; any other value only reads
+    the current mode (see include/ttt.h)."""
+    return int(lib().ttt_mlp_cluster_mode(int(mode)))
 
 
 def linear_kernel_kind(io: int, d: int, mb: int) -> int:

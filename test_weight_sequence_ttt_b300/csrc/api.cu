@@ -114,6 +114,8 @@ int ttt_debug_drop_load(int32_t step)
 
 int32_t ttt_linear_cluster_mode(int32_t mode) { return ttt::linear_cluster_mode(mode); }
 
+int32_t ttt_mlp_cluster_mode(int32_t mode) { return ttt::mlp_cluster_mode(mode); }
+
 int ttt_linear_kernel_kind(int32_t io, int32_t d, int32_t mb)
 {
     if (ttt::linear_tc_supported(io, d, mb)) return 2;

@@ -54,6 +54,21 @@ __device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity,
     }
 }
 
+// Wait for data or a release that the other CTA of the cluster sends every
+// step, aborted or not: it does not give up when this CTA has aborted, so the
+// two CTAs' exchanges stay in step (a barrier is never re-armed before its
+// phase completed, and no CTA leaves with the peer's stores still landing).
+// Bounded all the same.
+__device__ __forceinline__ bool wait_peer(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait_cluster(bar, parity, 0)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity, kSleepHintNs)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 __device__ __forceinline__ void abort_chain(volatile int *flags, int *status)
 {
     flags[0] = 1;

@@ -133,6 +133,9 @@ cudaError_t launch_mlp_f32(const MlpParams &p, int io, int chains, cudaStream_t 
 // Tensor-core TTT-MLP kernel (io bf16, d = 64, hidden = 256, mb = 16).
 bool mlp_tc_supported(int io, int d, int hidden, int mb);
 cudaError_t launch_mlp_tc(const MlpParams &p, int chains, cudaStream_t s);
+// Chains on two-CTA clusters (hidden units split): 0 never, 1 when
+// 2 * chains <= SMs (default), 2 always. A mode outside 0..2 only reads it.
+int mlp_cluster_mode(int mode);
 
 // fp32 FFMA backward kernel (io f32 or bf16), d <= 128, mb <= 64.
 bool linear_bwd_supported(int io, int d, int mb);

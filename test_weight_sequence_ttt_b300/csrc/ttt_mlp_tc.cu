@@ -41,6 +41,21 @@
 // failed wait a warp keeps running in step with the others (its results are
 // discarded, the status word says why), so every barrier is always met.
 //
+// Cluster form (few chains): one chain over a cluster of two CTAs, CTA r owning
+// hidden units 128r..128r+127 (W1 rows, c1, W2 columns; eight H warps of 16 units
+// each, against 32 in the one-CTA form, so the issue slots still have three warps
+// per partition to pick from). Every contraction over the hidden units is then
+// a sum of the two CTAs' partials:
+//   - Y of the recurrence: each CTA's Y warps send their partial (the A~2 Gram
+//     term included) to the other CTA through distributed shared memory
+//     (st.async, completion counted on the receiver's mbarrier) and add the
+//     one they receive; both CTAs then run the same LayerNorm backward, so G,
+//     A~2 and c2 are bitwise the same in both (fp32 addition commutes).
+//   - Yq of the outputs: CTA 1 sends its partial (and its part of the X2q X2k^T
+//     Gram, through A~2) to CTA 0, whose P warp adds it and writes Z; P releases
+//     the slot with a remote arrive.
+// The K/Q/V tiles are loaded by both CTAs; the d-wide Grams are built in both.
+//
 // Precision: fp16 MMA operands (W1, W2, K, Q, X2, G, A~) with fp32
 // accumulation; W1, W2, c1, c2, LayerNorm statistics and gradients fp32. GELU
 // uses the hardware tanh approximation.
@@ -56,11 +71,8 @@ namespace {
 using namespace tc;
 
 constexpr int kD = 64, kHid = 256, kB = 16;
-constexpr int kNH = 8;  // H warps, 32 hidden units each
 constexpr int kNY = 2;  // Y warps, 32 output features each
-constexpr int kWarpL = 0, kWarpP = 1, kWarpH = 2, kWarpY = kWarpH + kNH;
-constexpr int kWarps = kWarpY + kNY;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarpL = 0, kWarpP = 1, kWarpH = 2;
 constexpr int kStages = 5;
 // stage layout (bytes)
 constexpr int kTile = 32 * kD;
@@ -70,41 +82,72 @@ constexpr int kOffMq = 5 * kTile;                          // causal q.k + 1, fp
 constexpr int kOffKx = kOffMq + 512;                       // k_{i-1}.k_i + 1, fp16 B fragments
 constexpr int kOffEta = kOffKx + 512;
 constexpr int kStageBytes = ((kOffEta + 64 + 1023) / 1024) * 1024;
-// fp16 activation / weight buffers, rows padded by 16 bytes (conflict-free ldmatrix)
-constexpr int kHS = kHid + 8;  // halves per row of a [*][hidden] buffer
-constexpr int kFS = kD + 8;    // halves per row of a [16][d] buffer
+constexpr int kFS = kD + 8;  // halves per row of a [16][d] fp16 buffer (rows padded by 16 bytes)
 constexpr int kOffStages = 0;
-constexpr int kW2hBytes = kD * kHS * 2;                  // one fp16 copy of W2, [d][kHS]
-constexpr int kOffW2h = kStages * kStageBytes;          // 3 copies: W2_j in buffer j % 3
-constexpr int kX2Bytes = kB * kHS * 2;                  // one [16][kHS] fp16 activation tile
-constexpr int kOffX2k = kOffW2h + 3 * kW2hBytes;        // 3 x gelu(Z1) of the keys, step j in j % 3
-constexpr int kOffX2q = kOffX2k + 3 * kX2Bytes;         // 2 x gelu(Z1q), step j in j & 1
 constexpr int kGBytes = kB * kFS * 2;
-constexpr int kOffGh = kOffX2q + 2 * kX2Bytes;          // 2 x [16][kFS] G, step j in j & 1
-constexpr int kOffGt = kOffGh + 2 * kGBytes;            // 2 x [16][kFS] A~2 = -(eta/b) G
-constexpr int kOffRed = kOffGt + 2 * kGBytes;           // 2 bufs x [2 Y warps][16] float4
-constexpr int kYS = kD + 4;                              // floats per row of the Yq hand-off
-constexpr int kOffYq = kOffRed + 2 * kNY * kB * 16;      // 2 slots x [16][kYS] fp32 Yq (Y -> P)
-constexpr int kOffMq2 = kOffYq + 2 * kB * kYS * 4;       // causal x2q.x2k + 1 fragments (P -> Y)
-constexpr int kOffTmem = kOffMq2 + 512;
-constexpr int kOffBar = kOffTmem + 16;
-constexpr int kNumBars = 3 * kStages + 7;
-constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
-constexpr int kSmemAlloc = kSmem + 1024;
+constexpr int kYS = kD + 4;  // floats per row of the Yq hand-off
 constexpr uint32_t kTmemCols = 128;  // two H warps per lane quarter x 64 columns
-// named barriers: H <-> Y hand-offs (all 320 H and Y threads), Y-internal rounds
+// named barriers: H <-> Y hand-offs (all H and Y threads), Y-internal rounds
 constexpr int kBarX2k = 1, kBarG = 2, kBarX2q = 3 /* and 4, by step parity */, kBarYln = 5;
-constexpr int kHY = (kNH + kNY) * 32;
+
+// Warps and shared memory of a CTA that owns kHid / NR hidden units: the whole
+// chain (NR = 1) or one half of it in a two-CTA cluster (NR = 2).
+template <int NR>
+struct Lay {
+    static constexpr int kHidL = kHid / NR;  // hidden units of this CTA
+    static constexpr int kMH = NR == 1 ? 2 : 1;  // 16-unit row blocks per H warp
+    static constexpr int kHW = 16 * kMH;         // hidden units per H warp
+    static constexpr int kNH = kHidL / kHW;      // H warps
+    static constexpr int kWarpY = kWarpH + kNH;
+    static constexpr int kWarps = kWarpY + kNY;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kHY = (kNH + kNY) * 32;
+    // fp16 activation / weight buffers, rows padded by 16 bytes (conflict-free ldmatrix)
+    static constexpr int kHS = kHidL + 8;                    // halves per row of a [*][hidden] buffer
+    static constexpr int kW2hBytes = kD * kHS * 2;           // one fp16 copy of W2, [d][kHS]
+    static constexpr int kOffW2h = kStages * kStageBytes;    // 3 copies: W2_j in buffer j % 3
+    static constexpr int kX2Bytes = kB * kHS * 2;            // one [16][kHS] fp16 activation tile
+    static constexpr int kOffX2k = kOffW2h + 3 * kW2hBytes;  // 3 x gelu(Z1) of the keys, step j in j % 3
+    static constexpr int kOffX2q = kOffX2k + 3 * kX2Bytes;   // 2 x gelu(Z1q), step j in j & 1
+    static constexpr int kOffGh = kOffX2q + 2 * kX2Bytes;    // 2 x [16][kFS] G, step j in j & 1
+    static constexpr int kOffGt = kOffGh + 2 * kGBytes;      // 2 x [16][kFS] A~2 = -(eta/b) G
+    static constexpr int kOffRed = kOffGt + 2 * kGBytes;     // 2 bufs x [2 Y warps][16] float4
+    static constexpr int kOffYq = kOffRed + 2 * kNY * kB * 16;  // 2 slots x [16][kYS] fp32 Yq (Y -> P)
+    static constexpr int kOffMq2 = kOffYq + 2 * kB * kYS * 4;   // 2 x causal x2q.x2k + 1 fragments (P -> Y)
+    // cluster form: the other CTA's Y partial (2 slots x [Y warp][4][32 lanes] float4)
+    static constexpr int kOffYp = kOffMq2 + 2 * 512;
+    static constexpr int kYpBytes = NR == 2 ? 2 * kNY * 4 * 32 * 16 : 0;
+    // cluster form, CTA 0: the other CTA's Yq partial (2 slots x [16][kYS] fp32)
+    static constexpr int kOffYqp = kOffYp + kYpBytes;
+    static constexpr int kYqpBytes = NR == 2 ? 2 * kB * kYS * 4 : 0;
+    static constexpr int kOffTmem = kOffYqp + kYqpBytes;
+    static constexpr int kOffBar = kOffTmem + 16;
+    static constexpr int kNumBars = 3 * kStages + 8 + (NR == 2 ? 6 : 0);
+    static constexpr int kSmem = kOffBar + kNumBars * 8 + 16;
+    static constexpr int kSmemAlloc = kSmem + 1024;
+    // Warp roles: L 0, P 1, H 2..9, Y 10, 11. A warp issues on scheduler
+    // partition warp % 4, and tensor memory lets it reach the lanes of quarter
+    // warp % 4 only: H warps w and w + 4 share a quarter, w + 4 taking the
+    // columns after w's (16 * kMH x 2 per warp: its W2 columns, 64 features).
+    __device__ static int h_index(int warp) { return warp >= kWarpH && warp < kWarpY ? warp - kWarpH : -1; }
+    __device__ static int y_index(int warp) { return warp >= kWarpY && warp < kWarps ? warp - kWarpY : -1; }
+    __device__ static uint32_t tmem_cols(int w) { return (uint32_t)(32 * kMH * (w / 4)); }
+    static constexpr int kYpTx = kNY * 32 * 64;       // bytes of one Y partial
+    static constexpr int kYqpTx = kNY * 32 * 16 * 4;  // bytes of one Yq partial
+};
 constexpr float kGeluA = 0.7978845608028654f;  // sqrt(2/pi)
 constexpr float kGeluC = 0.044715f;
 
 // mbarriers: full/prep/empty (stage ring); hq[2] (H -> P: X2q of step j is
 // written; by step parity, because the H warps may arrive for step j + 1
 // before P has waited for step j, never for step j + 2: that needs G_{j+2},
-// which the Y warps hand over only after P's Gram of step j); mq2 (P -> Y:
-// Gram fragments); yqfull/yqempty[2] (Yq hand-off Y <-> P).
+// which the Y warps hand over only after P's Gram of step j); mq2[2] (P -> Y:
+// Gram fragments of step j in buffer j & 1); yqfull/yqempty[2] (Yq hand-off Y <-> P). Cluster form:
+// ypeer[2] (the other CTA's Y partial of step j landed, slot j & 1), yqpfull[2]
+// (CTA 0: the other CTA's Yq partial landed), yqpempty[2] (CTA 1: CTA 0's P
+// has read the slot).
 struct Ring {
-    uint64_t *full, *prep, *empty, *hq, *mq2, *yqfull, *yqempty;
+    uint64_t *full, *prep, *empty, *hq, *mq2, *yqfull, *yqempty, *ypeer, *yqpfull, *yqpempty;
     volatile int *flags;  // [0] abort, [1] fp16 range violation seen
 };
 
@@ -180,12 +223,26 @@ __device__ __forceinline__ void prep_stage(uint8_t *stg, const uint8_t *stg_prev
                    pack_h2(mq(1, 2), mq(1, 3)));
 }
 
-// P runs the input side two steps ahead of the output side: iteration i preps
-// stage i, then finishes step i - 2 (the X2q X2k^T Gram for the Y warps, and
-// Z = Q + LN(Yq), L_t once the Y warps hand Yq over).
-constexpr int kPrepLead = 2;
-__device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi, size_t tok0, int lane, int nsteps)
+// P runs the input side ahead of the output side: iteration i preps stage i,
+// builds the X2q X2k^T Gram of step i - 2 for the Y warps, then writes the
+// outputs (Z = Q + LN(Yq), L_t) of step i - kOutLag once the Y warps have
+// handed Yq over. In the cluster form kOutLag is 3, not 2, which keeps P's own
+// waits off the recurrence there (its outputs also wait for the other CTA's
+// Yq): the H warps' look-ahead at step i needs stage i + 2 prepared, and the
+// Y warps' output product of step i needs the Gram of step i, neither of which
+// then waits for an output of a step less than two back. (The Gram of step j lands in buffer j & 1: the Y
+// warps may still read step j - 1's when P builds step j's.) In the cluster
+// form the Gram covers this CTA's hidden units (its "+ 1" only in CTA 0), and
+// only CTA 0 writes outputs, from its own Yq plus the one CTA 1 sends. After
+// a failed wait P keeps going in step like the other warps (the cluster's
+// exchanges need every step's arrivals).
+constexpr int kGramLag = 2;
+template <int NR>
+__device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi, size_t tok0, int lane, int nsteps,
+                          int rank)
 {
+    using L = Lay<NR>;
+    constexpr int kOutLag = NR == 1 ? 2 : 3;
     const int g = lane >> 2, c4 = lane & 3;
     uint32_t mag = 0;  // per-halfword max of |bf16 bits|: >= 0x4780 means |x| >= 2^16 (or inf/nan)
     const int tl = lane >> 1, half = lane & 1;  // output side: token and half of the features
@@ -195,17 +252,15 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
         gam[k] = p.ln_g[hi * kD + 32 * half + k];
         bet[k] = p.ln_b[hi * kD + 32 * half + k];
     }
-    const uint32_t sX2k = smem_u32(sm + kOffX2k), sX2q = smem_u32(sm + kOffX2q);
+    const uint32_t sX2k = smem_u32(sm + L::kOffX2k), sX2q = smem_u32(sm + L::kOffX2q);
     const int offQ = p.q_is_k ? kOffK : kOffQ;  // the key tile stands in for the queries
     const float invD = 1.f / (float)kD, eps = p.eps;
-    bool ok = true;
-    for (int i = 0; i < nsteps + kPrepLead && ok; ++i) {
+    const float gram_one = rank == 0 ? 1.f : 0.f;  // the "+ 1" of Mq2 enters once
+    const bool writes_out = NR == 1 || rank == 0;
+    for (int i = 0; i < nsteps + kOutLag; ++i) {
         if (i < nsteps) {
             const int st = i % kStages;
-            if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) {
-                abort_chain(R.flags, p.status);
-                break;
-            }
+            if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) abort_chain(R.flags, p.status);
             if (p.eta_gate && lane < kB) {  // eta = eta_base * sigmoid(logit); 0 past T
                 float *se = reinterpret_cast<float *>(stage_ptr(sm, st) + kOffEta);
                 const int t = i * kB + lane;
@@ -215,60 +270,74 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
                        p.prefix != 0, p.q_is_k != 0);
             warp_arrive(&R.prep[st], lane);
         }
-        if (i < kPrepLead) continue;
-        const int j = i - kPrepLead, stj = j % kStages, slot = j & 1;
-        uint8_t *stg = stage_ptr(sm, stj);
-        // Gram of step j: Mq2[s][t] = (s <= t)(x2q_t . x2k_s + 1) as B fragments (k = s, n = t).
-        if (!wait_bar(&R.hq[j & 1], parity_of(j >> 1), R.flags)) {
-            abort_chain(R.flags, p.status);
-            break;
-        }
-        if (!p.prefix) {  // anchor rule: Yq sees no update of the batch
-            reinterpret_cast<uint4 *>(sm + kOffMq2)[lane] = make_uint4(0u, 0u, 0u, 0u);
-        } else {
-            const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);
-            const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);
-            // four k-slices of independent accumulators (the mma latency, not its rate, bounds this)
-            float dq4[4][2][4] = {};
-            const uint32_t sQj = sX2q + (uint32_t)((j & 1) * kX2Bytes), sKj = sX2k + (uint32_t)((j % 3) * kX2Bytes);
-#pragma unroll
-            for (int ks = 0; ks < kHid / 16; ++ks) {
-                uint32_t aq[4], bk[4];
-                ldsm_x4(aq, hb(sQj, ra, 16 * ks + ca, kHS));
-                ldsm_x4(bk, hb(sKj, rb, 16 * ks + cb, kHS));
-                mma16816(dq4[ks & 3][0], aq, bk[0], bk[1]);
-                mma16816(dq4[ks & 3][1], aq, bk[2], bk[3]);
+        const int jg = i - kGramLag;
+        // Gram of step jg: Mq2[s][t] = (s <= t)(x2q_t . x2k_s + 1) as B fragments (k = s, n = t).
+        if (jg >= 0 && jg < nsteps) {
+            if (!wait_bar(&R.hq[jg & 1], parity_of(jg >> 1), R.flags)) abort_chain(R.flags, p.status);
+            uint4 *mq2 = reinterpret_cast<uint4 *>(sm + L::kOffMq2 + (jg & 1) * 512);
+            if (!p.prefix) {  // anchor rule: Yq sees no update of the batch
+                mq2[lane] = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                const int j = jg;
+                const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);
+                const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);
+                // four k-slices of independent accumulators (the mma latency, not its rate, bounds this)
+                float dq4[4][2][4] = {};
+                const uint32_t sQj = sX2q + (uint32_t)((j & 1) * L::kX2Bytes);
+                const uint32_t sKj = sX2k + (uint32_t)((j % 3) * L::kX2Bytes);
+    #pragma unroll
+                for (int ks = 0; ks < L::kHidL / 16; ++ks) {
+                    uint32_t aq[4], bk[4];
+                    ldsm_x4(aq, hb(sQj, ra, 16 * ks + ca, L::kHS));
+                    ldsm_x4(bk, hb(sKj, rb, 16 * ks + cb, L::kHS));
+                    mma16816(dq4[ks & 3][0], aq, bk[0], bk[1]);
+                    mma16816(dq4[ks & 3][1], aq, bk[2], bk[3]);
+                }
+                float dq[2][4];
+    #pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+    #pragma unroll
+                    for (int r = 0; r < 4; ++r) dq[jj][r] = (dq4[0][jj][r] + dq4[1][jj][r]) + (dq4[2][jj][r] + dq4[3][jj][r]);
+                auto mq = [&](int jj, int r) {
+                    const int t = g + 8 * (r >> 1), s = 8 * jj + 2 * c4 + (r & 1);
+                    return s <= t ? dq[jj][r] + gram_one : 0.f;
+                };
+                mq2[lane] = make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)),
+                                       pack_h2(mq(0, 2), mq(0, 3)), pack_h2(mq(1, 2), mq(1, 3)));
             }
-            float dq[2][4];
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) dq[jj][r] = (dq4[0][jj][r] + dq4[1][jj][r]) + (dq4[2][jj][r] + dq4[3][jj][r]);
-            auto mq = [&](int jj, int r) {
-                const int t = g + 8 * (r >> 1), s = 8 * jj + 2 * c4 + (r & 1);
-                return s <= t ? dq[jj][r] + 1.f : 0.f;
-            };
-            reinterpret_cast<uint4 *>(sm + kOffMq2)[lane] =
-                make_uint4(pack_h2(mq(0, 0), mq(0, 1)), pack_h2(mq(1, 0), mq(1, 1)), pack_h2(mq(0, 2), mq(0, 3)),
-                           pack_h2(mq(1, 2), mq(1, 3)));
+            warp_arrive(&R.mq2[jg & 1], lane);
         }
-        warp_arrive(R.mq2, lane);
+        if (i < kOutLag) continue;
+        const int j = i - kOutLag, stj = j % kStages, slot = j & 1;
+        uint8_t *stg = stage_ptr(sm, stj);
+        if (!writes_out) {
+            warp_arrive(&R.empty[stj], lane);
+            continue;
+        }
         // Output of step j: z = q + LN(yq), L_t = ||z_t - v_t||^2; lane pair per token.
-        if (!wait_bar(&R.yqfull[slot], parity_of(j >> 1), R.flags)) {
-            abort_chain(R.flags, p.status);
-            break;
+        if (!wait_bar(&R.yqfull[slot], parity_of(j >> 1), R.flags)) abort_chain(R.flags, p.status);
+        if constexpr (NR == 2) {  // the other CTA's Yq partial (every step, aborted or not)
+            if (lane == 0) mbar_arrive_expect_tx(&R.yqpfull[slot], L::kYqpTx);
+            if (!wait_peer(&R.yqpfull[slot], parity_of(j >> 1))) abort_chain(R.flags, p.status);
         }
-        const float *ys = reinterpret_cast<const float *>(sm + kOffYq) + slot * kB * kYS + tl * kYS + 32 * half;
+        const float *ys = reinterpret_cast<const float *>(sm + L::kOffYq) + slot * kB * kYS + tl * kYS + 32 * half;
         float yv[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const float4 v = *reinterpret_cast<const float4 *>(ys + 4 * k);
+            float4 v = *reinterpret_cast<const float4 *>(ys + 4 * k);
+            if constexpr (NR == 2) {
+                const float4 u = *reinterpret_cast<const float4 *>(ys + (L::kOffYqp - L::kOffYq) / 4 + 4 * k);
+                v = make_float4(v.x + u.x, v.y + u.y, v.z + u.z, v.w + u.w);
+            }
             yv[4 * k] = v.x;
             yv[4 * k + 1] = v.y;
             yv[4 * k + 2] = v.z;
             yv[4 * k + 3] = v.w;
         }
         warp_arrive(&R.yqempty[slot], lane);
+        if constexpr (NR == 2) {  // the slot may be rewritten by CTA 1
+            if (lane == 0) mbar_arrive_remote(map_shared(smem_u32(&R.yqpempty[slot]), 1));
+        }
         float s = 0.f;
 #pragma unroll
         for (int k = 0; k < 32; ++k) s += yv[k];
@@ -330,53 +399,61 @@ __device__ __forceinline__ uint32_t hb(uint32_t base, int row, int col, int stri
 // H warps, before the main loop: W2 columns h0 + 8nt + 2c4 (+1) of rows
 // 16mf + g (+8) into this warp's tensor-memory columns (fp32 master) and into
 // fp16 buffers 1 and 2 (the copies steps 0 and 1 read as W2_{-2}, W2_{-1}).
+// h0 and the buffers count this CTA's hidden units; hbase is its first one.
+template <int NR>
 __device__ void hidden_init_w2(const MlpParams &p, uint8_t *sm, int w, int warp, int bi, int hi, uint32_t tmem,
-                               int lane)
+                               int lane, int hbase)
 {
+    using L = Lay<NR>;
+    constexpr int MH = L::kMH, NT = 2 * MH;  // 16-unit row blocks, 8-unit column tiles
     const int g = lane >> 2, c4 = lane & 3;
-    const int h0 = 32 * w;
+    const int h0 = L::kHW * w;
     const float *W20 = p.W2 + bi * p.w_bstride + (long long)hi * kD * kHid;
-    const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(w >= 4 ? 64 : 0);
-    uint32_t v[2][32];
+    const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + L::tmem_cols(w);
+    uint32_t v[MH][32];
 #pragma unroll
     for (int mf = 0; mf < 4; ++mf)
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
+        for (int nt = 0; nt < NT; ++nt) {
             const int f0 = 16 * mf + g, hc = h0 + 8 * nt + 2 * c4;
-            const float2 a = *reinterpret_cast<const float2 *>(W20 + f0 * kHid + hc);
-            const float2 b = *reinterpret_cast<const float2 *>(W20 + (f0 + 8) * kHid + hc);
-            const int idx = (mf * 4 + nt) * 4;
+            const float2 a = *reinterpret_cast<const float2 *>(W20 + f0 * kHid + hbase + hc);
+            const float2 b = *reinterpret_cast<const float2 *>(W20 + (f0 + 8) * kHid + hbase + hc);
+            const int idx = (mf * NT + nt) * 4;
             v[idx >> 5][(idx & 31) + 0] = __float_as_uint(a.x);
             v[idx >> 5][(idx & 31) + 1] = __float_as_uint(a.y);
             v[idx >> 5][(idx & 31) + 2] = __float_as_uint(b.x);
             v[idx >> 5][(idx & 31) + 3] = __float_as_uint(b.y);
 #pragma unroll
             for (int buf = 1; buf <= 2; ++buf) {  // W2_{-2} = W2_{-1} = W2_0 (buffers 1 and 2)
-                uint8_t *w2 = sm + kOffW2h + buf * kW2hBytes;
-                *reinterpret_cast<uint32_t *>(w2 + (f0 * kHS + hc) * 2) = pack_h2(a.x, a.y);
-                *reinterpret_cast<uint32_t *>(w2 + ((f0 + 8) * kHS + hc) * 2) = pack_h2(b.x, b.y);
+                uint8_t *w2 = sm + L::kOffW2h + buf * L::kW2hBytes;
+                *reinterpret_cast<uint32_t *>(w2 + (f0 * L::kHS + hc) * 2) = pack_h2(a.x, a.y);
+                *reinterpret_cast<uint32_t *>(w2 + ((f0 + 8) * L::kHS + hc) * 2) = pack_h2(b.x, b.y);
             }
         }
-    tmem_st32(taddr, v[0]);
-    tmem_st32(taddr + 32, v[1]);
+#pragma unroll
+    for (int c = 0; c < MH; ++c) tmem_st32(taddr + 32 * c, v[c]);
     tmem_wait_st();
 }
 
 // ------------------------------------------------------------------ H: hidden-unit warps
+template <int NR>
 __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int w, int warp, int chain, int bi,
-                            int hi, uint32_t tmem, int lane, int nsteps)
+                            int hi, uint32_t tmem, int lane, int nsteps, int hbase)
 {
+    using L = Lay<NR>;
+    constexpr int kHS = L::kHS, kHY = L::kHY, kX2Bytes = L::kX2Bytes, kW2hBytes = L::kW2hBytes;
+    constexpr int MH = L::kMH, NT = 2 * MH;  // 16-unit row blocks, 8-unit column tiles
     const int g = lane >> 2, c4 = lane & 3;
-    const int h0 = 32 * w;  // first hidden unit of this warp
+    const int h0 = L::kHW * w;  // first hidden unit of this warp among the CTA's (hbase + h0 of the chain's)
     const int offQh = p.q_is_k ? kOffKh : kOffQh;  // the key tile stands in for the queries
     const float *W10 = p.W1 + bi * p.w_bstride + (long long)hi * kHid * kD;
     const float *c10 = p.c1 + bi * p.c1_bstride + (long long)hi * kHid;
-    // W1 rows h0 + 16m + g (+8), columns 8nt + 2c4 (+1)
-    float W1a[2][8][4];
-    float c1v[2][2];
+    // W1 rows hbase + h0 + 16m + g (+8), columns 8nt + 2c4 (+1)
+    float W1a[MH][8][4];
+    float c1v[MH][2];
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const int r0 = h0 + 16 * m + g;
+    for (int m = 0; m < MH; ++m) {
+        const int r0 = hbase + h0 + 16 * m + g;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
             const float2 a = *reinterpret_cast<const float2 *>(W10 + r0 * kD + 8 * nt + 2 * c4);
@@ -390,9 +467,10 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
         c1v[m][1] = c10[r0 + 8];
     }
     // This warp's 64 tensor-memory columns: lanes of its quarter, columns 0 or 64.
-    const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(w >= 4 ? 64 : 0);
-    const uint32_t sW2h = smem_u32(sm + kOffW2h), sX2k = smem_u32(sm + kOffX2k), sX2q = smem_u32(sm + kOffX2q);
-    const uint32_t sGh = smem_u32(sm + kOffGh), sGt = smem_u32(sm + kOffGt);
+    const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + L::tmem_cols(w);
+    const uint32_t sW2h = smem_u32(sm + L::kOffW2h), sX2k = smem_u32(sm + L::kOffX2k);
+    const uint32_t sX2q = smem_u32(sm + L::kOffX2q);
+    const uint32_t sGh = smem_u32(sm + L::kOffGh), sGt = smem_u32(sm + L::kOffGt);
     const int rb = (lane & 7) + (lane >> 4) * 8, cb16 = (lane >> 3) & 1;  // non-transposed B fragment rows
     const int rt = (lane & 7) + ((lane >> 3) & 1) * 8, ct = lane >> 4;   // transposed B fragment rows
     const int srow = (lane & 7) + 8 * (lane >> 4), scol = 8 * ((lane >> 3) & 1);  // stmatrix / trans-A rows
@@ -403,10 +481,10 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
     };
     // acc = c1 + W1 tile^T for this warp's 32 hidden units, for one or two tiles at
     // once (W1 packed to fp16 on the fly, once for both).
-    auto w1_gemm2 = [&](uint32_t tile0, float (&acc0)[2][2][4], uint32_t tile1, float (&acc1)[2][2][4],
+    auto w1_gemm2 = [&](uint32_t tile0, float (&acc0)[MH][2][4], uint32_t tile1, float (&acc1)[MH][2][4],
                         bool two) {
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < MH; ++m)
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -417,7 +495,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             ldsm_x4(bk, tile0 + swz(rb, 2 * ks + cb16));
             if (two) ldsm_x4(bq, tile1 + swz(rb, 2 * ks + cb16));
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
+            for (int m = 0; m < MH; ++m) {
                 const uint32_t af[4] = {pack_h2(W1a[m][2 * ks][0], W1a[m][2 * ks][1]),
                                         pack_h2(W1a[m][2 * ks][2], W1a[m][2 * ks][3]),
                                         pack_h2(W1a[m][2 * ks + 1][0], W1a[m][2 * ks + 1][1]),
@@ -432,19 +510,19 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
         }
     };
     // this warp's hidden columns of an activation tile [16 t][hidden] (fp16)
-    auto write_x = [&](uint32_t base, const float (&x)[2][2][4]) {
+    auto write_x = [&](uint32_t base, const float (&x)[MH][2][4]) {
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < MH; ++m)
             stsm_x4_t(hb(base, srow, h0 + 16 * m + scol, kHS), pack_h2(x[m][0][0], x[m][0][1]),
                       pack_h2(x[m][0][2], x[m][0][3]), pack_h2(x[m][1][0], x[m][1][1]),
                       pack_h2(x[m][1][2], x[m][1][3]));
     };
     // Prologue: Z1_0 = W1_0 K_0^T + c1_0, Rq1_0, and S1_1 = W1_0 K_1^T + c1_0.
-    float z1[2][2][4], s1[2][2][4], rq[2][2][4];
-    __half2 gp[2][2][2];  // gelu'(Z1) of the next step, fp16 pairs (it only scales an fp16-rounded value)
-    auto gelu_x = [&](float (&x)[2][2][4]) {  // x <- gelu(x), gp <- gelu'(x)
+    float z1[MH][2][4], s1[MH][2][4], rq[MH][2][4];
+    __half2 gp[MH][2][2];  // gelu'(Z1) of the next step, fp16 pairs (it only scales an fp16-rounded value)
+    auto gelu_x = [&](float (&x)[MH][2][4]) {  // x <- gelu(x), gp <- gelu'(x)
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < MH; ++m)
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -477,13 +555,13 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
         // G1pre^T = W2_{i-1}^T G_i^T (W2 columns of buffer (i+2) % 3, transposed as the A operand).
         const uint32_t sW2p = sW2h + (uint32_t)(((i + 2) % 3) * kW2hBytes);
         const uint32_t sG = sGh + (uint32_t)((i & 1) * kGBytes);
-        float gg[2][2][4] = {}, gg2[2][2][4] = {};  // even / odd k-steps: two independent chains each
+        float gg[MH][2][4] = {}, gg2[MH][2][4] = {};  // even / odd k-steps: two independent chains each
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
             uint32_t bg[4];
             ldsm_x4(bg, hb(sG, rb, 16 * ks + 8 * cb16, kFS));
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
+            for (int m = 0; m < MH; ++m) {
                 uint32_t aw[4];
                 ldsm_x4_t(aw, hb(sW2p, 16 * ks + srow, h0 + 16 * m + scol, kHS));
                 mma16816(ks & 1 ? gg2[m][0] : gg[m][0], aw, bg[0], bg[1]);
@@ -491,7 +569,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             }
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < MH; ++m)
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -506,9 +584,9 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             es[n][0] = -e2.x * (1.f / (float)kB);
             es[n][1] = -e2.y * (1.f / (float)kB);
         }
-        uint32_t af1[2][4];
+        uint32_t af1[MH][4];
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
+        for (int m = 0; m < MH; ++m) {
             float a[2][4];
 #pragma unroll
             for (int n = 0; n < 2; ++n)
@@ -536,7 +614,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
             // The chain: Z1_{i+1}^T = S1_{i+1} + A~1_i (K_i K_{i+1}^T + 1), X2k_{i+1} -> Y warps.
             const uint4 kx = reinterpret_cast<const uint4 *>(stage_ptr(sm, (i + 1) % kStages) + kOffKx)[lane];
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
+            for (int m = 0; m < MH; ++m) {
 #pragma unroll
                 for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -553,13 +631,13 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
         {
             const uint4 mq = reinterpret_cast<const uint4 *>(stg + kOffMq)[lane];
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
+            for (int m = 0; m < MH; ++m) {
                 mma16816(rq[m][0], af1[m], mq.x, mq.y);
                 mma16816(rq[m][1], af1[m], mq.z, mq.w);
             }
         }
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < MH; ++m)
 #pragma unroll
             for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -575,7 +653,7 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
                 uint32_t bt[4];
                 ldsm_x4_t(bt, sK + swz(rt, 2 * j + ct));
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
+                for (int m = 0; m < MH; ++m) {
                     mma16816(W1a[m][2 * j], af1[m], bt[0], bt[1]);
                     mma16816(W1a[m][2 * j + 1], af1[m], bt[2], bt[3]);
                 }
@@ -583,28 +661,28 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
         }
         if (w == 0) TTT_TRACE_AT(p, i, 5);
         // W2_i = W2_{i-1} + A~2_i^T X2k_i (rows f, this warp's hidden columns): the fp32
-        // master goes through tensor memory (two halves of 32 columns: features 0-31,
-        // 32-63), the fp16 copy to buffer i % 3.
+        // master goes through tensor memory in chunks of 32 columns (MH of them: 4 / MH
+        // feature blocks of 16 each), the fp16 copy to buffer i % 3.
         if (commit) {
-            uint32_t bx[2][4];  // B = X2k_i (k = t, n = h), two pairs of n-tiles
+            uint32_t bx[MH][4];  // B = X2k_i (k = t, n = h), pairs of n-tiles
             const uint32_t sXk = sX2k + (uint32_t)((i % 3) * kX2Bytes);
 #pragma unroll
-            for (int q = 0; q < 2; ++q) ldsm_x4_t(bx[q], hb(sXk, rt, h0 + 16 * q + 8 * ct, kHS));
-            uint8_t *w2 = sm + kOffW2h + (i % 3) * kW2hBytes;
+            for (int q = 0; q < MH; ++q) ldsm_x4_t(bx[q], hb(sXk, rt, h0 + 16 * q + 8 * ct, kHS));
+            uint8_t *w2 = sm + L::kOffW2h + (i % 3) * kW2hBytes;
             const uint32_t sGa = sGt + (uint32_t)((i & 1) * kGBytes);
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            for (int hf = 0; hf < MH; ++hf) {
                 uint32_t v[32];
                 tmem_ld32(taddr + 32 * hf, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int mh = 0; mh < 2; ++mh) {
-                    const int mf = 2 * hf + mh;
+                for (int mh = 0; mh < 4 / MH; ++mh) {
+                    const int mf = (4 / MH) * hf + mh;
                     uint32_t ag[4];  // A = A~2 (rows f, columns t) from Gt[t][f], transposed
                     ldsm_x4_t(ag, hb(sGa, srow, 16 * mf + scol, kFS));
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt) {
-                        uint32_t *vv = &v[(mh * 4 + nt) * 4];
+                    for (int nt = 0; nt < NT; ++nt) {
+                        uint32_t *vv = &v[(mh * NT + nt) * 4];
                         float acc[4] = {__uint_as_float(vv[0]), __uint_as_float(vv[1]), __uint_as_float(vv[2]),
                                         __uint_as_float(vv[3])};
                         mma16816(acc, ag, bx[nt >> 1][2 * (nt & 1)], bx[nt >> 1][2 * (nt & 1) + 1]);
@@ -634,8 +712,8 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
     bool bad = false;
     const size_t ch = (size_t)chain;
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const int r0 = h0 + 16 * m + g;
+    for (int m = 0; m < MH; ++m) {
+        const int r0 = hbase + h0 + 16 * m + g;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
@@ -656,21 +734,21 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
         }
     }
     {
-        uint32_t v[2][32];
-        tmem_ld32(taddr, v[0]);
-        tmem_ld32(taddr + 32, v[1]);
+        uint32_t v[MH][32];
+#pragma unroll
+        for (int c = 0; c < MH; ++c) tmem_ld32(taddr + 32 * c, v[c]);
         tmem_wait_ld();
 #pragma unroll
         for (int mf = 0; mf < 4; ++mf)
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int idx = (mf * 4 + nt) * 4;
+            for (int nt = 0; nt < NT; ++nt) {
+                const int idx = (mf * NT + nt) * 4;
                 const float a0 = __uint_as_float(v[idx >> 5][idx & 31]), a1v = __uint_as_float(v[idx >> 5][(idx & 31) + 1]);
                 const float b0 = __uint_as_float(v[idx >> 5][(idx & 31) + 2]), b1 = __uint_as_float(v[idx >> 5][(idx & 31) + 3]);
                 bad |= !isfinite(a0) || !isfinite(a1v) || !isfinite(b0) || !isfinite(b1);
                 if (p.W2_out) {
                     float *Wo = p.W2_out + ch * kD * kHid;
-                    const int f0 = 16 * mf + g, hc = h0 + 8 * nt + 2 * c4;
+                    const int f0 = 16 * mf + g, hc = hbase + h0 + 8 * nt + 2 * c4;
                     *reinterpret_cast<float2 *>(Wo + f0 * kHid + hc) = make_float2(a0, a1v);
                     *reinterpret_cast<float2 *>(Wo + (f0 + 8) * kHid + hc) = make_float2(b0, b1);
                 }
@@ -759,15 +837,18 @@ __device__ __forceinline__ void y_sum3(float (&a)[2][2], float (&b)[2][2], float
         }
 }
 
-// Y^T (rows f0..f0+31, 16 token columns) += W2 (fp16 buffer) X^T over all hidden
-// units; even and odd k-steps go to separate accumulators (8 independent chains).
+// Y^T (rows f0..f0+31, 16 token columns) += W2 (fp16 buffer) X^T over the CTA's
+// hidden units; even and odd k-steps go to separate accumulators (8 independent chains).
+template <int NR>
 __device__ __forceinline__ void y_gemm(uint32_t sW2, uint32_t sX, int f0, int lane, float (&acc)[2][2][4])
 {
+    using L = Lay<NR>;
+    constexpr int kHS = L::kHS;
     const int ra = (lane & 7) + ((lane >> 3) & 1) * 8, ca = 8 * (lane >> 4);   // A rows (non-transposed)
     const int rb = (lane & 7) + (lane >> 4) * 8, cb = 8 * ((lane >> 3) & 1);   // B rows (non-transposed)
     float acc2[2][2][4] = {};
 #pragma unroll 4
-    for (int ks = 0; ks < kHid / 16; ks += 2) {
+    for (int ks = 0; ks < L::kHidL / 16; ks += 2) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             uint32_t bx[4];
@@ -792,10 +873,17 @@ __device__ __forceinline__ void y_gemm(uint32_t sW2, uint32_t sX, int f0, int la
 // Y warps. Iteration i first runs step i's part of the recurrence (Y from the
 // look-ahead, LayerNorm backward, G and A~2 to the H warps), then the output
 // product of step i - 1 (Yq = X2q W2^T + c2 + A~2 Mq2, handed to P), which is
-// off the recurrence and overlaps the H warps' work on step i.
+// off the recurrence and overlaps the H warps' work on step i. In the cluster
+// form both products are this CTA's partials: the Y partial goes to the other
+// CTA and comes back as the sum before the LayerNorm; CTA 1 sends its Yq
+// partial to CTA 0 instead of handing it to its own P.
+template <int NR>
 __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, int chain, int bi, int hi, size_t tok0,
-                       int lane, int nsteps)
+                       int lane, int nsteps, int rank)
 {
+    using L = Lay<NR>;
+    constexpr int kHS = L::kHS, kHY = L::kHY, kX2Bytes = L::kX2Bytes, kW2hBytes = L::kW2hBytes;
+    const bool lead = NR == 1 || rank == 0;  // adds c2 to Yq, writes inner_loss and c2_out
     const int g = lane >> 2, c4 = lane & 3;
     const int f0 = 32 * y;  // first output feature of this warp
     const float *c20 = p.c2 + bi * p.c2_bstride + (long long)hi * kD;
@@ -809,9 +897,10 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
             gam[m][u] = p.ln_g[hi * kD + f];
             bet[m][u] = p.ln_b[hi * kD + f];
         }
-    const uint32_t sW2h = smem_u32(sm + kOffW2h), sX2k = smem_u32(sm + kOffX2k), sX2q = smem_u32(sm + kOffX2q);
-    const uint32_t sGh = smem_u32(sm + kOffGh), sGt = smem_u32(sm + kOffGt);
-    float4 *red = reinterpret_cast<float4 *>(sm + kOffRed);
+    const uint32_t sW2h = smem_u32(sm + L::kOffW2h), sX2k = smem_u32(sm + L::kOffX2k);
+    const uint32_t sX2q = smem_u32(sm + L::kOffX2q);
+    const uint32_t sGh = smem_u32(sm + L::kOffGh), sGt = smem_u32(sm + L::kOffGt);
+    float4 *red = reinterpret_cast<float4 *>(sm + L::kOffRed);
     int rnd = 0;
     const int rbt = (lane & 7) + (lane >> 4) * 8, cbt = (lane >> 3) & 1;        // ldmatrix.trans of a tile
     const int srow = (lane & 7) + 8 * (lane >> 4), scol = 8 * ((lane >> 3) & 1);  // stmatrix rows
@@ -862,20 +951,20 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
             // Y^T = W2_{i-1} X2k^T + c2_{i-1}, read as W2_{i-2} X2k^T + c2_{i-1} + A~2_{i-1} (X2k_{i-1} X2k^T)
             // so that the W2 update of step i-1 is off this path.
             const uint32_t sXk = sX2k + (uint32_t)((i % 3) * kX2Bytes);
-            float yk[2][2][4];
+            float yk[2][2][4];  // NR = 2: this CTA's partial, c2 added after the exchange
 #pragma unroll
             for (int m = 0; m < 2; ++m)
 #pragma unroll
                 for (int n = 0; n < 2; ++n)
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) yk[m][n][r] = c2v[m][r >> 1];
-            y_gemm(sW2h + (uint32_t)(((i + 1) % 3) * kW2hBytes), sXk, f0, lane, yk);
+                    for (int r = 0; r < 4; ++r) yk[m][n][r] = NR == 1 ? c2v[m][r >> 1] : 0.f;
+            y_gemm<NR>(sW2h + (uint32_t)(((i + 1) % 3) * kW2hBytes), sXk, f0, lane, yk);
             if (i > 0) {
                 // dx[j][r] = x2_t . x2'_s, t in step i (rows), s in step i-1; four k-slices
                 const uint32_t sXp = sX2k + (uint32_t)(((i + 2) % 3) * kX2Bytes);
                 float dx4[4][2][4] = {};
 #pragma unroll
-                for (int ks = 0; ks < kHid / 16; ++ks) {
+                for (int ks = 0; ks < L::kHidL / 16; ++ks) {
                     uint32_t ax[4], bp[4];
                     ldsm_x4(ax, hb(sXk, ra, 16 * ks + ca, kHS));
                     ldsm_x4(bp, hb(sXp, rb, 16 * ks + cb, kHS));
@@ -894,6 +983,36 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
                 for (int m = 0; m < 2; ++m) {
                     mma16816(yk[m][0], a2f[m], bx[0], bx[1]);
                     mma16816(yk[m][1], a2f[m], bx[2], bx[3]);
+                }
+            }
+            if constexpr (NR == 2) {
+                // Exchange the partials: ours into the other CTA's slot i & 1 ([Y warp][4][lane]
+                // float4), then theirs from our own slot; Y = (ours + theirs) + c2, the same
+                // value in both CTAs.
+                const int slot = i & 1;
+                float4 *yp = reinterpret_cast<float4 *>(sm + L::kOffYp) + (slot * kNY + y) * 4 * 32 + lane;
+                const uint32_t peer = (uint32_t)(rank ^ 1);
+                const uint32_t rdst = map_shared(smem_u32(yp), peer);
+                const uint32_t rbar = map_shared(smem_u32(&R.ypeer[slot]), peer);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float *v = yk[q >> 1][q & 1];
+                    st_async_v4(rdst + (uint32_t)(q * 32 * 16),
+                                make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                                           __float_as_uint(v[3])),
+                                rbar);
+                }
+                if (y == 0 && lane == 0) mbar_arrive_expect_tx(&R.ypeer[slot], L::kYpTx);
+                if (!wait_peer(&R.ypeer[slot], parity_of(i >> 1))) abort_chain(R.flags, p.status);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 u = yp[q * 32];
+                    float *v = yk[q >> 1][q & 1];
+                    const int m = q >> 1;
+                    v[0] = (v[0] + u.x) + c2v[m][0];
+                    v[1] = (v[1] + u.y) + c2v[m][0];
+                    v[2] = (v[2] + u.z) + c2v[m][1];
+                    v[3] = (v[3] + u.w) + c2v[m][1];
                 }
             }
             if (y == 0) TTT_TRACE_AT(p, i, 10);
@@ -943,7 +1062,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
             }
             named_bar_arrive(kBarG, kHY);
             if (y == 0) TTT_TRACE_AT(p, i, 11);
-            if (p.inner_loss && y == 0 && g == 0) {
+            if (p.inner_loss && lead && y == 0 && g == 0) {
 #pragma unroll
                 for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -982,11 +1101,12 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
 #pragma unroll
                 for (int n = 0; n < 2; ++n)
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) yq[m][n][r] = c2p[m][r >> 1];
-            y_gemm(sW2h + (uint32_t)(((j + 2) % 3) * kW2hBytes), sX2q + (uint32_t)((j & 1) * kX2Bytes), f0, lane, yq);
-            if (!wait_bar(R.mq2, parity_of(j), R.flags)) abort_chain(R.flags, p.status);
+                    for (int r = 0; r < 4; ++r) yq[m][n][r] = lead ? c2p[m][r >> 1] : 0.f;
+            y_gemm<NR>(sW2h + (uint32_t)(((j + 2) % 3) * kW2hBytes), sX2q + (uint32_t)((j & 1) * kX2Bytes), f0, lane,
+                       yq);
+            if (!wait_bar(&R.mq2[j & 1], parity_of(j >> 1), R.flags)) abort_chain(R.flags, p.status);
             {
-                const uint4 mq2 = reinterpret_cast<const uint4 *>(sm + kOffMq2)[lane];
+                const uint4 mq2 = reinterpret_cast<const uint4 *>(sm + L::kOffMq2 + (j & 1) * 512)[lane];
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
                     mma16816(yq[m][0], a2f[m], mq2.x, mq2.y);
@@ -995,16 +1115,33 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
             }
             if (y == 0) TTT_TRACE_AT(p, j, 13);
             const int slot = j & 1;
-            if (!wait_bar(&R.yqempty[slot], parity_of(j >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
-            float *ys = reinterpret_cast<float *>(sm + kOffYq) + slot * kB * kYS;
+            if (lead) {
+                if (!wait_bar(&R.yqempty[slot], parity_of(j >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
+                float *ys = reinterpret_cast<float *>(sm + L::kOffYq) + slot * kB * kYS;
 #pragma unroll
-            for (int m = 0; m < 2; ++m)
+                for (int m = 0; m < 2; ++m)
 #pragma unroll
-                for (int n = 0; n < 2; ++n)
+                    for (int n = 0; n < 2; ++n)
 #pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        ys[(8 * n + 2 * c4 + (r & 1)) * kYS + f0 + 16 * m + g + 8 * (r >> 1)] = yq[m][n][r];
-            warp_arrive(&R.yqfull[slot], lane);
+                        for (int r = 0; r < 4; ++r)
+                            ys[(8 * n + 2 * c4 + (r & 1)) * kYS + f0 + 16 * m + g + 8 * (r >> 1)] = yq[m][n][r];
+                warp_arrive(&R.yqfull[slot], lane);
+            } else if constexpr (NR == 2) {
+                // CTA 1: the partial goes to CTA 0's slot, same [token][feature] layout, once
+                // CTA 0's P has read what was there (every step, aborted or not).
+                if (!wait_peer(&R.yqpempty[slot], parity_of(j >> 1) ^ 1u)) abort_chain(R.flags, p.status);
+                const uint32_t rys = map_shared(smem_u32(sm + L::kOffYqp + slot * kB * kYS * 4), 0);
+                const uint32_t rbar = map_shared(smem_u32(&R.yqpfull[slot]), 0);
+#pragma unroll
+                for (int m = 0; m < 2; ++m)
+#pragma unroll
+                    for (int n = 0; n < 2; ++n)
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            st_async_b32(rys + (uint32_t)(((8 * n + 2 * c4 + (r & 1)) * kYS + f0 + 16 * m + g +
+                                                           8 * (r >> 1)) * 4),
+                                         __float_as_uint(yq[m][n][r]), rbar);
+            }
             if (y == 0) TTT_TRACE_AT(p, j, 14);
         }
         if (i < nsteps) {
@@ -1026,35 +1163,41 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             bad |= !isfinite(c2v[m][u]);
-            if (p.c2_out && c4 == 0) p.c2_out[(size_t)chain * kD + f0 + 16 * m + g + 8 * u] = c2v[m][u];
+            if (p.c2_out && lead && c4 == 0) p.c2_out[(size_t)chain * kD + f0 + 16 * m + g + 8 * u] = c2v[m][u];
         }
     if (__any_sync(kFull, bad) && lane == 0) record(p.status, TTT_ERR_NONFINITE);
 }
 
 // ------------------------------------------------------------------ kernel
-__global__ void __launch_bounds__(kThreads, 1)
-mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const MlpParams p)
+template <int NR>
+__device__ __forceinline__ void mlp_tc_body(const CUtensorMap *tmQ, const CUtensorMap *tmK, const CUtensorMap *tmV,
+                                            const MlpParams &p)
 {
+    using L = Lay<NR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = smem_align1024(smem_raw);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int chain = blockIdx.x;
+    const int rank = NR == 2 ? (int)cluster_ctarank() : 0;
+    const int chain = blockIdx.x / NR;
     const int bi = chain / p.H, hi = chain % p.H;
     const int nsteps = (p.T + kB - 1) / kB;  // a partial last step (T % 16 tokens) is not committed
     const size_t tok0 = (size_t)chain * p.T;
+    const int hbase = rank * L::kHidL;  // first hidden unit of this CTA
 
     Ring R;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kOffBar);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kOffBar);
     R.full = bar;
     R.prep = bar + kStages;
     R.empty = bar + 2 * kStages;
     R.hq = bar + 3 * kStages;
     R.mq2 = R.hq + 2;
-    R.yqfull = R.hq + 3;
-    R.yqempty = R.hq + 5;
-    R.flags = reinterpret_cast<volatile int *>(bar + kNumBars);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffTmem);
+    R.yqfull = R.hq + 4;
+    R.yqempty = R.hq + 6;
+    R.ypeer = R.hq + 8;  // cluster form only (the next six)
+    R.yqpfull = R.hq + 10;
+    R.yqpempty = R.hq + 12;
+    R.flags = reinterpret_cast<volatile int *>(bar + L::kNumBars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::kOffTmem);
 
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -1062,16 +1205,21 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
     if (threadIdx.x == 32) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&R.full[s], 33);               // expect_tx arrive + 32 cp.async arrivals
+            mbar_init(&R.full[s], 33);                 // expect_tx arrive + 32 cp.async arrivals
             mbar_init(&R.prep[s], 1);
-            mbar_init(&R.empty[s], kNH + kNY + 1);  // H warps, Y warps, P
+            mbar_init(&R.empty[s], L::kNH + kNY + 1);  // H warps, Y warps, P
         }
-        mbar_init(&R.hq[0], kNH);
-        mbar_init(&R.hq[1], kNH);
-        mbar_init(R.mq2, 1);
+        mbar_init(&R.hq[0], L::kNH);
+        mbar_init(&R.hq[1], L::kNH);
         for (int j = 0; j < 2; ++j) {
+            mbar_init(&R.mq2[j], 1);
             mbar_init(&R.yqfull[j], kNY);
             mbar_init(&R.yqempty[j], 1);
+            if (NR == 2) {
+                mbar_init(&R.ypeer[j], 1);     // Y warp 0's expect_tx arrival + the peer's bytes
+                mbar_init(&R.yqpfull[j], 1);   // P's expect_tx arrival + the peer's bytes
+                mbar_init(&R.yqpempty[j], 1);  // CTA 0's P, remotely
+            }
         }
         R.flags[0] = 0;
         R.flags[1] = 0;
@@ -1082,15 +1230,17 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tmem_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp >= kWarpH && warp < kWarpY) hidden_init_w2(p, sm, warp - kWarpH, warp, bi, hi, tmem, lane);
+    const int hw = L::h_index(warp), yw = L::y_index(warp);
+    if (hw >= 0) hidden_init_w2<NR>(p, sm, hw, warp, bi, hi, tmem, lane, hbase);
     tmem_fence_before_sync();
     __syncthreads();  // (1) initial W2 copies visible; tensor-memory stores complete
     tmem_fence_after_sync();
+    if constexpr (NR == 2) cluster_sync();  // both CTAs' barriers are initialised before any remote use
 
     if (warp == kWarpL) {
         const StageGeom geom{kStages, kStageBytes, kOffK, p.q_is_k ? -1 : kOffQ, kOffV, kOffEta};
-        role_loader<kD>(&tmQ, &tmK, &tmV, p.eta + tok0, p.T, p.status, sm + kOffStages, geom, R.full, R.empty,
-                        R.flags, chain, lane, nsteps,
+        role_loader<kD>(tmQ, tmK, tmV, p.eta + tok0, p.T, p.status, sm + kOffStages, geom, R.full, R.empty, R.flags,
+                        chain, lane, nsteps,
 #ifdef TTT_FAULT_HOOKS
                         p.drop_step
 #else
@@ -1098,18 +1248,57 @@ mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #endif
         );
     } else if (warp == kWarpP) {
-        role_prep(p, sm, R, hi, tok0, lane, nsteps);
-    } else if (warp < kWarpY) {
-        role_hidden(p, sm, R, warp - kWarpH, warp, chain, bi, hi, tmem, lane, nsteps);
-    } else {
-        role_y(p, sm, R, warp - kWarpY, chain, bi, hi, tok0, lane, nsteps);
+        role_prep<NR>(p, sm, R, hi, tok0, lane, nsteps, rank);
+    } else if (hw >= 0) {
+        role_hidden<NR>(p, sm, R, hw, warp, chain, bi, hi, tmem, lane, nsteps, hbase);
+    } else if (yw >= 0) {
+        role_y<NR>(p, sm, R, yw, chain, bi, hi, tok0, lane, nsteps, rank);
     }
     tmem_fence_before_sync();
     __syncthreads();  // (2) every tensor-memory access is complete
+    // Cluster form: every store and arrival one CTA makes in the other's shared memory
+    // was waited for by the other (the exchanges run every step), so neither leaves
+    // while the other may still write to it.
+    if constexpr (NR == 2) cluster_sync();
     if (warp == 0) {
         tmem_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+__global__ void __launch_bounds__(Lay<1>::kThreads, 1)
+mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const MlpParams p)
+{
+    mlp_tc_body<1>(&tmQ, &tmK, &tmV, p);
+}
+
+// One chain per cluster of two CTAs (blocks 2c and 2c + 1), hidden units split.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<2>::kThreads, 1)
+mlp_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const MlpParams p)
+{
+    mlp_tc_body<2>(&tmQ, &tmK, &tmV, p);
+}
+
+std::atomic<int> g_mlp_cluster_mode{1};
+
+// The cluster form runs when every chain gets its pair of SMs in one wave
+// (mode 1, the default), always (2) or never (0).
+bool mlp_use_cluster_form(int chains)
+{
+    const int mode = g_mlp_cluster_mode.load(std::memory_order_relaxed);
+    if (mode == 0) return false;
+    if (mode == 2) return true;
+    static std::atomic<int> sms[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    int n = sms[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        sms[dev].store(n, std::memory_order_relaxed);
+    }
+    return 2 * chains <= n;
 }
 
 }  // namespace
@@ -1119,15 +1308,27 @@ bool mlp_tc_supported(int io, int d, int hidden, int mb)
     return io == TTT_BF16 && d == kD && hidden == kHid && mb == kB;
 }
 
+int mlp_cluster_mode(int mode)
+{
+    if (mode >= 0 && mode <= 2) g_mlp_cluster_mode.store(mode, std::memory_order_relaxed);
+    return g_mlp_cluster_mode.load(std::memory_order_relaxed);
+}
+
 cudaError_t launch_mlp_tc(const MlpParams &p, int chains, cudaStream_t s)
 {
     CUtensorMap mQ, mK, mV;
     if (!make_map(&mQ, p.Q, kD, p.T, chains, 16) || !make_map(&mK, p.K, kD, p.T, chains, 16) ||
         !make_map(&mV, p.V, kD, p.T, chains, 16))
         return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem<mlp_tc_kernel>(kSmemAlloc);
+    if (mlp_use_cluster_form(chains)) {
+        cudaError_t e = ensure_smem<mlp_tc_cluster_kernel>(Lay<2>::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        mlp_tc_cluster_kernel<<<2 * chains, Lay<2>::kThreads, Lay<2>::kSmemAlloc, s>>>(mQ, mK, mV, p);
+        return cudaGetLastError();
+    }
+    cudaError_t e = ensure_smem<mlp_tc_kernel>(Lay<1>::kSmemAlloc);
     if (e != cudaSuccess) return e;
-    mlp_tc_kernel<<<chains, kThreads, kSmemAlloc, s>>>(mQ, mK, mV, p);
+    mlp_tc_kernel<<<chains, Lay<1>::kThreads, Lay<1>::kSmemAlloc, s>>>(mQ, mK, mV, p);
     return cudaGetLastError();
 }
 

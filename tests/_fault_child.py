@@ -55,7 +55,11 @@ def run_mlp(inp):
 
 
 _, res["linear_status"], res["linear_s"] = run_linear(lin)
+ttt.mlp_cluster_mode(0)   # one CTA per chain
 _, res["mlp_status"], res["mlp_s"] = run_mlp(mlp)
+ttt.mlp_cluster_mode(2)   # two-CTA clusters: both CTAs time out, their exchanges stay in step
+_, res["mlp_cluster_status"], res["mlp_cluster_s"] = run_mlp(mlp)
+ttt.mlp_cluster_mode(1)
 res["hook_off"] = L.ttt_debug_drop_load(-1)
 o, res["after_status"], _ = run_linear(lin)
 res["after_err"] = rel_err(to_np(o["Z"]), oracle_linear(lin)["Z"])

@@ -39,3 +39,15 @@ def linear_form(request):
     ttt.linear_cluster_mode(request.param)
     yield request.param
     ttt.linear_cluster_mode(0)
+
+
+@pytest.fixture(params=[0, 2], ids=["one_cta", "cluster"])
+def mlp_form(request):
+    """Runs a test with each form of the tensor-core TTT-MLP kernel: one CTA per
+    chain (0) and the two-CTA cluster with the hidden units split (2). The
+    default (1: the cluster when the chains fit half the SMs) comes back
+    afterwards."""
+    import test_weight_sequence_ttt_b300 as ttt
+    ttt.mlp_cluster_mode(request.param)
+    yield request.param
+    ttt.mlp_cluster_mode(1)

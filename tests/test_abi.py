@@ -44,7 +44,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_version_and_strings(L):
-    assert ttt.abi_version() == 9
+    assert ttt.abi_version() == 10
     for code in ttt.STATUS:
         assert len(ttt.status_string(code)) > 0
     assert ttt.status_string(999) == "unknown status"

@@ -43,7 +43,7 @@ def test_linear_gate(d, b, T, io, linear_form):
 
 
 @pytest.mark.parametrize("d,h,b,T,io", [(64, 256, 16, 48, "bf16"), (64, 256, 16, 40, "bf16"), (16, 48, 4, 24, "f32")])
-def test_mlp_gate(d, h, b, T, io):
+def test_mlp_gate(d, h, b, T, io, mlp_form):
     tail = T % b != 0
     w = WORKLOADS["mlp_b4h12_d64_t8k"].with_(B=1, H=2, T=T, d=d, hidden=h, b=b, io=io, seed=700 + T, eta_base=0.6,
                                              partial_tail=tail)

@@ -27,20 +27,20 @@ def test_mlp_f32(d, h, b, T):
 
 
 @pytest.mark.parametrize("d,h,b,T", [(64, 256, 16, 64), (64, 256, 4, 40)])
-def test_mlp_bf16(d, h, b, T):
+def test_mlp_bf16(d, h, b, T, mlp_form):
     inp = _small(d, h, b, T)
     got = run_mlp(inp)
     assert int(got["status"].item()) == 0
     compare(got, oracle_mlp(inp), KEYS, TOL["bf16"])
 
 
-def test_mlp_bf16_z_output():
+def test_mlp_bf16_z_output(mlp_form):
     inp = _small(64, 256, 16, 32)
     got = run_mlp(inp, z_dtype=torch.bfloat16)
     check_bf16_z(got["Z"], oracle_mlp(inp)["Z"], TOL["bf16"])
 
 
-def test_mlp_full_size_sampled_chains():
+def test_mlp_full_size_sampled_chains(mlp_form):
     w = WORKLOADS["mlp_b4h12_d64_t8k"]
     inp = make_inputs(w)
     got = run_mlp(inp)
@@ -69,14 +69,14 @@ def test_mlp_tc_kernel_kind():
 
 
 @pytest.mark.parametrize("T", [16, 32, 160])
-def test_mlp_tc_lengths(T):
+def test_mlp_tc_lengths(T, mlp_form):
     inp = _tc(T=T, B=1, H=3)
     got = run_mlp(inp)
     assert int(got["status"].item()) == 0
     compare(got, oracle_mlp(inp), KEYS, TOL["bf16"])
 
 
-def test_mlp_tc_per_sequence_weights_and_ln_params():
+def test_mlp_tc_per_sequence_weights_and_ln_params(mlp_form):
     inp = _tc(T=48, B=3, H=2)
     g = torch.Generator().manual_seed(11)
     inp["W1"] = torch.randn(3, 2, 256, 64, generator=g) * 0.05
@@ -90,7 +90,7 @@ def test_mlp_tc_per_sequence_weights_and_ln_params():
     compare(got, oracle_mlp(inp), KEYS, TOL["bf16"])
 
 
-def test_mlp_tc_causality_bit_exact():
+def test_mlp_tc_causality_bit_exact(mlp_form):
     inp = _tc(T=64, B=1, H=2)
     base = run_mlp(inp)
     t = 37
@@ -105,7 +105,7 @@ def test_mlp_tc_causality_bit_exact():
         assert not torch.equal(r["Z"][0, 1, t:], base["Z"][0, 1, t:]), key
 
 
-def test_mlp_tc_chain_permutation():
+def test_mlp_tc_chain_permutation(mlp_form):
     inp = _tc(T=32, B=3, H=2)
     base = run_mlp(inp)
     perm = torch.tensor([2, 0, 1])
@@ -117,7 +117,7 @@ def test_mlp_tc_chain_permutation():
         assert torch.equal(r[k], base[k][perm]), k
 
 
-def test_mlp_tc_resume_two_calls():
+def test_mlp_tc_resume_two_calls(mlp_form):
     inp = _tc(T=96, B=1, H=2)
     full = run_mlp(inp)
     T1 = 48
@@ -134,7 +134,7 @@ def test_mlp_tc_resume_two_calls():
     assert rel_err(to_np(rb["W2"]), to_np(full["W2"])) < 1e-2
 
 
-def test_mlp_tc_outputs_fully_written():
+def test_mlp_tc_outputs_fully_written(mlp_form):
     inp = _tc(T=32, B=2, H=2)
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     nan = lambda *s: torch.full(s, float("nan"), device="cuda")
@@ -147,3 +147,31 @@ def test_mlp_tc_outputs_fully_written():
     assert int(st.item()) == 0
     for k in out:
         assert torch.isfinite(r[k]).all(), k
+
+
+def test_mlp_tc_forms_agree():
+    """The two-CTA cluster form (hidden units split, partial sums exchanged)
+    against the one-CTA form: the same arithmetic up to the order of the sums
+    over the hidden units, so they agree far inside the oracle tolerance; each
+    form is deterministic."""
+    inp = _tc(T=256, B=2, H=3, seed=93)
+    try:
+        ttt.mlp_cluster_mode(0)
+        one = run_mlp(inp)
+        ttt.mlp_cluster_mode(2)
+        two = run_mlp(inp)
+        again = run_mlp(inp)
+    finally:
+        ttt.mlp_cluster_mode(1)
+    assert int(one["status"].item()) == 0 and int(two["status"].item()) == 0
+    for k in KEYS:
+        assert torch.equal(two[k], again[k]), k
+        e = rel_err(to_np(two[k]), to_np(one[k]))
+        assert e <= 2e-3, (k, e)
+
+
+def test_mlp_cluster_mode_default_and_readback():
+    assert ttt.mlp_cluster_mode(-1) == 1
+    assert ttt.mlp_cluster_mode(7) == 1
+    assert ttt.mlp_cluster_mode(0) == 0
+    assert ttt.mlp_cluster_mode(1) == 1

@@ -47,7 +47,7 @@ def test_linear_rule_vs_oracle(rule, d, b, T, io, kind, linear_form):
 
 @pytest.mark.parametrize("rule", RULES)
 @pytest.mark.parametrize("d,h,b,T,io,kind", [(64, 256, 16, 48, "bf16", 2), (16, 48, 4, 24, "f32", 1)])
-def test_mlp_rule_vs_oracle(rule, d, h, b, T, io, kind):
+def test_mlp_rule_vs_oracle(rule, d, h, b, T, io, kind, mlp_form):
     w = WORKLOADS["mlp_b4h12_d64_t8k"].with_(B=2, H=2, T=T, d=d, hidden=h, b=b, io=io, seed=124)
     assert ttt.mlp_kernel_kind(ttt.BF16 if io == "bf16" else ttt.F32, d, h, b) == kind
     inp = make_inputs(w)
@@ -95,7 +95,7 @@ def test_full_size_sampled_chains_rule(rule):
         assert rel_err(g, ref[k].reshape(g.shape)) <= 5 * TOL["bf16"], k
 
 
-def test_mlp_key_rule_equals_anchor_rule_with_keys_as_queries():
+def test_mlp_key_rule_equals_anchor_rule_with_keys_as_queries(mlp_form):
     w = WORKLOADS["mlp_b4h12_d64_t8k"].with_(B=1, H=2, T=48, seed=125)
     inp = make_inputs(w)
     a = run_mlp(inp, rule="key", q_none=True)

@@ -62,7 +62,7 @@ def test_linear_partial_tail(rule, d, b, T, io, kind, linear_form):
 
 
 @pytest.mark.parametrize("d,h,b,T,io", [(64, 256, 16, 40, "bf16"), (64, 256, 16, 7, "bf16"), (16, 48, 4, 10, "f32")])
-def test_mlp_partial_tail(d, h, b, T, io):
+def test_mlp_partial_tail(d, h, b, T, io, mlp_form):
     Tfull = -(-T // b) * b
     w = WORKLOADS["mlp_b4h12_d64_t8k"].with_(B=2, H=2, T=Tfull, d=d, hidden=h, b=b, io=io, seed=400 + T)
     inp = make_inputs(w)
