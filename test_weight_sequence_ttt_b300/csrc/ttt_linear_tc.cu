@@ -43,7 +43,7 @@
 // gamma kv d; the five sums of the W warps add up (split-phase mbarrier) and give
 // the mean, variance and the two LayerNorm-backward means in closed form.
 //
-// Chain/weight split (d = 64). The chain above runs on its own warps (C, d/16
+// Chain/weight split (d = 64; d = 128 with b < 16). The chain above runs on its own warps (C, d/16
 // of them, rows 16w..16w+15 of Y^T) that do nothing else: partial sums, one
 // named-barrier reduction round, G and A~, the 16-wide correction. Separate
 // weight warps (T) hold W and c, apply W += A~ K, and compute S_{i+2},
@@ -51,8 +51,11 @@
 // memory and alternating producer/consumer named barriers, so the chain warps
 // never wait on an mbarrier. No warp of either group leaves early: after a
 // failed wait a T warp keeps running in step (results discarded, status set).
-// For d = 128 the W warps do both jobs (20 warps of the split form would not
-// fit the register file).
+// At d = 128 the split form has 20 warps at 96 registers a thread (some
+// spilled). It runs for b < 16, where a super-step holds 16/b LayerNorm rounds
+// and the chain warps, free of the weight products, shorten each round. At
+// b = 16 (one round per super-step) the W warps of the merged kernel do both
+// jobs, which measured faster.
 //
 // Precision. MMA operands are fp16 (10-bit mantissa) with fp32 accumulation;
 // W, c, LayerNorm statistics and gradients stay fp32. Inputs and W must stay
@@ -2187,7 +2190,10 @@ cudaError_t launch_dsub(const LinearParams &p, int chains, cudaStream_t s)
             return cudaGetLastError();
         }
     }
-    if constexpr (D == 64 && SUBB <= kSS) {
+    // The chain/weight split: d = 64 for b <= 16; d = 128 for b < 16 only, where the
+    // per-mini-batch LayerNorm rounds of a super-step dominate (at b = 16 the one
+    // round per super-step runs faster on the merged kernel).
+    if constexpr ((D == 64 && SUBB <= kSS) || (D == 128 && SUBB < kSS)) {
         cudaError_t e = ensure_smem<linear_tc_split_kernel<D, SUBB>>(smem);
         if (e != cudaSuccess) return e;
         linear_tc_split_kernel<D, SUBB><<<chains, Cfg<D>::kSplitThreads, smem, s>>>(mQ, mK, mV, p);
