@@ -577,8 +577,12 @@ def run_gpu_backward(args):
         return None
     bytes_launch, flops_launch = backward_cost(w)
     achieved = flops_launch / (ms / 1e3) / 1e12
-    tc = args.bwd_math == "tf32" and w.variant == "linear" and w.d == 64 and w.b == 16
-    if tc:  # the contractions run on the tensor cores with tf32 operands
+    # TTT-Linear at d = 64 / 128, b = 16: the contractions run on the tensor cores with tf32
+    # operands, split into hi + lo parts (three products each, two where one operand is a bf16
+    # input) unless --bwd-math tf32; the fraction counts the algorithmic FLOPs once.
+    tc = w.variant == "linear" and w.d in (64, 128) and w.b == 16
+    split = tc and args.bwd_math == "fp32"
+    if tc:
         pk = _peaks()
         peak, bound = pk["bf16_tflops"] * TF32_PER_BF16, "tensor"
         peak_src = "%s bf16 burst x %.3f (nominal dense tf32 / bf16, 1.1 / 2.25 PFLOP/s)" % (pk["source"],
@@ -591,7 +595,7 @@ def run_gpu_backward(args):
                   % ("Linear" if w.variant == "linear" else "MLP"),
         "value": tokens / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "tf32-mma/f32" if tc else "f32",
+        "vs_baseline": None, "dtype": ("tf32x3-mma/f32" if split else "tf32-mma/f32") if tc else "f32",
         "precision": "bf16 Q/K/V/dZ inputs; fp32 FFMA arithmetic, fp32 gradients",
         "data": "synthetic (seeded Gaussian Q/K/V/dZ, sigmoid-gated eta, N(0,0.02^2) W0)",
         "config": {"workload": w.name, "direction": "backward", "variant": "ttt-" + w.variant, "B": w.B,
@@ -616,9 +620,15 @@ def run_gpu_backward(args):
         line["cpu_baseline"] = {"value": toks / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
                                 "sample": "%d of %d chains x %d tokens (fp64 torch autograd through the "
                                           "primal token loop)" % (chains, w.chains, Ts), "seconds": dt}
-    line["precision"] = ("%s Q/K/V/dZ inputs; tensor-core products with tf32 operands and fp32 accumulation, "
-                         "fp32 LayerNorm rows and gradients" % w.io) if tc else \
-        "%s Q/K/V/dZ inputs; fp32 FFMA arithmetic, fp32 gradients" % w.io
+    if split:
+        line["precision"] = ("%s Q/K/V/dZ inputs; tensor-core products of fp32 operands split into tf32 hi + lo "
+                             "parts (hi.hi + hi.lo + lo.hi, fp32 accumulation), fp32 LayerNorm rows and gradients"
+                             % w.io)
+    elif tc:
+        line["precision"] = ("%s Q/K/V/dZ inputs; tensor-core products with tf32 operands and fp32 accumulation, "
+                             "fp32 LayerNorm rows and gradients" % w.io)
+    else:
+        line["precision"] = "%s Q/K/V/dZ inputs; fp32 FFMA arithmetic, fp32 gradients" % w.io
     line["config"]["math"] = args.bwd_math
     return line
 
