@@ -175,3 +175,12 @@ def test_mlp_cluster_mode_default_and_readback():
     assert ttt.mlp_cluster_mode(7) == 1
     assert ttt.mlp_cluster_mode(0) == 0
     assert ttt.mlp_cluster_mode(1) == 1
+
+
+@pytest.mark.parametrize("T", [16, 48])
+def test_mlp_tc_single_chain(T, mlp_form):
+    """One (sequence, head) chain: one CTA, or one cluster of two, on the whole GPU."""
+    inp = _tc(T=T, B=1, H=1, seed=97)
+    got = run_mlp(inp)
+    assert int(got["status"].item()) == 0
+    compare(got, oracle_mlp(inp), KEYS, TOL["bf16"])
