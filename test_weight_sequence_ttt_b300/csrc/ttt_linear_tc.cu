@@ -1513,9 +1513,11 @@ constexpr int kBarS0 = 4;   // S_k ready (T -> C), ids 4 and 5 by k & 1
 // 16 CB c .. 16 CB (c + 1) - 1 as CB = MT / NC blocks of 16 (block w = CB c + bk
 // in the weight warps' numbering) with the tokens on the mma M axis: lane
 // (g, c4) has tokens g, g+8 and features 16w + 8nt + 2c4 + e, so a token's sums
-// over the warp's features need 4 CB in-register terms and two shuffle levels,
-// and one exchange with the other chain warps through shared memory completes
-// them. Every lane then forms the statistics of both its tokens itself.
+// over the warp's features need 4 CB in-register terms and two shuffle levels
+// (which also split the ten sums of a lane's two tokens over the four lanes of
+// its quad: eight shuffles), and one exchange through shared memory completes
+// them. Every lane then reads every chain warp's totals of both its tokens, in
+// the same order in every warp, and forms their statistics itself.
 // SEND (cluster kernel): every step's A~ also goes to the output CTA (rank 1)
 // through its ring of kNA slots, each 16-byte piece by st.async completing on
 // that CTA's afull[slot]; a slot is written again only after the output CTA
@@ -1635,22 +1637,36 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
                 q[u][3] = ac;
                 q[u][4] = ad;
             }
+            if (c == 0 && m == 0) TTT_TRACE_AT(p, i, 1);
+            // Sum the ten values over the four lanes (c4) that share g, the lanes splitting
+            // the work as they go: at the first level lane bit 0 picks the token (u = c4 & 1),
+            // at the second lane bit 1 picks sums 0-2 or 3-4. Eight shuffles instead of twenty;
+            // each lane then holds two or three of the warp's ten totals.
+            const int b0 = c4 & 1, b1 = c4 >> 1;
+            float hq[5];
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
-#pragma unroll
-                for (int k = 0; k < 5; ++k) {
-                    q[u][k] += __shfl_xor_sync(kFull, q[u][k], 1);
-                    q[u][k] += __shfl_xor_sync(kFull, q[u][k], 2);
-                }
+            for (int k = 0; k < 5; ++k)
+                hq[k] = (b0 ? q[1][k] : q[0][k]) + __shfl_xor_sync(kFull, b0 ? q[0][k] : q[1][k], 1);
+            const float x0 = __shfl_xor_sync(kFull, b1 ? hq[0] : hq[3], 2);
+            const float x1 = __shfl_xor_sync(kFull, b1 ? hq[1] : hq[4], 2);
+            const float x2 = __shfl_xor_sync(kFull, hq[2], 2);
+            const float r0 = (b1 ? hq[3] : hq[0]) + x0;  // sum 0 (b1 = 0) or 3 (b1 = 1) of token g + 8 b0
+            const float r1 = (b1 ? hq[4] : hq[1]) + x1;  // sum 1 or 4
+            const float r2 = hq[2] + x2;                 // sum 2 (b1 = 0 lanes)
             if (c == 0 && m == 0) TTT_TRACE_AT(p, i, 15);
             const int buf = rnd & 1;
             float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * NC * kSS;
             float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * NC * kSS;
-            if (c4 == 0) {
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    redX[c * kSS + g + 8 * u] = make_float4(q[u][0], q[u][1], q[u][2], q[u][3]);
-                    redY[c * kSS + g + 8 * u] = q[u][4];
+            {
+                const int t = g + 8 * b0;
+                float *rx = reinterpret_cast<float *>(redX + c * kSS + t);
+                if (b1 == 0) {
+                    rx[0] = r0;
+                    rx[1] = r1;
+                    rx[2] = r2;
+                } else {
+                    rx[3] = r0;
+                    redY[c * kSS + t] = r1;
                 }
             }
             named_bar_sync(kBarRed, NC * 32);
@@ -1659,11 +1675,10 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
             float mu[2], rsv[2], rsE[2], cst[2], M2v[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                // add the other chain warps' partial sums of this token
-                float S1 = q[u][0], S2 = q[u][1], SB = q[u][2], SC = q[u][3], SD = q[u][4];
+                // every chain warp's sums of this token, added in the same order in every warp
+                float S1 = 0.f, S2 = 0.f, SB = 0.f, SC = 0.f, SD = 0.f;
 #pragma unroll
-                for (int o = 1; o < NC; ++o) {
-                    const int src = (c + o) % NC;
+                for (int src = 0; src < NC; ++src) {
                     const float4 x = redX[src * kSS + g + 8 * u];
                     S1 += x.x;
                     S2 += x.y;
@@ -1686,6 +1701,7 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
                 rsE[u] = rs * escale[u];   // a~ = rs escale (2 gamma E - M1 - yh M2)
                 cst[u] = -rsE[u] * M1;
             }
+            if (c == 0 && m == 0) TTT_TRACE_AT(p, i, 12);
             float ad[CB][2][4];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
@@ -1705,6 +1721,7 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
                             if (in_m) at[bk][nt][r] = a;
                         }
             }
+            if (c == 0 && m == 0) TTT_TRACE_AT(p, i, 13);
             if (NSUB > 1 && m + 1 < NSUB) {
                 // Later mini-batches of this super-step see this one's update:
                 // Y[t][f] += sum_{s in mini-batch m} (k_s . k_t + 1) A~[f][s].
@@ -1755,6 +1772,7 @@ __device__ void role_chain_split(const LinearParams &p, uint8_t *sm, const Ring 
         if (has_next) {
             // Y_{i+1} = S_{i+1} + (K_{i+1} K_i^T + 1) A~_i^T
             named_bar_sync(kBarS0 + ((i + 1) & 1), kNAS);
+            if (c == 0) TTT_TRACE_AT(p, i, 11);
             load_in(stgn);
             load_s((i + 1) & 1);
             const uint4 kx = reinterpret_cast<const uint4 *>(stgn + C::kOffKxA)[lane];
