@@ -556,6 +556,41 @@ __device__ __forceinline__ void rows_gemm2(const float (&Wa)[D / 8][4], const fl
     }
 }
 
+// A weight warp's entry of a reduction round: its twenty per-column moments
+// (five moments x the lane's four columns 8nt + 2c4 + e), summed over the
+// warp's rows, i.e. over the eight lanes g that share c4, stored as
+// redX[w][t] = moments 0-3 and redY[w][t] = moment 4. The lanes split the
+// values as they reduce them (g bit 2 picks the column tile nt, bit 1 the
+// column e, bit 0 moments 0-2 or 3-4): eighteen shuffles where summing each
+// value over all eight lanes takes sixty.
+__device__ __forceinline__ void store_moments(const float (&q5)[5][2][2], float4 *redX, float *redY, int w, int g,
+                                              int c4)
+{
+    const int bA = (g >> 2) & 1, bB = (g >> 1) & 1, bC = g & 1;
+    float hA[5][2], hB[5];
+#pragma unroll
+    for (int k = 0; k < 5; ++k)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+            hA[k][e] = (bA ? q5[k][1][e] : q5[k][0][e]) + __shfl_xor_sync(kFull, bA ? q5[k][0][e] : q5[k][1][e], 16);
+#pragma unroll
+    for (int k = 0; k < 5; ++k)
+        hB[k] = (bB ? hA[k][1] : hA[k][0]) + __shfl_xor_sync(kFull, bB ? hA[k][0] : hA[k][1], 8);
+    const float x0 = __shfl_xor_sync(kFull, bC ? hB[0] : hB[3], 4);
+    const float x1 = __shfl_xor_sync(kFull, bC ? hB[1] : hB[4], 4);
+    const float x2 = __shfl_xor_sync(kFull, hB[2], 4);
+    const int t = 8 * bA + 2 * c4 + bB;
+    float *rx = reinterpret_cast<float *>(redX + w * kSS + t);
+    if (bC == 0) {  // moments 0, 1, 2
+        rx[0] = hB[0] + x0;
+        rx[1] = hB[1] + x1;
+        rx[2] = hB[2] + x2;
+    } else {        // moments 3, 4
+        rx[3] = hB[3] + x0;
+        redY[w * kSS + t] = hB[4] + x1;
+    }
+}
+
 template <int D, int SUBB>
 __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, int w, int chain, int bi,
                              int hi, size_t tok0, int lane, int nsteps)
@@ -659,7 +694,7 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
 #pragma unroll
         for (int m = 0; m < NSUB; ++m) {
             // --- this warp's shifted sums over its 16 rows, for every column.
-            float s1[2][2], s2[2][2], sb[2][2], sc[2][2], sd[2][2];
+            float q5[5][2][2];  // [moment][nt][e]
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -675,26 +710,17 @@ __device__ void role_weights(const LinearParams &p, uint8_t *sm, const Ring &R, 
                         ac = fmaf(g2d, dv, ac);
                         ad = fmaf(gam[u] * kv[nt][e + 2 * u], dv, ad);
                     }
-                    s1[nt][e] = col_sum(a1);
-                    s2[nt][e] = col_sum(a2);
-                    sb[nt][e] = col_sum(ab);
-                    sc[nt][e] = col_sum(ac);
-                    sd[nt][e] = col_sum(ad);
+                    q5[0][nt][e] = a1;
+                    q5[1][nt][e] = a2;
+                    q5[2][nt][e] = ab;
+                    q5[3][nt][e] = ac;
+                    q5[4][nt][e] = ad;
                 }
             if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 5);
             const int buf = rnd & 1;
             float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
             float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
-            if (g == 0) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = 8 * nt + 2 * c4 + e;
-                        redX[w * kSS + t] = make_float4(s1[nt][e], s2[nt][e], sb[nt][e], sc[nt][e]);
-                        redY[w * kSS + t] = sd[nt][e];
-                    }
-            }
+            store_moments(q5, redX, redY, w, g, c4);
             warp_arrive(&R.red[buf], lane);
             if (w == 0 && m == 0) TTT_TRACE_AT(p, i, 6);
             if (m == 0) {
@@ -968,7 +994,7 @@ __device__ void role_weights_mb2(const LinearParams &p, uint8_t *sm, const Ring 
             const float sh_c = ssh[tc];
             const float pk_c = reinterpret_cast<const float *>(stg + C::kOffPk)[tc];
             const float qk_c = reinterpret_cast<const float *>(stg + C::kOffQk)[tc];
-            float s1[2][2], s2[2][2], sb[2][2], sc[2][2], sd[2][2];
+            float q5[5][2][2];  // [moment][nt][e]
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -984,25 +1010,16 @@ __device__ void role_weights_mb2(const LinearParams &p, uint8_t *sm, const Ring 
                         ac = fmaf(g2d, dv, ac);
                         ad = fmaf(gam[u] * kv[nt][e + 2 * u], dv, ad);
                     }
-                    s1[nt][e] = col_sum(a1);
-                    s2[nt][e] = col_sum(a2);
-                    sb[nt][e] = col_sum(ab);
-                    sc[nt][e] = col_sum(ac);
-                    sd[nt][e] = col_sum(ad);
+                    q5[0][nt][e] = a1;
+                    q5[1][nt][e] = a2;
+                    q5[2][nt][e] = ab;
+                    q5[3][nt][e] = ac;
+                    q5[4][nt][e] = ad;
                 }
             const int buf = rnd & 1;
             float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
             float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
-            if (g == 0) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = 8 * nt + 2 * c4 + e;
-                        redX[w * kSS + t] = make_float4(s1[nt][e], s2[nt][e], sb[nt][e], sc[nt][e]);
-                        redY[w * kSS + t] = sd[nt][e];
-                    }
-            }
+            store_moments(q5, redX, redY, w, g, c4);
             warp_arrive(&R.red[buf], lane);
             if (!wait_bar(&R.red[buf], parity_of(rnd >> 1), R.flags)) {
                 abort_chain(R.flags, p.status);
@@ -1255,7 +1272,7 @@ __device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &
             const float sh_c = ssh[tc];
             const float pk_c = reinterpret_cast<const float *>(stg + C::kOffPk)[tc];
             const float qk_c = reinterpret_cast<const float *>(stg + C::kOffQk)[tc];
-            float s1[2][2], s2[2][2], sb[2][2], sc[2][2], sd[2][2];
+            float q5[5][2][2];  // [moment][nt][e]
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -1271,25 +1288,16 @@ __device__ void role_weights_mb(const LinearParams &p, uint8_t *sm, const Ring &
                         ac = fmaf(g2d, dv, ac);
                         ad = fmaf(gam[u] * kv[nt][e + 2 * u], dv, ad);
                     }
-                    s1[nt][e] = col_sum(a1);
-                    s2[nt][e] = col_sum(a2);
-                    sb[nt][e] = col_sum(ab);
-                    sc[nt][e] = col_sum(ac);
-                    sd[nt][e] = col_sum(ad);
+                    q5[0][nt][e] = a1;
+                    q5[1][nt][e] = a2;
+                    q5[2][nt][e] = ab;
+                    q5[3][nt][e] = ac;
+                    q5[4][nt][e] = ad;
                 }
             const int buf = rnd & 1;
             float4 *redX = reinterpret_cast<float4 *>(sm + C::kOffRedX) + buf * MT * kSS;
             float *redY = reinterpret_cast<float *>(sm + C::kOffRedY) + buf * MT * kSS;
-            if (g == 0) {
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = 8 * nt + 2 * c4 + e;
-                        redX[w * kSS + t] = make_float4(s1[nt][e], s2[nt][e], sb[nt][e], sc[nt][e]);
-                        redY[w * kSS + t] = sd[nt][e];
-                    }
-            }
+            store_moments(q5, redX, redY, w, g, c4);
             warp_arrive(&R.red[buf], lane);
             if (!wait_bar(&R.red[buf], parity_of(rnd >> 1), R.flags)) {
                 abort_chain(R.flags, p.status);
