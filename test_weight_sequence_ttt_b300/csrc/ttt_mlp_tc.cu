@@ -804,24 +804,37 @@ __device__ __forceinline__ void y_ln_stats(const float (&x)[2][2][4], float4 *re
         }
 }
 
-// Sums over the 64 features of up to three per-element quantities per column.
+// Sums over the 64 features of three per-element quantities per column: each
+// Y warp's twelve values (three quantities x the lane's four columns) are
+// summed over its eight lanes g that share c4, the lanes splitting them as they
+// go (g bit 2 picks n, bit 1 the column e, bit 0 quantity a or b, c): eleven
+// shuffles where summing each value over all eight lanes takes thirty-six.
+// The Y warps' totals then meet in shared memory as before.
 __device__ __forceinline__ void y_sum3(float (&a)[2][2], float (&b)[2][2], float (&c)[2][2], float4 *red, int &rnd,
                                        int y, int g, int c4)
 {
+    const int bA = (g >> 2) & 1, bB = (g >> 1) & 1, bC = g & 1;
+    float hA[3][2], hB[3];
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+    for (int e = 0; e < 2; ++e) {
+        hA[0][e] = (bA ? a[1][e] : a[0][e]) + __shfl_xor_sync(kFull, bA ? a[0][e] : a[1][e], 16);
+        hA[1][e] = (bA ? b[1][e] : b[0][e]) + __shfl_xor_sync(kFull, bA ? b[0][e] : b[1][e], 16);
+        hA[2][e] = (bA ? c[1][e] : c[0][e]) + __shfl_xor_sync(kFull, bA ? c[0][e] : c[1][e], 16);
+    }
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            a[n][e] = col_sum(a[n][e]);
-            b[n][e] = col_sum(b[n][e]);
-            c[n][e] = col_sum(c[n][e]);
-        }
+    for (int k = 0; k < 3; ++k)
+        hB[k] = (bB ? hA[k][1] : hA[k][0]) + __shfl_xor_sync(kFull, bB ? hA[k][0] : hA[k][1], 8);
+    const float x0 = __shfl_xor_sync(kFull, bC ? hB[0] : hB[1], 4);
+    const float x1 = __shfl_xor_sync(kFull, hB[2], 4);
     float4 *rb = red + (rnd & 1) * kNY * kB;
-    if (g == 0) {
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) rb[y * kB + 8 * n + 2 * c4 + e] = make_float4(a[n][e], b[n][e], c[n][e], 0.f);
+    {
+        float *rx = reinterpret_cast<float *>(rb + y * kB + 8 * bA + 2 * c4 + bB);
+        if (bC == 0) {  // quantity a
+            rx[0] = hB[0] + x0;
+        } else {        // quantities b and c
+            rx[1] = hB[1] + x0;
+            rx[2] = hB[2] + x1;
+        }
     }
     named_bar_sync(kBarYln, kNY * 32);
     ++rnd;
