@@ -760,35 +760,41 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
 // ------------------------------------------------------------------ Y: output-feature warps
 // LayerNorm statistics of the 16 token columns over the 64 features held by
 // the two Y warps (32 rows each): local (mean, M2) per column, combined across
-// the two warps by the parallel-variance formula. Returns mean and 1/std of
-// the lane's four columns (8n + 2c4 + e).
+// the two warps by the parallel-variance formula. The local means are summed
+// over the warp's eight lanes g of a column with three shuffle levels (every
+// lane needs them); the M2s only by the lane that stores them, so the lanes
+// split the four columns as they reduce (four shuffles instead of twelve).
+// Returns mean and 1/std of the lane's four columns (8n + 2c4 + e).
 __device__ __forceinline__ void y_ln_stats(const float (&x)[2][2][4], float4 *red, int &rnd, int y, int g, int c4,
                                            float eps, float (&mu)[2][2], float (&rs)[2][2])
 {
-    float ml[2][2], m2l[2][2];
+    float ml[2][2], q[2][2];
 #pragma unroll
     for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const float s = col_sum(x[0][n][e] + x[0][n][e + 2] + x[1][n][e] + x[1][n][e + 2]) * (1.f / 32.f);
-            float q = 0.f;
+            float qq = 0.f;
 #pragma unroll
             for (int m = 0; m < 2; ++m)
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const float d = x[m][n][e + 2 * u] - s;
-                    q = fmaf(d, d, q);
+                    qq = fmaf(d, d, qq);
                 }
             ml[n][e] = s;
-            m2l[n][e] = col_sum(q);
+            q[n][e] = qq;
         }
+    // M2 of column (n, e) = (g bit 2, g bit 1) ends in the lanes with g bit 0 clear.
+    const int bA = (g >> 2) & 1, bB = (g >> 1) & 1;
+    float hA[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) hA[e] = (bA ? q[1][e] : q[0][e]) + __shfl_xor_sync(kFull, bA ? q[0][e] : q[1][e], 16);
+    float m2 = (bB ? hA[1] : hA[0]) + __shfl_xor_sync(kFull, bB ? hA[0] : hA[1], 8);
+    m2 += __shfl_xor_sync(kFull, m2, 4);
     float4 *rb = red + (rnd & 1) * kNY * kB;
-    if (g == 0) {
-#pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) rb[y * kB + 8 * n + 2 * c4 + e] = make_float4(ml[n][e], m2l[n][e], 0.f, 0.f);
-    }
+    const float mlc = bA ? (bB ? ml[1][1] : ml[1][0]) : (bB ? ml[0][1] : ml[0][0]);
+    if ((g & 1) == 0) rb[y * kB + 8 * bA + 2 * c4 + bB] = make_float4(mlc, m2, 0.f, 0.f);
     named_bar_sync(kBarYln, kNY * 32);
     ++rnd;
 #pragma unroll
@@ -798,9 +804,9 @@ __device__ __forceinline__ void y_ln_stats(const float (&x)[2][2][4], float4 *re
             const int t = 8 * n + 2 * c4 + e;
             const float4 a = rb[t], b = rb[kB + t];
             const float mean = 0.5f * (a.x + b.x);
-            const float m2 = a.y + b.y + 32.f * ((a.x - mean) * (a.x - mean) + (b.x - mean) * (b.x - mean));
+            const float m2t = a.y + b.y + 32.f * ((a.x - mean) * (a.x - mean) + (b.x - mean) * (b.x - mean));
             mu[n][e] = mean;
-            rs[n][e] = rsqrtf(m2 * (1.f / (float)kD) + eps);
+            rs[n][e] = rsqrtf(m2t * (1.f / (float)kD) + eps);
         }
 }
 
