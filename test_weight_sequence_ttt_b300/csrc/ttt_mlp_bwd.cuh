@@ -713,6 +713,56 @@ __host__ __device__ inline size_t mlp_bwd_cluster_smem_floats(int d, int h)
     return 2 * hh * ldw + 2 * hh + 6 * (size_t)d + 13 * b * d + 9 * b * hh + 4 * b * b + 5 * b + 2 * xs;
 }
 
+// The 16 x 16 Gram out[t][s] = sign (sum_k X[t][k] Y[s][k] + add) for s <= t when
+// causal (else 0), with one warp per row t: the lanes split k (k = lane + 32 j:
+// no shared-memory bank conflicts, where one thread per entry reads 16 rows at
+// one column) and reduce the row's 16 partial sums over the warp, splitting them
+// as they go (16 shuffles). rout, if given, receives a copy. Kd <= 128 (callers
+// with a longer row use gram).
+__device__ __forceinline__ void gram_w(float *out, float *rout, const float *X, const float *Y, int Kd, float add,
+                                       float sign, bool causal, int warp, int lane)
+{
+    constexpr int MB = 16;
+    static_assert(kNW == MB, "one warp per row of the Gram");
+    const int t = warp;
+    float xr[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int k = lane + 32 * j;
+        xr[j] = k < Kd ? X[t * Kd + k] : 0.f;
+    }
+    float v[MB];
+#pragma unroll
+    for (int r = 0; r < MB; ++r) {
+        float a = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = lane + 32 * j;
+            if (k < Kd) a = fmaf(xr[j], Y[r * Kd + k], a);
+        }
+        v[r] = a;
+    }
+    const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1, b1 = (lane >> 1) & 1;
+    float v8[8], v4[4], v2[2];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        v8[q] = (b4 ? v[8 + q] : v[q]) + __shfl_xor_sync(0xffffffffu, b4 ? v[q] : v[8 + q], 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        v4[q] = (b3 ? v8[4 + q] : v8[q]) + __shfl_xor_sync(0xffffffffu, b3 ? v8[q] : v8[4 + q], 8);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+        v2[q] = (b2 ? v4[2 + q] : v4[q]) + __shfl_xor_sync(0xffffffffu, b2 ? v4[q] : v4[2 + q], 4);
+    float v1 = (b1 ? v2[1] : v2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? v2[0] : v2[1], 2);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+    const int sc = 8 * b4 + 4 * b3 + 2 * b2 + b1;  // the column this lane (and lane ^ 1) now holds
+    if ((lane & 1) == 0) {
+        const float r = (!causal || sc <= t) ? sign * (v1 + add) : 0.f;
+        out[t * MB + sc] = r;
+        if (rout) rout[t * MB + sc] = r;
+    }
+}
+
 template <typename IO>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_cluster_kernel(MlpBwdParams p)
 {
@@ -954,7 +1004,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         }
         __syncthreads();
         prod_rows_ld<MB, 2>(S.Q, W1h, LW, HH, d, [&](int s, int m, float a) { S.Z1q[s * HH + m] = a + c1h[m]; });
-        gram<MB>(S.QK1, S.Q, S.K, d, 1.f, 1.f, false);
+        if (d <= 128)
+            gram_w(S.QK1, nullptr, S.Q, S.K, d, 1.f, 1.f, false, warp, lane);
+        else
+            gram<MB>(S.QK1, S.Q, S.K, d, 1.f, 1.f, false);
         __syncthreads();
         for (int x = tid; x < MB * HH; x += kNT) {
             const int t = x / HH, m = x % HH;
@@ -967,15 +1020,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         // exchange: the X2q X2^T Gram (partial over h, at 0) and X2q W2^T (at MB*MB)
         {
             float *rm = remote();
-            for (int it = tid; it < MB * MB; it += kNT) {
-                const int t = it / MB, s = it % MB;
-                float acc = 0.f;
-                for (int k = 0; k < HH; k += 4) {
-                    const float4 x = ld4(S.X2q + t * HH + k), y = ld4(S.X2 + s * HH + k);
-                    acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+            if (HH <= 128) {
+                gram_w(S.QK2, rm, S.X2q, S.X2, HH, 0.f, 1.f, false, warp, lane);
+            } else {
+                for (int it = tid; it < MB * MB; it += kNT) {
+                    const int t = it / MB, s = it % MB;
+                    float acc = 0.f;
+                    for (int k = 0; k < HH; k += 4) {
+                        const float4 x = ld4(S.X2q + t * HH + k), y = ld4(S.X2 + s * HH + k);
+                        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+                    }
+                    S.QK2[it] = acc;
+                    rm[it] = acc;
                 }
-                S.QK2[it] = acc;
-                rm[it] = acc;
             }
             prod_cols_ld<MB, 2>(S.X2q, W2h, LW, d, HH, [&](int s, int j, float a) {
                 S.P[s * d + j] = a;
@@ -1028,7 +1085,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
             S.dgam[j] += ag;
             S.dbet[j] += ab;
         }
-        gram<MB>(S.DA2, S.DYq, S.G, d, 0.f, -1.f, true);
+        if (d <= 128)
+            gram_w(S.DA2, nullptr, S.DYq, S.G, d, 0.f, -1.f, true, warp, lane);
+        else
+            gram<MB>(S.DA2, S.DYq, S.G, d, 0.f, -1.f, true);
         prod_rows_ld<MB>(S.K, dW1h, d, HH, d, [&](int s, int m, float a) { S.R1[s * HH + m] = a + dc1h[m]; });
         {
             float *rm = remote();
@@ -1071,16 +1131,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         // exchange: the dZ1q G1^T Gram (partial over h)
         {
             float *rm = remote();
-            for (int it = tid; it < MB * MB; it += kNT) {
-                const int t = it / MB, s = it % MB;
-                float acc = 0.f;
-                if (s <= t)
-                    for (int k = 0; k < HH; k += 4) {
-                        const float4 x = ld4(S.Z1q + t * HH + k), y = ld4(S.G1 + s * HH + k);
-                        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
-                    }
-                S.DA1[it] = acc;
-                rm[it] = acc;
+            if (HH <= 128) {
+                gram_w(S.DA1, rm, S.Z1q, S.G1, HH, 0.f, 1.f, true, warp, lane);
+            } else {
+                for (int it = tid; it < MB * MB; it += kNT) {
+                    const int t = it / MB, s = it % MB;
+                    float acc = 0.f;
+                    if (s <= t)
+                        for (int k = 0; k < HH; k += 4) {
+                            const float4 x = ld4(S.Z1q + t * HH + k), y = ld4(S.G1 + s * HH + k);
+                            acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+                        }
+                    S.DA1[it] = acc;
+                    rm[it] = acc;
+                }
             }
         }
         cluster.sync();
