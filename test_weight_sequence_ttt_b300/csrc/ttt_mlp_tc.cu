@@ -89,6 +89,11 @@ constexpr int kYS = kD + 4;  // floats per row of the Yq hand-off
 constexpr uint32_t kTmemCols = 128;  // two H warps per lane quarter x 64 columns
 // named barriers: H <-> Y hand-offs (all H and Y threads), Y-internal rounds
 constexpr int kBarX2k = 1, kBarG = 2, kBarX2q = 3 /* and 4, by step parity */, kBarYln = 5;
+// Every mbarrier wait of this kernel polls without suspending the thread: the
+// waits on the recurrence (the Y exchange, the H/Y hand-offs) then resume as
+// soon as their phase completes, which measured faster than letting the
+// hardware suspend the waiting warps.
+constexpr bool kSpinWaits = true;
 
 // Warps and shared memory of a CTA that owns kHid / NR hidden units: the whole
 // chain (NR = 1) or one half of it in a two-CTA cluster (NR = 2).
@@ -260,7 +265,7 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
     for (int i = 0; i < nsteps + kOutLag; ++i) {
         if (i < nsteps) {
             const int st = i % kStages;
-            if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags)) abort_chain(R.flags, p.status);
+            if (!wait_bar<kSpinWaits>(&R.full[st], parity_of(i / kStages), R.flags)) abort_chain(R.flags, p.status);
             if (p.eta_gate && lane < kB) {  // eta = eta_base * sigmoid(logit); 0 past T
                 float *se = reinterpret_cast<float *>(stage_ptr(sm, st) + kOffEta);
                 const int t = i * kB + lane;
@@ -273,7 +278,7 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
         const int jg = i - kGramLag;
         // Gram of step jg: Mq2[s][t] = (s <= t)(x2q_t . x2k_s + 1) as B fragments (k = s, n = t).
         if (jg >= 0 && jg < nsteps) {
-            if (!wait_bar(&R.hq[jg & 1], parity_of(jg >> 1), R.flags)) abort_chain(R.flags, p.status);
+            if (!wait_bar<kSpinWaits>(&R.hq[jg & 1], parity_of(jg >> 1), R.flags)) abort_chain(R.flags, p.status);
             uint4 *mq2 = reinterpret_cast<uint4 *>(sm + L::kOffMq2 + (jg & 1) * 512);
             if (!p.prefix) {  // anchor rule: Yq sees no update of the batch
                 mq2[lane] = make_uint4(0u, 0u, 0u, 0u);
@@ -315,10 +320,10 @@ __device__ void role_prep(const MlpParams &p, uint8_t *sm, const Ring &R, int hi
             continue;
         }
         // Output of step j: z = q + LN(yq), L_t = ||z_t - v_t||^2; lane pair per token.
-        if (!wait_bar(&R.yqfull[slot], parity_of(j >> 1), R.flags)) abort_chain(R.flags, p.status);
+        if (!wait_bar<kSpinWaits>(&R.yqfull[slot], parity_of(j >> 1), R.flags)) abort_chain(R.flags, p.status);
         if constexpr (NR == 2) {  // the other CTA's Yq partial (every step, aborted or not)
             if (lane == 0) mbar_arrive_expect_tx(&R.yqpfull[slot], L::kYqpTx);
-            if (!wait_peer(&R.yqpfull[slot], parity_of(j >> 1))) abort_chain(R.flags, p.status);
+            if (!wait_peer<kSpinWaits>(&R.yqpfull[slot], parity_of(j >> 1))) abort_chain(R.flags, p.status);
         }
         const float *ys = reinterpret_cast<const float *>(sm + L::kOffYq) + slot * kB * kYS + tl * kYS + 32 * half;
         float yv[32];
@@ -475,8 +480,8 @@ __device__ void role_hidden(const MlpParams &p, uint8_t *sm, const Ring &R, int 
     const int rt = (lane & 7) + ((lane >> 3) & 1) * 8, ct = lane >> 4;   // transposed B fragment rows
     const int srow = (lane & 7) + 8 * (lane >> 4), scol = 8 * ((lane >> 3) & 1);  // stmatrix / trans-A rows
     auto wait_stage = [&](int k) {
-        if (!wait_bar(&R.full[k % kStages], parity_of(k / kStages), R.flags) ||
-            !wait_bar(&R.prep[k % kStages], parity_of(k / kStages), R.flags))
+        if (!wait_bar<kSpinWaits>(&R.full[k % kStages], parity_of(k / kStages), R.flags) ||
+            !wait_bar<kSpinWaits>(&R.prep[k % kStages], parity_of(k / kStages), R.flags))
             abort_chain(R.flags, p.status);  // keep going in step with the other warps
     };
     // acc = c1 + W1 tile^T for this warp's 32 hidden units, for one or two tiles at
@@ -934,8 +939,8 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
         if (i < nsteps) {
             const int st = i % kStages;
             uint8_t *stg = stage_ptr(sm, st);
-            if (!wait_bar(&R.full[st], parity_of(i / kStages), R.flags) ||
-                !wait_bar(&R.prep[st], parity_of(i / kStages), R.flags))
+            if (!wait_bar<kSpinWaits>(&R.full[st], parity_of(i / kStages), R.flags) ||
+                !wait_bar<kSpinWaits>(&R.prep[st], parity_of(i / kStages), R.flags))
                 abort_chain(R.flags, p.status);
             // k - v + beta at this lane's (feature, token) positions: ldmatrix.trans of the bf16 tiles.
             float kv[2][2][4];
@@ -1022,7 +1027,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
                                 rbar);
                 }
                 if (y == 0 && lane == 0) mbar_arrive_expect_tx(&R.ypeer[slot], L::kYpTx);
-                if (!wait_peer(&R.ypeer[slot], parity_of(i >> 1))) abort_chain(R.flags, p.status);
+                if (!wait_peer<kSpinWaits>(&R.ypeer[slot], parity_of(i >> 1))) abort_chain(R.flags, p.status);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const float4 u = yp[q * 32];
@@ -1123,7 +1128,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
                     for (int r = 0; r < 4; ++r) yq[m][n][r] = lead ? c2p[m][r >> 1] : 0.f;
             y_gemm<NR>(sW2h + (uint32_t)(((j + 2) % 3) * kW2hBytes), sX2q + (uint32_t)((j & 1) * kX2Bytes), f0, lane,
                        yq);
-            if (!wait_bar(&R.mq2[j & 1], parity_of(j >> 1), R.flags)) abort_chain(R.flags, p.status);
+            if (!wait_bar<kSpinWaits>(&R.mq2[j & 1], parity_of(j >> 1), R.flags)) abort_chain(R.flags, p.status);
             {
                 const uint4 mq2 = reinterpret_cast<const uint4 *>(sm + L::kOffMq2 + (j & 1) * 512)[lane];
 #pragma unroll
@@ -1135,7 +1140,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
             if (y == 0) TTT_TRACE_AT(p, j, 13);
             const int slot = j & 1;
             if (lead) {
-                if (!wait_bar(&R.yqempty[slot], parity_of(j >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
+                if (!wait_bar<kSpinWaits>(&R.yqempty[slot], parity_of(j >> 1) ^ 1u, R.flags)) abort_chain(R.flags, p.status);
                 float *ys = reinterpret_cast<float *>(sm + L::kOffYq) + slot * kB * kYS;
 #pragma unroll
                 for (int m = 0; m < 2; ++m)
@@ -1148,7 +1153,7 @@ __device__ void role_y(const MlpParams &p, uint8_t *sm, const Ring &R, int y, in
             } else if constexpr (NR == 2) {
                 // CTA 1: the partial goes to CTA 0's slot, same [token][feature] layout, once
                 // CTA 0's P has read what was there (every step, aborted or not).
-                if (!wait_peer(&R.yqpempty[slot], parity_of(j >> 1) ^ 1u)) abort_chain(R.flags, p.status);
+                if (!wait_peer<kSpinWaits>(&R.yqpempty[slot], parity_of(j >> 1) ^ 1u)) abort_chain(R.flags, p.status);
                 const uint32_t rys = map_shared(smem_u32(sm + L::kOffYqp + slot * kB * kYS * 4), 0);
                 const uint32_t rbar = map_shared(smem_u32(&R.yqpfull[slot]), 0);
 #pragma unroll
@@ -1258,7 +1263,7 @@ __device__ __forceinline__ void mlp_tc_body(const CUtensorMap *tmQ, const CUtens
 
     if (warp == kWarpL) {
         const StageGeom geom{kStages, kStageBytes, kOffK, p.q_is_k ? -1 : kOffQ, kOffV, kOffEta};
-        role_loader<kD>(tmQ, tmK, tmV, p.eta + tok0, p.T, p.status, sm + kOffStages, geom, R.full, R.empty, R.flags,
+        role_loader<kD, kSpinWaits>(tmQ, tmK, tmV, p.eta + tok0, p.T, p.status, sm + kOffStages, geom, R.full, R.empty, R.flags,
                         chain, lane, nsteps,
 #ifdef TTT_FAULT_HOOKS
                         p.drop_step
