@@ -20,6 +20,7 @@ pytestmark = pytest.mark.gpu
 # (d, b, T, io, kind): split d=64 (b=16, b=4), merged d=128 (b=16, b=8), the
 # b=64 / b=32 paths (tail of several super-steps; tail only), fp32 kernels.
 LIN = [(64, 16, 37, "bf16", 2), (64, 4, 42, "bf16", 2), (64, 16, 9, "bf16", 2), (128, 16, 23, "bf16", 2),
+       (64, 16, 1, "bf16", 2), (64, 16, 47, "bf16", 2),
        (128, 8, 45, "bf16", 2), (64, 64, 100, "bf16", 2), (128, 32, 40, "bf16", 2), (64, 64, 20, "bf16", 2),
        (64, 256, 600, "bf16", 2), (128, 128, 300, "bf16", 2),
        (16, 16, 21, "f32", 1), (32, 16, 40, "bf16", 1)]
@@ -61,7 +62,8 @@ def test_linear_partial_tail(rule, d, b, T, io, kind, linear_form):
             assert torch.equal(got[k], full[k][:, :, :T]), k
 
 
-@pytest.mark.parametrize("d,h,b,T,io", [(64, 256, 16, 40, "bf16"), (64, 256, 16, 7, "bf16"), (16, 48, 4, 10, "f32")])
+@pytest.mark.parametrize("d,h,b,T,io", [(64, 256, 16, 40, "bf16"), (64, 256, 16, 7, "bf16"), (64, 256, 16, 1, "bf16"),
+                                        (64, 256, 16, 17, "bf16"), (64, 256, 16, 63, "bf16"), (16, 48, 4, 10, "f32")])
 def test_mlp_partial_tail(d, h, b, T, io, mlp_form):
     Tfull = -(-T // b) * b
     w = WORKLOADS["mlp_b4h12_d64_t8k"].with_(B=2, H=2, T=Tfull, d=d, hidden=h, b=b, io=io, seed=400 + T)
