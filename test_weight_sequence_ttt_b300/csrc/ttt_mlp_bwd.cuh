@@ -859,6 +859,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
             S.et[s] = p.eta_gate ? p.eta_base / (1.f + __expf(-e)) : e;
         }
     };
+    // Ask L2 for the 128-byte lines of [a, a + bytes), the threads splitting the
+    // lines. The reverse sweep does this for the mini-batch before the current
+    // one: its starting state and kept key side were written long before and
+    // left L2, and its loads then find them there.
+    auto pf = [&](const void *a, size_t bytes) {
+        const char *c = static_cast<const char *>(a);
+        for (size_t o = (size_t)tid * 128; o < bytes; o += (size_t)kNT * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
+    };
+    auto prefetch_rev = [&](int i) {  // what reverse step i loads from global memory
+        const size_t t0 = (size_t)i * MB;
+        pf(W1s(i), (size_t)HH * d * 4);
+        pf(W2s(i), (size_t)HH * d * 4);
+        pf(c1s(i), (size_t)HH * 4);
+        pf(c2s(i), (size_t)d * 4);
+        const float *sv = Svs(i);
+        pf(sv + (size_t)rank * MB * HH, (size_t)MB * HH * 4);
+        pf(sv + (size_t)(2 + rank) * MB * HH, (size_t)MB * HH * 4);
+        pf(sv + (size_t)4 * MB * HH, ((size_t)3 * MB * d + 2 * MB) * 4);
+        pf(Kg + t0 * d, (size_t)MB * d * sizeof(IO));
+        pf(Qg + t0 * d, (size_t)MB * d * sizeof(IO));
+        pf(DZg + t0 * d, (size_t)MB * d * sizeof(IO));
+        pf(eg + t0, MB * 4);
+    };
     // Y = X2 W2^T + c2 summed over both halves into Yh (the key side's only exchange).
     auto key_side = [&]() {
         prod_rows_ld<MB, 2>(S.K, W1h, LW, HH, d, [&](int s, int m, float a) {
@@ -1002,6 +1026,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
                 S.m2k[x] = yd[3 * MB * d + MB + x];
             }
         }
+        if (i > 0) prefetch_rev(i - 1);
         __syncthreads();
         prod_rows_ld<MB, 2>(S.Q, W1h, LW, HH, d, [&](int s, int m, float a) { S.Z1q[s * HH + m] = a + c1h[m]; });
         if (d <= 128)
