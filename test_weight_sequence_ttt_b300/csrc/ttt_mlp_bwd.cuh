@@ -860,9 +860,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
         }
     };
     // Ask L2 for the 128-byte lines of [a, a + bytes), the threads splitting the
-    // lines. The reverse sweep does this for the mini-batch before the current
-    // one: its starting state and kept key side were written long before and
-    // left L2, and its loads then find them there.
+    // lines. The forward sweep does this for the next mini-batch's tiles, the
+    // reverse sweep for the mini-batch before the current one: its starting
+    // state and kept key side were written long before and left L2, and its
+    // loads then find them there.
     auto pf = [&](const void *a, size_t bytes) {
         const char *c = static_cast<const char *>(a);
         for (size_t o = (size_t)tid * 128; o < bytes; o += (size_t)kNT * 128)
@@ -933,6 +934,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_clus
             S.E[x] = ldx<IO>(Vg + (size_t)t0 * d + x);
         }
         load_eta(t0);
+        if (i + 1 < n) {  // the next mini-batch's tiles into L2
+            pf(Kg + (size_t)(t0 + MB) * d, (size_t)MB * d * sizeof(IO));
+            pf(Vg + (size_t)(t0 + MB) * d, (size_t)MB * d * sizeof(IO));
+            pf(eg + t0 + MB, MB * 4);
+        }
         __syncthreads();
         key_side();
         __syncthreads();
