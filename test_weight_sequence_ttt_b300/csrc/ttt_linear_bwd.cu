@@ -1490,6 +1490,13 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             issue_tiles(t0 - MB, true);
             issue_anchor(i - 1);
             if (PFS) issue_saved(i - 1);
+            // d = 128 loads the key side at the start of its mini-batch (no registers to
+            // hold it meanwhile): have L2 fetch it now, so that those loads hit L2.
+            if (SAVE && !PFS) {
+                const char *sv = reinterpret_cast<const char *>(svb + (size_t)(i - 1) * SVL);
+                for (size_t o = (size_t)tid * 128; o < SVL * 4; o += (size_t)NT * 128)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(sv + o));
+            }
         }
         if constexpr (TC) {
             float *dKc = p.dK + (tok0 + t0) * D;
