@@ -1491,11 +1491,23 @@ __global__ void __launch_bounds__(NT, 1) linear_bwd_tiled_kernel(LinearBwdParams
             issue_anchor(i - 1);
             if (PFS) issue_saved(i - 1);
             // d = 128 loads the key side at the start of its mini-batch (no registers to
-            // hold it meanwhile): have L2 fetch it now, so that those loads hit L2.
+            // hold it meanwhile): have L2 fetch it now, so that those loads hit L2; and
+            // the tiles and starting state two mini-batches ahead, so that the register
+            // prefetch of the next step finds them there too (at d = 64 neither helps).
             if (SAVE && !PFS) {
-                const char *sv = reinterpret_cast<const char *>(svb + (size_t)(i - 1) * SVL);
-                for (size_t o = (size_t)tid * 128; o < SVL * 4; o += (size_t)NT * 128)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(sv + o));
+                auto l2 = [&](const void *a, size_t bytes) {
+                    const char *c = static_cast<const char *>(a);
+                    for (size_t o = (size_t)tid * 128; o < bytes; o += (size_t)NT * 128)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + o));
+                };
+                l2(svb + (size_t)(i - 1) * SVL, SVL * 4);
+                if (i > 1) {
+                    const size_t t2 = (size_t)(t0 - 2 * MB) * D;
+                    l2(Kg + t2, (size_t)MB * D * sizeof(IO));
+                    l2(Qg + t2, (size_t)MB * D * sizeof(IO));
+                    l2(DZg + t2, (size_t)MB * D * sizeof(IO));
+                    l2(ws + (size_t)(i - 2) * ((size_t)D * D + D), ((size_t)D * D + D) * 4);
+                }
             }
         }
         if constexpr (TC) {
