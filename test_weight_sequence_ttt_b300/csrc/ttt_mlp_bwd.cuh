@@ -763,14 +763,18 @@ __device__ __forceinline__ void gram_w(float *out, float *rout, const float *X, 
     }
 }
 
-template <typename IO>
+// DC, HC: d and the hidden width fixed at compile time (0: read from p). The
+// fixed sizes fold the index arithmetic and each product helper's choice of work
+// split, and unroll the loops whose bounds they set: for d = 64, h = 256 the
+// kernel runs in about 0.7 of the time the runtime-sized one takes.
+template <typename IO, int DC = 0, int HC = 0>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNT, 1) mlp_bwd_cluster_kernel(MlpBwdParams p)
 {
     constexpr int MB = kCB;
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ __align__(16) float smc[];
-    const int d = p.d, h = p.hidden, HH = h / 2, LW = d + 4, T = p.T, n = T / MB;
+    const int d = DC ? DC : p.d, h = HC ? HC : p.hidden, HH = h / 2, LW = d + 4, T = p.T, n = T / MB;
     const int rank = (int)cluster.block_rank(), peer = rank ^ 1;
     const int chain = blockIdx.x / 2;
     const int bi = chain / p.H, hi = chain % p.H;
@@ -1395,6 +1399,12 @@ template <typename IO>
 cudaError_t launch_cluster(const MlpBwdParams &p, int chains, cudaStream_t s)
 {
     const size_t smem = sizeof(float) * mlp_bwd_cluster_smem_floats(p.d, p.hidden);
+    if (p.d == 64 && p.hidden == 256) {  // the TTT-MLP shape of d = 64 (hidden 4d), compiled for it
+        cudaError_t e = ensure_smem<mlp_bwd_cluster_kernel<IO, 64, 256>>((int)smem);
+        if (e != cudaSuccess) return e;
+        mlp_bwd_cluster_kernel<IO, 64, 256><<<2 * chains, kNT, smem, s>>>(p);
+        return cudaGetLastError();
+    }
     cudaError_t e = ensure_smem<mlp_bwd_cluster_kernel<IO>>((int)smem);
     if (e != cudaSuccess) return e;
     mlp_bwd_cluster_kernel<IO><<<2 * chains, kNT, smem, s>>>(p);
