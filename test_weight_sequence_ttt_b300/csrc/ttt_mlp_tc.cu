@@ -1290,19 +1290,38 @@ __device__ __forceinline__ void mlp_tc_body(const CUtensorMap *tmQ, const CUtens
     }
 }
 
+// kStd: the prefix rule with separate queries, no in-kernel gate and bf16 Z, fixed
+// at compile time, so the branches on those fields drop out of the hot code (the
+// cluster form measured 1.53 -> 1.46 ms on the 4 x 12-chain T = 8192 workload).
+__device__ __forceinline__ MlpParams std_params(const MlpParams &p, bool std_case)
+{
+    MlpParams q = p;
+    if (std_case) {
+        q.prefix = 1;
+        q.q_is_k = 0;
+        q.eta_gate = 0;
+        q.z_f32 = 0;
+    }
+    return q;
+}
+
+template <bool kStd>
 __global__ void __launch_bounds__(Lay<1>::kThreads, 1)
 mlp_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const MlpParams p)
 {
-    mlp_tc_body<1>(&tmQ, &tmK, &tmV, p);
+    const MlpParams q = std_params(p, kStd);
+    mlp_tc_body<1>(&tmQ, &tmK, &tmV, q);
 }
 
 // One chain per cluster of two CTAs (blocks 2c and 2c + 1), hidden units split.
+template <bool kStd>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Lay<2>::kThreads, 1)
 mlp_tc_cluster_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const MlpParams p)
 {
-    mlp_tc_body<2>(&tmQ, &tmK, &tmV, p);
+    const MlpParams q = std_params(p, kStd);
+    mlp_tc_body<2>(&tmQ, &tmK, &tmV, q);
 }
 
 std::atomic<int> g_mlp_cluster_mode{1};
@@ -1344,15 +1363,28 @@ cudaError_t launch_mlp_tc(const MlpParams &p, int chains, cudaStream_t s)
     if (!make_map(&mQ, p.Q, kD, p.T, chains, 16) || !make_map(&mK, p.K, kD, p.T, chains, 16) ||
         !make_map(&mV, p.V, kD, p.T, chains, 16))
         return cudaErrorInvalidValue;
+    const bool std_case = p.prefix != 0 && !p.q_is_k && !p.eta_gate && !p.z_f32;
     if (mlp_use_cluster_form(chains)) {
-        cudaError_t e = ensure_smem<mlp_tc_cluster_kernel>(Lay<2>::kSmemAlloc);
-        if (e != cudaSuccess) return e;
-        mlp_tc_cluster_kernel<<<2 * chains, Lay<2>::kThreads, Lay<2>::kSmemAlloc, s>>>(mQ, mK, mV, p);
+        if (std_case) {
+            cudaError_t e = ensure_smem<mlp_tc_cluster_kernel<true>>(Lay<2>::kSmemAlloc);
+            if (e != cudaSuccess) return e;
+            mlp_tc_cluster_kernel<true><<<2 * chains, Lay<2>::kThreads, Lay<2>::kSmemAlloc, s>>>(mQ, mK, mV, p);
+        } else {
+            cudaError_t e = ensure_smem<mlp_tc_cluster_kernel<false>>(Lay<2>::kSmemAlloc);
+            if (e != cudaSuccess) return e;
+            mlp_tc_cluster_kernel<false><<<2 * chains, Lay<2>::kThreads, Lay<2>::kSmemAlloc, s>>>(mQ, mK, mV, p);
+        }
         return cudaGetLastError();
     }
-    cudaError_t e = ensure_smem<mlp_tc_kernel>(Lay<1>::kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    mlp_tc_kernel<<<chains, Lay<1>::kThreads, Lay<1>::kSmemAlloc, s>>>(mQ, mK, mV, p);
+    if (std_case) {
+        cudaError_t e = ensure_smem<mlp_tc_kernel<true>>(Lay<1>::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        mlp_tc_kernel<true><<<chains, Lay<1>::kThreads, Lay<1>::kSmemAlloc, s>>>(mQ, mK, mV, p);
+    } else {
+        cudaError_t e = ensure_smem<mlp_tc_kernel<false>>(Lay<1>::kSmemAlloc);
+        if (e != cudaSuccess) return e;
+        mlp_tc_kernel<false><<<chains, Lay<1>::kThreads, Lay<1>::kSmemAlloc, s>>>(mQ, mK, mV, p);
+    }
     return cudaGetLastError();
 }
 
