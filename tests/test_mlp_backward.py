@@ -97,13 +97,16 @@ def test_mlp_backward_matches_oracle(B, H, T, d, h, b, io):
     _compare(got, _oracle(x))
 
 
-def test_mlp_backward_gate_no_seeds_per_sequence():
-    x = _case(2, 1, 32, 16, 64, 16, seed=31, gate=True, per_seq=True)
+# d = 64, h = 256 runs the cluster kernel compiled for that shape; the others the runtime-sized one
+@pytest.mark.parametrize("d,h", [(16, 64), (64, 256)])
+def test_mlp_backward_gate_no_seeds_per_sequence(d, h):
+    x = _case(2, 1, 32, d, h, 16, seed=31, gate=True, per_seq=True)
     _compare(_run(x, gate=True, eta_base=0.6, seeds=False), _oracle(x, gate=True, eta_base=0.6, seeds=False))
 
 
-def test_mlp_backward_deterministic():
-    x = _case(1, 2, 32, 32, 128, 16, seed=32)
+@pytest.mark.parametrize("d,h", [(32, 128), (64, 256)])
+def test_mlp_backward_deterministic(d, h):
+    x = _case(1, 2, 32, d, h, 16, seed=32)
     a, b_ = _run(x), _run(x)
     for k in KEYS:
         assert torch.equal(a[k], b_[k]), k
