@@ -55,6 +55,20 @@ def test_mlp_full_size_sampled_chains(mlp_form):
         assert errs[k] <= 5 * TOL["bf16"], errs
 
 
+def test_mlp_full_size_bf16_z_matches_fp32_z(mlp_form):
+    """bf16 Z (the kernels instantiated for the standard flags) against fp32 Z (the
+    general ones) at the benchmark size: the same state and losses bit for bit, and
+    Z the round-to-nearest-even bf16 of the fp32 Z."""
+    w = WORKLOADS["mlp_b4h12_d64_t8k"]
+    inp = make_inputs(w)
+    a = run_mlp(inp, z_dtype=torch.bfloat16)
+    b = run_mlp(inp, z_dtype=torch.float32)
+    assert int(a["status"].item()) == 0 and int(b["status"].item()) == 0
+    for k in ("W1", "c1", "W2", "c2", "loss", "inner_loss"):
+        assert torch.equal(a[k], b[k]), k
+    assert torch.equal(a["Z"], b["Z"].to(torch.bfloat16))
+
+
 # ---------------------------------------------------------------- tensor-core MLP kernel (d=64, h=256, b=16)
 
 def _tc(T=64, B=2, H=2, seed=91):
